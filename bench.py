@@ -1,0 +1,419 @@
+"""Benchmark: KDA chunked prefill, 8 sequences x 2048 tokens, H=16, D=128.
+
+One step = one kda_chunk_prefill_fwd call over the whole batch (every step of
+the method runs inside that call's kernels).  Prints ONE JSON line (rank 0).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                  [--kernel auto|tc|ref] [--workload 1] [--no-cpu-baseline]
+
+value       tokens/s of the whole job (all ranks), inputs resident in HBM;
+            device time from CUDA events over exactly K steps, max over ranks.
+e2e         the same metric through the C ABI with host buffers: pinned
+            host -> device copies of every input, the call, device -> host
+            copies of out and final_state, all inside the timed region.
+roofline    the prefill kernel against the HBM roofline: algorithmic bytes
+            per launch / mean launch time (CUDA events on the launch stream).
+cpu_baseline  the fp64 CPU oracle (test infrastructure) on a bounded sample
+            of the same workload, on this host's cores (rank 0, N=1 only).
+--impl reference  times that oracle as the reference arm.
+
+L2: the inputs (352 MB per step) exceed the 129 MB L2, and four copies of
+them are rotated so that no step finds the previous step's data in L2.
+Multi-GPU: every rank runs its own full batch (replicas; the prefill has no
+exchange step), "scaling": "weak".
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+import kda_workloads as W  # noqa: E402
+
+METRIC = "KDA prefill us/layer & tokens/s (8x2048, H=16, D=128); % of roofline"
+UNIT = "tokens/s"
+D = W.HEAD_DIM
+
+
+def algorithmic_bytes(w: W.Workload) -> int:
+    """Bytes the prefill must move at least once: q, k, v, g, out (bf16),
+    beta (bf16), A_log and dt_bias (fp32), cu_seqlens, the state in and out."""
+    T = sum(w.lengths)
+    H, N = w.heads, w.num_seqs
+    s = 4 if w.state_dtype == "f32" else 2
+    return T * H * (5 * 2 * D + 2) + 2 * N * H * D * D * s + H * (D + 1) * 4 + (N + 1) * 4
+
+
+def algorithmic_flops(w: W.Workload, C: int = 64) -> int:
+    """Chunked-form tensor FLOPs with full C x C tiles: 2 D (5 C + 3 D) per token-head."""
+    return sum(w.lengths) * w.heads * 2 * D * (5 * C + 3 * D)
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), "measured"
+    return 6800.0, 1900.0, "fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "kda_gated_delta_chunk_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        if name.endswith((".cu", ".cuh")):
+            h.update(open(os.path.join(csrc, name), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def load_traffic(kernel_name: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current kernel sources (else None)."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    d = json.load(open(p))
+    ent = d.get(kernel_name)
+    if not ent or ent.get("source_hash") != kernel_source_hash():
+        return None
+    return ent.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples while the timed region runs."""
+    FIELDS = ("uuid,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, uuid: str):
+        self.uuid = uuid
+        self.rows = []
+        self.proc = None
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+        t0 = time.time()
+        while not self.rows and time.time() - t0 < 5.0:
+            time.sleep(0.02)
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) >= 9 and self.uuid in parts[0]:
+                self.rows.append((time.time(), parts))
+
+    def stop(self, t_begin: float, t_end: float):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        inside = [p for (t, p) in self.rows if t_begin <= t <= t_end] or [p for (_, p) in self.rows]
+        if not inside:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [num(p[1]) for p in inside if num(p[1]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for p in inside for i in range(4)
+                          if p[5 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": num(inside[0][2]), "reasons": reasons,
+                "samples": len(inside), "power_w_max": max((num(p[3]) or 0.0) for p in inside)}
+
+
+def dist_setup(gpus: int):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        torch.cuda.set_device(local)
+        torch.distributed.init_process_group("nccl", device_id=torch.device("cuda", local))
+    else:
+        torch.cuda.set_device(0)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        torch.distributed.barrier()
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def oracle_sample_run(inp, heads):
+    """The fp64 oracle on all sequences of the workload for the given heads."""
+    import oracle
+    N = inp["cu_seqlens"].numel() - 1
+    sub = W.select(inp, range(N), heads)
+    f = lambda t: t.float().double().numpy()
+    args = (f(sub["q"]), f(sub["k"]), f(sub["v"]), f(sub["g"]), f(sub["beta"]),
+            f(sub["A_log"]), f(sub["dt_bias"]), sub["lower_bound"], sub["scale"],
+            f(sub["initial_state"]), sub["cu_seqlens"].numpy())
+    t0 = time.perf_counter()
+    oracle.kda_oracle_fwd(*args)
+    return time.perf_counter() - t0
+
+
+def cpu_baseline(inp, w: W.Workload, budget_s: float = 12.0):
+    """Time the oracle as it stands on a bounded sample: all sequences, the
+    first h heads, h chosen from a 1-head probe to fill about budget_s."""
+    import oracle
+    oracle.build()
+    T = sum(w.lengths)
+    t1 = oracle_sample_run(inp, [0])
+    h = int(max(1, min(w.heads, budget_s // max(t1, 1e-3))))
+    t = oracle_sample_run(inp, list(range(h))) if h > 1 else t1
+    tok_per_s = T * h / t / w.heads   # token-heads/s expressed as tokens of the H-head layer
+    return {"value": tok_per_s, "unit": UNIT, "cores": oracle.max_threads(), "kind": "oracle",
+            "sample": f"{w.name}: all {w.num_seqs} sequences x {h} of {w.heads} heads "
+                      f"({T * h} token-heads, fp64, {t:.2f} s); tokens/s = token-heads/s / {w.heads}",
+            "seconds": t}
+
+
+def run_reference(args, w):
+    """Reference arm: the oracle as it stands, a bounded sample per step."""
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    import oracle
+    oracle.build()
+    inp = W.make_inputs(w)
+    T = sum(w.lengths)
+    for _ in range(args.warmup):
+        oracle_sample_run(inp, [0])
+    ts = [oracle_sample_run(inp, [0]) for _ in range(args.steps)]
+    total = sum(ts)
+    val = T * args.steps / total / w.heads
+    line = {"impl": "reference", "metric": METRIC, "value": val, "unit": UNIT,
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1e3 * total / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": w.name, "tokens": T, "seqs": w.num_seqs, "heads": w.heads,
+                       "head_dim": D, "state": w.state_dtype,
+                       "step": "oracle on all sequences x 1 head"},
+            "cpu_baseline": {"value": val, "unit": UNIT, "cores": oracle.max_threads(),
+                             "kind": "oracle",
+                             "sample": f"{w.name}: all {w.num_seqs} sequences x 1 of {w.heads} "
+                                       f"heads per step; tokens/s = token-heads/s / {w.heads}"},
+            "e2e": {"value": val, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=0, help="timed steps (0: ~1.5 s worth)")
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--kernel", default="auto", choices=["auto", "tc", "ref"])
+    ap.add_argument("--workload", type=int, default=1)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--e2e-steps", type=int, default=10)
+    args = ap.parse_args()
+    w = W.workload(args.workload)
+    if args.impl == "reference":
+        if args.steps <= 0:
+            args.steps = 5
+        return run_reference(args, w)
+
+    import kda_gated_delta_chunk_gb300 as kda
+    from kda_gated_delta_chunk_gb300 import build as kbuild
+    world, rank, local = dist_setup(args.gpus)
+    if rank == 0:
+        kbuild.build()
+    barrier(world)
+    kbuild.build()
+    kernel = {"auto": kda.KERNEL_AUTO, "tc": kda.KERNEL_TC, "ref": kda.KERNEL_REF}[args.kernel]
+    dev = torch.device("cuda", torch.cuda.current_device())
+    rc = kda.device_check(dev.index)
+    if rc != kda.OK:
+        raise kda.KDAError(rc, "device check")
+
+    host = W.make_inputs(w)
+    T, H, N = sum(w.lengths), w.heads, w.num_seqs
+    stream = torch.cuda.Stream(dev)
+    NB = 4
+    sets = []
+    with torch.cuda.stream(stream):
+        for _ in range(NB):
+            d = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in host.items()}
+            d["out"] = torch.empty_like(d["q"])
+            d["fin"] = torch.empty_like(d["initial_state"])
+            d["ws"] = kda.alloc_workspace(T, H, N, device=dev)
+            sets.append(d)
+    stream.synchronize()
+
+    def step(i, ev_pair=None):
+        d = sets[i % NB]
+        if ev_pair is not None:
+            ev_pair[0].record(stream)
+        kda.chunk_prefill_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], d["A_log"],
+                              d["dt_bias"], d["lower_bound"], d["scale"], d["initial_state"],
+                              d["cu_seqlens"], out=d["out"], final_state=d["fin"],
+                              workspace=d["ws"], stream=stream, kernel=kernel)
+        if ev_pair is not None:
+            ev_pair[1].record(stream)
+
+    for i in range(max(3, args.warmup)):
+        step(i)
+    stream.synchronize()
+    for d in sets:
+        st = kda.last_device_status(d["ws"], stream)
+        if st != kda.OK:
+            raise kda.KDAError(st, "device status after warm-up")
+
+    if args.steps <= 0:   # about 1.5 s of timed work so the clock sampler sees it
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for i in range(8):
+            step(i)
+        e1.record(stream)
+        e1.synchronize()
+        per = e0.elapsed_time(e1) / 8 / 1e3
+        args.steps = int(min(20000, max(20, 1.5 / max(per, 1e-6))))
+        if world > 1:
+            t = torch.tensor([args.steps], device=dev)
+            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+            args.steps = int(t.item())
+
+    K = args.steps
+    uuid = str(torch.cuda.get_device_properties(dev).uuid)
+    sampler = ClockSampler(uuid.replace("GPU-", ""))
+    sampler.start()
+    launch_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                 for _ in range(K)]
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize()
+    wall0 = time.time()
+    start.record(stream)
+    for i in range(K):
+        step(i, launch_ev[i])
+    stop.record(stream)
+    stop.synchronize()
+    torch.cuda.synchronize()
+    barrier(world)
+    wall1 = time.time()
+    clocks = sampler.stop(wall0, wall1)
+    elapsed = start.elapsed_time(stop) / 1e3
+    launch_s = [a.elapsed_time(b) / 1e3 for a, b in launch_ev]
+    elapsed = max_over_ranks(elapsed, world)
+    mean_launch = max_over_ranks(sum(launch_s) / K, world)
+    for d in sets:
+        st = kda.last_device_status(d["ws"], stream)
+        if st != kda.OK:
+            raise kda.KDAError(st, "device status after the timed steps")
+
+    # ---- end to end through the C ABI with host buffers
+    pinned = {k: (v.pin_memory() if isinstance(v, torch.Tensor) else v) for k, v in host.items()}
+    out_h = torch.empty(tuple(host["q"].shape), dtype=torch.bfloat16).pin_memory()
+    fin_h = torch.empty(tuple(host["initial_state"].shape),
+                        dtype=host["initial_state"].dtype).pin_memory()
+    d = sets[0]
+    names = ("q", "k", "v", "g", "beta", "A_log", "dt_bias", "initial_state", "cu_seqlens")
+    h2d = sum(pinned[k].numel() * pinned[k].element_size() for k in names)
+    d2h = out_h.numel() * out_h.element_size() + fin_h.numel() * fin_h.element_size()
+
+    def e2e_step():
+        for k in names:
+            d[k].copy_(pinned[k], non_blocking=True)
+        kda.chunk_prefill_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], d["A_log"],
+                              d["dt_bias"], d["lower_bound"], d["scale"], d["initial_state"],
+                              d["cu_seqlens"], out=d["out"], final_state=d["fin"],
+                              workspace=d["ws"], stream=stream, kernel=kernel)
+        out_h.copy_(d["out"], non_blocking=True)
+        fin_h.copy_(d["fin"], non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        for _ in range(2):
+            e2e_step()
+        stream.synchronize()
+        KE = max(1, args.e2e_steps)
+        barrier(world)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(KE):
+            e2e_step()
+        e1.record(stream)
+        e1.synchronize()
+        barrier(world)
+    e2e_elapsed = max_over_ranks(e0.elapsed_time(e1) / 1e3, world)
+
+    if rank != 0:
+        if world > 1:
+            torch.distributed.destroy_process_group()
+        return
+
+    kernel_name = "kda_tc_chunk_kernel" if kernel != kda.KERNEL_REF else "kda_ref_chunk_kernel"
+    if kernel == kda.KERNEL_AUTO:
+        kernel_name = "kda_auto"
+    hbm, tflops, peak_kind = load_peaks()
+    abytes = algorithmic_bytes(w)
+    achieved = abytes / mean_launch / 1e9
+    value = world * T * K / elapsed
+    us = 1e6 * elapsed / K
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": 1e3 * elapsed / K, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": w.name, "tokens": T, "seqs": N, "heads": H, "head_dim": D,
+                   "state": w.state_dtype, "chunk": 64, "kernel": args.kernel,
+                   "l2": "inputs 352 MB > 129 MB L2, 4 input sets rotated",
+                   "parallelism": f"replicas x{world}"},
+        "us_per_layer": us,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
+                     "frac": achieved / hbm, "traffic": load_traffic(kernel_name),
+                     "algorithmic_bytes_per_launch": abytes,
+                     "mean_launch_us": 1e6 * mean_launch, "peak_source": peak_kind,
+                     "roofline_us": 1e6 * abytes / (hbm * 1e9),
+                     "tensor_flops_per_launch": algorithmic_flops(w),
+                     "tensor_frac": algorithmic_flops(w) / mean_launch / (tflops * 1e12)},
+        "e2e": {"value": world * T * KE / e2e_elapsed, "unit": UNIT,
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": KE},
+        "gpu_launches": K,
+        "clocks": clocks,
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(host, w)
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,164 @@
+/*
+ * kda.h -- C ABI of libkda.so: chunked prefill of Kimi Delta Attention (KDA)
+ * on a GB300 (sm_103a) GPU.
+ *
+ * The operation is the one the vLLM PR report "[Perf][GLM-5.3-Flash] Use
+ * FlashKDA for KDA chunked prefill" (PR #55737) describes for FlashKDA's
+ * `get_workspace_size` / `fwd` pair (Implementation breakdown, items 2 and
+ * 3, and the "FlashKDA prefill call wrapper" listing), with the bf16 / fp32
+ * state of "[KDA] Update flashKDA to support bf16 checkpoint state"
+ * (PR #56485, Implementation breakdown item 2) and the value-dimension
+ * split of "[Kimi-K3][Perf] Update FlashKDA for automatic K2 V-split"
+ * (PR #52458, Features & motivation).  Per (sequence n, head h), token by
+ * token, with S the 128 x 128 state (row = key channel, column = value
+ * channel):
+ *
+ *   qh = scale * q / |q|      kh = k / |k|          (l2norm, eps 1e-6)
+ *   a  = lower_bound * sigmoid(exp(A_log[h]) * (g + dt_bias[h, :]))
+ *   S  = diag(exp(a)) S;      b = sigmoid(beta)
+ *   S  = S + kh * (b * (v - S^T kh))^T;   out = S^T qh
+ *
+ * computed chunk by chunk (64 tokens, WY/UT form) on tcgen05 tensor cores.
+ *
+ * Conventions for every call below:
+ *   - All tensor pointers are DEVICE pointers of the current CUDA device,
+ *     owned by the caller.  The library allocates no device memory, takes
+ *     no ownership and never synchronises inside kda_chunk_prefill_fwd*:
+ *     the work is enqueued on `stream` and returns.
+ *   - The workspace must be zero-filled once before its first use (the
+ *     device status word starts at 0; kda_last_device_status() leaves it
+ *     zero again).
+ *   - Dense row-major layouts; T = total_tokens, H = heads, N = num_seqs,
+ *     D = 128 (the only supported head dim):
+ *       q, k, v, g      bf16  [T, H, D]   (g: raw gate logits)
+ *       beta            bf16  [T, H]      (raw beta logits)
+ *       A_log           fp32  [H]         dt_bias  fp32 [H, D]
+ *       initial_state   [N, H, D, D] in state_dtype, or NULL for zeros
+ *       final_state     [N, H, D, D] in state_dtype (may equal
+ *                       initial_state: the update is then in place)
+ *       cu_seqlens      int32 [N + 1], 0 = cu[0] <= cu[1] <= ... <= cu[N] <= T
+ *       out             bf16  [T, H, D]; rows of tokens past cu[N] are not
+ *                       written.  out must not overlap any input.
+ *   - q, k, v, g, out, initial_state, final_state and workspace must be
+ *     16-byte aligned; beta 2-byte; A_log and dt_bias 16-byte.
+ *   - lower_bound must lie in [KDA_MIN_LOWER_BOUND, 0]: the gate is a log
+ *     decay in (lower_bound, 0]; past -5.5 the per-32-token exponent
+ *     anchoring the kernels use would leave the fp32 range.
+ *   - Return value: KDA_OK (0) or a negative KDA_ERR_* code; nothing is
+ *     enqueued when an error is returned.  Errors found on the device
+ *     (malformed cu_seqlens, a bounded wait that gave up) are recorded in
+ *     the workspace and read back with kda_last_device_status().
+ */
+#ifndef KDA_H_
+#define KDA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* The same handle as cudaStream_t (NULL = the legacy default stream). */
+typedef struct CUstream_st* kda_stream_t;
+
+#define KDA_HEAD_DIM 128
+#define KDA_MIN_LOWER_BOUND (-5.5f)
+
+/* state storage dtypes (PR #56485: fp32 or bf16 checkpoint state) */
+#define KDA_STATE_F32 0
+#define KDA_STATE_BF16 1
+
+/* status codes */
+#define KDA_OK 0
+#define KDA_ERR_INVALID_ARG (-1)         /* null pointer, bad size or dtype   */
+#define KDA_ERR_UNSUPPORTED_DEVICE (-2)  /* current device is not sm_103      */
+#define KDA_ERR_WORKSPACE_TOO_SMALL (-3) /* workspace_bytes below the query   */
+#define KDA_ERR_UNSAFE_LOWER_BOUND (-4)  /* lower_bound outside [-5.5, 0]     */
+#define KDA_ERR_MISALIGNED (-5)          /* a pointer breaks its alignment    */
+#define KDA_ERR_LAUNCH_FAILED (-6)       /* the kernel launch was rejected    */
+#define KDA_ERR_DEVICE_TIMEOUT (-7)      /* (device) a bounded wait gave up   */
+#define KDA_ERR_BAD_CU_SEQLENS (-8)      /* (device) cu_seqlens not monotone
+                                            or past total_tokens            */
+#define KDA_ERR_CUDA (-9)                /* a CUDA runtime call failed        */
+
+/* kernel selectors for kda_chunk_prefill_fwd_ex */
+#define KDA_KERNEL_AUTO 0 /* the production kernel                            */
+#define KDA_KERNEL_TC 1   /* tcgen05 + TMA chunk kernel, C = 64                */
+#define KDA_KERNEL_REF 2  /* plain-CUDA-core chunk kernel (GPU parity aid)     */
+
+/*
+ * Bytes of device workspace a call needs for up to `total_tokens` tokens,
+ * `heads` heads and `max_seqs` sequences.  Counterpart of FlashKDA's
+ * get_workspace_size(max_num_batched_tokens, local_num_heads,
+ * max_num_seqs) (PR #55737, Implementation breakdown item 2), where the
+ * caller sizes a uint8 buffer once and reuses it every step.  The
+ * workspace holds a device status word and the per-call work order; its
+ * size depends on max_seqs only.  Returns 0 for negative arguments.
+ */
+size_t kda_workspace_size(int64_t total_tokens, int32_t heads, int32_t max_seqs);
+
+/*
+ * Chunked KDA prefill over N packed sequences (PR #55737, Implementation
+ * breakdown item 3; argument order of FlashKDA's fwd, with the sizes a C
+ * caller must pass explicitly appended).  `scale` multiplies the
+ * normalised q (callers pass head_dim ** -0.5).  `state_dtype` is
+ * KDA_STATE_F32 or KDA_STATE_BF16 and applies to both states; a bf16 final
+ * state is rounded to nearest even.  `workspace` must hold at least
+ * kda_workspace_size(total_tokens, heads, num_seqs) bytes
+ * (`workspace_bytes`), else KDA_ERR_WORKSPACE_TOO_SMALL.  Concurrent calls
+ * on different streams need different workspaces.  The value dimension is
+ * split across CTAs automatically when 2 * heads * num_seqs <= SM count
+ * (PR #52458); the split does not change the result beyond rounding.
+ */
+int kda_chunk_prefill_fwd(const void* q, const void* k, const void* v, const void* g,
+                          const void* beta, const float* A_log, const float* dt_bias,
+                          float lower_bound, float scale, const void* initial_state,
+                          const int32_t* cu_seqlens, void* out, void* final_state,
+                          int state_dtype, void* workspace, kda_stream_t stream,
+                          int64_t total_tokens, int32_t num_seqs, int32_t heads,
+                          size_t workspace_bytes);
+
+/*
+ * As kda_chunk_prefill_fwd, with two overrides for tests and sweeps:
+ * `vsplit` -1 = automatic, or a forced split factor in {1, 2, 4, 8};
+ * `kernel` one of KDA_KERNEL_*.  Other values give KDA_ERR_INVALID_ARG.
+ */
+int kda_chunk_prefill_fwd_ex(const void* q, const void* k, const void* v, const void* g,
+                             const void* beta, const float* A_log, const float* dt_bias,
+                             float lower_bound, float scale, const void* initial_state,
+                             const int32_t* cu_seqlens, void* out, void* final_state,
+                             int state_dtype, void* workspace, kda_stream_t stream,
+                             int64_t total_tokens, int32_t num_seqs, int32_t heads,
+                             size_t workspace_bytes, int vsplit, int kernel);
+
+/*
+ * The value-dimension split factor the automatic path uses for a batch of
+ * `num_seqs` sequences and `heads` heads on a GPU with `sm_count` SMs.
+ * The trigger is PR #52458's: split only when 2 * heads * num_seqs <=
+ * sm_count (else 1).  When it triggers, the factor is the largest P in
+ * {2, 4, 8} with P * heads * num_seqs <= sm_count (P > 2 extends the
+ * pages' split).  Host logic only; returns 1 for non-positive arguments.
+ */
+int kda_choose_vsplit(int32_t num_seqs, int32_t heads, int32_t sm_count);
+
+/* Static text for a status code (never NULL). */
+const char* kda_status_string(int status);
+
+/*
+ * Reads and clears the device status word that kernels enqueued with this
+ * `workspace` leave behind.  Synchronises `stream` first (the only call of
+ * this library that does).  Returns KDA_OK, the recorded KDA_ERR_* code,
+ * or KDA_ERR_CUDA if the copy failed.
+ */
+int kda_last_device_status(void* workspace, kda_stream_t stream);
+
+/* KDA_OK when `device` is an sm_103 GPU this library can run on, else
+ * KDA_ERR_UNSUPPORTED_DEVICE (or KDA_ERR_CUDA when no device answers). */
+int kda_device_check(int device);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KDA_H_ */

@@ -1,0 +1,193 @@
+"""Python binding of libkda.so (chunked KDA prefill on GB300 / sm_103a).
+
+Argument marshalling only: every step of the computation runs in the
+library's CUDA kernels.  PyTorch supplies device memory and streams.  The
+names follow the C ABI in ``include/kda.h``:
+
+    workspace_size(total_tokens, heads, max_seqs) -> int
+    chunk_prefill_fwd(q, k, v, g, beta, A_log, dt_bias, lower_bound, scale,
+                      initial_state, cu_seqlens, out=None, final_state=None,
+                      workspace=None, ...) -> (out, final_state)
+    choose_vsplit(num_seqs, heads, sm_count) -> int
+    last_device_status(workspace) -> int
+    status_string(code) -> str
+
+There is no CPU fallback: if the library is missing or the device is not an
+sm_103 GPU, these calls raise.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libkda.so")
+
+HEAD_DIM = 128
+STATE_F32, STATE_BF16 = 0, 1
+KERNEL_AUTO, KERNEL_TC, KERNEL_REF = 0, 1, 2
+OK = 0
+ERR_INVALID_ARG = -1
+ERR_UNSUPPORTED_DEVICE = -2
+ERR_WORKSPACE_TOO_SMALL = -3
+ERR_UNSAFE_LOWER_BOUND = -4
+ERR_MISALIGNED = -5
+ERR_LAUNCH_FAILED = -6
+ERR_DEVICE_TIMEOUT = -7
+ERR_BAD_CU_SEQLENS = -8
+ERR_CUDA = -9
+
+# every symbol include/kda.h declares
+EXPORTS = ("kda_workspace_size", "kda_chunk_prefill_fwd", "kda_chunk_prefill_fwd_ex",
+           "kda_choose_vsplit", "kda_status_string", "kda_last_device_status",
+           "kda_device_check")
+
+_lib = None
+_lock = threading.Lock()
+
+
+class KDAError(RuntimeError):
+    def __init__(self, code: int, what: str = ""):
+        self.code = int(code)
+        super().__init__(f"{what}: {status_string(code)} ({code})" if what else
+                         f"{status_string(code)} ({code})")
+
+
+def lib() -> ctypes.CDLL:
+    """Load libkda.so (built in-tree by ``build.build()``); raise if absent."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise RuntimeError(f"{LIB_PATH} is missing: build it with "
+                                   "kda_gated_delta_chunk_gb300.build.build()")
+            L = ctypes.CDLL(LIB_PATH)
+            P, I32, I64, SZ, F = (ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64,
+                                  ctypes.c_size_t, ctypes.c_float)
+            L.kda_workspace_size.restype = SZ
+            L.kda_workspace_size.argtypes = [I64, I32, I32]
+            fwd_args = [P, P, P, P, P, P, P, F, F, P, P, P, P, ctypes.c_int, P, P,
+                        I64, I32, I32, SZ]
+            L.kda_chunk_prefill_fwd.restype = ctypes.c_int
+            L.kda_chunk_prefill_fwd.argtypes = fwd_args
+            L.kda_chunk_prefill_fwd_ex.restype = ctypes.c_int
+            L.kda_chunk_prefill_fwd_ex.argtypes = fwd_args + [ctypes.c_int, ctypes.c_int]
+            L.kda_choose_vsplit.restype = ctypes.c_int
+            L.kda_choose_vsplit.argtypes = [I32, I32, I32]
+            L.kda_status_string.restype = ctypes.c_char_p
+            L.kda_status_string.argtypes = [ctypes.c_int]
+            L.kda_last_device_status.restype = ctypes.c_int
+            L.kda_last_device_status.argtypes = [P, P]
+            L.kda_device_check.restype = ctypes.c_int
+            L.kda_device_check.argtypes = [ctypes.c_int]
+            _lib = L
+    return _lib
+
+
+def status_string(code: int) -> str:
+    return lib().kda_status_string(int(code)).decode()
+
+
+def workspace_size(total_tokens: int, heads: int, max_seqs: int) -> int:
+    return int(lib().kda_workspace_size(int(total_tokens), int(heads), int(max_seqs)))
+
+
+def choose_vsplit(num_seqs: int, heads: int, sm_count: int) -> int:
+    return int(lib().kda_choose_vsplit(int(num_seqs), int(heads), int(sm_count)))
+
+
+def device_check(device: int = 0) -> int:
+    return int(lib().kda_device_check(int(device)))
+
+
+def alloc_workspace(total_tokens: int, heads: int, max_seqs: int, device=None) -> torch.Tensor:
+    """A zero-filled uint8 workspace of ``workspace_size`` bytes (16-byte aligned)."""
+    n = workspace_size(total_tokens, heads, max_seqs)
+    return torch.zeros(max(n, 16), dtype=torch.uint8, device=device or "cuda")
+
+
+def last_device_status(workspace: torch.Tensor, stream=None) -> int:
+    s = stream if stream is not None else torch.cuda.current_stream(workspace.device)
+    return int(lib().kda_last_device_status(ctypes.c_void_p(workspace.data_ptr()),
+                                            ctypes.c_void_p(s.cuda_stream)))
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _need(t, name, dtype, shape=None):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.device.type != "cuda":
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+
+
+def chunk_prefill_fwd(q, k, v, g, beta, A_log, dt_bias, lower_bound, scale,
+                      initial_state, cu_seqlens, out=None, final_state=None,
+                      workspace=None, state_dtype=None, stream=None, vsplit: int = -1,
+                      kernel: int = KERNEL_AUTO):
+    """Run ``kda_chunk_prefill_fwd`` (``_ex`` when vsplit/kernel are overridden).
+
+    q, k, v, g: bf16 [T, H, 128] (a leading batch dim of 1 is accepted);
+    beta: bf16 [T, H]; A_log: fp32 [H]; dt_bias: fp32 [H, 128];
+    initial_state: [N, H, 128, 128] fp32/bf16 or None; cu_seqlens: int32 [N+1].
+    Returns (out, final_state).  Asynchronous on ``stream`` (default: the
+    current torch stream).
+    """
+    squeeze = q.dim() == 4
+    if squeeze:
+        q, k, v, g = (x.view(x.shape[1:]) for x in (q, k, v, g))
+        if out is not None:
+            out = out.view(out.shape[1:])
+        if beta.dim() == 3:
+            beta = beta.view(beta.shape[1:])
+    T, H, D = q.shape
+    if D != HEAD_DIM:
+        raise KDAError(ERR_INVALID_ARG, f"head_dim {D} (only {HEAD_DIM} is supported)")
+    N = cu_seqlens.numel() - 1
+    for name, t in (("q", q), ("k", k), ("v", v), ("g", g)):
+        _need(t, name, torch.bfloat16, (T, H, D))
+    _need(beta, "beta", torch.bfloat16, (T, H))
+    _need(A_log, "A_log", torch.float32, (H,))
+    _need(dt_bias, "dt_bias", torch.float32, (H, D))
+    _need(cu_seqlens, "cu_seqlens", torch.int32, (N + 1,))
+    if state_dtype is None:
+        state_dtype = initial_state.dtype if initial_state is not None else torch.float32
+    sd = {torch.float32: STATE_F32, torch.bfloat16: STATE_BF16}.get(state_dtype)
+    if sd is None:
+        raise TypeError("state dtype must be float32 or bfloat16")
+    if initial_state is not None:
+        _need(initial_state, "initial_state", state_dtype, (N, H, D, D))
+    if out is None:
+        out = torch.empty_like(q)
+    _need(out, "out", torch.bfloat16, (T, H, D))
+    if final_state is None:
+        final_state = torch.empty((N, H, D, D), dtype=state_dtype, device=q.device)
+    _need(final_state, "final_state", state_dtype, (N, H, D, D))
+    if workspace is None:
+        workspace = alloc_workspace(T, H, N, device=q.device)
+    _need(workspace, "workspace", torch.uint8)
+    s = stream if stream is not None else torch.cuda.current_stream(q.device)
+    args = (_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(A_log), _ptr(dt_bias),
+            float(lower_bound), float(scale), _ptr(initial_state), _ptr(cu_seqlens),
+            _ptr(out), _ptr(final_state), sd, _ptr(workspace), ctypes.c_void_p(s.cuda_stream),
+            int(T), int(N), int(H), int(workspace.numel()))
+    if vsplit == -1 and kernel == KERNEL_AUTO:
+        rc = lib().kda_chunk_prefill_fwd(*args)
+    else:
+        rc = lib().kda_chunk_prefill_fwd_ex(*args, int(vsplit), int(kernel))
+    if rc != OK:
+        raise KDAError(rc, "kda_chunk_prefill_fwd")
+    if squeeze:
+        out = out.unsqueeze(0)
+    return out, final_state

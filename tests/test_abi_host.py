@@ -1,0 +1,123 @@
+"""Host-side checks of libkda.so that need no GPU.
+
+The library must load, export every function include/kda.h declares, size
+the workspace, choose the value split as the V-split PR report states, and
+refuse bad arguments with its documented codes before touching a device.
+"""
+import ctypes
+import json
+import os
+import re
+
+import pytest
+
+import kda_gated_delta_chunk_gb300 as kda
+from kda_gated_delta_chunk_gb300 import build as kbuild
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+GOLDEN = os.path.join(ROOT, "tests", "golden")
+
+
+@pytest.fixture(scope="module")
+def L():
+    kbuild.build()
+    return kda.lib()
+
+
+def header_functions():
+    src = open(os.path.join(ROOT, "include", "kda.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(kda_[a-z0-9_]+)\s*\(", src)))
+
+
+def test_exports_every_declared_symbol(L):
+    names = header_functions()
+    assert len(names) >= 7
+    for name in names:
+        assert hasattr(L, name), name
+    assert set(names) == set(kda.EXPORTS)
+
+
+def test_workspace_size(L):
+    n = kda.workspace_size(16384, 16, 8)
+    assert n >= 16 and n % 16 == 0
+    assert kda.workspace_size(-1, 16, 8) == 0
+    assert kda.workspace_size(0, 0, 0) >= 0
+
+
+def test_vsplit_boundary_matches_pages(L):
+    g = json.load(open(os.path.join(GOLDEN, "vsplit_boundary.json")))
+    for case in g["cases"]:
+        for h in case["heads"]:
+            split = [n for n in range(1, 40) if kda.choose_vsplit(n, h, case["sm_count"]) > 1]
+            assert split == list(range(1, case["max_split_seqs"] + 1)), (case, h)
+
+
+def test_vsplit_factor_values(L):
+    assert kda.choose_vsplit(8, 16, 152) == 1        # 8x2048, H=16: 256 > 152
+    assert kda.choose_vsplit(1, 16, 152) == 8        # 1x16384, H=16
+    assert kda.choose_vsplit(7, 8, 152) == 2
+    assert kda.choose_vsplit(3, 8, 152) == 4
+    assert kda.choose_vsplit(1, 8, 152) == 8
+    assert kda.choose_vsplit(0, 8, 152) == 1
+    for n in range(1, 30):
+        for h in (1, 4, 8, 16, 32):
+            p = kda.choose_vsplit(n, h, 152)
+            assert p in (1, 2, 4, 8)
+            assert p == 1 or p * n * h <= 152
+
+
+def test_status_strings(L):
+    for code in range(-9, 1):
+        assert kda.status_string(code) and kda.status_string(code) != "unknown status"
+    assert kda.status_string(-99) == "unknown status"
+
+
+def _call(L, **over):
+    """Call kda_chunk_prefill_fwd_ex with fake (never dereferenced) pointers."""
+    a = dict(q=0x10000, k=0x20000, v=0x30000, g=0x40000, beta=0x50000, A_log=0x60000,
+             dt_bias=0x70000, lb=-5.0, scale=128 ** -0.5, s0=0x80000, cu=0x90000,
+             out=0xA0000, fin=0xB0000, sd=0, ws=0xC0000, stream=None, T=64, N=1, H=2,
+             wsb=kda.workspace_size(64, 2, 1), vsplit=-1, kernel=0)
+    a.update(over)
+    P = ctypes.c_void_p
+    return L.kda_chunk_prefill_fwd_ex(
+        P(a["q"]), P(a["k"]), P(a["v"]), P(a["g"]), P(a["beta"]), P(a["A_log"]),
+        P(a["dt_bias"]), a["lb"], a["scale"], P(a["s0"]), P(a["cu"]), P(a["out"]),
+        P(a["fin"]), a["sd"], P(a["ws"]), P(a["stream"]), a["T"], a["N"], a["H"], a["wsb"],
+        a["vsplit"], a["kernel"])
+
+
+@pytest.mark.parametrize("over,code", [
+    (dict(lb=-6.0), kda.ERR_UNSAFE_LOWER_BOUND),
+    (dict(lb=0.5), kda.ERR_UNSAFE_LOWER_BOUND),
+    (dict(lb=float("nan")), kda.ERR_INVALID_ARG),
+    (dict(scale=float("inf")), kda.ERR_INVALID_ARG),
+    (dict(H=0), kda.ERR_INVALID_ARG),
+    (dict(T=-1), kda.ERR_INVALID_ARG),
+    (dict(N=-1), kda.ERR_INVALID_ARG),
+    (dict(sd=2), kda.ERR_INVALID_ARG),
+    (dict(q=0), kda.ERR_INVALID_ARG),
+    (dict(out=0), kda.ERR_INVALID_ARG),
+    (dict(cu=0), kda.ERR_INVALID_ARG),
+    (dict(fin=0), kda.ERR_INVALID_ARG),
+    (dict(fin=0, N=0, T=0), kda.ERR_CUDA),
+    (dict(ws=0), kda.ERR_INVALID_ARG),
+    (dict(wsb=8), kda.ERR_WORKSPACE_TOO_SMALL),
+    (dict(q=0x10008), kda.ERR_MISALIGNED),
+    (dict(fin=0xB0004), kda.ERR_MISALIGNED),
+    (dict(beta=0x50001), kda.ERR_MISALIGNED),
+    (dict(vsplit=3), kda.ERR_INVALID_ARG),
+    (dict(kernel=7), kda.ERR_INVALID_ARG),
+])
+def test_argument_gate(L, over, code):
+    assert _call(L, **over) == code
+
+
+def test_valid_arguments_reach_the_device_check(L):
+    """Valid arguments pass validation; without an sm_103 GPU the call then
+    stops at the device check and enqueues nothing."""
+    rc = _call(L)
+    import torch
+    if not torch.cuda.is_available():
+        assert rc in (kda.ERR_CUDA, kda.ERR_UNSUPPORTED_DEVICE)

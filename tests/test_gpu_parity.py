@@ -1,0 +1,247 @@
+"""GPU parity: libkda.so's kernels against the fp64 oracle, element by element.
+
+Every workload's inputs come from the seeded generator; the oracle reads
+the exact bf16/fp32 values the GPU reads.  The pass bar is the tolerance the
+bf16-checkpoint PR report uses (max |delta| 0.01 with an fp32 state, 0.03
+with a bf16 state) on both out and final_state; mean |delta| is printed.
+Full-size workloads run on the GPU exactly as the benchmark launches them;
+the oracle then checks every (sequence, head) pair it can afford (all of
+them for the smaller workloads, a sample that always includes the longest
+sequence for the largest).
+"""
+import json
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import kda_gated_delta_chunk_gb300 as kda
+import kda_workloads as W
+
+pytestmark = pytest.mark.gpu
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+TOL = json.load(open(os.path.join(ROOT, "tests", "golden", "tolerances.json")))["max_abs"]
+KERNELS = [kda.KERNEL_REF]
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from kda_gated_delta_chunk_gb300 import build as kbuild
+    kbuild.build()
+    rc = kda.device_check(torch.cuda.current_device())
+    assert rc == kda.OK, kda.status_string(rc)
+
+
+def to_dev(inp):
+    return {k: (v.cuda() if isinstance(v, torch.Tensor) and k != "rows" else v)
+            for k, v in inp.items()}
+
+
+def run_gpu(inp, kernel=kda.KERNEL_AUTO, vsplit=-1, out=None, final_state=None, init="keep"):
+    d = to_dev(inp)
+    s0 = d["initial_state"] if init == "keep" else None
+    out, fin = kda.chunk_prefill_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], d["A_log"],
+                                     d["dt_bias"], d["lower_bound"], d["scale"], s0,
+                                     d["cu_seqlens"], out=out, final_state=final_state,
+                                     state_dtype=inp["initial_state"].dtype, vsplit=vsplit,
+                                     kernel=kernel)
+    torch.cuda.synchronize()
+    return out, fin
+
+
+def f64(t):
+    return t.float().double().cpu().numpy()
+
+
+def oracle_sub(oracle_mod, inp, seqs, heads, zero_init=False):
+    sub = W.select(inp, seqs, heads)
+    o, f = oracle_mod.kda_oracle_fwd(
+        f64(sub["q"]), f64(sub["k"]), f64(sub["v"]), f64(sub["g"]), f64(sub["beta"]),
+        f64(sub["A_log"]), f64(sub["dt_bias"]), sub["lower_bound"], sub["scale"],
+        None if zero_init else f64(sub["initial_state"]), sub["cu_seqlens"].numpy())
+    return sub["rows"], o, f
+
+
+def check(oracle_mod, inp, out, fin, seqs=None, heads=None, tol=None, zero_init=False, tag=""):
+    N = inp["cu_seqlens"].numel() - 1
+    H = inp["q"].shape[1]
+    seqs = list(range(N)) if seqs is None else list(seqs)
+    heads = list(range(H)) if heads is None else list(heads)
+    tol = TOL[inp["state_dtype"]] if tol is None else tol
+    rows, o_ref, f_ref = oracle_sub(oracle_mod, inp, seqs, heads, zero_init)
+    hidx = torch.tensor(heads)
+    o_gpu = f64(out.cpu().index_select(0, rows).index_select(1, hidx))
+    f_gpu = f64(fin.cpu().index_select(0, torch.tensor(seqs, dtype=torch.long)).index_select(1, hidx))
+    assert np.all(np.isfinite(o_gpu)) and np.all(np.isfinite(f_gpu))
+    do, df = np.abs(o_gpu - o_ref), np.abs(f_gpu - f_ref)
+    print(f"{tag}: out max {do.max() if do.size else 0:.3e} mean {do.mean() if do.size else 0:.3e}"
+          f" | state max {df.max():.3e} mean {df.mean():.3e}")
+    assert (do.max() if do.size else 0.0) <= tol, ("out", do.max())
+    assert df.max() <= tol, ("final_state", df.max())
+    return do, df
+
+
+# ----------------------------------------------------------------- workloads
+@pytest.mark.parametrize("kernel", KERNELS)
+def test_workload0_tiny(oracle_mod, kernel):
+    inp = W.make_inputs(W.workload(0))
+    out, fin = run_gpu(inp, kernel)
+    check(oracle_mod, inp, out, fin, tag=f"w0 k{kernel}")
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
+@pytest.mark.parametrize("vsplit", [1, 2, 4, 8])
+def test_ragged_tiles_and_tails(oracle_mod, kernel, vsplit):
+    """Several chunks, ragged tails, a 1-token and an empty sequence."""
+    w = W.custom([1, 63, 64, 65, 130, 0, 200, 17, 129], 3, seed=21)
+    inp = W.make_inputs(w)
+    out, fin = run_gpu(inp, kernel, vsplit)
+    check(oracle_mod, inp, out, fin, tag=f"ragged k{kernel} P{vsplit}")
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
+def test_bf16_state(oracle_mod, kernel):
+    w = W.custom([300, 5, 64, 129], 4, state_dtype="bf16", seed=22)
+    inp = W.make_inputs(w)
+    out, fin = run_gpu(inp, kernel)
+    assert fin.dtype == torch.bfloat16
+    check(oracle_mod, inp, out, fin, tag=f"bf16 state k{kernel}")
+
+
+@pytest.mark.parametrize("cfg", [1, 2])
+def test_workloads_1_2_full_size(oracle_mod, cfg):
+    inp = W.make_inputs(W.workload(cfg))
+    out, fin = run_gpu(inp)
+    heads = None if cfg == 1 else [0, 5, 11, 15]
+    check(oracle_mod, inp, out, fin, heads=heads, tag=f"workload {cfg}")
+
+
+@pytest.mark.parametrize("n", [1, 2, 3, 7])
+def test_workload3_vsplit_vs_unsplit(oracle_mod, n):
+    """Split and unsplit paths: same layout, values within tolerance of each
+    other and of the oracle (bit identity is not required)."""
+    inp = W.make_inputs(W.workload(3, n))
+    out_a, fin_a = run_gpu(inp)                 # automatic split
+    out_1, fin_1 = run_gpu(inp, vsplit=1)       # forced unsplit
+    assert out_a.shape == out_1.shape and fin_a.shape == fin_1.shape
+    tol = TOL["f32"]
+    assert (out_a.float() - out_1.float()).abs().max().item() <= tol
+    assert (fin_a - fin_1).abs().max().item() <= tol
+    heads = [0, 3, 7]
+    check(oracle_mod, inp, out_a, fin_a, heads=heads, tag=f"w3 n={n} auto")
+    check(oracle_mod, inp, out_1, fin_1, heads=heads, tag=f"w3 n={n} P=1")
+
+
+def test_workload4_ragged_bf16_state(oracle_mod):
+    w = W.workload(4)
+    inp = W.make_inputs(w)
+    out, fin = run_gpu(inp)
+    lens = list(w.lengths)
+    longest = int(np.argmax(lens))
+    shortest = int(np.argmin(lens))
+    seqs = sorted({longest, shortest, 0, 17, 40, 63})
+    check(oracle_mod, inp, out, fin, seqs=seqs, heads=[0, 13, 31], tag="workload 4")
+
+
+# ----------------------------------------------------------------- edge cases
+def test_inplace_state_update(oracle_mod):
+    inp = W.make_inputs(W.custom([90, 40], 2, seed=23))
+    d = to_dev(inp)
+    state = d["initial_state"].clone()
+    out, fin = kda.chunk_prefill_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], d["A_log"],
+                                     d["dt_bias"], d["lower_bound"], d["scale"], state,
+                                     d["cu_seqlens"], final_state=state)
+    torch.cuda.synchronize()
+    assert fin.data_ptr() == state.data_ptr()
+    check(oracle_mod, inp, out, fin, tag="in place")
+
+
+def test_null_initial_state(oracle_mod):
+    inp = W.make_inputs(W.custom([70, 3], 2, seed=24))
+    out, fin = run_gpu(inp, init=None)
+    check(oracle_mod, inp, out, fin, zero_init=True, tag="null initial state")
+
+
+def test_rows_past_last_sequence_untouched(oracle_mod):
+    inp = W.make_inputs(W.custom([50, 20], 2, seed=25, pad_tokens=9))
+    sentinel = torch.full(inp["q"].shape, 7.0, dtype=torch.bfloat16, device="cuda")
+    out, fin = run_gpu(inp, out=sentinel)
+    assert torch.all(out[70:].float() == 7.0)
+    check(oracle_mod, inp, out, fin, tag="padded")
+
+
+@pytest.mark.parametrize("sd", ["f32", "bf16"])
+def test_empty_sequences_pass_state_through(sd):
+    inp = W.make_inputs(W.custom([0, 0, 5, 0], 2, state_dtype=sd, seed=26))
+    out, fin = run_gpu(inp)
+    s0 = inp["initial_state"]
+    for n in (0, 1, 3):
+        assert torch.equal(fin[n].cpu(), s0[n])   # bit-exact copy
+
+
+def test_no_sequences_is_a_no_op():
+    inp = W.make_inputs(W.custom([], 2, seed=27))
+    d = to_dev(inp)
+    out, fin = kda.chunk_prefill_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], d["A_log"],
+                                     d["dt_bias"], d["lower_bound"], d["scale"],
+                                     d["initial_state"], d["cu_seqlens"])
+    torch.cuda.synchronize()
+    assert fin.shape[0] == 0
+
+
+@pytest.mark.parametrize("bad", [[0, 40, 20], [5, 20, 40], [0, 20, 999]])
+def test_bad_cu_seqlens_reported_on_device(bad):
+    inp = W.make_inputs(W.custom([20, 20], 2, seed=28))
+    inp["cu_seqlens"] = torch.tensor(bad, dtype=torch.int32)
+    d = to_dev(inp)
+    ws = kda.alloc_workspace(40, 2, 2)
+    out, fin = kda.chunk_prefill_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], d["A_log"],
+                                     d["dt_bias"], d["lower_bound"], d["scale"],
+                                     d["initial_state"], d["cu_seqlens"], workspace=ws)
+    assert kda.last_device_status(ws) == kda.ERR_BAD_CU_SEQLENS
+    assert kda.last_device_status(ws) == kda.OK      # read clears it
+
+
+def test_errors_returned_with_a_device():
+    inp = W.make_inputs(W.custom([20], 2, seed=29))
+    d = to_dev(inp)
+    with pytest.raises(kda.KDAError) as e:
+        kda.chunk_prefill_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], d["A_log"],
+                              d["dt_bias"], -6.0, d["scale"], d["initial_state"],
+                              d["cu_seqlens"])
+    assert e.value.code == kda.ERR_UNSAFE_LOWER_BOUND
+    with pytest.raises(kda.KDAError) as e:
+        kda.chunk_prefill_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], d["A_log"],
+                              d["dt_bias"], d["lower_bound"], d["scale"], d["initial_state"],
+                              d["cu_seqlens"], workspace=torch.zeros(8, dtype=torch.uint8,
+                                                                      device="cuda"))
+    assert e.value.code == kda.ERR_WORKSPACE_TOO_SMALL
+
+
+def test_cuda_graph_capture_and_replay(oracle_mod):
+    """Capture the call on a side stream, replay it, compare with eager."""
+    inp = W.make_inputs(W.custom([200, 64, 3], 4, seed=30))
+    d = to_dev(inp)
+    out_e, fin_e = run_gpu(inp)
+    out = torch.empty_like(d["q"])
+    fin = torch.empty_like(d["initial_state"])
+    ws = kda.alloc_workspace(d["q"].shape[0], 4, 3)
+    side = torch.cuda.Stream()
+    args = (d["q"], d["k"], d["v"], d["g"], d["beta"], d["A_log"], d["dt_bias"],
+            d["lower_bound"], d["scale"], d["initial_state"], d["cu_seqlens"])
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):        # warm-up outside capture
+        kda.chunk_prefill_fwd(*args, out=out, final_state=fin, workspace=ws, stream=side)
+    side.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=side):
+        kda.chunk_prefill_fwd(*args, out=out, final_state=fin, workspace=ws, stream=side)
+    out.zero_()
+    fin.zero_()
+    graph.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(out, out_e) and torch.equal(fin, fin_e)
