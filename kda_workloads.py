@@ -116,7 +116,10 @@ def custom(lengths, heads, state_dtype="f32", init="normal", seed=0,
 def _randn_bf16(shape, gen, std=1.0, chunk_rows=1 << 14):
     """N(0, std^2) drawn in fp32 row-block by row-block, rounded to bf16."""
     out = torch.empty(shape, dtype=torch.bfloat16)
-    flat = out.view(shape[0], -1)
+    inner = 1
+    for x in shape[1:]:
+        inner *= int(x)
+    flat = out.view(shape[0], inner)
     for r0 in range(0, shape[0], chunk_rows):
         r1 = min(shape[0], r0 + chunk_rows)
         blk = torch.randn((r1 - r0, flat.shape[1]), generator=gen, dtype=torch.float32)

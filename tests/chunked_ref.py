@@ -25,10 +25,11 @@ tokens (32 for C = 64).  Inside sub-block j the cumsum is taken from the
 sub-block start (c_r) and anchored at its middle row m_j (alpha_j = c_m):
 E_r = exp(c_r - alpha_j) and Ei_r = exp(alpha_j - c_r) stay within
 exp(+-|lb| sub/2) -- inside fp32 for |lb| <= 5.5.  Products inside one
-sub-block use E (row) and Ei (column); products between sub-blocks use
-factors anchored at the end of the column's sub-block, which are <= 1; the
-chunk-level factors exp(Gam_r) and exp(Gam_last - Gam_s) are built from the
-same per-element E/Ei times per-channel constants.
+sub-block use E (row) and Ei (column).  Between sub-blocks the row operand
+is the row block's own E and the column operand carries all the remaining
+factors (each <= 1), so the diagonal and off-diagonal products share one row
+operand.  The chunk-level factors exp(Gam_r) and exp(Gam_last - Gam_s) are
+built from the same per-element E/Ei times per-channel constants.
 """
 from __future__ import annotations
 
@@ -97,8 +98,11 @@ def _factors_anchored(a, sub, dt):
                 mid = mid + btot[t]
             r0, r1 = i * sub, min(L, (i + 1) * sub)
             s0, s1 = j * sub, (j + 1) * sub
-            pair_row[(i, j)] = E[r0:r1] * np.exp(alpha[i]) * np.exp(mid)
-            pair_col[(i, j)] = Ei[s0:s1] * np.exp(btot[j] - alpha[j])
+            # the row operand is block i's own E; every other factor (each
+            # <= 1) is folded into the column operand
+            pair_row[(i, j)] = E[r0:r1]
+            pair_col[(i, j)] = (Ei[s0:s1] * np.exp(btot[j] - alpha[j])) * (np.exp(alpha[i])
+                                                                          * np.exp(mid))
     decay = np.exp(total)
     return dict(E=E, Ei=Ei, g_row=g_row, g_end=g_end, decay=decay,
                 pair_row=pair_row, pair_col=pair_col, nb=nb)

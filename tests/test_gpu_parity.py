@@ -23,7 +23,7 @@ pytestmark = pytest.mark.gpu
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 TOL = json.load(open(os.path.join(ROOT, "tests", "golden", "tolerances.json")))["max_abs"]
-KERNELS = [kda.KERNEL_REF]
+KERNELS = [kda.KERNEL_REF, kda.KERNEL_TC]
 
 
 @pytest.fixture(scope="module", autouse=True)
