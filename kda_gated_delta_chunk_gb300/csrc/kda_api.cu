@@ -109,8 +109,7 @@ int fwd_impl(const void* q, const void* k, const void* v, const void* g, const v
   p.vsplit = vsplit == -1 ? kda_choose_vsplit(num_seqs, heads, sms) : vsplit;
 
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  // AUTO resolves to the tcgen05 kernel once it is built into this library
-  cudaError_t err = (kernel == KDA_KERNEL_TC) ? kda::launch_tc(p, s) : kda::launch_ref(p, s);
+  cudaError_t err = (kernel == KDA_KERNEL_REF) ? kda::launch_ref(p, s) : kda::launch_tc(p, s);
   if (err != cudaSuccess) {
     cudaGetLastError();
     return KDA_ERR_LAUNCH_FAILED;

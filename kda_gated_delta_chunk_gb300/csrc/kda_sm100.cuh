@@ -51,18 +51,22 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
-// Bounded wait: spins with a growing back-off and gives up after about a
-// second (returns false) instead of hanging the GPU.
+__device__ __forceinline__ uint64_t globaltimer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+// Bounded wait: spins on try_wait (which itself suspends the thread for a
+// short while) and gives up after about one second of wall time, returning
+// false, instead of hanging the GPU.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
-  uint32_t ns = 8;
-  for (uint32_t it = 0; it < (1u << 22); ++it) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if (it > 64) {
-      __nanosleep(ns);
-      if (ns < 256) ns <<= 1;
-    }
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  while (true) {
+    for (int i = 0; i < 64; ++i)
+      if (mbar_try_wait(bar, parity)) return true;
+    if (globaltimer_ns() - t0 > 1000000000ull) return mbar_try_wait(bar, parity);
   }
-  return mbar_try_wait(bar, parity);
 }
 
 // Generic-proxy shared-memory writes -> visible to the async proxy (TMA,

@@ -251,6 +251,9 @@ __global__ void __launch_bounds__(NT, 1)
   uint32_t ph_qkg = 0, ph_v = 0, ph_mma = 0;
   bool failed = false;
   int site = 0;
+  // beta logits are fetched one chunk ahead (their load latency hides behind a chunk)
+  float b_raw = 0.0f;
+  if (tid < C && t0 + tid < t1) b_raw = __bfloat162float(p.beta[(size_t)(t0 + tid) * H + h]);
 
   for (int c0 = t0; c0 < t1; c0 += C) {
     const int L = min(C, t1 - c0);
@@ -265,9 +268,8 @@ __global__ void __launch_bounds__(NT, 1)
 
     // ---- P1: beta and the row norms of q and k (one warp per row)
     if (tid < C) {
-      float b = 0.0f;
-      if (tid < L) b = sigm(__bfloat162float(p.beta[(size_t)(c0 + tid) * H + h]));
-      beta_s[tid] = b;
+      beta_s[tid] = (tid < L) ? sigm(b_raw) : 0.0f;
+      if (c0 + C + tid < t1) b_raw = __bfloat162float(p.beta[(size_t)(c0 + C + tid) * H + h]);
     }
     for (int r = warp * 8; r < warp * 8 + 8; ++r) {
       const uint2 qv = *reinterpret_cast<const uint2*>(sm + OFF_INQ + r * 256 + lane * 8);
