@@ -157,6 +157,37 @@ int kda_last_device_status(void* workspace, kda_stream_t stream);
  * KDA_ERR_UNSUPPORTED_DEVICE (or KDA_ERR_CUDA when no device answers). */
 int kda_device_check(int device);
 
+/*
+ * kda_chunk_prefill_fwd for callers that cannot allocate device memory and
+ * so cannot pass a workspace: for instance a plugin inside a host framework
+ * that owns all device memory, or a hot loop where a cudaMalloc (which may
+ * synchronise the device) is not allowed.  The pages have no counterpart of
+ * this entry point.
+ *
+ * Arguments, layouts and ownership are those of kda_chunk_prefill_fwd
+ * without the workspace; the tcgen05 kernel runs with automatic value split.
+ * The scratch it needs (the 16-byte device status word) lives in a 256-byte
+ * file-scope device array of this library, which every GPU that loads the
+ * library holds until exit.  The library allocates nothing: no cudaMalloc,
+ * cudaFree or allocating library call on any path of this function.
+ *   - The first call on a device looks up the array's device address (with
+ *     that device current); make that first call before any stream capture.
+ *   - Every call shares the array.  Each call clears the status word on
+ *     `stream` before its kernel (this clearing may be enqueued even when
+ *     the call then returns an argument error).  Calls that overlap on the
+ *     GPU race on the array.  Device-side errors land in the array and are
+ *     not reported back here; use kda_chunk_prefill_fwd with a workspace to
+ *     read them.
+ *   - Returns KDA_ERR_WORKSPACE_TOO_SMALL if the call would need more than
+ *     the 256-byte maximum, otherwise the codes of kda_chunk_prefill_fwd.
+ */
+int kda_chunk_prefill_fwd_noalloc(const void* q, const void* k, const void* v, const void* g,
+                                  const void* beta, const float* A_log, const float* dt_bias,
+                                  float lower_bound, float scale, const void* initial_state,
+                                  const int32_t* cu_seqlens, void* out, void* final_state,
+                                  int state_dtype, kda_stream_t stream, int64_t total_tokens,
+                                  int32_t num_seqs, int32_t heads);
+
 #ifdef __cplusplus
 }
 #endif

@@ -43,7 +43,7 @@ ERR_CUDA = -9
 # every symbol include/kda.h declares
 EXPORTS = ("kda_workspace_size", "kda_chunk_prefill_fwd", "kda_chunk_prefill_fwd_ex",
            "kda_choose_vsplit", "kda_status_string", "kda_last_device_status",
-           "kda_device_check")
+           "kda_device_check", "kda_chunk_prefill_fwd_noalloc")
 
 _lib = None
 _lock = threading.Lock()
@@ -83,6 +83,9 @@ def lib() -> ctypes.CDLL:
             L.kda_last_device_status.argtypes = [P, P]
             L.kda_device_check.restype = ctypes.c_int
             L.kda_device_check.argtypes = [ctypes.c_int]
+            L.kda_chunk_prefill_fwd_noalloc.restype = ctypes.c_int
+            L.kda_chunk_prefill_fwd_noalloc.argtypes = [P, P, P, P, P, P, P, F, F, P, P, P, P,
+                                                        ctypes.c_int, P, I64, I32, I32]
             _lib = L
     return _lib
 
@@ -190,4 +193,42 @@ def chunk_prefill_fwd(q, k, v, g, beta, A_log, dt_bias, lower_bound, scale,
         raise KDAError(rc, "kda_chunk_prefill_fwd")
     if squeeze:
         out = out.unsqueeze(0)
+    return out, final_state
+
+
+def chunk_prefill_fwd_noalloc(q, k, v, g, beta, A_log, dt_bias, lower_bound, scale,
+                              initial_state, cu_seqlens, out, final_state, stream=None):
+    """Run ``kda_chunk_prefill_fwd_noalloc``: no workspace, no allocation.
+
+    For callers that cannot allocate device memory.  ``out`` and
+    ``final_state`` must be given (this wrapper allocates nothing either);
+    the library keeps its small scratch in a static device array shared by
+    all calls, so calls that overlap on the GPU race.
+    """
+    if q.dim() == 4:
+        q, k, v, g = (x.view(x.shape[1:]) for x in (q, k, v, g))
+        out = out.view(out.shape[1:])
+        if beta.dim() == 3:
+            beta = beta.view(beta.shape[1:])
+    T, H, D = q.shape
+    N = cu_seqlens.numel() - 1
+    for name, t in (("q", q), ("k", k), ("v", v), ("g", g), ("out", out)):
+        _need(t, name, torch.bfloat16, (T, H, D))
+    _need(beta, "beta", torch.bfloat16, (T, H))
+    _need(A_log, "A_log", torch.float32, (H,))
+    _need(dt_bias, "dt_bias", torch.float32, (H, D))
+    _need(cu_seqlens, "cu_seqlens", torch.int32, (N + 1,))
+    sd = {torch.float32: STATE_F32, torch.bfloat16: STATE_BF16}.get(final_state.dtype)
+    if sd is None:
+        raise TypeError("state dtype must be float32 or bfloat16")
+    _need(final_state, "final_state", final_state.dtype, (N, H, D, D))
+    if initial_state is not None:
+        _need(initial_state, "initial_state", final_state.dtype, (N, H, D, D))
+    s = stream if stream is not None else torch.cuda.current_stream(q.device)
+    rc = lib().kda_chunk_prefill_fwd_noalloc(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(A_log), _ptr(dt_bias),
+        float(lower_bound), float(scale), _ptr(initial_state), _ptr(cu_seqlens), _ptr(out),
+        _ptr(final_state), sd, ctypes.c_void_p(s.cuda_stream), int(T), int(N), int(H))
+    if rc != OK:
+        raise KDAError(rc, "kda_chunk_prefill_fwd_noalloc")
     return out, final_state
