@@ -1,6 +1,6 @@
 // tcgen05 + TMA chunked KDA prefill (KDA_KERNEL_TC), 64-token chunks.
 //
-// One CTA (256 threads, ~213 KB shared memory, 512 TMEM columns) owns one
+// One CTA (256 threads, ~190 KB shared memory, 512 TMEM columns) owns one
 // (sequence, head, value slice) and walks the sequence's chunks in order,
 // keeping the 128 x 128 fp32 state in tensor memory the whole time.
 //
@@ -30,8 +30,11 @@
 // memory, fp32 accumulators in TMEM), transposed so that M = 128 is the
 // value (or key) channel:
 //   D = [Kr; Qr] [Kc; Kc2]^T                          (A and QK, M = 128, N = 96)
-//   W^T = Kg^T (T diag b)^T,  U'^T = V^T (T diag b)^T
-//   U^T += S^T (-W)^T,  O^T = S^T Qg^T,  O^T += U^T QK^T,  S^T += U^T Ke
+//   W_b^T = Kr_b^T (T diag b)_b^T  (b = 32-token block; Kr read as an MN-major
+//           operand, the per-channel block factors applied when W is converted)
+//   U'^T = V^T (T diag b)^T,  O^T = S^T Qg^T,  U^T += S^T (-W)^T,
+//   O^T += U^T QK^T,  S^T += U^T Ke
+// S^T and U^T enter the MMAs as bf16 A operands held in TMEM.
 // The unit-lower-triangular inverse T runs on CUDA cores in fp32.  Inputs
 // arrive by TMA; the next chunk's q/k/g (and v) are fetched while this one
 // is being processed.
@@ -56,39 +59,40 @@ constexpr int OFF_INQ = 0;                  // q tile [64][128] bf16 row-major (
 constexpr int OFF_INK = 16384;              // k tile
 constexpr int OFF_ING = 32768;              // g tile
 constexpr int OFF_INV = 49152;              // v tile: 2 SW128 boxes [64 tok][64 dv]
-constexpr int OFF_RA = 65536;               // region A (88 KB), reused within a chunk:
-constexpr int OFF_RKQ = OFF_RA;             //  [Kr; Qr]  K-major, 128 rows x 128
-constexpr int OFF_CKC = OFF_RA + 32768;     //  [Kc; Kc2] K-major,  96 rows x 128
-constexpr int OFF_TB = OFF_RA;              //  T diag(b) K-major,  64 rows x 64
-constexpr int OFF_WN = OFF_RA + 8192;       //  -W        MN-major, N = 64 tok, K = 128
-constexpr int OFF_SB = OFF_RA + 24576;      //  S^T bf16  K-major, 128 rows x 128
-constexpr int OFF_UB = OFF_RA + 57344;      //  U^T bf16  K-major, 128 rows x 64
-constexpr int OFF_OST = OFF_RA + 73728;     //  O staging [64][128] bf16 row-major
-constexpr int OFF_NM = OFF_RA + 24576;      //  fp32 N = diag(b) strict(A)  [64][65]
-constexpr int OFF_TM = OFF_NM + 16640;      //  fp32 T                      [64][65]
-constexpr int OFF_Y = OFF_TM + 16640;       //  fp32 scratch (2x16x17 and 32x33)
-constexpr int OFF_QG = OFF_RA + 90112;      // Qg  K-major 64 rows x 128   (B of O = S^T Qg^T)
-constexpr int OFF_KG = OFF_QG + 16384;      // Kg  MN-major mn = dk, k = tok (A of W^T)
-constexpr int OFF_KE = OFF_KG + 16384;      // Ke  MN-major mn = dk, k = tok (B of S^T += U^T Ke)
-constexpr int OFF_QKB = OFF_KE + 16384;     // QK  K-major 64 rows x 64    (B of O^T += U^T QK^T)
+constexpr int OFF_RA = 65536;               // region reused within a chunk:
+constexpr int OFF_RKQ = OFF_RA;             //  [Kr; Qr] K-major 128 rows x 128 (live to W)
+constexpr int OFF_CKC = OFF_RA + 32768;     //  [Kc; Kc2] K-major 96 rows x 128 (live to D)
+constexpr int NS = 68;                      //  fp32 row stride of the T scratch (16-B rows)
+constexpr int OFF_NM = OFF_RA + 32768;      //  N = diag(b) strict(A)  [64][NS]  (after D)
+constexpr int OFF_TM = OFF_NM + 64 * NS * 4;//  T                      [64][NS]
+constexpr int OFF_Y = OFF_TM + 64 * NS * 4; //  products scratch       [32][36]
+constexpr int OFF_WN = OFF_RA + 32768;      //  -W MN-major, N = 64 tok, K = 128 (after T)
+constexpr int OFF_TB = OFF_RA + 73728;      //  T diag(b) K-major 64 x 64
+constexpr int OFF_QG = OFF_RA + 81920;      // Qg K-major 64 rows x 128 (B of O^T = S^T Qg^T)
+constexpr int OFF_KE = OFF_QG + 16384;      // Ke MN-major mn = dk, k = tok (B of S^T += U^T Ke)
+constexpr int OFF_QKB = OFF_KE + 16384;     // QK K-major 64 x 64 (B of O^T += U^T QK^T)
 constexpr int OFF_MISC = OFF_QKB + 8192;
 constexpr int OFF_INVN = OFF_MISC;          // inv |q| * scale [64], inv |k| [64]
 constexpr int OFF_BETA = OFF_MISC + 512;    // b [64]
 constexpr int OFF_DECAY = OFF_MISC + 768;   // 2^Gam_last [128]
-constexpr int OFF_GT = OFF_MISC + 1280;     // group totals [4][128] (also sequence lengths)
-constexpr int OFF_BAR = OFF_MISC + 3328;    // 3 mbarriers
-constexpr int OFF_TSLOT = OFF_MISC + 3360;  // TMEM base address
-constexpr int OFF_FLAGS = OFF_MISC + 3364;  // [0] sequence chosen for this CTA
-constexpr int SMEM_USED = OFF_MISC + 3584;
+constexpr int OFF_WF = OFF_MISC + 1280;     // W factors [3][128]: 2^G0, 2^G2, 2^B0
+constexpr int OFF_GT = OFF_MISC + 2816;     // group totals [4][128] (also sequence lengths)
+constexpr int OFF_BAR = OFF_MISC + 4864;    // 3 mbarriers
+constexpr int OFF_TSLOT = OFF_MISC + 4896;  // TMEM base address
+constexpr int OFF_FLAGS = OFF_MISC + 4900;  // [0] sequence chosen for this CTA
+constexpr int SMEM_USED = OFF_MISC + 5120;
 constexpr int SMEM_BYTES = SMEM_USED + 1024;
-static_assert(OFF_Y + 6400 <= OFF_RA + 73728, "T scratch overlaps O staging");
+static_assert(OFF_Y + 32 * 36 * 4 <= OFF_TB, "T scratch overlaps T diag(b)");
+static_assert(OFF_CKC + 24576 <= OFF_TB, "operands overlap T diag(b)");
 static_assert(SMEM_BYTES <= 227 * 1024, "shared memory");
 
-// ---- TMEM columns (fp32 accumulators; lane = value or key channel)
-constexpr uint32_t TM_S = 0;      // S^T   128 cols (lane = dv, col = dk)
-constexpr uint32_t TM_U = 128;    // U^T    64 cols (lane = dv, col = token)
-constexpr uint32_t TM_O = 192;    // O^T    64 cols
-constexpr uint32_t TM_D1 = 256;   // D      96 cols (lanes 0-63: A, 64-127: QK); then W^T
+// ---- TMEM columns (fp32 unless noted; lane = value channel, or key channel for D/W)
+constexpr uint32_t TM_S = 0;      // S^T        128 cols (col = dk)
+constexpr uint32_t TM_SB = 128;   // S^T bf16    64 cols (A operand, 2 dk per col)
+constexpr uint32_t TM_U = 192;    // U^T         64 cols (col = token)
+constexpr uint32_t TM_O = 256;    // O^T         64 cols
+constexpr uint32_t TM_D = 320;    // D (A|QK)    96 cols, then W0^T at +0, W1^T at +64
+constexpr uint32_t TM_UB = 448;   // U^T bf16    32 cols (A operand, 2 tokens per col)
 constexpr uint32_t TM_COLS = 512;
 
 constexpr uint32_t ID_KK64 = idesc_bf16(128, 64, 0, 0);
@@ -119,6 +123,13 @@ __device__ __forceinline__ float2 ld_bf16x2(const unsigned char* base, uint32_t 
   const __nv_bfloat162 v = *reinterpret_cast<const __nv_bfloat162*>(base + off);
   return __bfloat1622float2(v);
 }
+__device__ __forceinline__ float4 ld4(const float* p) { return *reinterpret_cast<const float4*>(p); }
+__device__ __forceinline__ void fma4(float4& acc, float a, const float4& b) {
+  acc.x = fmaf(a, b.x, acc.x);
+  acc.y = fmaf(a, b.y, acc.y);
+  acc.z = fmaf(a, b.z, acc.z);
+  acc.w = fmaf(a, b.w, acc.w);
+}
 
 // K-step descriptors
 __device__ __forceinline__ uint64_t kdesc(uint32_t tile, int rows, int ks) {
@@ -141,6 +152,7 @@ __global__ void __launch_bounds__(NT, 1)
   float* inv_k = inv_q + 64;
   float* beta_s = reinterpret_cast<float*>(sm + OFF_BETA);
   float* decay_s = reinterpret_cast<float*>(sm + OFF_DECAY);
+  float* wf = reinterpret_cast<float*>(sm + OFF_WF);
   float* gt = reinterpret_cast<float*>(sm + OFF_GT);
   int* flags = reinterpret_cast<int*>(sm + OFF_FLAGS);
   uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + OFF_TSLOT);
@@ -201,13 +213,12 @@ __global__ void __launch_bounds__(NT, 1)
   const uint32_t tmem = *tslot;
   const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
   const int my_lane = 32 * (warp & 3) + lane;     // TMEM lane this thread reads
-  const int col_half = warp >> 2;                 // warps 4-7 take the second half of columns
+  const int half = warp >> 2;                     // warps 4-7 take the second column half
 
   const size_t HD = (size_t)H * D;
   const size_t sbase = ((size_t)n * H + h) * D * D;
   const int xcol = h * D;
 
-  // first chunk's tiles
   if (tid == 0 && t1 > t0) {
     mbar_expect_tx(bar_qkg, 3 * 16384);
     tma_load_2d(sb + OFF_INQ, &tm_q, xcol, t0, bar_qkg);
@@ -223,7 +234,7 @@ __global__ void __launch_bounds__(NT, 1)
     const int dv = my_lane;
     const bool mine = dv >= dv_lo && dv < dv_hi && p.initial_state != nullptr;
     for (int cb = 0; cb < 2; ++cb) {
-      const int dk0 = col_half * 64 + cb * 32;
+      const int dk0 = half * 64 + cb * 32;
       uint32_t r[32];
 #pragma unroll
       for (int j = 0; j < 32; ++j) {
@@ -247,6 +258,9 @@ __global__ void __launch_bounds__(NT, 1)
   const int grp = tid >> 6;           // 16-row group of the gate/operand phase
   const int d0 = 2 * cp;
   const float db0 = p.dt_bias[h * D + d0], db1 = p.dt_bias[h * D + d0 + 1];
+  float* Nm = reinterpret_cast<float*>(sm + OFF_NM);
+  float* Tm = reinterpret_cast<float*>(sm + OFF_TM);
+  float* Y = reinterpret_cast<float*>(sm + OFF_Y);
 
   uint32_t ph_qkg = 0, ph_v = 0, ph_mma = 0;
   bool failed = false;
@@ -313,26 +327,29 @@ __global__ void __launch_bounds__(NT, 1)
     }
     __syncthreads();
 
-    // ---- P2b: anchored factors and the bf16 operand tiles
+    // ---- P2b: anchored factors and the bf16 operand tiles [Kr; Qr], [Kc; Kc2], Qg, Ke
     {
-      float G[4][2];
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        G[j][0] = gt[j * 128 + d0];
-        G[j][1] = gt[j * 128 + d0 + 1];
-      }
       const bool blk1 = grp >= 2;
-      float mE[2], cA[2], cB[2], cX[2];
+      float mE[2], cA[2], cB[2], cX[2], cR[2];
+#pragma unroll
       for (int c = 0; c < 2; ++c) {
-        const float B0 = G[0][c] + G[1][c], B1 = G[2][c] + G[3][c];
-        mE[c] = (grp & 1) ? 0.0f : G[grp][c];
-        // block 0: cA = 2^G0 (row -> 2^Gam), cB = 2^G1 (col -> 2^(B0 - c)), then 2^B1
-        // block 1: cA = 2^G2 (row -> 2^c),   cB = 2^G3 (col -> 2^(B1 - c)), then 2^B0
-        cA[c] = ex2f(blk1 ? G[2][c] : G[0][c]);
-        cB[c] = ex2f(blk1 ? G[3][c] : G[1][c]);
-        cX[c] = ex2f(G[2][c]);            // alpha_1, folded into Kc2
-        if (grp == 0) decay_s[d0 + c] = ex2f(B0 + B1);
-        G[0][c] = ex2f(blk1 ? B0 : B1);   // reuse: the cross-block factor
+        const float G0 = gt[d0 + c], G1 = gt[128 + d0 + c];
+        const float G2 = gt[256 + d0 + c], G3 = gt[384 + d0 + c];
+        const float B0 = G0 + G1, B1 = G2 + G3;
+        const float Gown = blk1 ? (grp == 2 ? G2 : G3) : (grp == 0 ? G0 : G1);
+        mE[c] = (grp & 1) ? 0.0f : Gown;
+        // block 0: cA = 2^G0 (E -> 2^Gam), cB = 2^G1 (Ei -> 2^(B0 - c)), cR = 2^B1
+        // block 1: cA = 2^G2 (E -> 2^c),   cB = 2^G3 (Ei -> 2^(B1 - c)), cR = 2^B0
+        cA[c] = ex2f(blk1 ? G2 : G0);
+        cB[c] = ex2f(blk1 ? G3 : G1);
+        cX[c] = ex2f(G2);                 // alpha_1, folded into Kc2
+        cR[c] = ex2f(blk1 ? B0 : B1);
+        if (grp == 0) {
+          decay_s[d0 + c] = ex2f(B0 + B1);
+          wf[d0 + c] = cA[c];              // W block 0: 2^G0
+          wf[128 + d0 + c] = cX[c];        // W block 1: 2^G2, then
+          wf[256 + d0 + c] = ex2f(B0);     //            2^B0
+        }
       }
 #pragma unroll
       for (int i = 0; i < 16; ++i) {
@@ -356,29 +373,28 @@ __global__ void __launch_bounds__(NT, 1)
                  pack_bf16x2(kh0 * (oc0 * cX[0]), kh1 * (oc1 * cX[1])));
           g0 = E0 * cA[0];
           g1 = E1 * cA[1];
-          ke0 = oc0 * G[0][0];
-          ke1 = oc1 * G[0][1];
+          ke0 = oc0 * cR[0];
+          ke1 = oc1 * cR[1];
         } else {
-          const float orw0 = E0 * cA[0], orw1 = E1 * cA[1];     // 2^c_r in block 1
-          g0 = orw0 * G[0][0];
-          g1 = orw1 * G[0][1];
+          g0 = (E0 * cA[0]) * cR[0];
+          g1 = (E1 * cA[1]) * cR[1];
           ke0 = Ei0 * cB[0];
           ke1 = Ei1 * cB[1];
         }
         st_u32(sm, OFF_QG + kmajor_off(r, d0, 64), pack_bf16x2(qh0 * g0, qh1 * g1));
-        st_u32(sm, OFF_KG + mnmajor_off(d0, r, 8192), pack_bf16x2(kh0 * g0, kh1 * g1));
         st_u32(sm, OFF_KE + mnmajor_off(d0, r, 8192), pack_bf16x2(kh0 * ke0, kh1 * ke1));
       }
     }
     fence_proxy_async();
     __syncthreads();
 
-    // ---- P3: D = [Kr; Qr] [Kc; Kc2]^T on the tensor cores; fetch the next q, k, g
+    // ---- P3: D = [Kr; Qr] [Kc; Kc2]^T on the tensor cores; fetch the next q, k, g.
+    //          Warps 4-7 meanwhile make the bf16 copy of S^T and apply this chunk's decay.
     if (tid == 0) {
       tc_fence_after();
 #pragma unroll
       for (int ks = 0; ks < 8; ++ks)
-        mma_bf16(tmem + TM_D1, kdesc(sb + OFF_RKQ, 128, ks), kdesc(sb + OFF_CKC, 96, ks), ID_KK96,
+        mma_bf16(tmem + TM_D, kdesc(sb + OFF_RKQ, 128, ks), kdesc(sb + OFF_CKC, 96, ks), ID_KK96,
                  ks > 0);
       mma_commit(bar_mma);
       if (more) {
@@ -388,46 +404,72 @@ __global__ void __launch_bounds__(NT, 1)
         tma_load_2d(sb + OFF_ING, &tm_g, xcol, c0 + C, bar_qkg);
       }
     }
+    if (half == 1) {
+      for (int cb = 0; cb < 4; ++cb) {      // 32 key columns per pass
+        uint32_t x[32], pk[16];
+        tmem_ld32(tmem + lane_base + TM_S + cb * 32, x);
+        tmem_wait_ld();
+#pragma unroll
+        for (int j = 0; j < 16; ++j)
+          pk[j] = pack_bf16x2(__uint_as_float(x[2 * j]), __uint_as_float(x[2 * j + 1]));
+        tmem_st16(tmem + lane_base + TM_SB + cb * 16, pk);
+#pragma unroll
+        for (int j4 = 0; j4 < 8; ++j4) {
+          const float4 dl = ld4(decay_s + cb * 32 + 4 * j4);
+          x[4 * j4] = __float_as_uint(__uint_as_float(x[4 * j4]) * dl.x);
+          x[4 * j4 + 1] = __float_as_uint(__uint_as_float(x[4 * j4 + 1]) * dl.y);
+          x[4 * j4 + 2] = __float_as_uint(__uint_as_float(x[4 * j4 + 2]) * dl.z);
+          x[4 * j4 + 3] = __float_as_uint(__uint_as_float(x[4 * j4 + 3]) * dl.w);
+        }
+        tmem_st32(tmem + lane_base + TM_S + cb * 32, x);
+      }
+      tmem_wait_st();
+    }
     {
       const bool ok = mbar_wait(bar_mma, ph_mma) && mbar_wait(bar_v, ph_v);
       ph_mma ^= 1;
       ph_v ^= 1;
+      tc_fence_before();
       if (__syncthreads_or(!ok)) { failed = true; site = 30; break; }
     }
     tc_fence_after();
 
     // ---- P4a: A rows (lanes 0-63) -> N = diag(b) strict(A); QK rows (64-127) -> bf16 tile;
     //            warps 4-7 clear v rows past the sequence end and T above the diagonal blocks
-    float* Nm = reinterpret_cast<float*>(sm + OFF_NM);
-    float* Tm = reinterpret_cast<float*>(sm + OFF_TM);
-    if (warp < 4) {
-      uint32_t a[64], o2[32];
-      tmem_ld32(tmem + lane_base + TM_D1, *reinterpret_cast<uint32_t(*)[32]>(a));
-      tmem_ld32(tmem + lane_base + TM_D1 + 32, *reinterpret_cast<uint32_t(*)[32]>(a + 32));
-      tmem_ld32(tmem + lane_base + TM_D1 + 64, o2);
-      tmem_wait_ld();
+    if (half == 0) {
+      // columns 0-31 come from D[:, 64:96] for rows 32-63 (the off-diagonal block)
       const int r = my_lane & 63;
       const bool use2 = r >= 32;
-      if (warp < 2) {
-        const float br = beta_s[r];
+      for (int cb = 0; cb < 2; ++cb) {
+        uint32_t a[32];
+        tmem_ld32(tmem + lane_base + TM_D + ((cb == 0 && use2) ? 64 : 32 * cb), a);
+        tmem_wait_ld();
+        if (warp < 2) {
+          const float br = beta_s[r];
 #pragma unroll
-        for (int s = 0; s < 64; ++s) {
-          const float v = (s < 32 && use2) ? __uint_as_float(o2[s]) : __uint_as_float(a[s]);
-          Nm[r * 65 + s] = (s < r) ? br * v : 0.0f;
-        }
-      } else {
+          for (int s4 = 0; s4 < 8; ++s4) {
+            float v[4];
 #pragma unroll
-        for (int c8 = 0; c8 < 8; ++c8) {
-          uint32_t w[4];
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int s = c8 * 8 + e * 2;
-            const float v0 = (s < 32 && use2) ? __uint_as_float(o2[s]) : __uint_as_float(a[s]);
-            const float v1 =
-                (s + 1 < 32 && use2) ? __uint_as_float(o2[s + 1]) : __uint_as_float(a[s + 1]);
-            w[e] = pack_bf16x2(s <= r ? v0 : 0.0f, s + 1 <= r ? v1 : 0.0f);
+            for (int e = 0; e < 4; ++e) {
+              const int s = 32 * cb + 4 * s4 + e;
+              v[e] = (s < r) ? br * __uint_as_float(a[4 * s4 + e]) : 0.0f;
+            }
+            *reinterpret_cast<float4*>(Nm + r * NS + 32 * cb + 4 * s4) =
+                make_float4(v[0], v[1], v[2], v[3]);
           }
-          st_u128(sm, OFF_QKB + kmajor_off(r, c8 * 8, 64), make_uint4(w[0], w[1], w[2], w[3]));
+        } else {
+#pragma unroll
+          for (int c8 = 0; c8 < 4; ++c8) {
+            uint32_t w[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const int s = 32 * cb + c8 * 8 + e * 2;
+              w[e] = pack_bf16x2(s <= r ? __uint_as_float(a[c8 * 8 + e * 2]) : 0.0f,
+                                 s + 1 <= r ? __uint_as_float(a[c8 * 8 + e * 2 + 1]) : 0.0f);
+            }
+            st_u128(sm, OFF_QKB + kmajor_off(r, 32 * cb + c8 * 8, 64),
+                    make_uint4(w[0], w[1], w[2], w[3]));
+          }
         }
       }
     } else {
@@ -438,12 +480,13 @@ __global__ void __launch_bounds__(NT, 1)
           st_u128(sm, OFF_INV + (cc >> 3) * 8192 + r * 128 + (cc & 7) * 16, make_uint4(0, 0, 0, 0));
         }
       }
-      // T above the diagonal blocks is zero
-      for (int idx = t4; idx < 6 * 256; idx += 128) {
-        const int b = idx >> 8, e = idx & 255;
+      // T above the diagonal 16x16 blocks is zero
+      for (int idx = t4; idx < 6 * 64; idx += 128) {
+        const int b = idx >> 6, e = idx & 63;
         const int bi = (b < 3) ? 0 : (b < 5 ? 1 : 2);
         const int bj = (b < 3) ? b + 1 : (b < 5 ? b - 1 : 3);
-        Tm[(bi * 16 + (e >> 4)) * 65 + bj * 16 + (e & 15)] = 0.0f;
+        *reinterpret_cast<float4*>(Tm + (bi * 16 + (e >> 2)) * NS + bj * 16 + 4 * (e & 3)) =
+            make_float4(0.f, 0.f, 0.f, 0.f);
       }
     }
     fence_proxy_async();
@@ -458,81 +501,113 @@ __global__ void __launch_bounds__(NT, 1)
       for (int i = 0; i < 16; ++i) {
         float acc = (i == j) ? 1.0f : 0.0f;
 #pragma unroll
-        for (int s = 0; s < i; ++s) acc -= Nm[(o + i) * 65 + o + s] * x[s];
+        for (int q4 = 0; q4 < 4; ++q4) {
+          if (4 * q4 < i) {
+            const float4 nv = ld4(Nm + (o + i) * NS + o + 4 * q4);
+            if (4 * q4 + 0 < i) acc -= nv.x * x[4 * q4 + 0];
+            if (4 * q4 + 1 < i) acc -= nv.y * x[4 * q4 + 1];
+            if (4 * q4 + 2 < i) acc -= nv.z * x[4 * q4 + 2];
+            if (4 * q4 + 3 < i) acc -= nv.w * x[4 * q4 + 3];
+          }
+        }
         x[i] = acc;
       }
 #pragma unroll
-      for (int i = 0; i < 16; ++i) Tm[(o + i) * 65 + o + j] = x[i];
+      for (int i = 0; i < 16; ++i) Tm[(o + i) * NS + o + j] = x[i];
     }
     __syncthreads();
-    float* Y = reinterpret_cast<float*>(sm + OFF_Y);
-    {   // Y_b = N[lower of pair b] T[upper of pair b], pairs (1,0) and (3,2)
-      for (int idx = tid; idx < 512; idx += NT) {
-        const int b = idx >> 8, i = (idx >> 4) & 15, j = idx & 15;
-        const int ro = (2 * b + 1) * 16, co = 2 * b * 16;
-        float acc = 0.0f;
+    if (tid < 128) {   // Y_b = N[rows of b] T[diag block of b], pairs b = (1,0) and (3,2)
+      const int b = tid >> 6, i = (tid >> 2) & 15, jq = tid & 3;
+      const int ro = (2 * b + 1) * 16, co = 2 * b * 16;
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-        for (int s = 0; s < 16; ++s) acc += Nm[(ro + i) * 65 + co + s] * Tm[(co + s) * 65 + co + j];
-        Y[b * 272 + i * 17 + j] = acc;
+      for (int s4 = 0; s4 < 4; ++s4) {
+        const float4 nv = ld4(Nm + (ro + i) * NS + co + 4 * s4);
+        fma4(acc, nv.x, ld4(Tm + (co + 4 * s4 + 0) * NS + co + 4 * jq));
+        fma4(acc, nv.y, ld4(Tm + (co + 4 * s4 + 1) * NS + co + 4 * jq));
+        fma4(acc, nv.z, ld4(Tm + (co + 4 * s4 + 2) * NS + co + 4 * jq));
+        fma4(acc, nv.w, ld4(Tm + (co + 4 * s4 + 3) * NS + co + 4 * jq));
       }
+      *reinterpret_cast<float4*>(Y + (b * 16 + i) * 20 + 4 * jq) = acc;
     }
     __syncthreads();
-    {
-      for (int idx = tid; idx < 512; idx += NT) {
-        const int b = idx >> 8, i = (idx >> 4) & 15, j = idx & 15;
-        const int ro = (2 * b + 1) * 16, co = 2 * b * 16;
-        float acc = 0.0f;
+    if (tid < 128) {   // T[lower of b] = -T[diag of b, rows] Y_b
+      const int b = tid >> 6, i = (tid >> 2) & 15, jq = tid & 3;
+      const int ro = (2 * b + 1) * 16, co = 2 * b * 16;
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-        for (int s = 0; s < 16; ++s) acc += Tm[(ro + i) * 65 + ro + s] * Y[b * 272 + s * 17 + j];
-        Tm[(ro + i) * 65 + co + j] = -acc;
+      for (int s4 = 0; s4 < 4; ++s4) {
+        const float4 tv = ld4(Tm + (ro + i) * NS + ro + 4 * s4);
+        fma4(acc, tv.x, ld4(Y + (b * 16 + 4 * s4 + 0) * 20 + 4 * jq));
+        fma4(acc, tv.y, ld4(Y + (b * 16 + 4 * s4 + 1) * 20 + 4 * jq));
+        fma4(acc, tv.z, ld4(Y + (b * 16 + 4 * s4 + 2) * 20 + 4 * jq));
+        fma4(acc, tv.w, ld4(Y + (b * 16 + 4 * s4 + 3) * 20 + 4 * jq));
       }
+      *reinterpret_cast<float4*>(Tm + (ro + i) * NS + co + 4 * jq) =
+          make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
     }
     __syncthreads();
     {   // Y2 = N[32:64, 0:32] T[0:32, 0:32]
-      for (int idx = tid; idx < 1024; idx += NT) {
-        const int i = idx >> 5, j = idx & 31;
-        float acc = 0.0f;
-#pragma unroll 8
-        for (int s = 0; s < 32; ++s) acc += Nm[(32 + i) * 65 + s] * Tm[s * 65 + j];
-        Y[i * 33 + j] = acc;
+      const int i = tid >> 3, jq = tid & 7;
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int s4 = 0; s4 < 8; ++s4) {
+        const float4 nv = ld4(Nm + (32 + i) * NS + 4 * s4);
+        fma4(acc, nv.x, ld4(Tm + (4 * s4 + 0) * NS + 4 * jq));
+        fma4(acc, nv.y, ld4(Tm + (4 * s4 + 1) * NS + 4 * jq));
+        fma4(acc, nv.z, ld4(Tm + (4 * s4 + 2) * NS + 4 * jq));
+        fma4(acc, nv.w, ld4(Tm + (4 * s4 + 3) * NS + 4 * jq));
       }
+      *reinterpret_cast<float4*>(Y + i * 36 + 4 * jq) = acc;
     }
     __syncthreads();
     {   // T[32:64, 0:32] = -T[32:64, 32:64] Y2
-      for (int idx = tid; idx < 1024; idx += NT) {
-        const int i = idx >> 5, j = idx & 31;
-        float acc = 0.0f;
-#pragma unroll 8
-        for (int s = 0; s < 32; ++s) acc += Tm[(32 + i) * 65 + 32 + s] * Y[s * 33 + j];
-        Tm[(32 + i) * 65 + j] = -acc;
+      const int i = tid >> 3, jq = tid & 7;
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int s4 = 0; s4 < 8; ++s4) {
+        const float4 tv = ld4(Tm + (32 + i) * NS + 32 + 4 * s4);
+        fma4(acc, tv.x, ld4(Y + (4 * s4 + 0) * 36 + 4 * jq));
+        fma4(acc, tv.y, ld4(Y + (4 * s4 + 1) * 36 + 4 * jq));
+        fma4(acc, tv.z, ld4(Y + (4 * s4 + 2) * 36 + 4 * jq));
+        fma4(acc, tv.w, ld4(Y + (4 * s4 + 3) * 36 + 4 * jq));
       }
+      *reinterpret_cast<float4*>(Tm + (32 + i) * NS + 4 * jq) =
+          make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
     }
     __syncthreads();
     // T diag(b) -> bf16 (K-major, row r, k = s)
     for (int idx = tid; idx < 512; idx += NT) {
       const int r = idx >> 3, c8 = idx & 7;
-      uint32_t w[4];
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int s = c8 * 8 + e * 2;
-        w[e] = pack_bf16x2(Tm[r * 65 + s] * beta_s[s], Tm[r * 65 + s + 1] * beta_s[s + 1]);
-      }
-      st_u128(sm, OFF_TB + kmajor_off(r, c8 * 8, 64), make_uint4(w[0], w[1], w[2], w[3]));
+      const float4 t0v = ld4(Tm + r * NS + c8 * 8), t1v = ld4(Tm + r * NS + c8 * 8 + 4);
+      const float4 b0v = ld4(beta_s + c8 * 8), b1v = ld4(beta_s + c8 * 8 + 4);
+      st_u128(sm, OFF_TB + kmajor_off(r, c8 * 8, 64),
+              make_uint4(pack_bf16x2(t0v.x * b0v.x, t0v.y * b0v.y),
+                         pack_bf16x2(t0v.z * b0v.z, t0v.w * b0v.w),
+                         pack_bf16x2(t1v.x * b1v.x, t1v.y * b1v.y),
+                         pack_bf16x2(t1v.z * b1v.z, t1v.w * b1v.w)));
     }
     fence_proxy_async();
     __syncthreads();
 
-    // ---- P5: W^T = Kg^T (T diag b)^T -> D1 region;  U'^T = V^T (T diag b)^T -> U
+    // ---- P5: W_b^T = (Kr rows of block b)^T (T diag b)[:, b]^T for b = 0, 1 (D region);
+    //          U'^T = V^T (T diag b)^T;  O^T = S^T Qg^T
     if (tid == 0) {
       tc_fence_after();
 #pragma unroll
-      for (int ks = 0; ks < 4; ++ks)
-        mma_bf16(tmem + TM_D1, mndesc(sb + OFF_KG, 8192, ks), kdesc(sb + OFF_TB, 64, ks),
-                 ID_MK64, ks > 0);
+      for (int b = 0; b < 2; ++b)
+#pragma unroll
+        for (int ks = 0; ks < 2; ++ks)
+          mma_bf16(tmem + TM_D + 64 * b, mndesc(sb + OFF_RKQ + 4096 * b, 16384, ks),
+                   kdesc(sb + OFF_TB, 64, 2 * b + ks), ID_MK64, ks > 0);
 #pragma unroll
       for (int ks = 0; ks < 4; ++ks)
         mma_bf16(tmem + TM_U, mndesc(sb + OFF_INV, 8192, ks), kdesc(sb + OFF_TB, 64, ks),
                  ID_MK64, ks > 0);
+#pragma unroll
+      for (int ks = 0; ks < 8; ++ks)
+        mma_bf16_ts(tmem + TM_O, tmem + TM_SB + 8 * ks, kdesc(sb + OFF_QG, 64, ks), ID_KK64,
+                    ks > 0);
       mma_commit(bar_mma);
     }
     {
@@ -547,63 +622,40 @@ __global__ void __launch_bounds__(NT, 1)
       tma_load_2d(sb + OFF_INV + 8192, &tm_v, xcol + 64, c0 + C, bar_v);
     }
 
-    // ---- P6: -W (bf16, MN-major, n = token, k = dk) from W^T; state pass:
-    //          S^T -> bf16 operand, S^T <- S^T diag(2^Gam_last)
-    if (warp < 4) {
+    // ---- P6: -W = -(2^G0 W0 + 2^B0 (2^G2 W1)) -> bf16, MN-major (n = token, k = dk)
+    {
       const int dk = my_lane;
-      for (int cb = 0; cb < 2; ++cb) {
-        uint32_t r[32];
-        tmem_ld32(tmem + lane_base + TM_D1 + cb * 32, r);
-        tmem_wait_ld();
+      const float f0 = wf[dk], f1a = wf[128 + dk], f1b = wf[256 + dk];
+      uint32_t w0[32], w1[32];
+      tmem_ld32(tmem + lane_base + TM_D + half * 32, w0);
+      tmem_ld32(tmem + lane_base + TM_D + 64 + half * 32, w1);
+      tmem_wait_ld();
 #pragma unroll
-        for (int c8 = 0; c8 < 4; ++c8) {
-          uint32_t w[4];
+      for (int c8 = 0; c8 < 4; ++c8) {
+        uint32_t w[4];
 #pragma unroll
-          for (int e = 0; e < 4; ++e)
-            w[e] = pack_bf16x2(-__uint_as_float(r[c8 * 8 + e * 2]),
-                               -__uint_as_float(r[c8 * 8 + e * 2 + 1]));
-          st_u128(sm, OFF_WN + mnmajor_off(cb * 32 + c8 * 8, dk, 8192),
-                  make_uint4(w[0], w[1], w[2], w[3]));
+        for (int e = 0; e < 4; ++e) {
+          const int j = c8 * 8 + e * 2;
+          const float x0 = f0 * __uint_as_float(w0[j]) + f1b * (f1a * __uint_as_float(w1[j]));
+          const float x1 =
+              f0 * __uint_as_float(w0[j + 1]) + f1b * (f1a * __uint_as_float(w1[j + 1]));
+          w[e] = pack_bf16x2(-x0, -x1);
         }
+        st_u128(sm, OFF_WN + mnmajor_off(half * 32 + c8 * 8, dk, 8192),
+                make_uint4(w[0], w[1], w[2], w[3]));
       }
-    } else {
-      const int dv = my_lane;
-      for (int cb = 0; cb < 4; ++cb) {
-        uint32_t r[32];
-        tmem_ld32(tmem + lane_base + TM_S + cb * 32, r);
-        tmem_wait_ld();
-#pragma unroll
-        for (int c8 = 0; c8 < 4; ++c8) {
-          uint32_t w[4];
-#pragma unroll
-          for (int e = 0; e < 4; ++e)
-            w[e] = pack_bf16x2(__uint_as_float(r[c8 * 8 + e * 2]),
-                               __uint_as_float(r[c8 * 8 + e * 2 + 1]));
-          st_u128(sm, OFF_SB + kmajor_off(dv, cb * 32 + c8 * 8, 128),
-                  make_uint4(w[0], w[1], w[2], w[3]));
-        }
-#pragma unroll
-        for (int j = 0; j < 32; ++j)
-          r[j] = __float_as_uint(__uint_as_float(r[j]) * decay_s[cb * 32 + j]);
-        tmem_st32(tmem + lane_base + TM_S + cb * 32, r);
-      }
-      tmem_wait_st();
     }
     fence_proxy_async();
     tc_fence_before();
     __syncthreads();
 
-    // ---- P7: U^T += S^T (-W)^T;  O^T = S^T Qg^T
+    // ---- P7: U^T += S^T (-W)^T
     if (tid == 0) {
       tc_fence_after();
 #pragma unroll
       for (int ks = 0; ks < 8; ++ks)
-        mma_bf16(tmem + TM_U, kdesc(sb + OFF_SB, 128, ks), mndesc(sb + OFF_WN, 8192, ks), ID_KM64,
-                 1);
-#pragma unroll
-      for (int ks = 0; ks < 8; ++ks)
-        mma_bf16(tmem + TM_O, kdesc(sb + OFF_SB, 128, ks), kdesc(sb + OFF_QG, 64, ks), ID_KK64,
-                 ks > 0);
+        mma_bf16_ts(tmem + TM_U, tmem + TM_SB + 8 * ks, mndesc(sb + OFF_WN, 8192, ks), ID_KM64,
+                    1);
       mma_commit(bar_mma);
     }
     {
@@ -613,26 +665,17 @@ __global__ void __launch_bounds__(NT, 1)
     }
     tc_fence_after();
 
-    // ---- P8: U^T -> bf16 operand (K-major, row dv, k = token)
-    if (warp < 4) {
-      const int dv = my_lane;
-      for (int cb = 0; cb < 2; ++cb) {
-        uint32_t r[32];
-        tmem_ld32(tmem + lane_base + TM_U + cb * 32, r);
-        tmem_wait_ld();
+    // ---- P8: U^T -> bf16 operand in TMEM (2 tokens per column)
+    {   // 8 warps: lane quadrant x half of the 64 token columns
+      uint32_t x[32], pk[16];
+      tmem_ld32(tmem + lane_base + TM_U + half * 32, x);
+      tmem_wait_ld();
 #pragma unroll
-        for (int c8 = 0; c8 < 4; ++c8) {
-          uint32_t w[4];
-#pragma unroll
-          for (int e = 0; e < 4; ++e)
-            w[e] = pack_bf16x2(__uint_as_float(r[c8 * 8 + e * 2]),
-                               __uint_as_float(r[c8 * 8 + e * 2 + 1]));
-          st_u128(sm, OFF_UB + kmajor_off(dv, cb * 32 + c8 * 8, 128),
-                  make_uint4(w[0], w[1], w[2], w[3]));
-        }
-      }
+      for (int j = 0; j < 16; ++j)
+        pk[j] = pack_bf16x2(__uint_as_float(x[2 * j]), __uint_as_float(x[2 * j + 1]));
+      tmem_st16(tmem + lane_base + TM_UB + half * 16, pk);
+      tmem_wait_st();
     }
-    fence_proxy_async();
     tc_fence_before();
     __syncthreads();
 
@@ -641,12 +684,11 @@ __global__ void __launch_bounds__(NT, 1)
       tc_fence_after();
 #pragma unroll
       for (int ks = 0; ks < 4; ++ks)
-        mma_bf16(tmem + TM_O, kdesc(sb + OFF_UB, 128, ks), kdesc(sb + OFF_QKB, 64, ks), ID_KK64,
-                 1);
+        mma_bf16_ts(tmem + TM_O, tmem + TM_UB + 8 * ks, kdesc(sb + OFF_QKB, 64, ks), ID_KK64, 1);
 #pragma unroll
       for (int ks = 0; ks < 4; ++ks)
-        mma_bf16(tmem + TM_S, kdesc(sb + OFF_UB, 128, ks), mndesc(sb + OFF_KE, 8192, ks),
-                 ID_KM128, 1);
+        mma_bf16_ts(tmem + TM_S, tmem + TM_UB + 8 * ks, mndesc(sb + OFF_KE, 8192, ks), ID_KM128,
+                    1);
       mma_commit(bar_mma);
     }
     {
@@ -656,27 +698,20 @@ __global__ void __launch_bounds__(NT, 1)
     }
     tc_fence_after();
 
-    // ---- P10: O^T -> bf16 staging [token][dv] -> global rows < L of this value slice
-    if (warp < 4) {
+    // ---- P10: O^T -> bf16 -> global rows < L of this value slice (32 tokens per warp)
+    {
       const int dv = my_lane;
-      __nv_bfloat16* ost = reinterpret_cast<__nv_bfloat16*>(sm + OFF_OST);
-      for (int cb = 0; cb < 2; ++cb) {
-        uint32_t r[32];
-        tmem_ld32(tmem + lane_base + TM_O + cb * 32, r);
-        tmem_wait_ld();
+      uint32_t r[32];
+      tmem_ld32(tmem + lane_base + TM_O + half * 32, r);
+      tmem_wait_ld();
+      if (dv >= dv_lo && dv < dv_hi) {
+        __nv_bfloat16* op = p.out + (size_t)(c0 + half * 32) * HD + xcol + dv;
 #pragma unroll
-        for (int j = 0; j < 32; ++j) ost[(cb * 32 + j) * D + dv] = __float2bfloat16_rn(__uint_as_float(r[j]));
+        for (int j = 0; j < 32; ++j)
+          if (half * 32 + j < L) op[(size_t)j * HD] = __float2bfloat16_rn(__uint_as_float(r[j]));
       }
     }
     tc_fence_before();
-    __syncthreads();
-    for (int idx = tid; idx < C * 16; idx += NT) {
-      const int r = idx >> 4, v8 = idx & 15;
-      if (r < L && v8 * 8 >= dv_lo && v8 * 8 < dv_hi) {
-        const uint4 val = *reinterpret_cast<const uint4*>(sm + OFF_OST + r * 256 + v8 * 16);
-        *reinterpret_cast<uint4*>(p.out + (size_t)(c0 + r) * HD + xcol + v8 * 8) = val;
-      }
-    }
     __syncthreads();
   }
 
@@ -691,7 +726,7 @@ __global__ void __launch_bounds__(NT, 1)
     const int dv = my_lane;
     const bool mine = dv >= dv_lo && dv < dv_hi;
     for (int cb = 0; cb < 2; ++cb) {
-      const int dk0 = col_half * 64 + cb * 32;
+      const int dk0 = half * 64 + cb * 32;
       uint32_t r[32];
       tmem_ld32(tmem + lane_base + TM_S + dk0, r);
       tmem_wait_ld();
