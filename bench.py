@@ -241,10 +241,12 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--kernel", default="auto", choices=["auto", "tc", "ref"])
     ap.add_argument("--workload", type=int, default=1)
+    ap.add_argument("--n", type=int, default=None, help="sequences of the V-split workload (3)")
+    ap.add_argument("--vsplit", type=int, default=-1, help="-1 automatic, or 1/2/4/8")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=10)
     args = ap.parse_args()
-    w = W.workload(args.workload)
+    w = W.workload(args.workload, args.n) if args.workload == 3 else W.workload(args.workload)
     if args.impl == "reference":
         if args.steps <= 0:
             args.steps = 5
@@ -284,7 +286,7 @@ def main():
         kda.chunk_prefill_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], d["A_log"],
                               d["dt_bias"], d["lower_bound"], d["scale"], d["initial_state"],
                               d["cu_seqlens"], out=d["out"], final_state=d["fin"],
-                              workspace=d["ws"], stream=stream, kernel=kernel)
+                              workspace=d["ws"], stream=stream, kernel=kernel, vsplit=args.vsplit)
         if ev_pair is not None:
             ev_pair[1].record(stream)
 
@@ -393,7 +395,8 @@ def main():
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": w.name, "tokens": T, "seqs": N, "heads": H, "head_dim": D,
                    "state": w.state_dtype, "chunk": 64, "kernel": args.kernel,
-                   "l2": "inputs 352 MB > 129 MB L2, 4 input sets rotated",
+                   "vsplit": args.vsplit,
+                   "l2": f"inputs {algorithmic_bytes(w) / 1e6:.0f} MB per step, 4 input sets rotated",
                    "parallelism": f"replicas x{world}"},
         "us_per_layer": us,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",

@@ -1,6 +1,6 @@
 // tcgen05 + TMA chunked KDA prefill (KDA_KERNEL_TC), 64-token chunks.
 //
-// One CTA (256 threads, ~190 KB shared memory, 512 TMEM columns) owns one
+// One CTA (512 threads, ~207 KB shared memory, 512 TMEM columns) owns one
 // (sequence, head, value slice) and walks the sequence's chunks in order,
 // keeping the 128 x 128 fp32 state in tensor memory the whole time.
 //
@@ -50,7 +50,7 @@ using namespace sm100;
 
 constexpr int C = 64;
 constexpr int D = kHeadDim;
-constexpr int NT = 256;
+constexpr int NT = 512;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr int kMaxRankSeqs = 128;   // longest-first ordering for up to this many sequences
 
@@ -65,25 +65,28 @@ constexpr int OFF_CKC = OFF_RA + 32768;     //  [Kc; Kc2] K-major 96 rows x 128 
 constexpr int NS = 68;                      //  fp32 row stride of the T scratch (16-B rows)
 constexpr int OFF_NM = OFF_RA + 32768;      //  N = diag(b) strict(A)  [64][NS]  (after D)
 constexpr int OFF_TM = OFF_NM + 64 * NS * 4;//  T                      [64][NS]
-constexpr int OFF_Y = OFF_TM + 64 * NS * 4; //  products scratch       [32][36]
+constexpr int OFF_Y = OFF_TM + 64 * NS * 4; //  products scratch       [32][NS]
 constexpr int OFF_WN = OFF_RA + 32768;      //  -W MN-major, N = 64 tok, K = 128 (after T)
-constexpr int OFF_TB = OFF_RA + 73728;      //  T diag(b) K-major 64 x 64
-constexpr int OFF_QG = OFF_RA + 81920;      // Qg K-major 64 rows x 128 (B of O^T = S^T Qg^T)
+constexpr int OFF_TB = OFF_RA + 76800;      //  T diag(b/|k|) K-major 64 x 64 (for W)
+constexpr int OFF_TBU = OFF_RA + 84992;     //  T diag(b)     K-major 64 x 64 (for U')
+constexpr int OFF_QG = OFF_RA + 93184;      // Qg K-major 64 rows x 128 (B of O^T = S^T Qg^T)
 constexpr int OFF_KE = OFF_QG + 16384;      // Ke MN-major mn = dk, k = tok (B of S^T += U^T Ke)
 constexpr int OFF_QKB = OFF_KE + 16384;     // QK K-major 64 x 64 (B of O^T += U^T QK^T)
 constexpr int OFF_MISC = OFF_QKB + 8192;
-constexpr int OFF_INVN = OFF_MISC;          // inv |q| * scale [64], inv |k| [64]
+constexpr int OFF_INVN = OFF_MISC;          // scale / |q| [64], 1 / |k| [64]
 constexpr int OFF_BETA = OFF_MISC + 512;    // b [64]
 constexpr int OFF_DECAY = OFF_MISC + 768;   // 2^Gam_last [128]
-constexpr int OFF_WF = OFF_MISC + 1280;     // W factors [3][128]: 2^G0, 2^G2, 2^B0
-constexpr int OFF_GT = OFF_MISC + 2816;     // group totals [4][128] (also sequence lengths)
-constexpr int OFF_BAR = OFF_MISC + 4864;    // 3 mbarriers
-constexpr int OFF_TSLOT = OFF_MISC + 4896;  // TMEM base address
-constexpr int OFF_FLAGS = OFF_MISC + 4900;  // [0] sequence chosen for this CTA
-constexpr int SMEM_USED = OFF_MISC + 5120;
+constexpr int OFF_WF = OFF_MISC + 1280;     // W factors [3][128]: 2^alpha0, 2^alpha1, 2^B0
+constexpr int OFF_GT = OFF_MISC + 2816;     // 8-row group totals [8][128] (also sequence lengths)
+constexpr int OFF_PART = OFF_MISC + 6912;   // norm partial sums [16 warps][16]
+constexpr int OFF_BAR = OFF_MISC + 7936;    // 4 mbarriers
+constexpr int OFF_TSLOT = OFF_MISC + 7968;  // TMEM base address
+constexpr int OFF_FLAGS = OFF_MISC + 7972;  // [0] sequence chosen for this CTA
+constexpr int SMEM_USED = OFF_MISC + 8192;
 constexpr int SMEM_BYTES = SMEM_USED + 1024;
-static_assert(OFF_Y + 32 * 36 * 4 <= OFF_TB, "T scratch overlaps T diag(b)");
+static_assert(OFF_Y + 32 * NS * 4 <= OFF_TB, "T scratch overlaps T diag(b)");
 static_assert(OFF_CKC + 24576 <= OFF_TB, "operands overlap T diag(b)");
+static_assert(OFF_TBU + 8192 <= OFF_QG, "T tiles overlap Qg");
 static_assert(SMEM_BYTES <= 227 * 1024, "shared memory");
 
 // ---- TMEM columns (fp32 unless noted; lane = value channel, or key channel for D/W)
@@ -112,6 +115,12 @@ __device__ __forceinline__ float rcpf(float x) {
   return y;
 }
 __device__ __forceinline__ float sigm(float x) { return rcpf(1.0f + ex2f(-x * kLog2e)); }
+// bf16x2 product, rounded to nearest even
+__device__ __forceinline__ uint32_t bmul2(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  return r;
+}
 
 __device__ __forceinline__ void st_u32(unsigned char* base, uint32_t off, uint32_t v) {
   *reinterpret_cast<uint32_t*>(base + off) = v;
@@ -119,17 +128,13 @@ __device__ __forceinline__ void st_u32(unsigned char* base, uint32_t off, uint32
 __device__ __forceinline__ void st_u128(unsigned char* base, uint32_t off, uint4 v) {
   *reinterpret_cast<uint4*>(base + off) = v;
 }
-__device__ __forceinline__ float2 ld_bf16x2(const unsigned char* base, uint32_t off) {
-  const __nv_bfloat162 v = *reinterpret_cast<const __nv_bfloat162*>(base + off);
-  return __bfloat1622float2(v);
+__device__ __forceinline__ uint32_t ld_u32(const unsigned char* base, uint32_t off) {
+  return *reinterpret_cast<const uint32_t*>(base + off);
+}
+__device__ __forceinline__ float2 unpack_bf16x2(uint32_t v) {
+  return make_float2(__uint_as_float(v << 16), __uint_as_float(v & 0xffff0000u));
 }
 __device__ __forceinline__ float4 ld4(const float* p) { return *reinterpret_cast<const float4*>(p); }
-__device__ __forceinline__ void fma4(float4& acc, float a, const float4& b) {
-  acc.x = fmaf(a, b.x, acc.x);
-  acc.y = fmaf(a, b.y, acc.y);
-  acc.z = fmaf(a, b.z, acc.z);
-  acc.w = fmaf(a, b.w, acc.w);
-}
 
 // K-step descriptors
 __device__ __forceinline__ uint64_t kdesc(uint32_t tile, int rows, int ks) {
@@ -137,6 +142,34 @@ __device__ __forceinline__ uint64_t kdesc(uint32_t tile, int rows, int ks) {
 }
 __device__ __forceinline__ uint64_t mndesc(uint32_t tile, uint32_t lbo, int ks) {
   return sdesc_sw128(tile + ks * 2048, lbo, 1024);
+}
+
+// One warp: D(16 x 16) = -? A(16 x K) B(K x 16), fp32 smem matrices with row stride NS,
+// tf32 tensor-core products, K a multiple of 8.  Result written to `dst` (stride NS).
+template <int K>
+__device__ __forceinline__ void warp_gemm_16x16(const float* A, const float* B, float* dst,
+                                                float sign, int lane) {
+  const int g = lane >> 2, t = lane & 3;
+  float d0[4] = {0.f, 0.f, 0.f, 0.f}, d1[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+  for (int k0 = 0; k0 < K; k0 += 8) {
+    uint32_t a[4], b0[2], b1[2];
+    a[0] = to_tf32(A[g * NS + k0 + t]);
+    a[1] = to_tf32(A[(g + 8) * NS + k0 + t]);
+    a[2] = to_tf32(A[g * NS + k0 + t + 4]);
+    a[3] = to_tf32(A[(g + 8) * NS + k0 + t + 4]);
+    b0[0] = to_tf32(B[(k0 + t) * NS + g]);
+    b0[1] = to_tf32(B[(k0 + t + 4) * NS + g]);
+    b1[0] = to_tf32(B[(k0 + t) * NS + 8 + g]);
+    b1[1] = to_tf32(B[(k0 + t + 4) * NS + 8 + g]);
+    mma_tf32_16x8x8(d0, a, b0);
+    mma_tf32_16x8x8(d1, a, b1);
+  }
+  *reinterpret_cast<float2*>(dst + g * NS + 2 * t) = make_float2(sign * d0[0], sign * d0[1]);
+  *reinterpret_cast<float2*>(dst + (g + 8) * NS + 2 * t) = make_float2(sign * d0[2], sign * d0[3]);
+  *reinterpret_cast<float2*>(dst + g * NS + 8 + 2 * t) = make_float2(sign * d1[0], sign * d1[1]);
+  *reinterpret_cast<float2*>(dst + (g + 8) * NS + 8 + 2 * t) =
+      make_float2(sign * d1[2], sign * d1[3]);
 }
 
 __global__ void __launch_bounds__(NT, 1)
@@ -154,14 +187,16 @@ __global__ void __launch_bounds__(NT, 1)
   float* decay_s = reinterpret_cast<float*>(sm + OFF_DECAY);
   float* wf = reinterpret_cast<float*>(sm + OFF_WF);
   float* gt = reinterpret_cast<float*>(sm + OFF_GT);
+  float* part = reinterpret_cast<float*>(sm + OFF_PART);
   int* flags = reinterpret_cast<int*>(sm + OFF_FLAGS);
   uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + OFF_TSLOT);
   const uint32_t bar_qkg = sb + OFF_BAR, bar_v = bar_qkg + 8, bar_mma = bar_qkg + 16;
+  const uint32_t bar_o = bar_qkg + 24;      // O^T = S^T Qg^T, issued by warp 4
 
   // ---- work unit: (rank, head, part), longest sequence first
   const int P = p.vsplit, H = p.heads, N = p.num_seqs;
   const int unit = blockIdx.x;
-  const int part = unit % P;
+  const int vpart = unit % P;
   const int h = (unit / P) % H;
   const int rank = unit / (P * H);
   if (N <= kMaxRankSeqs) {
@@ -190,13 +225,14 @@ __global__ void __launch_bounds__(NT, 1)
     return;
   }
   const int DV = D / P;
-  const int dv_lo = part * DV, dv_hi = dv_lo + DV;
+  const int dv_lo = vpart * DV, dv_hi = dv_lo + DV;
 
   // ---- barriers and tensor memory
   if (tid == 0) {
     mbar_init(bar_qkg, 1);
     mbar_init(bar_v, 1);
     mbar_init(bar_mma, 1);
+    mbar_init(bar_o, 1);
     mbar_fence_init();
     tma_prefetch_desc(&tm_q);
     tma_prefetch_desc(&tm_k);
@@ -211,9 +247,10 @@ __global__ void __launch_bounds__(NT, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tslot;
-  const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
-  const int my_lane = 32 * (warp & 3) + lane;     // TMEM lane this thread reads
-  const int half = warp >> 2;                     // warps 4-7 take the second column half
+  const int q4 = warp & 3;                        // TMEM lane quadrant of this warp
+  const int cs = warp >> 2;                       // column slice (0..3) of this warp
+  const uint32_t lane_base = (uint32_t)(32 * q4) << 16;
+  const int my_lane = 32 * q4 + lane;             // TMEM lane this thread reads
 
   const size_t HD = (size_t)H * D;
   const size_t sbase = ((size_t)n * H + h) * D * D;
@@ -229,40 +266,41 @@ __global__ void __launch_bounds__(NT, 1)
     tma_load_2d(sb + OFF_INV + 8192, &tm_v, xcol + 64, t0, bar_v);
   }
 
-  // ---- state in: S^T[dv][dk] -> TMEM (lane = dv); this thread covers 64 key columns
+  // ---- state in: S^T[dv][dk] -> TMEM (lane = dv); this warp covers 32 key columns
   {
     const int dv = my_lane;
     const bool mine = dv >= dv_lo && dv < dv_hi && p.initial_state != nullptr;
-    for (int cb = 0; cb < 2; ++cb) {
-      const int dk0 = half * 64 + cb * 32;
-      uint32_t r[32];
+    const int dk0 = cs * 32;
+    uint32_t r[32];
 #pragma unroll
-      for (int j = 0; j < 32; ++j) {
-        float s = 0.0f;
-        if (mine) {
-          const size_t idx = sbase + (size_t)(dk0 + j) * D + dv;
-          s = p.state_bf16
-                  ? __bfloat162float(static_cast<const __nv_bfloat16*>(p.initial_state)[idx])
-                  : static_cast<const float*>(p.initial_state)[idx];
-        }
-        r[j] = __float_as_uint(s);
+    for (int j = 0; j < 32; ++j) {
+      float s = 0.0f;
+      if (mine) {
+        const size_t idx = sbase + (size_t)(dk0 + j) * D + dv;
+        s = p.state_bf16
+                ? __bfloat162float(static_cast<const __nv_bfloat16*>(p.initial_state)[idx])
+                : static_cast<const float*>(p.initial_state)[idx];
       }
-      tmem_st32(tmem + lane_base + TM_S + dk0, r);
+      r[j] = __float_as_uint(s);
     }
+    tmem_st32(tmem + lane_base + TM_S + dk0, r);
     tmem_wait_st();
   }
 
   const float gate_scale = expf(p.A_log[h]);
   const float lb2 = p.lower_bound * kLog2e;
   const int cp = tid & 63;            // channel pair of the gate/operand phase
-  const int grp = tid >> 6;           // 16-row group of the gate/operand phase
+  const int grp = tid >> 6;           // 8-row group of the gate/operand phase
   const int d0 = 2 * cp;
-  const float db0 = p.dt_bias[h * D + d0], db1 = p.dt_bias[h * D + d0 + 1];
+  const int blk = grp >> 2;           // 32-token block of the group
+  // sigmoid argument in log2 units: -gate_scale * log2e * (g + dt_bias)
+  const float sg = -gate_scale * kLog2e;
+  const float sg0 = sg * p.dt_bias[h * D + d0], sg1 = sg * p.dt_bias[h * D + d0 + 1];
   float* Nm = reinterpret_cast<float*>(sm + OFF_NM);
   float* Tm = reinterpret_cast<float*>(sm + OFF_TM);
   float* Y = reinterpret_cast<float*>(sm + OFF_Y);
 
-  uint32_t ph_qkg = 0, ph_v = 0, ph_mma = 0;
+  uint32_t ph_qkg = 0, ph_v = 0, ph_mma = 0, ph_o = 0;
   bool failed = false;
   int site = 0;
   // beta logits are fetched one chunk ahead (their load latency hides behind a chunk)
@@ -273,48 +311,32 @@ __global__ void __launch_bounds__(NT, 1)
     const int L = min(C, t1 - c0);
     const bool more = c0 + C < t1;
 
-    // ---- P0: q, k, g of this chunk have landed
-    {
-      const bool ok = mbar_wait(bar_qkg, ph_qkg);
-      ph_qkg ^= 1;
-      if (__syncthreads_or(!ok)) { failed = true; site = 10; break; }
-    }
-
-    // ---- P1: beta and the row norms of q and k (one warp per row)
+    // ---- P0: q, k, g of this chunk have landed (every thread waits for the TMA itself;
+    //          a timeout is acted on at the next barrier); beta; zero q/k rows past the end
+    const bool tma_ok = mbar_wait(bar_qkg, ph_qkg);
+    ph_qkg ^= 1;
     if (tid < C) {
       beta_s[tid] = (tid < L) ? sigm(b_raw) : 0.0f;
       if (c0 + C + tid < t1) b_raw = __bfloat162float(p.beta[(size_t)(c0 + C + tid) * H + h]);
     }
-    for (int r = warp * 8; r < warp * 8 + 8; ++r) {
-      const uint2 qv = *reinterpret_cast<const uint2*>(sm + OFF_INQ + r * 256 + lane * 8);
-      const uint2 kv = *reinterpret_cast<const uint2*>(sm + OFF_INK + r * 256 + lane * 8);
-      const float2 q01 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&qv.x));
-      const float2 q23 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&qv.y));
-      const float2 k01 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&kv.x));
-      const float2 k23 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&kv.y));
-      float sq = q01.x * q01.x + q01.y * q01.y + q23.x * q23.x + q23.y * q23.y;
-      float sk = k01.x * k01.x + k01.y * k01.y + k23.x * k23.x + k23.y * k23.y;
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {
-        sq += __shfl_xor_sync(0xffffffffu, sq, o);
-        sk += __shfl_xor_sync(0xffffffffu, sk, o);
-      }
-      if (lane == 0) {
-        inv_q[r] = (r < L) ? p.scale * rsqrtf(sq + kL2Eps) : 0.0f;
-        inv_k[r] = (r < L) ? rsqrtf(sk + kL2Eps) : 0.0f;
+    if (L < C) {
+      for (int idx = tid; idx < (C - L) * 32; idx += NT) {
+        const int r = L + (idx >> 5), c16 = idx & 31;
+        st_u128(sm, (c16 < 16 ? OFF_INQ : OFF_INK) + r * 256 + (c16 & 15) * 16,
+                make_uint4(0, 0, 0, 0));
       }
     }
 
-    // ---- P2a: gate -> log2 decay, cumsum inside this thread's 16-row group
-    float cl0[16], cl1[16];
+    // ---- P2a: gate -> log2 decay, cumsum inside this thread's 8-row group
+    float cl0[8], cl1[8];
     {
       float run0 = 0.0f, run1 = 0.0f;
 #pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        const int r = grp * 16 + i;
-        const float2 gv = ld_bf16x2(sm + OFF_ING, (uint32_t)(r * 256 + d0 * 2));
-        float a0 = lb2 * sigm(gate_scale * (gv.x + db0));
-        float a1 = lb2 * sigm(gate_scale * (gv.y + db1));
+      for (int i = 0; i < 8; ++i) {
+        const int r = grp * 8 + i;
+        const float2 gv = unpack_bf16x2(ld_u32(sm + OFF_ING, (uint32_t)(r * 256 + d0 * 2)));
+        float a0 = lb2 * rcpf(1.0f + ex2f(fmaf(gv.x, sg, sg0)));
+        float a1 = lb2 * rcpf(1.0f + ex2f(fmaf(gv.y, sg, sg1)));
         a0 = (r < L) ? a0 : 0.0f;
         a1 = (r < L) ? a1 : 0.0f;
         run0 += a0;
@@ -322,55 +344,60 @@ __global__ void __launch_bounds__(NT, 1)
         cl0[i] = run0;
         cl1[i] = run1;
       }
-      gt[grp * 128 + d0] = run0;
-      gt[grp * 128 + d0 + 1] = run1;
+      *reinterpret_cast<float2*>(gt + grp * 128 + d0) = make_float2(run0, run1);
     }
-    __syncthreads();
+    if (__syncthreads_or(!tma_ok)) { failed = true; site = 10; break; }
 
-    // ---- P2b: anchored factors and the bf16 operand tiles [Kr; Qr], [Kc; Kc2], Qg, Ke
+    // ---- P2b: anchored factors, bf16 operand tiles of the raw q, k (their norms are
+    //           applied to the products later), and the partial sums of squares
     {
-      const bool blk1 = grp >= 2;
       float mE[2], cA[2], cB[2], cX[2], cR[2];
 #pragma unroll
       for (int c = 0; c < 2; ++c) {
-        const float G0 = gt[d0 + c], G1 = gt[128 + d0 + c];
-        const float G2 = gt[256 + d0 + c], G3 = gt[384 + d0 + c];
-        const float B0 = G0 + G1, B1 = G2 + G3;
-        const float Gown = blk1 ? (grp == 2 ? G2 : G3) : (grp == 0 ? G0 : G1);
-        mE[c] = (grp & 1) ? 0.0f : Gown;
-        // block 0: cA = 2^G0 (E -> 2^Gam), cB = 2^G1 (Ei -> 2^(B0 - c)), cR = 2^B1
-        // block 1: cA = 2^G2 (E -> 2^c),   cB = 2^G3 (Ei -> 2^(B1 - c)), cR = 2^B0
-        cA[c] = ex2f(blk1 ? G2 : G0);
-        cB[c] = ex2f(blk1 ? G3 : G1);
-        cX[c] = ex2f(G2);                 // alpha_1, folded into Kc2
-        cR[c] = ex2f(blk1 ? B0 : B1);
+        float G[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) G[j] = gt[j * 128 + d0 + c];
+        const float B0 = (G[0] + G[1]) + (G[2] + G[3]);
+        const float B1 = (G[4] + G[5]) + (G[6] + G[7]);
+        const float al0 = G[0] + G[1], al1 = G[4] + G[5];
+        float pre = 0.0f;                          // totals of earlier groups of the block
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+          if ((j >> 2) == blk && j < grp) pre += G[j];
+        const float al = blk ? al1 : al0;
+        mE[c] = al - pre;                          // exponent of E = cl - mE
+        cA[c] = ex2f(al);                          // E -> 2^c (within the block)
+        cB[c] = ex2f((blk ? B1 : B0) - al);        // Ei -> 2^(B_blk - c)
+        cX[c] = ex2f(al1);                         // alpha_1, folded into Kc2
+        cR[c] = ex2f(blk ? B0 : B1);               // the other block's total
         if (grp == 0) {
           decay_s[d0 + c] = ex2f(B0 + B1);
-          wf[d0 + c] = cA[c];              // W block 0: 2^G0
-          wf[128 + d0 + c] = cX[c];        // W block 1: 2^G2, then
-          wf[256 + d0 + c] = ex2f(B0);     //            2^B0
+          wf[d0 + c] = cA[c];                      // W block 0: 2^alpha0
+          wf[128 + d0 + c] = cX[c];                // W block 1: 2^alpha1, then
+          wf[256 + d0 + c] = ex2f(B0);             //            2^B0
         }
       }
+      float sq[8], sk[8];
 #pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        const int r = grp * 16 + i;
-        const float iq = inv_q[r], ik = inv_k[r];
-        const float2 qv = ld_bf16x2(sm + OFF_INQ, (uint32_t)(r * 256 + d0 * 2));
-        const float2 kv = ld_bf16x2(sm + OFF_INK, (uint32_t)(r * 256 + d0 * 2));
-        const bool live = r < L;
-        const float qh0 = live ? qv.x * iq : 0.0f, qh1 = live ? qv.y * iq : 0.0f;
-        const float kh0 = live ? kv.x * ik : 0.0f, kh1 = live ? kv.y * ik : 0.0f;
+      for (int i = 0; i < 8; ++i) {
+        const int r = grp * 8 + i;
+        const uint32_t q2 = ld_u32(sm + OFF_INQ, (uint32_t)(r * 256 + d0 * 2));
+        const uint32_t k2 = ld_u32(sm + OFF_INK, (uint32_t)(r * 256 + d0 * 2));
+        const float2 qf = unpack_bf16x2(q2), kf = unpack_bf16x2(k2);
+        sq[i] = fmaf(qf.x, qf.x, qf.y * qf.y);
+        sk[i] = fmaf(kf.x, kf.x, kf.y * kf.y);
         const float e0 = cl0[i] - mE[0], e1 = cl1[i] - mE[1];
         const float E0 = ex2f(e0), E1 = ex2f(e1);
         const float Ei0 = ex2f(-e0), Ei1 = ex2f(-e1);
-        st_u32(sm, OFF_RKQ + kmajor_off(r, d0, 128), pack_bf16x2(kh0 * E0, kh1 * E1));
-        st_u32(sm, OFF_RKQ + kmajor_off(64 + r, d0, 128), pack_bf16x2(qh0 * E0, qh1 * E1));
-        st_u32(sm, OFF_CKC + kmajor_off(r, d0, 96), pack_bf16x2(kh0 * Ei0, kh1 * Ei1));
+        const uint32_t E2 = pack_bf16x2(E0, E1), Ei2 = pack_bf16x2(Ei0, Ei1);
+        st_u32(sm, OFF_RKQ + kmajor_off(r, d0, 128), bmul2(k2, E2));
+        st_u32(sm, OFF_RKQ + kmajor_off(64 + r, d0, 128), bmul2(q2, E2));
+        st_u32(sm, OFF_CKC + kmajor_off(r, d0, 96), bmul2(k2, Ei2));
         float g0, g1, ke0, ke1;
-        if (!blk1) {
+        if (blk == 0) {
           const float oc0 = Ei0 * cB[0], oc1 = Ei1 * cB[1];    // 2^(B0 - c_s)
           st_u32(sm, OFF_CKC + kmajor_off(64 + r, d0, 96),
-                 pack_bf16x2(kh0 * (oc0 * cX[0]), kh1 * (oc1 * cX[1])));
+                 bmul2(k2, pack_bf16x2(oc0 * cX[0], oc1 * cX[1])));
           g0 = E0 * cA[0];
           g1 = E1 * cA[1];
           ke0 = oc0 * cR[0];
@@ -381,15 +408,38 @@ __global__ void __launch_bounds__(NT, 1)
           ke0 = Ei0 * cB[0];
           ke1 = Ei1 * cB[1];
         }
-        st_u32(sm, OFF_QG + kmajor_off(r, d0, 64), pack_bf16x2(qh0 * g0, qh1 * g1));
-        st_u32(sm, OFF_KE + mnmajor_off(d0, r, 8192), pack_bf16x2(kh0 * ke0, kh1 * ke1));
+        st_u32(sm, OFF_QG + kmajor_off(r, d0, 64), bmul2(q2, pack_bf16x2(g0, g1)));
+        st_u32(sm, OFF_KE + mnmajor_off(d0, r, 8192), bmul2(k2, pack_bf16x2(ke0, ke1)));
+      }
+      // reduce-scatter the 16 partial sums (8 rows x q, k) over the warp's 32 lanes
+      float v[16];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        v[i] = sq[i];
+        v[8 + i] = sk[i];
+      }
+#pragma unroll
+      for (int o = 16, m = 8; o >= 2; o >>= 1, m >>= 1) {
+        const bool up = (lane & o) != 0;
+#pragma unroll
+        for (int i = 0; i < m; ++i) {
+          const float send = up ? v[i] : v[i + m];
+          const float keep = up ? v[i + m] : v[i];
+          v[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+        }
+      }
+      v[0] += __shfl_xor_sync(0xffffffffu, v[0], 1);
+      if ((lane & 1) == 0) {
+        const int idx = ((lane >> 4) & 1) * 8 + ((lane >> 3) & 1) * 4 + ((lane >> 2) & 1) * 2 +
+                        ((lane >> 1) & 1);
+        part[warp * 16 + idx] = v[0];
       }
     }
     fence_proxy_async();
     __syncthreads();
 
     // ---- P3: D = [Kr; Qr] [Kc; Kc2]^T on the tensor cores; fetch the next q, k, g.
-    //          Warps 4-7 meanwhile make the bf16 copy of S^T and apply this chunk's decay.
+    //          Meanwhile: norms of q and k.
     if (tid == 0) {
       tc_fence_after();
 #pragma unroll
@@ -404,8 +454,124 @@ __global__ void __launch_bounds__(NT, 1)
         tma_load_2d(sb + OFF_ING, &tm_g, xcol, c0 + C, bar_qkg);
       }
     }
-    if (half == 1) {
-      for (int cb = 0; cb < 4; ++cb) {      // 32 key columns per pass
+    if (tid < 128) {   // row r = tid & 63 of q (tid < 64) or k
+      const int r = tid & 63, t = tid >> 6;
+      const int g8 = r >> 3, i = r & 7;
+      const float ss = part[(2 * g8) * 16 + t * 8 + i] + part[(2 * g8 + 1) * 16 + t * 8 + i];
+      const float inv = (r < L) ? rsqrtf(ss + kL2Eps) : 0.0f;
+      inv_q[t * 64 + r] = (t == 0) ? p.scale * inv : inv;
+    }
+    {
+      // one thread waits for the MMA (the others park on the barrier); all see the v tile land
+      const bool ok = (tid != 0 || mbar_wait(bar_mma, ph_mma)) && mbar_wait(bar_v, ph_v);
+      ph_mma ^= 1;
+      ph_v ^= 1;
+      tc_fence_before();
+      if (__syncthreads_or(!ok)) { failed = true; site = 30; break; }
+    }
+    tc_fence_after();
+
+    // ---- P4a: A rows (lanes 0-63) -> N = diag(b/|k|) strict(A) diag(1/|k|);
+    //           QK rows (64-127) -> bf16 tile (raw); other warps: v tail rows, T upper blocks
+    if (cs < 2) {
+      const int r = my_lane & 63;
+      uint32_t a[32];
+      // columns 0-31 of rows 32-63 come from D[:, 64:96] (the off-diagonal block)
+      tmem_ld32(tmem + lane_base + TM_D + ((cs == 0 && r >= 32) ? 64 : 32 * cs), a);
+      tmem_wait_ld();
+      if (q4 < 2) {
+        const float br = beta_s[r] * inv_k[r];
+#pragma unroll
+        for (int s4 = 0; s4 < 8; ++s4) {
+          const float4 ik = ld4(inv_k + 32 * cs + 4 * s4);
+          const float ikv[4] = {ik.x, ik.y, ik.z, ik.w};
+          float vv[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int s = 32 * cs + 4 * s4 + e;
+            vv[e] = (s < r) ? br * ikv[e] * __uint_as_float(a[4 * s4 + e]) : 0.0f;
+          }
+          *reinterpret_cast<float4*>(Nm + r * NS + 32 * cs + 4 * s4) =
+              make_float4(vv[0], vv[1], vv[2], vv[3]);
+        }
+      } else {
+#pragma unroll
+        for (int c8 = 0; c8 < 4; ++c8) {
+          uint32_t w[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int s = 32 * cs + c8 * 8 + e * 2;
+            w[e] = pack_bf16x2(s <= r ? __uint_as_float(a[c8 * 8 + e * 2]) : 0.0f,
+                               s + 1 <= r ? __uint_as_float(a[c8 * 8 + e * 2 + 1]) : 0.0f);
+          }
+          st_u128(sm, OFF_QKB + kmajor_off(r, 32 * cs + c8 * 8, 64),
+                  make_uint4(w[0], w[1], w[2], w[3]));
+        }
+      }
+    } else {
+      const int t8 = tid - 256;
+      if (L < C) {   // v rows past the sequence end -> 0 (both 64-column boxes)
+        for (int idx = t8; idx < (C - L) * 16; idx += 256) {
+          const int r = L + idx / 16, cc = idx % 16;
+          st_u128(sm, OFF_INV + (cc >> 3) * 8192 + r * 128 + (cc & 7) * 16, make_uint4(0, 0, 0, 0));
+        }
+      }
+      // T above the diagonal 16x16 blocks is zero
+      for (int idx = t8; idx < 6 * 64; idx += 256) {
+        const int b = idx >> 6, e = idx & 63;
+        const int bi = (b < 3) ? 0 : (b < 5 ? 1 : 2);
+        const int bj = (b < 3) ? b + 1 : (b < 5 ? b - 1 : 3);
+        *reinterpret_cast<float4*>(Tm + (bi * 16 + (e >> 2)) * NS + bj * 16 + 4 * (e & 3)) =
+            make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+    }
+    fence_proxy_async();
+    tc_fence_before();
+    __syncthreads();
+
+    // ---- P4b: T = (I + N)^-1 on warps 0-1: 16x16 diagonal blocks by substitution (fp32),
+    //           then the off-diagonal blocks as tf32 tensor-core products, 16 -> 32 -> 64.
+    //           Warps 4-7 meanwhile make the bf16 copy of S^T and apply this chunk's decay.
+    if (warp < 4) {
+      if (warp < 2) {
+        const int o = (tid >> 4) * 16, j = tid & 15;
+        float x[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          float acc = (i == j) ? 1.0f : 0.0f;
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            if (4 * q < i) {
+              const float4 nv = ld4(Nm + (o + i) * NS + o + 4 * q);
+              if (4 * q + 0 < i) acc -= nv.x * x[4 * q + 0];
+              if (4 * q + 1 < i) acc -= nv.y * x[4 * q + 1];
+              if (4 * q + 2 < i) acc -= nv.z * x[4 * q + 2];
+              if (4 * q + 3 < i) acc -= nv.w * x[4 * q + 3];
+            }
+          }
+          x[i] = acc;
+        }
+#pragma unroll
+        for (int i = 0; i < 16; ++i) Tm[(o + i) * NS + o + j] = x[i];
+      }
+      named_barrier_sync(1, 128);
+      if (warp < 2) {   // pair (1,0) on warp 0, (3,2) on warp 1: T_rc = -T_rr (N_rc T_cc)
+        const int ro = (2 * warp + 1) * 16, co = 2 * warp * 16;
+        float* Yw = Y + warp * 16 * NS;
+        warp_gemm_16x16<16>(Nm + ro * NS + co, Tm + co * NS + co, Yw, 1.0f, lane);
+        __syncwarp();
+        warp_gemm_16x16<16>(Tm + ro * NS + ro, Yw, Tm + ro * NS + co, -1.0f, lane);
+      }
+      named_barrier_sync(1, 128);
+      const int mi = warp >> 1, ni = warp & 1;   // Y2 = N[32:64, 0:32] T[0:32, 0:32]
+      warp_gemm_16x16<32>(Nm + (32 + 16 * mi) * NS, Tm + 16 * ni, Y + 16 * mi * NS + 16 * ni,
+                          1.0f, lane);
+      named_barrier_sync(1, 128);               // T[32:64, 0:32] = -T[32:64, 32:64] Y2
+      warp_gemm_16x16<32>(Tm + (32 + 16 * mi) * NS + 32, Y + 16 * ni,
+                          Tm + (32 + 16 * mi) * NS + 16 * ni, -1.0f, lane);
+    } else if (warp >= 4 && warp < 8) {
+#pragma unroll 1
+      for (int cb = 0; cb < 4; ++cb) {   // state pass: 32 key columns at a time
         uint32_t x[32], pk[16];
         tmem_ld32(tmem + lane_base + TM_S + cb * 32, x);
         tmem_wait_ld();
@@ -424,174 +590,42 @@ __global__ void __launch_bounds__(NT, 1)
         tmem_st32(tmem + lane_base + TM_S + cb * 32, x);
       }
       tmem_wait_st();
-    }
-    {
-      const bool ok = mbar_wait(bar_mma, ph_mma) && mbar_wait(bar_v, ph_v);
-      ph_mma ^= 1;
-      ph_v ^= 1;
+      // O^T = S^T Qg^T needs only the bf16 state: issue it now, it overlaps the T inverse
       tc_fence_before();
-      if (__syncthreads_or(!ok)) { failed = true; site = 30; break; }
-    }
-    tc_fence_after();
-
-    // ---- P4a: A rows (lanes 0-63) -> N = diag(b) strict(A); QK rows (64-127) -> bf16 tile;
-    //            warps 4-7 clear v rows past the sequence end and T above the diagonal blocks
-    if (half == 0) {
-      // columns 0-31 come from D[:, 64:96] for rows 32-63 (the off-diagonal block)
-      const int r = my_lane & 63;
-      const bool use2 = r >= 32;
-      for (int cb = 0; cb < 2; ++cb) {
-        uint32_t a[32];
-        tmem_ld32(tmem + lane_base + TM_D + ((cb == 0 && use2) ? 64 : 32 * cb), a);
-        tmem_wait_ld();
-        if (warp < 2) {
-          const float br = beta_s[r];
+      named_barrier_sync(2, 128);
+      if (tid == 128) {
+        tc_fence_after();
 #pragma unroll
-          for (int s4 = 0; s4 < 8; ++s4) {
-            float v[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const int s = 32 * cb + 4 * s4 + e;
-              v[e] = (s < r) ? br * __uint_as_float(a[4 * s4 + e]) : 0.0f;
-            }
-            *reinterpret_cast<float4*>(Nm + r * NS + 32 * cb + 4 * s4) =
-                make_float4(v[0], v[1], v[2], v[3]);
-          }
-        } else {
-#pragma unroll
-          for (int c8 = 0; c8 < 4; ++c8) {
-            uint32_t w[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const int s = 32 * cb + c8 * 8 + e * 2;
-              w[e] = pack_bf16x2(s <= r ? __uint_as_float(a[c8 * 8 + e * 2]) : 0.0f,
-                                 s + 1 <= r ? __uint_as_float(a[c8 * 8 + e * 2 + 1]) : 0.0f);
-            }
-            st_u128(sm, OFF_QKB + kmajor_off(r, 32 * cb + c8 * 8, 64),
-                    make_uint4(w[0], w[1], w[2], w[3]));
-          }
-        }
-      }
-    } else {
-      const int t4 = tid - 128;
-      if (L < C) {   // v rows past the sequence end -> 0 (both 64-column boxes)
-        for (int idx = t4; idx < (C - L) * 16; idx += 128) {
-          const int r = L + idx / 16, cc = idx % 16;
-          st_u128(sm, OFF_INV + (cc >> 3) * 8192 + r * 128 + (cc & 7) * 16, make_uint4(0, 0, 0, 0));
-        }
-      }
-      // T above the diagonal 16x16 blocks is zero
-      for (int idx = t4; idx < 6 * 64; idx += 128) {
-        const int b = idx >> 6, e = idx & 63;
-        const int bi = (b < 3) ? 0 : (b < 5 ? 1 : 2);
-        const int bj = (b < 3) ? b + 1 : (b < 5 ? b - 1 : 3);
-        *reinterpret_cast<float4*>(Tm + (bi * 16 + (e >> 2)) * NS + bj * 16 + 4 * (e & 3)) =
-            make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int ks = 0; ks < 8; ++ks)
+          mma_bf16_ts(tmem + TM_O, tmem + TM_SB + 8 * ks, kdesc(sb + OFF_QG, 64, ks), ID_KK64,
+                      ks > 0);
+        mma_commit(bar_o);
       }
     }
-    fence_proxy_async();
     tc_fence_before();
     __syncthreads();
-
-    // ---- P4b: T = (I + N)^-1, blocked: 16x16 diagonal blocks, then 32, then 64
-    if (tid < 64) {
-      const int o = (tid >> 4) * 16, j = tid & 15;
-      float x[16];
-#pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        float acc = (i == j) ? 1.0f : 0.0f;
-#pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4) {
-          if (4 * q4 < i) {
-            const float4 nv = ld4(Nm + (o + i) * NS + o + 4 * q4);
-            if (4 * q4 + 0 < i) acc -= nv.x * x[4 * q4 + 0];
-            if (4 * q4 + 1 < i) acc -= nv.y * x[4 * q4 + 1];
-            if (4 * q4 + 2 < i) acc -= nv.z * x[4 * q4 + 2];
-            if (4 * q4 + 3 < i) acc -= nv.w * x[4 * q4 + 3];
-          }
-        }
-        x[i] = acc;
-      }
-#pragma unroll
-      for (int i = 0; i < 16; ++i) Tm[(o + i) * NS + o + j] = x[i];
-    }
-    __syncthreads();
-    if (tid < 128) {   // Y_b = N[rows of b] T[diag block of b], pairs b = (1,0) and (3,2)
-      const int b = tid >> 6, i = (tid >> 2) & 15, jq = tid & 3;
-      const int ro = (2 * b + 1) * 16, co = 2 * b * 16;
-      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-      for (int s4 = 0; s4 < 4; ++s4) {
-        const float4 nv = ld4(Nm + (ro + i) * NS + co + 4 * s4);
-        fma4(acc, nv.x, ld4(Tm + (co + 4 * s4 + 0) * NS + co + 4 * jq));
-        fma4(acc, nv.y, ld4(Tm + (co + 4 * s4 + 1) * NS + co + 4 * jq));
-        fma4(acc, nv.z, ld4(Tm + (co + 4 * s4 + 2) * NS + co + 4 * jq));
-        fma4(acc, nv.w, ld4(Tm + (co + 4 * s4 + 3) * NS + co + 4 * jq));
-      }
-      *reinterpret_cast<float4*>(Y + (b * 16 + i) * 20 + 4 * jq) = acc;
-    }
-    __syncthreads();
-    if (tid < 128) {   // T[lower of b] = -T[diag of b, rows] Y_b
-      const int b = tid >> 6, i = (tid >> 2) & 15, jq = tid & 3;
-      const int ro = (2 * b + 1) * 16, co = 2 * b * 16;
-      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-      for (int s4 = 0; s4 < 4; ++s4) {
-        const float4 tv = ld4(Tm + (ro + i) * NS + ro + 4 * s4);
-        fma4(acc, tv.x, ld4(Y + (b * 16 + 4 * s4 + 0) * 20 + 4 * jq));
-        fma4(acc, tv.y, ld4(Y + (b * 16 + 4 * s4 + 1) * 20 + 4 * jq));
-        fma4(acc, tv.z, ld4(Y + (b * 16 + 4 * s4 + 2) * 20 + 4 * jq));
-        fma4(acc, tv.w, ld4(Y + (b * 16 + 4 * s4 + 3) * 20 + 4 * jq));
-      }
-      *reinterpret_cast<float4*>(Tm + (ro + i) * NS + co + 4 * jq) =
-          make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
-    }
-    __syncthreads();
-    {   // Y2 = N[32:64, 0:32] T[0:32, 0:32]
-      const int i = tid >> 3, jq = tid & 7;
-      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-      for (int s4 = 0; s4 < 8; ++s4) {
-        const float4 nv = ld4(Nm + (32 + i) * NS + 4 * s4);
-        fma4(acc, nv.x, ld4(Tm + (4 * s4 + 0) * NS + 4 * jq));
-        fma4(acc, nv.y, ld4(Tm + (4 * s4 + 1) * NS + 4 * jq));
-        fma4(acc, nv.z, ld4(Tm + (4 * s4 + 2) * NS + 4 * jq));
-        fma4(acc, nv.w, ld4(Tm + (4 * s4 + 3) * NS + 4 * jq));
-      }
-      *reinterpret_cast<float4*>(Y + i * 36 + 4 * jq) = acc;
-    }
-    __syncthreads();
-    {   // T[32:64, 0:32] = -T[32:64, 32:64] Y2
-      const int i = tid >> 3, jq = tid & 7;
-      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-      for (int s4 = 0; s4 < 8; ++s4) {
-        const float4 tv = ld4(Tm + (32 + i) * NS + 32 + 4 * s4);
-        fma4(acc, tv.x, ld4(Y + (4 * s4 + 0) * 36 + 4 * jq));
-        fma4(acc, tv.y, ld4(Y + (4 * s4 + 1) * 36 + 4 * jq));
-        fma4(acc, tv.z, ld4(Y + (4 * s4 + 2) * 36 + 4 * jq));
-        fma4(acc, tv.w, ld4(Y + (4 * s4 + 3) * 36 + 4 * jq));
-      }
-      *reinterpret_cast<float4*>(Tm + (32 + i) * NS + 4 * jq) =
-          make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
-    }
-    __syncthreads();
-    // T diag(b) -> bf16 (K-major, row r, k = s)
-    for (int idx = tid; idx < 512; idx += NT) {
-      const int r = idx >> 3, c8 = idx & 7;
-      const float4 t0v = ld4(Tm + r * NS + c8 * 8), t1v = ld4(Tm + r * NS + c8 * 8 + 4);
+    {   // T diag(b) and T diag(b / |k|) -> bf16 (K-major, row r, k = s), 8 columns per thread
+      const int r = tid >> 3, c8 = tid & 7;
+      float4 t0v = ld4(Tm + r * NS + c8 * 8), t1v = ld4(Tm + r * NS + c8 * 8 + 4);
       const float4 b0v = ld4(beta_s + c8 * 8), b1v = ld4(beta_s + c8 * 8 + 4);
-      st_u128(sm, OFF_TB + kmajor_off(r, c8 * 8, 64),
-              make_uint4(pack_bf16x2(t0v.x * b0v.x, t0v.y * b0v.y),
-                         pack_bf16x2(t0v.z * b0v.z, t0v.w * b0v.w),
-                         pack_bf16x2(t1v.x * b1v.x, t1v.y * b1v.y),
-                         pack_bf16x2(t1v.z * b1v.z, t1v.w * b1v.w)));
+      const float4 k0v = ld4(inv_k + c8 * 8), k1v = ld4(inv_k + c8 * 8 + 4);
+      t0v = make_float4(t0v.x * b0v.x, t0v.y * b0v.y, t0v.z * b0v.z, t0v.w * b0v.w);
+      t1v = make_float4(t1v.x * b1v.x, t1v.y * b1v.y, t1v.z * b1v.z, t1v.w * b1v.w);
+      const uint32_t off = kmajor_off(r, c8 * 8, 64);
+      st_u128(sm, OFF_TBU + off,
+              make_uint4(pack_bf16x2(t0v.x, t0v.y), pack_bf16x2(t0v.z, t0v.w),
+                         pack_bf16x2(t1v.x, t1v.y), pack_bf16x2(t1v.z, t1v.w)));
+      st_u128(sm, OFF_TB + off,
+              make_uint4(pack_bf16x2(t0v.x * k0v.x, t0v.y * k0v.y),
+                         pack_bf16x2(t0v.z * k0v.z, t0v.w * k0v.w),
+                         pack_bf16x2(t1v.x * k1v.x, t1v.y * k1v.y),
+                         pack_bf16x2(t1v.z * k1v.z, t1v.w * k1v.w)));
     }
     fence_proxy_async();
     __syncthreads();
 
-    // ---- P5: W_b^T = (Kr rows of block b)^T (T diag b)[:, b]^T for b = 0, 1 (D region);
-    //          U'^T = V^T (T diag b)^T;  O^T = S^T Qg^T
+    // ---- P5: W_b^T = (raw Kr rows of block b)^T (T diag(b/|k|))[:, b]^T (D region);
+    //          U'^T = V^T (T diag(b))^T
     if (tid == 0) {
       tc_fence_after();
 #pragma unroll
@@ -602,16 +636,12 @@ __global__ void __launch_bounds__(NT, 1)
                    kdesc(sb + OFF_TB, 64, 2 * b + ks), ID_MK64, ks > 0);
 #pragma unroll
       for (int ks = 0; ks < 4; ++ks)
-        mma_bf16(tmem + TM_U, mndesc(sb + OFF_INV, 8192, ks), kdesc(sb + OFF_TB, 64, ks),
+        mma_bf16(tmem + TM_U, mndesc(sb + OFF_INV, 8192, ks), kdesc(sb + OFF_TBU, 64, ks),
                  ID_MK64, ks > 0);
-#pragma unroll
-      for (int ks = 0; ks < 8; ++ks)
-        mma_bf16_ts(tmem + TM_O, tmem + TM_SB + 8 * ks, kdesc(sb + OFF_QG, 64, ks), ID_KK64,
-                    ks > 0);
       mma_commit(bar_mma);
     }
     {
-      const bool ok = mbar_wait(bar_mma, ph_mma);
+      const bool ok = tid != 0 || mbar_wait(bar_mma, ph_mma);
       ph_mma ^= 1;
       if (__syncthreads_or(!ok)) { failed = true; site = 50; break; }
     }
@@ -622,16 +652,16 @@ __global__ void __launch_bounds__(NT, 1)
       tma_load_2d(sb + OFF_INV + 8192, &tm_v, xcol + 64, c0 + C, bar_v);
     }
 
-    // ---- P6: -W = -(2^G0 W0 + 2^B0 (2^G2 W1)) -> bf16, MN-major (n = token, k = dk)
+    // ---- P6: -W = -(2^a0 W0 + 2^B0 (2^a1 W1)) -> bf16, MN-major (n = token, k = dk)
     {
       const int dk = my_lane;
       const float f0 = wf[dk], f1a = wf[128 + dk], f1b = wf[256 + dk];
-      uint32_t w0[32], w1[32];
-      tmem_ld32(tmem + lane_base + TM_D + half * 32, w0);
-      tmem_ld32(tmem + lane_base + TM_D + 64 + half * 32, w1);
+      uint32_t w0[16], w1[16];
+      tmem_ld16(tmem + lane_base + TM_D + cs * 16, w0);
+      tmem_ld16(tmem + lane_base + TM_D + 64 + cs * 16, w1);
       tmem_wait_ld();
 #pragma unroll
-      for (int c8 = 0; c8 < 4; ++c8) {
+      for (int c8 = 0; c8 < 2; ++c8) {
         uint32_t w[4];
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
@@ -641,7 +671,7 @@ __global__ void __launch_bounds__(NT, 1)
               f0 * __uint_as_float(w0[j + 1]) + f1b * (f1a * __uint_as_float(w1[j + 1]));
           w[e] = pack_bf16x2(-x0, -x1);
         }
-        st_u128(sm, OFF_WN + mnmajor_off(half * 32 + c8 * 8, dk, 8192),
+        st_u128(sm, OFF_WN + mnmajor_off(cs * 16 + c8 * 8, dk, 8192),
                 make_uint4(w[0], w[1], w[2], w[3]));
       }
     }
@@ -659,59 +689,82 @@ __global__ void __launch_bounds__(NT, 1)
       mma_commit(bar_mma);
     }
     {
-      const bool ok = mbar_wait(bar_mma, ph_mma);
+      const bool ok = tid != 0 || mbar_wait(bar_mma, ph_mma);
       ph_mma ^= 1;
       if (__syncthreads_or(!ok)) { failed = true; site = 70; break; }
     }
     tc_fence_after();
 
-    // ---- P8: U^T -> bf16 operand in TMEM (2 tokens per column)
-    {   // 8 warps: lane quadrant x half of the 64 token columns
+    // ---- P8: U^T diag(1/|k|) -> bf16 operand in TMEM (2 tokens per column)
+    if (cs < 2) {
       uint32_t x[32], pk[16];
-      tmem_ld32(tmem + lane_base + TM_U + half * 32, x);
+      tmem_ld32(tmem + lane_base + TM_U + cs * 32, x);
       tmem_wait_ld();
 #pragma unroll
-      for (int j = 0; j < 16; ++j)
-        pk[j] = pack_bf16x2(__uint_as_float(x[2 * j]), __uint_as_float(x[2 * j + 1]));
-      tmem_st16(tmem + lane_base + TM_UB + half * 16, pk);
+      for (int j4 = 0; j4 < 8; ++j4) {
+        const float4 ik = ld4(inv_k + cs * 32 + 4 * j4);
+        pk[2 * j4] = pack_bf16x2(__uint_as_float(x[4 * j4]) * ik.x,
+                                 __uint_as_float(x[4 * j4 + 1]) * ik.y);
+        pk[2 * j4 + 1] = pack_bf16x2(__uint_as_float(x[4 * j4 + 2]) * ik.z,
+                                     __uint_as_float(x[4 * j4 + 3]) * ik.w);
+      }
+      tmem_st16(tmem + lane_base + TM_UB + cs * 16, pk);
       tmem_wait_st();
     }
     tc_fence_before();
     __syncthreads();
 
-    // ---- P9: O^T += U^T QK^T;  S^T += U^T Ke
+    // ---- P9: O^T += U^T QK^T;  S^T += U^T Ke  (after warp 4's O^T = S^T Qg^T completed)
+    bool o_ok = true;
     if (tid == 0) {
+      o_ok = mbar_wait(bar_o, ph_o);
       tc_fence_after();
 #pragma unroll
-      for (int ks = 0; ks < 4; ++ks)
+      for (int ks = 0; ks < 4; ++ks) {   // the two chains interleaved
         mma_bf16_ts(tmem + TM_O, tmem + TM_UB + 8 * ks, kdesc(sb + OFF_QKB, 64, ks), ID_KK64, 1);
-#pragma unroll
-      for (int ks = 0; ks < 4; ++ks)
         mma_bf16_ts(tmem + TM_S, tmem + TM_UB + 8 * ks, mndesc(sb + OFF_KE, 8192, ks), ID_KM128,
                     1);
+      }
       mma_commit(bar_mma);
     }
+    ph_o ^= 1;
     {
-      const bool ok = mbar_wait(bar_mma, ph_mma);
+      const bool ok = tid != 0 || (o_ok && mbar_wait(bar_mma, ph_mma));
       ph_mma ^= 1;
       if (__syncthreads_or(!ok)) { failed = true; site = 90; break; }
     }
     tc_fence_after();
 
-    // ---- P10: O^T -> bf16 -> global rows < L of this value slice (32 tokens per warp)
+    // ---- P10: O^T diag(scale/|q|) -> bf16 staging [token][dv] -> 16-byte global stores of
+    //           rows < L of this value slice (the [Kr; Qr] tile is free by now)
     {
       const int dv = my_lane;
-      uint32_t r[32];
-      tmem_ld32(tmem + lane_base + TM_O + half * 32, r);
+      uint32_t r[16];
+      tmem_ld16(tmem + lane_base + TM_O + cs * 16, r);
       tmem_wait_ld();
-      if (dv >= dv_lo && dv < dv_hi) {
-        __nv_bfloat16* op = p.out + (size_t)(c0 + half * 32) * HD + xcol + dv;
+      __nv_bfloat16* ost = reinterpret_cast<__nv_bfloat16*>(sm + OFF_RKQ);
 #pragma unroll
-        for (int j = 0; j < 32; ++j)
-          if (half * 32 + j < L) op[(size_t)j * HD] = __float2bfloat16_rn(__uint_as_float(r[j]));
+      for (int j4 = 0; j4 < 4; ++j4) {
+        const float4 iq = ld4(inv_q + cs * 16 + 4 * j4);
+        const float iqv[4] = {iq.x, iq.y, iq.z, iq.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int j = 4 * j4 + e;
+          ost[(cs * 16 + j) * D + dv] = __float2bfloat16_rn(__uint_as_float(r[j]) * iqv[e]);
+        }
       }
     }
     tc_fence_before();
+    __syncthreads();
+#pragma unroll
+    for (int k2 = 0; k2 < 2; ++k2) {
+      const int idx = tid + k2 * NT;
+      const int r = idx >> 4, v8 = idx & 15;
+      if (r < L && v8 * 8 >= dv_lo && v8 * 8 < dv_hi) {
+        const uint4 val = *reinterpret_cast<const uint4*>(sm + OFF_RKQ + r * 256 + v8 * 16);
+        *reinterpret_cast<uint4*>(p.out + (size_t)(c0 + r) * HD + xcol + v8 * 8) = val;
+      }
+    }
     __syncthreads();
   }
 
@@ -721,25 +774,23 @@ __global__ void __launch_bounds__(NT, 1)
     mbar_wait(bar_qkg, ph_qkg);
     mbar_wait(bar_v, ph_v);
     mbar_wait(bar_mma, ph_mma);
+    mbar_wait(bar_o, ph_o);
   } else {
     // ---- state out (slice columns only)
     const int dv = my_lane;
-    const bool mine = dv >= dv_lo && dv < dv_hi;
-    for (int cb = 0; cb < 2; ++cb) {
-      const int dk0 = half * 64 + cb * 32;
-      uint32_t r[32];
-      tmem_ld32(tmem + lane_base + TM_S + dk0, r);
-      tmem_wait_ld();
-      if (mine) {
+    const int dk0 = cs * 32;
+    uint32_t r[32];
+    tmem_ld32(tmem + lane_base + TM_S + dk0, r);
+    tmem_wait_ld();
+    if (dv >= dv_lo && dv < dv_hi) {
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          const size_t idx = sbase + (size_t)(dk0 + j) * D + dv;
-          const float s = __uint_as_float(r[j]);
-          if (p.state_bf16)
-            static_cast<__nv_bfloat16*>(p.final_state)[idx] = __float2bfloat16_rn(s);
-          else
-            static_cast<float*>(p.final_state)[idx] = s;
-        }
+      for (int j = 0; j < 32; ++j) {
+        const size_t idx = sbase + (size_t)(dk0 + j) * D + dv;
+        const float s = __uint_as_float(r[j]);
+        if (p.state_bf16)
+          static_cast<__nv_bfloat16*>(p.final_state)[idx] = __float2bfloat16_rn(s);
+        else
+          static_cast<float*>(p.final_state)[idx] = s;
       }
     }
   }
