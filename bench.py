@@ -4,15 +4,18 @@ One step = one kda_chunk_prefill_fwd call over the whole batch (every step of
 the method runs inside that call's kernels).  Prints ONE JSON line (rank 0).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                  [--kernel auto|tc|ref] [--workload 1] [--no-cpu-baseline]
+                  [--kernel auto|tc|split|ref] [--workload 1] [--no-cpu-baseline]
 
 value       tokens/s of the whole job (all ranks), inputs resident in HBM;
             device time from CUDA events over exactly K steps, max over ranks.
 e2e         the same metric through the C ABI with host buffers: pinned
             host -> device copies of every input, the call, device -> host
             copies of out and final_state, all inside the timed region.
-roofline    the prefill kernel against the HBM roofline: algorithmic bytes
-            per launch / mean launch time (CUDA events on the launch stream).
+roofline    the prefill call against the HBM roofline: algorithmic bytes per
+            call / mean call time (CUDA events on the launch stream).  On the
+            default workload the call is one launch of the fused tcgen05
+            kernel; on the split path (few sequences x heads) it is the
+            k-side kernel followed by the chain kernel.
 cpu_baseline  the fp64 CPU oracle (test infrastructure) on a bounded sample
             of the same workload, on this host's cores (rank 0, N=1 only).
 --impl reference  times that oracle as the reference arm.
@@ -239,7 +242,7 @@ def main():
     ap.add_argument("--steps", type=int, default=0, help="timed steps (0: ~1.5 s worth)")
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--kernel", default="auto", choices=["auto", "tc", "ref"])
+    ap.add_argument("--kernel", default="auto", choices=["auto", "tc", "split", "ref"])
     ap.add_argument("--workload", type=int, default=1)
     ap.add_argument("--n", type=int, default=None, help="sequences of the V-split workload (3)")
     ap.add_argument("--vsplit", type=int, default=-1, help="-1 automatic, or 1/2/4/8")
@@ -259,7 +262,8 @@ def main():
         kbuild.build()
     barrier(world)
     kbuild.build()
-    kernel = {"auto": kda.KERNEL_AUTO, "tc": kda.KERNEL_TC, "ref": kda.KERNEL_REF}[args.kernel]
+    kernel = {"auto": kda.KERNEL_AUTO, "tc": kda.KERNEL_TC, "ref": kda.KERNEL_REF,
+              "split": kda.KERNEL_SPLIT}[args.kernel]
     dev = torch.device("cuda", torch.cuda.current_device())
     rc = kda.device_check(dev.index)
     if rc != kda.OK:
@@ -278,6 +282,8 @@ def main():
             d["ws"] = kda.alloc_workspace(T, H, N, device=dev)
             sets.append(d)
     stream.synchronize()
+    path, vsplit_used, launches_per_step = kda.plan(T, N, H, sets[0]["ws"].numel(), args.vsplit,
+                                                    kernel)
 
     def step(i, ev_pair=None):
         d = sets[i % NB]
@@ -381,9 +387,8 @@ def main():
             torch.distributed.destroy_process_group()
         return
 
-    kernel_name = "kda_tc_chunk_kernel" if kernel != kda.KERNEL_REF else "kda_ref_chunk_kernel"
-    if kernel == kda.KERNEL_AUTO:
-        kernel_name = "kda_auto"
+    kernel_name = {kda.KERNEL_TC: "kda_tc_chunk_kernel", kda.KERNEL_REF: "kda_ref_chunk_kernel",
+                   kda.KERNEL_SPLIT: "kda_split_path"}[path]
     hbm, tflops, peak_kind = load_peaks()
     abytes = algorithmic_bytes(w)
     achieved = abytes / mean_launch / 1e9
@@ -395,11 +400,11 @@ def main():
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": w.name, "tokens": T, "seqs": N, "heads": H, "head_dim": D,
                    "state": w.state_dtype, "chunk": 64, "kernel": args.kernel,
-                   "vsplit": args.vsplit,
+                   "path": kernel_name, "vsplit": vsplit_used,
                    "l2": f"inputs {algorithmic_bytes(w) / 1e6:.0f} MB per step, 4 input sets rotated",
                    "parallelism": f"replicas x{world}"},
         "us_per_layer": us,
-        "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
+        "roofline": {"bound": "hbm", "kernel": kernel_name, "achieved": achieved, "peak": hbm, "unit": "GB/s",
                      "frac": achieved / hbm, "traffic": load_traffic(kernel_name),
                      "algorithmic_bytes_per_launch": abytes,
                      "mean_launch_us": 1e6 * mean_launch, "peak_source": peak_kind,
@@ -408,7 +413,7 @@ def main():
                      "tensor_frac": algorithmic_flops(w) / mean_launch / (tflops * 1e12)},
         "e2e": {"value": world * T * KE / e2e_elapsed, "unit": UNIT,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": KE},
-        "gpu_launches": K,
+        "gpu_launches": K * launches_per_step,
         "clocks": clocks,
     }
     if world == 1 and not args.no_cpu_baseline:

@@ -83,18 +83,32 @@ typedef struct CUstream_st* kda_stream_t;
 #define KDA_ERR_CUDA (-9)                /* a CUDA runtime call failed        */
 
 /* kernel selectors for kda_chunk_prefill_fwd_ex */
-#define KDA_KERNEL_AUTO 0 /* the production kernel                            */
-#define KDA_KERNEL_TC 1   /* tcgen05 + TMA chunk kernel, C = 64                */
-#define KDA_KERNEL_REF 2  /* plain-CUDA-core chunk kernel (GPU parity aid)     */
+#define KDA_KERNEL_AUTO 0  /* SPLIT when the value split triggers and the
+                              workspace holds its records, else TC          */
+#define KDA_KERNEL_TC 1    /* fused tcgen05 + TMA chunk kernel, C = 64: one CTA
+                              per (sequence, head[, value slice])            */
+#define KDA_KERNEL_REF 2   /* plain-CUDA-core chunk kernel (GPU parity aid)    */
+#define KDA_KERNEL_SPLIT 3 /* value-split path of PR #52458: a chunk-parallel
+                              k-side kernel writes per-(chunk, head) records to
+                              the workspace, then one chain CTA per (sequence,
+                              head, value slice of 128 / P columns), P >= 2  */
 
 /*
  * Bytes of device workspace a call needs for up to `total_tokens` tokens,
  * `heads` heads and `max_seqs` sequences.  Counterpart of FlashKDA's
  * get_workspace_size(max_num_batched_tokens, local_num_heads,
  * max_num_seqs) (PR #55737, Implementation breakdown item 2), where the
- * caller sizes a uint8 buffer once and reuses it every step.  The
- * workspace holds a device status word and the per-call work order; its
- * size depends on max_seqs only.  Returns 0 for negative arguments.
+ * caller sizes a uint8 buffer once and reuses it every step.
+ *
+ * The workspace starts with the device status word (256 bytes: all the
+ * fused kernel needs).  When some batch of up to max_seqs sequences would
+ * take the value split on the current device (2 * heads * N <= SM count;
+ * 152 SMs are assumed when no device answers), it also holds the split
+ * path's records: 66,560 bytes per (chunk slot, head), with
+ * ceil(total_tokens / 64) + N slots for the largest such N -- about 1 KB
+ * per token-head.  A smaller workspace (at least 256 bytes) is accepted;
+ * KDA_KERNEL_AUTO then runs the fused kernel.  Always a multiple of 16;
+ * 0 for negative arguments.
  */
 size_t kda_workspace_size(int64_t total_tokens, int32_t heads, int32_t max_seqs);
 
@@ -106,7 +120,8 @@ size_t kda_workspace_size(int64_t total_tokens, int32_t heads, int32_t max_seqs)
  * KDA_STATE_F32 or KDA_STATE_BF16 and applies to both states; a bf16 final
  * state is rounded to nearest even.  `workspace` must hold at least
  * kda_workspace_size(total_tokens, heads, num_seqs) bytes
- * (`workspace_bytes`), else KDA_ERR_WORKSPACE_TOO_SMALL.  Concurrent calls
+ * (`workspace_bytes`) for the split path, else the fused kernel runs; below
+ * 256 bytes the call returns KDA_ERR_WORKSPACE_TOO_SMALL.  Concurrent calls
  * on different streams need different workspaces.  The value dimension is
  * split across CTAs automatically when 2 * heads * num_seqs <= SM count
  * (PR #52458); the split does not change the result beyond rounding.
@@ -122,7 +137,10 @@ int kda_chunk_prefill_fwd(const void* q, const void* k, const void* v, const voi
 /*
  * As kda_chunk_prefill_fwd, with two overrides for tests and sweeps:
  * `vsplit` -1 = automatic, or a forced split factor in {1, 2, 4, 8};
- * `kernel` one of KDA_KERNEL_*.  Other values give KDA_ERR_INVALID_ARG.
+ * `kernel` one of KDA_KERNEL_*.  Other values give KDA_ERR_INVALID_ARG, as
+ * does KDA_KERNEL_SPLIT with vsplit 1 (with -1 it uses at least 2).
+ * KDA_KERNEL_SPLIT needs the full kda_workspace_size() of this call (its
+ * records), else KDA_ERR_WORKSPACE_TOO_SMALL.
  */
 int kda_chunk_prefill_fwd_ex(const void* q, const void* k, const void* v, const void* g,
                              const void* beta, const float* A_log, const float* dt_bias,
@@ -158,6 +176,21 @@ int kda_last_device_status(void* workspace, kda_stream_t stream);
 int kda_device_check(int device);
 
 /*
+ * The path a kda_chunk_prefill_fwd_ex call with these sizes, workspace size
+ * and selectors would take on the current device, without enqueuing
+ * anything: *kernel_out gets KDA_KERNEL_TC, KDA_KERNEL_SPLIT or
+ * KDA_KERNEL_REF (AUTO resolved), *vsplit_out the value split factor P and
+ * *launches_out the number of kernels the call enqueues (0, 1 or 2); any
+ * output pointer may be NULL.  Returns the code such a call would return
+ * for its sizes, selectors and workspace size (pointer checks aside), or
+ * KDA_ERR_UNSUPPORTED_DEVICE / KDA_ERR_CUDA.  The pages have no
+ * counterpart of this query; it lets callers and benchmarks see which
+ * kernels ran.
+ */
+int kda_plan(int64_t total_tokens, int32_t num_seqs, int32_t heads, size_t workspace_bytes,
+             int vsplit, int kernel, int* kernel_out, int* vsplit_out, int* launches_out);
+
+/*
  * kda_chunk_prefill_fwd for callers that cannot allocate device memory and
  * so cannot pass a workspace: for instance a plugin inside a host framework
  * that owns all device memory, or a hot loop where a cudaMalloc (which may
@@ -165,7 +198,9 @@ int kda_device_check(int device);
  * this entry point.
  *
  * Arguments, layouts and ownership are those of kda_chunk_prefill_fwd
- * without the workspace; the tcgen05 kernel runs with automatic value split.
+ * without the workspace; the fused tcgen05 kernel runs (KDA_KERNEL_TC with
+ * automatic value split; never the split path, whose records need a real
+ * workspace).
  * The scratch it needs (the 16-byte device status word) lives in a 256-byte
  * file-scope device array of this library, which every GPU that loads the
  * library holds until exit.  The library allocates nothing: no cudaMalloc,
@@ -178,8 +213,8 @@ int kda_device_check(int device);
  *     GPU race on the array.  Device-side errors land in the array and are
  *     not reported back here; use kda_chunk_prefill_fwd with a workspace to
  *     read them.
- *   - Returns KDA_ERR_WORKSPACE_TOO_SMALL if the call would need more than
- *     the 256-byte maximum, otherwise the codes of kda_chunk_prefill_fwd.
+ *   - Returns the codes of kda_chunk_prefill_fwd (the fused kernel needs
+ *     only the 256 bytes the array holds).
  */
 int kda_chunk_prefill_fwd_noalloc(const void* q, const void* k, const void* v, const void* g,
                                   const void* beta, const float* A_log, const float* dt_bias,

@@ -9,6 +9,8 @@ names follow the C ABI in ``include/kda.h``:
                       initial_state, cu_seqlens, out=None, final_state=None,
                       workspace=None, ...) -> (out, final_state)
     choose_vsplit(num_seqs, heads, sm_count) -> int
+    plan(total_tokens, num_seqs, heads, workspace_bytes, vsplit, kernel)
+        -> (kernel, vsplit, launches)
     last_device_status(workspace) -> int
     status_string(code) -> str
 
@@ -28,7 +30,7 @@ LIB_PATH = os.path.join(_PKG, "libkda.so")
 
 HEAD_DIM = 128
 STATE_F32, STATE_BF16 = 0, 1
-KERNEL_AUTO, KERNEL_TC, KERNEL_REF = 0, 1, 2
+KERNEL_AUTO, KERNEL_TC, KERNEL_REF, KERNEL_SPLIT = 0, 1, 2, 3
 OK = 0
 ERR_INVALID_ARG = -1
 ERR_UNSUPPORTED_DEVICE = -2
@@ -43,7 +45,7 @@ ERR_CUDA = -9
 # every symbol include/kda.h declares
 EXPORTS = ("kda_workspace_size", "kda_chunk_prefill_fwd", "kda_chunk_prefill_fwd_ex",
            "kda_choose_vsplit", "kda_status_string", "kda_last_device_status",
-           "kda_device_check", "kda_chunk_prefill_fwd_noalloc")
+           "kda_device_check", "kda_plan", "kda_chunk_prefill_fwd_noalloc")
 
 _lib = None
 _lock = threading.Lock()
@@ -83,6 +85,8 @@ def lib() -> ctypes.CDLL:
             L.kda_last_device_status.argtypes = [P, P]
             L.kda_device_check.restype = ctypes.c_int
             L.kda_device_check.argtypes = [ctypes.c_int]
+            L.kda_plan.restype = ctypes.c_int
+            L.kda_plan.argtypes = [I64, I32, I32, SZ, ctypes.c_int, ctypes.c_int, P, P, P]
             L.kda_chunk_prefill_fwd_noalloc.restype = ctypes.c_int
             L.kda_chunk_prefill_fwd_noalloc.argtypes = [P, P, P, P, P, P, P, F, F, P, P, P, P,
                                                         ctypes.c_int, P, I64, I32, I32]
@@ -104,6 +108,18 @@ def choose_vsplit(num_seqs: int, heads: int, sm_count: int) -> int:
 
 def device_check(device: int = 0) -> int:
     return int(lib().kda_device_check(int(device)))
+
+
+def plan(total_tokens: int, num_seqs: int, heads: int, workspace_bytes: int,
+         vsplit: int = -1, kernel: int = KERNEL_AUTO):
+    """``kda_plan``: (kernel, vsplit, launches) a call would use on the current device."""
+    k, p, n = ctypes.c_int(0), ctypes.c_int(0), ctypes.c_int(0)
+    rc = lib().kda_plan(int(total_tokens), int(num_seqs), int(heads), int(workspace_bytes),
+                        int(vsplit), int(kernel), ctypes.byref(k), ctypes.byref(p),
+                        ctypes.byref(n))
+    if rc != OK:
+        raise KDAError(rc, "kda_plan")
+    return k.value, p.value, n.value
 
 
 def alloc_workspace(total_tokens: int, heads: int, max_seqs: int, device=None) -> torch.Tensor:

@@ -7,6 +7,7 @@
 // listing): head_dim 128, bf16 activations, a bounded gate -- refused with
 // an error, never a silent fallback.  It also asserts the workspace bound
 // that report lists as unchecked (Risks & impact, item 2).
+#include <algorithm>
 #include <cmath>
 #include <cstdint>
 #include <cstring>
@@ -55,13 +56,45 @@ int validate(const void* q, const void* k, const void* v, const void* g, const v
   if (!cu_seqlens || !A_log || !dt_bias || !workspace) return KDA_ERR_INVALID_ARG;
   if (num_seqs > 0 && !final_state) return KDA_ERR_INVALID_ARG;
   if (total_tokens > 0 && (!q || !k || !v || !g || !beta || !out)) return KDA_ERR_INVALID_ARG;
-  if (workspace_bytes < kda_workspace_size(total_tokens, heads, num_seqs))
-    return KDA_ERR_WORKSPACE_TOO_SMALL;
+  if (workspace_bytes < (size_t)kda::kWorkspaceBytes) return KDA_ERR_WORKSPACE_TOO_SMALL;
   const void* a16[] = {q, k, v, g, out, initial_state, final_state, workspace, A_log, dt_bias};
   for (const void* p : a16)
     if (p && !aligned(p, 16)) return KDA_ERR_MISALIGNED;
   if (beta && !aligned(beta, 2)) return KDA_ERR_MISALIGNED;
   if (!aligned(cu_seqlens, 4)) return KDA_ERR_MISALIGNED;
+  return KDA_OK;
+}
+
+// The path of a call: validated selectors, then AUTO resolved.  The split path (k-side
+// records + chain per value slice) needs its record area in the workspace; AUTO takes it
+// when the value split triggers and the workspace holds the records, else the fused kernel
+// with one CTA per (sequence, head).
+int plan(int64_t total_tokens, int32_t num_seqs, int32_t heads, size_t workspace_bytes,
+         int vsplit, int kernel, int sms, int* kernel_out, int* vsplit_out, int* launches_out) {
+  if (vsplit != -1 && vsplit != 1 && vsplit != 2 && vsplit != 4 && vsplit != 8)
+    return KDA_ERR_INVALID_ARG;
+  if (kernel != KDA_KERNEL_AUTO && kernel != KDA_KERNEL_TC && kernel != KDA_KERNEL_REF &&
+      kernel != KDA_KERNEL_SPLIT)
+    return KDA_ERR_INVALID_ARG;
+  if (kernel == KDA_KERNEL_SPLIT && vsplit == 1) return KDA_ERR_INVALID_ARG;
+  const size_t split_need = kda::split_workspace_bytes(total_tokens, heads, num_seqs);
+  int P = vsplit == -1 ? kda_choose_vsplit(num_seqs, heads, sms) : vsplit;
+  if (kernel == KDA_KERNEL_SPLIT) {
+    if (P < 2) P = 2;
+    if (workspace_bytes < split_need) return KDA_ERR_WORKSPACE_TOO_SMALL;
+  } else if (kernel == KDA_KERNEL_AUTO) {
+    if (P > 1 && workspace_bytes >= split_need && total_tokens > 0)
+      kernel = KDA_KERNEL_SPLIT;
+    else {
+      kernel = KDA_KERNEL_TC;
+      if (vsplit == -1) P = 1;
+    }
+  }
+  int launches = num_seqs == 0 ? 0 : 1;
+  if (kernel == KDA_KERNEL_SPLIT && num_seqs > 0) launches = total_tokens > 0 ? 2 : 1;
+  if (kernel_out) *kernel_out = kernel;
+  if (vsplit_out) *vsplit_out = P;
+  if (launches_out) *launches_out = launches;
   return KDA_OK;
 }
 
@@ -74,16 +107,23 @@ int fwd_impl(const void* q, const void* k, const void* v, const void* g, const v
                     cu_seqlens, out, final_state, state_dtype, workspace, total_tokens,
                     num_seqs, heads, workspace_bytes);
   if (rc != KDA_OK) return rc;
+  // selectors first: they are host-side checks and need no device
   if (vsplit != -1 && vsplit != 1 && vsplit != 2 && vsplit != 4 && vsplit != 8)
     return KDA_ERR_INVALID_ARG;
-  if (kernel != KDA_KERNEL_AUTO && kernel != KDA_KERNEL_TC && kernel != KDA_KERNEL_REF)
+  if (kernel != KDA_KERNEL_AUTO && kernel != KDA_KERNEL_TC && kernel != KDA_KERNEL_REF &&
+      kernel != KDA_KERNEL_SPLIT)
     return KDA_ERR_INVALID_ARG;
+  if (kernel == KDA_KERNEL_SPLIT && vsplit == 1) return KDA_ERR_INVALID_ARG;
   int dev = 0, sms = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) {
     cudaGetLastError();
     return KDA_ERR_CUDA;
   }
   rc = check_device(dev, &sms);
+  if (rc != KDA_OK) return rc;
+  int P = 1, launches = 0;
+  rc = plan(total_tokens, num_seqs, heads, workspace_bytes, vsplit, kernel, sms, &kernel, &P,
+            &launches);
   if (rc != KDA_OK) return rc;
   if (num_seqs == 0) return KDA_OK;
 
@@ -106,10 +146,13 @@ int fwd_impl(const void* q, const void* k, const void* v, const void* g, const v
   p.total_tokens = total_tokens;
   p.num_seqs = num_seqs;
   p.heads = heads;
-  p.vsplit = vsplit == -1 ? kda_choose_vsplit(num_seqs, heads, sms) : vsplit;
+  p.vsplit = P;
+  p.sm_count = sms;
 
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  cudaError_t err = (kernel == KDA_KERNEL_REF) ? kda::launch_ref(p, s) : kda::launch_tc(p, s);
+  cudaError_t err = (kernel == KDA_KERNEL_REF)     ? kda::launch_ref(p, s)
+                    : (kernel == KDA_KERNEL_SPLIT) ? kda::launch_split(p, s)
+                                                   : kda::launch_tc(p, s);
   if (err != cudaSuccess) {
     cudaGetLastError();
     return KDA_ERR_LAUNCH_FAILED;
@@ -123,7 +166,19 @@ extern "C" {
 
 size_t kda_workspace_size(int64_t total_tokens, int32_t heads, int32_t max_seqs) {
   if (total_tokens < 0 || heads < 0 || max_seqs < 0) return 0;
-  return (size_t)kda::kWorkspaceBytes;
+  size_t need = (size_t)kda::kWorkspaceBytes;
+  // room for the split path's records whenever some batch of up to max_seqs sequences
+  // would take it on this device: N sequences qualify when 2 * heads * N <= SMs
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || check_device(dev, &sms) == KDA_ERR_CUDA || sms <= 0) {
+    cudaGetLastError();
+    sms = kda::kDefaultSmCount;
+  }
+  if (heads > 0 && total_tokens > 0 && max_seqs > 0 && 2 * (int64_t)heads <= sms) {
+    const int32_t n_split = (int32_t)std::min<int64_t>(max_seqs, sms / (2 * (int64_t)heads));
+    need = std::max(need, kda::split_workspace_bytes(total_tokens, heads, n_split));
+  }
+  return need;
 }
 
 int kda_chunk_prefill_fwd(const void* q, const void* k, const void* v, const void* g,
@@ -195,5 +250,20 @@ int kda_last_device_status(void* workspace, kda_stream_t stream) {
 }
 
 int kda_device_check(int device) { return check_device(device, nullptr); }
+
+int kda_plan(int64_t total_tokens, int32_t num_seqs, int32_t heads, size_t workspace_bytes,
+             int vsplit, int kernel, int* kernel_out, int* vsplit_out, int* launches_out) {
+  if (total_tokens < 0 || num_seqs < 0 || heads <= 0) return KDA_ERR_INVALID_ARG;
+  if (workspace_bytes < (size_t)kda::kWorkspaceBytes) return KDA_ERR_WORKSPACE_TOO_SMALL;
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return KDA_ERR_CUDA;
+  }
+  const int rc = check_device(dev, &sms);
+  if (rc != KDA_OK) return rc;
+  return plan(total_tokens, num_seqs, heads, workspace_bytes, vsplit, kernel, sms, kernel_out,
+              vsplit_out, launches_out);
+}
 
 }  // extern "C"

@@ -1,0 +1,438 @@
+// Split path, second kernel: the serial inter-chunk chain for one value slice.
+//
+// The chunk-parallel k-side kernel has already written, for every (chunk, head),
+// a record with -W, Qg (raw q times 2^Gam), Ke (raw k times 2^(Gam_last - Gam)),
+// T diag(b), the raw masked QK, the chunk decay 2^Gam_last and the norm scalars.
+// This kernel walks one sequence's chunks in order for one head and one slice of
+// DV = 128 / P value columns -- the value-dimension split of "[Kimi-K3][Perf]
+// Update FlashKDA for automatic K2 V-split" (PR #52458, Features & motivation),
+// which gives low-parallelism batches more CTAs.  Per chunk (S: 128 x DV, fp32):
+//   U  = T diag(b) V + (-W) S           (64 x DV)
+//   O  = (Qg S + QK (U/|k|)) scale/|q|  -> out
+//   S  = diag(2^Gam_last) S + Ke^T (U/|k|)
+// The products are narrow (N = DV), so they run as warp-level mma.sync tiles
+// (bf16 in, fp32 accumulate) with S held in registers; the record of the next
+// chunk is fetched by TMA while this one is processed.
+#include <cuda.h>
+
+#include "kda_internal.cuh"
+#include "kda_sm100.cuh"
+
+namespace kda {
+namespace {
+
+using namespace sm100;
+
+constexpr int NT2 = 256;   // 8 warps
+
+// shared memory per record buffer
+constexpr int B_WN = 0, B_QG = 16384, B_KE = 32768, B_TB = 49152, B_QK = 57344;
+constexpr int B_VEC = 65536, B_V = 66560 + 1024;   // V slice (aligned up to 1 KB)
+constexpr int BUF_BYTES = B_V + 8192;               // room for V of DV <= 64
+
+template <int DV>
+struct ChainSmem {
+  static constexpr int SP = DV + 8;                 // padded row (bf16) of the staging tiles
+  static constexpr int OFF_BUF0 = 0;
+  static constexpr int OFF_BUF1 = BUF_BYTES;
+  static constexpr int OFF_SB = 2 * BUF_BYTES;      // S bf16 [2][128][SP]
+  static constexpr int OFF_UB = OFF_SB + 2 * 128 * SP * 2;  // U bf16 [64][SP]
+  static constexpr int OFF_BAR = OFF_UB + 64 * SP * 2;
+  static constexpr int OFF_MISC = OFF_BAR + 64;
+  static constexpr int BYTES = OFF_MISC + 64 + 1024;
+};
+
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t (&r)[4]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t (&r)[4]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x2_t(uint32_t addr, uint32_t (&r)[2]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x2.trans.shared.b16 {%0, %1}, [%2];"
+               : "=r"(r[0]), "=r"(r[1])
+               : "r"(addr));
+}
+__device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                         uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, "
+      "{%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+__device__ __forceinline__ uint32_t bf2(float lo, float hi) { return pack_bf16x2(lo, hi); }
+
+// byte offset of (row, col) in a tile of 128-byte swizzled rows written by TMA as boxes of
+// 64 columns (box b of a `rows`-row tile starts at b * rows * 128)
+__device__ __forceinline__ uint32_t sw128(int row, int col, int rows) {
+  return (uint32_t)((col >> 6) * rows * 128 + row * 128 + ((((col & 63) >> 3) ^ (row & 7)) << 4) +
+                    (col & 7) * 2);
+}
+// byte offset of (row, col) of a [rows][DV] bf16 tile written by TMA with the swizzle
+// whose span equals the row (32, 64 or 128 bytes): address bits [4, 4+B) ^= bits [7, 7+B)
+template <int DV>
+__device__ __forceinline__ uint32_t swv(int row, int col) {
+  constexpr int B = (DV == 16) ? 1 : (DV == 32 ? 2 : 3);
+  const uint32_t off = (uint32_t)(row * DV * 2 + col * 2);
+  return off ^ (((off >> 7) & ((1u << B) - 1)) << 4);
+}
+
+struct ChainMaps {
+  CUtensorMap rec128;   // workspace as [rows][128] bf16 (256-B rows)
+  CUtensorMap rec64;    // workspace as [rows][64] bf16 (128-B rows)
+  CUtensorMap v;        // v as [T][H*128] bf16, box {DV, 64}
+};
+
+template <int DV>
+__global__ void __launch_bounds__(NT2, 1)
+    kda_chain_kernel(const __grid_constant__ Params p, const __grid_constant__ ChainMaps maps) {
+  using L_ = ChainSmem<DV>;
+  constexpr int SP = L_::SP;
+  constexpr int P = 128 / DV;
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  unsigned char* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  const uint32_t sb = smem_u32(sm);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int g = lane >> 2, t = lane & 3;
+  const uint32_t bar0 = sb + L_::OFF_BAR, bar1 = bar0 + 8;
+
+  const int H = p.heads;
+  const int unit = blockIdx.x;
+  const int part = unit % P;
+  const int h = (unit / P) % H;
+  const int n = unit / (P * H);
+  const int t0 = p.cu_seqlens[n], t1 = p.cu_seqlens[n + 1];
+  if (t0 < 0 || t1 < t0 || (int64_t)t1 > p.total_tokens || p.cu_seqlens[0] != 0) {
+    if (tid == 0) record_error(p.status, KDA_ERR_BAD_CU_SEQLENS, 3);
+    return;
+  }
+  if (tid == 0) {
+    mbar_init(bar0, 1);
+    mbar_init(bar1, 1);
+    mbar_fence_init();
+  }
+  __syncthreads();
+  // chunk c of sequence n was stored in slot floor(t0 / 64) + n + c by the k-side kernel
+  const int slot0 = (t0 >> 6) + n;
+  const int nch = (t1 - t0 + kChunk - 1) / kChunk;
+  const int dv0 = part * DV;
+  const size_t HD = (size_t)H * 128;
+  const size_t sbase = ((size_t)n * H + h) * 128 * 128;
+
+  auto issue = [&](int i, int buf) {
+    const uint32_t base = sb + (buf ? L_::OFF_BUF1 : L_::OFF_BUF0);
+    const uint32_t bar = buf ? bar1 : bar0;
+    const int64_t rec = (int64_t)(slot0 + i) * H + h;
+    const int r128 = (int)((kSplitHeader + rec * kRecBytes) / 256);
+    const int r64 = (int)((kSplitHeader + rec * kRecBytes) / 128);
+    mbar_expect_tx(bar, 5 * 16384 + 1024 + 64 * DV * 2 - 16384);
+#pragma unroll
+    for (int tile = 0; tile < 3; ++tile)
+#pragma unroll
+      for (int b = 0; b < 2; ++b)
+        tma_load_2d(base + tile * 16384 + b * 8192, &maps.rec128, 64 * b, r128 + 64 * tile, bar);
+    tma_load_2d(base + B_TB, &maps.rec64, 0, r64 + kRecTB / 128, bar);
+    tma_load_2d(base + B_QK, &maps.rec64, 0, r64 + kRecQK / 128, bar);
+    const unsigned char* vec = reinterpret_cast<const unsigned char*>(p.status) + kSplitHeader +
+                               rec * kRecBytes + kRecVec;
+    bulk_load(base + B_VEC, vec, 1024, bar);
+    tma_load_2d(base + B_V, &maps.v, h * 128 + dv0, t0 + kChunk * i, bar);
+  };
+
+  // ---- state in: this warp's S rows (key channels 16w..16w+15), all DV columns
+  float S[DV / 8][4];
+#pragma unroll
+  for (int nt = 0; nt < DV / 8; ++nt)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int dk = 16 * warp + g + ((e >> 1) << 3);
+      const int dv = dv0 + 8 * nt + 2 * t + (e & 1);
+      float s = 0.0f;
+      if (p.initial_state) {
+        const size_t idx = sbase + (size_t)dk * 128 + dv;
+        s = p.state_bf16 ? __bfloat162float(static_cast<const __nv_bfloat16*>(p.initial_state)[idx])
+                         : static_cast<const float*>(p.initial_state)[idx];
+      }
+      S[nt][e] = s;
+    }
+  auto stage_s = [&](int which) {
+    unsigned char* sbf = sm + L_::OFF_SB + which * 128 * SP * 2;
+#pragma unroll
+    for (int nt = 0; nt < DV / 8; ++nt) {
+      const int r0 = 16 * warp + g, c = 8 * nt + 2 * t;
+      *reinterpret_cast<uint32_t*>(sbf + (r0 * SP + c) * 2) = bf2(S[nt][0], S[nt][1]);
+      *reinterpret_cast<uint32_t*>(sbf + ((r0 + 8) * SP + c) * 2) = bf2(S[nt][2], S[nt][3]);
+    }
+  };
+  stage_s(0);
+  uint32_t phase = 0;   // bit b: parity to wait for on buffer b
+  int pending = 0;   // buffers with a fetch in flight (thread 0's view)
+  if (tid == 0 && nch > 0) {
+    issue(0, 0);
+    pending = 1;
+  }
+  __syncthreads();
+
+  bool failed = false;
+  const int mt = warp & 3;                 // 16-token row tile of U and O
+  const int ng = warp >> 2;                // which half of the n8 tiles
+  constexpr int NPW = DV / 16;             // n8 tiles per warp in U and O
+  for (int i = 0; i < nch; ++i) {
+    const int buf = i & 1;
+    const int c0 = t0 + kChunk * i;
+    const int L = min(kChunk, t1 - c0);
+    if (tid == 0 && i + 1 < nch) {
+      issue(i + 1, buf ^ 1);
+      pending |= 2 >> buf;
+    }
+    const bool ok = mbar_wait(buf ? bar1 : bar0, (phase >> buf) & 1u);
+    if (__syncthreads_or(!ok)) { failed = true; break; }
+    phase ^= 1u << buf;
+    pending &= ~(1 << buf);
+    unsigned char* rb = sm + (buf ? L_::OFF_BUF1 : L_::OFF_BUF0);
+    const uint32_t rbs = smem_u32(rb);
+    const float* vec = reinterpret_cast<const float*>(rb + B_VEC);   // decay[128], iq[64], ik[64]
+    if (L < kChunk) {   // v rows past the sequence end -> 0
+      for (int idx = tid; idx < (kChunk - L) * DV / 2; idx += NT2) {
+        const int r = L + idx / (DV / 2), c = 2 * (idx % (DV / 2));
+        *reinterpret_cast<uint32_t*>(rb + B_V + swv<DV>(r, c)) = 0u;
+      }
+      __syncthreads();
+    }
+
+    const uint32_t sbf = sb + L_::OFF_SB + buf * 128 * SP * 2;   // S bf16 of this chunk
+    const uint32_t ubf = sb + L_::OFF_UB;
+    // ---- U = T diag(b) V + (-W) S    (rows 16 mt.., n8 tiles ng + 2 j)
+    float U[NPW][4];
+#pragma unroll
+    for (int j = 0; j < NPW; ++j) U[j][0] = U[j][1] = U[j][2] = U[j][3] = 0.0f;
+#pragma unroll
+    for (int ks = 0; ks < 4; ++ks) {
+      uint32_t a[4];
+      {
+        const int row = 16 * mt + (lane & 15), col = 16 * ks + 8 * (lane >> 4);
+        ldsm_x4(rbs + B_TB + sw128(row, col, 64), a);
+      }
+#pragma unroll
+      for (int j = 0; j < NPW; ++j) {
+        uint32_t b[2];
+        const int k = 16 * ks + (lane & 15), c = 8 * (ng + 2 * j);
+        ldsm_x2_t(rbs + B_V + swv<DV>(k, c), b);
+        mma16816(U[j], a, b[0], b[1]);
+      }
+    }
+#pragma unroll
+    for (int ks = 0; ks < 8; ++ks) {
+      uint32_t a[4];
+      {
+        const int row = 16 * mt + (lane & 15), col = 16 * ks + 8 * (lane >> 4);
+        ldsm_x4(rbs + B_WN + sw128(row, col, 64), a);
+      }
+#pragma unroll
+      for (int j = 0; j < NPW; ++j) {
+        uint32_t b[2];
+        const int k = 16 * ks + (lane & 15), c = 8 * (ng + 2 * j);
+        ldsm_x2_t(sbf + (k * SP + c) * 2, b);
+        mma16816(U[j], a, b[0], b[1]);
+      }
+    }
+    // U / |k| (per token row) -> bf16 staging
+    {
+      const float ik0 = vec[192 + 16 * mt + g], ik1 = vec[192 + 16 * mt + g + 8];
+      unsigned char* ub = sm + L_::OFF_UB;
+#pragma unroll
+      for (int j = 0; j < NPW; ++j) {
+        const int c = 8 * (ng + 2 * j) + 2 * t;
+        *reinterpret_cast<uint32_t*>(ub + ((16 * mt + g) * SP + c) * 2) =
+            bf2(U[j][0] * ik0, U[j][1] * ik0);
+        *reinterpret_cast<uint32_t*>(ub + ((16 * mt + g + 8) * SP + c) * 2) =
+            bf2(U[j][2] * ik1, U[j][3] * ik1);
+      }
+    }
+    __syncthreads();
+
+    // ---- O = (Qg S + QK U') scale/|q|  -> out
+    {
+      float O[NPW][4];
+#pragma unroll
+      for (int j = 0; j < NPW; ++j) O[j][0] = O[j][1] = O[j][2] = O[j][3] = 0.0f;
+#pragma unroll
+      for (int ks = 0; ks < 8; ++ks) {
+        uint32_t a[4];
+        const int row = 16 * mt + (lane & 15), col = 16 * ks + 8 * (lane >> 4);
+        ldsm_x4(rbs + B_QG + sw128(row, col, 64), a);
+#pragma unroll
+        for (int j = 0; j < NPW; ++j) {
+          uint32_t b[2];
+          const int k = 16 * ks + (lane & 15), c = 8 * (ng + 2 * j);
+          ldsm_x2_t(sbf + (k * SP + c) * 2, b);
+          mma16816(O[j], a, b[0], b[1]);
+        }
+      }
+#pragma unroll
+      for (int ks = 0; ks < 4; ++ks) {
+        uint32_t a[4];
+        const int row = 16 * mt + (lane & 15), col = 16 * ks + 8 * (lane >> 4);
+        ldsm_x4(rbs + B_QK + sw128(row, col, 64), a);
+#pragma unroll
+        for (int j = 0; j < NPW; ++j) {
+          uint32_t b[2];
+          const int k = 16 * ks + (lane & 15), c = 8 * (ng + 2 * j);
+          ldsm_x2_t(ubf + (k * SP + c) * 2, b);
+          mma16816(O[j], a, b[0], b[1]);
+        }
+      }
+      const int r0 = 16 * mt + g;
+      const float iq0 = vec[128 + r0], iq1 = vec[128 + r0 + 8];
+#pragma unroll
+      for (int j = 0; j < NPW; ++j) {
+        const int c = dv0 + 8 * (ng + 2 * j) + 2 * t;
+        if (r0 < L)
+          *reinterpret_cast<uint32_t*>(p.out + (size_t)(c0 + r0) * HD + h * 128 + c) =
+              bf2(O[j][0] * iq0, O[j][1] * iq0);
+        if (r0 + 8 < L)
+          *reinterpret_cast<uint32_t*>(p.out + (size_t)(c0 + r0 + 8) * HD + h * 128 + c) =
+              bf2(O[j][2] * iq1, O[j][3] * iq1);
+      }
+    }
+
+    // ---- S = diag(2^Gam_last) S + Ke^T U'   (this warp: key rows 16 warp.., all columns)
+    {
+      const float d0 = vec[16 * warp + g], d1 = vec[16 * warp + g + 8];
+#pragma unroll
+      for (int nt = 0; nt < DV / 8; ++nt) {
+        S[nt][0] *= d0;
+        S[nt][1] *= d0;
+        S[nt][2] *= d1;
+        S[nt][3] *= d1;
+      }
+#pragma unroll
+      for (int ks = 0; ks < 4; ++ks) {
+        uint32_t a[4];
+        {   // A = Ke^T (rows dk, k = token) from Ke stored [token][dk]
+          const int j = lane >> 3, rr = lane & 7;
+          const int s = 16 * ks + ((j >> 1) << 3) + rr, dk = 16 * warp + ((j & 1) << 3);
+          ldsm_x4_t(rbs + B_KE + sw128(s, dk, 64), a);
+        }
+#pragma unroll
+        for (int nt = 0; nt < DV / 8; ++nt) {
+          uint32_t b[2];
+          const int k = 16 * ks + (lane & 15), c = 8 * nt;
+          ldsm_x2_t(ubf + (k * SP + c) * 2, b);
+          mma16816(S[nt], a, b[0], b[1]);
+        }
+      }
+    }
+    stage_s(buf ^ 1);
+    __syncthreads();
+  }
+
+  if (failed) {
+    if (tid == 0) {
+      record_error(p.status, KDA_ERR_DEVICE_TIMEOUT, 4);
+      // let fetches still in flight land (bounded) before the CTA exits
+      if (pending & 1) mbar_wait(bar0, phase & 1u);
+      if (pending & 2) mbar_wait(bar1, (phase >> 1) & 1u);
+    }
+    return;
+  }
+  // ---- state out
+#pragma unroll
+  for (int nt = 0; nt < DV / 8; ++nt)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int dk = 16 * warp + g + ((e >> 1) << 3);
+      const int dv = dv0 + 8 * nt + 2 * t + (e & 1);
+      const size_t idx = sbase + (size_t)dk * 128 + dv;
+      if (p.state_bf16)
+        static_cast<__nv_bfloat16*>(p.final_state)[idx] = __float2bfloat16_rn(S[nt][e]);
+      else
+        static_cast<float*>(p.final_state)[idx] = S[nt][e];
+    }
+}
+
+}  // namespace
+
+// host side ----------------------------------------------------------------
+namespace {
+typedef CUresult (*EncodeTiledFn2)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+bool make_chain_maps(ChainMaps* m, const Params& p, int dv) {
+  EncodeTiledFn2 enc = reinterpret_cast<EncodeTiledFn2>(tensor_map_encoder());
+  if (!enc) return false;
+  const size_t wsb = split_workspace_bytes(p.total_tokens, p.heads, p.num_seqs);
+  const cuuint32_t es[2] = {1, 1};
+  {
+    cuuint64_t dims[2] = {128, (cuuint64_t)(wsb / 256)};
+    cuuint64_t strides[1] = {256};
+    cuuint32_t box[2] = {64, 64};
+    if (enc(&m->rec128, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.status, dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return false;
+  }
+  {
+    cuuint64_t dims[2] = {64, (cuuint64_t)(wsb / 128)};
+    cuuint64_t strides[1] = {128};
+    cuuint32_t box[2] = {64, 64};
+    if (enc(&m->rec64, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.status, dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return false;
+  }
+  {
+    cuuint64_t dims[2] = {(cuuint64_t)p.heads * 128, (cuuint64_t)(p.total_tokens > 0 ? p.total_tokens : 1)};
+    cuuint64_t strides[1] = {(cuuint64_t)p.heads * 256};
+    cuuint32_t box[2] = {(cuuint32_t)dv, 64};
+    const CUtensorMapSwizzle sw = dv == 16 ? CU_TENSOR_MAP_SWIZZLE_32B
+                                           : (dv == 32 ? CU_TENSOR_MAP_SWIZZLE_64B
+                                                       : CU_TENSOR_MAP_SWIZZLE_128B);
+    if (enc(&m->v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<__nv_bfloat16*>(p.v), dims,
+            strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return false;
+  }
+  return true;
+}
+
+template <int DV>
+cudaError_t launch_chain_dv(const Params& p, cudaStream_t stream) {
+  static bool attr_set[64] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  constexpr int smem = ChainSmem<DV>::BYTES;
+  if (dev >= 0 && dev < 64 && !attr_set[dev]) {
+    e = cudaFuncSetAttribute(kda_chain_kernel<DV>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    attr_set[dev] = true;
+  }
+  ChainMaps maps;
+  if (!make_chain_maps(&maps, p, DV)) return cudaErrorInvalidValue;
+  const long long blocks = (long long)p.num_seqs * p.heads * (128 / DV);
+  kda_chain_kernel<DV><<<(unsigned)blocks, NT2, smem, stream>>>(p, maps);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_split(const Params& p, cudaStream_t stream) {
+  if (p.vsplit != 2 && p.vsplit != 4 && p.vsplit != 8) return cudaErrorInvalidValue;
+  cudaError_t e = launch_kside(p, stream);
+  if (e != cudaSuccess) return e;
+  switch (p.vsplit) {
+    case 2: return launch_chain_dv<64>(p, stream);
+    case 4: return launch_chain_dv<32>(p, stream);
+    default: return launch_chain_dv<16>(p, stream);
+  }
+}
+
+}  // namespace kda

@@ -11,7 +11,21 @@ namespace kda {
 
 constexpr int kHeadDim = 128;
 constexpr float kL2Eps = 1e-6f;      // l2norm epsilon inside the square root
-constexpr int kWorkspaceBytes = 256;  // device status word + error detail
+constexpr int kWorkspaceBytes = 256;  // device status word + error detail (fused path)
+constexpr int kDefaultSmCount = 152;  // GB300; sizes the workspace when no device answers
+
+// Split path (chunk-parallel k-side kernel, then the chain kernel): one record per
+// (chunk slot, head) in the workspace after a 1 KB header.  bf16 row-major tiles
+// plus fp32 vectors, all offsets 1024-byte aligned:
+constexpr int kRecWN = 0;         // -W          [64 tok][128 dk]
+constexpr int kRecQG = 16384;     // q_raw * g   [64 tok][128 dk]
+constexpr int kRecKE = 32768;     // k_raw * ke  [64 tok][128 dk]
+constexpr int kRecTB = 49152;     // T diag(b)   [64][64]
+constexpr int kRecQK = 57344;     // raw masked QK [64][64]
+constexpr int kRecVec = 65536;    // fp32: decay [128], scale/|q| [64], 1/|k| [64]
+constexpr int kRecBytes = 66560;
+constexpr int kSplitHeader = 1024;
+constexpr int kChunk = 64;
 
 // Layout of the workspace (all int32):
 //   [0] status: KDA_OK or the first KDA_ERR_* a kernel recorded
@@ -36,6 +50,7 @@ struct Params {
   int32_t num_seqs;
   int32_t heads;
   int32_t vsplit;              // 1, 2, 4 or 8
+  int32_t sm_count;            // multiprocessors of the device
 };
 
 // Record a device-side error (first writer wins) with its block and site.
@@ -48,5 +63,19 @@ __device__ __forceinline__ void record_error(int* status, int code, int site) {
 
 cudaError_t launch_ref(const Params& p, cudaStream_t stream);
 cudaError_t launch_tc(const Params& p, cudaStream_t stream);
+// Split path: k-side records for every chunk slot (launch_kside), then the chain
+// per value slice; launch_split runs both.
+cudaError_t launch_kside(const Params& p, cudaStream_t stream);
+cudaError_t launch_split(const Params& p, cudaStream_t stream);
+// cuTensorMapEncodeTiled from the driver (null if unavailable)
+void* tensor_map_encoder();
+
+// Chunk slots the split path reserves: every sequence adds at most one partial chunk.
+__host__ __device__ inline int64_t split_slots(int64_t total_tokens, int32_t num_seqs) {
+  return (total_tokens + kChunk - 1) / kChunk + num_seqs;
+}
+inline size_t split_workspace_bytes(int64_t total_tokens, int32_t heads, int32_t num_seqs) {
+  return (size_t)kSplitHeader + (size_t)split_slots(total_tokens, num_seqs) * heads * kRecBytes;
+}
 
 }  // namespace kda

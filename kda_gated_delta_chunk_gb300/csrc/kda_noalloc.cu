@@ -55,8 +55,10 @@ extern "C" int kda_chunk_prefill_fwd_noalloc(
     const void* initial_state, const int32_t* cu_seqlens, void* out, void* final_state,
     int state_dtype, kda_stream_t stream, int64_t total_tokens, int32_t num_seqs,
     int32_t heads) {
-  const size_t need = kda_workspace_size(total_tokens, heads, num_seqs);
-  if (need == 0 || need > (size_t)kNoAllocScratchBytes) return KDA_ERR_WORKSPACE_TOO_SMALL;
+  // The fused tcgen05 kernel needs only the status words; the split path (whose per-chunk
+  // records need a real workspace) is never taken here.
+  static_assert(kda::kWorkspaceBytes <= kNoAllocScratchBytes, "scratch too small");
+  if (total_tokens < 0 || num_seqs < 0 || heads <= 0) return KDA_ERR_INVALID_ARG;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) {
     cudaGetLastError();

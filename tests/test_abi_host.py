@@ -45,6 +45,35 @@ def test_workspace_size(L):
     assert kda.workspace_size(0, 0, 0) >= 0
 
 
+SLOT_HEAD_BYTES = 66560      # one split-path record: 3 tiles 64x128 + 2 tiles 64x64 bf16 + 1 KB
+
+
+def _sms():
+    try:
+        import torch
+        if torch.cuda.is_available():
+            return torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
+    except Exception:
+        pass
+    return 152               # the library's assumption when no device answers
+
+
+def test_workspace_size_holds_split_records(L):
+    """Records for ceil(T/64) + N chunk slots per head whenever some batch of up to
+    max_seqs sequences would take the value split (2 H N <= SMs), else 256 bytes."""
+    sms = _sms()
+    for T, H, N in [(1000, 2, 3), (16384, 16, 1), (4096, 8, 7), (64, 1, 500), (65536, 32, 64)]:
+        got = kda.workspace_size(T, H, N)
+        if 2 * H <= sms:
+            n_split = min(N, sms // (2 * H))
+            assert got == 1024 + ((T + 63) // 64 + n_split) * H * SLOT_HEAD_BYTES, (T, H, N)
+        else:
+            assert got == 256
+        assert got % 16 == 0
+    assert kda.workspace_size(0, 4, 2) == 256          # no tokens, no records
+    assert kda.workspace_size(100, 4, 0) == 256
+
+
 def test_vsplit_boundary_matches_pages(L):
     g = json.load(open(os.path.join(GOLDEN, "vsplit_boundary.json")))
     for case in g["cases"]:
@@ -109,6 +138,8 @@ def _call(L, **over):
     (dict(beta=0x50001), kda.ERR_MISALIGNED),
     (dict(vsplit=3), kda.ERR_INVALID_ARG),
     (dict(kernel=7), kda.ERR_INVALID_ARG),
+    (dict(kernel=-1), kda.ERR_INVALID_ARG),
+    (dict(kernel=3, vsplit=1), kda.ERR_INVALID_ARG),   # the split path always splits
 ])
 def test_argument_gate(L, over, code):
     assert _call(L, **over) == code

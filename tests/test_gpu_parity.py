@@ -23,7 +23,7 @@ pytestmark = pytest.mark.gpu
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 TOL = json.load(open(os.path.join(ROOT, "tests", "golden", "tolerances.json")))["max_abs"]
-KERNELS = [kda.KERNEL_REF, kda.KERNEL_TC]
+KERNELS = [kda.KERNEL_REF, kda.KERNEL_TC, kda.KERNEL_SPLIT]
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -99,6 +99,11 @@ def test_ragged_tiles_and_tails(oracle_mod, kernel, vsplit):
     """Several chunks, ragged tails, a 1-token and an empty sequence."""
     w = W.custom([1, 63, 64, 65, 130, 0, 200, 17, 129], 3, seed=21)
     inp = W.make_inputs(w)
+    if kernel == kda.KERNEL_SPLIT and vsplit == 1:
+        with pytest.raises(kda.KDAError) as e:     # the split path always splits
+            run_gpu(inp, kernel, vsplit)
+        assert e.value.code == kda.ERR_INVALID_ARG
+        return
     out, fin = run_gpu(inp, kernel, vsplit)
     check(oracle_mod, inp, out, fin, tag=f"ragged k{kernel} P{vsplit}")
 
@@ -134,6 +139,34 @@ def test_workload3_vsplit_vs_unsplit(oracle_mod, n):
     heads = [0, 3, 7]
     check(oracle_mod, inp, out_a, fin_a, heads=heads, tag=f"w3 n={n} auto")
     check(oracle_mod, inp, out_1, fin_1, heads=heads, tag=f"w3 n={n} P=1")
+
+
+@pytest.mark.parametrize("cfg", [2, 3])
+def test_auto_takes_split_path_when_it_triggers(oracle_mod, cfg):
+    """One long sequence (16 heads) and 2 x 4096 (8 heads): AUTO runs the split
+    path (k-side records + chain per value slice) -- same values as forcing it."""
+    inp = W.make_inputs(W.workload(cfg, 2) if cfg == 3 else W.workload(cfg))
+    out_a, fin_a = run_gpu(inp)
+    out_s, fin_s = run_gpu(inp, kda.KERNEL_SPLIT)
+    assert torch.equal(out_a, out_s) and torch.equal(fin_a, fin_s)
+
+
+def test_split_falls_back_to_fused_on_small_workspace(oracle_mod):
+    """AUTO with a workspace below the split path's record area runs the fused
+    kernel; forcing the split path with it is refused."""
+    inp = W.make_inputs(W.custom([150, 70], 2, seed=31))
+    d = to_dev(inp)
+    small = torch.zeros(256, dtype=torch.uint8, device="cuda")
+    args = (d["q"], d["k"], d["v"], d["g"], d["beta"], d["A_log"], d["dt_bias"],
+            d["lower_bound"], d["scale"], d["initial_state"], d["cu_seqlens"])
+    out, fin = kda.chunk_prefill_fwd(*args, workspace=small)
+    torch.cuda.synchronize()
+    out_t, fin_t = run_gpu(inp, kda.KERNEL_TC, vsplit=1)
+    assert torch.equal(out, out_t) and torch.equal(fin, fin_t)
+    check(oracle_mod, inp, out, fin, tag="small workspace")
+    with pytest.raises(kda.KDAError) as e:
+        kda.chunk_prefill_fwd(*args, workspace=small, kernel=kda.KERNEL_SPLIT)
+    assert e.value.code == kda.ERR_WORKSPACE_TOO_SMALL
 
 
 def test_workload4_ragged_bf16_state(oracle_mod):
