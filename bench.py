@@ -280,6 +280,9 @@ def main():
             d["out"] = torch.empty_like(d["q"])
             d["fin"] = torch.empty_like(d["initial_state"])
             d["ws"] = kda.alloc_workspace(T, H, N, device=dev)
+            if kernel == kda.KERNEL_SPLIT:   # records for every chunk slot of this batch
+                n_ws = 1024 + ((T + 63) // 64 + N) * H * 66560
+                d["ws"] = torch.zeros(max(n_ws, d["ws"].numel()), dtype=torch.uint8, device=dev)
             sets.append(d)
     stream.synchronize()
     path, vsplit_used, launches_per_step = kda.plan(T, N, H, sets[0]["ws"].numel(), args.vsplit,

@@ -76,11 +76,9 @@ int plan(int64_t total_tokens, int32_t num_seqs, int32_t heads, size_t workspace
   if (kernel != KDA_KERNEL_AUTO && kernel != KDA_KERNEL_TC && kernel != KDA_KERNEL_REF &&
       kernel != KDA_KERNEL_SPLIT)
     return KDA_ERR_INVALID_ARG;
-  if (kernel == KDA_KERNEL_SPLIT && vsplit == 1) return KDA_ERR_INVALID_ARG;
   const size_t split_need = kda::split_workspace_bytes(total_tokens, heads, num_seqs);
   int P = vsplit == -1 ? kda_choose_vsplit(num_seqs, heads, sms) : vsplit;
   if (kernel == KDA_KERNEL_SPLIT) {
-    if (P < 2) P = 2;
     if (workspace_bytes < split_need) return KDA_ERR_WORKSPACE_TOO_SMALL;
   } else if (kernel == KDA_KERNEL_AUTO) {
     if (P > 1 && workspace_bytes >= split_need && total_tokens > 0)
@@ -113,7 +111,6 @@ int fwd_impl(const void* q, const void* k, const void* v, const void* g, const v
   if (kernel != KDA_KERNEL_AUTO && kernel != KDA_KERNEL_TC && kernel != KDA_KERNEL_REF &&
       kernel != KDA_KERNEL_SPLIT)
     return KDA_ERR_INVALID_ARG;
-  if (kernel == KDA_KERNEL_SPLIT && vsplit == 1) return KDA_ERR_INVALID_ARG;
   int dev = 0, sms = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) {
     cudaGetLastError();

@@ -2,7 +2,9 @@
 //
 // The chunk-parallel k-side kernel has already written, for every (chunk, head),
 // a record with -W, Qg (raw q times 2^Gam), Ke (raw k times 2^(Gam_last - Gam)),
-// T diag(b), the raw masked QK, the chunk decay 2^Gam_last and the norm scalars.
+// T diag(b), the raw masked QK, the chunk decay 2^Gam_last and the norm scalars,
+// as the image of 128-byte-swizzled K-major shared-memory tiles; it is copied in
+// as is (bulk copies) and read with ldmatrix.
 // This kernel walks one sequence's chunks in order for one head and one slice of
 // DV = 128 / P value columns -- the value-dimension split of "[Kimi-K3][Perf]
 // Update FlashKDA for automatic K2 V-split" (PR #52458, Features & motivation),
@@ -26,8 +28,9 @@ using namespace sm100;
 constexpr int NT2 = 256;   // 8 warps
 
 // shared memory per record buffer
-constexpr int B_WN = 0, B_QG = 16384, B_KE = 32768, B_TB = 49152, B_QK = 57344;
-constexpr int B_VEC = 65536, B_V = 66560 + 1024;   // V slice (aligned up to 1 KB)
+// shared memory per record buffer: the record image, then the V slice
+constexpr int B_WQ = kRecWQ, B_QKE = kRecQKE, B_TB = kRecTB, B_VEC = kRecVec;
+constexpr int B_V = kRecBytes + 1024;   // V slice (aligned up to 1 KB)
 constexpr int BUF_BYTES = B_V + 8192;               // room for V of DV <= 64
 
 template <int DV>
@@ -44,11 +47,6 @@ struct ChainSmem {
 
 __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t (&r)[4]) {
   asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
-               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-               : "r"(addr));
-}
-__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t (&r)[4]) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
                : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
                : "r"(addr));
 }
@@ -83,8 +81,6 @@ __device__ __forceinline__ uint32_t swv(int row, int col) {
 }
 
 struct ChainMaps {
-  CUtensorMap rec128;   // workspace as [rows][128] bf16 (256-B rows)
-  CUtensorMap rec64;    // workspace as [rows][64] bf16 (128-B rows)
   CUtensorMap v;        // v as [T][H*128] bf16, box {DV, 64}
 };
 
@@ -128,19 +124,13 @@ __global__ void __launch_bounds__(NT2, 1)
     const uint32_t base = sb + (buf ? L_::OFF_BUF1 : L_::OFF_BUF0);
     const uint32_t bar = buf ? bar1 : bar0;
     const int64_t rec = (int64_t)(slot0 + i) * H + h;
-    const int r128 = (int)((kSplitHeader + rec * kRecBytes) / 256);
-    const int r64 = (int)((kSplitHeader + rec * kRecBytes) / 128);
-    mbar_expect_tx(bar, 5 * 16384 + 1024 + 64 * DV * 2 - 16384);
+    const unsigned char* src =
+        reinterpret_cast<const unsigned char*>(p.status) + kSplitHeader + rec * kRecBytes;
+    mbar_expect_tx(bar, kRecBytes + 64 * DV * 2);
 #pragma unroll
-    for (int tile = 0; tile < 3; ++tile)
-#pragma unroll
-      for (int b = 0; b < 2; ++b)
-        tma_load_2d(base + tile * 16384 + b * 8192, &maps.rec128, 64 * b, r128 + 64 * tile, bar);
-    tma_load_2d(base + B_TB, &maps.rec64, 0, r64 + kRecTB / 128, bar);
-    tma_load_2d(base + B_QK, &maps.rec64, 0, r64 + kRecQK / 128, bar);
-    const unsigned char* vec = reinterpret_cast<const unsigned char*>(p.status) + kSplitHeader +
-                               rec * kRecBytes + kRecVec;
-    bulk_load(base + B_VEC, vec, 1024, bar);
+    for (int part = 0; part < 4; ++part)
+      bulk_load(base + part * 16384, src + part * 16384, 16384, bar);
+    bulk_load(base + kRecVec, src + kRecVec, kRecBytes - kRecVec, bar);
     tma_load_2d(base + B_V, &maps.v, h * 128 + dv0, t0 + kChunk * i, bar);
   };
 
@@ -216,7 +206,7 @@ __global__ void __launch_bounds__(NT2, 1)
       uint32_t a[4];
       {
         const int row = 16 * mt + (lane & 15), col = 16 * ks + 8 * (lane >> 4);
-        ldsm_x4(rbs + B_TB + sw128(row, col, 64), a);
+        ldsm_x4(rbs + B_TB + sw128(row, col, 64), a);   // T diag(b)
       }
 #pragma unroll
       for (int j = 0; j < NPW; ++j) {
@@ -231,7 +221,7 @@ __global__ void __launch_bounds__(NT2, 1)
       uint32_t a[4];
       {
         const int row = 16 * mt + (lane & 15), col = 16 * ks + 8 * (lane >> 4);
-        ldsm_x4(rbs + B_WN + sw128(row, col, 64), a);
+        ldsm_x4(rbs + B_WQ + sw128(row, col, 128), a);   // -W: rows 0-63 of [-W; Qg]
       }
 #pragma unroll
       for (int j = 0; j < NPW; ++j) {
@@ -265,7 +255,7 @@ __global__ void __launch_bounds__(NT2, 1)
       for (int ks = 0; ks < 8; ++ks) {
         uint32_t a[4];
         const int row = 16 * mt + (lane & 15), col = 16 * ks + 8 * (lane >> 4);
-        ldsm_x4(rbs + B_QG + sw128(row, col, 64), a);
+        ldsm_x4(rbs + B_WQ + sw128(64 + row, col, 128), a);   // Qg: rows 64-127
 #pragma unroll
         for (int j = 0; j < NPW; ++j) {
           uint32_t b[2];
@@ -278,7 +268,7 @@ __global__ void __launch_bounds__(NT2, 1)
       for (int ks = 0; ks < 4; ++ks) {
         uint32_t a[4];
         const int row = 16 * mt + (lane & 15), col = 16 * ks + 8 * (lane >> 4);
-        ldsm_x4(rbs + B_QK + sw128(row, col, 64), a);
+        ldsm_x4(rbs + B_QKE + sw128(row, col, 192), a);   // QK: rows 0-63 of [QK; Ke]
 #pragma unroll
         for (int j = 0; j < NPW; ++j) {
           uint32_t b[2];
@@ -314,10 +304,9 @@ __global__ void __launch_bounds__(NT2, 1)
 #pragma unroll
       for (int ks = 0; ks < 4; ++ks) {
         uint32_t a[4];
-        {   // A = Ke^T (rows dk, k = token) from Ke stored [token][dk]
-          const int j = lane >> 3, rr = lane & 7;
-          const int s = 16 * ks + ((j >> 1) << 3) + rr, dk = 16 * warp + ((j & 1) << 3);
-          ldsm_x4_t(rbs + B_KE + sw128(s, dk, 64), a);
+        {   // A = Ke^T: rows 64 + dk of [QK; Ke], K = token
+          const int row = 16 * warp + (lane & 15), col = 16 * ks + 8 * (lane >> 4);
+          ldsm_x4(rbs + B_QKE + sw128(64 + row, col, 192), a);
         }
 #pragma unroll
         for (int nt = 0; nt < DV / 8; ++nt) {
@@ -368,26 +357,7 @@ typedef CUresult (*EncodeTiledFn2)(CUtensorMap*, CUtensorMapDataType, cuuint32_t
 bool make_chain_maps(ChainMaps* m, const Params& p, int dv) {
   EncodeTiledFn2 enc = reinterpret_cast<EncodeTiledFn2>(tensor_map_encoder());
   if (!enc) return false;
-  const size_t wsb = split_workspace_bytes(p.total_tokens, p.heads, p.num_seqs);
   const cuuint32_t es[2] = {1, 1};
-  {
-    cuuint64_t dims[2] = {128, (cuuint64_t)(wsb / 256)};
-    cuuint64_t strides[1] = {256};
-    cuuint32_t box[2] = {64, 64};
-    if (enc(&m->rec128, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.status, dims, strides, box, es,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-      return false;
-  }
-  {
-    cuuint64_t dims[2] = {64, (cuuint64_t)(wsb / 128)};
-    cuuint64_t strides[1] = {128};
-    cuuint32_t box[2] = {64, 64};
-    if (enc(&m->rec64, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.status, dims, strides, box, es,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-      return false;
-  }
   {
     cuuint64_t dims[2] = {(cuuint64_t)p.heads * 128, (cuuint64_t)(p.total_tokens > 0 ? p.total_tokens : 1)};
     cuuint64_t strides[1] = {(cuuint64_t)p.heads * 256};
@@ -425,10 +395,11 @@ cudaError_t launch_chain_dv(const Params& p, cudaStream_t stream) {
 }  // namespace
 
 cudaError_t launch_split(const Params& p, cudaStream_t stream) {
-  if (p.vsplit != 2 && p.vsplit != 4 && p.vsplit != 8) return cudaErrorInvalidValue;
+  if (p.vsplit != 1 && p.vsplit != 2 && p.vsplit != 4 && p.vsplit != 8) return cudaErrorInvalidValue;
   cudaError_t e = launch_kside(p, stream);
   if (e != cudaSuccess) return e;
   switch (p.vsplit) {
+    case 1: return launch_chain_tc(p, stream);
     case 2: return launch_chain_dv<64>(p, stream);
     case 4: return launch_chain_dv<32>(p, stream);
     default: return launch_chain_dv<16>(p, stream);

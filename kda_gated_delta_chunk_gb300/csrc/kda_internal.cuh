@@ -14,14 +14,16 @@ constexpr float kL2Eps = 1e-6f;      // l2norm epsilon inside the square root
 constexpr int kWorkspaceBytes = 256;  // device status word + error detail (fused path)
 constexpr int kDefaultSmCount = 152;  // GB300; sizes the workspace when no device answers
 
-// Split path (chunk-parallel k-side kernel, then the chain kernel): one record per
-// (chunk slot, head) in the workspace after a 1 KB header.  bf16 row-major tiles
-// plus fp32 vectors, all offsets 1024-byte aligned:
-constexpr int kRecWN = 0;         // -W          [64 tok][128 dk]
-constexpr int kRecQG = 16384;     // q_raw * g   [64 tok][128 dk]
-constexpr int kRecKE = 32768;     // k_raw * ke  [64 tok][128 dk]
-constexpr int kRecTB = 49152;     // T diag(b)   [64][64]
-constexpr int kRecQK = 57344;     // raw masked QK [64][64]
+// Split path (chunk-parallel k-side kernel, then a chain kernel): one record per
+// (chunk slot, head) in the workspace after a 1 KB header.  Each record is the image of
+// the shared-memory operand tiles the chain kernels read: bf16, K-major with the 128-byte
+// swizzle (a tile of R rows keeps K columns 64 kb .. 64 kb + 63 at kb * R * 128 bytes;
+// row r at r * 128 within that block; the 16-byte chunk index XORed with r % 8):
+constexpr int kRecWQ = 0;         // [-W; Qg]  128 rows x K 128: rows 0-63 -W (token rows,
+                                  //           K = dk), rows 64-127 q_raw * 2^Gam
+constexpr int kRecQKE = 32768;    // [QK; Ke]  192 rows x K 64: rows 0-63 raw masked QK
+                                  //           (r, K = s), rows 64-191 Ke (dk rows, K = token)
+constexpr int kRecTB = 57344;     // T diag(b) 64 rows x K 64
 constexpr int kRecVec = 65536;    // fp32: decay [128], scale/|q| [64], 1/|k| [64]
 constexpr int kRecBytes = 66560;
 constexpr int kSplitHeader = 1024;
@@ -66,6 +68,7 @@ cudaError_t launch_tc(const Params& p, cudaStream_t stream);
 // Split path: k-side records for every chunk slot (launch_kside), then the chain
 // per value slice; launch_split runs both.
 cudaError_t launch_kside(const Params& p, cudaStream_t stream);
+cudaError_t launch_chain_tc(const Params& p, cudaStream_t stream);   // P = 1
 cudaError_t launch_split(const Params& p, cudaStream_t stream);
 // cuTensorMapEncodeTiled from the driver (null if unavailable)
 void* tensor_map_encoder();

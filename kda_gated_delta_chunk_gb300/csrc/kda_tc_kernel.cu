@@ -493,11 +493,12 @@ __global__ void __launch_bounds__(NT, 1)
           ke0 = Ei0 * cB[0];
           ke1 = Ei1 * cB[1];
         }
-        if constexpr (SPLIT) {   // record tiles, row-major [token][dk]
-          st_u32(sm, OFF_QG + r * 256 + d0 * 2, bmul2(q2, pack_bf16x2(g0, g1)));
-          st_u32(sm, OFF_KE + r * 256 + d0 * 2, bmul2(k2, pack_bf16x2(ke0, ke1)));
+        st_u32(sm, OFF_QG + kmajor_off(r, d0, 64), bmul2(q2, pack_bf16x2(g0, g1)));
+        if constexpr (SPLIT) {   // record tile: Ke K-major with dk rows, K = token
+          const uint32_t ke2 = bmul2(k2, pack_bf16x2(ke0, ke1));
+          *reinterpret_cast<uint16_t*>(sm + OFF_INV + kmajor_off(d0, r, 128)) = (uint16_t)(ke2 & 0xffffu);
+          *reinterpret_cast<uint16_t*>(sm + OFF_INV + kmajor_off(d0 + 1, r, 128)) = (uint16_t)(ke2 >> 16);
         } else {
-          st_u32(sm, OFF_QG + kmajor_off(r, d0, 64), bmul2(q2, pack_bf16x2(g0, g1)));
           st_u32(sm, OFF_KE + mnmajor_off(d0, r, 8192), bmul2(k2, pack_bf16x2(ke0, ke1)));
         }
       }
@@ -594,8 +595,7 @@ __global__ void __launch_bounds__(NT, 1)
             w[e] = pack_bf16x2(s <= r ? __uint_as_float(a[c8 * 8 + e * 2]) : 0.0f,
                                s + 1 <= r ? __uint_as_float(a[c8 * 8 + e * 2 + 1]) : 0.0f);
           }
-          st_u128(sm, OFF_QKB + (SPLIT ? (uint32_t)(r * 128 + (32 * cs + c8 * 8) * 2)
-                                       : kmajor_off(r, 32 * cs + c8 * 8, 64)),
+          st_u128(sm, OFF_QKB + kmajor_off(r, 32 * cs + c8 * 8, 64),
                   make_uint4(w[0], w[1], w[2], w[3]));
         }
       }
@@ -709,7 +709,7 @@ __global__ void __launch_bounds__(NT, 1)
       t0v = make_float4(t0v.x * b0v.x, t0v.y * b0v.y, t0v.z * b0v.z, t0v.w * b0v.w);
       t1v = make_float4(t1v.x * b1v.x, t1v.y * b1v.y, t1v.z * b1v.z, t1v.w * b1v.w);
       const uint32_t off = kmajor_off(r, c8 * 8, 64);
-      st_u128(sm, OFF_TBU + (SPLIT ? (uint32_t)(r * 128 + c8 * 16) : off),
+      st_u128(sm, OFF_TBU + off,
               make_uint4(pack_bf16x2(t0v.x, t0v.y), pack_bf16x2(t0v.z, t0v.w),
                          pack_bf16x2(t1v.x, t1v.y), pack_bf16x2(t1v.z, t1v.w)));
       st_u128(sm, OFF_TB + off,
@@ -770,12 +770,12 @@ __global__ void __launch_bounds__(NT, 1)
               f0 * __uint_as_float(w0[j + 1]) + f1b * (f1a * __uint_as_float(w1[j + 1]));
           w[e] = pack_bf16x2(-x0, -x1);
         }
-        if constexpr (SPLIT) {   // record tile, row-major [token][dk]
+        if constexpr (SPLIT) {   // record tile: -W K-major with token rows, K = dk
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
             const int tok = cs * 16 + c8 * 8 + e * 2;
-            *reinterpret_cast<uint16_t*>(sm + OFF_WN + tok * 256 + dk * 2) = (uint16_t)(w[e] & 0xffffu);
-            *reinterpret_cast<uint16_t*>(sm + OFF_WN + (tok + 1) * 256 + dk * 2) = (uint16_t)(w[e] >> 16);
+            *reinterpret_cast<uint16_t*>(sm + OFF_WN + kmajor_off(tok, dk, 64)) = (uint16_t)(w[e] & 0xffffu);
+            *reinterpret_cast<uint16_t*>(sm + OFF_WN + kmajor_off(tok + 1, dk, 64)) = (uint16_t)(w[e] >> 16);
           }
         } else {
           st_u128(sm, OFF_WN + mnmajor_off(cs * 16 + c8 * 8, dk, 8192),
@@ -792,11 +792,14 @@ __global__ void __launch_bounds__(NT, 1)
       if (tid == 0) {
         unsigned char* rec = reinterpret_cast<unsigned char*>(p.status) + kSplitHeader +
                              (size_t)item * kRecBytes;
-        bulk_store(rec + kRecWN, sb + OFF_WN, 16384);
-        bulk_store(rec + kRecQG, sb + OFF_QG, 16384);
-        bulk_store(rec + kRecKE, sb + OFF_KE, 16384);
+        // [-W; Qg]: per 64-column block of K, the 64 rows of -W then the 64 rows of Qg
+        bulk_store(rec + kRecWQ, sb + OFF_WN, 8192);
+        bulk_store(rec + kRecWQ + 8192, sb + OFF_QG, 8192);
+        bulk_store(rec + kRecWQ + 16384, sb + OFF_WN + 8192, 8192);
+        bulk_store(rec + kRecWQ + 24576, sb + OFF_QG + 8192, 8192);
+        bulk_store(rec + kRecQKE, sb + OFF_QKB, 8192);          // [QK; Ke]
+        bulk_store(rec + kRecQKE + 8192, sb + OFF_INV, 16384);
         bulk_store(rec + kRecTB, sb + OFF_TBU, 8192);
-        bulk_store(rec + kRecQK, sb + OFF_QKB, 8192);
         bulk_store(rec + kRecVec, sb + OFF_DECAY, 512);
         bulk_store(rec + kRecVec + 512, sb + OFF_INVN, 512);
         bulk_commit();

@@ -139,7 +139,6 @@ def _call(L, **over):
     (dict(vsplit=3), kda.ERR_INVALID_ARG),
     (dict(kernel=7), kda.ERR_INVALID_ARG),
     (dict(kernel=-1), kda.ERR_INVALID_ARG),
-    (dict(kernel=3, vsplit=1), kda.ERR_INVALID_ARG),   # the split path always splits
 ])
 def test_argument_gate(L, over, code):
     assert _call(L, **over) == code

@@ -41,14 +41,24 @@ def to_dev(inp):
             for k, v in inp.items()}
 
 
+def split_workspace(T, H, N):
+    """Workspace with the split path's records for exactly this batch: a 1 KB header and
+    66,560 bytes per (chunk slot, head), ceil(T / 64) + N slots."""
+    n = 1024 + ((T + 63) // 64 + N) * H * 66560
+    return torch.zeros(n, dtype=torch.uint8, device="cuda")
+
+
 def run_gpu(inp, kernel=kda.KERNEL_AUTO, vsplit=-1, out=None, final_state=None, init="keep"):
     d = to_dev(inp)
     s0 = d["initial_state"] if init == "keep" else None
+    ws = None
+    if kernel == kda.KERNEL_SPLIT:
+        ws = split_workspace(d["q"].shape[0], d["q"].shape[1], d["cu_seqlens"].numel() - 1)
     out, fin = kda.chunk_prefill_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], d["A_log"],
                                      d["dt_bias"], d["lower_bound"], d["scale"], s0,
                                      d["cu_seqlens"], out=out, final_state=final_state,
-                                     state_dtype=inp["initial_state"].dtype, vsplit=vsplit,
-                                     kernel=kernel)
+                                     workspace=ws, state_dtype=inp["initial_state"].dtype,
+                                     vsplit=vsplit, kernel=kernel)
     torch.cuda.synchronize()
     return out, fin
 
@@ -99,11 +109,6 @@ def test_ragged_tiles_and_tails(oracle_mod, kernel, vsplit):
     """Several chunks, ragged tails, a 1-token and an empty sequence."""
     w = W.custom([1, 63, 64, 65, 130, 0, 200, 17, 129], 3, seed=21)
     inp = W.make_inputs(w)
-    if kernel == kda.KERNEL_SPLIT and vsplit == 1:
-        with pytest.raises(kda.KDAError) as e:     # the split path always splits
-            run_gpu(inp, kernel, vsplit)
-        assert e.value.code == kda.ERR_INVALID_ARG
-        return
     out, fin = run_gpu(inp, kernel, vsplit)
     check(oracle_mod, inp, out, fin, tag=f"ragged k{kernel} P{vsplit}")
 
@@ -118,11 +123,12 @@ def test_bf16_state(oracle_mod, kernel):
 
 
 @pytest.mark.parametrize("cfg", [1, 2])
-def test_workloads_1_2_full_size(oracle_mod, cfg):
+@pytest.mark.parametrize("kernel", [kda.KERNEL_AUTO, kda.KERNEL_TC, kda.KERNEL_SPLIT])
+def test_workloads_1_2_full_size(oracle_mod, cfg, kernel):
     inp = W.make_inputs(W.workload(cfg))
-    out, fin = run_gpu(inp)
+    out, fin = run_gpu(inp, kernel, 1 if kernel == kda.KERNEL_TC else -1)
     heads = None if cfg == 1 else [0, 5, 11, 15]
-    check(oracle_mod, inp, out, fin, heads=heads, tag=f"workload {cfg}")
+    check(oracle_mod, inp, out, fin, heads=heads, tag=f"workload {cfg} k{kernel}")
 
 
 @pytest.mark.parametrize("n", [1, 2, 3, 7])
@@ -169,10 +175,11 @@ def test_split_falls_back_to_fused_on_small_workspace(oracle_mod):
     assert e.value.code == kda.ERR_WORKSPACE_TOO_SMALL
 
 
-def test_workload4_ragged_bf16_state(oracle_mod):
+@pytest.mark.parametrize("kernel", [kda.KERNEL_AUTO, kda.KERNEL_SPLIT])
+def test_workload4_ragged_bf16_state(oracle_mod, kernel):
     w = W.workload(4)
     inp = W.make_inputs(w)
-    out, fin = run_gpu(inp)
+    out, fin = run_gpu(inp, kernel)
     lens = list(w.lengths)
     longest = int(np.argmax(lens))
     shortest = int(np.argmin(lens))
