@@ -3,8 +3,8 @@
 // The chunk-parallel k-side kernel has already written, for every (chunk, head),
 // a record with -W, Qg (raw q times 2^Gam), Ke (raw k times 2^(Gam_last - Gam)),
 // T diag(b), the raw masked QK, the chunk decay 2^Gam_last and the norm scalars,
-// as the image of 128-byte-swizzled K-major shared-memory tiles; it is copied in
-// as is (bulk copies) and read with ldmatrix.
+// as the image of 128-byte-swizzled shared-memory tiles; it is copied in as is
+// (bulk copies) and read with ldmatrix.
 // This kernel walks one sequence's chunks in order for one head and one slice of
 // DV = 128 / P value columns -- the value-dimension split of "[Kimi-K3][Perf]
 // Update FlashKDA for automatic K2 V-split" (PR #52458, Features & motivation),
@@ -47,6 +47,11 @@ struct ChainSmem {
 
 __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t (&r)[4]) {
   asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t (&r)[4]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
                : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
                : "r"(addr));
 }
@@ -159,12 +164,20 @@ __global__ void __launch_bounds__(NT2, 1)
       *reinterpret_cast<uint32_t*>(sbf + ((r0 + 8) * SP + c) * 2) = bf2(S[nt][2], S[nt][3]);
     }
   };
+  auto prefetch_l2 = [&](int i) {   // record + v slice of chunk i -> L2
+    const int64_t rec = (int64_t)(slot0 + i) * H + h;
+    l2_prefetch(reinterpret_cast<const unsigned char*>(p.status) + kSplitHeader + rec * kRecBytes,
+                kRecBytes);
+    tma_prefetch_2d(&maps.v, h * 128 + dv0, t0 + kChunk * i);
+  };
   stage_s(0);
   uint32_t phase = 0;   // bit b: parity to wait for on buffer b
   int pending = 0;   // buffers with a fetch in flight (thread 0's view)
   if (tid == 0 && nch > 0) {
     issue(0, 0);
     pending = 1;
+    if (nch > 1) prefetch_l2(1);
+    if (nch > 2) prefetch_l2(2);
   }
   __syncthreads();
 
@@ -179,6 +192,7 @@ __global__ void __launch_bounds__(NT2, 1)
     if (tid == 0 && i + 1 < nch) {
       issue(i + 1, buf ^ 1);
       pending |= 2 >> buf;
+      if (i + 3 < nch) prefetch_l2(i + 3);
     }
     const bool ok = mbar_wait(buf ? bar1 : bar0, (phase >> buf) & 1u);
     if (__syncthreads_or(!ok)) { failed = true; break; }
@@ -219,9 +233,10 @@ __global__ void __launch_bounds__(NT2, 1)
 #pragma unroll
     for (int ks = 0; ks < 8; ++ks) {
       uint32_t a[4];
-      {
-        const int row = 16 * mt + (lane & 15), col = 16 * ks + 8 * (lane >> 4);
-        ldsm_x4(rbs + B_WQ + sw128(row, col, 128), a);   // -W: rows 0-63 of [-W; Qg]
+      {   // -W (token rows, K = dk) from the MN-major [-W | Qg] image, transposed
+        const int j = lane >> 3;
+        const int m0 = 16 * mt + 8 * (j & 1), k = 16 * ks + 8 * (j >> 1) + (lane & 7);
+        ldsm_x4_t(rbs + B_WQ + mnmajor_off(m0, k, 16384), a);
       }
 #pragma unroll
       for (int j = 0; j < NPW; ++j) {
@@ -254,8 +269,9 @@ __global__ void __launch_bounds__(NT2, 1)
 #pragma unroll
       for (int ks = 0; ks < 8; ++ks) {
         uint32_t a[4];
-        const int row = 16 * mt + (lane & 15), col = 16 * ks + 8 * (lane >> 4);
-        ldsm_x4(rbs + B_WQ + sw128(64 + row, col, 128), a);   // Qg: rows 64-127
+        const int j = lane >> 3;   // Qg: tokens 64-127 of the [-W | Qg] image
+        const int m0 = 16 * mt + 8 * (j & 1), k = 16 * ks + 8 * (j >> 1) + (lane & 7);
+        ldsm_x4_t(rbs + B_WQ + mnmajor_off(64 + m0, k, 16384), a);
 #pragma unroll
         for (int j = 0; j < NPW; ++j) {
           uint32_t b[2];

@@ -2,11 +2,11 @@
 // inter-chunk chain on tcgen05, one CTA (256 threads) per (sequence, head).
 //
 // The k-side kernel left, per (chunk, head), the shared-memory image of the
-// operand tiles this kernel needs ([-W; Qg], [QK; Ke], T diag(b), decay and norm
+// operand tiles this kernel needs ([-W | Qg], [QK; Ke], T diag(b), decay and norm
 // scalars).  Each record and the chunk's v tile are fetched (bulk copy + TMA)
 // into one of two stages while the previous chunk runs.  The 128 x 128 fp32
 // state stays in tensor memory, transposed (lane = value channel):
-//   [U^T | O^T]  = S^T [-W; Qg]^T        one MMA group, N = 128 (U = -W S, O = Qg S)
+//   [U^T | O^T]  = S^T [-W | Qg]^T        one MMA group, N = 128 (U = -W S, O = Qg S)
 //   U^T         += V^T (T diag(b))^T      (U' of the WY/UT form)
 //   U_b^T        = bf16(U^T diag(1/|k|))
 //   S^T          = S^T diag(2^Gam_last)   (before the group below)
@@ -53,7 +53,7 @@ constexpr uint32_t T_SB = 256;   // S^T bf16, 64 cols (2 dk per col)
 constexpr uint32_t T_UB = 320;   // U_b^T bf16, 32 cols (2 tokens per col)
 constexpr uint32_t T_COLS = 512;
 
-constexpr uint32_t ID_G1 = idesc_bf16(128, 128, 0, 0);   // [U|O]  += SB  x [-W; Qg]^T
+constexpr uint32_t ID_G1 = idesc_bf16(128, 128, 0, 1);   // [U|O]  += SB  x [-W | Qg]^T
 constexpr uint32_t ID_G2 = idesc_bf16(128, 192, 0, 0);   // [O|S]  += UB  x [QK; Ke]^T
 constexpr uint32_t ID_UP = idesc_bf16(128, 64, 1, 0);    // U      += V^T x (T diag b)^T
 
@@ -145,7 +145,18 @@ __global__ void __launch_bounds__(NT3, 1)
     tma_load_2d(base + STAGE_V, &maps.v, xcol, t0 + kChunk * i, bar);
     tma_load_2d(base + STAGE_V + 8192, &maps.v, xcol + 64, t0 + kChunk * i, bar);
   };
-  if (tid == 0 && nch > 0) issue(0);
+  auto prefetch_l2 = [&](int i) {               // record + v of chunk i -> L2
+    const unsigned char* src = reinterpret_cast<const unsigned char*>(p.status) + kSplitHeader +
+                               ((int64_t)(slot0 + i) * H + h) * kRecBytes;
+    l2_prefetch(src, kRecBytes);
+    tma_prefetch_2d(&maps.v, xcol, t0 + kChunk * i);
+    tma_prefetch_2d(&maps.v, xcol + 64, t0 + kChunk * i);
+  };
+  if (tid == 0 && nch > 0) {
+    issue(0);
+    if (nch > 1) prefetch_l2(1);
+    if (nch > 2) prefetch_l2(2);
+  }
 
   // ---- state in: S^T[dv][dk] -> TMEM (lane = dv); this warp covers 64 key columns
   {
@@ -266,12 +277,12 @@ __global__ void __launch_bounds__(NT3, 1)
     tc_fence_before();
     __syncthreads();   // (A) SB ready, S decayed, O(i-1) staged; stage buf^1 free
 
-    // ---- 3. [U | O] = SB [-W; Qg]^T, U += V^T (T diag b)^T; prefetch chunk i+1
+    // ---- 3. [U | O] = SB [-W | Qg]^T, U += V^T (T diag b)^T; prefetch chunk i+1
     if (tid == 0) {
       tc_fence_after();
 #pragma unroll
       for (int ks = 0; ks < 8; ++ks)
-        mma_bf16_ts(tmem + T_U, tmem + T_SB + 8 * ks, kdesc3(st + kRecWQ, 128, ks), ID_G1, ks > 0);
+        mma_bf16_ts(tmem + T_U, tmem + T_SB + 8 * ks, mndesc3(st + kRecWQ, 16384, ks), ID_G1, ks > 0);
 #pragma unroll
       for (int ks = 0; ks < 4; ++ks)
         mma_bf16(tmem + T_U, mndesc3(st + STAGE_V, 8192, ks), kdesc3(st + kRecTB, 64, ks), ID_UP, 1);
@@ -281,6 +292,7 @@ __global__ void __launch_bounds__(NT3, 1)
         issue(i + 1);
         pending |= 1 << (buf ^ 1);
       }
+      if (i + 3 < nch) prefetch_l2(i + 3);
     }
     if (i > 0) store_o(c0 - kChunk, L_prev);
     {

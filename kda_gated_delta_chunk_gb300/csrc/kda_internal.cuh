@@ -16,14 +16,13 @@ constexpr int kDefaultSmCount = 152;  // GB300; sizes the workspace when no devi
 
 // Split path (chunk-parallel k-side kernel, then a chain kernel): one record per
 // (chunk slot, head) in the workspace after a 1 KB header.  Each record is the image of
-// the shared-memory operand tiles the chain kernels read: bf16, K-major with the 128-byte
-// swizzle (a tile of R rows keeps K columns 64 kb .. 64 kb + 63 at kb * R * 128 bytes;
-// row r at r * 128 within that block; the 16-byte chunk index XORed with r % 8):
-constexpr int kRecWQ = 0;         // [-W; Qg]  128 rows x K 128: rows 0-63 -W (token rows,
-                                  //           K = dk), rows 64-127 q_raw * 2^Gam
-constexpr int kRecQKE = 32768;    // [QK; Ke]  192 rows x K 64: rows 0-63 raw masked QK
-                                  //           (r, K = s), rows 64-191 Ke (dk rows, K = token)
-constexpr int kRecTB = 57344;     // T diag(b) 64 rows x K 64
+// the shared-memory operand tiles the chain kernels read, bf16 with the 128-byte swizzle
+// (layouts of kda_sm100.cuh):
+constexpr int kRecWQ = 0;         // [-W | Qg] MN-major, MN = 128 tokens (0-63 of -W, 64-127
+                                  //           of q_raw * 2^Gam) in blocks 16 KB apart, K = dk
+constexpr int kRecQKE = 32768;    // [QK; Ke]  K-major, 192 rows x K 64: rows 0-63 raw masked
+                                  //           QK (r, K = s), rows 64-191 Ke (dk rows, K = token)
+constexpr int kRecTB = 57344;     // T diag(b) K-major, 64 rows x K 64
 constexpr int kRecVec = 65536;    // fp32: decay [128], scale/|q| [64], 1/|k| [64]
 constexpr int kRecBytes = 66560;
 constexpr int kSplitHeader = 1024;

@@ -38,28 +38,21 @@
 // The unit-lower-triangular inverse T runs on CUDA cores in fp32.  Inputs
 // arrive by TMA; the next chunk's q/k/g (and v) are fetched while this one
 // is being processed.
-//
-// The same kernel, instantiated with SPLIT = true, is the first kernel of the
-// value-split path: it runs only the chunk-local part (gate, factors, A/QK,
-// T, W) for every (chunk, head) independently -- one persistent CTA per SM
-// walking the (chunk slot, head) items -- and stores each item's record
-// (-W, Qg, Ke, T diag(b), QK, decay, norms) to the workspace by bulk copy.
-// The serial chain then runs in the chain kernel, one CTA per (sequence,
-// head, value slice).
 #include <cuda.h>
 
 #include "kda_internal.cuh"
 #include "kda_sm100.cuh"
+#include "kda_tc_common.cuh"
 
 namespace kda {
 namespace {
 
 using namespace sm100;
+using namespace tcc;
 
 constexpr int C = 64;
 constexpr int D = kHeadDim;
 constexpr int NT = 512;
-constexpr float kLog2e = 1.4426950408889634f;
 constexpr int kMaxRankSeqs = 128;   // longest-first ordering for up to this many sequences
 
 // ---- shared memory map (offsets from a 1024-byte aligned base)
@@ -70,7 +63,6 @@ constexpr int OFF_INV = 49152;              // v tile: 2 SW128 boxes [64 tok][64
 constexpr int OFF_RA = 65536;               // region reused within a chunk:
 constexpr int OFF_RKQ = OFF_RA;             //  [Kr; Qr] K-major 128 rows x 128 (live to W)
 constexpr int OFF_CKC = OFF_RA + 32768;     //  [Kc; Kc2] K-major 96 rows x 128 (live to D)
-constexpr int NS = 68;                      //  fp32 row stride of the T scratch (16-B rows)
 constexpr int OFF_NM = OFF_RA + 32768;      //  N = diag(b) strict(A)  [64][NS]  (after D)
 constexpr int OFF_TM = OFF_NM + 64 * NS * 4;//  T                      [64][NS]
 constexpr int OFF_Y = OFF_TM + 64 * NS * 4; //  products scratch       [32][NS]
@@ -112,116 +104,6 @@ constexpr uint32_t ID_MK64 = idesc_bf16(128, 64, 1, 0);
 constexpr uint32_t ID_KM64 = idesc_bf16(128, 64, 0, 1);
 constexpr uint32_t ID_KM128 = idesc_bf16(128, 128, 0, 1);
 
-__device__ __forceinline__ float ex2f(float x) {
-  float y;
-  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-  return y;
-}
-__device__ __forceinline__ float rcpf(float x) {
-  float y;
-  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-  return y;
-}
-__device__ __forceinline__ float sigm(float x) { return rcpf(1.0f + ex2f(-x * kLog2e)); }
-// bf16x2 product, rounded to nearest even
-__device__ __forceinline__ uint32_t bmul2(uint32_t a, uint32_t b) {
-  uint32_t r;
-  asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
-  return r;
-}
-
-__device__ __forceinline__ void st_u32(unsigned char* base, uint32_t off, uint32_t v) {
-  *reinterpret_cast<uint32_t*>(base + off) = v;
-}
-__device__ __forceinline__ void st_u128(unsigned char* base, uint32_t off, uint4 v) {
-  *reinterpret_cast<uint4*>(base + off) = v;
-}
-__device__ __forceinline__ uint32_t ld_u32(const unsigned char* base, uint32_t off) {
-  return *reinterpret_cast<const uint32_t*>(base + off);
-}
-__device__ __forceinline__ float2 unpack_bf16x2(uint32_t v) {
-  return make_float2(__uint_as_float(v << 16), __uint_as_float(v & 0xffff0000u));
-}
-__device__ __forceinline__ float4 ld4(const float* p) { return *reinterpret_cast<const float4*>(p); }
-
-// K-step descriptors
-__device__ __forceinline__ uint64_t kdesc(uint32_t tile, int rows, int ks) {
-  return sdesc_sw128(tile + (ks >> 2) * rows * 128 + (ks & 3) * 32, 16, 1024);
-}
-__device__ __forceinline__ uint64_t mndesc(uint32_t tile, uint32_t lbo, int ks) {
-  return sdesc_sw128(tile + ks * 2048, lbo, 1024);
-}
-
-// One warp: D(16 x 16) = -? A(16 x K) B(K x 16), fp32 smem matrices with row stride NS,
-// tf32 tensor-core products, K a multiple of 8.  Result written to `dst` (stride NS).
-template <int K>
-__device__ __forceinline__ void warp_gemm_16x16(const float* A, const float* B, float* dst,
-                                                float sign, int lane) {
-  const int g = lane >> 2, t = lane & 3;
-  float d0[4] = {0.f, 0.f, 0.f, 0.f}, d1[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-  for (int k0 = 0; k0 < K; k0 += 8) {
-    uint32_t a[4], b0[2], b1[2];
-    a[0] = to_tf32(A[g * NS + k0 + t]);
-    a[1] = to_tf32(A[(g + 8) * NS + k0 + t]);
-    a[2] = to_tf32(A[g * NS + k0 + t + 4]);
-    a[3] = to_tf32(A[(g + 8) * NS + k0 + t + 4]);
-    b0[0] = to_tf32(B[(k0 + t) * NS + g]);
-    b0[1] = to_tf32(B[(k0 + t + 4) * NS + g]);
-    b1[0] = to_tf32(B[(k0 + t) * NS + 8 + g]);
-    b1[1] = to_tf32(B[(k0 + t + 4) * NS + 8 + g]);
-    mma_tf32_16x8x8(d0, a, b0);
-    mma_tf32_16x8x8(d1, a, b1);
-  }
-  *reinterpret_cast<float2*>(dst + g * NS + 2 * t) = make_float2(sign * d0[0], sign * d0[1]);
-  *reinterpret_cast<float2*>(dst + (g + 8) * NS + 2 * t) = make_float2(sign * d0[2], sign * d0[3]);
-  *reinterpret_cast<float2*>(dst + g * NS + 8 + 2 * t) = make_float2(sign * d1[0], sign * d1[1]);
-  *reinterpret_cast<float2*>(dst + (g + 8) * NS + 8 + 2 * t) =
-      make_float2(sign * d1[2], sign * d1[3]);
-}
-
-// Item `it` of the split k-side grid is chunk slot it / H of head it % H.  Chunk c of
-// sequence n sits in slot floor(cu[n] / 64) + n + c (one-to-one, below split_slots()).
-// Returns false for the slots no chunk maps to and for inconsistent cu_seqlens.
-__device__ bool decode_item(const Params& p, int it, int* c0, int* t1) {
-  const int slot = it / p.heads;
-  int lo = 0, hi = p.num_seqs - 1;
-  while (lo < hi) {
-    const int mid = (lo + hi + 1) >> 1;
-    if ((p.cu_seqlens[mid] >> 6) + mid <= slot)
-      lo = mid;
-    else
-      hi = mid - 1;
-  }
-  const int a = p.cu_seqlens[lo], b = p.cu_seqlens[lo + 1];
-  const int c = slot - ((a >> 6) + lo);
-  if (a < 0 || c < 0 || (int64_t)b > p.total_tokens) return false;
-  const int64_t s = (int64_t)a + (int64_t)C * c;
-  if (s >= b) return false;
-  *c0 = (int)s;
-  *t1 = b;
-  return true;
-}
-// First item >= `from` (stepping by the grid) that holds a chunk: {item, c0, t1, head},
-// item = -1 when none is left.
-__device__ void find_item(const Params& p, int from, int total, int* out) {
-  out[0] = -1;
-  out[1] = 0;
-  out[2] = 0;
-  out[3] = 0;
-  for (int it = from; it < total && it >= 0; it += gridDim.x) {
-    int c0, t1;
-    if (decode_item(p, it, &c0, &t1)) {
-      out[0] = it;
-      out[1] = c0;
-      out[2] = t1;
-      out[3] = it % p.heads;
-      return;
-    }
-  }
-}
-
-template <bool SPLIT>
 __global__ void __launch_bounds__(NT, 1)
     kda_tc_chunk_kernel(const __grid_constant__ Params p, const __grid_constant__ CUtensorMap tm_q,
                         const __grid_constant__ CUtensorMap tm_k,
@@ -243,23 +125,11 @@ __global__ void __launch_bounds__(NT, 1)
   const uint32_t bar_qkg = sb + OFF_BAR, bar_v = bar_qkg + 8, bar_mma = bar_qkg + 16;
   const uint32_t bar_o = bar_qkg + 24;      // O^T = S^T Qg^T, issued by warp 4
 
-  const int P = SPLIT ? 1 : p.vsplit, H = p.heads, N = p.num_seqs;
-  int h = 0, vpart = 0, n = 0, t0 = 0, t1 = 0;
-  // split: items {item, c0, t1, head} at flags[4..7] (current), [8..11] (next),
-  // [12..15] (the one after, found during the T inverse)
-  const int total_items = SPLIT ? (int)(split_slots(p.total_tokens, N) * H) : 0;
-  if constexpr (SPLIT) {
-    if (tid == 0) {
-      find_item(p, blockIdx.x, total_items, flags + 4);
-      flags[8] = -1;
-      if (flags[4] >= 0) find_item(p, flags[4] + gridDim.x, total_items, flags + 8);
-    }
-    __syncthreads();
-  } else {
   // ---- work unit: (rank, head, part), longest sequence first
+  const int P = p.vsplit, H = p.heads, N = p.num_seqs;
   const int unit = blockIdx.x;
-  vpart = unit % P;
-  h = (unit / P) % H;
+  const int vpart = unit % P;
+  const int h = (unit / P) % H;
   const int rank = unit / (P * H);
   if (N <= kMaxRankSeqs) {
     int* lens = reinterpret_cast<int*>(gt);
@@ -279,13 +149,12 @@ __global__ void __launch_bounds__(NT, 1)
     flags[0] = rank;
   }
   __syncthreads();
-  n = flags[0];
-  t0 = p.cu_seqlens[n];
-  t1 = p.cu_seqlens[n + 1];
+  const int n = flags[0];
+  const int t0 = p.cu_seqlens[n];
+  const int t1 = p.cu_seqlens[n + 1];
   if (t0 < 0 || t1 < t0 || (int64_t)t1 > p.total_tokens || p.cu_seqlens[0] != 0) {
     if (tid == 0) record_error(p.status, KDA_ERR_BAD_CU_SEQLENS, 1);
     return;
-  }
   }
   const int DV = D / P;
   const int dv_lo = vpart * DV, dv_hi = dv_lo + DV;
@@ -317,28 +186,20 @@ __global__ void __launch_bounds__(NT, 1)
 
   const size_t HD = (size_t)H * D;
   const size_t sbase = ((size_t)n * H + h) * D * D;
-  if constexpr (SPLIT) {
-    t0 = flags[5];
-    t1 = flags[6];
-    h = flags[7];
-    if (flags[4] < 0) t1 = t0;
-  }
-  int xcol = h * D;
+  const int xcol = h * D;
 
   if (tid == 0 && t1 > t0) {
     mbar_expect_tx(bar_qkg, 3 * 16384);
     tma_load_2d(sb + OFF_INQ, &tm_q, xcol, t0, bar_qkg);
     tma_load_2d(sb + OFF_INK, &tm_k, xcol, t0, bar_qkg);
     tma_load_2d(sb + OFF_ING, &tm_g, xcol, t0, bar_qkg);
-    if constexpr (!SPLIT) {
-      mbar_expect_tx(bar_v, 16384);
-      tma_load_2d(sb + OFF_INV, &tm_v, xcol, t0, bar_v);
-      tma_load_2d(sb + OFF_INV + 8192, &tm_v, xcol + 64, t0, bar_v);
-    }
+    mbar_expect_tx(bar_v, 16384);
+    tma_load_2d(sb + OFF_INV, &tm_v, xcol, t0, bar_v);
+    tma_load_2d(sb + OFF_INV + 8192, &tm_v, xcol + 64, t0, bar_v);
   }
 
   // ---- state in: S^T[dv][dk] -> TMEM (lane = dv); this warp covers 32 key columns
-  if constexpr (!SPLIT) {
+  {
     const int dv = my_lane;
     const bool mine = dv >= dv_lo && dv < dv_hi && p.initial_state != nullptr;
     const int dk0 = cs * 32;
@@ -358,15 +219,15 @@ __global__ void __launch_bounds__(NT, 1)
     tmem_wait_st();
   }
 
-  float gate_scale = expf(p.A_log[h]);
+  const float gate_scale = expf(p.A_log[h]);
   const float lb2 = p.lower_bound * kLog2e;
   const int cp = tid & 63;            // channel pair of the gate/operand phase
   const int grp = tid >> 6;           // 8-row group of the gate/operand phase
   const int d0 = 2 * cp;
   const int blk = grp >> 2;           // 32-token block of the group
   // sigmoid argument in log2 units: -gate_scale * log2e * (g + dt_bias)
-  float sg = -gate_scale * kLog2e;
-  float sg0 = sg * p.dt_bias[h * D + d0], sg1 = sg * p.dt_bias[h * D + d0 + 1];
+  const float sg = -gate_scale * kLog2e;
+  const float sg0 = sg * p.dt_bias[h * D + d0], sg1 = sg * p.dt_bias[h * D + d0 + 1];
   float* Nm = reinterpret_cast<float*>(sm + OFF_NM);
   float* Tm = reinterpret_cast<float*>(sm + OFF_TM);
   float* Y = reinterpret_cast<float*>(sm + OFF_Y);
@@ -378,20 +239,9 @@ __global__ void __launch_bounds__(NT, 1)
   float b_raw = 0.0f;
   if (tid < C && t0 + tid < t1) b_raw = __bfloat162float(p.beta[(size_t)(t0 + tid) * H + h]);
 
-  int c0 = t0;
-  int item = SPLIT ? flags[4] : 0;
-  while (c0 < t1) {
+  for (int c0 = t0; c0 < t1; c0 += C) {
     const int L = min(C, t1 - c0);
-    // the chunk after this one: the sequence's next chunk, or the next split item
-    int nc0 = c0 + C, nt1 = t1, nh = h, nitem = -1;
-    if constexpr (SPLIT) {
-      nitem = flags[8];
-      nc0 = flags[9];
-      nt1 = flags[10];
-      nh = flags[11];
-      if (nitem < 0) nt1 = nc0;
-    }
-    const bool more = nc0 < nt1;
+    const bool more = c0 + C < t1;
 
     // ---- P0: q, k, g of this chunk have landed (every thread waits for the TMA itself;
     //          a timeout is acted on at the next barrier); beta; zero q/k rows past the end
@@ -399,7 +249,7 @@ __global__ void __launch_bounds__(NT, 1)
     ph_qkg ^= 1;
     if (tid < C) {
       beta_s[tid] = (tid < L) ? sigm(b_raw) : 0.0f;
-      if (nc0 + tid < nt1) b_raw = __bfloat162float(p.beta[(size_t)(nc0 + tid) * H + nh]);
+      if (c0 + C + tid < t1) b_raw = __bfloat162float(p.beta[(size_t)(c0 + C + tid) * H + h]);
     }
     if (L < C) {
       for (int idx = tid; idx < (C - L) * 32; idx += NT) {
@@ -427,9 +277,6 @@ __global__ void __launch_bounds__(NT, 1)
         cl1[i] = run1;
       }
       *reinterpret_cast<float2*>(gt + grp * 128 + d0) = make_float2(run0, run1);
-    }
-    if constexpr (SPLIT) {
-      if (tid == 0) bulk_wait_read();   // the previous item's record left shared memory
     }
     if (__syncthreads_or(!tma_ok)) { failed = true; site = 10; break; }
 
@@ -494,13 +341,7 @@ __global__ void __launch_bounds__(NT, 1)
           ke1 = Ei1 * cB[1];
         }
         st_u32(sm, OFF_QG + kmajor_off(r, d0, 64), bmul2(q2, pack_bf16x2(g0, g1)));
-        if constexpr (SPLIT) {   // record tile: Ke K-major with dk rows, K = token
-          const uint32_t ke2 = bmul2(k2, pack_bf16x2(ke0, ke1));
-          *reinterpret_cast<uint16_t*>(sm + OFF_INV + kmajor_off(d0, r, 128)) = (uint16_t)(ke2 & 0xffffu);
-          *reinterpret_cast<uint16_t*>(sm + OFF_INV + kmajor_off(d0 + 1, r, 128)) = (uint16_t)(ke2 >> 16);
-        } else {
-          st_u32(sm, OFF_KE + mnmajor_off(d0, r, 8192), bmul2(k2, pack_bf16x2(ke0, ke1)));
-        }
+        st_u32(sm, OFF_KE + mnmajor_off(d0, r, 8192), bmul2(k2, pack_bf16x2(ke0, ke1)));
       }
       // reduce-scatter the 16 partial sums (8 rows x q, k) over the warp's 32 lanes
       float v[16];
@@ -540,9 +381,9 @@ __global__ void __launch_bounds__(NT, 1)
       mma_commit(bar_mma);
       if (more) {
         mbar_expect_tx(bar_qkg, 3 * 16384);
-        tma_load_2d(sb + OFF_INQ, &tm_q, nh * D, nc0, bar_qkg);
-        tma_load_2d(sb + OFF_INK, &tm_k, nh * D, nc0, bar_qkg);
-        tma_load_2d(sb + OFF_ING, &tm_g, nh * D, nc0, bar_qkg);
+        tma_load_2d(sb + OFF_INQ, &tm_q, xcol, c0 + C, bar_qkg);
+        tma_load_2d(sb + OFF_INK, &tm_k, xcol, c0 + C, bar_qkg);
+        tma_load_2d(sb + OFF_ING, &tm_g, xcol, c0 + C, bar_qkg);
       }
     }
     if (tid < 128) {   // row r = tid & 63 of q (tid < 64) or k
@@ -554,9 +395,9 @@ __global__ void __launch_bounds__(NT, 1)
     }
     {
       // one thread waits for the MMA (the others park on the barrier); all see the v tile land
-      const bool ok = (tid != 0 || mbar_wait(bar_mma, ph_mma)) && (SPLIT || mbar_wait(bar_v, ph_v));
+      const bool ok = (tid != 0 || mbar_wait(bar_mma, ph_mma)) && mbar_wait(bar_v, ph_v);
       ph_mma ^= 1;
-      if constexpr (!SPLIT) ph_v ^= 1;
+      ph_v ^= 1;
       tc_fence_before();
       if (__syncthreads_or(!ok)) { failed = true; site = 30; break; }
     }
@@ -601,7 +442,7 @@ __global__ void __launch_bounds__(NT, 1)
       }
     } else {
       const int t8 = tid - 256;
-      if (!SPLIT && L < C) {   // v rows past the sequence end -> 0 (both 64-column boxes)
+      if (L < C) {   // v rows past the sequence end -> 0 (both 64-column boxes)
         for (int idx = t8; idx < (C - L) * 16; idx += 256) {
           const int r = L + idx / 16, cc = idx % 16;
           st_u128(sm, OFF_INV + (cc >> 3) * 8192 + r * 128 + (cc & 7) * 16, make_uint4(0, 0, 0, 0));
@@ -660,12 +501,6 @@ __global__ void __launch_bounds__(NT, 1)
       named_barrier_sync(1, 128);               // T[32:64, 0:32] = -T[32:64, 32:64] Y2
       warp_gemm_16x16<32>(Tm + (32 + 16 * mi) * NS + 32, Y + 16 * ni,
                           Tm + (32 + 16 * mi) * NS + 16 * ni, -1.0f, lane);
-    } else if (SPLIT) {
-      // the item after the next one (its search hides behind the T inverse)
-      if (tid == 128) {
-        flags[12] = -1;
-        if (nitem >= 0) find_item(p, nitem + (int)gridDim.x, total_items, flags + 12);
-      }
     } else if (warp >= 4 && warp < 8) {
 #pragma unroll 1
       for (int cb = 0; cb < 4; ++cb) {   // state pass: 32 key columns at a time
@@ -731,12 +566,10 @@ __global__ void __launch_bounds__(NT, 1)
         for (int ks = 0; ks < 2; ++ks)
           mma_bf16(tmem + TM_D + 64 * b, mndesc(sb + OFF_RKQ + 4096 * b, 16384, ks),
                    kdesc(sb + OFF_TB, 64, 2 * b + ks), ID_MK64, ks > 0);
-      if constexpr (!SPLIT) {
 #pragma unroll
-        for (int ks = 0; ks < 4; ++ks)
-          mma_bf16(tmem + TM_U, mndesc(sb + OFF_INV, 8192, ks), kdesc(sb + OFF_TBU, 64, ks),
-                   ID_MK64, ks > 0);
-      }
+      for (int ks = 0; ks < 4; ++ks)
+        mma_bf16(tmem + TM_U, mndesc(sb + OFF_INV, 8192, ks), kdesc(sb + OFF_TBU, 64, ks),
+                 ID_MK64, ks > 0);
       mma_commit(bar_mma);
     }
     {
@@ -745,7 +578,7 @@ __global__ void __launch_bounds__(NT, 1)
       if (__syncthreads_or(!ok)) { failed = true; site = 50; break; }
     }
     tc_fence_after();
-    if (!SPLIT && tid == 0 && more) {   // v tile is free again
+    if (tid == 0 && more) {   // v tile is free again
       mbar_expect_tx(bar_v, 16384);
       tma_load_2d(sb + OFF_INV, &tm_v, xcol, c0 + C, bar_v);
       tma_load_2d(sb + OFF_INV + 8192, &tm_v, xcol + 64, c0 + C, bar_v);
@@ -770,59 +603,13 @@ __global__ void __launch_bounds__(NT, 1)
               f0 * __uint_as_float(w0[j + 1]) + f1b * (f1a * __uint_as_float(w1[j + 1]));
           w[e] = pack_bf16x2(-x0, -x1);
         }
-        if constexpr (SPLIT) {   // record tile: -W K-major with token rows, K = dk
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int tok = cs * 16 + c8 * 8 + e * 2;
-            *reinterpret_cast<uint16_t*>(sm + OFF_WN + kmajor_off(tok, dk, 64)) = (uint16_t)(w[e] & 0xffffu);
-            *reinterpret_cast<uint16_t*>(sm + OFF_WN + kmajor_off(tok + 1, dk, 64)) = (uint16_t)(w[e] >> 16);
-          }
-        } else {
-          st_u128(sm, OFF_WN + mnmajor_off(cs * 16 + c8 * 8, dk, 8192),
-                  make_uint4(w[0], w[1], w[2], w[3]));
-        }
+        st_u128(sm, OFF_WN + mnmajor_off(cs * 16 + c8 * 8, dk, 8192),
+                make_uint4(w[0], w[1], w[2], w[3]));
       }
     }
     fence_proxy_async();
     tc_fence_before();
     __syncthreads();
-
-    if constexpr (SPLIT) {
-      // ---- record of this (chunk, head) -> workspace; move on to the next item
-      if (tid == 0) {
-        unsigned char* rec = reinterpret_cast<unsigned char*>(p.status) + kSplitHeader +
-                             (size_t)item * kRecBytes;
-        // [-W; Qg]: per 64-column block of K, the 64 rows of -W then the 64 rows of Qg
-        bulk_store(rec + kRecWQ, sb + OFF_WN, 8192);
-        bulk_store(rec + kRecWQ + 8192, sb + OFF_QG, 8192);
-        bulk_store(rec + kRecWQ + 16384, sb + OFF_WN + 8192, 8192);
-        bulk_store(rec + kRecWQ + 24576, sb + OFF_QG + 8192, 8192);
-        bulk_store(rec + kRecQKE, sb + OFF_QKB, 8192);          // [QK; Ke]
-        bulk_store(rec + kRecQKE + 8192, sb + OFF_INV, 16384);
-        bulk_store(rec + kRecTB, sb + OFF_TBU, 8192);
-        bulk_store(rec + kRecVec, sb + OFF_DECAY, 512);
-        bulk_store(rec + kRecVec + 512, sb + OFF_INVN, 512);
-        bulk_commit();
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          flags[4 + i] = flags[8 + i];
-          flags[8 + i] = flags[12 + i];
-        }
-      }
-      __syncthreads();
-      item = nitem;
-      c0 = nc0;
-      t1 = nt1;
-      if (nh != h) {
-        h = nh;
-        gate_scale = expf(p.A_log[h]);
-        sg = -gate_scale * kLog2e;
-        sg0 = sg * p.dt_bias[h * D + d0];
-        sg1 = sg * p.dt_bias[h * D + d0 + 1];
-      }
-      xcol = h * D;
-      continue;
-    }
 
     // ---- P7: U^T += S^T (-W)^T
     if (tid == 0) {
@@ -911,22 +698,16 @@ __global__ void __launch_bounds__(NT, 1)
       }
     }
     __syncthreads();
-    c0 += C;
   }
 
   if (failed) {
     if (tid == 0) record_error(p.status, KDA_ERR_DEVICE_TIMEOUT, site);
     // let copies still in flight finish (bounded) before the CTA exits
     mbar_wait(bar_qkg, ph_qkg);
+    mbar_wait(bar_v, ph_v);
     mbar_wait(bar_mma, ph_mma);
-    if constexpr (!SPLIT) {
-      mbar_wait(bar_v, ph_v);
-      mbar_wait(bar_o, ph_o);
-    }
-  }
-  if constexpr (SPLIT) {
-    if (tid == 0) bulk_wait_all();
-  } else if (!failed) {
+    mbar_wait(bar_o, ph_o);
+  } else {
     // ---- state out (slice columns only)
     const int dv = my_lane;
     const int dk0 = cs * 32;
@@ -986,46 +767,21 @@ bool make_map(EncodeTiledFn enc, CUtensorMap* m, const void* base, int64_t T, in
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <bool SPLIT>
-cudaError_t set_smem_attr() {
+}  // namespace
+
+void* tensor_map_encoder() { return reinterpret_cast<void*>(encode_fn()); }
+
+cudaError_t launch_tc(const Params& p, cudaStream_t stream) {
   static bool attr_set[64] = {};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev >= 0 && dev < 64 && !attr_set[dev]) {
-    e = cudaFuncSetAttribute(kda_tc_chunk_kernel<SPLIT>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    e = cudaFuncSetAttribute(kda_tc_chunk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             SMEM_BYTES);
     if (e != cudaSuccess) return e;
     attr_set[dev] = true;
   }
-  return cudaSuccess;
-}
-
-}  // namespace
-
-void* tensor_map_encoder() { return reinterpret_cast<void*>(encode_fn()); }
-
-cudaError_t launch_kside(const Params& p, cudaStream_t stream) {
-  cudaError_t e = set_smem_attr<true>();
-  if (e != cudaSuccess) return e;
-  const int64_t items = split_slots(p.total_tokens, p.num_seqs) * p.heads;
-  if (items <= 0 || p.total_tokens == 0) return cudaSuccess;
-  if (items > 0x7fffffffLL - 4096) return cudaErrorInvalidValue;
-  EncodeTiledFn enc = encode_fn();
-  if (!enc) return cudaErrorNotSupported;
-  CUtensorMap mq, mk, mg;
-  if (!make_map(enc, &mq, p.q, p.total_tokens, p.heads, D, false) ||
-      !make_map(enc, &mk, p.k, p.total_tokens, p.heads, D, false) ||
-      !make_map(enc, &mg, p.g, p.total_tokens, p.heads, D, false))
-    return cudaErrorInvalidValue;
-  const int64_t grid = items < p.sm_count ? items : p.sm_count;
-  kda_tc_chunk_kernel<true><<<(unsigned)grid, NT, SMEM_BYTES, stream>>>(p, mq, mk, mg, mq);
-  return cudaGetLastError();
-}
-
-cudaError_t launch_tc(const Params& p, cudaStream_t stream) {
-  cudaError_t e = set_smem_attr<false>();
-  if (e != cudaSuccess) return e;
   const long long blocks = (long long)p.num_seqs * p.heads * p.vsplit;
   if (blocks <= 0) return cudaSuccess;
   if (blocks > 0x7fffffffLL) return cudaErrorInvalidValue;
@@ -1043,7 +799,7 @@ cudaError_t launch_tc(const Params& p, cudaStream_t stream) {
       !make_map(enc, &mg, gb, p.total_tokens, p.heads, D, false) ||
       !make_map(enc, &mv, vb, p.total_tokens, p.heads, 64, true))
     return cudaErrorInvalidValue;
-  kda_tc_chunk_kernel<false><<<(unsigned)blocks, NT, SMEM_BYTES, stream>>>(p, mq, mk, mg, mv);
+  kda_tc_chunk_kernel<<<(unsigned)blocks, NT, SMEM_BYTES, stream>>>(p, mq, mk, mg, mv);
   return cudaGetLastError();
 }
 
