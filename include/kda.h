@@ -88,10 +88,11 @@ typedef struct CUstream_st* kda_stream_t;
 #define KDA_KERNEL_TC 1    /* fused tcgen05 + TMA chunk kernel, C = 64: one CTA
                               per (sequence, head[, value slice])            */
 #define KDA_KERNEL_REF 2   /* plain-CUDA-core chunk kernel (GPU parity aid)    */
-#define KDA_KERNEL_SPLIT 3 /* value-split path of PR #52458: a chunk-parallel
+#define KDA_KERNEL_SPLIT 3 /* the K1/K2 structure of PR #52458: a chunk-parallel
                               k-side kernel writes per-(chunk, head) records to
                               the workspace, then one chain CTA per (sequence,
-                              head, value slice of 128 / P columns), P >= 2  */
+                              head, value slice of 128 / P columns); P = 1 runs
+                              the chain on tcgen05 with the state in TMEM   */
 
 /*
  * Bytes of device workspace a call needs for up to `total_tokens` tokens,
@@ -137,10 +138,10 @@ int kda_chunk_prefill_fwd(const void* q, const void* k, const void* v, const voi
 /*
  * As kda_chunk_prefill_fwd, with two overrides for tests and sweeps:
  * `vsplit` -1 = automatic, or a forced split factor in {1, 2, 4, 8};
- * `kernel` one of KDA_KERNEL_*.  Other values give KDA_ERR_INVALID_ARG, as
- * does KDA_KERNEL_SPLIT with vsplit 1 (with -1 it uses at least 2).
- * KDA_KERNEL_SPLIT needs the full kda_workspace_size() of this call (its
- * records), else KDA_ERR_WORKSPACE_TOO_SMALL.
+ * `kernel` one of KDA_KERNEL_*.  Other values give KDA_ERR_INVALID_ARG.
+ * KDA_KERNEL_SPLIT needs room for its records: 1024 + 66,560 bytes per
+ * (chunk slot, head) with ceil(total_tokens / 64) + num_seqs slots, else
+ * KDA_ERR_WORKSPACE_TOO_SMALL.
  */
 int kda_chunk_prefill_fwd_ex(const void* q, const void* k, const void* v, const void* g,
                              const void* beta, const float* A_log, const float* dt_bias,
