@@ -53,13 +53,14 @@ constexpr int K_PART = K_MISC + 6400;     // norm partial sums [8 warps][32]
 constexpr int K_BAR = K_MISC + 7424;      // 2 mbarriers
 constexpr int K_TSLOT = K_MISC + 7440;
 constexpr int K_FLAGS = K_MISC + 7456;    // items {item, c0, t1, head, k} x 3, 8 ints apart
+constexpr int K_SGD = K_MISC + 7552;      // gate terms -e^{A_log} log2e dt_bias [128], -e^{A_log} log2e
 constexpr int K_CU = K_MISC + 8192;       // cu_seqlens cache (batches of up to kCuCache sequences)
 constexpr int kCuCache = 1023;
 constexpr int K_SMEM_USED = K_CU + 4 * (kCuCache + 1);
 constexpr int K_SMEM_BYTES = K_SMEM_USED + 1024;
 static_assert(K_Y + 32 * NS * 4 <= K_RKQ, "T scratch overlaps [Kr; Qr]");
 static_assert(K_NM + 64 * NS * 4 <= K_TB, "N overlaps T diag(b)");
-static_assert(K_FLAGS + 24 * 4 <= K_CU, "misc");
+static_assert(K_FLAGS + 24 * 4 <= K_SGD && K_SGD + 129 * 4 <= K_CU, "misc");
 static_assert(2 * (K_SMEM_BYTES + 1024) <= 228 * 1024, "two CTAs per SM");
 
 constexpr uint32_t TM_D = 0;      // A | QK (96 cols), then W0^T at 0, W1^T at 64
@@ -175,6 +176,32 @@ __global__ void __launch_bounds__(NT, 2)
   bool failed = false;
   int site = 0;
 
+  // head parameters and beta of an item -> shared memory, one item ahead (the sigmoid
+  // argument of the gate in log2 units is sgd[128] * g + sgd[channel])
+  float* sgd = reinterpret_cast<float*>(sm + K_SGD);
+  auto load_params = [&](int c0n, int t1n, int hn) {
+    if (tid < 128) {
+      const float sgn = -expf(p.A_log[hn]) * kLog2e;
+      sgd[tid] = sgn * p.dt_bias[hn * D + tid];
+      if (tid == 0) sgd[128] = sgn;
+    } else if (tid < 128 + C) {
+      const int j = tid - 128;
+      const float b = (c0n + j < t1n) ? __bfloat162float(p.beta[(size_t)(c0n + j) * H + hn]) : 0.0f;
+      beta_s[j] = (c0n + j < t1n) ? sigm(b) : 0.0f;
+    }
+  };
+  auto load_inputs = [&](int c0n, int hn) {   // thread 0: q, k, g tiles of an item
+    mbar_expect_tx(bar_in, 3 * 16384);
+    tma_load_2d(sb + K_INQ, &tm_q, hn * D, c0n, bar_in);
+    tma_load_2d(sb + K_INK, &tm_k, hn * D, c0n, bar_in);
+    tma_load_2d(sb + K_ING, &tm_g, hn * D, c0n, bar_in);
+  };
+  if (flags[0] >= 0) {
+    if (tid == 0) load_inputs(flags[1], flags[3]);
+    load_params(flags[1], flags[2], flags[3]);
+  }
+  __syncthreads();
+
 #pragma unroll 1
   while (true) {
     const int item = flags[0];
@@ -183,25 +210,14 @@ __global__ void __launch_bounds__(NT, 2)
     const int L = min(C, t1 - c0);
     unsigned char* rec = ws + (size_t)item * kRecBytes;
 
-    // ---- P0: inputs of this item (the next item's go to L2 meanwhile)
-    if (tid == 0) {
-      mbar_expect_tx(bar_in, 3 * 16384);
-      tma_load_2d(sb + K_INQ, &tm_q, h * D, c0, bar_in);
-      tma_load_2d(sb + K_INK, &tm_k, h * D, c0, bar_in);
-      tma_load_2d(sb + K_ING, &tm_g, h * D, c0, bar_in);
-      if (flags[8] >= 0) {
-        tma_prefetch_2d(&tm_q, flags[11] * D, flags[9]);
-        tma_prefetch_2d(&tm_k, flags[11] * D, flags[9]);
-        tma_prefetch_2d(&tm_g, flags[11] * D, flags[9]);
-      }
+    // ---- P0: inputs of this item (issued during the previous item); the next item's go
+    //          to L2 meanwhile
+    if (tid == 0 && flags[8] >= 0) {
+      tma_prefetch_2d(&tm_q, flags[11] * D, flags[9]);
+      tma_prefetch_2d(&tm_k, flags[11] * D, flags[9]);
+      tma_prefetch_2d(&tm_g, flags[11] * D, flags[9]);
     }
-    const float gate_scale = expf(p.A_log[h]);
-    const float sg = -gate_scale * kLog2e;   // sigmoid argument in log2 units
-    const float sg0 = sg * p.dt_bias[h * D + d0], sg1 = sg * p.dt_bias[h * D + d0 + 1];
-    if (tid < C) {
-      const float b_raw = (tid < L) ? __bfloat162float(p.beta[(size_t)(c0 + tid) * H + h]) : 0.0f;
-      beta_s[tid] = (tid < L) ? sigm(b_raw) : 0.0f;
-    }
+    const float sg = sgd[128], sg0 = sgd[d0], sg1 = sgd[d0 + 1];
     const bool tma_ok = mbar_wait(bar_in, ph_in);
     ph_in ^= 1;
     if (L < C) {   // q, k rows past the sequence end -> 0
@@ -212,7 +228,8 @@ __global__ void __launch_bounds__(NT, 2)
     }
     if (__syncthreads_or(!tma_ok)) { failed = true; site = 60; break; }
 
-    // ---- P2a: gate -> log2 decay, cumsum inside each 8-row group of this thread
+    // ---- P2a: gate -> log2 decay, cumsum inside each 8-row group of this thread; the
+    //           partial sums of squares of q and k
     float cl0[16], cl1[16];
 #pragma unroll
     for (int gh = 0; gh < 2; ++gh) {
@@ -231,43 +248,71 @@ __global__ void __launch_bounds__(NT, 2)
         cl1[8 * gh + i] = run1;
       }
       *reinterpret_cast<float2*>(gt + (2 * rq + gh) * 128 + d0) = make_float2(run0, run1);
+      // sums of squares of the group's q and k rows over this warp's 64 channels,
+      // reduce-scattered: lanes 2j, 2j + 1 end with the sum of v[j] ([0, 8) q, [8, 16) k)
+      float v[16];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int r = 16 * rq + 8 * gh + i;
+        const float2 qf = unpack_bf16x2(ld_u32(sm + K_INQ, (uint32_t)(r * 256 + d0 * 2)));
+        const float2 kf = unpack_bf16x2(ld_u32(sm + K_INK, (uint32_t)(r * 256 + d0 * 2)));
+        v[i] = fmaf(qf.x, qf.x, qf.y * qf.y);
+        v[8 + i] = fmaf(kf.x, kf.x, kf.y * kf.y);
+      }
+#pragma unroll
+      for (int o = 16, m = 8; o >= 2; o >>= 1, m >>= 1) {
+        const bool up = (lane & o) != 0;
+#pragma unroll
+        for (int i = 0; i < m; ++i) {
+          const float send = up ? v[i] : v[i + m];
+          const float keep = up ? v[i + m] : v[i];
+          v[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+        }
+      }
+      v[0] += __shfl_xor_sync(0xffffffffu, v[0], 1);
+      if ((lane & 1) == 0) part[warp * 32 + gh * 16 + (lane >> 1)] = v[0];
     }
     __syncthreads();
 
     // ---- P2b: anchored factors; [Kr; Qr], [Kc; Kc2] operand tiles (raw q, k); Qg and Ke
-    //           record tiles straight to global; partial sums of squares
+    //           record tiles straight to global
     {
-      float cA[2], cB[2], cX[2], cR[2], mE[2][2];
+      // per-channel factors, applied per element in fp32 and rounded once (a factor rounded
+      // to bf16 per chunk would give every token the same error in that channel).  The
+      // products keep the order E cA, Ei cB first: those are near 1, while cA cR or cB cX
+      // alone can fall below the fp32 normal range.
+      float mE[2][2], cA[2], cB[2], cX[2], cR[2];
+      {
 #pragma unroll
-      for (int c = 0; c < 2; ++c) {
-        float G[8];
+        for (int c = 0; c < 2; ++c) {
+          float G[8];
 #pragma unroll
-        for (int j = 0; j < 8; ++j) G[j] = gt[j * 128 + d0 + c];
-        const float B0 = (G[0] + G[1]) + (G[2] + G[3]);
-        const float B1 = (G[4] + G[5]) + (G[6] + G[7]);
-        const float al0 = G[0] + G[1], al1 = G[4] + G[5];
-        const float al = blk ? al1 : al0;
+          for (int j = 0; j < 8; ++j) G[j] = gt[j * 128 + d0 + c];
+          const float B0 = (G[0] + G[1]) + (G[2] + G[3]);
+          const float B1 = (G[4] + G[5]) + (G[6] + G[7]);
+          const float al0 = G[0] + G[1], al1 = G[4] + G[5];
+          const float al = blk ? al1 : al0;
 #pragma unroll
-        for (int gh = 0; gh < 2; ++gh) {
-          const int grp = 2 * rq + gh;
-          float pre = 0.0f;                      // totals of earlier groups of the block
+          for (int gh = 0; gh < 2; ++gh) {
+            const int grp = 2 * rq + gh;
+            float pre = 0.0f;                      // totals of earlier groups of the block
 #pragma unroll
-          for (int j = 0; j < 8; ++j)
-            if ((j >> 2) == blk && j < grp) pre += G[j];
-          mE[gh][c] = al - pre;                  // exponent of E = cl - mE
-        }
-        cA[c] = ex2f(al);                        // E -> 2^c (within the block)
-        cB[c] = ex2f((blk ? B1 : B0) - al);      // Ei -> 2^(B_blk - c)
-        cX[c] = ex2f(al1);                       // alpha_1, folded into Kc2
-        cR[c] = ex2f(blk ? B0 : B1);             // the other block's total
-        if (rq == 0) {
-          reinterpret_cast<float*>(rec + kRecVec)[d0 + c] = ex2f(B0 + B1);   // 2^Gam_last
-          wf[d0 + c] = cA[c];                    // W block 0: 2^alpha0
-          wf[128 + d0 + c] = cX[c];              // W block 1: 2^alpha1, then
-          wf[256 + d0 + c] = ex2f(B0);           //            2^B0
+            for (int j = 0; j < 8; ++j)
+              if ((j >> 2) == blk && j < grp) pre += G[j];
+            mE[gh][c] = al - pre;                  // exponent of E = cl - mE
+          }
+          cA[c] = ex2f(al);                        // E -> 2^c (within the block)
+          cB[c] = ex2f((blk ? B1 : B0) - al);      // Ei -> 2^(B_blk - c)
+          cX[c] = ex2f(al1);                       // alpha_1, folded into Kc2
+          cR[c] = ex2f(blk ? B0 : B1);             // the other block's total
+          if (rq == 0) {
+            reinterpret_cast<float*>(rec + kRecVec)[d0 + c] = ex2f(B0 + B1);   // 2^Gam_last
+            wf[d0 + c] = cA[c];                    // W block 0: 2^alpha0
+            wf[128 + d0 + c] = cX[c];              // W block 1: 2^alpha1, then
+            wf[256 + d0 + c] = ex2f(B0);           //            2^B0
+          }
         }
       }
-      float v[32];                               // sums of squares: [0, 16) q rows, [16, 32) k
 #pragma unroll
       for (int gh = 0; gh < 2; ++gh) {
         uint32_t qg[8], ke[8];
@@ -277,12 +322,8 @@ __global__ void __launch_bounds__(NT, 2)
           const int r = 16 * rq + ii;
           const uint32_t q2 = ld_u32(sm + K_INQ, (uint32_t)(r * 256 + d0 * 2));
           const uint32_t k2 = ld_u32(sm + K_INK, (uint32_t)(r * 256 + d0 * 2));
-          const float2 qf = unpack_bf16x2(q2), kf = unpack_bf16x2(k2);
-          v[ii] = fmaf(qf.x, qf.x, qf.y * qf.y);
-          v[16 + ii] = fmaf(kf.x, kf.x, kf.y * kf.y);
           const float e0 = cl0[ii] - mE[gh][0], e1 = cl1[ii] - mE[gh][1];
-          const float E0 = ex2f(e0), E1 = ex2f(e1);
-          const float Ei0 = ex2f(-e0), Ei1 = ex2f(-e1);
+          const float E0 = ex2f(e0), E1 = ex2f(e1), Ei0 = ex2f(-e0), Ei1 = ex2f(-e1);
           const uint32_t E2 = pack_bf16x2(E0, E1), Ei2 = pack_bf16x2(Ei0, Ei1);
           st_u32(sm, K_RKQ + kmajor_off(r, d0, 128), bmul2(k2, E2));
           st_u32(sm, K_RKQ + kmajor_off(64 + r, d0, 128), bmul2(q2, E2));
@@ -327,18 +368,6 @@ __global__ void __launch_bounds__(NT, 2)
           *reinterpret_cast<uint4*>(rec + kRecQKE + kmajor_off(64 + d0 + c, r0, 192)) = wk;
         }
       }
-      // reduce-scatter the 32 partial sums over the warp: lane l ends with the sum of v[l]
-#pragma unroll
-      for (int o = 16; o >= 1; o >>= 1) {
-        const bool up = (lane & o) != 0;
-#pragma unroll
-        for (int i = 0; i < o; ++i) {
-          const float send = up ? v[i] : v[i + o];
-          const float keep = up ? v[i + o] : v[i];
-          v[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
-        }
-      }
-      part[warp * 32 + lane] = v[0];
     }
     fence_proxy_async();
     __syncthreads();
@@ -353,8 +382,9 @@ __global__ void __launch_bounds__(NT, 2)
     }
     if (tid < 128) {   // row r = tid & 63 of q (tid < 64) or k; warps 2 rq, 2 rq + 1 hold its halves
       const int r = tid & 63, t = tid >> 6;
-      const int q16 = r >> 4, i = r & 15;
-      const float ss = part[(2 * q16) * 32 + 16 * t + i] + part[(2 * q16 + 1) * 32 + 16 * t + i];
+      const int q16 = r >> 4, gh = (r >> 3) & 1, i = r & 7;
+      const int pi = gh * 16 + t * 8 + i;
+      const float ss = part[(2 * q16) * 32 + pi] + part[(2 * q16 + 1) * 32 + pi];
       const float inv = (r < L) ? rsqrtf(ss + kL2Eps) : 0.0f;
       const float val = (t == 0) ? p.scale * inv : inv;
       inv_q[t * 64 + r] = val;
@@ -507,6 +537,12 @@ __global__ void __launch_bounds__(NT, 2)
       ph_mma ^= 1;
     }
     tc_fence_after();
+    // the input tiles, beta and the gate terms of this item are no longer read: fetch and
+    // load the next item's
+    if (flags[8] >= 0) {
+      if (tid == 0) load_inputs(flags[9], flags[11]);
+      load_params(flags[9], flags[10], flags[11]);
+    }
 
     // ---- P6: -W = -(2^a0 W0 + 2^B0 (2^a1 W1)) -> bf16, MN-major tokens 0-63 of [-W | Qg]
     {
