@@ -36,11 +36,12 @@ constexpr int OFF_STAGE0 = 0;
 constexpr int OFF_STAGE1 = STAGE_BYTES;
 constexpr int OFF_OST = 2 * STAGE_BYTES;            // O staging [64 tok][128 dv] bf16
 constexpr int OFF_MISC3 = OFF_OST + 16384;
-constexpr int OFF_BAR3 = OFF_MISC3;                 // full[2], mma
+constexpr int OFF_BAR3 = OFF_MISC3;                 // full[2], mma, u
 constexpr int OFF_TSLOT3 = OFF_MISC3 + 32;
 constexpr int OFF_FLAGS3 = OFF_MISC3 + 48;
 constexpr int OFF_LENS3 = OFF_MISC3 + 64;           // sequence lengths for the ordering
-constexpr int SMEM3_USED = OFF_LENS3 + 4 * kMaxRankSeqs3;
+constexpr int OFF_IQ3 = OFF_LENS3 + 4 * kMaxRankSeqs3;   // scale/|q| of the last two chunks [2][64]
+constexpr int SMEM3_USED = OFF_IQ3 + 2 * 64 * 4;
 constexpr int SMEM3_BYTES = SMEM3_USED + 1024;
 static_assert(STAGE_V % 1024 == 0 && STAGE_BYTES % 1024 == 0, "stage alignment");
 static_assert(SMEM3_BYTES <= 227 * 1024, "shared memory");
@@ -53,7 +54,9 @@ constexpr uint32_t T_SB = 256;   // S^T bf16, 64 cols (2 dk per col)
 constexpr uint32_t T_UB = 320;   // U_b^T bf16, 32 cols (2 tokens per col)
 constexpr uint32_t T_COLS = 512;
 
-constexpr uint32_t ID_G1 = idesc_bf16(128, 128, 0, 1);   // [U|O]  += SB  x [-W | Qg]^T
+constexpr uint32_t ID_G1 = idesc_bf16(128, 128, 0, 1);   // [U|O]  = SB  x [-W | Qg]^T
+// (tcgen05 MMAs of M = 128 cost about the same per instruction for N = 64 and 128, so the
+// two products that share the A operand S^T run as one N = 128 group)
 constexpr uint32_t ID_G2 = idesc_bf16(128, 192, 0, 0);   // [O|S]  += UB  x [QK; Ke]^T
 constexpr uint32_t ID_UP = idesc_bf16(128, 64, 1, 0);    // U      += V^T x (T diag b)^T
 
@@ -78,6 +81,7 @@ __global__ void __launch_bounds__(NT3, 1)
   int* flags = reinterpret_cast<int*>(sm + OFF_FLAGS3);
   uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + OFF_TSLOT3);
   const uint32_t bar_full0 = sb + OFF_BAR3, bar_full1 = bar_full0 + 8, bar_mma = bar_full0 + 16;
+  const uint32_t bar_u = bar_full0 + 24;
 
   // ---- work unit: (rank, head), longest sequence first
   const int H = p.heads, N = p.num_seqs;
@@ -116,6 +120,7 @@ __global__ void __launch_bounds__(NT3, 1)
     mbar_init(bar_full0, 1);
     mbar_init(bar_full1, 1);
     mbar_init(bar_mma, 1);
+    mbar_init(bar_u, 1);
     mbar_fence_init();
     tma_prefetch_desc(&maps.v);
   }
@@ -158,26 +163,25 @@ __global__ void __launch_bounds__(NT3, 1)
     if (nch > 2) prefetch_l2(2);
   }
 
-  // ---- state in: S^T[dv][dk] -> TMEM (lane = dv); this warp covers 64 key columns
+  // ---- state in: S^T[dv][dk] -> TMEM (lane = dv); this warp covers 64 key columns, all
+  //      64 loads in flight at once
   {
     const int dv = my_lane;
-#pragma unroll 1
-    for (int cb = 0; cb < 2; ++cb) {
-      const int dk0 = half * 64 + cb * 32;
-      uint32_t r[32];
+    const int dk0 = half * 64;
+    uint32_t r[64];
 #pragma unroll
-      for (int j = 0; j < 32; ++j) {
-        float s = 0.0f;
-        if (p.initial_state) {
-          const size_t idx = sbase + (size_t)(dk0 + j) * D3 + dv;
-          s = p.state_bf16
-                  ? __bfloat162float(static_cast<const __nv_bfloat16*>(p.initial_state)[idx])
-                  : static_cast<const float*>(p.initial_state)[idx];
-        }
-        r[j] = __float_as_uint(s);
+    for (int j = 0; j < 64; ++j) {
+      float s = 0.0f;
+      if (p.initial_state) {
+        const size_t idx = sbase + (size_t)(dk0 + j) * D3 + dv;
+        s = p.state_bf16
+                ? __bfloat162float(static_cast<const __nv_bfloat16*>(p.initial_state)[idx])
+                : static_cast<const float*>(p.initial_state)[idx];
       }
-      tmem_st32(tmem + lane_base + T_S + dk0, r);
+      r[j] = __float_as_uint(s);
     }
+    tmem_st32(tmem + lane_base + T_S + dk0, *reinterpret_cast<uint32_t(*)[32]>(r));
+    tmem_st32(tmem + lane_base + T_S + dk0 + 32, *reinterpret_cast<uint32_t(*)[32]>(r + 32));
     tmem_wait_st();
   }
 
@@ -189,12 +193,13 @@ __global__ void __launch_bounds__(NT3, 1)
   bool mma_out = false;              // an MMA commit not yet waited for (thread 0)
   int L_prev = 0;
 
-  // O of the previous chunk: TMEM -> bf16 staging [token][dv] (warps 0-3: tokens 0-63)
+  // O of the previous chunk: TMEM -> bf16 staging [token][dv]; this warp: tokens
+  // 32 half .. 32 half + 31 of its value channels
   auto drain_o = [&](const float* iq) {
     const int dv = my_lane;
     __nv_bfloat16* ost = reinterpret_cast<__nv_bfloat16*>(sm + OFF_OST);
-#pragma unroll 1
-    for (int cb = 0; cb < 2; ++cb) {
+    {
+      const int cb = half;
       uint32_t r[32];
       tmem_ld32(tmem + lane_base + T_O + cb * 32, r);
       tmem_wait_ld();
@@ -230,8 +235,7 @@ __global__ void __launch_bounds__(NT3, 1)
     const uint32_t st = sb + (buf ? OFF_STAGE1 : OFF_STAGE0);
     unsigned char* stp = sm + (buf ? OFF_STAGE1 : OFF_STAGE0);
     const float* vec = reinterpret_cast<const float*>(stp + kRecVec);   // decay, iq, ik
-    const float* vec_prev =
-        reinterpret_cast<const float*>(sm + (buf ? OFF_STAGE0 : OFF_STAGE1) + kRecVec);
+    float* iqs = reinterpret_cast<float*>(sm + OFF_IQ3);   // [2][64], by chunk parity
 
     // ---- 1. the record of this chunk has landed
     {
@@ -240,6 +244,8 @@ __global__ void __launch_bounds__(NT3, 1)
       phase ^= 1u << buf;
       pending &= ~(1 << buf);
     }
+    // scale/|q| of this chunk, kept past the stage's reuse (O is drained during the next chunk)
+    if (tid < kChunk) iqs[buf * 64 + tid] = vec[128 + tid];
     if (L < kChunk) {   // v rows past the sequence end -> 0 (both 64-column boxes)
       for (int idx = tid; idx < (kChunk - L) * 16; idx += NT3) {
         const int r = L + idx / 16, cc = idx % 16;
@@ -249,31 +255,29 @@ __global__ void __launch_bounds__(NT3, 1)
       fence_proxy_async();
     }
 
-    // ---- 2. warps 4-7: S^T -> bf16 copy, then S^T *= 2^Gam_last; warps 0-3: drain O(i-1)
-    if (half == 1) {
+    // ---- 2. S^T -> bf16 copy, then S^T *= 2^Gam_last (this warp: 64 key columns); O(i-1)
 #pragma unroll 1
-      for (int cb = 0; cb < 4; ++cb) {
-        uint32_t x[32], pk[16];
-        tmem_ld32(tmem + lane_base + T_S + cb * 32, x);
-        tmem_wait_ld();
+    for (int cb = 0; cb < 2; ++cb) {
+      const int col = half * 64 + cb * 32;
+      uint32_t x[32], pk[16];
+      tmem_ld32(tmem + lane_base + T_S + col, x);
+      tmem_wait_ld();
 #pragma unroll
-        for (int j = 0; j < 16; ++j)
-          pk[j] = pack_bf16x2(__uint_as_float(x[2 * j]), __uint_as_float(x[2 * j + 1]));
-        tmem_st16(tmem + lane_base + T_SB + cb * 16, pk);
+      for (int j = 0; j < 16; ++j)
+        pk[j] = pack_bf16x2(__uint_as_float(x[2 * j]), __uint_as_float(x[2 * j + 1]));
+      tmem_st16(tmem + lane_base + T_SB + col / 2, pk);
 #pragma unroll
-        for (int j4 = 0; j4 < 8; ++j4) {
-          const float4 dl = ld4s(vec + cb * 32 + 4 * j4);
-          x[4 * j4] = __float_as_uint(__uint_as_float(x[4 * j4]) * dl.x);
-          x[4 * j4 + 1] = __float_as_uint(__uint_as_float(x[4 * j4 + 1]) * dl.y);
-          x[4 * j4 + 2] = __float_as_uint(__uint_as_float(x[4 * j4 + 2]) * dl.z);
-          x[4 * j4 + 3] = __float_as_uint(__uint_as_float(x[4 * j4 + 3]) * dl.w);
-        }
-        tmem_st32(tmem + lane_base + T_S + cb * 32, x);
+      for (int j4 = 0; j4 < 8; ++j4) {
+        const float4 dl = ld4s(vec + col + 4 * j4);
+        x[4 * j4] = __float_as_uint(__uint_as_float(x[4 * j4]) * dl.x);
+        x[4 * j4 + 1] = __float_as_uint(__uint_as_float(x[4 * j4 + 1]) * dl.y);
+        x[4 * j4 + 2] = __float_as_uint(__uint_as_float(x[4 * j4 + 2]) * dl.z);
+        x[4 * j4 + 3] = __float_as_uint(__uint_as_float(x[4 * j4 + 3]) * dl.w);
       }
-      tmem_wait_st();
-    } else if (i > 0) {
-      drain_o(vec_prev + 128);
+      tmem_st32(tmem + lane_base + T_S + col, x);
     }
+    tmem_wait_st();
+    if (i > 0) drain_o(iqs + (buf ^ 1) * 64);   // O(i-1) -> staging before it is overwritten
     tc_fence_before();
     __syncthreads();   // (A) SB ready, S decayed, O(i-1) staged; stage buf^1 free
 
@@ -286,7 +290,7 @@ __global__ void __launch_bounds__(NT3, 1)
 #pragma unroll
       for (int ks = 0; ks < 4; ++ks)
         mma_bf16(tmem + T_U, mndesc3(st + STAGE_V, 8192, ks), kdesc3(st + kRecTB, 64, ks), ID_UP, 1);
-      mma_commit(bar_mma);
+      mma_commit(bar_u);
       mma_out = true;
       if (i + 1 < nch) {
         issue(i + 1);
@@ -296,11 +300,9 @@ __global__ void __launch_bounds__(NT3, 1)
     }
     if (i > 0) store_o(c0 - kChunk, L_prev);
     {
-      const bool ok = tid != 0 || mbar_wait(bar_mma, ph_mma);
+      const bool ok = tid != 0 || mbar_wait(bar_u, ph_mma);
       tc_fence_before();
       if (__syncthreads_or(!ok)) { failed = true; site = 53; break; }   // (B)
-      ph_mma ^= 1;
-      mma_out = false;
     }
     tc_fence_after();
 
@@ -336,7 +338,7 @@ __global__ void __launch_bounds__(NT3, 1)
       const bool ok = tid != 0 || mbar_wait(bar_mma, ph_mma);
       tc_fence_before();
       if (__syncthreads_or(!ok)) { failed = true; site = 55; break; }   // (D)
-      ph_mma ^= 1;
+      ph_mma ^= 1;   // one fill per chunk of both bar_u and bar_mma
       mma_out = false;
     }
     tc_fence_after();
@@ -349,14 +351,15 @@ __global__ void __launch_bounds__(NT3, 1)
       // let fetches and MMAs still in flight finish (bounded) before the CTA exits
       if (pending & 1) mbar_wait(bar_full0, phase & 1u);
       if (pending & 2) mbar_wait(bar_full1, (phase >> 1) & 1u);
-      if (mma_out) mbar_wait(bar_mma, ph_mma);
+      if (mma_out) {   // the commit not waited for: bar_u at site 53, bar_mma at 55
+        if (site == 53) mbar_wait(bar_u, ph_mma);
+        else mbar_wait(bar_mma, ph_mma);
+      }
     }
   } else {
     if (nch > 0) {   // O of the last chunk
       const int last = nch - 1;
-      const float* vec_last =
-          reinterpret_cast<const float*>(sm + ((last & 1) ? OFF_STAGE1 : OFF_STAGE0) + kRecVec);
-      if (half == 0) drain_o(vec_last + 128);
+      drain_o(reinterpret_cast<const float*>(sm + OFF_IQ3) + (last & 1) * 64);
       __syncthreads();
       store_o(t0 + kChunk * last, L_prev);
     }

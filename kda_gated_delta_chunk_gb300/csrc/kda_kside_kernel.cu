@@ -206,7 +206,7 @@ __global__ void __launch_bounds__(NT, 2)
   while (true) {
     const int item = flags[0];
     if (item < 0) break;
-    const int c0 = flags[1], t1 = flags[2], h = flags[3];
+    const int c0 = flags[1], t1 = flags[2];
     const int L = min(C, t1 - c0);
     unsigned char* rec = ws + (size_t)item * kRecBytes;
 
