@@ -70,9 +70,9 @@ constexpr int OFF_WN = OFF_RA + 32768;      //  -W MN-major, N = 64 tok, K = 128
 constexpr int OFF_TB = OFF_RA + 76800;      //  T diag(b/|k|) K-major 64 x 64 (for W)
 constexpr int OFF_TBU = OFF_RA + 84992;     //  T diag(b)     K-major 64 x 64 (for U')
 constexpr int OFF_QG = OFF_RA + 93184;      // Qg K-major 64 rows x 128 (B of O^T = S^T Qg^T)
-constexpr int OFF_KE = OFF_QG + 16384;      // Ke MN-major mn = dk, k = tok (B of S^T += U^T Ke)
-constexpr int OFF_QKB = OFF_KE + 16384;     // QK K-major 64 x 64 (B of O^T += U^T QK^T)
-constexpr int OFF_MISC = OFF_QKB + 8192;
+constexpr int OFF_QKB = OFF_QG + 16384;     // [QK; Ke] K-major 192 rows x 64: QK (r, K = s), then
+constexpr int OFF_KE = OFF_QKB + 8192;      //   Ke (dk rows, K = token): B of [O^T | S^T] += U^T [QK; Ke]^T
+constexpr int OFF_MISC = OFF_KE + 16384;
 constexpr int OFF_INVN = OFF_MISC;          // scale / |q| [64], 1 / |k| [64]
 constexpr int OFF_BETA = OFF_MISC + 512;    // b [64]
 constexpr int OFF_DECAY = OFF_MISC + 768;   // 2^Gam_last [128]
@@ -90,10 +90,10 @@ static_assert(OFF_TBU + 8192 <= OFF_QG, "T tiles overlap Qg");
 static_assert(SMEM_BYTES <= 227 * 1024, "shared memory");
 
 // ---- TMEM columns (fp32 unless noted; lane = value channel, or key channel for D/W)
-constexpr uint32_t TM_S = 0;      // S^T        128 cols (col = dk)
-constexpr uint32_t TM_SB = 128;   // S^T bf16    64 cols (A operand, 2 dk per col)
-constexpr uint32_t TM_U = 192;    // U^T         64 cols (col = token)
-constexpr uint32_t TM_O = 256;    // O^T         64 cols
+constexpr uint32_t TM_O = 0;      // O^T         64 cols (col = token), then
+constexpr uint32_t TM_S = 64;     // S^T        128 cols (col = dk): one N = 192 accumulator
+constexpr uint32_t TM_SB = 192;   // S^T bf16    64 cols (A operand, 2 dk per col)
+constexpr uint32_t TM_U = 256;    // U^T         64 cols (col = token)
 constexpr uint32_t TM_D = 320;    // D (A|QK)    96 cols, then W0^T at +0, W1^T at +64
 constexpr uint32_t TM_UB = 448;   // U^T bf16    32 cols (A operand, 2 tokens per col)
 constexpr uint32_t TM_COLS = 512;
@@ -102,7 +102,7 @@ constexpr uint32_t ID_KK64 = idesc_bf16(128, 64, 0, 0);
 constexpr uint32_t ID_KK96 = idesc_bf16(128, 96, 0, 0);
 constexpr uint32_t ID_MK64 = idesc_bf16(128, 64, 1, 0);
 constexpr uint32_t ID_KM64 = idesc_bf16(128, 64, 0, 1);
-constexpr uint32_t ID_KM128 = idesc_bf16(128, 128, 0, 1);
+constexpr uint32_t ID_KK192 = idesc_bf16(128, 192, 0, 0);
 
 __global__ void __launch_bounds__(NT, 1)
     kda_tc_chunk_kernel(const __grid_constant__ Params p, const __grid_constant__ CUtensorMap tm_q,
@@ -310,6 +310,7 @@ __global__ void __launch_bounds__(NT, 1)
         }
       }
       float sq[8], sk[8];
+      uint32_t kep[8];                             // Ke pairs (d0, d0 + 1) of the 8 rows
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
         const int r = grp * 8 + i;
@@ -341,8 +342,15 @@ __global__ void __launch_bounds__(NT, 1)
           ke1 = Ei1 * cB[1];
         }
         st_u32(sm, OFF_QG + kmajor_off(r, d0, 64), bmul2(q2, pack_bf16x2(g0, g1)));
-        st_u32(sm, OFF_KE + mnmajor_off(d0, r, 8192), bmul2(k2, pack_bf16x2(ke0, ke1)));
+        kep[i] = bmul2(k2, pack_bf16x2(ke0, ke1));
       }
+      // Ke: the 8 tokens of channel d0 (d0 + 1) form one 16-byte chunk of row d0 (d0 + 1)
+      st_u128(sm, OFF_KE + kmajor_off(d0, grp * 8, 128),
+              make_uint4(__byte_perm(kep[0], kep[1], 0x5410), __byte_perm(kep[2], kep[3], 0x5410),
+                         __byte_perm(kep[4], kep[5], 0x5410), __byte_perm(kep[6], kep[7], 0x5410)));
+      st_u128(sm, OFF_KE + kmajor_off(d0 + 1, grp * 8, 128),
+              make_uint4(__byte_perm(kep[0], kep[1], 0x7632), __byte_perm(kep[2], kep[3], 0x7632),
+                         __byte_perm(kep[4], kep[5], 0x7632), __byte_perm(kep[6], kep[7], 0x7632)));
       // reduce-scatter the 16 partial sums (8 rows x q, k) over the warp's 32 lanes
       float v[16];
 #pragma unroll
@@ -646,17 +654,15 @@ __global__ void __launch_bounds__(NT, 1)
     tc_fence_before();
     __syncthreads();
 
-    // ---- P9: O^T += U^T QK^T;  S^T += U^T Ke  (after warp 4's O^T = S^T Qg^T completed)
+    // ---- P9: [O^T | S^T] += U^T [QK; Ke]^T, one N = 192 group (after warp 4's
+    //          O^T = S^T Qg^T completed)
     bool o_ok = true;
     if (tid == 0) {
       o_ok = mbar_wait(bar_o, ph_o);
       tc_fence_after();
 #pragma unroll
-      for (int ks = 0; ks < 4; ++ks) {   // the two chains interleaved
-        mma_bf16_ts(tmem + TM_O, tmem + TM_UB + 8 * ks, kdesc(sb + OFF_QKB, 64, ks), ID_KK64, 1);
-        mma_bf16_ts(tmem + TM_S, tmem + TM_UB + 8 * ks, mndesc(sb + OFF_KE, 8192, ks), ID_KM128,
-                    1);
-      }
+      for (int ks = 0; ks < 4; ++ks)
+        mma_bf16_ts(tmem + TM_O, tmem + TM_UB + 8 * ks, kdesc(sb + OFF_QKB, 192, ks), ID_KK192, 1);
       mma_commit(bar_mma);
     }
     ph_o ^= 1;
