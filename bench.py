@@ -355,40 +355,61 @@ def main():
         if st != kda.OK:
             raise kda.KDAError(st, "device status after the timed steps")
 
-    # ---- end to end through the C ABI with host buffers
+    # ---- end to end through the C ABI with host buffers.  Every step copies its inputs
+    #      from pinned host memory and reads its out and final_state back; steps are
+    #      pipelined over two device buffer sets and three streams (copy in, compute,
+    #      copy out), so step i+1's inputs travel while step i computes.
     pinned = {k: (v.pin_memory() if isinstance(v, torch.Tensor) else v) for k, v in host.items()}
-    out_h = torch.empty(tuple(host["q"].shape), dtype=torch.bfloat16).pin_memory()
-    fin_h = torch.empty(tuple(host["initial_state"].shape),
-                        dtype=host["initial_state"].dtype).pin_memory()
-    d = sets[0]
+    out_h = [torch.empty(tuple(host["q"].shape), dtype=torch.bfloat16).pin_memory()
+             for _ in range(2)]
+    fin_h = [torch.empty(tuple(host["initial_state"].shape),
+                         dtype=host["initial_state"].dtype).pin_memory() for _ in range(2)]
     names = ("q", "k", "v", "g", "beta", "A_log", "dt_bias", "initial_state", "cu_seqlens")
     h2d = sum(pinned[k].numel() * pinned[k].element_size() for k in names)
-    d2h = out_h.numel() * out_h.element_size() + fin_h.numel() * fin_h.element_size()
+    d2h = out_h[0].numel() * out_h[0].element_size() + fin_h[0].numel() * fin_h[0].element_size()
+    s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    in_done = [torch.cuda.Event() for _ in range(2)]     # inputs of slot b copied in
+    comp_done = [torch.cuda.Event() for _ in range(2)]   # slot b computed
+    out_done = [torch.cuda.Event() for _ in range(2)]    # slot b's results copied out
+    used = [False, False]
 
-    def e2e_step():
-        for k in names:
-            d[k].copy_(pinned[k], non_blocking=True)
+    def e2e_step(i):
+        b = i % 2
+        d = sets[b]
+        if used[b]:
+            s_in.wait_event(comp_done[b])     # the slot's previous step no longer reads it
+        with torch.cuda.stream(s_in):
+            for k in names:
+                d[k].copy_(pinned[k], non_blocking=True)
+        in_done[b].record(s_in)
+        stream.wait_event(in_done[b])
+        if used[b]:
+            stream.wait_event(out_done[b])    # its previous results have been copied out
         kda.chunk_prefill_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], d["A_log"],
                               d["dt_bias"], d["lower_bound"], d["scale"], d["initial_state"],
                               d["cu_seqlens"], out=d["out"], final_state=d["fin"],
                               workspace=d["ws"], stream=stream, kernel=kernel)
-        out_h.copy_(d["out"], non_blocking=True)
-        fin_h.copy_(d["fin"], non_blocking=True)
+        comp_done[b].record(stream)
+        s_out.wait_event(comp_done[b])
+        with torch.cuda.stream(s_out):
+            out_h[b].copy_(d["out"], non_blocking=True)
+            fin_h[b].copy_(d["fin"], non_blocking=True)
+        out_done[b].record(s_out)
+        used[b] = True
 
-    with torch.cuda.stream(stream):
-        for _ in range(2):
-            e2e_step()
-        stream.synchronize()
-        KE = max(1, args.e2e_steps)
-        barrier(world)
-        torch.cuda.synchronize()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        for _ in range(KE):
-            e2e_step()
-        e1.record(stream)
-        e1.synchronize()
-        barrier(world)
+    for i in range(2):
+        e2e_step(i)
+    torch.cuda.synchronize()
+    KE = max(1, args.e2e_steps)
+    barrier(world)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(s_in)
+    for i in range(KE):
+        e2e_step(i)
+    e1.record(s_out)
+    e1.synchronize()
+    barrier(world)
     e2e_elapsed = max_over_ranks(e0.elapsed_time(e1) / 1e3, world)
 
     if rank != 0:
