@@ -41,9 +41,13 @@
  *                       written.  out must not overlap any input.
  *   - q, k, v, g, out, initial_state, final_state and workspace must be
  *     16-byte aligned; beta 2-byte; A_log and dt_bias 16-byte.
- *   - lower_bound must lie in [KDA_MIN_LOWER_BOUND, 0]: the gate is a log
- *     decay in (lower_bound, 0]; past -5.5 the per-32-token exponent
- *     anchoring the kernels use would leave the fp32 range.
+ *   - lower_bound must lie in [KDA_MIN_LOWER_BOUND, 0] = [-5, 0]: the gate
+ *     is a log decay in (lower_bound, 0].  The kernels split each decay
+ *     factor of a 64-token chunk into a row and a column factor anchored
+ *     inside 32-token blocks; at saturated gates these reach
+ *     2^(+-16 |lower_bound| log2 e), and past -5 the column factors of the
+ *     cross-block products would leave the fp32/bf16 normal range for the
+ *     smaller q/k entries.
  *   - Return value: KDA_OK (0) or a negative KDA_ERR_* code; nothing is
  *     enqueued when an error is returned.  Errors found on the device
  *     (malformed cu_seqlens, a bounded wait that gave up) are recorded in
@@ -63,7 +67,7 @@ extern "C" {
 typedef struct CUstream_st* kda_stream_t;
 
 #define KDA_HEAD_DIM 128
-#define KDA_MIN_LOWER_BOUND (-5.5f)
+#define KDA_MIN_LOWER_BOUND (-5.0f)
 
 /* state storage dtypes (PR #56485: fp32 or bf16 checkpoint state) */
 #define KDA_STATE_F32 0
@@ -74,7 +78,7 @@ typedef struct CUstream_st* kda_stream_t;
 #define KDA_ERR_INVALID_ARG (-1)         /* null pointer, bad size or dtype   */
 #define KDA_ERR_UNSUPPORTED_DEVICE (-2)  /* current device is not sm_103      */
 #define KDA_ERR_WORKSPACE_TOO_SMALL (-3) /* workspace_bytes below the query   */
-#define KDA_ERR_UNSAFE_LOWER_BOUND (-4)  /* lower_bound outside [-5.5, 0]     */
+#define KDA_ERR_UNSAFE_LOWER_BOUND (-4)  /* lower_bound outside [-5, 0]       */
 #define KDA_ERR_MISALIGNED (-5)          /* a pointer breaks its alignment    */
 #define KDA_ERR_LAUNCH_FAILED (-6)       /* the kernel launch was rejected    */
 #define KDA_ERR_DEVICE_TIMEOUT (-7)      /* (device) a bounded wait gave up   */

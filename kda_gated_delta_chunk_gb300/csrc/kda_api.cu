@@ -217,7 +217,7 @@ const char* kda_status_string(int status) {
     case KDA_ERR_INVALID_ARG: return "invalid argument";
     case KDA_ERR_UNSUPPORTED_DEVICE: return "unsupported device (needs an sm_103 GPU)";
     case KDA_ERR_WORKSPACE_TOO_SMALL: return "workspace smaller than kda_workspace_size()";
-    case KDA_ERR_UNSAFE_LOWER_BOUND: return "lower_bound outside [-5.5, 0]";
+    case KDA_ERR_UNSAFE_LOWER_BOUND: return "lower_bound outside [-5, 0]";
     case KDA_ERR_MISALIGNED: return "pointer not aligned as required";
     case KDA_ERR_LAUNCH_FAILED: return "kernel launch failed";
     case KDA_ERR_DEVICE_TIMEOUT: return "a bounded device-side wait timed out";

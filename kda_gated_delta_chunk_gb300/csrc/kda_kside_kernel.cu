@@ -54,7 +54,8 @@ constexpr int K_BAR = K_MISC + 7424;      // 2 mbarriers
 constexpr int K_TSLOT = K_MISC + 7440;
 constexpr int K_FLAGS = K_MISC + 7456;    // items {item, c0, t1, head, k} x 3, 8 ints apart
 constexpr int K_SGD = K_MISC + 7552;      // gate terms -e^{A_log} log2e dt_bias [128], -e^{A_log} log2e
-constexpr int K_CU = K_MISC + 8192;       // cu_seqlens cache (batches of up to kCuCache sequences)
+constexpr int K_RSC = K_MISC + 8192;      // per-row power-of-two operand scales, bf16x2 [q 64][k 64]
+constexpr int K_CU = K_RSC + 512;         // cu_seqlens cache (batches of up to kCuCache sequences)
 constexpr int kCuCache = 1023;
 constexpr int K_SMEM_USED = K_CU + 4 * (kCuCache + 1);
 constexpr int K_SMEM_BYTES = K_SMEM_USED + 1024;
@@ -274,6 +275,28 @@ __global__ void __launch_bounds__(NT, 2)
     }
     __syncthreads();
 
+    // ---- P2c: norms -> scale/|q_r|, 1/|k_r|, and a power of two 2^-s_r per row with
+    //           |row| 2^-s_r <= 1.  The operands are built from the rows times 2^-s_r (exact in
+    //           bf16) and the scalars carry 2^s_r: the same products, but a raw row can no
+    //           longer push an anchored factor (up to 2^(16 |lb| log2 e)) out of range.
+    uint32_t* rsc = reinterpret_cast<uint32_t*>(sm + K_RSC);
+    if (tid < 128) {   // row r = tid & 63 of q (tid < 64) or k; warps 2 rq, 2 rq + 1 hold its halves
+      const int r = tid & 63, t = tid >> 6;
+      const int q16 = r >> 4, gh = (r >> 3) & 1, i = r & 7;
+      const int pi = gh * 16 + t * 8 + i;
+      const float ss = part[(2 * q16) * 32 + pi] + part[(2 * q16 + 1) * 32 + pi];
+      // ss < 2^(e+1) -> |row| < 2^ceil((e+1)/2)
+      const int e = ((__float_as_int(ss) >> 23) & 255) - 127;
+      const int sh = max(-60, min(60, (e + 2) >> 1));
+      const float inv = (r < L) ? rsqrtf(ss + kL2Eps) * __int_as_float((127 + sh) << 23) : 0.0f;
+      const float val = (t == 0) ? p.scale * inv : inv;
+      inv_q[t * 64 + r] = val;
+      reinterpret_cast<float*>(rec + kRecVec)[128 + t * 64 + r] = val;
+      const uint32_t b = (uint32_t)(127 - sh) << 7;   // bf16 bits of 2^-sh
+      rsc[t * 64 + r] = b | (b << 16);
+    }
+    __syncthreads();
+
     // ---- P2b: anchored factors; [Kr; Qr], [Kc; Kc2] operand tiles (raw q, k); Qg and Ke
     //           record tiles straight to global
     {
@@ -320,8 +343,8 @@ __global__ void __launch_bounds__(NT, 2)
         for (int i = 0; i < 8; ++i) {
           const int ii = 8 * gh + i;
           const int r = 16 * rq + ii;
-          const uint32_t q2 = ld_u32(sm + K_INQ, (uint32_t)(r * 256 + d0 * 2));
-          const uint32_t k2 = ld_u32(sm + K_INK, (uint32_t)(r * 256 + d0 * 2));
+          const uint32_t q2 = bmul2(ld_u32(sm + K_INQ, (uint32_t)(r * 256 + d0 * 2)), rsc[r]);
+          const uint32_t k2 = bmul2(ld_u32(sm + K_INK, (uint32_t)(r * 256 + d0 * 2)), rsc[64 + r]);
           const float e0 = cl0[ii] - mE[gh][0], e1 = cl1[ii] - mE[gh][1];
           const float E0 = ex2f(e0), E1 = ex2f(e1), Ei0 = ex2f(-e0), Ei1 = ex2f(-e1);
           const uint32_t E2 = pack_bf16x2(E0, E1), Ei2 = pack_bf16x2(Ei0, Ei1);
@@ -372,23 +395,13 @@ __global__ void __launch_bounds__(NT, 2)
     fence_proxy_async();
     __syncthreads();
 
-    // ---- P3: D = [Kr; Qr] [Kc; Kc2]^T on the tensor cores; norms of q and k meanwhile
+    // ---- P3: D = [Kr; Qr] [Kc; Kc2]^T on the tensor cores
     if (tid == 0) {
       tc_fence_after();
 #pragma unroll
       for (int ks = 0; ks < 8; ++ks)
         mma_bf16(tmem + TM_D, kdesc(sb + K_RKQ, 128, ks), kdesc(sb + K_CKC, 96, ks), ID_KK96, ks > 0);
       mma_commit(bar_mma);
-    }
-    if (tid < 128) {   // row r = tid & 63 of q (tid < 64) or k; warps 2 rq, 2 rq + 1 hold its halves
-      const int r = tid & 63, t = tid >> 6;
-      const int q16 = r >> 4, gh = (r >> 3) & 1, i = r & 7;
-      const int pi = gh * 16 + t * 8 + i;
-      const float ss = part[(2 * q16) * 32 + pi] + part[(2 * q16 + 1) * 32 + pi];
-      const float inv = (r < L) ? rsqrtf(ss + kL2Eps) : 0.0f;
-      const float val = (t == 0) ? p.scale * inv : inv;
-      inv_q[t * 64 + r] = val;
-      reinterpret_cast<float*>(rec + kRecVec)[128 + t * 64 + r] = val;
     }
     {
       const bool ok = tid != 0 || mbar_wait(bar_mma, ph_mma);

@@ -20,11 +20,14 @@
 // and a column factor so the products run on tensor cores.  The chunk is
 // cut into two 32-token blocks; inside block b the cumsum is anchored at
 // its 16th token, so every per-element factor stays within 2^(+-16|lb|
-// log2 e), inside the fp32/bf16 range for |lb| <= 5.5.  Products between
-// the blocks reuse the block-1 row operand; their column operand Kc2 carries
-// 2^(B0 - c_s) * 2^(alpha_1), a product of two factors <= 1, so one MMA with
-// N = 96 yields the diagonal blocks (columns 0-63) and the off-diagonal
-// block (columns 64-95) together.
+// log2 e).  Products between the blocks reuse the block-1 row operand; their
+// column operand Kc2 carries 2^(B0 - c_s) * 2^(alpha_1), a product of two
+// factors <= 1, so one MMA with N = 96 yields the diagonal blocks (columns
+// 0-63) and the off-diagonal block (columns 64-95) together.  At the block
+// boundary Kc2's factor is 2^(alpha_1) >= 2^(-16|lb| log2 e): with |lb| <= 5
+// that is >= 2^-116, leaving 2^10 of headroom above the smallest normal
+// number for the smaller entries of a row.  q and k rows enter scaled by a
+// power of two to |row| <= 1, so the factors bound the operands.
 //
 // The dense products run on tcgen05 (kind::f16: bf16 operands in shared
 // memory, fp32 accumulators in TMEM), transposed so that M = 128 is the
@@ -82,7 +85,8 @@ constexpr int OFF_PART = OFF_MISC + 6912;   // norm partial sums [16 warps][16]
 constexpr int OFF_BAR = OFF_MISC + 7936;    // 4 mbarriers
 constexpr int OFF_TSLOT = OFF_MISC + 7968;  // TMEM base address
 constexpr int OFF_FLAGS = OFF_MISC + 7972;  // [0] sequence chosen for this CTA
-constexpr int SMEM_USED = OFF_MISC + 8192;
+constexpr int OFF_RSC = OFF_MISC + 8192;    // per-row power-of-two operand scales, bf16x2 [q 64][k 64]
+constexpr int SMEM_USED = OFF_RSC + 512;
 constexpr int SMEM_BYTES = SMEM_USED + 1024;
 static_assert(OFF_Y + 32 * NS * 4 <= OFF_TB, "T scratch overlaps T diag(b)");
 static_assert(OFF_CKC + 24576 <= OFF_TB, "operands overlap T diag(b)");
@@ -120,6 +124,7 @@ __global__ void __launch_bounds__(NT, 1)
   float* wf = reinterpret_cast<float*>(sm + OFF_WF);
   float* gt = reinterpret_cast<float*>(sm + OFF_GT);
   float* part = reinterpret_cast<float*>(sm + OFF_PART);
+  uint32_t* rsc = reinterpret_cast<uint32_t*>(sm + OFF_RSC);
   int* flags = reinterpret_cast<int*>(sm + OFF_FLAGS);
   uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + OFF_TSLOT);
   const uint32_t bar_qkg = sb + OFF_BAR, bar_v = bar_qkg + 8, bar_mma = bar_qkg + 16;
@@ -277,11 +282,52 @@ __global__ void __launch_bounds__(NT, 1)
         cl1[i] = run1;
       }
       *reinterpret_cast<float2*>(gt + grp * 128 + d0) = make_float2(run0, run1);
+      // sums of squares of the group's q and k rows over this warp's 64 channels,
+      // reduce-scattered: lanes 2j, 2j + 1 end with the sum of v[j] ([0, 8) q, [8, 16) k)
+      float v[16];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int r = grp * 8 + i;
+        const float2 qf = unpack_bf16x2(ld_u32(sm + OFF_INQ, (uint32_t)(r * 256 + d0 * 2)));
+        const float2 kf = unpack_bf16x2(ld_u32(sm + OFF_INK, (uint32_t)(r * 256 + d0 * 2)));
+        v[i] = fmaf(qf.x, qf.x, qf.y * qf.y);
+        v[8 + i] = fmaf(kf.x, kf.x, kf.y * kf.y);
+      }
+#pragma unroll
+      for (int o = 16, m = 8; o >= 2; o >>= 1, m >>= 1) {
+        const bool up = (lane & o) != 0;
+#pragma unroll
+        for (int i = 0; i < m; ++i) {
+          const float send = up ? v[i] : v[i + m];
+          const float keep = up ? v[i + m] : v[i];
+          v[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+        }
+      }
+      v[0] += __shfl_xor_sync(0xffffffffu, v[0], 1);
+      if ((lane & 1) == 0) part[warp * 16 + (lane >> 1)] = v[0];
     }
     if (__syncthreads_or(!tma_ok)) { failed = true; site = 10; break; }
 
-    // ---- P2b: anchored factors, bf16 operand tiles of the raw q, k (their norms are
-    //           applied to the products later), and the partial sums of squares
+    // ---- P2c: norms -> scale/|q_r|, 1/|k_r|, and a power of two 2^-s_r per row with
+    //           |row| 2^-s_r <= 1.  The operands are built from the rows times 2^-s_r (exact in
+    //           bf16) and the scalars carry 2^s_r: the same products, but a raw row can no
+    //           longer push an anchored factor (up to 2^(16 |lb| log2 e)) out of range.
+    if (tid < 128) {   // row r = tid & 63 of q (tid < 64) or k; warps 2 g8, 2 g8 + 1 hold it
+      const int r = tid & 63, t = tid >> 6;
+      const int g8 = r >> 3, i = r & 7;
+      const float ss = part[(2 * g8) * 16 + t * 8 + i] + part[(2 * g8 + 1) * 16 + t * 8 + i];
+      // ss < 2^(e+1) -> |row| < 2^ceil((e+1)/2)
+      const int e = ((__float_as_int(ss) >> 23) & 255) - 127;
+      const int sh = max(-60, min(60, (e + 2) >> 1));
+      const float inv = (r < L) ? rsqrtf(ss + kL2Eps) * __int_as_float((127 + sh) << 23) : 0.0f;
+      inv_q[t * 64 + r] = (t == 0) ? p.scale * inv : inv;
+      const uint32_t b = (uint32_t)(127 - sh) << 7;   // bf16 bits of 2^-sh
+      rsc[t * 64 + r] = b | (b << 16);
+    }
+    __syncthreads();
+
+    // ---- P2b: anchored factors, bf16 operand tiles of the (power-of-two scaled) q, k rows
+    //           (their norms are applied to the products later)
     {
       float mE[2], cA[2], cB[2], cX[2], cR[2];
 #pragma unroll
@@ -309,16 +355,12 @@ __global__ void __launch_bounds__(NT, 1)
           wf[256 + d0 + c] = ex2f(B0);             //            2^B0
         }
       }
-      float sq[8], sk[8];
       uint32_t kep[8];                             // Ke pairs (d0, d0 + 1) of the 8 rows
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
         const int r = grp * 8 + i;
-        const uint32_t q2 = ld_u32(sm + OFF_INQ, (uint32_t)(r * 256 + d0 * 2));
-        const uint32_t k2 = ld_u32(sm + OFF_INK, (uint32_t)(r * 256 + d0 * 2));
-        const float2 qf = unpack_bf16x2(q2), kf = unpack_bf16x2(k2);
-        sq[i] = fmaf(qf.x, qf.x, qf.y * qf.y);
-        sk[i] = fmaf(kf.x, kf.x, kf.y * kf.y);
+        const uint32_t q2 = bmul2(ld_u32(sm + OFF_INQ, (uint32_t)(r * 256 + d0 * 2)), rsc[r]);
+        const uint32_t k2 = bmul2(ld_u32(sm + OFF_INK, (uint32_t)(r * 256 + d0 * 2)), rsc[64 + r]);
         const float e0 = cl0[i] - mE[0], e1 = cl1[i] - mE[1];
         const float E0 = ex2f(e0), E1 = ex2f(e1);
         const float Ei0 = ex2f(-e0), Ei1 = ex2f(-e1);
@@ -351,35 +393,11 @@ __global__ void __launch_bounds__(NT, 1)
       st_u128(sm, OFF_KE + kmajor_off(d0 + 1, grp * 8, 128),
               make_uint4(__byte_perm(kep[0], kep[1], 0x7632), __byte_perm(kep[2], kep[3], 0x7632),
                          __byte_perm(kep[4], kep[5], 0x7632), __byte_perm(kep[6], kep[7], 0x7632)));
-      // reduce-scatter the 16 partial sums (8 rows x q, k) over the warp's 32 lanes
-      float v[16];
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        v[i] = sq[i];
-        v[8 + i] = sk[i];
-      }
-#pragma unroll
-      for (int o = 16, m = 8; o >= 2; o >>= 1, m >>= 1) {
-        const bool up = (lane & o) != 0;
-#pragma unroll
-        for (int i = 0; i < m; ++i) {
-          const float send = up ? v[i] : v[i + m];
-          const float keep = up ? v[i + m] : v[i];
-          v[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
-        }
-      }
-      v[0] += __shfl_xor_sync(0xffffffffu, v[0], 1);
-      if ((lane & 1) == 0) {
-        const int idx = ((lane >> 4) & 1) * 8 + ((lane >> 3) & 1) * 4 + ((lane >> 2) & 1) * 2 +
-                        ((lane >> 1) & 1);
-        part[warp * 16 + idx] = v[0];
-      }
     }
     fence_proxy_async();
     __syncthreads();
 
-    // ---- P3: D = [Kr; Qr] [Kc; Kc2]^T on the tensor cores; fetch the next q, k, g.
-    //          Meanwhile: norms of q and k.
+    // ---- P3: D = [Kr; Qr] [Kc; Kc2]^T on the tensor cores; fetch the next q, k, g
     if (tid == 0) {
       tc_fence_after();
 #pragma unroll
@@ -393,13 +411,6 @@ __global__ void __launch_bounds__(NT, 1)
         tma_load_2d(sb + OFF_INK, &tm_k, xcol, c0 + C, bar_qkg);
         tma_load_2d(sb + OFF_ING, &tm_g, xcol, c0 + C, bar_qkg);
       }
-    }
-    if (tid < 128) {   // row r = tid & 63 of q (tid < 64) or k
-      const int r = tid & 63, t = tid >> 6;
-      const int g8 = r >> 3, i = r & 7;
-      const float ss = part[(2 * g8) * 16 + t * 8 + i] + part[(2 * g8 + 1) * 16 + t * 8 + i];
-      const float inv = (r < L) ? rsqrtf(ss + kL2Eps) : 0.0f;
-      inv_q[t * 64 + r] = (t == 0) ? p.scale * inv : inv;
     }
     {
       // one thread waits for the MMA (the others park on the barrier); all see the v tile land

@@ -119,6 +119,7 @@ def _call(L, **over):
 
 @pytest.mark.parametrize("over,code", [
     (dict(lb=-6.0), kda.ERR_UNSAFE_LOWER_BOUND),
+    (dict(lb=-5.01), kda.ERR_UNSAFE_LOWER_BOUND),
     (dict(lb=0.5), kda.ERR_UNSAFE_LOWER_BOUND),
     (dict(lb=float("nan")), kda.ERR_INVALID_ARG),
     (dict(scale=float("inf")), kda.ERR_INVALID_ARG),

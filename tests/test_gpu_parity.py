@@ -187,6 +187,22 @@ def test_workload4_ragged_bf16_state(oracle_mod, kernel):
     check(oracle_mod, inp, out, fin, seqs=seqs, heads=[0, 13, 31], tag="workload 4")
 
 
+@pytest.mark.parametrize("kernel", KERNELS)
+@pytest.mark.parametrize("lb,shift", [(-5.0, 40.0), (-5.0, -40.0), (-5.0, 0.0), (0.0, 0.0)])
+def test_extreme_gates(oracle_mod, kernel, lb, shift):
+    """The gate at its limits: every token decays by e^lb with the largest accepted |lb|
+    (sigmoid saturated at 1: the anchored exponents reach 2^(+-16 |lb| log2 e)), no decay
+    (sigmoid saturated at 0, or lb = 0), and the largest |lb| with ordinary gates.  The raw
+    q/k rows are scaled up by 64 too: the kernels must not depend on normalised inputs."""
+    w = W.custom([130, 64, 1, 77], 2, seed=33, lower_bound=lb)
+    inp = W.make_inputs(w)
+    inp["g"] = (inp["g"].float() + shift).to(torch.bfloat16)
+    inp["q"] = (inp["q"].float() * 64.0).to(torch.bfloat16)   # exact: a power of two
+    inp["k"] = (inp["k"].float() * 64.0).to(torch.bfloat16)
+    out, fin = run_gpu(inp, kernel)
+    check(oracle_mod, inp, out, fin, tag=f"gates lb={lb} shift={shift} k{kernel}")
+
+
 # ----------------------------------------------------------------- edge cases
 def test_inplace_state_update(oracle_mod):
     inp = W.make_inputs(W.custom([90, 40], 2, seed=23))
