@@ -169,9 +169,11 @@ def barrier(world):
 
 
 def max_over_ranks(x: float, world: int) -> float:
+    """Largest x over the ranks (the job's time is the slowest rank's)."""
     if world == 1:
         return x
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    on_gpu = torch.distributed.get_backend() == "nccl"
+    t = torch.tensor([x], dtype=torch.float64, device="cuda" if on_gpu else "cpu")
     torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
     return float(t.item())
 
