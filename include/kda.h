@@ -156,6 +156,31 @@ int kda_chunk_prefill_fwd_ex(const void* q, const void* k, const void* v, const 
                              size_t workspace_bytes, int vsplit, int kernel);
 
 /*
+ * As kda_chunk_prefill_fwd_ex, for inputs that are views rather than dense
+ * tensors -- for instance q, k, v and g as slices of one fused projection
+ * output [T, 4 * H * 128], so that no copy to a dense layout is needed (the
+ * vLLM PR report "[Perf][GLM-5.3-Flash] Use FlashKDA for KDA chunked
+ * prefill", PR #55737, measures such copies at about 115 us per layer at
+ * 16k tokens: Risks & impact and the "FlashKDA prefill call wrapper"
+ * listing).  Each stride is the distance in elements between consecutive
+ * tokens: q element (t, h, d) is read at q[t * q_stride + h * 128 + d] (the
+ * same for k, v, g) and beta (t, h) at beta[t * beta_stride + h].  The head
+ * and channel dimensions stay dense; out is dense as before.  q/k/v/g
+ * strides must be at least heads * 128 and a multiple of 8 (16-byte rows for
+ * the TMA loads), beta_stride at least heads; otherwise KDA_ERR_INVALID_ARG
+ * or KDA_ERR_MISALIGNED.
+ */
+int kda_chunk_prefill_fwd_strided(const void* q, const void* k, const void* v, const void* g,
+                                  const void* beta, const float* A_log, const float* dt_bias,
+                                  float lower_bound, float scale, const void* initial_state,
+                                  const int32_t* cu_seqlens, void* out, void* final_state,
+                                  int state_dtype, void* workspace, kda_stream_t stream,
+                                  int64_t total_tokens, int32_t num_seqs, int32_t heads,
+                                  size_t workspace_bytes, int64_t q_stride, int64_t k_stride,
+                                  int64_t v_stride, int64_t g_stride, int64_t beta_stride,
+                                  int vsplit, int kernel);
+
+/*
  * The value-dimension split factor the automatic path uses for a batch of
  * `num_seqs` sequences and `heads` heads on a GPU with `sm_count` SMs.
  * The trigger is PR #52458's: split only when 2 * heads * num_seqs <=

@@ -45,7 +45,8 @@ ERR_CUDA = -9
 # every symbol include/kda.h declares
 EXPORTS = ("kda_workspace_size", "kda_chunk_prefill_fwd", "kda_chunk_prefill_fwd_ex",
            "kda_choose_vsplit", "kda_status_string", "kda_last_device_status",
-           "kda_device_check", "kda_plan", "kda_chunk_prefill_fwd_noalloc")
+           "kda_device_check", "kda_plan", "kda_chunk_prefill_fwd_strided",
+           "kda_chunk_prefill_fwd_noalloc")
 
 _lib = None
 _lock = threading.Lock()
@@ -77,6 +78,9 @@ def lib() -> ctypes.CDLL:
             L.kda_chunk_prefill_fwd.argtypes = fwd_args
             L.kda_chunk_prefill_fwd_ex.restype = ctypes.c_int
             L.kda_chunk_prefill_fwd_ex.argtypes = fwd_args + [ctypes.c_int, ctypes.c_int]
+            L.kda_chunk_prefill_fwd_strided.restype = ctypes.c_int
+            L.kda_chunk_prefill_fwd_strided.argtypes = fwd_args + [I64] * 5 + [ctypes.c_int,
+                                                                             ctypes.c_int]
             L.kda_choose_vsplit.restype = ctypes.c_int
             L.kda_choose_vsplit.argtypes = [I32, I32, I32]
             L.kda_status_string.restype = ctypes.c_char_p
@@ -138,17 +142,25 @@ def _ptr(t):
     return None if t is None else ctypes.c_void_p(t.data_ptr())
 
 
-def _need(t, name, dtype, shape=None):
+def _need(t, name, dtype, shape=None, token_strided=False):
+    """Type/device/shape checks.  With token_strided, only the leading (token) dimension may
+    be strided: the rest must be dense (views into a wider buffer, e.g. a fused projection)."""
     if not isinstance(t, torch.Tensor):
         raise TypeError(f"{name} must be a torch.Tensor")
     if t.device.type != "cuda":
         raise ValueError(f"{name} must be a CUDA tensor")
     if t.dtype != dtype:
         raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
-    if not t.is_contiguous():
-        raise ValueError(f"{name} must be contiguous")
     if shape is not None and tuple(t.shape) != tuple(shape):
         raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+    if token_strided:
+        inner = 1
+        for size, stride in zip(reversed(t.shape[1:]), reversed(t.stride()[1:])):
+            if size > 1 and stride != inner:
+                raise ValueError(f"{name}: only the token dimension may be strided")
+            inner *= size
+    elif not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
 
 
 def chunk_prefill_fwd(q, k, v, g, beta, A_log, dt_bias, lower_bound, scale,
@@ -175,11 +187,14 @@ def chunk_prefill_fwd(q, k, v, g, beta, A_log, dt_bias, lower_bound, scale,
         raise KDAError(ERR_INVALID_ARG, f"head_dim {D} (only {HEAD_DIM} is supported)")
     N = cu_seqlens.numel() - 1
     for name, t in (("q", q), ("k", k), ("v", v), ("g", g)):
-        _need(t, name, torch.bfloat16, (T, H, D))
-    _need(beta, "beta", torch.bfloat16, (T, H))
+        _need(t, name, torch.bfloat16, (T, H, D), token_strided=True)
+    _need(beta, "beta", torch.bfloat16, (T, H), token_strided=True)
     _need(A_log, "A_log", torch.float32, (H,))
     _need(dt_bias, "dt_bias", torch.float32, (H, D))
     _need(cu_seqlens, "cu_seqlens", torch.int32, (N + 1,))
+    tok_strides = [int(t.stride(0)) if T > 1 else H * D for t in (q, k, v, g)]
+    tok_strides.append(int(beta.stride(0)) if T > 1 else H)
+    dense = tok_strides == [H * D] * 4 + [H]
     if state_dtype is None:
         state_dtype = initial_state.dtype if initial_state is not None else torch.float32
     sd = {torch.float32: STATE_F32, torch.bfloat16: STATE_BF16}.get(state_dtype)
@@ -188,7 +203,7 @@ def chunk_prefill_fwd(q, k, v, g, beta, A_log, dt_bias, lower_bound, scale,
     if initial_state is not None:
         _need(initial_state, "initial_state", state_dtype, (N, H, D, D))
     if out is None:
-        out = torch.empty_like(q)
+        out = torch.empty((T, H, D), dtype=torch.bfloat16, device=q.device)
     _need(out, "out", torch.bfloat16, (T, H, D))
     if final_state is None:
         final_state = torch.empty((N, H, D, D), dtype=state_dtype, device=q.device)
@@ -201,7 +216,9 @@ def chunk_prefill_fwd(q, k, v, g, beta, A_log, dt_bias, lower_bound, scale,
             float(lower_bound), float(scale), _ptr(initial_state), _ptr(cu_seqlens),
             _ptr(out), _ptr(final_state), sd, _ptr(workspace), ctypes.c_void_p(s.cuda_stream),
             int(T), int(N), int(H), int(workspace.numel()))
-    if vsplit == -1 and kernel == KERNEL_AUTO:
+    if not dense:
+        rc = lib().kda_chunk_prefill_fwd_strided(*args, *tok_strides, int(vsplit), int(kernel))
+    elif vsplit == -1 and kernel == KERNEL_AUTO:
         rc = lib().kda_chunk_prefill_fwd(*args)
     else:
         rc = lib().kda_chunk_prefill_fwd_ex(*args, int(vsplit), int(kernel))

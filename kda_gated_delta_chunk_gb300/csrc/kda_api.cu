@@ -100,11 +100,23 @@ int fwd_impl(const void* q, const void* k, const void* v, const void* g, const v
              const float* A_log, const float* dt_bias, float lower_bound, float scale,
              const void* initial_state, const int32_t* cu_seqlens, void* out, void* final_state,
              int state_dtype, void* workspace, kda_stream_t stream, int64_t total_tokens,
-             int32_t num_seqs, int32_t heads, size_t workspace_bytes, int vsplit, int kernel) {
+             int32_t num_seqs, int32_t heads, size_t workspace_bytes, int vsplit, int kernel,
+             const int64_t* strides) {
   int rc = validate(q, k, v, g, beta, A_log, dt_bias, lower_bound, scale, initial_state,
                     cu_seqlens, out, final_state, state_dtype, workspace, total_tokens,
                     num_seqs, heads, workspace_bytes);
   if (rc != KDA_OK) return rc;
+  // token strides (elements) of q, k, v, g, beta; NULL = dense
+  int64_t st[5] = {(int64_t)heads * kda::kHeadDim, (int64_t)heads * kda::kHeadDim,
+                   (int64_t)heads * kda::kHeadDim, (int64_t)heads * kda::kHeadDim, heads};
+  if (strides) {
+    for (int i = 0; i < 5; ++i) {
+      st[i] = strides[i];
+      if (st[i] < (i < 4 ? (int64_t)heads * kda::kHeadDim : (int64_t)heads)) return KDA_ERR_INVALID_ARG;
+      if (st[i] > ((int64_t)1 << 40) / (total_tokens > 0 ? total_tokens : 1)) return KDA_ERR_INVALID_ARG;
+      if (i < 4 && (st[i] % 8) != 0) return KDA_ERR_MISALIGNED;   // 16-byte rows for TMA
+    }
+  }
   // selectors first: they are host-side checks and need no device
   if (vsplit != -1 && vsplit != 1 && vsplit != 2 && vsplit != 4 && vsplit != 8)
     return KDA_ERR_INVALID_ARG;
@@ -145,6 +157,11 @@ int fwd_impl(const void* q, const void* k, const void* v, const void* g, const v
   p.heads = heads;
   p.vsplit = P;
   p.sm_count = sms;
+  p.s_q = st[0];
+  p.s_k = st[1];
+  p.s_v = st[2];
+  p.s_g = st[3];
+  p.s_beta = st[4];
 
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   cudaError_t err = (kernel == KDA_KERNEL_REF)     ? kda::launch_ref(p, s)
@@ -187,7 +204,7 @@ int kda_chunk_prefill_fwd(const void* q, const void* k, const void* v, const voi
                           size_t workspace_bytes) {
   return fwd_impl(q, k, v, g, beta, A_log, dt_bias, lower_bound, scale, initial_state,
                   cu_seqlens, out, final_state, state_dtype, workspace, stream, total_tokens,
-                  num_seqs, heads, workspace_bytes, -1, KDA_KERNEL_AUTO);
+                  num_seqs, heads, workspace_bytes, -1, KDA_KERNEL_AUTO, nullptr);
 }
 
 int kda_chunk_prefill_fwd_ex(const void* q, const void* k, const void* v, const void* g,
@@ -199,7 +216,22 @@ int kda_chunk_prefill_fwd_ex(const void* q, const void* k, const void* v, const 
                              size_t workspace_bytes, int vsplit, int kernel) {
   return fwd_impl(q, k, v, g, beta, A_log, dt_bias, lower_bound, scale, initial_state,
                   cu_seqlens, out, final_state, state_dtype, workspace, stream, total_tokens,
-                  num_seqs, heads, workspace_bytes, vsplit, kernel);
+                  num_seqs, heads, workspace_bytes, vsplit, kernel, nullptr);
+}
+
+int kda_chunk_prefill_fwd_strided(const void* q, const void* k, const void* v, const void* g,
+                                  const void* beta, const float* A_log, const float* dt_bias,
+                                  float lower_bound, float scale, const void* initial_state,
+                                  const int32_t* cu_seqlens, void* out, void* final_state,
+                                  int state_dtype, void* workspace, kda_stream_t stream,
+                                  int64_t total_tokens, int32_t num_seqs, int32_t heads,
+                                  size_t workspace_bytes, int64_t q_stride, int64_t k_stride,
+                                  int64_t v_stride, int64_t g_stride, int64_t beta_stride,
+                                  int vsplit, int kernel) {
+  const int64_t strides[5] = {q_stride, k_stride, v_stride, g_stride, beta_stride};
+  return fwd_impl(q, k, v, g, beta, A_log, dt_bias, lower_bound, scale, initial_state,
+                  cu_seqlens, out, final_state, state_dtype, workspace, stream, total_tokens,
+                  num_seqs, heads, workspace_bytes, vsplit, kernel, strides);
 }
 
 int kda_choose_vsplit(int32_t num_seqs, int32_t heads, int32_t sm_count) {

@@ -376,7 +376,7 @@ bool make_chain_maps(ChainMaps* m, const Params& p, int dv) {
   const cuuint32_t es[2] = {1, 1};
   {
     cuuint64_t dims[2] = {(cuuint64_t)p.heads * 128, (cuuint64_t)(p.total_tokens > 0 ? p.total_tokens : 1)};
-    cuuint64_t strides[1] = {(cuuint64_t)p.heads * 256};
+    cuuint64_t strides[1] = {(cuuint64_t)p.s_v * 2};
     cuuint32_t box[2] = {(cuuint32_t)dv, 64};
     const CUtensorMapSwizzle sw = dv == 16 ? CU_TENSOR_MAP_SWIZZLE_32B
                                            : (dv == 32 ? CU_TENSOR_MAP_SWIZZLE_64B

@@ -413,7 +413,7 @@ cudaError_t launch_chain_tc(const Params& p, cudaStream_t stream) {
   ChainTcMaps maps;
   const void* vb = p.v ? (const void*)p.v : (const void*)p.dt_bias;
   cuuint64_t dims[2] = {(cuuint64_t)p.heads * D3, (cuuint64_t)(p.total_tokens > 0 ? p.total_tokens : 1)};
-  cuuint64_t strides[1] = {(cuuint64_t)p.heads * D3 * 2};
+  cuuint64_t strides[1] = {(cuuint64_t)p.s_v * 2};
   cuuint32_t box[2] = {64, 64};
   cuuint32_t es[2] = {1, 1};
   if (enc(&maps.v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(vb), dims, strides, box,

@@ -52,6 +52,9 @@ struct Params {
   int32_t heads;
   int32_t vsplit;              // 1, 2, 4 or 8
   int32_t sm_count;            // multiprocessors of the device
+  // token strides in elements: q/k/v/g element (t, h, d) at t * s + h * 128 + d, beta (t, h)
+  // at t * s_beta + h (dense: s = H * 128, s_beta = H)
+  int64_t s_q, s_k, s_v, s_g, s_beta;
 };
 
 // Record a device-side error (first writer wins) with its block and site.

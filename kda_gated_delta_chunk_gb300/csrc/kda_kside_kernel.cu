@@ -187,7 +187,7 @@ __global__ void __launch_bounds__(NT, 2)
       if (tid == 0) sgd[128] = sgn;
     } else if (tid < 128 + C) {
       const int j = tid - 128;
-      const float b = (c0n + j < t1n) ? __bfloat162float(p.beta[(size_t)(c0n + j) * H + hn]) : 0.0f;
+      const float b = (c0n + j < t1n) ? __bfloat162float(p.beta[(size_t)(c0n + j) * p.s_beta + hn]) : 0.0f;
       beta_s[j] = (c0n + j < t1n) ? sigm(b) : 0.0f;
     }
   };
@@ -605,9 +605,10 @@ typedef CUresult (*EncodeTiledFnK)(CUtensorMap*, CUtensorMapDataType, cuuint32_t
                                    const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
                                    CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 
-bool make_in_map(EncodeTiledFnK enc, CUtensorMap* m, const void* base, int64_t T, int H) {
+bool make_in_map(EncodeTiledFnK enc, CUtensorMap* m, const void* base, int64_t T, int H,
+                 int64_t stride) {
   cuuint64_t dims[2] = {(cuuint64_t)H * D, (cuuint64_t)(T > 0 ? T : 1)};
-  cuuint64_t strides[1] = {(cuuint64_t)H * D * 2};
+  cuuint64_t strides[1] = {(cuuint64_t)stride * 2};
   cuuint32_t box[2] = {(cuuint32_t)D, (cuuint32_t)C};
   cuuint32_t es[2] = {1, 1};
   return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
@@ -634,9 +635,9 @@ cudaError_t launch_kside(const Params& p, cudaStream_t stream) {
   EncodeTiledFnK enc = reinterpret_cast<EncodeTiledFnK>(tensor_map_encoder());
   if (!enc) return cudaErrorNotSupported;
   CUtensorMap mq, mk, mg;
-  if (!make_in_map(enc, &mq, p.q, p.total_tokens, p.heads) ||
-      !make_in_map(enc, &mk, p.k, p.total_tokens, p.heads) ||
-      !make_in_map(enc, &mg, p.g, p.total_tokens, p.heads))
+  if (!make_in_map(enc, &mq, p.q, p.total_tokens, p.heads, p.s_q) ||
+      !make_in_map(enc, &mk, p.k, p.total_tokens, p.heads, p.s_k) ||
+      !make_in_map(enc, &mg, p.g, p.total_tokens, p.heads, p.s_g))
     return cudaErrorInvalidValue;
   const int64_t cap = 2 * (int64_t)p.sm_count;
   const int64_t grid = items < cap ? items : cap;

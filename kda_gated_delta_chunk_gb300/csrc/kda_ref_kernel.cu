@@ -95,9 +95,9 @@ __global__ void __launch_bounds__(RT, 1) kda_ref_chunk_kernel(Params p) {
         const int d = lane * 4 + j;
         qv[j] = kv[j] = 0.f;
         if (r < L) {
-          const size_t idx = (size_t)(c0 + r) * HD + (size_t)h * D + d;
-          qv[j] = __bfloat162float(p.q[idx]);
-          kv[j] = __bfloat162float(p.k[idx]);
+          const size_t off = (size_t)h * D + d;
+          qv[j] = __bfloat162float(p.q[(size_t)(c0 + r) * p.s_q + off]);
+          kv[j] = __bfloat162float(p.k[(size_t)(c0 + r) * p.s_k + off]);
         }
         sq += qv[j] * qv[j];
         sk += kv[j] * kv[j];
@@ -117,15 +117,15 @@ __global__ void __launch_bounds__(RT, 1) kda_ref_chunk_kernel(Params p) {
       const int r = i / D, d = i % D;
       float a2 = 0.f, vvv = 0.f;
       if (r < L) {
-        const size_t idx = (size_t)(c0 + r) * HD + (size_t)h * D + d;
+        const size_t idx = (size_t)(c0 + r) * p.s_g + (size_t)h * D + d;
         a2 = lb2 * sigmoidf_(gate_scale * (__bfloat162float(p.g[idx]) + p.dt_bias[h * D + d]));
-        if (d < DV) vvv = __bfloat162float(p.v[(size_t)(c0 + r) * HD + (size_t)h * D + dv0 + d]);
+        if (d < DV) vvv = __bfloat162float(p.v[(size_t)(c0 + r) * p.s_v + (size_t)h * D + dv0 + d]);
       }
       sm.gam[r][d] = a2;
       if (d < DV) sm.vv[r][d] = vvv;
     }
     if (tid < RC)
-      sm.b[tid] = tid < L ? sigmoidf_(__bfloat162float(p.beta[(size_t)(c0 + tid) * H + h])) : 0.f;
+      sm.b[tid] = tid < L ? sigmoidf_(__bfloat162float(p.beta[(size_t)(c0 + tid) * p.s_beta + h])) : 0.f;
     __syncthreads();
 
     // 2. inclusive cumsum of the log2 decay over the chunk, per key channel

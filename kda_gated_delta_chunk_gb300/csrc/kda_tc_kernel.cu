@@ -242,7 +242,7 @@ __global__ void __launch_bounds__(NT, 1)
   int site = 0;
   // beta logits are fetched one chunk ahead (their load latency hides behind a chunk)
   float b_raw = 0.0f;
-  if (tid < C && t0 + tid < t1) b_raw = __bfloat162float(p.beta[(size_t)(t0 + tid) * H + h]);
+  if (tid < C && t0 + tid < t1) b_raw = __bfloat162float(p.beta[(size_t)(t0 + tid) * p.s_beta + h]);
 
   for (int c0 = t0; c0 < t1; c0 += C) {
     const int L = min(C, t1 - c0);
@@ -254,7 +254,7 @@ __global__ void __launch_bounds__(NT, 1)
     ph_qkg ^= 1;
     if (tid < C) {
       beta_s[tid] = (tid < L) ? sigm(b_raw) : 0.0f;
-      if (c0 + C + tid < t1) b_raw = __bfloat162float(p.beta[(size_t)(c0 + C + tid) * H + h]);
+      if (c0 + C + tid < t1) b_raw = __bfloat162float(p.beta[(size_t)(c0 + C + tid) * p.s_beta + h]);
     }
     if (L < C) {
       for (int idx = tid; idx < (C - L) * 32; idx += NT) {
@@ -771,11 +771,12 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
-// A [T rows][H*128 cols] bf16 view of q/k/g/v; box {box_cols, 64 rows}.
+// A [T rows][H*128 cols] bf16 view of q/k/g/v with a row stride of `stride` elements;
+// box {box_cols, 64 rows}.
 bool make_map(EncodeTiledFn enc, CUtensorMap* m, const void* base, int64_t T, int H,
-              int box_cols, bool swizzle) {
+              int64_t stride, int box_cols, bool swizzle) {
   cuuint64_t dims[2] = {(cuuint64_t)H * D, (cuuint64_t)(T > 0 ? T : 1)};
-  cuuint64_t strides[1] = {(cuuint64_t)H * D * 2};
+  cuuint64_t strides[1] = {(cuuint64_t)stride * 2};
   cuuint32_t box[2] = {(cuuint32_t)box_cols, (cuuint32_t)C};
   cuuint32_t es[2] = {1, 1};
   return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
@@ -811,10 +812,10 @@ cudaError_t launch_tc(const Params& p, cudaStream_t stream) {
   const void* kb = p.k ? (const void*)p.k : (const void*)p.dt_bias;
   const void* gb = p.g ? (const void*)p.g : (const void*)p.dt_bias;
   const void* vb = p.v ? (const void*)p.v : (const void*)p.dt_bias;
-  if (!make_map(enc, &mq, qb, p.total_tokens, p.heads, D, false) ||
-      !make_map(enc, &mk, kb, p.total_tokens, p.heads, D, false) ||
-      !make_map(enc, &mg, gb, p.total_tokens, p.heads, D, false) ||
-      !make_map(enc, &mv, vb, p.total_tokens, p.heads, 64, true))
+  if (!make_map(enc, &mq, qb, p.total_tokens, p.heads, p.s_q, D, false) ||
+      !make_map(enc, &mk, kb, p.total_tokens, p.heads, p.s_k, D, false) ||
+      !make_map(enc, &mg, gb, p.total_tokens, p.heads, p.s_g, D, false) ||
+      !make_map(enc, &mv, vb, p.total_tokens, p.heads, p.s_v, 64, true))
     return cudaErrorInvalidValue;
   kda_tc_chunk_kernel<<<(unsigned)blocks, NT, SMEM_BYTES, stream>>>(p, mq, mk, mg, mv);
   return cudaGetLastError();

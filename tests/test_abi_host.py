@@ -145,6 +145,25 @@ def test_argument_gate(L, over, code):
     assert _call(L, **over) == code
 
 
+def _call_strided(L, strides):
+    P = ctypes.c_void_p
+    return L.kda_chunk_prefill_fwd_strided(
+        P(0x10000), P(0x20000), P(0x30000), P(0x40000), P(0x50000), P(0x60000), P(0x70000),
+        -5.0, 128 ** -0.5, P(0x80000), P(0x90000), P(0xA0000), P(0xB0000), 0, P(0xC0000),
+        P(None), 64, 1, 2, kda.workspace_size(64, 2, 1), *strides, -1, 0)
+
+
+@pytest.mark.parametrize("strides,code", [
+    ((255, 256, 256, 256, 2), kda.ERR_INVALID_ARG),      # q rows overlap (H * 128 = 256)
+    ((256, 256, 256, 256, 1), kda.ERR_INVALID_ARG),      # beta rows overlap (H = 2)
+    ((260, 256, 256, 256, 2), kda.ERR_MISALIGNED),       # 16-byte TMA rows: multiple of 8
+    ((256, 256, 260, 256, 2), kda.ERR_MISALIGNED),
+    ((0, 256, 256, 256, 2), kda.ERR_INVALID_ARG),
+])
+def test_strided_argument_gate(L, strides, code):
+    assert _call_strided(L, strides) == code
+
+
 def test_valid_arguments_reach_the_device_check(L):
     """Valid arguments pass validation; without an sm_103 GPU the call then
     stops at the device check and enqueues nothing."""

@@ -203,6 +203,35 @@ def test_extreme_gates(oracle_mod, kernel, lb, shift):
     check(oracle_mod, inp, out, fin, tag=f"gates lb={lb} shift={shift} k{kernel}")
 
 
+@pytest.mark.parametrize("kernel", KERNELS)
+def test_strided_inputs_equal_dense(kernel):
+    """q, k, v, g as views into one fused [T, 4 * H * 128 + 64] buffer and beta as a view
+    into a wider [T, H + 3] buffer: the strided entry point gives exactly what the dense
+    call gives (the same arithmetic on the same values)."""
+    inp = W.make_inputs(W.custom([130, 64, 1, 77], 2, seed=35))
+    d = to_dev(inp)
+    T, H, D = d["q"].shape
+    fused = torch.zeros(T, 4 * H * D + 64, dtype=torch.bfloat16, device="cuda")
+    views = {}
+    for j, name in enumerate(("q", "k", "v", "g")):
+        fused[:, j * H * D:(j + 1) * H * D] = d[name].reshape(T, H * D)
+        views[name] = fused[:, j * H * D:(j + 1) * H * D].view(T, H, D)
+    wide = torch.zeros(T, H + 3, dtype=torch.bfloat16, device="cuda")
+    wide[:, 1:H + 1] = d["beta"]
+    views["beta"] = wide[:, 1:H + 1]
+    assert not views["q"].is_contiguous() and not views["beta"].is_contiguous()
+    ws = split_workspace(T, H, d["cu_seqlens"].numel() - 1) if kernel == kda.KERNEL_SPLIT else None
+    outs = []
+    for src in (d, views):
+        o, f = kda.chunk_prefill_fwd(src["q"], src["k"], src["v"], src["g"], src["beta"],
+                                     d["A_log"], d["dt_bias"], d["lower_bound"], d["scale"],
+                                     d["initial_state"], d["cu_seqlens"], workspace=ws,
+                                     kernel=kernel)
+        torch.cuda.synchronize()
+        outs.append((o.clone(), f.clone()))
+    assert torch.equal(outs[0][0], outs[1][0]) and torch.equal(outs[0][1], outs[1][1])
+
+
 # ----------------------------------------------------------------- edge cases
 def test_inplace_state_update(oracle_mod):
     inp = W.make_inputs(W.custom([90, 40], 2, seed=23))
