@@ -181,6 +181,29 @@ int kda_chunk_prefill_fwd_strided(const void* q, const void* k, const void* v, c
                                   int vsplit, int kernel);
 
 /*
+ * Token-by-token KDA for decode and speculative-verify steps, where each
+ * sequence brings a few tokens (1..k): the recurrent form of the same
+ * operation, on the same state layout and dtypes, so a sequence can switch
+ * between prefill and decode calls freely.  The pages route speculative
+ * tokens through this recurrent form so that a rejected draft can be rolled
+ * back via num_accepted_tokens (PR #55737, Discussion and Features &
+ * motivation).  Arguments are those of kda_chunk_prefill_fwd (dense
+ * inputs), plus `token_states`: NULL, or [T, H, 128, 128] in state_dtype,
+ * which receives the state after every token -- a caller that accepts the
+ * first m draft tokens of a sequence continues from the entry of its m-th
+ * token.  The workspace needs only the 256 bytes of status words.  One CTA
+ * per (sequence, head, 32 value columns); the time is the state's read and
+ * write (plus the token states, if asked for).
+ */
+int kda_recurrent_fwd(const void* q, const void* k, const void* v, const void* g,
+                      const void* beta, const float* A_log, const float* dt_bias,
+                      float lower_bound, float scale, const void* initial_state,
+                      const int32_t* cu_seqlens, void* out, void* final_state, int state_dtype,
+                      void* token_states, void* workspace, kda_stream_t stream,
+                      int64_t total_tokens, int32_t num_seqs, int32_t heads,
+                      size_t workspace_bytes);
+
+/*
  * The value-dimension split factor the automatic path uses for a batch of
  * `num_seqs` sequences and `heads` heads on a GPU with `sm_count` SMs.
  * The trigger is PR #52458's: split only when 2 * heads * num_seqs <=

@@ -46,7 +46,7 @@ ERR_CUDA = -9
 EXPORTS = ("kda_workspace_size", "kda_chunk_prefill_fwd", "kda_chunk_prefill_fwd_ex",
            "kda_choose_vsplit", "kda_status_string", "kda_last_device_status",
            "kda_device_check", "kda_plan", "kda_chunk_prefill_fwd_strided",
-           "kda_chunk_prefill_fwd_noalloc")
+           "kda_recurrent_fwd", "kda_chunk_prefill_fwd_noalloc")
 
 _lib = None
 _lock = threading.Lock()
@@ -89,6 +89,9 @@ def lib() -> ctypes.CDLL:
             L.kda_last_device_status.argtypes = [P, P]
             L.kda_device_check.restype = ctypes.c_int
             L.kda_device_check.argtypes = [ctypes.c_int]
+            L.kda_recurrent_fwd.restype = ctypes.c_int
+            L.kda_recurrent_fwd.argtypes = [P, P, P, P, P, P, P, F, F, P, P, P, P, ctypes.c_int,
+                                            P, P, P, I64, I32, I32, SZ]
             L.kda_plan.restype = ctypes.c_int
             L.kda_plan.argtypes = [I64, I32, I32, SZ, ctypes.c_int, ctypes.c_int, P, P, P]
             L.kda_chunk_prefill_fwd_noalloc.restype = ctypes.c_int
@@ -227,6 +230,60 @@ def chunk_prefill_fwd(q, k, v, g, beta, A_log, dt_bias, lower_bound, scale,
     if squeeze:
         out = out.unsqueeze(0)
     return out, final_state
+
+
+def recurrent_fwd(q, k, v, g, beta, A_log, dt_bias, lower_bound, scale, initial_state,
+                  cu_seqlens, out=None, final_state=None, token_states=False, workspace=None,
+                  state_dtype=None, stream=None):
+    """Run ``kda_recurrent_fwd`` (decode / speculative verify: a few tokens per sequence).
+
+    Same tensors as chunk_prefill_fwd (dense).  token_states: False (none), True (allocate
+    [T, H, 128, 128] in the state dtype) or a tensor to fill with the state after every
+    token.  Returns (out, final_state, token_states or None).
+    """
+    if q.dim() == 4:
+        q, k, v, g = (x.view(x.shape[1:]) for x in (q, k, v, g))
+        if beta.dim() == 3:
+            beta = beta.view(beta.shape[1:])
+    T, H, D = q.shape
+    N = cu_seqlens.numel() - 1
+    for name, t in (("q", q), ("k", k), ("v", v), ("g", g)):
+        _need(t, name, torch.bfloat16, (T, H, D))
+    _need(beta, "beta", torch.bfloat16, (T, H))
+    _need(A_log, "A_log", torch.float32, (H,))
+    _need(dt_bias, "dt_bias", torch.float32, (H, D))
+    _need(cu_seqlens, "cu_seqlens", torch.int32, (N + 1,))
+    if state_dtype is None:
+        state_dtype = initial_state.dtype if initial_state is not None else torch.float32
+    sd = {torch.float32: STATE_F32, torch.bfloat16: STATE_BF16}.get(state_dtype)
+    if sd is None:
+        raise TypeError("state dtype must be float32 or bfloat16")
+    if initial_state is not None:
+        _need(initial_state, "initial_state", state_dtype, (N, H, D, D))
+    if out is None:
+        out = torch.empty((T, H, D), dtype=torch.bfloat16, device=q.device)
+    _need(out, "out", torch.bfloat16, (T, H, D))
+    if final_state is None:
+        final_state = torch.empty((N, H, D, D), dtype=state_dtype, device=q.device)
+    _need(final_state, "final_state", state_dtype, (N, H, D, D))
+    if token_states is True:
+        token_states = torch.empty((T, H, D, D), dtype=state_dtype, device=q.device)
+    elif token_states is False:
+        token_states = None
+    if token_states is not None:
+        _need(token_states, "token_states", state_dtype, (T, H, D, D))
+    if workspace is None:
+        workspace = torch.zeros(256, dtype=torch.uint8, device=q.device)
+    _need(workspace, "workspace", torch.uint8)
+    s = stream if stream is not None else torch.cuda.current_stream(q.device)
+    rc = lib().kda_recurrent_fwd(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(A_log), _ptr(dt_bias),
+        float(lower_bound), float(scale), _ptr(initial_state), _ptr(cu_seqlens), _ptr(out),
+        _ptr(final_state), sd, _ptr(token_states), _ptr(workspace),
+        ctypes.c_void_p(s.cuda_stream), int(T), int(N), int(H), int(workspace.numel()))
+    if rc != OK:
+        raise KDAError(rc, "kda_recurrent_fwd")
+    return out, final_state, token_states
 
 
 def chunk_prefill_fwd_noalloc(q, k, v, g, beta, A_log, dt_bias, lower_bound, scale,

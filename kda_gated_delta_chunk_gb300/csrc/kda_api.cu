@@ -234,6 +234,57 @@ int kda_chunk_prefill_fwd_strided(const void* q, const void* k, const void* v, c
                   num_seqs, heads, workspace_bytes, vsplit, kernel, strides);
 }
 
+int kda_recurrent_fwd(const void* q, const void* k, const void* v, const void* g,
+                      const void* beta, const float* A_log, const float* dt_bias,
+                      float lower_bound, float scale, const void* initial_state,
+                      const int32_t* cu_seqlens, void* out, void* final_state, int state_dtype,
+                      void* token_states, void* workspace, kda_stream_t stream,
+                      int64_t total_tokens, int32_t num_seqs, int32_t heads,
+                      size_t workspace_bytes) {
+  int rc = validate(q, k, v, g, beta, A_log, dt_bias, lower_bound, scale, initial_state,
+                    cu_seqlens, out, final_state, state_dtype, workspace, total_tokens,
+                    num_seqs, heads, workspace_bytes);
+  if (rc != KDA_OK) return rc;
+  if (token_states && !aligned(token_states, 16)) return KDA_ERR_MISALIGNED;
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return KDA_ERR_CUDA;
+  }
+  rc = check_device(dev, &sms);
+  if (rc != KDA_OK) return rc;
+  if (num_seqs == 0) return KDA_OK;
+  kda::Params p;
+  p.q = static_cast<const __nv_bfloat16*>(q);
+  p.k = static_cast<const __nv_bfloat16*>(k);
+  p.v = static_cast<const __nv_bfloat16*>(v);
+  p.g = static_cast<const __nv_bfloat16*>(g);
+  p.beta = static_cast<const __nv_bfloat16*>(beta);
+  p.A_log = A_log;
+  p.dt_bias = dt_bias;
+  p.lower_bound = lower_bound;
+  p.scale = scale;
+  p.initial_state = initial_state;
+  p.cu_seqlens = cu_seqlens;
+  p.out = static_cast<__nv_bfloat16*>(out);
+  p.final_state = final_state;
+  p.state_bf16 = state_dtype == KDA_STATE_BF16 ? 1 : 0;
+  p.status = static_cast<int*>(workspace);
+  p.total_tokens = total_tokens;
+  p.num_seqs = num_seqs;
+  p.heads = heads;
+  p.vsplit = 1;
+  p.sm_count = sms;
+  p.s_q = p.s_k = p.s_v = p.s_g = (int64_t)heads * kda::kHeadDim;
+  p.s_beta = heads;
+  if (kda::launch_recurrent(p, token_states, reinterpret_cast<cudaStream_t>(stream)) !=
+      cudaSuccess) {
+    cudaGetLastError();
+    return KDA_ERR_LAUNCH_FAILED;
+  }
+  return KDA_OK;
+}
+
 int kda_choose_vsplit(int32_t num_seqs, int32_t heads, int32_t sm_count) {
   if (num_seqs <= 0 || heads <= 0 || sm_count <= 0) return 1;
   const int64_t units = (int64_t)num_seqs * heads;

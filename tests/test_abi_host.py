@@ -171,3 +171,17 @@ def test_valid_arguments_reach_the_device_check(L):
     import torch
     if not torch.cuda.is_available():
         assert rc in (kda.ERR_CUDA, kda.ERR_UNSUPPORTED_DEVICE)
+
+
+def test_recurrent_argument_gate(L):
+    """kda_recurrent_fwd refuses bad arguments on the host, before any device work."""
+    P = ctypes.c_void_p
+    base = [P(0x10000), P(0x20000), P(0x30000), P(0x40000), P(0x50000), P(0x60000),
+            P(0x70000), -5.0, 128 ** -0.5, P(0x80000), P(0x90000), P(0xA0000), P(0xB0000), 0]
+    assert L.kda_recurrent_fwd(*base, P(0xD0004), P(0xC0000), P(None), 4, 1, 2, 256) == \
+        kda.ERR_MISALIGNED                                   # token_states not 16-byte aligned
+    assert L.kda_recurrent_fwd(*base, P(None), P(0xC0000), P(None), 4, 1, 2, 8) == \
+        kda.ERR_WORKSPACE_TOO_SMALL
+    base[7] = -7.0
+    assert L.kda_recurrent_fwd(*base, P(None), P(0xC0000), P(None), 4, 1, 2, 256) == \
+        kda.ERR_UNSAFE_LOWER_BOUND
