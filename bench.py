@@ -244,6 +244,60 @@ def run_reference(args, w):
     print(json.dumps(line), flush=True)
 
 
+def run_decode(args):
+    """Decode / speculative-verify step through kda_recurrent_fwd: 64 sequences x K tokens,
+    H = 32, fp32 state.  The time is bound by reading and writing the state."""
+    import kda_gated_delta_chunk_gb300 as kda
+    from kda_gated_delta_chunk_gb300 import build as kbuild
+    kbuild.build()
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    K, N, H = args.decode, 64, 32
+    w = W.custom([K] * N, H, seed=61)
+    host = W.make_inputs(w)
+    NB = 4
+    sets = []
+    for _ in range(NB):
+        d = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in host.items()}
+        d["out"] = torch.empty_like(d["q"])
+        d["fin"] = torch.empty_like(d["initial_state"])
+        d["ws"] = torch.zeros(256, dtype=torch.uint8, device=dev)
+        sets.append(d)
+    stream = torch.cuda.Stream(dev)
+
+    def step(i):
+        d = sets[i % NB]
+        kda.recurrent_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], d["A_log"], d["dt_bias"],
+                          d["lower_bound"], d["scale"], d["initial_state"], d["cu_seqlens"],
+                          out=d["out"], final_state=d["fin"], workspace=d["ws"], stream=stream)
+    for i in range(max(3, args.warmup)):
+        step(i)
+    stream.synchronize()
+    steps = args.steps if args.steps > 0 else 200
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(steps):
+        step(i)
+    e1.record(stream)
+    e1.synchronize()
+    t = e0.elapsed_time(e1) / 1e3 / steps
+    T = N * K
+    abytes = T * H * (5 * 2 * D + 2) + 2 * N * H * D * D * 4 + H * (D + 1) * 4 + (N + 1) * 4
+    hbm, _, peak_kind = load_peaks()
+    line = {"metric": "KDA decode step (recurrent form)", "value": T / t, "unit": UNIT,
+            "n_gpus": 1, "steps": steps, "warmup": args.warmup, "ms_per_step": 1e3 * t,
+            "higher_is_better": True, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": f"decode_{N}x{K}_h{H}", "seqs": N, "tokens_per_seq": K,
+                       "heads": H, "head_dim": D, "state": "f32",
+                       "l2": f"{abytes / 1e6:.0f} MB per step, 4 input sets rotated"},
+            "roofline": {"bound": "hbm", "kernel": "kda_recurrent_kernel",
+                         "achieved": abytes / t / 1e9, "peak": hbm, "unit": "GB/s",
+                         "frac": abytes / t / 1e9 / hbm, "algorithmic_bytes_per_launch": abytes,
+                         "peak_source": peak_kind},
+            "gpu_launches": steps}
+    print(json.dumps(line), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -256,7 +310,11 @@ def main():
     ap.add_argument("--vsplit", type=int, default=-1, help="-1 automatic, or 1/2/4/8")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=10)
+    ap.add_argument("--decode", type=int, default=0,
+                    help="time a decode step (kda_recurrent_fwd) with this many tokens per sequence")
     args = ap.parse_args()
+    if args.decode > 0:
+        return run_decode(args)
     w = W.workload(args.workload, args.n) if args.workload == 3 else W.workload(args.workload)
     if args.impl == "reference":
         if args.steps <= 0:
