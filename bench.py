@@ -293,7 +293,8 @@ def run_decode(args):
             "roofline": {"bound": "hbm", "kernel": "kda_recurrent_kernel",
                          "achieved": abytes / t / 1e9, "peak": hbm, "unit": "GB/s",
                          "frac": abytes / t / 1e9 / hbm, "algorithmic_bytes_per_launch": abytes,
-                         "peak_source": peak_kind},
+                         "peak_source": peak_kind,
+                         "traffic": load_traffic("kda_recurrent_kernel", f"decode_{N}x{K}_h{H}")},
             "gpu_launches": steps}
     print(json.dumps(line), flush=True)
 
