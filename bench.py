@@ -305,7 +305,7 @@ def main():
     ap.add_argument("--steps", type=int, default=0, help="timed steps (0: ~1.5 s worth)")
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--kernel", default="auto", choices=["auto", "tc", "split", "ref"])
+    ap.add_argument("--kernel", default="auto", choices=["auto", "tc", "helpers", "split", "ref"])
     ap.add_argument("--workload", type=int, default=1)
     ap.add_argument("--n", type=int, default=None, help="sequences of the V-split workload (3)")
     ap.add_argument("--vsplit", type=int, default=-1, help="-1 automatic, or 1/2/4/8")
@@ -330,7 +330,7 @@ def main():
     barrier(world)
     kbuild.build()
     kernel = {"auto": kda.KERNEL_AUTO, "tc": kda.KERNEL_TC, "ref": kda.KERNEL_REF,
-              "split": kda.KERNEL_SPLIT}[args.kernel]
+              "split": kda.KERNEL_SPLIT, "helpers": kda.KERNEL_TC_HELPERS}[args.kernel]
     dev = torch.device("cuda", torch.cuda.current_device())
     rc = kda.device_check(dev.index)
     if rc != kda.OK:
@@ -347,8 +347,8 @@ def main():
             d["out"] = torch.empty_like(d["q"])
             d["fin"] = torch.empty_like(d["initial_state"])
             d["ws"] = kda.alloc_workspace(T, H, N, device=dev)
-            if kernel == kda.KERNEL_SPLIT:   # records for every chunk slot of this batch
-                n_ws = 1024 + ((T + 63) // 64 + N) * H * 66560
+            if kernel in (kda.KERNEL_SPLIT, kda.KERNEL_TC_HELPERS):   # records (+ claim words)
+                n_ws = 1024 + ((T + 63) // 64 + N) * H * (66560 + 4)
                 d["ws"] = torch.zeros(max(n_ws, d["ws"].numel()), dtype=torch.uint8, device=dev)
             sets.append(d)
     stream.synchronize()
@@ -479,7 +479,7 @@ def main():
         return
 
     kernel_name = {kda.KERNEL_TC: "kda_tc_chunk_kernel", kda.KERNEL_REF: "kda_ref_chunk_kernel",
-                   kda.KERNEL_SPLIT: "kda_split_path"}[path]
+                   kda.KERNEL_SPLIT: "kda_split_path", kda.KERNEL_TC_HELPERS: "kda_tc_helpers_path"}[path]
     hbm, tflops, peak_kind = load_peaks()
     abytes = algorithmic_bytes(w)
     achieved = abytes / mean_launch / 1e9

@@ -88,7 +88,10 @@ typedef struct CUstream_st* kda_stream_t;
 
 /* kernel selectors for kda_chunk_prefill_fwd_ex */
 #define KDA_KERNEL_AUTO 0  /* SPLIT when the value split triggers and the
-                              workspace holds its records, else TC          */
+                              workspace holds its records; else TC_HELPERS
+                              when at least 8 SMs stay free, N <= 128, the
+                              sequences average 4 or more chunks and the
+                              workspace holds the records; else TC          */
 #define KDA_KERNEL_TC 1    /* fused tcgen05 + TMA chunk kernel, C = 64: one CTA
                               per (sequence, head[, value slice])            */
 #define KDA_KERNEL_REF 2   /* plain-CUDA-core chunk kernel (GPU parity aid)    */
@@ -97,6 +100,12 @@ typedef struct CUstream_st* kda_stream_t;
                               the workspace, then one chain CTA per (sequence,
                               head, value slice of 128 / P columns); P = 1 runs
                               the chain on tcgen05 with the state in TMEM   */
+#define KDA_KERNEL_TC_HELPERS 4 /* TC (P = 1) plus k-side helper CTAs on the SMs
+                              it leaves free: they write records for chunks
+                              taken from the end of each sequence, which the
+                              fused CTAs then read instead of computing them;
+                              needs N * heads < SM count and the records'
+                              workspace                                      */
 
 /*
  * Bytes of device workspace a call needs for up to `total_tokens` tokens,
@@ -108,12 +117,14 @@ typedef struct CUstream_st* kda_stream_t;
  * The workspace starts with the device status word (256 bytes: all the
  * fused kernel needs).  When some batch of up to max_seqs sequences would
  * take the value split on the current device (2 * heads * N <= SM count;
- * 152 SMs are assumed when no device answers), it also holds the split
- * path's records: 66,560 bytes per (chunk slot, head), with
- * ceil(total_tokens / 64) + N slots for the largest such N -- about 1 KB
- * per token-head.  A smaller workspace (at least 256 bytes) is accepted;
- * KDA_KERNEL_AUTO then runs the fused kernel.  Always a multiple of 16;
- * 0 for negative arguments.
+ * 152 SMs are assumed when no device answers) or leave at least 8 SMs to
+ * k-side helpers (heads * N + 8 <= SM count), it also holds the records of
+ * those paths: a 1 KB header, then 66,560 bytes per (chunk slot, head),
+ * with ceil(total_tokens / 64) + N slots for the largest such N -- about
+ * 1 KB per token-head -- and, for the helpers, one int32 claim word per
+ * (chunk slot, head).  A smaller workspace (at least 256 bytes) is
+ * accepted; KDA_KERNEL_AUTO then runs the fused kernel alone.  Always a
+ * multiple of 16; 0 for negative arguments.
  */
 size_t kda_workspace_size(int64_t total_tokens, int32_t heads, int32_t max_seqs);
 
@@ -145,7 +156,10 @@ int kda_chunk_prefill_fwd(const void* q, const void* k, const void* v, const voi
  * `kernel` one of KDA_KERNEL_*.  Other values give KDA_ERR_INVALID_ARG.
  * KDA_KERNEL_SPLIT needs room for its records: 1024 + 66,560 bytes per
  * (chunk slot, head) with ceil(total_tokens / 64) + num_seqs slots, else
- * KDA_ERR_WORKSPACE_TOO_SMALL.
+ * KDA_ERR_WORKSPACE_TOO_SMALL.  KDA_KERNEL_TC_HELPERS needs the same plus
+ * 4 bytes per (chunk slot, head), vsplit -1 or 1 (else
+ * KDA_ERR_INVALID_ARG), num_seqs * heads below the SM count and num_seqs
+ * <= 128 (else KDA_ERR_INVALID_ARG).
  */
 int kda_chunk_prefill_fwd_ex(const void* q, const void* k, const void* v, const void* g,
                              const void* beta, const float* A_log, const float* dt_bias,
@@ -231,8 +245,8 @@ int kda_device_check(int device);
 /*
  * The path a kda_chunk_prefill_fwd_ex call with these sizes, workspace size
  * and selectors would take on the current device, without enqueuing
- * anything: *kernel_out gets KDA_KERNEL_TC, KDA_KERNEL_SPLIT or
- * KDA_KERNEL_REF (AUTO resolved), *vsplit_out the value split factor P and
+ * anything: *kernel_out gets KDA_KERNEL_TC, KDA_KERNEL_TC_HELPERS,
+ * KDA_KERNEL_SPLIT or KDA_KERNEL_REF (AUTO resolved), *vsplit_out the value split factor P and
  * *launches_out the number of kernels the call enqueues (0, 1 or 2); any
  * output pointer may be NULL.  Returns the code such a call would return
  * for its sizes, selectors and workspace size (pointer checks aside), or

@@ -9,8 +9,13 @@ names follow the C ABI in ``include/kda.h``:
                       initial_state, cu_seqlens, out=None, final_state=None,
                       workspace=None, ...) -> (out, final_state)
     choose_vsplit(num_seqs, heads, sm_count) -> int
+    chunk_prefill_fwd(..., vsplit=-1, kernel=KERNEL_AUTO): strided views of q, k, v, g,
+        beta are passed through kda_chunk_prefill_fwd_strided
+    recurrent_fwd(q, k, v, g, beta, A_log, dt_bias, lower_bound, scale, initial_state,
+                  cu_seqlens, token_states=False, ...) -> (out, final_state, token_states)
     plan(total_tokens, num_seqs, heads, workspace_bytes, vsplit, kernel)
         -> (kernel, vsplit, launches)
+    KERNEL_AUTO / KERNEL_TC / KERNEL_TC_HELPERS / KERNEL_SPLIT / KERNEL_REF
     last_device_status(workspace) -> int
     status_string(code) -> str
 
@@ -30,7 +35,7 @@ LIB_PATH = os.path.join(_PKG, "libkda.so")
 
 HEAD_DIM = 128
 STATE_F32, STATE_BF16 = 0, 1
-KERNEL_AUTO, KERNEL_TC, KERNEL_REF, KERNEL_SPLIT = 0, 1, 2, 3
+KERNEL_AUTO, KERNEL_TC, KERNEL_REF, KERNEL_SPLIT, KERNEL_TC_HELPERS = 0, 1, 2, 3, 4
 OK = 0
 ERR_INVALID_ARG = -1
 ERR_UNSUPPORTED_DEVICE = -2

@@ -74,22 +74,37 @@ int plan(int64_t total_tokens, int32_t num_seqs, int32_t heads, size_t workspace
   if (vsplit != -1 && vsplit != 1 && vsplit != 2 && vsplit != 4 && vsplit != 8)
     return KDA_ERR_INVALID_ARG;
   if (kernel != KDA_KERNEL_AUTO && kernel != KDA_KERNEL_TC && kernel != KDA_KERNEL_REF &&
-      kernel != KDA_KERNEL_SPLIT)
+      kernel != KDA_KERNEL_SPLIT && kernel != KDA_KERNEL_TC_HELPERS)
     return KDA_ERR_INVALID_ARG;
   const size_t split_need = kda::split_workspace_bytes(total_tokens, heads, num_seqs);
+  const size_t help_need = kda::helper_workspace_bytes(total_tokens, heads, num_seqs);
   int P = vsplit == -1 ? kda_choose_vsplit(num_seqs, heads, sms) : vsplit;
   if (kernel == KDA_KERNEL_SPLIT) {
     if (workspace_bytes < split_need) return KDA_ERR_WORKSPACE_TOO_SMALL;
+  } else if (kernel == KDA_KERNEL_TC_HELPERS) {
+    if (vsplit != -1 && vsplit != 1) return KDA_ERR_INVALID_ARG;
+    if ((int64_t)num_seqs * heads >= sms || num_seqs > kda::kHelperMaxSeqs ||
+        ((total_tokens + kda::kChunk - 1) / kda::kChunk) * num_seqs * heads >= ((int64_t)1 << 30))
+      return KDA_ERR_INVALID_ARG;
+    if (workspace_bytes < help_need) return KDA_ERR_WORKSPACE_TOO_SMALL;
+    P = 1;
   } else if (kernel == KDA_KERNEL_AUTO) {
-    if (P > 1 && workspace_bytes >= split_need && total_tokens > 0)
+    if (P > 1 && workspace_bytes >= split_need && total_tokens > 0) {
       kernel = KDA_KERNEL_SPLIT;
-    else {
+    } else {
       kernel = KDA_KERNEL_TC;
       if (vsplit == -1) P = 1;
+      // the fused kernel leaves SMs free: helpers take the far ends of the sequences
+      if (P == 1 && num_seqs > 0 && num_seqs <= kda::kHelperMaxSeqs &&
+          (int64_t)num_seqs * heads + kda::kHelperMinFreeSms <= sms &&
+          ((total_tokens + kda::kChunk - 1) / kda::kChunk) * num_seqs * heads < ((int64_t)1 << 30) &&
+          total_tokens >= (int64_t)4 * kda::kChunk * num_seqs && workspace_bytes >= help_need)
+        kernel = KDA_KERNEL_TC_HELPERS;
     }
   }
   int launches = num_seqs == 0 ? 0 : 1;
   if (kernel == KDA_KERNEL_SPLIT && num_seqs > 0) launches = total_tokens > 0 ? 2 : 1;
+  if (kernel == KDA_KERNEL_TC_HELPERS && num_seqs > 0 && total_tokens > 0) launches = 2;
   if (kernel_out) *kernel_out = kernel;
   if (vsplit_out) *vsplit_out = P;
   if (launches_out) *launches_out = launches;
@@ -121,7 +136,7 @@ int fwd_impl(const void* q, const void* k, const void* v, const void* g, const v
   if (vsplit != -1 && vsplit != 1 && vsplit != 2 && vsplit != 4 && vsplit != 8)
     return KDA_ERR_INVALID_ARG;
   if (kernel != KDA_KERNEL_AUTO && kernel != KDA_KERNEL_TC && kernel != KDA_KERNEL_REF &&
-      kernel != KDA_KERNEL_SPLIT)
+      kernel != KDA_KERNEL_SPLIT && kernel != KDA_KERNEL_TC_HELPERS)
     return KDA_ERR_INVALID_ARG;
   int dev = 0, sms = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) {
@@ -136,7 +151,7 @@ int fwd_impl(const void* q, const void* k, const void* v, const void* g, const v
   if (rc != KDA_OK) return rc;
   if (num_seqs == 0) return KDA_OK;
 
-  kda::Params p;
+  kda::Params p{};
   p.q = static_cast<const __nv_bfloat16*>(q);
   p.k = static_cast<const __nv_bfloat16*>(k);
   p.v = static_cast<const __nv_bfloat16*>(v);
@@ -162,6 +177,7 @@ int fwd_impl(const void* q, const void* k, const void* v, const void* g, const v
   p.s_v = st[2];
   p.s_g = st[3];
   p.s_beta = st[4];
+  p.helpers = (kernel == KDA_KERNEL_TC_HELPERS && total_tokens > 0) ? 1 : 0;
 
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   cudaError_t err = (kernel == KDA_KERNEL_REF)     ? kda::launch_ref(p, s)
@@ -192,7 +208,14 @@ size_t kda_workspace_size(int64_t total_tokens, int32_t heads, int32_t max_seqs)
     const int32_t n_split = (int32_t)std::min<int64_t>(max_seqs, sms / (2 * (int64_t)heads));
     need = std::max(need, kda::split_workspace_bytes(total_tokens, heads, n_split));
   }
-  return need;
+  // ... and for the fused kernel's k-side helpers: N * heads + 8 <= SMs
+  if (heads > 0 && total_tokens > 0 && max_seqs > 0 &&
+      (int64_t)heads + kda::kHelperMinFreeSms <= sms) {
+    const int32_t n_help = (int32_t)std::min<int64_t>(
+        std::min<int64_t>(max_seqs, kda::kHelperMaxSeqs), (sms - kda::kHelperMinFreeSms) / (int64_t)heads);
+    need = std::max(need, kda::helper_workspace_bytes(total_tokens, heads, n_help));
+  }
+  return (need + 15) & ~(size_t)15;
 }
 
 int kda_chunk_prefill_fwd(const void* q, const void* k, const void* v, const void* g,
@@ -254,7 +277,7 @@ int kda_recurrent_fwd(const void* q, const void* k, const void* v, const void* g
   rc = check_device(dev, &sms);
   if (rc != KDA_OK) return rc;
   if (num_seqs == 0) return KDA_OK;
-  kda::Params p;
+  kda::Params p{};
   p.q = static_cast<const __nv_bfloat16*>(q);
   p.k = static_cast<const __nv_bfloat16*>(k);
   p.v = static_cast<const __nv_bfloat16*>(v);

@@ -55,6 +55,8 @@ struct Params {
   // token strides in elements: q/k/v/g element (t, h, d) at t * s + h * 128 + d, beta (t, h)
   // at t * s_beta + h (dense: s = H * 128, s_beta = H)
   int64_t s_q, s_k, s_v, s_g, s_beta;
+  // 1: the fused kernel shares the chunk-local work with k-side helper CTAs (P = 1 only)
+  int32_t helpers;
 };
 
 // Record a device-side error (first writer wins) with its block and site.
@@ -84,5 +86,32 @@ __host__ __device__ inline int64_t split_slots(int64_t total_tokens, int32_t num
 inline size_t split_workspace_bytes(int64_t total_tokens, int32_t heads, int32_t num_seqs) {
   return (size_t)kSplitHeader + (size_t)split_slots(total_tokens, num_seqs) * heads * kRecBytes;
 }
+
+// Fused kernel with k-side helpers: the fused CTAs (one per sequence and head) walk their
+// chunks forward; helper CTAs on the remaining SMs write records for chunks taken from
+// the far end, newest chunk index first.  One claim word per (slot, head) item follows
+// the records: 0 free, 1 taken by a helper, 2 its record is written, 3 taken by the
+// sequence's own CTA (indexed by claim_index).  The helpers' item counter sits in the header.
+constexpr int kClaimFree = 0, kClaimHelper = 1, kClaimReady = 2, kClaimOwn = 3;
+constexpr int kHelperCounterWord = 128;   // int index in the workspace header
+constexpr int kHelperMinFreeSms = 8;      // helpers only with at least this many free SMs
+constexpr int kHelperMaxSeqs = 128;       // ... and at most this many sequences
+__host__ __device__ inline size_t helper_claims_offset(int64_t total_tokens, int32_t heads,
+                                                       int32_t num_seqs) {
+  return (size_t)kSplitHeader + (size_t)split_slots(total_tokens, num_seqs) * heads * kRecBytes;
+}
+// Claim word of item (slot, head): head-major, so the words that the CTAs of different
+// sequences and heads claim at the same moment (the same chunk index) sit in different
+// cache lines rather than contending for one.
+__host__ __device__ inline int64_t claim_index(int64_t slot, int32_t head, int64_t total_tokens,
+                                               int32_t num_seqs) {
+  return (int64_t)head * split_slots(total_tokens, num_seqs) + slot;
+}
+inline size_t helper_workspace_bytes(int64_t total_tokens, int32_t heads, int32_t num_seqs) {
+  return helper_claims_offset(total_tokens, heads, num_seqs) +
+         (size_t)split_slots(total_tokens, num_seqs) * heads * sizeof(int);
+}
+// k-side helpers launched behind the fused kernel (programmatic dependent launch)
+cudaError_t launch_kside_helpers(const Params& p, cudaStream_t stream);
 
 }  // namespace kda

@@ -18,6 +18,11 @@
 // 128 TMEM columns per CTA, two CTAs per SM, persistent over the (slot, head)
 // items; the record tiles go straight from registers to global memory as 16-byte
 // chunks of the swizzled images.
+//
+// Helper mode (KDA_KERNEL_TC_HELPERS): launched behind the fused kernel on the SMs
+// it leaves free, the CTAs take items from a shared counter, last chunk index
+// first, claim each as they start it and publish the record with a release
+// store; the first claim lost to the sequence's own CTA ends a helper.
 #include <cuda.h>
 
 #include "kda_internal.cuh"
@@ -55,13 +60,15 @@ constexpr int K_TSLOT = K_MISC + 7440;
 constexpr int K_FLAGS = K_MISC + 7456;    // items {item, c0, t1, head, k} x 3, 8 ints apart
 constexpr int K_SGD = K_MISC + 7552;      // gate terms -e^{A_log} log2e dt_bias [128], -e^{A_log} log2e
 constexpr int K_RSC = K_MISC + 8192;      // per-row power-of-two operand scales, bf16x2 [q 64][k 64]
+constexpr int K_MAXC = K_MISC + 8176;     // helper mode: chunks of the longest sequence
 constexpr int K_CU = K_RSC + 512;         // cu_seqlens cache (batches of up to kCuCache sequences)
 constexpr int kCuCache = 1023;
-constexpr int K_SMEM_USED = K_CU + 4 * (kCuCache + 1);
+constexpr int K_ORD = K_CU + 4 * (kCuCache + 1);   // helper mode: sequences, longest first
+constexpr int K_SMEM_USED = K_ORD + 4 * kHelperMaxSeqs;
 constexpr int K_SMEM_BYTES = K_SMEM_USED + 1024;
 static_assert(K_Y + 32 * NS * 4 <= K_RKQ, "T scratch overlaps [Kr; Qr]");
 static_assert(K_NM + 64 * NS * 4 <= K_TB, "N overlaps T diag(b)");
-static_assert(K_FLAGS + 24 * 4 <= K_SGD && K_SGD + 129 * 4 <= K_CU, "misc");
+static_assert(K_FLAGS + 24 * 4 <= K_SGD && K_SGD + 129 * 4 <= K_MAXC && K_MAXC + 4 <= K_RSC, "misc");
 static_assert(2 * (K_SMEM_BYTES + 1024) <= 228 * 1024, "two CTAs per SM");
 
 constexpr uint32_t TM_D = 0;      // A | QK (96 cols), then W0^T at 0, W1^T at 64
@@ -110,6 +117,44 @@ __device__ void find_item(const Params& p, const int* cu, int k, int total, int*
   }
 }
 
+// Helper mode (behind the fused kernel): the next item from the shared counter, in the
+// order last chunk index first, then (sequence by decreasing length, head).  It is claimed
+// only when its processing starts.  `ord` lists the sequences longest first, so a
+// sequence without chunk `col` ends that column for every helper.
+__device__ void find_helper_item(const Params& p, const int* cu, const int* ord, int max_chunks,
+                                 int* out) {
+  out[0] = -1;
+  out[1] = out[2] = out[3] = out[4] = 0;
+  const int NH = p.num_seqs * p.heads;
+  int* counter = p.status + kHelperCounterWord;
+  const int limit = max_chunks * NH;   // below 2^30 (checked on the host)
+  while (true) {
+    const int idx = atomicAdd(counter, 1);
+    if (idx < 0 || idx >= limit) return;
+    const int col = max_chunks - 1 - idx / NH;
+    const int r = idx % NH;
+    const int n = ord[r / p.heads], hh = r % p.heads;
+    const int a = cu[n], b = cu[n + 1];
+    if (a < 0 || b < a || (int64_t)b > p.total_tokens) return;   // malformed: the fused kernel reports it
+    const int64_t s = (int64_t)a + (int64_t)C * col;
+    if (s >= b) {   // no chunk `col` here nor in any shorter sequence: skip to the next column
+      atomicMax(counter, (max_chunks - col) * NH);
+      continue;
+    }
+    out[0] = ((a >> 6) + n + col) * p.heads + hh;
+    out[1] = (int)s;
+    out[2] = b;
+    out[3] = hh;
+    return;
+  }
+}
+
+__device__ __forceinline__ int* helper_claim(const Params& p, int item) {
+  return reinterpret_cast<int*>(reinterpret_cast<unsigned char*>(p.status) +
+                                helper_claims_offset(p.total_tokens, p.heads, p.num_seqs)) +
+         claim_index(item / p.heads, item % p.heads, p.total_tokens, p.num_seqs);
+}
+
 // two bf16x2 words (token i: lo = channel d0, hi = channel d0 + 1) -> per-channel pairs
 __device__ __forceinline__ uint32_t lo_pair(uint32_t a, uint32_t b) { return __byte_perm(a, b, 0x5410); }
 __device__ __forceinline__ uint32_t hi_pair(uint32_t a, uint32_t b) { return __byte_perm(a, b, 0x7632); }
@@ -144,6 +189,29 @@ __global__ void __launch_bounds__(NT, 2)
     cu = cu_s;
     __syncthreads();
   }
+  // helper mode: the sequences are those of the fused kernel's batch (at most 128, so
+  // cu_seqlens is in shared memory), ranked longest first, and the chunk count of the
+  // longest (at most ceil(T / 64) even for malformed cu_seqlens)
+  int* maxc_s = reinterpret_cast<int*>(sm + K_MAXC);
+  int* ord = reinterpret_cast<int*>(sm + K_ORD);
+  if (p.helpers) {
+    const int N = p.num_seqs;
+    if (tid == 0) *maxc_s = 0;
+    __syncthreads();
+    for (int i = tid; i < N; i += NT) {
+      const int li = cu[i + 1] - cu[i];
+      int r = 0;
+      for (int m = 0; m < N; ++m) {
+        const int lm = cu[m + 1] - cu[m];
+        r += (lm > li) || (lm == li && m < i);
+      }
+      ord[r] = i;
+      atomicMax(maxc_s, (li + C - 1) / C);
+    }
+    __syncthreads();
+    if (tid == 0) *maxc_s = min(*maxc_s, (int)((p.total_tokens + C - 1) / C));
+    __syncthreads();
+  }
   if (tid == 0) {
     mbar_init(bar_in, 1);
     mbar_init(bar_mma, 1);
@@ -151,9 +219,13 @@ __global__ void __launch_bounds__(NT, 2)
     tma_prefetch_desc(&tm_q);
     tma_prefetch_desc(&tm_k);
     tma_prefetch_desc(&tm_g);
-    find_item(p, cu, 0, total, flags);
     flags[8] = -1;
-    if (flags[0] >= 0) find_item(p, cu, flags[4] + 1, total, flags + 8);
+    if (p.helpers) {   // the next item is found during T of the current one
+      find_helper_item(p, cu, reinterpret_cast<const int*>(sm + K_ORD), *reinterpret_cast<const int*>(sm + K_MAXC), flags);
+    } else {
+      find_item(p, cu, 0, total, flags);
+      if (flags[0] >= 0) find_item(p, cu, flags[4] + 1, total, flags + 8);
+    }
   }
   if (warp == 0) {
     tmem_alloc(smem_u32(tslot), TM_COLS);
@@ -218,6 +290,10 @@ __global__ void __launch_bounds__(NT, 2)
       tma_prefetch_2d(&tm_k, flags[11] * D, flags[9]);
       tma_prefetch_2d(&tm_g, flags[11] * D, flags[9]);
     }
+    // helper mode: claim the item as its processing starts; the answer is looked at after
+    // the gate phase, before anything is written to the record
+    int claimed = kClaimFree;
+    if (p.helpers && tid == 0) claimed = atomicCAS(helper_claim(p, item), kClaimFree, kClaimHelper);
     const float sg = sgd[128], sg0 = sgd[d0], sg1 = sgd[d0 + 1];
     const bool tma_ok = mbar_wait(bar_in, ph_in);
     ph_in ^= 1;
@@ -273,7 +349,10 @@ __global__ void __launch_bounds__(NT, 2)
       v[0] += __shfl_xor_sync(0xffffffffu, v[0], 1);
       if ((lane & 1) == 0) part[warp * 32 + gh * 16 + (lane >> 1)] = v[0];
     }
+    if (p.helpers && tid == 0) flags[5] = claimed;
     __syncthreads();
+    // the sequence's own CTA took this chunk first: this helper stops (nothing in flight)
+    if (p.helpers && flags[5] != kClaimFree) break;
 
     // ---- P2c: norms -> scale/|q_r|, 1/|k_r|, and a power of two 2^-s_r per row with
     //           |row| 2^-s_r <= 1.  The operands are built from the rows times 2^-s_r (exact in
@@ -501,7 +580,11 @@ __global__ void __launch_bounds__(NT, 2)
                           Tm + (32 + 16 * mi) * NS + 16 * ni, -1.0f, lane);
     } else if (tid == 128) {
       flags[16] = -1;
-      if (flags[8] >= 0) find_item(p, cu, flags[12] + 1, total, flags + 16);
+      if (p.helpers)
+        find_helper_item(p, cu, reinterpret_cast<const int*>(sm + K_ORD),
+                         *reinterpret_cast<const int*>(sm + K_MAXC), flags + 8);
+      else if (flags[8] >= 0)
+        find_item(p, cu, flags[12] + 1, total, flags + 16);
     }
     __syncthreads();
 
@@ -589,6 +672,10 @@ __global__ void __launch_bounds__(NT, 2)
     }
     tc_fence_before();
     __syncthreads();
+    if (p.helpers && tid == 0) {   // publish the record (the barrier orders every thread's
+      __threadfence();             // part of it before this fence)
+      st_release_gpu(helper_claim(p, item), kClaimReady);
+    }
   }
 
   if (failed && tid == 0) {
@@ -598,6 +685,8 @@ __global__ void __launch_bounds__(NT, 2)
   tc_fence_before();
   __syncthreads();
   if (warp == 0) tmem_dealloc(tmem, TM_COLS);
+  // a helper grid completes only after the fused kernel it serves
+  if (p.helpers) pdl_wait();
 }
 
 typedef CUresult (*EncodeTiledFnK)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
@@ -643,6 +732,44 @@ cudaError_t launch_kside(const Params& p, cudaStream_t stream) {
   const int64_t grid = items < cap ? items : cap;
   kda_kside_kernel<<<(unsigned)grid, NT, K_SMEM_BYTES, stream>>>(p, mq, mk, mg);
   return cudaGetLastError();
+}
+
+// Two helper CTAs per SM that the fused kernel (one CTA per sequence and head) leaves free,
+// launched as its programmatic dependent: they start once every fused CTA has cleared its
+// claim words, run beside it, and the grid completes after it.
+cudaError_t launch_kside_helpers(const Params& p, cudaStream_t stream) {
+  static bool attr_set[64] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev >= 0 && dev < 64 && !attr_set[dev]) {
+    e = cudaFuncSetAttribute(kda_kside_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             K_SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    attr_set[dev] = true;
+  }
+  const int64_t free_sms = (int64_t)p.sm_count - (int64_t)p.num_seqs * p.heads;
+  if (p.total_tokens == 0 || free_sms <= 0 || p.num_seqs > kHelperMaxSeqs ||
+      ((p.total_tokens + C - 1) / C) * p.num_seqs * p.heads >= (1 << 30))
+    return cudaErrorInvalidValue;
+  EncodeTiledFnK enc = reinterpret_cast<EncodeTiledFnK>(tensor_map_encoder());
+  if (!enc) return cudaErrorNotSupported;
+  CUtensorMap mq, mk, mg;
+  if (!make_in_map(enc, &mq, p.q, p.total_tokens, p.heads, p.s_q) ||
+      !make_in_map(enc, &mk, p.k, p.total_tokens, p.heads, p.s_k) ||
+      !make_in_map(enc, &mg, p.g, p.total_tokens, p.heads, p.s_g))
+    return cudaErrorInvalidValue;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(2 * free_sms));
+  cfg.blockDim = dim3(NT);
+  cfg.dynamicSmemBytes = K_SMEM_BYTES;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kda_kside_kernel, p, mq, mk, mg);
 }
 
 }  // namespace kda

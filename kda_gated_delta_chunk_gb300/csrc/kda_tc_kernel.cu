@@ -1,6 +1,6 @@
 // tcgen05 + TMA chunked KDA prefill (KDA_KERNEL_TC), 64-token chunks.
 //
-// One CTA (512 threads, ~207 KB shared memory, 512 TMEM columns) owns one
+// One CTA (512 threads, ~209 KB shared memory, 512 TMEM columns) owns one
 // (sequence, head, value slice) and walks the sequence's chunks in order,
 // keeping the 128 x 128 fp32 state in tensor memory the whole time.
 //
@@ -41,6 +41,15 @@
 // The unit-lower-triangular inverse T runs on CUDA cores in fp32.  Inputs
 // arrive by TMA; the next chunk's q/k/g (and v) are fetched while this one
 // is being processed.
+//
+// With k-side helpers (KDA_KERNEL_TC_HELPERS) the CTAs of the k-side kernel
+// run on the SMs this grid leaves free, as its programmatic dependent: they
+// compute the chunk-local half of chunks taken from the end of each sequence
+// and write it as a record.  Once this CTA meets a chunk a helper has taken,
+// it reads that chunk and every later one from records (the chunk step of the
+// chain kernel: [U^T | O^T] and [O^T | S^T] as single accumulators), with the
+// same order of accumulation as above, so the result does not depend on which
+// CTA computed which chunk.
 #include <cuda.h>
 
 #include "kda_internal.cuh"
@@ -84,7 +93,8 @@ constexpr int OFF_GT = OFF_MISC + 2816;     // 8-row group totals [8][128] (also
 constexpr int OFF_PART = OFF_MISC + 6912;   // norm partial sums [16 warps][16]
 constexpr int OFF_BAR = OFF_MISC + 7936;    // 4 mbarriers
 constexpr int OFF_TSLOT = OFF_MISC + 7968;  // TMEM base address
-constexpr int OFF_FLAGS = OFF_MISC + 7972;  // [0] sequence chosen for this CTA
+constexpr int OFF_FLAGS = OFF_MISC + 7972;  // [0] sequence chosen for this CTA, [1] record mode
+constexpr int OFF_BAR_REC = OFF_MISC + 7984;   // 2 mbarriers: record buffers 0, 1
 constexpr int OFF_RSC = OFF_MISC + 8192;    // per-row power-of-two operand scales, bf16x2 [q 64][k 64]
 constexpr int SMEM_USED = OFF_RSC + 512;
 constexpr int SMEM_BYTES = SMEM_USED + 1024;
@@ -92,12 +102,20 @@ static_assert(OFF_Y + 32 * NS * 4 <= OFF_TB, "T scratch overlaps T diag(b)");
 static_assert(OFF_CKC + 24576 <= OFF_TB, "operands overlap T diag(b)");
 static_assert(OFF_TBU + 8192 <= OFF_QG, "T tiles overlap Qg");
 static_assert(SMEM_BYTES <= 227 * 1024, "shared memory");
+// Record mode (chunks whose k-side a helper CTA computed): two record images over the
+// k-side regions, the v tile where it always is, O staging over the q tile.
+constexpr int OFF_REC0 = OFF_RA;
+constexpr int OFF_REC1 = OFF_RA + kRecBytes;
+constexpr int OFF_OSTR = OFF_INQ;
+static_assert(kRecBytes % 1024 == 0 && OFF_REC1 + kRecBytes <= OFF_MISC, "record buffers");
+static_assert(OFF_BAR_REC + 16 <= OFF_RSC && OFF_FLAGS + 8 <= OFF_BAR_REC, "misc");
 
 // ---- TMEM columns (fp32 unless noted; lane = value channel, or key channel for D/W)
-constexpr uint32_t TM_O = 0;      // O^T         64 cols (col = token), then
-constexpr uint32_t TM_S = 64;     // S^T        128 cols (col = dk): one N = 192 accumulator
-constexpr uint32_t TM_SB = 192;   // S^T bf16    64 cols (A operand, 2 dk per col)
-constexpr uint32_t TM_U = 256;    // U^T         64 cols (col = token)
+// [U^T | O^T] and [O^T | S^T] are each one contiguous accumulator
+constexpr uint32_t TM_U = 0;      // U^T         64 cols (col = token)
+constexpr uint32_t TM_O = 64;     // O^T         64 cols (col = token), then
+constexpr uint32_t TM_S = 128;    // S^T        128 cols (col = dk)
+constexpr uint32_t TM_SB = 256;   // S^T bf16    64 cols (A operand, 2 dk per col)
 constexpr uint32_t TM_D = 320;    // D (A|QK)    96 cols, then W0^T at +0, W1^T at +64
 constexpr uint32_t TM_UB = 448;   // U^T bf16    32 cols (A operand, 2 tokens per col)
 constexpr uint32_t TM_COLS = 512;
@@ -107,6 +125,7 @@ constexpr uint32_t ID_KK96 = idesc_bf16(128, 96, 0, 0);
 constexpr uint32_t ID_MK64 = idesc_bf16(128, 64, 1, 0);
 constexpr uint32_t ID_KM64 = idesc_bf16(128, 64, 0, 1);
 constexpr uint32_t ID_KK192 = idesc_bf16(128, 192, 0, 0);
+constexpr uint32_t ID_KM128 = idesc_bf16(128, 128, 0, 1);
 
 __global__ void __launch_bounds__(NT, 1)
     kda_tc_chunk_kernel(const __grid_constant__ Params p, const __grid_constant__ CUtensorMap tm_q,
@@ -129,6 +148,7 @@ __global__ void __launch_bounds__(NT, 1)
   uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + OFF_TSLOT);
   const uint32_t bar_qkg = sb + OFF_BAR, bar_v = bar_qkg + 8, bar_mma = bar_qkg + 16;
   const uint32_t bar_o = bar_qkg + 24;      // O^T = S^T Qg^T, issued by warp 4
+  const uint32_t bar_rec0 = sb + OFF_BAR_REC, bar_rec1 = bar_rec0 + 8;
 
   // ---- work unit: (rank, head, part), longest sequence first
   const int P = p.vsplit, H = p.heads, N = p.num_seqs;
@@ -170,6 +190,8 @@ __global__ void __launch_bounds__(NT, 1)
     mbar_init(bar_v, 1);
     mbar_init(bar_mma, 1);
     mbar_init(bar_o, 1);
+    mbar_init(bar_rec0, 1);
+    mbar_init(bar_rec1, 1);
     mbar_fence_init();
     tma_prefetch_desc(&tm_q);
     tma_prefetch_desc(&tm_k);
@@ -192,15 +214,64 @@ __global__ void __launch_bounds__(NT, 1)
   const size_t HD = (size_t)H * D;
   const size_t sbase = ((size_t)n * H + h) * D * D;
   const int xcol = h * D;
+  const int nch = (t1 - t0 + C - 1) / C;
 
-  if (tid == 0 && t1 > t0) {
-    mbar_expect_tx(bar_qkg, 3 * 16384);
-    tma_load_2d(sb + OFF_INQ, &tm_q, xcol, t0, bar_qkg);
-    tma_load_2d(sb + OFF_INK, &tm_k, xcol, t0, bar_qkg);
-    tma_load_2d(sb + OFF_ING, &tm_g, xcol, t0, bar_qkg);
-    mbar_expect_tx(bar_v, 16384);
-    tma_load_2d(sb + OFF_INV, &tm_v, xcol, t0, bar_v);
-    tma_load_2d(sb + OFF_INV + 8192, &tm_v, xcol + 64, t0, bar_v);
+  // With helpers (P = 1): chunk c of this sequence is item (slot0, h) + c.  Its claim words
+  // start free, then the helper grid may launch.  The helpers claim (compare-and-swap) from
+  // the last chunk down as they start an item.  This CTA reads the word of its next chunk
+  // one chunk ahead: free -> it marks the chunk its own (a plain store: an atomic here would
+  // hold the next barrier for an L2 round trip) and computes it; taken -> this and every
+  // later chunk come from records.  A helper that takes the chunk between the read and the
+  // mark writes a record nobody reads and stops at its next claim.
+  const int slot0 = (t0 >> 6) + n;
+  // this CTA's claim words: chunk c at claims[c]
+  int* claims = p.helpers ? reinterpret_cast<int*>(reinterpret_cast<unsigned char*>(p.status) +
+                                                   helper_claims_offset(p.total_tokens, H, N)) +
+                                claim_index(slot0, h, p.total_tokens, N)
+                          : nullptr;
+  if (claims) {
+    for (int c = tid; c < nch; c += NT) claims[c] = kClaimFree;
+    if (blockIdx.x == 0 && tid == 0) p.status[kHelperCounterWord] = 0;
+    __threadfence();
+    __syncthreads();
+    pdl_launch_dependents();
+  }
+  auto claim = [&](int c) {   // thread 0: true if this CTA computes chunk c itself
+    return claims == nullptr ||
+           atomicCAS(&claims[c], kClaimFree, kClaimOwn) == kClaimFree;
+  };
+  // Record mode (one thread): wait (bounded) for the helper's record of chunk c, then copy
+  // it to buffer b
+  auto fetch_record = [&](int c, int b) {
+    const int* w = &claims[c];
+    if (!wait_flag(w, kClaimReady)) return false;
+    fence_proxy_async_global();
+    const unsigned char* src = reinterpret_cast<const unsigned char*>(p.status) + kSplitHeader +
+                               ((int64_t)(slot0 + c) * H + h) * kRecBytes;
+    const uint32_t dst = sb + (b ? OFF_REC1 : OFF_REC0), bar = b ? bar_rec1 : bar_rec0;
+    mbar_expect_tx(bar, kRecBytes);
+#pragma unroll
+    for (int part = 0; part < 4; ++part)
+      bulk_load(dst + part * 16384, src + part * 16384, 16384, bar);
+    bulk_load(dst + kRecVec, src + kRecVec, kRecBytes - kRecVec, bar);
+    return true;
+  };
+
+  if (tid == 0) {
+    flags[1] = 0;                              // 1: this and every later chunk from records
+    if (nch > 0) {
+      if (claim(0)) {
+        mbar_expect_tx(bar_qkg, 3 * 16384);
+        tma_load_2d(sb + OFF_INQ, &tm_q, xcol, t0, bar_qkg);
+        tma_load_2d(sb + OFF_INK, &tm_k, xcol, t0, bar_qkg);
+        tma_load_2d(sb + OFF_ING, &tm_g, xcol, t0, bar_qkg);
+      } else {
+        flags[1] = 1;
+      }
+      mbar_expect_tx(bar_v, 16384);
+      tma_load_2d(sb + OFF_INV, &tm_v, xcol, t0, bar_v);
+      tma_load_2d(sb + OFF_INV + 8192, &tm_v, xcol + 64, t0, bar_v);
+    }
   }
 
   // ---- state in: S^T[dv][dk] -> TMEM (lane = dv); this warp covers 32 key columns
@@ -223,6 +294,7 @@ __global__ void __launch_bounds__(NT, 1)
     tmem_st32(tmem + lane_base + TM_S + dk0, r);
     tmem_wait_st();
   }
+  __syncthreads();   // flags[1]
 
   const float gate_scale = expf(p.A_log[h]);
   const float lb2 = p.lower_bound * kLog2e;
@@ -238,15 +310,26 @@ __global__ void __launch_bounds__(NT, 1)
   float* Y = reinterpret_cast<float*>(sm + OFF_Y);
 
   uint32_t ph_qkg = 0, ph_v = 0, ph_mma = 0, ph_o = 0;
+  uint32_t ph_rec = 0;        // bit b: parity of record buffer b's next fill
+  int rec_pend = 0;           // record buffers with a copy in flight (thread 32's view)
+  constexpr int kFetcher = 32;   // thread that fetches records (warp 1; thread 0 issues MMAs)
+  int jr = 0, L_prev = 0;     // record-mode chunks done; rows of the previous one
   bool failed = false;
   int site = 0;
   // beta logits are fetched one chunk ahead (their load latency hides behind a chunk)
   float b_raw = 0.0f;
   if (tid < C && t0 + tid < t1) b_raw = __bfloat162float(p.beta[(size_t)(t0 + tid) * p.s_beta + h]);
 
-  for (int c0 = t0; c0 < t1; c0 += C) {
+  int c = 0;
+  for (; c < nch; ++c) {
+    if (flags[1]) break;   // from here on the chunks come from records (loop below)
+    const int c0 = t0 + C * c;
     const int L = min(C, t1 - c0);
-    const bool more = c0 + C < t1;
+    const bool more = c + 1 < nch;
+    // the next chunk's claim word now; the answer is needed when its inputs are fetched (P3)
+    int next_claim = kClaimFree;
+    if (claims && more && tid == 0) next_claim = ld_relaxed_gpu(&claims[c + 1]);
+
 
     // ---- P0: q, k, g of this chunk have landed (every thread waits for the TMA itself;
     //          a timeout is acted on at the next barrier); beta; zero q/k rows past the end
@@ -406,10 +489,15 @@ __global__ void __launch_bounds__(NT, 1)
                  ks > 0);
       mma_commit(bar_mma);
       if (more) {
-        mbar_expect_tx(bar_qkg, 3 * 16384);
-        tma_load_2d(sb + OFF_INQ, &tm_q, xcol, c0 + C, bar_qkg);
-        tma_load_2d(sb + OFF_INK, &tm_k, xcol, c0 + C, bar_qkg);
-        tma_load_2d(sb + OFF_ING, &tm_g, xcol, c0 + C, bar_qkg);
+        if (next_claim == kClaimFree) {
+          if (claims) st_relaxed_gpu(&claims[c + 1], kClaimOwn);
+          mbar_expect_tx(bar_qkg, 3 * 16384);
+          tma_load_2d(sb + OFF_INQ, &tm_q, xcol, c0 + C, bar_qkg);
+          tma_load_2d(sb + OFF_INK, &tm_k, xcol, c0 + C, bar_qkg);
+          tma_load_2d(sb + OFF_ING, &tm_g, xcol, c0 + C, bar_qkg);
+        } else {
+          flags[1] = 1;   // a helper has the next chunk, hence every later one
+        }
       }
     }
     {
@@ -717,8 +805,210 @@ __global__ void __launch_bounds__(NT, 1)
     __syncthreads();
   }
 
+  // ---- record mode: the chunks a helper computed the chunk-local half of ([-W | Qg],
+  //      [QK; Ke], T diag(b), decay and norm scalars in its record): the chunk step of the
+  //      chain kernel, one record fetched ahead
+  for (; !failed && c < nch; ++c) {
+    const int c0 = t0 + C * c;
+    const int L = min(C, t1 - c0);
+    const bool more = c + 1 < nch;
+    const int buf = jr & 1;
+    const uint32_t rb = sb + (buf ? OFF_REC1 : OFF_REC0);
+    const float* vec = reinterpret_cast<const float*>(sm + (buf ? OFF_REC1 : OFF_REC0) + kRecVec);
+    bool ok = true;
+    if (tid == kFetcher && jr == 0) {   // first record-mode chunk: nothing was fetched ahead
+      ok = fetch_record(c, buf);
+      if (ok) rec_pend |= 1 << buf;
+    }
+    // R1: the record and the v tile have landed; v rows past the sequence end -> 0
+    const bool got = ok && mbar_wait(buf ? bar_rec1 : bar_rec0, (ph_rec >> buf) & 1u);
+    ok = got && mbar_wait(bar_v, ph_v);
+    if (got) {
+      ph_rec ^= 1u << buf;
+      if (tid == kFetcher) rec_pend &= ~(1 << buf);
+    }
+    ph_v ^= 1;
+    if (ok && L < C) {
+      for (int idx = tid; idx < (C - L) * 16; idx += NT) {
+        const int r = L + idx / 16, cc = idx % 16;
+        st_u128(sm, OFF_INV + (cc >> 3) * 8192 + r * 128 + (cc & 7) * 16, make_uint4(0, 0, 0, 0));
+      }
+      fence_proxy_async();
+    }
+    if (__syncthreads_or(!ok)) { failed = true; site = 80; break; }
+    if (tid == 0 && c + 2 < nch) {   // v two chunks ahead -> L2 (its TMA is issued in R3 below)
+      tma_prefetch_2d(&tm_v, xcol, c0 + 2 * C);
+      tma_prefetch_2d(&tm_v, xcol + 64, c0 + 2 * C);
+    }
+
+    // R2: S^T -> bf16 copy, S^T *= 2^Gam_last (this warp: 32 key columns); O of the
+    //     previous chunk -> staging (its scale/|q| is in the other record buffer)
+    {
+      uint32_t x[32], pk[16];
+      tmem_ld32(tmem + lane_base + TM_S + cs * 32, x);
+      tmem_wait_ld();
+#pragma unroll
+      for (int j = 0; j < 16; ++j)
+        pk[j] = pack_bf16x2(__uint_as_float(x[2 * j]), __uint_as_float(x[2 * j + 1]));
+      tmem_st16(tmem + lane_base + TM_SB + cs * 16, pk);
+#pragma unroll
+      for (int j4 = 0; j4 < 8; ++j4) {
+        const float4 dl = ld4(vec + cs * 32 + 4 * j4);
+        x[4 * j4] = __float_as_uint(__uint_as_float(x[4 * j4]) * dl.x);
+        x[4 * j4 + 1] = __float_as_uint(__uint_as_float(x[4 * j4 + 1]) * dl.y);
+        x[4 * j4 + 2] = __float_as_uint(__uint_as_float(x[4 * j4 + 2]) * dl.z);
+        x[4 * j4 + 3] = __float_as_uint(__uint_as_float(x[4 * j4 + 3]) * dl.w);
+      }
+      tmem_st32(tmem + lane_base + TM_S + cs * 32, x);
+    }
+    {
+      uint32_t r[16];
+      if (jr > 0) {
+        const float* iqp =
+            reinterpret_cast<const float*>(sm + (buf ? OFF_REC0 : OFF_REC1) + kRecVec) + 128;
+        tmem_ld16(tmem + lane_base + TM_O + cs * 16, r);
+        tmem_wait_ld();
+        __nv_bfloat16* ost = reinterpret_cast<__nv_bfloat16*>(sm + OFF_OSTR);
+#pragma unroll
+        for (int j4 = 0; j4 < 4; ++j4) {
+          const float4 iq = ld4(iqp + cs * 16 + 4 * j4);
+          const float iqv[4] = {iq.x, iq.y, iq.z, iq.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int j = 4 * j4 + e;
+            ost[(cs * 16 + j) * D + my_lane] = __float2bfloat16_rn(__uint_as_float(r[j]) * iqv[e]);
+          }
+        }
+      }
+      // O^T starts from zero: the group below accumulates into [U^T | O^T]
+#pragma unroll
+      for (int j = 0; j < 16; ++j) r[j] = 0u;
+      tmem_st16(tmem + lane_base + TM_O + cs * 16, r);
+    }
+    tmem_wait_st();
+    tc_fence_before();
+    __syncthreads();   // (A) SB ready, S decayed, O(c-1) staged, O zeroed; the other buffer is free
+
+    // R3: U^T = V^T (T diag b)^T, then [U^T | O^T] += S^T [-W | Qg]^T (the fused kernel's
+    //     order of accumulation: the same bits whichever CTA computed the chunk-local
+    //     half); fetch the next record; O(c-1) -> out
+    bool next_ok = true;
+    if (tid == 0) {
+      tc_fence_after();
+#pragma unroll
+      for (int ks = 0; ks < 4; ++ks)
+        mma_bf16(tmem + TM_U, mndesc(sb + OFF_INV, 8192, ks), kdesc(rb + kRecTB, 64, ks), ID_MK64,
+                 ks > 0);
+#pragma unroll
+      for (int ks = 0; ks < 8; ++ks)
+        mma_bf16_ts(tmem + TM_U, tmem + TM_SB + 8 * ks, mndesc(rb + kRecWQ, 16384, ks), ID_KM128,
+                    1);
+      mma_commit(bar_mma);
+    } else if (tid == kFetcher && more) {   // meanwhile: the next record, and the one after to L2
+      next_ok = fetch_record(c + 1, buf ^ 1);
+      if (next_ok) rec_pend |= 1 << (buf ^ 1);
+      if (c + 2 < nch && ld_acquire_gpu(&claims[c + 2]) == kClaimReady)
+        l2_prefetch(reinterpret_cast<const unsigned char*>(p.status) + kSplitHeader +
+                        ((int64_t)(slot0 + c + 2) * H + h) * kRecBytes,
+                    kRecBytes);
+    }
+    if (jr > 0) {
+#pragma unroll
+      for (int k2 = 0; k2 < 2; ++k2) {
+        const int idx = tid + k2 * NT;
+        const int r = idx >> 4, v8 = idx & 15;
+        if (r < L_prev) {
+          const uint4 val = *reinterpret_cast<const uint4*>(sm + OFF_OSTR + r * 256 + v8 * 16);
+          *reinterpret_cast<uint4*>(p.out + (size_t)(c0 - C + r) * HD + xcol + v8 * 8) = val;
+        }
+      }
+    }
+    {
+      const bool okm = next_ok && (tid != 0 || mbar_wait(bar_mma, ph_mma));
+      ph_mma ^= 1;
+      tc_fence_before();
+      if (__syncthreads_or(!okm)) { failed = true; site = 81; break; }   // (B)
+    }
+    tc_fence_after();
+    if (tid == 0 && more) {   // the v tile is free again
+      mbar_expect_tx(bar_v, 16384);
+      tma_load_2d(sb + OFF_INV, &tm_v, xcol, c0 + C, bar_v);
+      tma_load_2d(sb + OFF_INV + 8192, &tm_v, xcol + 64, c0 + C, bar_v);
+    }
+
+    // R4: U^T diag(1/|k|) -> bf16 operand in TMEM
+    if (cs < 2) {
+      uint32_t x[32], pk[16];
+      tmem_ld32(tmem + lane_base + TM_U + cs * 32, x);
+      tmem_wait_ld();
+#pragma unroll
+      for (int j4 = 0; j4 < 8; ++j4) {
+        const float4 ik = ld4(vec + 192 + cs * 32 + 4 * j4);
+        pk[2 * j4] = pack_bf16x2(__uint_as_float(x[4 * j4]) * ik.x,
+                                 __uint_as_float(x[4 * j4 + 1]) * ik.y);
+        pk[2 * j4 + 1] = pack_bf16x2(__uint_as_float(x[4 * j4 + 2]) * ik.z,
+                                     __uint_as_float(x[4 * j4 + 3]) * ik.w);
+      }
+      tmem_st16(tmem + lane_base + TM_UB + cs * 16, pk);
+      tmem_wait_st();
+    }
+    tc_fence_before();
+    __syncthreads();   // (C)
+
+    // R5: [O^T | S^T] += U^T [QK; Ke]^T
+    if (tid == 0) {
+      tc_fence_after();
+#pragma unroll
+      for (int ks = 0; ks < 4; ++ks)
+        mma_bf16_ts(tmem + TM_O, tmem + TM_UB + 8 * ks, kdesc(rb + kRecQKE, 192, ks), ID_KK192, 1);
+      mma_commit(bar_mma);
+    }
+    {
+      const bool okm = tid != 0 || mbar_wait(bar_mma, ph_mma);
+      ph_mma ^= 1;
+      tc_fence_before();
+      if (__syncthreads_or(!okm)) { failed = true; site = 82; break; }   // (D)
+    }
+    tc_fence_after();
+    L_prev = L;
+    ++jr;
+  }
+
+  if (!failed && flags[1] && jr > 0) {   // O of the last (record-mode) chunk
+    const float* iqp =
+        reinterpret_cast<const float*>(sm + (((jr - 1) & 1) ? OFF_REC1 : OFF_REC0) + kRecVec) + 128;
+    uint32_t r[16];
+    tmem_ld16(tmem + lane_base + TM_O + cs * 16, r);
+    tmem_wait_ld();
+    __nv_bfloat16* ost = reinterpret_cast<__nv_bfloat16*>(sm + OFF_OSTR);
+#pragma unroll
+    for (int j4 = 0; j4 < 4; ++j4) {
+      const float4 iq = ld4(iqp + cs * 16 + 4 * j4);
+      const float iqv[4] = {iq.x, iq.y, iq.z, iq.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int j = 4 * j4 + e;
+        ost[(cs * 16 + j) * D + my_lane] = __float2bfloat16_rn(__uint_as_float(r[j]) * iqv[e]);
+      }
+    }
+    __syncthreads();
+    const int c0 = t0 + C * (nch - 1);
+#pragma unroll
+    for (int k2 = 0; k2 < 2; ++k2) {
+      const int idx = tid + k2 * NT;
+      const int r2 = idx >> 4, v8 = idx & 15;
+      if (r2 < L_prev) {
+        const uint4 val = *reinterpret_cast<const uint4*>(sm + OFF_OSTR + r2 * 256 + v8 * 16);
+        *reinterpret_cast<uint4*>(p.out + (size_t)(c0 + r2) * HD + xcol + v8 * 8) = val;
+      }
+    }
+  }
   if (failed) {
     if (tid == 0) record_error(p.status, KDA_ERR_DEVICE_TIMEOUT, site);
+    if (tid == kFetcher) {
+      if (rec_pend & 1) mbar_wait(bar_rec0, ph_rec & 1u);
+      if (rec_pend & 2) mbar_wait(bar_rec1, (ph_rec >> 1) & 1u);
+    }
     // let copies still in flight finish (bounded) before the CTA exits
     mbar_wait(bar_qkg, ph_qkg);
     mbar_wait(bar_v, ph_v);
@@ -818,7 +1108,9 @@ cudaError_t launch_tc(const Params& p, cudaStream_t stream) {
       !make_map(enc, &mv, vb, p.total_tokens, p.heads, p.s_v, 64, true))
     return cudaErrorInvalidValue;
   kda_tc_chunk_kernel<<<(unsigned)blocks, NT, SMEM_BYTES, stream>>>(p, mq, mk, mg, mv);
-  return cudaGetLastError();
+  e = cudaGetLastError();
+  if (e != cudaSuccess || !p.helpers) return e;
+  return launch_kside_helpers(p, stream);
 }
 
 }  // namespace kda

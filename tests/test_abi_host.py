@@ -60,15 +60,22 @@ def _sms():
 
 def test_workspace_size_holds_split_records(L):
     """Records for ceil(T/64) + N chunk slots per head whenever some batch of up to
-    max_seqs sequences would take the value split (2 H N <= SMs), else 256 bytes."""
+    max_seqs sequences would take the value split (2 H N <= SMs) or leave 8 SMs to k-side
+    helpers (H N + 8 <= SMs, N <= 128; plus a 4-byte claim word per slot and head), else
+    256 bytes; rounded up to 16."""
     sms = _sms()
-    for T, H, N in [(1000, 2, 3), (16384, 16, 1), (4096, 8, 7), (64, 1, 500), (65536, 32, 64)]:
+    cases = [(1000, 2, 3), (16384, 16, 1), (16384, 16, 8), (4096, 8, 7), (64, 1, 500),
+             (65536, 32, 64), (65536, 160, 2)]
+    for T, H, N in cases:
         got = kda.workspace_size(T, H, N)
+        need = 256
         if 2 * H <= sms:
             n_split = min(N, sms // (2 * H))
-            assert got == 1024 + ((T + 63) // 64 + n_split) * H * SLOT_HEAD_BYTES, (T, H, N)
-        else:
-            assert got == 256
+            need = max(need, 1024 + ((T + 63) // 64 + n_split) * H * SLOT_HEAD_BYTES)
+        if H + 8 <= sms:
+            n_help = min(N, 128, (sms - 8) // H)
+            need = max(need, 1024 + ((T + 63) // 64 + n_help) * H * (SLOT_HEAD_BYTES + 4))
+        assert got == (need + 15) // 16 * 16, (T, H, N)
         assert got % 16 == 0
     assert kda.workspace_size(0, 4, 2) == 256          # no tokens, no records
     assert kda.workspace_size(100, 4, 0) == 256

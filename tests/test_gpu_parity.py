@@ -23,7 +23,7 @@ pytestmark = pytest.mark.gpu
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 TOL = json.load(open(os.path.join(ROOT, "tests", "golden", "tolerances.json")))["max_abs"]
-KERNELS = [kda.KERNEL_REF, kda.KERNEL_TC, kda.KERNEL_SPLIT]
+KERNELS = [kda.KERNEL_REF, kda.KERNEL_TC, kda.KERNEL_SPLIT, kda.KERNEL_TC_HELPERS]
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -48,12 +48,24 @@ def split_workspace(T, H, N):
     return torch.zeros(n, dtype=torch.uint8, device="cuda")
 
 
+def helper_workspace(T, H, N):
+    """The same records plus one 4-byte claim word per (chunk slot, head)."""
+    n = 1024 + ((T + 63) // 64 + N) * H * (66560 + 4)
+    return torch.zeros(n, dtype=torch.uint8, device="cuda")
+
+
+def workspace_for(kernel, T, H, N):
+    if kernel == kda.KERNEL_SPLIT:
+        return split_workspace(T, H, N)
+    if kernel == kda.KERNEL_TC_HELPERS:
+        return helper_workspace(T, H, N)
+    return None
+
+
 def run_gpu(inp, kernel=kda.KERNEL_AUTO, vsplit=-1, out=None, final_state=None, init="keep"):
     d = to_dev(inp)
     s0 = d["initial_state"] if init == "keep" else None
-    ws = None
-    if kernel == kda.KERNEL_SPLIT:
-        ws = split_workspace(d["q"].shape[0], d["q"].shape[1], d["cu_seqlens"].numel() - 1)
+    ws = workspace_for(kernel, d["q"].shape[0], d["q"].shape[1], d["cu_seqlens"].numel() - 1)
     out, fin = kda.chunk_prefill_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], d["A_log"],
                                      d["dt_bias"], d["lower_bound"], d["scale"], s0,
                                      d["cu_seqlens"], out=out, final_state=final_state,
@@ -107,6 +119,8 @@ def test_workload0_tiny(oracle_mod, kernel):
 @pytest.mark.parametrize("vsplit", [1, 2, 4, 8])
 def test_ragged_tiles_and_tails(oracle_mod, kernel, vsplit):
     """Several chunks, ragged tails, a 1-token and an empty sequence."""
+    if kernel == kda.KERNEL_TC_HELPERS and vsplit != 1:
+        pytest.skip("the helpers serve the unsplit fused kernel only")
     w = W.custom([1, 63, 64, 65, 130, 0, 200, 17, 129], 3, seed=21)
     inp = W.make_inputs(w)
     out, fin = run_gpu(inp, kernel, vsplit)
@@ -123,7 +137,8 @@ def test_bf16_state(oracle_mod, kernel):
 
 
 @pytest.mark.parametrize("cfg", [1, 2])
-@pytest.mark.parametrize("kernel", [kda.KERNEL_AUTO, kda.KERNEL_TC, kda.KERNEL_SPLIT])
+@pytest.mark.parametrize("kernel", [kda.KERNEL_AUTO, kda.KERNEL_TC, kda.KERNEL_SPLIT,
+                                    kda.KERNEL_TC_HELPERS])
 def test_workloads_1_2_full_size(oracle_mod, cfg, kernel):
     inp = W.make_inputs(W.workload(cfg))
     out, fin = run_gpu(inp, kernel, 1 if kernel == kda.KERNEL_TC else -1)
@@ -220,7 +235,7 @@ def test_strided_inputs_equal_dense(kernel):
     wide[:, 1:H + 1] = d["beta"]
     views["beta"] = wide[:, 1:H + 1]
     assert not views["q"].is_contiguous() and not views["beta"].is_contiguous()
-    ws = split_workspace(T, H, d["cu_seqlens"].numel() - 1) if kernel == kda.KERNEL_SPLIT else None
+    ws = workspace_for(kernel, T, H, d["cu_seqlens"].numel() - 1)
     outs = []
     for src in (d, views):
         o, f = kda.chunk_prefill_fwd(src["q"], src["k"], src["v"], src["g"], src["beta"],
@@ -330,3 +345,82 @@ def test_cuda_graph_capture_and_replay(oracle_mod):
     graph.replay()
     torch.cuda.synchronize()
     assert torch.equal(out, out_e) and torch.equal(fin, fin_e)
+
+
+# ----------------------------------------------------------------- k-side helpers
+@pytest.mark.parametrize("lengths,H", [([2048] * 8, 16), ([300, 1000, 64, 129, 0, 700], 2),
+                                        ([4096, 64, 1, 4000], 4)])
+def test_helpers_agree_with_the_fused_kernel_alone(oracle_mod, lengths, H):
+    """The fused kernel with helper CTAs computes the chunk-local half of some chunks in
+    the helpers' records; which chunks depends on timing.  Its results match the fused
+    kernel alone and the oracle, on the benchmark shape and on small batches where the
+    helpers take nearly every chunk."""
+    inp = W.make_inputs(W.custom(lengths, H, seed=41))
+    out_t, fin_t = run_gpu(inp, kda.KERNEL_TC, vsplit=1)
+    out_h, fin_h = run_gpu(inp, kda.KERNEL_TC_HELPERS)
+    same = torch.equal(out_t, out_h) and torch.equal(fin_t, fin_h)
+    d_o = (out_t.float() - out_h.float()).abs().max().item()
+    d_f = (fin_t - fin_h).abs().max().item()
+    print(f"helpers vs alone: bitwise {same}, out {d_o:.3e}, state {d_f:.3e}")
+    assert d_o <= TOL["f32"] and d_f <= TOL["f32"]
+    N = len(lengths)
+    heads = list(range(H)) if H <= 4 else [0, 7, 15]
+    check(oracle_mod, inp, out_h, fin_h, heads=heads, tag=f"helpers {N}x{H}")
+
+
+def test_auto_takes_helpers_on_the_benchmark_shape():
+    """8 x 2048, H = 16 leaves 24 of 152 SMs free: AUTO runs the fused kernel with helpers."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    T, N, H = 16384, 8, 16
+    path, P, launches = kda.plan(T, N, H, kda.workspace_size(T, H, N), -1, kda.KERNEL_AUTO)
+    if N * H + 8 <= sms:
+        assert (path, P, launches) == (kda.KERNEL_TC_HELPERS, 1, 2)
+    else:
+        assert path == kda.KERNEL_TC
+    path, P, launches = kda.plan(T, N, H, 256, -1, kda.KERNEL_AUTO)   # no room for records
+    assert (path, P, launches) == (kda.KERNEL_TC, 1, 1)
+
+
+def test_helpers_under_cuda_graph_replay(oracle_mod):
+    """The helper grid is a programmatic dependent of the fused kernel; a captured call
+    replays to the eager result's values."""
+    inp = W.make_inputs(W.custom([700, 300, 1000], 2, seed=42))
+    d = to_dev(inp)
+    T = d["q"].shape[0]
+    out = torch.empty_like(d["q"])
+    fin = torch.empty_like(d["initial_state"])
+    ws = helper_workspace(T, 2, 3)
+    side = torch.cuda.Stream()
+    args = (d["q"], d["k"], d["v"], d["g"], d["beta"], d["A_log"], d["dt_bias"],
+            d["lower_bound"], d["scale"], d["initial_state"], d["cu_seqlens"])
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        kda.chunk_prefill_fwd(*args, out=out, final_state=fin, workspace=ws, stream=side,
+                              kernel=kda.KERNEL_TC_HELPERS)
+    side.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=side):
+        kda.chunk_prefill_fwd(*args, out=out, final_state=fin, workspace=ws, stream=side,
+                              kernel=kda.KERNEL_TC_HELPERS)
+    for _ in range(3):
+        out.zero_()
+        fin.zero_()
+        graph.replay()
+        torch.cuda.synchronize()
+        assert kda.last_device_status(ws) == kda.OK
+        check(oracle_mod, inp, out, fin, tag="helpers graph replay")
+
+
+def test_helpers_refused_when_they_cannot_run():
+    inp = W.make_inputs(W.custom([100, 50], 2, seed=43))
+    d = to_dev(inp)
+    args = (d["q"], d["k"], d["v"], d["g"], d["beta"], d["A_log"], d["dt_bias"],
+            d["lower_bound"], d["scale"], d["initial_state"], d["cu_seqlens"])
+    with pytest.raises(kda.KDAError) as e:    # records do not fit
+        kda.chunk_prefill_fwd(*args, workspace=split_workspace(150, 2, 2),
+                              kernel=kda.KERNEL_TC_HELPERS)
+    assert e.value.code == kda.ERR_WORKSPACE_TOO_SMALL
+    with pytest.raises(kda.KDAError) as e:    # a value split is not served
+        kda.chunk_prefill_fwd(*args, workspace=helper_workspace(150, 2, 2),
+                              kernel=kda.KERNEL_TC_HELPERS, vsplit=2)
+    assert e.value.code == kda.ERR_INVALID_ARG
