@@ -299,6 +299,70 @@ def run_decode(args):
     print(json.dumps(line), flush=True)
 
 
+def run_scatter(args):
+    """The benchmark workload written through a row map (a mixed step's non-speculative
+    tokens into the layer output): the prefill with out_index, against the dense call and
+    against the dense call followed by index_copy_ into the layer output."""
+    import kda_gated_delta_chunk_gb300 as kda
+    from kda_gated_delta_chunk_gb300 import build as kbuild
+    kbuild.build()
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    w = W.workload(1)
+    host = W.make_inputs(w)
+    T, H, N = sum(w.lengths), w.heads, w.num_seqs
+    NB = 4
+    gen = torch.Generator().manual_seed(71)
+    rows = torch.randperm(T + 1024, generator=gen)[:T].to(torch.int32).to(dev)
+    sets = []
+    for _ in range(NB):
+        d = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in host.items()}
+        d["out"] = torch.empty_like(d["q"])
+        d["layer"] = torch.empty((T + 1024, H, D), dtype=torch.bfloat16, device=dev)
+        d["fin"] = torch.empty_like(d["initial_state"])
+        d["ws"] = kda.alloc_workspace(T, H, N, device=dev)
+        sets.append(d)
+    stream = torch.cuda.Stream(dev)
+
+    def call(i, mode):
+        d = sets[i % NB]
+        a = (d["q"], d["k"], d["v"], d["g"], d["beta"], d["A_log"], d["dt_bias"],
+             d["lower_bound"], d["scale"], d["initial_state"], d["cu_seqlens"])
+        if mode == "scatter":
+            kda.chunk_prefill_fwd(*a, out=d["layer"], final_state=d["fin"], workspace=d["ws"],
+                                  stream=stream, out_index=rows)
+        else:
+            kda.chunk_prefill_fwd(*a, out=d["out"], final_state=d["fin"], workspace=d["ws"],
+                                  stream=stream)
+            if mode == "index_copy":
+                with torch.cuda.stream(stream):
+                    d["layer"].index_copy_(0, rows.long(), d["out"])
+    steps = args.steps if args.steps > 0 else 100
+    res = {}
+    for mode in ("dense", "scatter", "index_copy"):
+        for i in range(max(3, args.warmup)):
+            call(i, mode)
+        stream.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for i in range(steps):
+            call(i, mode)
+        e1.record(stream)
+        e1.synchronize()
+        res[mode] = e0.elapsed_time(e1) / 1e3 / steps
+    _, _, launches = kda.plan(T, N, H, sets[0]["ws"].numel(), -1, kda.KERNEL_AUTO)
+    line = {"metric": "KDA prefill with a scattered output (mixed step)", "value": T / res["scatter"],
+            "unit": UNIT, "n_gpus": 1, "steps": steps, "warmup": args.warmup,
+            "ms_per_step": 1e3 * res["scatter"], "higher_is_better": True, "dtype": "bf16",
+            "data": "synthetic",
+            "config": {"workload": w.name + "_scatter", "rows": "random one-to-one map into "
+                       f"{T + 1024} rows", "l2": "4 input sets rotated"},
+            "us_dense": 1e6 * res["dense"], "us_scatter": 1e6 * res["scatter"],
+            "us_dense_then_index_copy": 1e6 * res["index_copy"],
+            "gpu_launches": steps * launches}
+    print(json.dumps(line), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -311,11 +375,15 @@ def main():
     ap.add_argument("--vsplit", type=int, default=-1, help="-1 automatic, or 1/2/4/8")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=10)
+    ap.add_argument("--scatter", action="store_true",
+                    help="time the prefill writing through an output row map")
     ap.add_argument("--decode", type=int, default=0,
                     help="time a decode step (kda_recurrent_fwd) with this many tokens per sequence")
     args = ap.parse_args()
     if args.decode > 0:
         return run_decode(args)
+    if args.scatter:
+        return run_scatter(args)
     w = W.workload(args.workload, args.n) if args.workload == 3 else W.workload(args.workload)
     if args.impl == "reference":
         if args.steps <= 0:

@@ -85,6 +85,8 @@ typedef struct CUstream_st* kda_stream_t;
 #define KDA_ERR_BAD_CU_SEQLENS (-8)      /* (device) cu_seqlens not monotone
                                             or past total_tokens            */
 #define KDA_ERR_CUDA (-9)                /* a CUDA runtime call failed        */
+#define KDA_ERR_BAD_OUT_INDEX (-10)      /* (device) an out_index entry lies
+                                            outside [0, out_rows)            */
 
 /* kernel selectors for kda_chunk_prefill_fwd_ex */
 #define KDA_KERNEL_AUTO 0  /* SPLIT when the value split triggers and the
@@ -195,6 +197,33 @@ int kda_chunk_prefill_fwd_strided(const void* q, const void* k, const void* v, c
                                   int vsplit, int kernel);
 
 /*
+ * As kda_chunk_prefill_fwd_strided, writing each token's output row through a
+ * row map: the H x 128 outputs of token t (0 <= t < cu_seqlens[N]) go to
+ * out[out_index[t]], `out` being bf16 [out_rows, H, 128].  This is the
+ * mixed step of the vLLM PR report "[Perf][GLM-5.3-Flash] Use FlashKDA for
+ * KDA chunked prefill" (PR #55737, Implementation breakdown item 4): there
+ * the prefill of the non-speculative tokens writes a workspace buffer that
+ * index_copy_ then scatters into the layer output by non_spec_token_indx;
+ * with the map the kernels write the layer output directly.  out_index is
+ * device int32 [total_tokens] (entries past cu_seqlens[N] are not read),
+ * 4-byte aligned; rows not named by the map are left untouched; two tokens
+ * mapped to one row leave one of them there.  An entry outside
+ * [0, out_rows) is not written and is recorded as KDA_ERR_BAD_OUT_INDEX
+ * (kda_last_device_status).  A NULL out_index or a negative out_rows gives
+ * KDA_ERR_INVALID_ARG.
+ */
+int kda_chunk_prefill_fwd_scatter(const void* q, const void* k, const void* v, const void* g,
+                                  const void* beta, const float* A_log, const float* dt_bias,
+                                  float lower_bound, float scale, const void* initial_state,
+                                  const int32_t* cu_seqlens, void* out, void* final_state,
+                                  int state_dtype, void* workspace, kda_stream_t stream,
+                                  int64_t total_tokens, int32_t num_seqs, int32_t heads,
+                                  size_t workspace_bytes, int64_t q_stride, int64_t k_stride,
+                                  int64_t v_stride, int64_t g_stride, int64_t beta_stride,
+                                  const int32_t* out_index, int64_t out_rows, int vsplit,
+                                  int kernel);
+
+/*
  * Token-by-token KDA for decode and speculative-verify steps, where each
  * sequence brings a few tokens (1..k): the recurrent form of the same
  * operation, on the same state layout and dtypes, so a sequence can switch
@@ -216,6 +245,22 @@ int kda_recurrent_fwd(const void* q, const void* k, const void* v, const void* g
                       void* token_states, void* workspace, kda_stream_t stream,
                       int64_t total_tokens, int32_t num_seqs, int32_t heads,
                       size_t workspace_bytes);
+
+/*
+ * kda_recurrent_fwd writing token t's output row to out[out_index[t]] (out
+ * being [out_rows, H, 128]), with the conventions of
+ * kda_chunk_prefill_fwd_scatter: in a mixed step the speculative tokens
+ * (spec_token_indx in the pages' layer) and the prefill tokens write
+ * disjoint rows of one layer output.
+ */
+int kda_recurrent_fwd_scatter(const void* q, const void* k, const void* v, const void* g,
+                              const void* beta, const float* A_log, const float* dt_bias,
+                              float lower_bound, float scale, const void* initial_state,
+                              const int32_t* cu_seqlens, void* out, void* final_state,
+                              int state_dtype, void* token_states, void* workspace,
+                              kda_stream_t stream, int64_t total_tokens, int32_t num_seqs,
+                              int32_t heads, size_t workspace_bytes, const int32_t* out_index,
+                              int64_t out_rows);
 
 /*
  * The value-dimension split factor the automatic path uses for a batch of

@@ -46,12 +46,14 @@ ERR_LAUNCH_FAILED = -6
 ERR_DEVICE_TIMEOUT = -7
 ERR_BAD_CU_SEQLENS = -8
 ERR_CUDA = -9
+ERR_BAD_OUT_INDEX = -10
 
 # every symbol include/kda.h declares
 EXPORTS = ("kda_workspace_size", "kda_chunk_prefill_fwd", "kda_chunk_prefill_fwd_ex",
            "kda_choose_vsplit", "kda_status_string", "kda_last_device_status",
            "kda_device_check", "kda_plan", "kda_chunk_prefill_fwd_strided",
-           "kda_recurrent_fwd", "kda_chunk_prefill_fwd_noalloc")
+           "kda_recurrent_fwd", "kda_chunk_prefill_fwd_noalloc", "kda_chunk_prefill_fwd_scatter",
+           "kda_recurrent_fwd_scatter")
 
 _lib = None
 _lock = threading.Lock()
@@ -86,6 +88,10 @@ def lib() -> ctypes.CDLL:
             L.kda_chunk_prefill_fwd_strided.restype = ctypes.c_int
             L.kda_chunk_prefill_fwd_strided.argtypes = fwd_args + [I64] * 5 + [ctypes.c_int,
                                                                              ctypes.c_int]
+            L.kda_chunk_prefill_fwd_scatter.restype = ctypes.c_int
+            L.kda_chunk_prefill_fwd_scatter.argtypes = fwd_args + [I64] * 5 + [P, I64,
+                                                                             ctypes.c_int,
+                                                                             ctypes.c_int]
             L.kda_choose_vsplit.restype = ctypes.c_int
             L.kda_choose_vsplit.argtypes = [I32, I32, I32]
             L.kda_status_string.restype = ctypes.c_char_p
@@ -97,6 +103,8 @@ def lib() -> ctypes.CDLL:
             L.kda_recurrent_fwd.restype = ctypes.c_int
             L.kda_recurrent_fwd.argtypes = [P, P, P, P, P, P, P, F, F, P, P, P, P, ctypes.c_int,
                                             P, P, P, I64, I32, I32, SZ]
+            L.kda_recurrent_fwd_scatter.restype = ctypes.c_int
+            L.kda_recurrent_fwd_scatter.argtypes = L.kda_recurrent_fwd.argtypes + [P, I64]
             L.kda_plan.restype = ctypes.c_int
             L.kda_plan.argtypes = [I64, I32, I32, SZ, ctypes.c_int, ctypes.c_int, P, P, P]
             L.kda_chunk_prefill_fwd_noalloc.restype = ctypes.c_int
@@ -171,17 +179,34 @@ def _need(t, name, dtype, shape=None, token_strided=False):
         raise ValueError(f"{name} must be contiguous")
 
 
+def _out_rows(out, out_index, T, H, D, dev):
+    """The destination of the outputs: dense [T, H, D] (allocated if None), or with a row
+    map, ``out`` [R, H, D] given by the caller and out_index int32 [T]."""
+    if out_index is None:
+        if out is None:
+            out = torch.empty((T, H, D), dtype=torch.bfloat16, device=dev)
+        _need(out, "out", torch.bfloat16, (T, H, D))
+        return out, 0
+    if out is None:
+        raise ValueError("out_index needs the destination tensor out")
+    _need(out_index, "out_index", torch.int32, (T,))
+    _need(out, "out", torch.bfloat16, (out.shape[0], H, D))
+    return out, int(out.shape[0])
+
+
 def chunk_prefill_fwd(q, k, v, g, beta, A_log, dt_bias, lower_bound, scale,
                       initial_state, cu_seqlens, out=None, final_state=None,
                       workspace=None, state_dtype=None, stream=None, vsplit: int = -1,
-                      kernel: int = KERNEL_AUTO):
-    """Run ``kda_chunk_prefill_fwd`` (``_ex`` when vsplit/kernel are overridden).
+                      kernel: int = KERNEL_AUTO, out_index=None):
+    """Run ``kda_chunk_prefill_fwd`` (``_ex`` when vsplit/kernel are overridden,
+    ``_strided`` for views, ``_scatter`` with a row map).
 
     q, k, v, g: bf16 [T, H, 128] (a leading batch dim of 1 is accepted);
     beta: bf16 [T, H]; A_log: fp32 [H]; dt_bias: fp32 [H, 128];
     initial_state: [N, H, 128, 128] fp32/bf16 or None; cu_seqlens: int32 [N+1].
-    Returns (out, final_state).  Asynchronous on ``stream`` (default: the
-    current torch stream).
+    out_index: None, or int32 [T] -- token t's output goes to out[out_index[t]], out being
+    a caller's [R, H, 128] buffer.  Returns (out, final_state).  Asynchronous on ``stream``
+    (default: the current torch stream).
     """
     squeeze = q.dim() == 4
     if squeeze:
@@ -190,6 +215,8 @@ def chunk_prefill_fwd(q, k, v, g, beta, A_log, dt_bias, lower_bound, scale,
             out = out.view(out.shape[1:])
         if beta.dim() == 3:
             beta = beta.view(beta.shape[1:])
+        if out_index is not None and out_index.dim() == 2:
+            out_index = out_index.view(out_index.shape[1:])
     T, H, D = q.shape
     if D != HEAD_DIM:
         raise KDAError(ERR_INVALID_ARG, f"head_dim {D} (only {HEAD_DIM} is supported)")
@@ -210,9 +237,7 @@ def chunk_prefill_fwd(q, k, v, g, beta, A_log, dt_bias, lower_bound, scale,
         raise TypeError("state dtype must be float32 or bfloat16")
     if initial_state is not None:
         _need(initial_state, "initial_state", state_dtype, (N, H, D, D))
-    if out is None:
-        out = torch.empty((T, H, D), dtype=torch.bfloat16, device=q.device)
-    _need(out, "out", torch.bfloat16, (T, H, D))
+    out, out_rows = _out_rows(out, out_index, T, H, D, q.device)
     if final_state is None:
         final_state = torch.empty((N, H, D, D), dtype=state_dtype, device=q.device)
     _need(final_state, "final_state", state_dtype, (N, H, D, D))
@@ -224,7 +249,10 @@ def chunk_prefill_fwd(q, k, v, g, beta, A_log, dt_bias, lower_bound, scale,
             float(lower_bound), float(scale), _ptr(initial_state), _ptr(cu_seqlens),
             _ptr(out), _ptr(final_state), sd, _ptr(workspace), ctypes.c_void_p(s.cuda_stream),
             int(T), int(N), int(H), int(workspace.numel()))
-    if not dense:
+    if out_index is not None:
+        rc = lib().kda_chunk_prefill_fwd_scatter(*args, *tok_strides, _ptr(out_index), out_rows,
+                                                 int(vsplit), int(kernel))
+    elif not dense:
         rc = lib().kda_chunk_prefill_fwd_strided(*args, *tok_strides, int(vsplit), int(kernel))
     elif vsplit == -1 and kernel == KERNEL_AUTO:
         rc = lib().kda_chunk_prefill_fwd(*args)
@@ -239,12 +267,14 @@ def chunk_prefill_fwd(q, k, v, g, beta, A_log, dt_bias, lower_bound, scale,
 
 def recurrent_fwd(q, k, v, g, beta, A_log, dt_bias, lower_bound, scale, initial_state,
                   cu_seqlens, out=None, final_state=None, token_states=False, workspace=None,
-                  state_dtype=None, stream=None):
-    """Run ``kda_recurrent_fwd`` (decode / speculative verify: a few tokens per sequence).
+                  state_dtype=None, stream=None, out_index=None):
+    """Run ``kda_recurrent_fwd`` (decode / speculative verify: a few tokens per sequence;
+    ``_scatter`` with a row map).
 
     Same tensors as chunk_prefill_fwd (dense).  token_states: False (none), True (allocate
     [T, H, 128, 128] in the state dtype) or a tensor to fill with the state after every
-    token.  Returns (out, final_state, token_states or None).
+    token.  out_index as in chunk_prefill_fwd.  Returns (out, final_state, token_states or
+    None).
     """
     if q.dim() == 4:
         q, k, v, g = (x.view(x.shape[1:]) for x in (q, k, v, g))
@@ -265,9 +295,7 @@ def recurrent_fwd(q, k, v, g, beta, A_log, dt_bias, lower_bound, scale, initial_
         raise TypeError("state dtype must be float32 or bfloat16")
     if initial_state is not None:
         _need(initial_state, "initial_state", state_dtype, (N, H, D, D))
-    if out is None:
-        out = torch.empty((T, H, D), dtype=torch.bfloat16, device=q.device)
-    _need(out, "out", torch.bfloat16, (T, H, D))
+    out, out_rows = _out_rows(out, out_index, T, H, D, q.device)
     if final_state is None:
         final_state = torch.empty((N, H, D, D), dtype=state_dtype, device=q.device)
     _need(final_state, "final_state", state_dtype, (N, H, D, D))
@@ -281,11 +309,14 @@ def recurrent_fwd(q, k, v, g, beta, A_log, dt_bias, lower_bound, scale, initial_
         workspace = torch.zeros(256, dtype=torch.uint8, device=q.device)
     _need(workspace, "workspace", torch.uint8)
     s = stream if stream is not None else torch.cuda.current_stream(q.device)
-    rc = lib().kda_recurrent_fwd(
-        _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(A_log), _ptr(dt_bias),
-        float(lower_bound), float(scale), _ptr(initial_state), _ptr(cu_seqlens), _ptr(out),
-        _ptr(final_state), sd, _ptr(token_states), _ptr(workspace),
-        ctypes.c_void_p(s.cuda_stream), int(T), int(N), int(H), int(workspace.numel()))
+    args = (_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(A_log), _ptr(dt_bias),
+            float(lower_bound), float(scale), _ptr(initial_state), _ptr(cu_seqlens), _ptr(out),
+            _ptr(final_state), sd, _ptr(token_states), _ptr(workspace),
+            ctypes.c_void_p(s.cuda_stream), int(T), int(N), int(H), int(workspace.numel()))
+    if out_index is not None:
+        rc = lib().kda_recurrent_fwd_scatter(*args, _ptr(out_index), out_rows)
+    else:
+        rc = lib().kda_recurrent_fwd(*args)
     if rc != OK:
         raise KDAError(rc, "kda_recurrent_fwd")
     return out, final_state, token_states

@@ -116,11 +116,16 @@ int fwd_impl(const void* q, const void* k, const void* v, const void* g, const v
              const void* initial_state, const int32_t* cu_seqlens, void* out, void* final_state,
              int state_dtype, void* workspace, kda_stream_t stream, int64_t total_tokens,
              int32_t num_seqs, int32_t heads, size_t workspace_bytes, int vsplit, int kernel,
-             const int64_t* strides) {
+             const int64_t* strides, bool scatter = false, const int32_t* out_index = nullptr,
+             int64_t out_rows = 0) {
   int rc = validate(q, k, v, g, beta, A_log, dt_bias, lower_bound, scale, initial_state,
                     cu_seqlens, out, final_state, state_dtype, workspace, total_tokens,
                     num_seqs, heads, workspace_bytes);
   if (rc != KDA_OK) return rc;
+  if (scatter) {
+    if (!out_index || out_rows < 0) return KDA_ERR_INVALID_ARG;
+    if (!aligned(out_index, 4)) return KDA_ERR_MISALIGNED;
+  }
   // token strides (elements) of q, k, v, g, beta; NULL = dense
   int64_t st[5] = {(int64_t)heads * kda::kHeadDim, (int64_t)heads * kda::kHeadDim,
                    (int64_t)heads * kda::kHeadDim, (int64_t)heads * kda::kHeadDim, heads};
@@ -178,12 +183,71 @@ int fwd_impl(const void* q, const void* k, const void* v, const void* g, const v
   p.s_g = st[3];
   p.s_beta = st[4];
   p.helpers = (kernel == KDA_KERNEL_TC_HELPERS && total_tokens > 0) ? 1 : 0;
+  p.out_index = scatter ? out_index : nullptr;
+  p.out_rows = out_rows;
 
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   cudaError_t err = (kernel == KDA_KERNEL_REF)     ? kda::launch_ref(p, s)
                     : (kernel == KDA_KERNEL_SPLIT) ? kda::launch_split(p, s)
                                                    : kda::launch_tc(p, s);
   if (err != cudaSuccess) {
+    cudaGetLastError();
+    return KDA_ERR_LAUNCH_FAILED;
+  }
+  return KDA_OK;
+}
+
+int recurrent_impl(const void* q, const void* k, const void* v, const void* g, const void* beta,
+                   const float* A_log, const float* dt_bias, float lower_bound, float scale,
+                   const void* initial_state, const int32_t* cu_seqlens, void* out,
+                   void* final_state, int state_dtype, void* token_states, void* workspace,
+                   kda_stream_t stream, int64_t total_tokens, int32_t num_seqs, int32_t heads,
+                   size_t workspace_bytes, bool scatter, const int32_t* out_index,
+                   int64_t out_rows) {
+  int rc = validate(q, k, v, g, beta, A_log, dt_bias, lower_bound, scale, initial_state,
+                    cu_seqlens, out, final_state, state_dtype, workspace, total_tokens,
+                    num_seqs, heads, workspace_bytes);
+  if (rc != KDA_OK) return rc;
+  if (scatter) {
+    if (!out_index || out_rows < 0) return KDA_ERR_INVALID_ARG;
+    if (!aligned(out_index, 4)) return KDA_ERR_MISALIGNED;
+  }
+  if (token_states && !aligned(token_states, 16)) return KDA_ERR_MISALIGNED;
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return KDA_ERR_CUDA;
+  }
+  rc = check_device(dev, &sms);
+  if (rc != KDA_OK) return rc;
+  if (num_seqs == 0) return KDA_OK;
+  kda::Params p{};
+  p.q = static_cast<const __nv_bfloat16*>(q);
+  p.k = static_cast<const __nv_bfloat16*>(k);
+  p.v = static_cast<const __nv_bfloat16*>(v);
+  p.g = static_cast<const __nv_bfloat16*>(g);
+  p.beta = static_cast<const __nv_bfloat16*>(beta);
+  p.A_log = A_log;
+  p.dt_bias = dt_bias;
+  p.lower_bound = lower_bound;
+  p.scale = scale;
+  p.initial_state = initial_state;
+  p.cu_seqlens = cu_seqlens;
+  p.out = static_cast<__nv_bfloat16*>(out);
+  p.final_state = final_state;
+  p.state_bf16 = state_dtype == KDA_STATE_BF16 ? 1 : 0;
+  p.status = static_cast<int*>(workspace);
+  p.total_tokens = total_tokens;
+  p.num_seqs = num_seqs;
+  p.heads = heads;
+  p.vsplit = 1;
+  p.sm_count = sms;
+  p.s_q = p.s_k = p.s_v = p.s_g = (int64_t)heads * kda::kHeadDim;
+  p.s_beta = heads;
+  p.out_index = scatter ? out_index : nullptr;
+  p.out_rows = out_rows;
+  if (kda::launch_recurrent(p, token_states, reinterpret_cast<cudaStream_t>(stream)) !=
+      cudaSuccess) {
     cudaGetLastError();
     return KDA_ERR_LAUNCH_FAILED;
   }
@@ -257,6 +321,24 @@ int kda_chunk_prefill_fwd_strided(const void* q, const void* k, const void* v, c
                   num_seqs, heads, workspace_bytes, vsplit, kernel, strides);
 }
 
+int kda_chunk_prefill_fwd_scatter(const void* q, const void* k, const void* v, const void* g,
+                                  const void* beta, const float* A_log, const float* dt_bias,
+                                  float lower_bound, float scale, const void* initial_state,
+                                  const int32_t* cu_seqlens, void* out, void* final_state,
+                                  int state_dtype, void* workspace, kda_stream_t stream,
+                                  int64_t total_tokens, int32_t num_seqs, int32_t heads,
+                                  size_t workspace_bytes, int64_t q_stride, int64_t k_stride,
+                                  int64_t v_stride, int64_t g_stride, int64_t beta_stride,
+                                  const int32_t* out_index, int64_t out_rows, int vsplit,
+                                  int kernel) {
+  const int64_t strides[5] = {q_stride, k_stride, v_stride, g_stride, beta_stride};
+  return fwd_impl(q, k, v, g, beta, A_log, dt_bias, lower_bound, scale, initial_state,
+                  cu_seqlens, out, final_state, state_dtype, workspace, stream, total_tokens,
+                  num_seqs, heads, workspace_bytes, vsplit, kernel, strides, true, out_index,
+                  out_rows);
+}
+
+
 int kda_recurrent_fwd(const void* q, const void* k, const void* v, const void* g,
                       const void* beta, const float* A_log, const float* dt_bias,
                       float lower_bound, float scale, const void* initial_state,
@@ -264,48 +346,24 @@ int kda_recurrent_fwd(const void* q, const void* k, const void* v, const void* g
                       void* token_states, void* workspace, kda_stream_t stream,
                       int64_t total_tokens, int32_t num_seqs, int32_t heads,
                       size_t workspace_bytes) {
-  int rc = validate(q, k, v, g, beta, A_log, dt_bias, lower_bound, scale, initial_state,
-                    cu_seqlens, out, final_state, state_dtype, workspace, total_tokens,
-                    num_seqs, heads, workspace_bytes);
-  if (rc != KDA_OK) return rc;
-  if (token_states && !aligned(token_states, 16)) return KDA_ERR_MISALIGNED;
-  int dev = 0, sms = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) {
-    cudaGetLastError();
-    return KDA_ERR_CUDA;
-  }
-  rc = check_device(dev, &sms);
-  if (rc != KDA_OK) return rc;
-  if (num_seqs == 0) return KDA_OK;
-  kda::Params p{};
-  p.q = static_cast<const __nv_bfloat16*>(q);
-  p.k = static_cast<const __nv_bfloat16*>(k);
-  p.v = static_cast<const __nv_bfloat16*>(v);
-  p.g = static_cast<const __nv_bfloat16*>(g);
-  p.beta = static_cast<const __nv_bfloat16*>(beta);
-  p.A_log = A_log;
-  p.dt_bias = dt_bias;
-  p.lower_bound = lower_bound;
-  p.scale = scale;
-  p.initial_state = initial_state;
-  p.cu_seqlens = cu_seqlens;
-  p.out = static_cast<__nv_bfloat16*>(out);
-  p.final_state = final_state;
-  p.state_bf16 = state_dtype == KDA_STATE_BF16 ? 1 : 0;
-  p.status = static_cast<int*>(workspace);
-  p.total_tokens = total_tokens;
-  p.num_seqs = num_seqs;
-  p.heads = heads;
-  p.vsplit = 1;
-  p.sm_count = sms;
-  p.s_q = p.s_k = p.s_v = p.s_g = (int64_t)heads * kda::kHeadDim;
-  p.s_beta = heads;
-  if (kda::launch_recurrent(p, token_states, reinterpret_cast<cudaStream_t>(stream)) !=
-      cudaSuccess) {
-    cudaGetLastError();
-    return KDA_ERR_LAUNCH_FAILED;
-  }
-  return KDA_OK;
+  return recurrent_impl(q, k, v, g, beta, A_log, dt_bias, lower_bound, scale, initial_state,
+                        cu_seqlens, out, final_state, state_dtype, token_states, workspace,
+                        stream, total_tokens, num_seqs, heads, workspace_bytes, false, nullptr,
+                        0);
+}
+
+int kda_recurrent_fwd_scatter(const void* q, const void* k, const void* v, const void* g,
+                              const void* beta, const float* A_log, const float* dt_bias,
+                              float lower_bound, float scale, const void* initial_state,
+                              const int32_t* cu_seqlens, void* out, void* final_state,
+                              int state_dtype, void* token_states, void* workspace,
+                              kda_stream_t stream, int64_t total_tokens, int32_t num_seqs,
+                              int32_t heads, size_t workspace_bytes, const int32_t* out_index,
+                              int64_t out_rows) {
+  return recurrent_impl(q, k, v, g, beta, A_log, dt_bias, lower_bound, scale, initial_state,
+                        cu_seqlens, out, final_state, state_dtype, token_states, workspace,
+                        stream, total_tokens, num_seqs, heads, workspace_bytes, true, out_index,
+                        out_rows);
 }
 
 int kda_choose_vsplit(int32_t num_seqs, int32_t heads, int32_t sm_count) {
@@ -329,6 +387,7 @@ const char* kda_status_string(int status) {
     case KDA_ERR_DEVICE_TIMEOUT: return "a bounded device-side wait timed out";
     case KDA_ERR_BAD_CU_SEQLENS: return "cu_seqlens not non-decreasing from 0 or past total_tokens";
     case KDA_ERR_CUDA: return "CUDA runtime error";
+    case KDA_ERR_BAD_OUT_INDEX: return "an out_index entry lies outside [0, out_rows)";
     default: return "unknown status";
   }
 }

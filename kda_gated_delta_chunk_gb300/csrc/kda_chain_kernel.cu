@@ -295,14 +295,16 @@ __global__ void __launch_bounds__(NT2, 1)
       }
       const int r0 = 16 * mt + g;
       const float iq0 = vec[128 + r0], iq1 = vec[128 + r0 + 8];
+      const int64_t row0 = (r0 < L) ? out_row(p, c0 + r0) : -1;
+      const int64_t row1 = (r0 + 8 < L) ? out_row(p, c0 + r0 + 8) : -1;
 #pragma unroll
       for (int j = 0; j < NPW; ++j) {
         const int c = dv0 + 8 * (ng + 2 * j) + 2 * t;
-        if (r0 < L)
-          *reinterpret_cast<uint32_t*>(p.out + (size_t)(c0 + r0) * HD + h * 128 + c) =
+        if (row0 >= 0)
+          *reinterpret_cast<uint32_t*>(p.out + (size_t)row0 * HD + h * 128 + c) =
               bf2(O[j][0] * iq0, O[j][1] * iq0);
-        if (r0 + 8 < L)
-          *reinterpret_cast<uint32_t*>(p.out + (size_t)(c0 + r0 + 8) * HD + h * 128 + c) =
+        if (row1 >= 0)
+          *reinterpret_cast<uint32_t*>(p.out + (size_t)row1 * HD + h * 128 + c) =
               bf2(O[j][2] * iq1, O[j][3] * iq1);
       }
     }

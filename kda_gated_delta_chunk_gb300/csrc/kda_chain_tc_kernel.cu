@@ -41,7 +41,8 @@ constexpr int OFF_TSLOT3 = OFF_MISC3 + 32;
 constexpr int OFF_FLAGS3 = OFF_MISC3 + 48;
 constexpr int OFF_LENS3 = OFF_MISC3 + 64;           // sequence lengths for the ordering
 constexpr int OFF_IQ3 = OFF_LENS3 + 4 * kMaxRankSeqs3;   // scale/|q| of the last two chunks [2][64]
-constexpr int SMEM3_USED = OFF_IQ3 + 2 * 64 * 4;
+constexpr int OFF_OROW3 = OFF_IQ3 + 2 * 64 * 4;      // out rows of the last two chunks [2][64]
+constexpr int SMEM3_USED = OFF_OROW3 + 2 * 64 * 4;
 constexpr int SMEM3_BYTES = SMEM3_USED + 1024;
 static_assert(STAGE_V % 1024 == 0 && STAGE_BYTES % 1024 == 0, "stage alignment");
 static_assert(SMEM3_BYTES <= 227 * 1024, "shared memory");
@@ -185,6 +186,9 @@ __global__ void __launch_bounds__(NT3, 1)
     tmem_wait_st();
   }
 
+  // out rows of the next chunk (threads < 64, row map only), loaded a chunk ahead
+  int next_orow = -1;
+  if (p.out_index && tid < kChunk && tid < t1 - t0) next_orow = (int)out_row(p, t0 + tid);
   uint32_t phase = 0;        // bit b: parity of stage b's next fill
   uint32_t ph_mma = 0;
   bool failed = false;
@@ -215,15 +219,18 @@ __global__ void __launch_bounds__(NT3, 1)
       }
     }
   };
-  // staging -> out rows [c0, c0 + L) (all threads, 16-byte stores)
-  auto store_o = [&](int c0, int L) {
+  // staging -> out rows of tokens [c0, c0 + L) (all threads, 16-byte stores); with an
+  // out_index map the rows come from orow[b] (chunk parity b)
+  const int* orow = reinterpret_cast<const int*>(sm + OFF_OROW3);
+  auto store_o = [&](int c0, int L, int b) {
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
       const int idx = tid + k * NT3;
       const int r = idx >> 4, v8 = idx & 15;
-      if (r < L) {
+      const int64_t row = p.out_index ? (int64_t)orow[b * 64 + r] : (int64_t)(c0 + r);
+      if (r < L && row >= 0) {
         const uint4 val = *reinterpret_cast<const uint4*>(sm + OFF_OST + r * 256 + v8 * 16);
-        *reinterpret_cast<uint4*>(p.out + (size_t)(c0 + r) * HD + xcol + v8 * 8) = val;
+        *reinterpret_cast<uint4*>(p.out + (size_t)row * HD + xcol + v8 * 8) = val;
       }
     }
   };
@@ -244,8 +251,15 @@ __global__ void __launch_bounds__(NT3, 1)
       phase ^= 1u << buf;
       pending &= ~(1 << buf);
     }
-    // scale/|q| of this chunk, kept past the stage's reuse (O is drained during the next chunk)
-    if (tid < kChunk) iqs[buf * 64 + tid] = vec[128 + tid];
+    // scale/|q| (and out rows) of this chunk, kept past the stage's reuse (O is drained
+    // during the next chunk)
+    if (tid < kChunk) {
+      iqs[buf * 64 + tid] = vec[128 + tid];
+      if (p.out_index) {   // this chunk's out rows (loaded a chunk ahead), then the next's
+        reinterpret_cast<int*>(sm + OFF_OROW3)[buf * 64 + tid] = next_orow;
+        next_orow = (c0 + kChunk + tid < t1) ? (int)out_row(p, c0 + kChunk + tid) : -1;
+      }
+    }
     if (L < kChunk) {   // v rows past the sequence end -> 0 (both 64-column boxes)
       for (int idx = tid; idx < (kChunk - L) * 16; idx += NT3) {
         const int r = L + idx / 16, cc = idx % 16;
@@ -298,7 +312,7 @@ __global__ void __launch_bounds__(NT3, 1)
       }
       if (i + 3 < nch) prefetch_l2(i + 3);
     }
-    if (i > 0) store_o(c0 - kChunk, L_prev);
+    if (i > 0) store_o(c0 - kChunk, L_prev, buf ^ 1);
     {
       const bool ok = tid != 0 || mbar_wait(bar_u, ph_mma);
       tc_fence_before();
@@ -361,7 +375,7 @@ __global__ void __launch_bounds__(NT3, 1)
       const int last = nch - 1;
       drain_o(reinterpret_cast<const float*>(sm + OFF_IQ3) + (last & 1) * 64);
       __syncthreads();
-      store_o(t0 + kChunk * last, L_prev);
+      store_o(t0 + kChunk * last, L_prev, last & 1);
     }
     // ---- state out
     const int dv = my_lane;

@@ -57,6 +57,10 @@ struct Params {
   int64_t s_q, s_k, s_v, s_g, s_beta;
   // 1: the fused kernel shares the chunk-local work with k-side helper CTAs (P = 1 only)
   int32_t helpers;
+  // optional output row map: token t's output row goes to out[out_index[t]], out being
+  // [out_rows, H, 128]; null: to out[t]
+  const int32_t* out_index;
+  int64_t out_rows;
 };
 
 // Record a device-side error (first writer wins) with its block and site.
@@ -65,6 +69,18 @@ __device__ __forceinline__ void record_error(int* status, int code, int site) {
     status[1] = (int)(blockIdx.x + gridDim.x * (blockIdx.y + gridDim.y * blockIdx.z));
     status[2] = site;
   }
+}
+
+// Row of `out` that token t's output goes to: t, or out_index[t].  An index outside
+// [0, out_rows) records KDA_ERR_BAD_OUT_INDEX and gives -1 (the row is not written).
+__device__ __forceinline__ int64_t out_row(const Params& p, int64_t t) {
+  if (!p.out_index) return t;
+  const int r = p.out_index[t];
+  if (r < 0 || (int64_t)r >= p.out_rows) {
+    record_error(p.status, KDA_ERR_BAD_OUT_INDEX, 90);
+    return -1;
+  }
+  return r;
 }
 
 cudaError_t launch_ref(const Params& p, cudaStream_t stream);

@@ -544,21 +544,16 @@ __global__ void __launch_bounds__(NT, 2)
     if (warp < 4) {
       if (warp < 2) {
         const int o = (tid >> 4) * 16, j = tid & 15;
+        // column j of the block's inverse by forward substitution, right-looking: once x[k]
+        // is final its term leaves every later row at once (each row still subtracts its
+        // terms in the order k = 0, 1, ...; the dependent chain is 16 steps, not 120)
         float x[16];
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          float acc = (i == j) ? 1.0f : 0.0f;
+        for (int i = 0; i < 16; ++i) x[i] = (i == j) ? 1.0f : 0.0f;
 #pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            if (4 * q < i) {
-              const float4 nv = ld4(Nm + (o + i) * NS + o + 4 * q);
-              if (4 * q + 0 < i) acc -= nv.x * x[4 * q + 0];
-              if (4 * q + 1 < i) acc -= nv.y * x[4 * q + 1];
-              if (4 * q + 2 < i) acc -= nv.z * x[4 * q + 2];
-              if (4 * q + 3 < i) acc -= nv.w * x[4 * q + 3];
-            }
-          }
-          x[i] = acc;
+        for (int k = 0; k < 15; ++k) {
+#pragma unroll
+          for (int i = k + 1; i < 16; ++i) x[i] = fmaf(-Nm[(o + i) * NS + o + k], x[k], x[i]);
         }
 #pragma unroll
         for (int i = 0; i < 16; ++i) Tm[(o + i) * NS + o + j] = x[i];

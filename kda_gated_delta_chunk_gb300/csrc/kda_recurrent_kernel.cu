@@ -138,7 +138,8 @@ __global__ void __launch_bounds__(RT)
     __syncthreads();
     if (warp == 0) {
       const float ot = (red[0][lane] + red[1][lane]) + (red[2][lane] + red[3][lane]);
-      p.out[(size_t)t * H * kHeadDim + hoff + dv] = __float2bfloat16_rn(ot);
+      const int64_t row = out_row(p, t);
+      if (row >= 0) p.out[(size_t)row * H * kHeadDim + hoff + dv] = __float2bfloat16_rn(ot);
     }
     if (token_states) store_state(token_states, ((size_t)t * H + h) * HD2 + dv);
     __syncthreads();   // red, nrm, qs, ks, ds are rewritten by the next token

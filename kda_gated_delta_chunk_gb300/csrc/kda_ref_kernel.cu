@@ -206,7 +206,8 @@ __global__ void __launch_bounds__(RT, 1) kda_ref_chunk_kernel(Params p) {
         float acc = 0.f;
         for (int d = 0; d < D; ++d) acc += sm.qh[r][d] * sm.S[d][c];
         for (int s = 0; s <= r; ++s) acc += sm.QK[r][s] * sm.u[s][c];
-        p.out[(size_t)(c0 + r) * HD + (size_t)h * D + dv0 + c] = __float2bfloat16_rn(acc);
+        const int64_t row = out_row(p, c0 + r);
+        if (row >= 0) p.out[(size_t)row * HD + (size_t)h * D + dv0 + c] = __float2bfloat16_rn(acc);
       }
     }
     for (int i = tid; i < RC * D; i += RT) {

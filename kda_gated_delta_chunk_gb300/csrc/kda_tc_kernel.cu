@@ -96,7 +96,8 @@ constexpr int OFF_TSLOT = OFF_MISC + 7968;  // TMEM base address
 constexpr int OFF_FLAGS = OFF_MISC + 7972;  // [0] sequence chosen for this CTA, [1] record mode
 constexpr int OFF_BAR_REC = OFF_MISC + 7984;   // 2 mbarriers: record buffers 0, 1
 constexpr int OFF_RSC = OFF_MISC + 8192;    // per-row power-of-two operand scales, bf16x2 [q 64][k 64]
-constexpr int SMEM_USED = OFF_RSC + 512;
+constexpr int OFF_OROW = OFF_RSC + 512;     // out rows of the chunk's tokens [2 by chunk parity][64]
+constexpr int SMEM_USED = OFF_OROW + 512;
 constexpr int SMEM_BYTES = SMEM_USED + 1024;
 static_assert(OFF_Y + 32 * NS * 4 <= OFF_TB, "T scratch overlaps T diag(b)");
 static_assert(OFF_CKC + 24576 <= OFF_TB, "operands overlap T diag(b)");
@@ -109,6 +110,7 @@ constexpr int OFF_REC1 = OFF_RA + kRecBytes;
 constexpr int OFF_OSTR = OFF_INQ;
 static_assert(kRecBytes % 1024 == 0 && OFF_REC1 + kRecBytes <= OFF_MISC, "record buffers");
 static_assert(OFF_BAR_REC + 16 <= OFF_RSC && OFF_FLAGS + 8 <= OFF_BAR_REC, "misc");
+static_assert(OFF_OROW + 512 == SMEM_USED, "out rows");
 
 // ---- TMEM columns (fp32 unless noted; lane = value channel, or key channel for D/W)
 // [U^T | O^T] and [O^T | S^T] are each one contiguous accumulator
@@ -144,6 +146,7 @@ __global__ void __launch_bounds__(NT, 1)
   float* gt = reinterpret_cast<float*>(sm + OFF_GT);
   float* part = reinterpret_cast<float*>(sm + OFF_PART);
   uint32_t* rsc = reinterpret_cast<uint32_t*>(sm + OFF_RSC);
+  int* orow = reinterpret_cast<int*>(sm + OFF_OROW);   // used when an out_index map is given
   int* flags = reinterpret_cast<int*>(sm + OFF_FLAGS);
   uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + OFF_TSLOT);
   const uint32_t bar_qkg = sb + OFF_BAR, bar_v = bar_qkg + 8, bar_mma = bar_qkg + 16;
@@ -257,6 +260,9 @@ __global__ void __launch_bounds__(NT, 1)
     return true;
   };
 
+  // out rows of the next chunk to start, loaded a chunk ahead (threads < 64, row map only)
+  int next_orow = -1;
+  if (p.out_index && tid < C && tid < t1 - t0) next_orow = (int)out_row(p, t0 + tid);
   if (tid == 0) {
     flags[1] = 0;                              // 1: this and every later chunk from records
     if (nch > 0) {
@@ -338,6 +344,7 @@ __global__ void __launch_bounds__(NT, 1)
     if (tid < C) {
       beta_s[tid] = (tid < L) ? sigm(b_raw) : 0.0f;
       if (c0 + C + tid < t1) b_raw = __bfloat162float(p.beta[(size_t)(c0 + C + tid) * p.s_beta + h]);
+      if (p.out_index) orow[(c & 1) * C + tid] = next_orow;
     }
     if (L < C) {
       for (int idx = tid; idx < (C - L) * 32; idx += NT) {
@@ -408,6 +415,9 @@ __global__ void __launch_bounds__(NT, 1)
       rsc[t * 64 + r] = b | (b << 16);
     }
     __syncthreads();
+
+    if (p.out_index && tid < C)   // the next chunk's out rows (used from its P0 on)
+      next_orow = (more && c0 + C + tid < t1) ? (int)out_row(p, c0 + C + tid) : -1;
 
     // ---- P2b: anchored factors, bf16 operand tiles of the (power-of-two scaled) q, k rows
     //           (their norms are applied to the products later)
@@ -574,21 +584,16 @@ __global__ void __launch_bounds__(NT, 1)
     if (warp < 4) {
       if (warp < 2) {
         const int o = (tid >> 4) * 16, j = tid & 15;
+        // column j of the block's inverse by forward substitution, right-looking: once x[k]
+        // is final its term leaves every later row at once (each row still subtracts its
+        // terms in the order k = 0, 1, ...; the dependent chain is 16 steps, not 120)
         float x[16];
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          float acc = (i == j) ? 1.0f : 0.0f;
+        for (int i = 0; i < 16; ++i) x[i] = (i == j) ? 1.0f : 0.0f;
 #pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            if (4 * q < i) {
-              const float4 nv = ld4(Nm + (o + i) * NS + o + 4 * q);
-              if (4 * q + 0 < i) acc -= nv.x * x[4 * q + 0];
-              if (4 * q + 1 < i) acc -= nv.y * x[4 * q + 1];
-              if (4 * q + 2 < i) acc -= nv.z * x[4 * q + 2];
-              if (4 * q + 3 < i) acc -= nv.w * x[4 * q + 3];
-            }
-          }
-          x[i] = acc;
+        for (int k = 0; k < 15; ++k) {
+#pragma unroll
+          for (int i = k + 1; i < 16; ++i) x[i] = fmaf(-Nm[(o + i) * NS + o + k], x[k], x[i]);
         }
 #pragma unroll
         for (int i = 0; i < 16; ++i) Tm[(o + i) * NS + o + j] = x[i];
@@ -797,9 +802,10 @@ __global__ void __launch_bounds__(NT, 1)
     for (int k2 = 0; k2 < 2; ++k2) {
       const int idx = tid + k2 * NT;
       const int r = idx >> 4, v8 = idx & 15;
-      if (r < L && v8 * 8 >= dv_lo && v8 * 8 < dv_hi) {
+      const int64_t row = p.out_index ? (int64_t)orow[(c & 1) * C + r] : (int64_t)(c0 + r);
+      if (r < L && row >= 0 && v8 * 8 >= dv_lo && v8 * 8 < dv_hi) {
         const uint4 val = *reinterpret_cast<const uint4*>(sm + OFF_RKQ + r * 256 + v8 * 16);
-        *reinterpret_cast<uint4*>(p.out + (size_t)(c0 + r) * HD + xcol + v8 * 8) = val;
+        *reinterpret_cast<uint4*>(p.out + (size_t)row * HD + xcol + v8 * 8) = val;
       }
     }
     __syncthreads();
@@ -835,7 +841,10 @@ __global__ void __launch_bounds__(NT, 1)
       }
       fence_proxy_async();
     }
+    if (p.out_index && tid < C) orow[(c & 1) * C + tid] = next_orow;
     if (__syncthreads_or(!ok)) { failed = true; site = 80; break; }
+    if (p.out_index && tid < C)   // the next chunk's out rows
+      next_orow = (more && c0 + C + tid < t1) ? (int)out_row(p, c0 + C + tid) : -1;
     if (tid == 0 && c + 2 < nch) {   // v two chunks ahead -> L2 (its TMA is issued in R3 below)
       tma_prefetch_2d(&tm_v, xcol, c0 + 2 * C);
       tma_prefetch_2d(&tm_v, xcol + 64, c0 + 2 * C);
@@ -917,9 +926,11 @@ __global__ void __launch_bounds__(NT, 1)
       for (int k2 = 0; k2 < 2; ++k2) {
         const int idx = tid + k2 * NT;
         const int r = idx >> 4, v8 = idx & 15;
-        if (r < L_prev) {
+        const int64_t row =
+            p.out_index ? (int64_t)orow[((c - 1) & 1) * C + r] : (int64_t)(c0 - C + r);
+        if (r < L_prev && row >= 0) {
           const uint4 val = *reinterpret_cast<const uint4*>(sm + OFF_OSTR + r * 256 + v8 * 16);
-          *reinterpret_cast<uint4*>(p.out + (size_t)(c0 - C + r) * HD + xcol + v8 * 8) = val;
+          *reinterpret_cast<uint4*>(p.out + (size_t)row * HD + xcol + v8 * 8) = val;
         }
       }
     }
@@ -997,9 +1008,11 @@ __global__ void __launch_bounds__(NT, 1)
     for (int k2 = 0; k2 < 2; ++k2) {
       const int idx = tid + k2 * NT;
       const int r2 = idx >> 4, v8 = idx & 15;
-      if (r2 < L_prev) {
+      const int64_t row =
+          p.out_index ? (int64_t)orow[((nch - 1) & 1) * C + r2] : (int64_t)(c0 + r2);
+      if (r2 < L_prev && row >= 0) {
         const uint4 val = *reinterpret_cast<const uint4*>(sm + OFF_OSTR + r2 * 256 + v8 * 16);
-        *reinterpret_cast<uint4*>(p.out + (size_t)(c0 + r2) * HD + xcol + v8 * 8) = val;
+        *reinterpret_cast<uint4*>(p.out + (size_t)row * HD + xcol + v8 * 8) = val;
       }
     }
   }

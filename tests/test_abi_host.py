@@ -104,7 +104,7 @@ def test_vsplit_factor_values(L):
 
 
 def test_status_strings(L):
-    for code in range(-9, 1):
+    for code in range(-10, 1):
         assert kda.status_string(code) and kda.status_string(code) != "unknown status"
     assert kda.status_string(-99) == "unknown status"
 
@@ -192,3 +192,35 @@ def test_recurrent_argument_gate(L):
     base[7] = -7.0
     assert L.kda_recurrent_fwd(*base, P(None), P(0xC0000), P(None), 4, 1, 2, 256) == \
         kda.ERR_UNSAFE_LOWER_BOUND
+
+
+def _call_scatter(L, index, rows):
+    P = ctypes.c_void_p
+    return L.kda_chunk_prefill_fwd_scatter(
+        P(0x10000), P(0x20000), P(0x30000), P(0x40000), P(0x50000), P(0x60000), P(0x70000),
+        -5.0, 128 ** -0.5, P(0x80000), P(0x90000), P(0xA0000), P(0xB0000), 0, P(0xC0000),
+        P(None), 64, 1, 2, kda.workspace_size(64, 2, 1), 256, 256, 256, 256, 2, P(index),
+        rows, -1, 0)
+
+
+@pytest.mark.parametrize("index,rows,code", [
+    (None, 64, kda.ERR_INVALID_ARG),        # the map is required
+    (0xD0000, -1, kda.ERR_INVALID_ARG),     # negative row count
+    (0xD0002, 64, kda.ERR_MISALIGNED),      # int32 map: 4-byte aligned
+])
+def test_scatter_argument_gate(L, index, rows, code):
+    """kda_chunk_prefill_fwd_scatter / kda_recurrent_fwd_scatter refuse a missing or
+    misaligned row map and a negative row count on the host."""
+    assert _call_scatter(L, index, rows) == code
+    P = ctypes.c_void_p
+    base = [P(0x10000), P(0x20000), P(0x30000), P(0x40000), P(0x50000), P(0x60000),
+            P(0x70000), -5.0, 128 ** -0.5, P(0x80000), P(0x90000), P(0xA0000), P(0xB0000), 0,
+            P(None), P(0xC0000), P(None), 4, 1, 2, 256]
+    assert L.kda_recurrent_fwd_scatter(*base, P(index), rows) == code
+
+
+def test_scatter_valid_arguments_reach_the_device_check(L):
+    import torch
+    rc = _call_scatter(L, 0xD0000, 64)
+    if not torch.cuda.is_available():
+        assert rc in (kda.ERR_CUDA, kda.ERR_UNSUPPORTED_DEVICE)
