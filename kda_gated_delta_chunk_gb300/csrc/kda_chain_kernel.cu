@@ -89,7 +89,8 @@ struct ChainMaps {
   CUtensorMap v;        // v as [T][H*128] bf16, box {DV, 64}
 };
 
-template <int DV>
+// kRowMap: outputs through the out_index row map (its own instantiation)
+template <int DV, bool kRowMap>
 __global__ void __launch_bounds__(NT2, 1)
     kda_chain_kernel(const __grid_constant__ Params p, const __grid_constant__ ChainMaps maps) {
   using L_ = ChainSmem<DV>;
@@ -295,15 +296,21 @@ __global__ void __launch_bounds__(NT2, 1)
       }
       const int r0 = 16 * mt + g;
       const float iq0 = vec[128 + r0], iq1 = vec[128 + r0 + 8];
-      const int64_t row0 = (r0 < L) ? out_row(p, c0 + r0) : -1;
-      const int64_t row1 = (r0 + 8 < L) ? out_row(p, c0 + r0 + 8) : -1;
+      int64_t row0 = c0 + r0, row1 = c0 + r0 + 8;
+      bool w0 = r0 < L, w1 = r0 + 8 < L;
+      if (kRowMap) {
+        row0 = w0 ? out_row(p, row0) : -1;
+        row1 = w1 ? out_row(p, row1) : -1;
+        w0 = row0 >= 0;
+        w1 = row1 >= 0;
+      }
 #pragma unroll
       for (int j = 0; j < NPW; ++j) {
         const int c = dv0 + 8 * (ng + 2 * j) + 2 * t;
-        if (row0 >= 0)
+        if (w0)
           *reinterpret_cast<uint32_t*>(p.out + (size_t)row0 * HD + h * 128 + c) =
               bf2(O[j][0] * iq0, O[j][1] * iq0);
-        if (row1 >= 0)
+        if (w1)
           *reinterpret_cast<uint32_t*>(p.out + (size_t)row1 * HD + h * 128 + c) =
               bf2(O[j][2] * iq1, O[j][3] * iq1);
       }
@@ -399,14 +406,19 @@ cudaError_t launch_chain_dv(const Params& p, cudaStream_t stream) {
   if (e != cudaSuccess) return e;
   constexpr int smem = ChainSmem<DV>::BYTES;
   if (dev >= 0 && dev < 64 && !attr_set[dev]) {
-    e = cudaFuncSetAttribute(kda_chain_kernel<DV>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return e;
+    for (auto fn : {kda_chain_kernel<DV, false>, kda_chain_kernel<DV, true>}) {
+      e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+      if (e != cudaSuccess) return e;
+    }
     attr_set[dev] = true;
   }
   ChainMaps maps;
   if (!make_chain_maps(&maps, p, DV)) return cudaErrorInvalidValue;
   const long long blocks = (long long)p.num_seqs * p.heads * (128 / DV);
-  kda_chain_kernel<DV><<<(unsigned)blocks, NT2, smem, stream>>>(p, maps);
+  if (p.out_index)
+    kda_chain_kernel<DV, true><<<(unsigned)blocks, NT2, smem, stream>>>(p, maps);
+  else
+    kda_chain_kernel<DV, false><<<(unsigned)blocks, NT2, smem, stream>>>(p, maps);
   return cudaGetLastError();
 }
 

@@ -73,6 +73,9 @@ struct ChainTcMaps {
   CUtensorMap v;   // v as [T][H*128] bf16, box {64, 64}, 128-byte swizzle
 };
 
+// kRowMap: outputs go through the out_index row map (a separate instantiation, so that
+// the dense kernel carries none of it)
+template <bool kRowMap>
 __global__ void __launch_bounds__(NT3, 1)
     kda_chain_tc_kernel(const __grid_constant__ Params p, const __grid_constant__ ChainTcMaps maps) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
@@ -188,7 +191,7 @@ __global__ void __launch_bounds__(NT3, 1)
 
   // out rows of the next chunk (threads < 64, row map only), loaded a chunk ahead
   int next_orow = -1;
-  if (p.out_index && tid < kChunk && tid < t1 - t0) next_orow = (int)out_row(p, t0 + tid);
+  if (kRowMap && tid < kChunk && tid < t1 - t0) next_orow = (int)out_row(p, t0 + tid);
   uint32_t phase = 0;        // bit b: parity of stage b's next fill
   uint32_t ph_mma = 0;
   bool failed = false;
@@ -227,7 +230,7 @@ __global__ void __launch_bounds__(NT3, 1)
     for (int k = 0; k < 4; ++k) {
       const int idx = tid + k * NT3;
       const int r = idx >> 4, v8 = idx & 15;
-      const int64_t row = p.out_index ? (int64_t)orow[b * 64 + r] : (int64_t)(c0 + r);
+      const int64_t row = kRowMap ? (int64_t)orow[b * 64 + r] : (int64_t)(c0 + r);
       if (r < L && row >= 0) {
         const uint4 val = *reinterpret_cast<const uint4*>(sm + OFF_OST + r * 256 + v8 * 16);
         *reinterpret_cast<uint4*>(p.out + (size_t)row * HD + xcol + v8 * 8) = val;
@@ -255,7 +258,7 @@ __global__ void __launch_bounds__(NT3, 1)
     // during the next chunk)
     if (tid < kChunk) {
       iqs[buf * 64 + tid] = vec[128 + tid];
-      if (p.out_index) {   // this chunk's out rows (loaded a chunk ahead), then the next's
+      if (kRowMap) {   // this chunk's out rows (loaded a chunk ahead), then the next's
         reinterpret_cast<int*>(sm + OFF_OROW3)[buf * 64 + tid] = next_orow;
         next_orow = (c0 + kChunk + tid < t1) ? (int)out_row(p, c0 + kChunk + tid) : -1;
       }
@@ -414,9 +417,10 @@ cudaError_t launch_chain_tc(const Params& p, cudaStream_t stream) {
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev >= 0 && dev < 64 && !attr_set[dev]) {
-    e = cudaFuncSetAttribute(kda_chain_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             SMEM3_BYTES);
-    if (e != cudaSuccess) return e;
+    for (auto fn : {kda_chain_tc_kernel<false>, kda_chain_tc_kernel<true>}) {
+      e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM3_BYTES);
+      if (e != cudaSuccess) return e;
+    }
     attr_set[dev] = true;
   }
   const long long blocks = (long long)p.num_seqs * p.heads;
@@ -434,7 +438,10 @@ cudaError_t launch_chain_tc(const Params& p, cudaStream_t stream) {
           es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
     return cudaErrorInvalidValue;
-  kda_chain_tc_kernel<<<(unsigned)blocks, NT3, SMEM3_BYTES, stream>>>(p, maps);
+  if (p.out_index)
+    kda_chain_tc_kernel<true><<<(unsigned)blocks, NT3, SMEM3_BYTES, stream>>>(p, maps);
+  else
+    kda_chain_tc_kernel<false><<<(unsigned)blocks, NT3, SMEM3_BYTES, stream>>>(p, maps);
   return cudaGetLastError();
 }
 
