@@ -363,6 +363,80 @@ def run_scatter(args):
     print(json.dumps(line), flush=True)
 
 
+def run_proj(args):
+    """The low-M projections (kda_skinny_proj) at the shapes of the skinny-GEMM test in the
+    projection-overlap PR report: k = 7168 -> 144, first 128 columns -> 1536, for m token
+    rows.  64 distinct weight sets (157 MB, more than L2) are rotated so the weights come
+    from HBM, as they would for the layers of a model; the same calls through torch's
+    cuBLAS linear are timed beside it."""
+    import kda_gated_delta_chunk_gb300 as kda
+    from kda_gated_delta_chunk_gb300 import build as kbuild
+    kbuild.build()
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    K, NAB, R, NB = 7168, 144, 128, 1536
+    NS = 64
+    g = torch.Generator(device="cpu").manual_seed(81)
+    w_ab = [torch.randn(NAB, K, generator=g).to(torch.bfloat16).to(dev) for _ in range(NS)]
+    w_b = [torch.randn(NB, R, generator=g).to(torch.bfloat16).to(dev) for _ in range(NS)]
+    ws = torch.zeros(kda.skinny_proj_workspace_size(K, NAB), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.Stream(dev)
+    hbm, _, peak_kind = load_peaks()
+    rows = []
+    for m in (1, 2, 8, 14):
+        x = torch.randn(m, K, generator=g).to(torch.bfloat16).to(dev)
+        y = torch.empty(m, NAB, dtype=torch.bfloat16, device=dev)
+        z = torch.empty(m, NB, dtype=torch.bfloat16, device=dev)
+        res = {}
+        for mode in ("ours", "cublas"):
+            def call(i):
+                if mode == "ours":
+                    kda.skinny_proj(x, w_ab[i % NS], w_b[i % NS], R, y=y, z=z, workspace=ws,
+                                    stream=stream)
+                else:
+                    with torch.cuda.stream(stream):
+                        yy = torch.nn.functional.linear(x, w_ab[i % NS])
+                        torch.nn.functional.linear(yy[:, :R], w_b[i % NS])
+            for i in range(NS):
+                call(i)
+            stream.synchronize()
+            # one call per weight set captured in a CUDA graph (the host's per-call cost is
+            # not part of the layer's time), replayed
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph, stream=stream):
+                for i in range(NS):
+                    call(i)
+            with torch.cuda.stream(stream):   # replay() launches on the current stream
+                for _ in range(3):
+                    graph.replay()
+                stream.synchronize()
+                reps = 20
+                e0 = torch.cuda.Event(enable_timing=True)
+                e1 = torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                for _ in range(reps):
+                    graph.replay()
+                e1.record(stream)
+            e1.synchronize()
+            res[mode] = e0.elapsed_time(e1) / 1e3 / (reps * NS)
+        abytes = 2 * (NAB * K + NB * R + m * K + m * NAB + m * NB)
+        rows.append({"m": m, "us": 1e6 * res["ours"], "us_cublas": 1e6 * res["cublas"],
+                     "algorithmic_bytes": abytes,
+                     "achieved_gbs": abytes / res["ours"] / 1e9,
+                     "frac": abytes / res["ours"] / 1e9 / hbm})
+    r14 = rows[-1]
+    line = {"metric": "KDA low-M projections (x 7168 -> 144 -> 1536), us per layer",
+            "value": r14["us"], "unit": "us", "higher_is_better": False, "n_gpus": 1,
+            "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": "skinny_proj_m14_k7168_n144_r128_n1536",
+                       "l2": "64 weight sets rotated (157 MB)",
+                       "timing": "64 calls captured in a CUDA graph, replayed 20 times"},
+            "roofline": {"bound": "hbm", "achieved": r14["achieved_gbs"], "peak": hbm,
+                         "unit": "GB/s", "frac": r14["frac"], "peak_source": peak_kind},
+            "per_m": rows, "gpu_launches": 2}
+    print(json.dumps(line), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -375,6 +449,8 @@ def main():
     ap.add_argument("--vsplit", type=int, default=-1, help="-1 automatic, or 1/2/4/8")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=10)
+    ap.add_argument("--proj", action="store_true",
+                    help="time the low-M projections (kda_skinny_proj)")
     ap.add_argument("--scatter", action="store_true",
                     help="time the prefill writing through an output row map")
     ap.add_argument("--decode", type=int, default=0,
@@ -384,6 +460,8 @@ def main():
         return run_decode(args)
     if args.scatter:
         return run_scatter(args)
+    if args.proj:
+        return run_proj(args)
     w = W.workload(args.workload, args.n) if args.workload == 3 else W.workload(args.workload)
     if args.impl == "reference":
         if args.steps <= 0:

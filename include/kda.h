@@ -263,6 +263,31 @@ int kda_recurrent_fwd_scatter(const void* q, const void* k, const void* v, const
                               int64_t out_rows);
 
 /*
+ * The low-M projections in front of KDA, for decode and small prefill steps: two
+ * "skinny" GEMMs with bf16 operands, fp32 accumulation and bf16 results,
+ *     y = x w_ab^T                 x [m, k], w_ab [n_ab, k]   ->  y [m, n_ab]
+ *     z = y[:, :r] w_b^T           w_b [n_b, r]               ->  z [m, n_b]
+ * (the second reads y as the first wrote it, in bf16).  These are the shapes of the
+ * Kimi-K3 low-M KDA projection overlap in the vLLM PR report "[Bugfix] Fix Kimi-K3 KDA
+ * projection overlap compile on Hopper" (Implementation breakdown; its skinny-GEMM test
+ * uses k = 7168, n_ab = 144, r = 128, n_b = 1536 and m = 2, 8, 14).  Row strides are in
+ * elements: x[i, j] at x[i * ldx + j], likewise y and z; w_ab and w_b are dense.
+ * Requirements (else KDA_ERR_INVALID_ARG): 1 <= m <= 16; k a positive multiple of 512;
+ * n_ab and n_b positive multiples of 16; r a multiple of 16 in [16, min(n_ab, 512)];
+ * ldx >= k, ldy >= n_ab and ldz >= n_b.  Alignment (else KDA_ERR_MISALIGNED): x, w_ab,
+ * w_b, y 16 bytes, z 4 bytes, ldx and ldy multiples of 8, ldz even.  y and z must not
+ * overlap x or the weights.  The workspace holds fp32 partial sums and arrival counters:
+ * kda_skinny_proj_workspace_size(k, n_ab) bytes, zero-filled once before its first use
+ * (the kernels leave the counters at zero).  Asynchronous on `stream`; the second GEMM is
+ * launched as a programmatic dependent of the first.
+ */
+size_t kda_skinny_proj_workspace_size(int32_t k, int32_t n_ab);
+int kda_skinny_proj(const void* x, int64_t ldx, const void* w_ab, const void* w_b, void* y,
+                    int64_t ldy, void* z, int64_t ldz, int32_t m, int32_t k, int32_t n_ab,
+                    int32_t r, int32_t n_b, void* workspace, size_t workspace_bytes,
+                    kda_stream_t stream);
+
+/*
  * The value-dimension split factor the automatic path uses for a batch of
  * `num_seqs` sequences and `heads` heads on a GPU with `sm_count` SMs.
  * The trigger is PR #52458's: split only when 2 * heads * num_seqs <=

@@ -53,7 +53,7 @@ EXPORTS = ("kda_workspace_size", "kda_chunk_prefill_fwd", "kda_chunk_prefill_fwd
            "kda_choose_vsplit", "kda_status_string", "kda_last_device_status",
            "kda_device_check", "kda_plan", "kda_chunk_prefill_fwd_strided",
            "kda_recurrent_fwd", "kda_chunk_prefill_fwd_noalloc", "kda_chunk_prefill_fwd_scatter",
-           "kda_recurrent_fwd_scatter")
+           "kda_recurrent_fwd_scatter", "kda_skinny_proj_workspace_size", "kda_skinny_proj")
 
 _lib = None
 _lock = threading.Lock()
@@ -107,6 +107,11 @@ def lib() -> ctypes.CDLL:
             L.kda_recurrent_fwd_scatter.argtypes = L.kda_recurrent_fwd.argtypes + [P, I64]
             L.kda_plan.restype = ctypes.c_int
             L.kda_plan.argtypes = [I64, I32, I32, SZ, ctypes.c_int, ctypes.c_int, P, P, P]
+            L.kda_skinny_proj_workspace_size.restype = SZ
+            L.kda_skinny_proj_workspace_size.argtypes = [I32, I32]
+            L.kda_skinny_proj.restype = ctypes.c_int
+            L.kda_skinny_proj.argtypes = [P, I64, P, P, P, I64, P, I64, I32, I32, I32, I32, I32,
+                                          P, SZ, P]
             L.kda_chunk_prefill_fwd_noalloc.restype = ctypes.c_int
             L.kda_chunk_prefill_fwd_noalloc.argtypes = [P, P, P, P, P, P, P, F, F, P, P, P, P,
                                                         ctypes.c_int, P, I64, I32, I32]
@@ -320,6 +325,47 @@ def recurrent_fwd(q, k, v, g, beta, A_log, dt_bias, lower_bound, scale, initial_
     if rc != OK:
         raise KDAError(rc, "kda_recurrent_fwd")
     return out, final_state, token_states
+
+
+def skinny_proj_workspace_size(k: int, n_ab: int) -> int:
+    return int(lib().kda_skinny_proj_workspace_size(int(k), int(n_ab)))
+
+
+def skinny_proj(x, w_ab, w_b, r: int = 128, y=None, z=None, workspace=None, stream=None):
+    """Run ``kda_skinny_proj``: y = x w_ab^T, z = y[:, :r] w_b^T (bf16, fp32 accumulation).
+
+    x: bf16 [m, k] (rows may be strided), w_ab: bf16 [n_ab, k], w_b: bf16 [n_b, r];
+    y / z: optional bf16 [m, n_ab] / [m, n_b] outputs (rows may be strided, e.g. views into
+    the buffers the next kernels read).  workspace: a zero-filled uint8 buffer of
+    ``skinny_proj_workspace_size(k, n_ab)`` bytes, reusable across calls on one stream.
+    Returns (y, z).
+    """
+    if x.dim() != 2 or w_ab.dim() != 2 or w_b.dim() != 2:
+        raise ValueError("x, w_ab and w_b must be 2-D")
+    m, k = x.shape
+    n_ab, n_b = w_ab.shape[0], w_b.shape[0]
+    _need(x, "x", torch.bfloat16, (m, k), token_strided=True)
+    _need(w_ab, "w_ab", torch.bfloat16, (n_ab, k))
+    _need(w_b, "w_b", torch.bfloat16, (n_b, int(r)))
+    if y is None:
+        y = torch.empty((m, n_ab), dtype=torch.bfloat16, device=x.device)
+    if z is None:
+        z = torch.empty((m, n_b), dtype=torch.bfloat16, device=x.device)
+    _need(y, "y", torch.bfloat16, (m, n_ab), token_strided=True)
+    _need(z, "z", torch.bfloat16, (m, n_b), token_strided=True)
+    if workspace is None:
+        workspace = torch.zeros(skinny_proj_workspace_size(k, n_ab), dtype=torch.uint8,
+                                device=x.device)
+    _need(workspace, "workspace", torch.uint8)
+    s = stream if stream is not None else torch.cuda.current_stream(x.device)
+    ld = lambda t, n: int(t.stride(0)) if t.shape[0] > 1 else n
+    rc = lib().kda_skinny_proj(_ptr(x), ld(x, k), _ptr(w_ab), _ptr(w_b), _ptr(y), ld(y, n_ab),
+                               _ptr(z), ld(z, n_b), int(m), int(k), int(n_ab), int(r), int(n_b),
+                               _ptr(workspace), int(workspace.numel()),
+                               ctypes.c_void_p(s.cuda_stream))
+    if rc != OK:
+        raise KDAError(rc, "kda_skinny_proj")
+    return y, z
 
 
 def chunk_prefill_fwd_noalloc(q, k, v, g, beta, A_log, dt_bias, lower_bound, scale,

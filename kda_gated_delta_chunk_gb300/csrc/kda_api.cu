@@ -366,6 +366,41 @@ int kda_recurrent_fwd_scatter(const void* q, const void* k, const void* v, const
                         out_rows);
 }
 
+size_t kda_skinny_proj_workspace_size(int32_t k, int32_t n_ab) {
+  if (k <= 0 || n_ab <= 0) return 0;
+  return (kda::proj_workspace_bytes(k, n_ab) + 15) & ~(size_t)15;
+}
+
+int kda_skinny_proj(const void* x, int64_t ldx, const void* w_ab, const void* w_b, void* y,
+                    int64_t ldy, void* z, int64_t ldz, int32_t m, int32_t k, int32_t n_ab,
+                    int32_t r, int32_t n_b, void* workspace, size_t workspace_bytes,
+                    kda_stream_t stream) {
+  if (!x || !w_ab || !w_b || !y || !z || !workspace) return KDA_ERR_INVALID_ARG;
+  if (m < 1 || m > 16 || k < 512 || k % 512 != 0 || n_ab < 16 || n_ab % 16 != 0 || n_b < 16 ||
+      n_b % 16 != 0 || r < 16 || r % 16 != 0 || r > n_ab || r > 512)
+    return KDA_ERR_INVALID_ARG;
+  if (ldx < k || ldy < n_ab || ldz < n_b) return KDA_ERR_INVALID_ARG;
+  if ((int64_t)n_ab * k > ((int64_t)1 << 31) || (int64_t)n_b * r > ((int64_t)1 << 31))
+    return KDA_ERR_INVALID_ARG;
+  if (!aligned(x, 16) || !aligned(w_ab, 16) || !aligned(w_b, 16) || !aligned(y, 16) ||
+      !aligned(z, 4) || !aligned(workspace, 16) || ldx % 8 != 0 || ldy % 8 != 0 || ldz % 2 != 0)
+    return KDA_ERR_MISALIGNED;
+  if (workspace_bytes < kda::proj_workspace_bytes(k, n_ab)) return KDA_ERR_WORKSPACE_TOO_SMALL;
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return KDA_ERR_CUDA;
+  }
+  const int rc = check_device(dev, &sms);
+  if (rc != KDA_OK) return rc;
+  if (kda::launch_proj(x, ldx, w_ab, w_b, y, ldy, z, ldz, m, k, n_ab, r, n_b, workspace,
+                       reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) {
+    cudaGetLastError();
+    return KDA_ERR_LAUNCH_FAILED;
+  }
+  return KDA_OK;
+}
+
 int kda_choose_vsplit(int32_t num_seqs, int32_t heads, int32_t sm_count) {
   if (num_seqs <= 0 || heads <= 0 || sm_count <= 0) return 1;
   const int64_t units = (int64_t)num_seqs * heads;

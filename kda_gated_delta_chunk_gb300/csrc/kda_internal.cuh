@@ -94,6 +94,11 @@ cudaError_t launch_recurrent(const Params& p, void* token_states, cudaStream_t s
 cudaError_t launch_split(const Params& p, cudaStream_t stream);
 // cuTensorMapEncodeTiled from the driver (null if unavailable)
 void* tensor_map_encoder();
+// Low-M projections (kda_skinny_proj): workspace bytes and launch of the two GEMMs.
+size_t proj_workspace_bytes(int32_t k, int32_t n_ab);
+cudaError_t launch_proj(const void* x, int64_t ldx, const void* w_ab, const void* w_b, void* y,
+                        int64_t ldy, void* z, int64_t ldz, int32_t m, int32_t k, int32_t n_ab,
+                        int32_t r, int32_t n_b, void* workspace, cudaStream_t stream);
 
 // Chunk slots the split path reserves: every sequence adds at most one partial chunk.
 __host__ __device__ inline int64_t split_slots(int64_t total_tokens, int32_t num_seqs) {
