@@ -431,8 +431,11 @@ def run_proj(args):
             "config": {"workload": "skinny_proj_m14_k7168_n144_r128_n1536",
                        "l2": "64 weight sets rotated (157 MB)",
                        "timing": "64 calls captured in a CUDA graph, replayed 20 times"},
-            "roofline": {"bound": "hbm", "achieved": r14["achieved_gbs"], "peak": hbm,
-                         "unit": "GB/s", "frac": r14["frac"], "peak_source": peak_kind},
+            "roofline": {"bound": "hbm", "kernel": "kda_skinny_proj", "achieved": r14["achieved_gbs"],
+                         "peak": hbm, "unit": "GB/s", "frac": r14["frac"], "peak_source": peak_kind,
+                         "algorithmic_bytes_per_launch": r14["algorithmic_bytes"],
+                         "traffic": load_traffic("kda_skinny_proj",
+                                                 "skinny_proj_m14_k7168_n144_r128_n1536")},
             "per_m": rows, "gpu_launches": 2}
     print(json.dumps(line), flush=True)
 
