@@ -8,6 +8,7 @@
 // an error, never a silent fallback.  It also asserts the workspace bound
 // that report lists as unchecked (Risks & impact, item 2).
 #include <algorithm>
+#include <cstdlib>
 #include <cmath>
 #include <cstdint>
 #include <cstring>
@@ -183,6 +184,10 @@ int fwd_impl(const void* q, const void* k, const void* v, const void* g, const v
   p.s_g = st[3];
   p.s_beta = st[4];
   p.helpers = (kernel == KDA_KERNEL_TC_HELPERS && total_tokens > 0) ? 1 : 0;
+  {
+    const char* drop = std::getenv("KDA_TEST_DROP_ONE_RECORD");
+    p.test_drop_record = (p.helpers && drop && drop[0] == '1') ? 1 : 0;
+  }
   p.out_index = scatter ? out_index : nullptr;
   p.out_rows = out_rows;
 

@@ -61,6 +61,10 @@ struct Params {
   // [out_rows, H, 128]; null: to out[t]
   const int32_t* out_index;
   int64_t out_rows;
+  // tests only (KDA_TEST_DROP_ONE_RECORD set in the environment): the helpers leave the record
+  // of the last chunk of the longest sequence's head 0 unpublished, so the bounded wait of
+  // the fused CTA that needs it runs out
+  int32_t test_drop_record;
 };
 
 // Record a device-side error (first writer wins) with its block and site.

@@ -209,7 +209,13 @@ __global__ void __launch_bounds__(NT, 2)
       atomicMax(maxc_s, (li + C - 1) / C);
     }
     __syncthreads();
-    if (tid == 0) *maxc_s = min(*maxc_s, (int)((p.total_tokens + C - 1) / C));
+    if (tid == 0) {
+      *maxc_s = min(*maxc_s, (int)((p.total_tokens + C - 1) / C));
+      // test hook (Params::test_drop_record): the item of the counter's first index, the last
+      // chunk of the longest sequence's head 0, is left unpublished
+      const int n0 = ord[0];
+      flags[6] = ((cu[n0] >> 6) + n0 + *maxc_s - 1) * H;
+    }
     __syncthreads();
   }
   if (tid == 0) {
@@ -667,9 +673,9 @@ __global__ void __launch_bounds__(NT, 2)
     }
     tc_fence_before();
     __syncthreads();
-    if (p.helpers && tid == 0) {   // publish the record (the barrier orders every thread's
-      __threadfence();             // part of it before this fence)
-      st_release_gpu(helper_claim(p, item), kClaimReady);
+    if (p.helpers && tid == 0 && !(p.test_drop_record && item == flags[6])) {
+      __threadfence();   // publish the record (the barrier orders every thread's part of it
+      st_release_gpu(helper_claim(p, item), kClaimReady);   // before this fence)
     }
   }
 

@@ -788,7 +788,9 @@ __global__ void __launch_bounds__(NT, 1)
     }
     // R1: the record and the v tile have landed; v rows past the sequence end -> 0
     const bool got = ok && mbar_wait(buf ? bar_rec1 : bar_rec0, (ph_rec >> buf) & 1u);
-    ok = got && mbar_wait(bar_v, ph_v);
+    // the v tile was issued whatever happened to the record: always wait for it
+    const bool v_ok = mbar_wait(bar_v, ph_v);
+    ok = got && v_ok;
     if (got) {
       ph_rec ^= 1u << buf;
       if (tid == kFetcher) rec_pend &= ~(1 << buf);

@@ -424,3 +424,26 @@ def test_helpers_refused_when_they_cannot_run():
         kda.chunk_prefill_fwd(*args, workspace=helper_workspace(150, 2, 2),
                               kernel=kda.KERNEL_TC_HELPERS, vsplit=2)
     assert e.value.code == kda.ERR_INVALID_ARG
+
+
+def test_bounded_wait_runs_out_and_the_context_survives(monkeypatch):
+    """Failure detection without a GPU fault: with KDA_TEST_DROP_ONE_RECORD=1 the first
+    helper CTA claims its first chunk and never publishes the record.  The fused CTA that
+    needs it waits a bounded time (about a second), records KDA_ERR_DEVICE_TIMEOUT in the
+    workspace and ends; the next call on the same context and workspace is correct."""
+    inp = W.make_inputs(W.custom([1024, 1024], 2, seed=44))
+    d = to_dev(inp)
+    T = d["q"].shape[0]
+    ws = helper_workspace(T, 2, 2)
+    args = (d["q"], d["k"], d["v"], d["g"], d["beta"], d["A_log"], d["dt_bias"],
+            d["lower_bound"], d["scale"], d["initial_state"], d["cu_seqlens"])
+    monkeypatch.setenv("KDA_TEST_DROP_ONE_RECORD", "1")
+    kda.chunk_prefill_fwd(*args, workspace=ws, kernel=kda.KERNEL_TC_HELPERS)
+    torch.cuda.synchronize()
+    assert kda.last_device_status(ws) == kda.ERR_DEVICE_TIMEOUT
+    monkeypatch.delenv("KDA_TEST_DROP_ONE_RECORD")
+    out, fin = kda.chunk_prefill_fwd(*args, workspace=ws, kernel=kda.KERNEL_TC_HELPERS)
+    torch.cuda.synchronize()
+    assert kda.last_device_status(ws) == kda.OK
+    out_t, fin_t = run_gpu(inp, kda.KERNEL_TC, vsplit=1)
+    assert torch.equal(out, out_t) and torch.equal(fin, fin_t)
