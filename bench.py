@@ -452,6 +452,8 @@ def main():
     ap.add_argument("--vsplit", type=int, default=-1, help="-1 automatic, or 1/2/4/8")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=10)
+    ap.add_argument("--profile-range", action="store_true",
+                    help="run one call inside cudaProfilerStart/Stop after the warm-up, then exit")
     ap.add_argument("--proj", action="store_true",
                     help="time the low-M projections (kda_skinny_proj)")
     ap.add_argument("--scatter", action="store_true",
@@ -522,6 +524,14 @@ def main():
         st = kda.last_device_status(d["ws"], stream)
         if st != kda.OK:
             raise kda.KDAError(st, "device status after warm-up")
+    if args.profile_range:
+        # one call between cudaProfilerStart/Stop, for a profiler that replays the range as a
+        # whole (the grids of one call together, as they run in the timed loop)
+        torch.cuda.profiler.start()
+        step(0)
+        stream.synchronize()
+        torch.cuda.profiler.stop()
+        return
 
     if args.steps <= 0:   # about 1.5 s of timed work so the clock sampler sees it
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
