@@ -180,7 +180,7 @@ __global__ void __launch_bounds__(NT, 1)
   const int nch = (t1 - t0 + C - 1) / C;
 
   // With helpers (P = 1): chunk c of this sequence is item (slot0, h) + c.  Its claim words
-  // start free, then the helper grid may launch.  The helpers claim (compare-and-swap) from
+  // start free (chunk 0: this CTA's), then the helper grid may launch.  The helpers claim (compare-and-swap) from
   // the last chunk down as they start an item.  This CTA reads the word of its next chunk
   // one chunk ahead: free -> it marks the chunk its own (a plain store: an atomic here would
   // hold the next barrier for an L2 round trip) and computes it; taken -> this and every
@@ -192,17 +192,25 @@ __global__ void __launch_bounds__(NT, 1)
                                                    helper_claims_offset(p.total_tokens, H, N)) +
                                 claim_index(slot0, h, p.total_tokens, N)
                           : nullptr;
+  // chunk 0 is always this CTA's own: its inputs are fetched before the claim words are
+  // written (the helpers can only start after every CTA has written its words)
+  if (tid == 0 && nch > 0) {
+    mbar_expect_tx(bar_qkg, 3 * 16384);
+    tma_load_2d(sb + OFF_INQ, &tm_q, xcol, t0, bar_qkg);
+    tma_load_2d(sb + OFF_INK, &tm_k, xcol, t0, bar_qkg);
+    tma_load_2d(sb + OFF_ING, &tm_g, xcol, t0, bar_qkg);
+    mbar_expect_tx(bar_v, 16384);
+    tma_load_2d(sb + OFF_INV, &tm_v, xcol, t0, bar_v);
+    tma_load_2d(sb + OFF_INV + 8192, &tm_v, xcol + 64, t0, bar_v);
+  }
   if (claims) {
-    for (int c = tid; c < nch; c += NT) claims[c] = kClaimFree;
+    const bool writer = tid < nch || (blockIdx.x == 0 && tid == 0);
+    for (int c = tid; c < nch; c += NT) claims[c] = (c == 0) ? kClaimOwn : kClaimFree;
     if (blockIdx.x == 0 && tid == 0) p.status[kHelperCounterWord] = 0;
-    __threadfence();
+    if (writer) __threadfence();
     __syncthreads();
     pdl_launch_dependents();
   }
-  auto claim = [&](int c) {   // thread 0: true if this CTA computes chunk c itself
-    return claims == nullptr ||
-           atomicCAS(&claims[c], kClaimFree, kClaimOwn) == kClaimFree;
-  };
   // Record mode (one thread): wait (bounded) for the helper's record of chunk c, then copy
   // it to buffer b
   auto fetch_record = [&](int c, int b) {
@@ -223,22 +231,7 @@ __global__ void __launch_bounds__(NT, 1)
   // out rows of the next chunk to start, loaded a chunk ahead (threads < 64, row map only)
   int next_orow = -1;
   if (kRowMap && tid < C && tid < t1 - t0) next_orow = (int)out_row(p, t0 + tid);
-  if (tid == 0) {
-    flags[1] = 0;                              // 1: this and every later chunk from records
-    if (nch > 0) {
-      if (claim(0)) {
-        mbar_expect_tx(bar_qkg, 3 * 16384);
-        tma_load_2d(sb + OFF_INQ, &tm_q, xcol, t0, bar_qkg);
-        tma_load_2d(sb + OFF_INK, &tm_k, xcol, t0, bar_qkg);
-        tma_load_2d(sb + OFF_ING, &tm_g, xcol, t0, bar_qkg);
-      } else {
-        flags[1] = 1;
-      }
-      mbar_expect_tx(bar_v, 16384);
-      tma_load_2d(sb + OFF_INV, &tm_v, xcol, t0, bar_v);
-      tma_load_2d(sb + OFF_INV + 8192, &tm_v, xcol + 64, t0, bar_v);
-    }
-  }
+  if (tid == 0) flags[1] = 0;   // 1: this and every later chunk from records
 
   // ---- state in: S^T[dv][dk] -> TMEM (lane = dv); this warp covers 32 key columns
   {
