@@ -96,7 +96,7 @@ cudaError_t launch_chain_tc(const Params& p, cudaStream_t stream);   // P = 1
 // Token-by-token form (decode / speculative verify); token_states may be null.
 cudaError_t launch_recurrent(const Params& p, void* token_states, cudaStream_t stream);
 cudaError_t launch_split(const Params& p, cudaStream_t stream);
-// cuTensorMapEncodeTiled from the driver (null if unavailable)
+// cuTensorMapEncodeTiled from the CUDA driver (null if unavailable)
 void* tensor_map_encoder();
 // Low-M projections (kda_skinny_proj): workspace bytes and launch of the two GEMMs.
 size_t proj_workspace_bytes(int32_t k, int32_t n_ab);
