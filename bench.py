@@ -72,11 +72,18 @@ def load_peaks():
 
 
 def kernel_source_hash() -> str:
+    """Hash of the CUDA sources with comments and blank space removed: it changes when the
+    code does, not when a comment does."""
+    import re
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "kda_gated_delta_chunk_gb300", "csrc")
     for name in sorted(os.listdir(csrc)):
         if name.endswith((".cu", ".cuh")):
-            h.update(open(os.path.join(csrc, name), "rb").read())
+            text = open(os.path.join(csrc, name), encoding="utf-8").read()
+            text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+            text = re.sub(r"//[^\n]*", " ", text)
+            text = " ".join(text.split())
+            h.update(name.encode() + b"\0" + text.encode())
     return h.hexdigest()[:16]
 
 
