@@ -212,39 +212,43 @@ __global__ void __launch_bounds__(NT2, 1)
 
     const uint32_t sbf = sb + L_::OFF_SB + buf * 128 * SP * 2;   // S bf16 of this chunk
     const uint32_t ubf = sb + L_::OFF_UB;
-    // ---- U = T diag(b) V + (-W) S    (rows 16 mt.., n8 tiles ng + 2 j)
-    float U[NPW][4];
+    // ---- U = T diag(b) V + (-W) S and the Qg S half of O (rows 16 mt.., n8 tiles
+    //      ng + 2 j).  mma.sync latency, not issue, bounds this loop, so the sums run as
+    //      independent accumulator chains at most four deep: U in three partial sums (T V, the
+    //      key channels 0-63 of -W S, channels 64-127), Qg S in two; the S fragments are
+    //      loaded once for both products.
+    float U[NPW][4], U1[NPW][4], U2[NPW][4], O[NPW][4], O1[NPW][4];
 #pragma unroll
-    for (int j = 0; j < NPW; ++j) U[j][0] = U[j][1] = U[j][2] = U[j][3] = 0.0f;
+    for (int j = 0; j < NPW; ++j)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) U[j][e] = U1[j][e] = U2[j][e] = O[j][e] = O1[j][e] = 0.0f;
 #pragma unroll
     for (int ks = 0; ks < 4; ++ks) {
-      uint32_t a[4];
+      uint32_t a[4], aw0[4], aw1[4], aq0[4], aq1[4];
       {
         const int row = 16 * mt + (lane & 15), col = 16 * ks + 8 * (lane >> 4);
         ldsm_x4(rbs + B_TB + sw128(row, col, 64), a);   // T diag(b)
       }
-#pragma unroll
-      for (int j = 0; j < NPW; ++j) {
-        uint32_t b[2];
-        const int k = 16 * ks + (lane & 15), c = 8 * (ng + 2 * j);
-        ldsm_x2_t(rbs + B_V + swv<DV>(k, c), b);
-        mma16816(U[j], a, b[0], b[1]);
-      }
-    }
-#pragma unroll
-    for (int ks = 0; ks < 8; ++ks) {
-      uint32_t a[4];
-      {   // -W (token rows, K = dk) from the MN-major [-W | Qg] image, transposed
-        const int j = lane >> 3;
-        const int m0 = 16 * mt + 8 * (j & 1), k = 16 * ks + 8 * (j >> 1) + (lane & 7);
-        ldsm_x4_t(rbs + B_WQ + mnmajor_off(m0, k, 16384), a);
+      {   // -W (tokens 0-63) and Qg (tokens 64-127) of the MN-major [-W | Qg] image, transposed
+        const int jj = lane >> 3;
+        const int m0 = 16 * mt + 8 * (jj & 1), k = 16 * ks + 8 * (jj >> 1) + (lane & 7);
+        ldsm_x4_t(rbs + B_WQ + mnmajor_off(m0, k, 16384), aw0);
+        ldsm_x4_t(rbs + B_WQ + mnmajor_off(m0, k + 64, 16384), aw1);
+        ldsm_x4_t(rbs + B_WQ + mnmajor_off(64 + m0, k, 16384), aq0);
+        ldsm_x4_t(rbs + B_WQ + mnmajor_off(64 + m0, k + 64, 16384), aq1);
       }
 #pragma unroll
       for (int j = 0; j < NPW; ++j) {
-        uint32_t b[2];
+        uint32_t bv[2], b0[2], b1[2];
         const int k = 16 * ks + (lane & 15), c = 8 * (ng + 2 * j);
-        ldsm_x2_t(sbf + (k * SP + c) * 2, b);
-        mma16816(U[j], a, b[0], b[1]);
+        ldsm_x2_t(rbs + B_V + swv<DV>(k, c), bv);
+        ldsm_x2_t(sbf + (k * SP + c) * 2, b0);
+        ldsm_x2_t(sbf + ((k + 64) * SP + c) * 2, b1);
+        mma16816(U[j], a, bv[0], bv[1]);
+        mma16816(U1[j], aw0, b0[0], b0[1]);
+        mma16816(U2[j], aw1, b1[0], b1[1]);
+        mma16816(O[j], aq0, b0[0], b0[1]);
+        mma16816(O1[j], aq1, b1[0], b1[1]);
       }
     }
     // U / |k| (per token row) -> bf16 staging
@@ -254,33 +258,19 @@ __global__ void __launch_bounds__(NT2, 1)
 #pragma unroll
       for (int j = 0; j < NPW; ++j) {
         const int c = 8 * (ng + 2 * j) + 2 * t;
+        float u[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) u[e] = U[j][e] + (U1[j][e] + U2[j][e]);
         *reinterpret_cast<uint32_t*>(ub + ((16 * mt + g) * SP + c) * 2) =
-            bf2(U[j][0] * ik0, U[j][1] * ik0);
+            bf2(u[0] * ik0, u[1] * ik0);
         *reinterpret_cast<uint32_t*>(ub + ((16 * mt + g + 8) * SP + c) * 2) =
-            bf2(U[j][2] * ik1, U[j][3] * ik1);
+            bf2(u[2] * ik1, u[3] * ik1);
       }
     }
     __syncthreads();
 
     // ---- O = (Qg S + QK U') scale/|q|  -> out
     {
-      float O[NPW][4];
-#pragma unroll
-      for (int j = 0; j < NPW; ++j) O[j][0] = O[j][1] = O[j][2] = O[j][3] = 0.0f;
-#pragma unroll
-      for (int ks = 0; ks < 8; ++ks) {
-        uint32_t a[4];
-        const int j = lane >> 3;   // Qg: tokens 64-127 of the [-W | Qg] image
-        const int m0 = 16 * mt + 8 * (j & 1), k = 16 * ks + 8 * (j >> 1) + (lane & 7);
-        ldsm_x4_t(rbs + B_WQ + mnmajor_off(64 + m0, k, 16384), a);
-#pragma unroll
-        for (int j = 0; j < NPW; ++j) {
-          uint32_t b[2];
-          const int k = 16 * ks + (lane & 15), c = 8 * (ng + 2 * j);
-          ldsm_x2_t(sbf + (k * SP + c) * 2, b);
-          mma16816(O[j], a, b[0], b[1]);
-        }
-      }
 #pragma unroll
       for (int ks = 0; ks < 4; ++ks) {
         uint32_t a[4];
@@ -291,7 +281,7 @@ __global__ void __launch_bounds__(NT2, 1)
           uint32_t b[2];
           const int k = 16 * ks + (lane & 15), c = 8 * (ng + 2 * j);
           ldsm_x2_t(ubf + (k * SP + c) * 2, b);
-          mma16816(O[j], a, b[0], b[1]);
+          mma16816((ks & 1) ? O1[j] : O[j], a, b[0], b[1]);
         }
       }
       const int r0 = 16 * mt + g;
@@ -309,22 +299,25 @@ __global__ void __launch_bounds__(NT2, 1)
         const int c = dv0 + 8 * (ng + 2 * j) + 2 * t;
         if (w0)
           *reinterpret_cast<uint32_t*>(p.out + (size_t)row0 * HD + h * 128 + c) =
-              bf2(O[j][0] * iq0, O[j][1] * iq0);
+              bf2((O[j][0] + O1[j][0]) * iq0, (O[j][1] + O1[j][1]) * iq0);
         if (w1)
           *reinterpret_cast<uint32_t*>(p.out + (size_t)row1 * HD + h * 128 + c) =
-              bf2(O[j][2] * iq1, O[j][3] * iq1);
+              bf2((O[j][2] + O1[j][2]) * iq1, (O[j][3] + O1[j][3]) * iq1);
       }
     }
 
-    // ---- S = diag(2^Gam_last) S + Ke^T U'   (this warp: key rows 16 warp.., all columns)
+    // ---- S = diag(2^Gam_last) S + Ke^T U'   (this warp: key rows 16 warp.., all columns;
+    //      tokens 32-63 of the product in a second accumulator)
     {
       const float d0 = vec[16 * warp + g], d1 = vec[16 * warp + g + 8];
+      float S2[DV / 8][4];
 #pragma unroll
       for (int nt = 0; nt < DV / 8; ++nt) {
         S[nt][0] *= d0;
         S[nt][1] *= d0;
         S[nt][2] *= d1;
         S[nt][3] *= d1;
+        S2[nt][0] = S2[nt][1] = S2[nt][2] = S2[nt][3] = 0.0f;
       }
 #pragma unroll
       for (int ks = 0; ks < 4; ++ks) {
@@ -338,9 +331,13 @@ __global__ void __launch_bounds__(NT2, 1)
           uint32_t b[2];
           const int k = 16 * ks + (lane & 15), c = 8 * nt;
           ldsm_x2_t(ubf + (k * SP + c) * 2, b);
-          mma16816(S[nt], a, b[0], b[1]);
+          mma16816(ks < 2 ? S[nt] : S2[nt], a, b[0], b[1]);
         }
       }
+#pragma unroll
+      for (int nt = 0; nt < DV / 8; ++nt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) S[nt][e] += S2[nt][e];
     }
     stage_s(buf ^ 1);
     __syncthreads();
