@@ -27,22 +27,23 @@ using namespace sm100;
 
 constexpr int NT2 = 256;   // 8 warps
 
-// shared memory per record buffer
-// shared memory per record buffer: the record image, then the V slice
 constexpr int B_WQ = kRecWQ, B_QKE = kRecQKE, B_TB = kRecTB, B_VEC = kRecVec;
 constexpr int B_V = kRecBytes + 1024;   // V slice (aligned up to 1 KB)
-constexpr int BUF_BYTES = B_V + 8192;               // room for V of DV <= 64
 
 template <int DV>
 struct ChainSmem {
   static constexpr int SP = DV + 8;                 // padded row (bf16) of the staging tiles
-  static constexpr int OFF_BUF0 = 0;
-  static constexpr int OFF_BUF1 = BUF_BYTES;
-  static constexpr int OFF_SB = 2 * BUF_BYTES;      // S bf16 [2][128][SP]
+  // record buffers: three (records copied in two chunks ahead) where they fit, for the
+  // narrowest slice; else two (one chunk ahead, the record after next prefetched to L2)
+  static constexpr int BUF = B_V + ((64 * DV * 2 + 1023) / 1024) * 1024;
+  static constexpr int NB = (DV == 16) ? 3 : 2;
+  static constexpr int OFF_SB = NB * BUF;           // S bf16 [2][128][SP]
   static constexpr int OFF_UB = OFF_SB + 2 * 128 * SP * 2;  // U bf16 [64][SP]
   static constexpr int OFF_BAR = OFF_UB + 64 * SP * 2;
   static constexpr int OFF_MISC = OFF_BAR + 64;
   static constexpr int BYTES = OFF_MISC + 64 + 1024;
+  static_assert(BUF % 1024 == 0 && NB * 8 <= 64, "record buffers");
+  static_assert(BYTES <= 227 * 1024, "shared memory");
 };
 
 __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t (&r)[4]) {
@@ -101,7 +102,8 @@ __global__ void __launch_bounds__(NT2, 1)
   const uint32_t sb = smem_u32(sm);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int g = lane >> 2, t = lane & 3;
-  const uint32_t bar0 = sb + L_::OFF_BAR, bar1 = bar0 + 8;
+  constexpr int NB = L_::NB;
+  const uint32_t bar0 = sb + L_::OFF_BAR;   // one mbarrier per record buffer, 8 bytes apart
 
   const int H = p.heads;
   const int unit = blockIdx.x;
@@ -114,8 +116,7 @@ __global__ void __launch_bounds__(NT2, 1)
     return;
   }
   if (tid == 0) {
-    mbar_init(bar0, 1);
-    mbar_init(bar1, 1);
+    for (int b = 0; b < NB; ++b) mbar_init(bar0 + 8 * b, 1);
     mbar_fence_init();
   }
   __syncthreads();
@@ -127,8 +128,8 @@ __global__ void __launch_bounds__(NT2, 1)
   const size_t sbase = ((size_t)n * H + h) * 128 * 128;
 
   auto issue = [&](int i, int buf) {
-    const uint32_t base = sb + (buf ? L_::OFF_BUF1 : L_::OFF_BUF0);
-    const uint32_t bar = buf ? bar1 : bar0;
+    const uint32_t base = sb + buf * L_::BUF;
+    const uint32_t bar = bar0 + 8 * buf;
     const int64_t rec = (int64_t)(slot0 + i) * H + h;
     const unsigned char* src =
         reinterpret_cast<const unsigned char*>(p.status) + kSplitHeader + rec * kRecBytes;
@@ -165,20 +166,24 @@ __global__ void __launch_bounds__(NT2, 1)
       *reinterpret_cast<uint32_t*>(sbf + ((r0 + 8) * SP + c) * 2) = bf2(S[nt][2], S[nt][3]);
     }
   };
-  auto prefetch_l2 = [&](int i) {   // record + v slice of chunk i -> L2
-    const int64_t rec = (int64_t)(slot0 + i) * H + h;
-    l2_prefetch(reinterpret_cast<const unsigned char*>(p.status) + kSplitHeader + rec * kRecBytes,
-                kRecBytes);
+  // record + v slice of chunk i -> L2.  With three buffers the record copy itself is issued
+  // two chunks ahead, and a bulk prefetch of it as well only adds work for the TMA unit.
+  auto prefetch_l2 = [&](int i) {
+    if constexpr (NB == 2)
+      l2_prefetch(reinterpret_cast<const unsigned char*>(p.status) + kSplitHeader +
+                      ((int64_t)(slot0 + i) * H + h) * kRecBytes,
+                  kRecBytes);
     tma_prefetch_2d(&maps.v, h * 128 + dv0, t0 + kChunk * i);
   };
   stage_s(0);
   uint32_t phase = 0;   // bit b: parity to wait for on buffer b
   int pending = 0;   // buffers with a fetch in flight (thread 0's view)
-  if (tid == 0 && nch > 0) {
-    issue(0, 0);
-    pending = 1;
-    if (nch > 1) prefetch_l2(1);
-    if (nch > 2) prefetch_l2(2);
+  if (tid == 0) {   // chunks 0 .. NB-2 into their buffers; the next two to L2
+    for (int i = 0; i < NB - 1 && i < nch; ++i) {
+      issue(i, i);
+      pending |= 1 << i;
+    }
+    for (int i = NB - 1; i <= NB && i < nch; ++i) prefetch_l2(i);
   }
   __syncthreads();
 
@@ -187,19 +192,21 @@ __global__ void __launch_bounds__(NT2, 1)
   const int ng = warp >> 2;                // which half of the n8 tiles
   constexpr int NPW = DV / 16;             // n8 tiles per warp in U and O
   for (int i = 0; i < nch; ++i) {
-    const int buf = i & 1;
+    const int buf = i % NB;
+    const int sidx = i & 1;                  // S bf16 staging of this chunk
     const int c0 = t0 + kChunk * i;
     const int L = min(kChunk, t1 - c0);
-    if (tid == 0 && i + 1 < nch) {
-      issue(i + 1, buf ^ 1);
-      pending |= 2 >> buf;
-      if (i + 3 < nch) prefetch_l2(i + 3);
+    if (tid == 0 && i + NB - 1 < nch) {     // into the buffer chunk i-1 has finished with
+      const int nb = (i + NB - 1) % NB;
+      issue(i + NB - 1, nb);
+      pending |= 1 << nb;
+      if (i + NB + 1 < nch) prefetch_l2(i + NB + 1);
     }
-    const bool ok = mbar_wait(buf ? bar1 : bar0, (phase >> buf) & 1u);
+    const bool ok = mbar_wait(bar0 + 8 * buf, (phase >> buf) & 1u);
     if (__syncthreads_or(!ok)) { failed = true; break; }
     phase ^= 1u << buf;
     pending &= ~(1 << buf);
-    unsigned char* rb = sm + (buf ? L_::OFF_BUF1 : L_::OFF_BUF0);
+    unsigned char* rb = sm + buf * L_::BUF;
     const uint32_t rbs = smem_u32(rb);
     const float* vec = reinterpret_cast<const float*>(rb + B_VEC);   // decay[128], iq[64], ik[64]
     if (L < kChunk) {   // v rows past the sequence end -> 0
@@ -210,7 +217,7 @@ __global__ void __launch_bounds__(NT2, 1)
       __syncthreads();
     }
 
-    const uint32_t sbf = sb + L_::OFF_SB + buf * 128 * SP * 2;   // S bf16 of this chunk
+    const uint32_t sbf = sb + L_::OFF_SB + sidx * 128 * SP * 2;   // S bf16 of this chunk
     const uint32_t ubf = sb + L_::OFF_UB;
     // ---- U = T diag(b) V + (-W) S and the Qg S half of O (rows 16 mt.., n8 tiles
     //      ng + 2 j).  mma.sync latency, not issue, bounds this loop, so the sums run as
@@ -339,7 +346,7 @@ __global__ void __launch_bounds__(NT2, 1)
 #pragma unroll
         for (int e = 0; e < 4; ++e) S[nt][e] += S2[nt][e];
     }
-    stage_s(buf ^ 1);
+    stage_s(sidx ^ 1);
     __syncthreads();
   }
 
@@ -347,8 +354,8 @@ __global__ void __launch_bounds__(NT2, 1)
     if (tid == 0) {
       record_error(p.status, KDA_ERR_DEVICE_TIMEOUT, 4);
       // let fetches still in flight land (bounded) before the CTA exits
-      if (pending & 1) mbar_wait(bar0, phase & 1u);
-      if (pending & 2) mbar_wait(bar1, (phase >> 1) & 1u);
+      for (int b = 0; b < NB; ++b)
+        if (pending & (1 << b)) mbar_wait(bar0 + 8 * b, (phase >> b) & 1u);
     }
     return;
   }
