@@ -134,10 +134,7 @@ __global__ void __launch_bounds__(NT2, 1)
     const unsigned char* src =
         reinterpret_cast<const unsigned char*>(p.status) + kSplitHeader + rec * kRecBytes;
     mbar_expect_tx(bar, kRecBytes + 64 * DV * 2);
-#pragma unroll
-    for (int part = 0; part < 4; ++part)
-      bulk_load(base + part * 16384, src + part * 16384, 16384, bar);
-    bulk_load(base + kRecVec, src + kRecVec, kRecBytes - kRecVec, bar);
+    bulk_load(base, src, kRecBytes, bar);   // the record is contiguous at both ends
     tma_load_2d(base + B_V, &maps.v, h * 128 + dv0, t0 + kChunk * i, bar);
   };
 

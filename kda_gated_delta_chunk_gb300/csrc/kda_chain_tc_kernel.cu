@@ -147,10 +147,7 @@ __global__ void __launch_bounds__(NT3, 1)
     const unsigned char* src = reinterpret_cast<const unsigned char*>(p.status) + kSplitHeader +
                                ((int64_t)(slot0 + i) * H + h) * kRecBytes;
     mbar_expect_tx(bar, kRecBytes + 16384);
-#pragma unroll
-    for (int part = 0; part < 4; ++part)
-      bulk_load(base + part * 16384, src + part * 16384, 16384, bar);
-    bulk_load(base + kRecVec, src + kRecVec, kRecBytes - kRecVec, bar);
+    bulk_load(base, src, kRecBytes, bar);   // the record is contiguous at both ends
     tma_load_2d(base + STAGE_V, &maps.v, xcol, t0 + kChunk * i, bar);
     tma_load_2d(base + STAGE_V + 8192, &maps.v, xcol + 64, t0 + kChunk * i, bar);
   };
