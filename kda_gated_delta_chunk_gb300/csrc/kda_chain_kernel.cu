@@ -4,7 +4,7 @@
 // a record with -W, Qg (raw q times 2^Gam), Ke (raw k times 2^(Gam_last - Gam)),
 // T diag(b), the raw masked QK, the chunk decay 2^Gam_last and the norm scalars,
 // as the image of 128-byte-swizzled shared-memory tiles; it is copied in as is
-// (bulk copies) and read with ldmatrix.
+// (one bulk copy) and read with ldmatrix.
 // This kernel walks one sequence's chunks in order for one head and one slice of
 // DV = 128 / P value columns -- the value-dimension split of "[Kimi-K3][Perf]
 // Update FlashKDA for automatic K2 V-split" (PR #52458, Features & motivation),
@@ -13,8 +13,9 @@
 //   O  = (Qg S + QK (U/|k|)) scale/|q|  -> out
 //   S  = diag(2^Gam_last) S + Ke^T (U/|k|)
 // The products are narrow (N = DV), so they run as warp-level mma.sync tiles
-// (bf16 in, fp32 accumulate) with S held in registers; the record of the next
-// chunk is fetched by TMA while this one is processed.
+// (bf16 in, fp32 accumulate) with S held in registers; the records of the next
+// chunks (one ahead, or two for the 16-column slice) are copied in while this one
+// is processed.
 #include <cuda.h>
 
 #include "kda_internal.cuh"
