@@ -71,14 +71,19 @@ def load_peaks():
     return 6800.0, 1900.0, "fallback"
 
 
+# host-only translation unit (argument checks, planning, the C entry points): no device code
+HOST_ONLY_SOURCES = ("kda_api.cu",)
+
+
 def kernel_source_hash() -> str:
-    """Hash of the CUDA sources with comments and blank space removed: it changes when the
-    code does, not when a comment does."""
+    """Hash of the kernels' CUDA sources (every file but the host-only ones) with comments and
+    blank space removed: it changes when kernel or launch code does, not when a comment or
+    a host-side entry point does."""
     import re
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "kda_gated_delta_chunk_gb300", "csrc")
     for name in sorted(os.listdir(csrc)):
-        if name.endswith((".cu", ".cuh")):
+        if name.endswith((".cu", ".cuh")) and name not in HOST_ONLY_SOURCES:
             text = open(os.path.join(csrc, name), encoding="utf-8").read()
             text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
             text = re.sub(r"//[^\n]*", " ", text)

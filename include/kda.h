@@ -328,6 +328,17 @@ int kda_plan(int64_t total_tokens, int32_t num_seqs, int32_t heads, size_t works
              int vsplit, int kernel, int* kernel_out, int* vsplit_out, int* launches_out);
 
 /*
+ * kda_plan for a device with `sm_count` multiprocessors, without touching any
+ * device: the same checks of sizes and selectors, the same resolution of
+ * AUTO, value split and launch count.  For planning on a host that has no
+ * GPU (and for testing the dispatch there).  sm_count <= 0 gives
+ * KDA_ERR_INVALID_ARG.  Output pointers may be NULL.
+ */
+int kda_plan_for(int64_t total_tokens, int32_t num_seqs, int32_t heads, size_t workspace_bytes,
+                 int vsplit, int kernel, int32_t sm_count, int* kernel_out, int* vsplit_out,
+                 int* launches_out);
+
+/*
  * kda_chunk_prefill_fwd for callers that cannot allocate device memory and
  * so cannot pass a workspace: for instance a plugin inside a host framework
  * that owns all device memory, or a hot loop where a cudaMalloc (which may

@@ -51,7 +51,7 @@ ERR_BAD_OUT_INDEX = -10
 # every symbol include/kda.h declares
 EXPORTS = ("kda_workspace_size", "kda_chunk_prefill_fwd", "kda_chunk_prefill_fwd_ex",
            "kda_choose_vsplit", "kda_status_string", "kda_last_device_status",
-           "kda_device_check", "kda_plan", "kda_chunk_prefill_fwd_strided",
+           "kda_device_check", "kda_plan", "kda_plan_for", "kda_chunk_prefill_fwd_strided",
            "kda_recurrent_fwd", "kda_chunk_prefill_fwd_noalloc", "kda_chunk_prefill_fwd_scatter",
            "kda_recurrent_fwd_scatter", "kda_skinny_proj_workspace_size", "kda_skinny_proj")
 
@@ -107,6 +107,8 @@ def lib() -> ctypes.CDLL:
             L.kda_recurrent_fwd_scatter.argtypes = L.kda_recurrent_fwd.argtypes + [P, I64]
             L.kda_plan.restype = ctypes.c_int
             L.kda_plan.argtypes = [I64, I32, I32, SZ, ctypes.c_int, ctypes.c_int, P, P, P]
+            L.kda_plan_for.restype = ctypes.c_int
+            L.kda_plan_for.argtypes = [I64, I32, I32, SZ, ctypes.c_int, ctypes.c_int, I32, P, P, P]
             L.kda_skinny_proj_workspace_size.restype = SZ
             L.kda_skinny_proj_workspace_size.argtypes = [I32, I32]
             L.kda_skinny_proj.restype = ctypes.c_int
@@ -144,6 +146,19 @@ def plan(total_tokens: int, num_seqs: int, heads: int, workspace_bytes: int,
                         ctypes.byref(n))
     if rc != OK:
         raise KDAError(rc, "kda_plan")
+    return k.value, p.value, n.value
+
+
+def plan_for(total_tokens: int, num_seqs: int, heads: int, workspace_bytes: int, sm_count: int,
+             vsplit: int = -1, kernel: int = KERNEL_AUTO):
+    """``kda_plan_for``: (kernel, vsplit, launches) a call would use on a device with
+    ``sm_count`` multiprocessors; touches no device."""
+    k, p, n = ctypes.c_int(0), ctypes.c_int(0), ctypes.c_int(0)
+    rc = lib().kda_plan_for(int(total_tokens), int(num_seqs), int(heads), int(workspace_bytes),
+                            int(vsplit), int(kernel), int(sm_count), ctypes.byref(k),
+                            ctypes.byref(p), ctypes.byref(n))
+    if rc != OK:
+        raise KDAError(rc, "kda_plan_for")
     return k.value, p.value, n.value
 
 

@@ -453,6 +453,15 @@ int kda_last_device_status(void* workspace, kda_stream_t stream) {
 
 int kda_device_check(int device) { return check_device(device, nullptr); }
 
+int kda_plan_for(int64_t total_tokens, int32_t num_seqs, int32_t heads, size_t workspace_bytes,
+                 int vsplit, int kernel, int32_t sm_count, int* kernel_out, int* vsplit_out,
+                 int* launches_out) {
+  if (total_tokens < 0 || num_seqs < 0 || heads <= 0 || sm_count <= 0) return KDA_ERR_INVALID_ARG;
+  if (workspace_bytes < (size_t)kda::kWorkspaceBytes) return KDA_ERR_WORKSPACE_TOO_SMALL;
+  return plan(total_tokens, num_seqs, heads, workspace_bytes, vsplit, kernel, sm_count,
+              kernel_out, vsplit_out, launches_out);
+}
+
 int kda_plan(int64_t total_tokens, int32_t num_seqs, int32_t heads, size_t workspace_bytes,
              int vsplit, int kernel, int* kernel_out, int* vsplit_out, int* launches_out) {
   if (total_tokens < 0 || num_seqs < 0 || heads <= 0) return KDA_ERR_INVALID_ARG;
@@ -464,8 +473,8 @@ int kda_plan(int64_t total_tokens, int32_t num_seqs, int32_t heads, size_t works
   }
   const int rc = check_device(dev, &sms);
   if (rc != KDA_OK) return rc;
-  return plan(total_tokens, num_seqs, heads, workspace_bytes, vsplit, kernel, sms, kernel_out,
-              vsplit_out, launches_out);
+  return kda_plan_for(total_tokens, num_seqs, heads, workspace_bytes, vsplit, kernel, sms,
+                      kernel_out, vsplit_out, launches_out);
 }
 
 }  // extern "C"

@@ -12,6 +12,7 @@ import re
 import pytest
 
 import kda_gated_delta_chunk_gb300 as kda
+import kda_workloads as W
 from kda_gated_delta_chunk_gb300 import build as kbuild
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
@@ -101,6 +102,105 @@ def test_vsplit_factor_values(L):
             p = kda.choose_vsplit(n, h, 152)
             assert p in (1, 2, 4, 8)
             assert p == 1 or p * n * h <= 152
+
+
+# ------------------------------------------------------------------ dispatch, no device
+GB300_SMS = 152
+
+
+def _auto(lengths, H, ws=None, sms=GB300_SMS, **kw):
+    T, N = sum(lengths), len(lengths)
+    ws = kda.workspace_size(T, H, N) if ws is None else ws
+    return kda.plan_for(T, N, H, ws, sms, **kw)
+
+
+def _records_only(lengths, H):
+    """Bytes of the split path's header and records, without the helpers' claim words."""
+    T, N = sum(lengths), len(lengths)
+    return 1024 + ((T + 63) // 64 + N) * H * 66560
+
+
+@pytest.mark.parametrize("shape,H,want", [
+    ("tiny", 2, (kda.KERNEL_SPLIT, 8, 2)),                 # 1 x 128
+    ("batched", 16, (kda.KERNEL_TC_HELPERS, 1, 2)),        # 128 chains leave 24 SMs free
+    ("long", 16, (kda.KERNEL_SPLIT, 8, 2)),                # 1 x 16384
+    ("v1", 8, (kda.KERNEL_SPLIT, 8, 2)),                   # N x 4096, H = 8
+    ("v2", 8, (kda.KERNEL_SPLIT, 8, 2)),
+    ("v3", 8, (kda.KERNEL_SPLIT, 4, 2)),
+    ("v7", 8, (kda.KERNEL_SPLIT, 2, 2)),
+    ("ragged", 32, (kda.KERNEL_TC, 1, 1)),                 # 2048 chains: no SM left over
+])
+def test_auto_dispatch_of_the_benchmark_shapes(L, shape, H, want):
+    lengths = {"tiny": [128], "batched": [2048] * 8, "long": [16384], "v1": [4096],
+               "v2": [4096] * 2, "v3": [4096] * 3, "v7": [4096] * 7,
+               "ragged": list(W.workload(4).lengths)}[shape]
+    assert _auto(lengths, H) == want
+
+
+def test_auto_helper_conditions(L):
+    # at least 8 SMs stay free: 18 x 8 = 144 chains leave 8, 19 x 8 = 152 leave none
+    assert _auto([2048] * 18, 8)[0] == kda.KERNEL_TC_HELPERS
+    assert _auto([2048] * 19, 8)[0] == kda.KERNEL_TC
+    # the same batch on a smaller part: 136 > 132 SMs
+    assert _auto([2048] * 8, 16, sms=148)[0] == kda.KERNEL_TC_HELPERS
+    assert _auto([2048] * 8, 16, sms=132)[0] == kda.KERNEL_TC
+    # at most 128 sequences
+    assert _auto([256] * 128, 1)[0] == kda.KERNEL_TC_HELPERS
+    assert _auto([256] * 129, 1)[0] == kda.KERNEL_TC
+    # sequences of at least 4 chunks on average
+    assert _auto([256] * 8, 16)[0] == kda.KERNEL_TC_HELPERS
+    assert _auto([255] * 8, 16)[0] == kda.KERNEL_TC
+    # the claim words must fit as well as the records
+    lengths = [2048] * 8
+    assert _auto(lengths, 16, ws=_records_only(lengths, 16)) == (kda.KERNEL_TC, 1, 1)
+    claims = ((sum(lengths) + 63) // 64 + len(lengths)) * 16 * 4   # a word per (slot, head)
+    assert _auto(lengths, 16, ws=_records_only(lengths, 16) + claims - 4)[0] == kda.KERNEL_TC
+    assert _auto(lengths, 16, ws=_records_only(lengths, 16) + claims)[0] == \
+        kda.KERNEL_TC_HELPERS
+
+
+def test_auto_without_room_for_records_runs_the_fused_kernel(L):
+    # the value split triggers, but a bare status workspace holds no records
+    assert _auto([16384], 16, ws=256) == (kda.KERNEL_TC, 1, 1)
+    # a split factor given by the caller stays, on the fused kernel
+    assert _auto([16384], 16, ws=256, vsplit=4) == (kda.KERNEL_TC, 4, 1)
+    assert _auto([16384], 16, ws=_records_only([16384], 16)) == (kda.KERNEL_SPLIT, 8, 2)
+
+
+def test_forced_kernels_and_refusals(L):
+    assert _auto([2048] * 8, 16, kernel=kda.KERNEL_SPLIT) == (kda.KERNEL_SPLIT, 1, 2)
+    assert _auto([2048] * 8, 16, kernel=kda.KERNEL_TC) == (kda.KERNEL_TC, 1, 1)
+    assert _auto([2048] * 8, 16, kernel=kda.KERNEL_REF) == (kda.KERNEL_REF, 1, 1)
+    assert _auto([16384], 16, kernel=kda.KERNEL_TC_HELPERS) == (kda.KERNEL_TC_HELPERS, 1, 2)
+    refused = [
+        (dict(kernel=kda.KERNEL_SPLIT, ws=256), kda.ERR_WORKSPACE_TOO_SMALL),
+        (dict(kernel=kda.KERNEL_TC_HELPERS, ws=256), kda.ERR_WORKSPACE_TOO_SMALL),
+        (dict(kernel=kda.KERNEL_TC_HELPERS, vsplit=2), kda.ERR_INVALID_ARG),
+        (dict(kernel=kda.KERNEL_TC_HELPERS, sms=128), kda.ERR_INVALID_ARG),   # no SM free
+        (dict(vsplit=3), kda.ERR_INVALID_ARG),
+        (dict(kernel=99), kda.ERR_INVALID_ARG),
+        (dict(sms=0), kda.ERR_INVALID_ARG),
+        (dict(ws=255), kda.ERR_WORKSPACE_TOO_SMALL),
+    ]
+    for kw, code in refused:
+        with pytest.raises(kda.KDAError) as e:
+            _auto([2048] * 8, 16, **kw)
+        assert e.value.code == code, kw
+    with pytest.raises(kda.KDAError) as e:
+        kda.plan_for(2048, 1, 0, 1 << 20, GB300_SMS)     # no heads
+    assert e.value.code == kda.ERR_INVALID_ARG
+
+
+def test_launch_counts_of_degenerate_batches(L):
+    assert kda.plan_for(0, 0, 16, 256, GB300_SMS) == (kda.KERNEL_TC, 1, 0)     # no sequences
+    # sequences that are all empty: no records to make, one launch writes the states
+    assert kda.plan_for(0, 3, 8, 1 << 20, GB300_SMS) == (kda.KERNEL_TC, 1, 1)
+    # a forced split path keeps its documented record area, a slot per sequence included
+    ws = _records_only([0, 0, 0], 8)
+    assert kda.plan_for(0, 3, 8, ws, GB300_SMS, kernel=kda.KERNEL_SPLIT) == (kda.KERNEL_SPLIT, 4, 1)
+    with pytest.raises(kda.KDAError) as e:
+        kda.plan_for(0, 3, 8, 1 << 20, GB300_SMS, kernel=kda.KERNEL_SPLIT)
+    assert e.value.code == kda.ERR_WORKSPACE_TOO_SMALL
 
 
 def test_status_strings(L):
