@@ -256,6 +256,57 @@ def run_reference(args, w):
     print(json.dumps(line), flush=True)
 
 
+# phase stamps of the pipelined kernel (slots of the 16 per chunk; see kda_pipe_kernel.cu)
+CHAIN_SLOTS = {0: "stage full", 1: "G1a issued", 2: "G1a done", 3: "G1b done", 4: "G2 done",
+               5: "O stored"}
+KSIDE_SLOTS = {8: "inputs landed", 9: "gate, norms, factors", 10: "operand tiles",
+               11: "A|QK MMA done", 12: "A/QK extracted", 13: "T inverse", 14: "stage handed over"}
+
+
+def run_stamps(args):
+    """Phase breakdown of KDA_KERNEL_PIPE: build the phase-stamp variant of the library
+    (-DKDA_PHASE_STAMPS), run the workload a few times, read the clock64 stamps CTA 0 (the
+    longest sequence, head 0) wrote per chunk, print medians over its inner chunks."""
+    from kda_gated_delta_chunk_gb300 import build as kbuild
+    import kda_gated_delta_chunk_gb300 as kda
+    path = kbuild.build(stamps=True)
+    kda.use_library(path)
+    w = W.workload(args.workload, args.n) if args.workload == 3 else W.workload(args.workload)
+    dev = torch.device("cuda", torch.cuda.current_device())
+    d = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in W.make_inputs(w).items()}
+    T, H, N = sum(w.lengths), w.heads, w.num_seqs
+    ws_bytes = 1 << 16
+    ws = torch.zeros(ws_bytes, dtype=torch.uint8, device=dev)
+    off = (ws_bytes - 8192) & ~255
+    for _ in range(max(3, args.warmup) + 1):
+        ws[off:].zero_()
+        kda.chunk_prefill_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], d["A_log"],
+                              d["dt_bias"], d["lower_bound"], d["scale"], d["initial_state"],
+                              d["cu_seqlens"], workspace=ws, kernel=kda.KERNEL_PIPE)
+    torch.cuda.synchronize()
+    st = kda.last_device_status(ws)
+    if st != kda.OK:
+        raise kda.KDAError(st, "device status")
+    stamps = ws[off:off + 8192].cpu().view(torch.int64).view(64, 16).tolist()
+    nch = min(64, (max(w.lengths) + 63) // 64)
+    inner = range(1, max(2, nch - 1))
+
+    def med(a, b, prev_b=False):
+        vals = [stamps[c][b] - (stamps[c - 1][a] if prev_b else stamps[c][a]) for c in inner]
+        return statistics.median(vals) if vals else 0
+
+    res = {"workload": w.name, "chunks_of_cta0": nch, "unit": "SM cycles (clock64), median",
+           "chunk_period": med(14, 14, True),
+           "kside": {f"{KSIDE_SLOTS[a]} -> {KSIDE_SLOTS[a + 1]}": med(a, a + 1)
+                     for a in range(8, 14)},
+           "kside_wait_for_inputs": med(14, 8, True),
+           "chain": {f"{CHAIN_SLOTS[a]} -> {CHAIN_SLOTS[a + 1]}": med(a, a + 1)
+                     for a in range(0, 5)},
+           "chain_wait_for_stage": med(5, 0, True),
+           "chain_start_after_handover": med(14, 0)}
+    print(json.dumps(res, indent=1), flush=True)
+
+
 def run_decode(args):
     """Decode / speculative-verify step through kda_recurrent_fwd: 64 sequences x K tokens,
     H = 32, fp32 state.  The time is bound by reading and writing the state."""
@@ -458,7 +509,8 @@ def main():
     ap.add_argument("--steps", type=int, default=0, help="timed steps (0: ~1.5 s worth)")
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--kernel", default="auto", choices=["auto", "tc", "helpers", "split", "ref"])
+    ap.add_argument("--kernel", default="auto",
+                    choices=["auto", "tc", "helpers", "split", "ref", "pipe"])
     ap.add_argument("--workload", type=int, default=1)
     ap.add_argument("--n", type=int, default=None, help="sequences of the V-split workload (3)")
     ap.add_argument("--vsplit", type=int, default=-1, help="-1 automatic, or 1/2/4/8")
@@ -472,7 +524,12 @@ def main():
                     help="time the prefill writing through an output row map")
     ap.add_argument("--decode", type=int, default=0,
                     help="time a decode step (kda_recurrent_fwd) with this many tokens per sequence")
+    ap.add_argument("--stamps", action="store_true",
+                    help="per-chunk phase breakdown of the pipelined kernel from the phase-stamp "
+                         "build (clock64 stamps of CTA 0), then exit")
     args = ap.parse_args()
+    if args.stamps:
+        return run_stamps(args)
     if args.decode > 0:
         return run_decode(args)
     if args.scatter:
@@ -493,7 +550,8 @@ def main():
     barrier(world)
     kbuild.build()
     kernel = {"auto": kda.KERNEL_AUTO, "tc": kda.KERNEL_TC, "ref": kda.KERNEL_REF,
-              "split": kda.KERNEL_SPLIT, "helpers": kda.KERNEL_TC_HELPERS}[args.kernel]
+              "split": kda.KERNEL_SPLIT, "helpers": kda.KERNEL_TC_HELPERS,
+              "pipe": kda.KERNEL_PIPE}[args.kernel]
     dev = torch.device("cuda", torch.cuda.current_device())
     rc = kda.device_check(dev.index)
     if rc != kda.OK:
@@ -650,7 +708,8 @@ def main():
         return
 
     kernel_name = {kda.KERNEL_TC: "kda_tc_chunk_kernel", kda.KERNEL_REF: "kda_ref_chunk_kernel",
-                   kda.KERNEL_SPLIT: "kda_split_path", kda.KERNEL_TC_HELPERS: "kda_tc_helpers_path"}[path]
+                   kda.KERNEL_SPLIT: "kda_split_path", kda.KERNEL_TC_HELPERS: "kda_tc_helpers_path",
+                   kda.KERNEL_PIPE: "kda_pipe_kernel"}[path]
     hbm, tflops, peak_kind = load_peaks()
     abytes = algorithmic_bytes(w)
     achieved = abytes / mean_launch / 1e9

@@ -108,6 +108,12 @@ typedef struct CUstream_st* kda_stream_t;
                               fused CTAs then read instead of computing them;
                               needs N * heads < SM count and the records'
                               workspace                                      */
+#define KDA_KERNEL_PIPE 5  /* fused warp-specialised tcgen05 + TMA kernel, C = 64:
+                              one CTA per (sequence, head) whose k-side warps
+                              build chunk c+1's operands while its chain warps
+                              run chunk c; no value split (vsplit -1 or 1),
+                              dense outputs only (not the _scatter entry point),
+                              needs only the 256-byte workspace               */
 
 /*
  * Bytes of device workspace a call needs for up to `total_tokens` tokens,
@@ -339,6 +345,17 @@ int kda_plan_for(int64_t total_tokens, int32_t num_seqs, int32_t heads, size_t w
                  int* launches_out);
 
 /*
+ * Test hook, for the failure-detection test only: while `on` is nonzero,
+ * calls that take KDA_KERNEL_TC_HELPERS have the helpers leave one claimed
+ * record unpublished (the last chunk of the longest sequence's head 0), so
+ * the bounded device wait of the fused CTA that needs it runs out and the
+ * call records KDA_ERR_DEVICE_TIMEOUT.  Off at load.  Read once per call
+ * from an atomic flag (no environment lookup).  The pages have no
+ * counterpart.
+ */
+void kda_test_drop_one_record(int on);
+
+/*
  * kda_chunk_prefill_fwd for callers that cannot allocate device memory and
  * so cannot pass a workspace: for instance a plugin inside a host framework
  * that owns all device memory, or a hot loop where a cudaMalloc (which may
@@ -346,15 +363,17 @@ int kda_plan_for(int64_t total_tokens, int32_t num_seqs, int32_t heads, size_t w
  * this entry point.
  *
  * Arguments, layouts and ownership are those of kda_chunk_prefill_fwd
- * without the workspace; the fused tcgen05 kernel runs (KDA_KERNEL_TC with
- * automatic value split; never the split path, whose records need a real
- * workspace).
+ * without the workspace; the fused tcgen05 kernel runs unsplit (KDA_KERNEL_TC,
+ * P = 1, as AUTO's fused fallback; never the split path, whose records need
+ * a real workspace).
  * The scratch it needs (the 16-byte device status word) lives in a 256-byte
  * file-scope device array of this library, which every GPU that loads the
  * library holds until exit.  The library allocates nothing: no cudaMalloc,
  * cudaFree or allocating library call on any path of this function.
  *   - The first call on a device looks up the array's device address (with
  *     that device current); make that first call before any stream capture.
+ *     The address is kept for the life of the process: after a
+ *     cudaDeviceReset on that device, do not call this entry point again.
  *   - Every call shares the array.  Each call clears the status word on
  *     `stream` before its kernel (this clearing may be enqueued even when
  *     the call then returns an argument error).  Calls that overlap on the

@@ -15,7 +15,7 @@ names follow the C ABI in ``include/kda.h``:
                   cu_seqlens, token_states=False, ...) -> (out, final_state, token_states)
     plan(total_tokens, num_seqs, heads, workspace_bytes, vsplit, kernel)
         -> (kernel, vsplit, launches)
-    KERNEL_AUTO / KERNEL_TC / KERNEL_TC_HELPERS / KERNEL_SPLIT / KERNEL_REF
+    KERNEL_AUTO / KERNEL_TC / KERNEL_TC_HELPERS / KERNEL_SPLIT / KERNEL_REF / KERNEL_PIPE
     last_device_status(workspace) -> int
     status_string(code) -> str
 
@@ -35,7 +35,7 @@ LIB_PATH = os.path.join(_PKG, "libkda.so")
 
 HEAD_DIM = 128
 STATE_F32, STATE_BF16 = 0, 1
-KERNEL_AUTO, KERNEL_TC, KERNEL_REF, KERNEL_SPLIT, KERNEL_TC_HELPERS = 0, 1, 2, 3, 4
+KERNEL_AUTO, KERNEL_TC, KERNEL_REF, KERNEL_SPLIT, KERNEL_TC_HELPERS, KERNEL_PIPE = 0, 1, 2, 3, 4, 5
 OK = 0
 ERR_INVALID_ARG = -1
 ERR_UNSUPPORTED_DEVICE = -2
@@ -53,7 +53,8 @@ EXPORTS = ("kda_workspace_size", "kda_chunk_prefill_fwd", "kda_chunk_prefill_fwd
            "kda_choose_vsplit", "kda_status_string", "kda_last_device_status",
            "kda_device_check", "kda_plan", "kda_plan_for", "kda_chunk_prefill_fwd_strided",
            "kda_recurrent_fwd", "kda_chunk_prefill_fwd_noalloc", "kda_chunk_prefill_fwd_scatter",
-           "kda_recurrent_fwd_scatter", "kda_skinny_proj_workspace_size", "kda_skinny_proj")
+           "kda_recurrent_fwd_scatter", "kda_skinny_proj_workspace_size", "kda_skinny_proj",
+           "kda_test_drop_one_record")
 
 _lib = None
 _lock = threading.Lock()
@@ -66,15 +67,28 @@ class KDAError(RuntimeError):
                          f"{status_string(code)} ({code})")
 
 
+_lib_path = LIB_PATH
+
+
+def use_library(path: str) -> None:
+    """Load ``path`` instead of libkda.so (the phase-stamp build, for profiling); must come
+    before the first call into the library."""
+    global _lib_path
+    with _lock:
+        if _lib is not None and path != _lib_path:
+            raise RuntimeError("the library is already loaded")
+        _lib_path = path
+
+
 def lib() -> ctypes.CDLL:
     """Load libkda.so (built in-tree by ``build.build()``); raise if absent."""
     global _lib
     with _lock:
         if _lib is None:
-            if not os.path.exists(LIB_PATH):
-                raise RuntimeError(f"{LIB_PATH} is missing: build it with "
+            if not os.path.exists(_lib_path):
+                raise RuntimeError(f"{_lib_path} is missing: build it with "
                                    "kda_gated_delta_chunk_gb300.build.build()")
-            L = ctypes.CDLL(LIB_PATH)
+            L = ctypes.CDLL(_lib_path)
             P, I32, I64, SZ, F = (ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64,
                                   ctypes.c_size_t, ctypes.c_float)
             L.kda_workspace_size.restype = SZ
@@ -114,6 +128,8 @@ def lib() -> ctypes.CDLL:
             L.kda_skinny_proj.restype = ctypes.c_int
             L.kda_skinny_proj.argtypes = [P, I64, P, P, P, I64, P, I64, I32, I32, I32, I32, I32,
                                           P, SZ, P]
+            L.kda_test_drop_one_record.restype = None
+            L.kda_test_drop_one_record.argtypes = [ctypes.c_int]
             L.kda_chunk_prefill_fwd_noalloc.restype = ctypes.c_int
             L.kda_chunk_prefill_fwd_noalloc.argtypes = [P, P, P, P, P, P, P, F, F, P, P, P, P,
                                                         ctypes.c_int, P, I64, I32, I32]
@@ -135,6 +151,12 @@ def choose_vsplit(num_seqs: int, heads: int, sm_count: int) -> int:
 
 def device_check(device: int = 0) -> int:
     return int(lib().kda_device_check(int(device)))
+
+
+def test_drop_one_record(on: bool) -> None:
+    """Test hook (failure detection): while on, helper-path calls leave one record
+    unpublished so the waiting CTA's bounded wait runs out."""
+    lib().kda_test_drop_one_record(1 if on else 0)
 
 
 def plan(total_tokens: int, num_seqs: int, heads: int, workspace_bytes: int,
@@ -411,6 +433,13 @@ def chunk_prefill_fwd_noalloc(q, k, v, g, beta, A_log, dt_bias, lower_bound, sca
     _need(final_state, "final_state", final_state.dtype, (N, H, D, D))
     if initial_state is not None:
         _need(initial_state, "initial_state", final_state.dtype, (N, H, D, D))
+    # the library finds its static scratch on the current device: every tensor must live there
+    cur = torch.cuda.current_device()
+    for name, t in (("q", q), ("k", k), ("v", v), ("g", g), ("beta", beta), ("A_log", A_log),
+                    ("dt_bias", dt_bias), ("cu_seqlens", cu_seqlens), ("out", out),
+                    ("final_state", final_state), ("initial_state", initial_state)):
+        if t is not None and t.device.index != cur:
+            raise ValueError(f"{name} is on {t.device}, but the current device is cuda:{cur}")
     s = stream if stream is not None else torch.cuda.current_stream(q.device)
     rc = lib().kda_chunk_prefill_fwd_noalloc(
         _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(A_log), _ptr(dt_bias),

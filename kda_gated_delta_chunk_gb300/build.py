@@ -28,29 +28,38 @@ def nvcc() -> str:
     return path
 
 
-def _compile(src: str, extra: list) -> str:
-    obj = os.path.join(BUILD, os.path.basename(src) + ".o")
+def _compile(src: str, extra: list, build_dir: str = BUILD) -> str:
+    obj = os.path.join(build_dir, os.path.basename(src) + ".o")
     cmd = [nvcc(), *ARCH, "-std=c++17", "-O3", "-lineinfo", "-Xcompiler", "-fPIC",
            "--expt-relaxed-constexpr", "-I", INCLUDE, "-I", CSRC, *extra, "-c", src, "-o", obj]
     subprocess.run(cmd, check=True)
     return obj
 
 
-def build(force: bool = False, verbose_ptxas: bool = False) -> str:
-    """Build (if stale) and return the path of libkda.so."""
-    os.makedirs(BUILD, exist_ok=True)
+# The phase-stamp variant: kernels record clock64 stamps per chunk of CTA 0 into the end of
+# the workspace (KDA_PHASE_STAMPS); a separate library, never the one the package loads.
+STAMPS_LIB = os.path.join(PKG, "libkda_stamps.so")
+
+
+def build(force: bool = False, verbose_ptxas: bool = False, stamps: bool = False) -> str:
+    """Build (if stale) and return the path of libkda.so (or of the stamps variant)."""
+    lib = STAMPS_LIB if stamps else LIB
+    bdir = BUILD + ("_stamps" if stamps else "")
+    os.makedirs(bdir, exist_ok=True)
     srcs = sorted(glob.glob(os.path.join(CSRC, "*.cu")))
     deps = srcs + glob.glob(os.path.join(CSRC, "*.cuh")) + glob.glob(os.path.join(INCLUDE, "*.h"))
-    if not force and os.path.exists(LIB):
-        if os.path.getmtime(LIB) >= max(os.path.getmtime(d) for d in deps):
-            return LIB
+    if not force and os.path.exists(lib):
+        if os.path.getmtime(lib) >= max(os.path.getmtime(d) for d in deps):
+            return lib
     extra = ["-Xptxas", "-v"] if verbose_ptxas else []
+    if stamps:
+        extra = extra + ["-DKDA_PHASE_STAMPS"]
     with cf.ThreadPoolExecutor(max_workers=min(8, len(srcs))) as ex:
-        objs = list(ex.map(lambda s: _compile(s, extra), srcs))
-    tmp = LIB + f".tmp{os.getpid()}"
+        objs = list(ex.map(lambda s: _compile(s, extra, bdir), srcs))
+    tmp = lib + f".tmp{os.getpid()}"
     subprocess.run([nvcc(), *ARCH, "-shared", "-cudart", "static", "-o", tmp, *objs], check=True)
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":

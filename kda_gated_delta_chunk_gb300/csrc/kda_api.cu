@@ -8,7 +8,7 @@
 // an error, never a silent fallback.  It also asserts the workspace bound
 // that report lists as unchecked (Risks & impact, item 2).
 #include <algorithm>
-#include <cstdlib>
+#include <atomic>
 #include <cmath>
 #include <cstdint>
 #include <cstring>
@@ -19,6 +19,7 @@
 namespace {
 
 constexpr int kMaxDevices = 64;
+std::atomic<int> g_test_drop_record{0};   // kda_test_drop_one_record
 int g_dev_ok[kMaxDevices];      // 0 unknown, 1 supported, -1 not
 int g_dev_sms[kMaxDevices];
 std::mutex g_dev_mu;
@@ -75,13 +76,16 @@ int plan(int64_t total_tokens, int32_t num_seqs, int32_t heads, size_t workspace
   if (vsplit != -1 && vsplit != 1 && vsplit != 2 && vsplit != 4 && vsplit != 8)
     return KDA_ERR_INVALID_ARG;
   if (kernel != KDA_KERNEL_AUTO && kernel != KDA_KERNEL_TC && kernel != KDA_KERNEL_REF &&
-      kernel != KDA_KERNEL_SPLIT && kernel != KDA_KERNEL_TC_HELPERS)
+      kernel != KDA_KERNEL_SPLIT && kernel != KDA_KERNEL_TC_HELPERS && kernel != KDA_KERNEL_PIPE)
     return KDA_ERR_INVALID_ARG;
   const size_t split_need = kda::split_workspace_bytes(total_tokens, heads, num_seqs);
   const size_t help_need = kda::helper_workspace_bytes(total_tokens, heads, num_seqs);
   int P = vsplit == -1 ? kda_choose_vsplit(num_seqs, heads, sms) : vsplit;
   if (kernel == KDA_KERNEL_SPLIT) {
     if (workspace_bytes < split_need) return KDA_ERR_WORKSPACE_TOO_SMALL;
+  } else if (kernel == KDA_KERNEL_PIPE) {
+    if (vsplit != -1 && vsplit != 1) return KDA_ERR_INVALID_ARG;
+    P = 1;
   } else if (kernel == KDA_KERNEL_TC_HELPERS) {
     if (vsplit != -1 && vsplit != 1) return KDA_ERR_INVALID_ARG;
     if ((int64_t)num_seqs * heads >= sms || num_seqs > kda::kHelperMaxSeqs ||
@@ -142,8 +146,9 @@ int fwd_impl(const void* q, const void* k, const void* v, const void* g, const v
   if (vsplit != -1 && vsplit != 1 && vsplit != 2 && vsplit != 4 && vsplit != 8)
     return KDA_ERR_INVALID_ARG;
   if (kernel != KDA_KERNEL_AUTO && kernel != KDA_KERNEL_TC && kernel != KDA_KERNEL_REF &&
-      kernel != KDA_KERNEL_SPLIT && kernel != KDA_KERNEL_TC_HELPERS)
+      kernel != KDA_KERNEL_SPLIT && kernel != KDA_KERNEL_TC_HELPERS && kernel != KDA_KERNEL_PIPE)
     return KDA_ERR_INVALID_ARG;
+  if (kernel == KDA_KERNEL_PIPE && scatter) return KDA_ERR_INVALID_ARG;
   int dev = 0, sms = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) {
     cudaGetLastError();
@@ -184,16 +189,21 @@ int fwd_impl(const void* q, const void* k, const void* v, const void* g, const v
   p.s_g = st[3];
   p.s_beta = st[4];
   p.helpers = (kernel == KDA_KERNEL_TC_HELPERS && total_tokens > 0) ? 1 : 0;
-  {
-    const char* drop = std::getenv("KDA_TEST_DROP_ONE_RECORD");
-    p.test_drop_record = (p.helpers && drop && drop[0] == '1') ? 1 : 0;
-  }
+  p.test_drop_record =
+      (p.helpers && g_test_drop_record.load(std::memory_order_relaxed) != 0) ? 1 : 0;
+#ifdef KDA_PHASE_STAMPS
+  // stamps build: the last 8 KB of a workspace of at least 16 KB take the per-chunk stamps
+  if (kernel == KDA_KERNEL_PIPE && workspace_bytes >= 16384)
+    p.stamps = reinterpret_cast<unsigned long long*>(static_cast<unsigned char*>(workspace) +
+                                                     ((workspace_bytes - 8192) & ~(size_t)255));
+#endif
   p.out_index = scatter ? out_index : nullptr;
   p.out_rows = out_rows;
 
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   cudaError_t err = (kernel == KDA_KERNEL_REF)     ? kda::launch_ref(p, s)
                     : (kernel == KDA_KERNEL_SPLIT) ? kda::launch_split(p, s)
+                    : (kernel == KDA_KERNEL_PIPE)  ? kda::launch_pipe(p, s)
                                                    : kda::launch_tc(p, s);
   if (err != cudaSuccess) {
     cudaGetLastError();
@@ -452,6 +462,8 @@ int kda_last_device_status(void* workspace, kda_stream_t stream) {
 }
 
 int kda_device_check(int device) { return check_device(device, nullptr); }
+
+void kda_test_drop_one_record(int on) { g_test_drop_record.store(on != 0 ? 1 : 0); }
 
 int kda_plan_for(int64_t total_tokens, int32_t num_seqs, int32_t heads, size_t workspace_bytes,
                  int vsplit, int kernel, int32_t sm_count, int* kernel_out, int* vsplit_out,

@@ -5,6 +5,9 @@
 #include <cuda_bf16.h>
 #include <stdint.h>
 
+#include <atomic>
+#include <mutex>
+
 #include "kda.h"
 
 namespace kda {
@@ -61,10 +64,32 @@ struct Params {
   // [out_rows, H, 128]; null: to out[t]
   const int32_t* out_index;
   int64_t out_rows;
-  // tests only (KDA_TEST_DROP_ONE_RECORD set in the environment): the helpers leave the record
-  // of the last chunk of the longest sequence's head 0 unpublished, so the bounded wait of
-  // the fused CTA that needs it runs out
+  // tests only (kda_test_drop_one_record(1)): the helpers leave the record of the last chunk
+  // of the longest sequence's head 0 unpublished, so the bounded wait of the fused CTA that
+  // needs it runs out
   int32_t test_drop_record;
+  // builds with -DKDA_PHASE_STAMPS only: per-chunk clock64 stamps of CTA 0 (16 per chunk,
+  // first 64 chunks); null otherwise
+  unsigned long long* stamps;
+};
+
+// A per-device one-time host step (a kernel's shared-memory attribute): the fast path is one
+// atomic load; the first calls on a device serialise on a mutex, so two host threads that
+// make a device's first call at the same time both see the step done.
+struct PerDeviceOnce {
+  static constexpr int kMax = 64;
+  std::atomic<bool> done[kMax] = {};
+  std::mutex mu;
+  template <class Fn>
+  cudaError_t run(int dev, Fn&& fn) {
+    if (dev < 0 || dev >= kMax) return fn();
+    if (done[dev].load(std::memory_order_acquire)) return cudaSuccess;
+    std::lock_guard<std::mutex> lk(mu);
+    if (done[dev].load(std::memory_order_relaxed)) return cudaSuccess;
+    const cudaError_t e = fn();
+    if (e == cudaSuccess) done[dev].store(true, std::memory_order_release);
+    return e;
+  }
 };
 
 // Record a device-side error (first writer wins) with its block and site.
@@ -89,6 +114,8 @@ __device__ __forceinline__ int64_t out_row(const Params& p, int64_t t) {
 
 cudaError_t launch_ref(const Params& p, cudaStream_t stream);
 cudaError_t launch_tc(const Params& p, cudaStream_t stream);
+// Warp-specialised fused kernel (KDA_KERNEL_PIPE): P = 1, dense outputs.
+cudaError_t launch_pipe(const Params& p, cudaStream_t stream);
 // Split path: k-side records for every chunk slot (launch_kside), then the chain
 // per value slice; launch_split runs both.
 cudaError_t launch_kside(const Params& p, cudaStream_t stream);

@@ -11,7 +11,12 @@
 // host-side stand-in, not a device address), so the device address is looked
 // up with cudaGetSymbolAddress, once per device, by the first call made on
 // that device while it is current.  That first call should therefore come
-// before any stream capture.
+// before any stream capture.  The looked-up address is kept for the life of
+// the process: after a cudaDeviceReset (which unloads the library's device
+// module) this entry point must not be called again on that device.
+//
+// The fused kernel runs unsplit (P = 1), as the regular entry point's AUTO
+// does whenever it falls back to the fused kernel.
 //
 // Every call shares the array.  Each call clears the status word on its
 // stream before the kernel runs; calls that overlap on the GPU (different
@@ -76,5 +81,5 @@ extern "C" int kda_chunk_prefill_fwd_noalloc(
   return kda_chunk_prefill_fwd_ex(q, k, v, g, beta, A_log, dt_bias, lower_bound, scale,
                                   initial_state, cu_seqlens, out, final_state, state_dtype,
                                   scratch, stream, total_tokens, num_seqs, heads,
-                                  (size_t)kNoAllocScratchBytes, -1, KDA_KERNEL_TC);
+                                  (size_t)kNoAllocScratchBytes, 1, KDA_KERNEL_TC);
 }

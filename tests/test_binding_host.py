@@ -43,7 +43,7 @@ def test_skinny_proj_refuses_host_tensors():
 
 
 def test_missing_library_is_an_error(monkeypatch, tmp_path):
-    monkeypatch.setattr(kda, "LIB_PATH", str(tmp_path / "libkda.so"))
+    monkeypatch.setattr(kda, "_lib_path", str(tmp_path / "libkda.so"))
     monkeypatch.setattr(kda, "_lib", None)
     with pytest.raises(RuntimeError, match="missing"):
         kda.workspace_size(128, 2, 1)

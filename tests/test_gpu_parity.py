@@ -23,7 +23,8 @@ pytestmark = pytest.mark.gpu
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 TOL = json.load(open(os.path.join(ROOT, "tests", "golden", "tolerances.json")))["max_abs"]
-KERNELS = [kda.KERNEL_REF, kda.KERNEL_TC, kda.KERNEL_SPLIT, kda.KERNEL_TC_HELPERS]
+KERNELS = [kda.KERNEL_REF, kda.KERNEL_TC, kda.KERNEL_SPLIT, kda.KERNEL_TC_HELPERS,
+           kda.KERNEL_PIPE]
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -119,8 +120,8 @@ def test_workload0_tiny(oracle_mod, kernel):
 @pytest.mark.parametrize("vsplit", [1, 2, 4, 8])
 def test_ragged_tiles_and_tails(oracle_mod, kernel, vsplit):
     """Several chunks, ragged tails, a 1-token and an empty sequence."""
-    if kernel == kda.KERNEL_TC_HELPERS and vsplit != 1:
-        pytest.skip("the helpers serve the unsplit fused kernel only")
+    if kernel in (kda.KERNEL_TC_HELPERS, kda.KERNEL_PIPE) and vsplit != 1:
+        pytest.skip("the helpers and the pipelined kernel run unsplit only")
     w = W.custom([1, 63, 64, 65, 130, 0, 200, 17, 129], 3, seed=21)
     inp = W.make_inputs(w)
     out, fin = run_gpu(inp, kernel, vsplit)
@@ -138,7 +139,7 @@ def test_bf16_state(oracle_mod, kernel):
 
 @pytest.mark.parametrize("cfg", [1, 2])
 @pytest.mark.parametrize("kernel", [kda.KERNEL_AUTO, kda.KERNEL_TC, kda.KERNEL_SPLIT,
-                                    kda.KERNEL_TC_HELPERS])
+                                    kda.KERNEL_TC_HELPERS, kda.KERNEL_PIPE])
 def test_workloads_1_2_full_size(oracle_mod, cfg, kernel):
     inp = W.make_inputs(W.workload(cfg))
     out, fin = run_gpu(inp, kernel, 1 if kernel == kda.KERNEL_TC else -1)
@@ -190,7 +191,7 @@ def test_split_falls_back_to_fused_on_small_workspace(oracle_mod):
     assert e.value.code == kda.ERR_WORKSPACE_TOO_SMALL
 
 
-@pytest.mark.parametrize("kernel", [kda.KERNEL_AUTO, kda.KERNEL_SPLIT])
+@pytest.mark.parametrize("kernel", [kda.KERNEL_AUTO, kda.KERNEL_SPLIT, kda.KERNEL_PIPE])
 def test_workload4_ragged_bf16_state(oracle_mod, kernel):
     w = W.workload(4)
     inp = W.make_inputs(w)
@@ -218,23 +219,30 @@ def test_extreme_gates(oracle_mod, kernel, lb, shift):
     check(oracle_mod, inp, out, fin, tag=f"gates lb={lb} shift={shift} k{kernel}")
 
 
-@pytest.mark.parametrize("kernel", KERNELS)
-def test_strided_inputs_equal_dense(kernel):
-    """q, k, v, g as views into one fused [T, 4 * H * 128 + 64] buffer and beta as a view
-    into a wider [T, H + 3] buffer: the strided entry point gives exactly what the dense
-    call gives (the same arithmetic on the same values)."""
-    inp = W.make_inputs(W.custom([130, 64, 1, 77], 2, seed=35))
-    d = to_dev(inp)
+def fused_views(d, extra_cols=64, beta_pad=3):
+    """q, k, v, g as views into one fused [T, 4 * H * 128 + extra_cols] buffer and beta as a
+    view into a wider [T, H + beta_pad] buffer (the layout of a fused projection output)."""
     T, H, D = d["q"].shape
-    fused = torch.zeros(T, 4 * H * D + 64, dtype=torch.bfloat16, device="cuda")
+    fused = torch.zeros(T, 4 * H * D + extra_cols, dtype=torch.bfloat16, device="cuda")
     views = {}
     for j, name in enumerate(("q", "k", "v", "g")):
         fused[:, j * H * D:(j + 1) * H * D] = d[name].reshape(T, H * D)
         views[name] = fused[:, j * H * D:(j + 1) * H * D].view(T, H, D)
-    wide = torch.zeros(T, H + 3, dtype=torch.bfloat16, device="cuda")
+    wide = torch.zeros(T, H + beta_pad, dtype=torch.bfloat16, device="cuda")
     wide[:, 1:H + 1] = d["beta"]
     views["beta"] = wide[:, 1:H + 1]
     assert not views["q"].is_contiguous() and not views["beta"].is_contiguous()
+    return views
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
+def test_strided_inputs_equal_dense(kernel):
+    """The strided entry point gives exactly what the dense call gives (the same
+    arithmetic on the same values)."""
+    inp = W.make_inputs(W.custom([130, 64, 1, 77], 2, seed=35))
+    d = to_dev(inp)
+    views = fused_views(d)
+    T, H = d["q"].shape[:2]
     ws = workspace_for(kernel, T, H, d["cu_seqlens"].numel() - 1)
     outs = []
     for src in (d, views):
@@ -247,37 +255,62 @@ def test_strided_inputs_equal_dense(kernel):
     assert torch.equal(outs[0][0], outs[1][0]) and torch.equal(outs[0][1], outs[1][1])
 
 
+@pytest.mark.parametrize("kernel", KERNELS + [kda.KERNEL_AUTO])
+@pytest.mark.parametrize("sd", ["f32", "bf16"])
+def test_strided_inputs_against_the_oracle(oracle_mod, kernel, sd):
+    """Strided q/k/v/g/beta (views of a fused projection output and of a wider beta
+    buffer, as the FlashKDA prefill wrapper passes them) checked element by element
+    against the oracle: several sequences over many chunks, ragged tails, a 1-token
+    sequence, both state dtypes."""
+    inp = W.make_inputs(W.custom([700, 64, 1, 333, 1030], 3, state_dtype=sd, seed=36))
+    d = to_dev(inp)
+    views = fused_views(d, extra_cols=24, beta_pad=5)
+    T, H = d["q"].shape[:2]
+    ws = workspace_for(kernel, T, H, d["cu_seqlens"].numel() - 1)
+    out, fin = kda.chunk_prefill_fwd(views["q"], views["k"], views["v"], views["g"],
+                                     views["beta"], d["A_log"], d["dt_bias"], d["lower_bound"],
+                                     d["scale"], d["initial_state"], d["cu_seqlens"],
+                                     workspace=ws, kernel=kernel,
+                                     state_dtype=inp["initial_state"].dtype)
+    torch.cuda.synchronize()
+    check(oracle_mod, inp, out, fin, tag=f"strided {sd} k{kernel}")
+
+
 # ----------------------------------------------------------------- edge cases
-def test_inplace_state_update(oracle_mod):
+@pytest.mark.parametrize("kernel", [kda.KERNEL_AUTO, kda.KERNEL_PIPE])
+def test_inplace_state_update(oracle_mod, kernel):
     inp = W.make_inputs(W.custom([90, 40], 2, seed=23))
     d = to_dev(inp)
     state = d["initial_state"].clone()
     out, fin = kda.chunk_prefill_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], d["A_log"],
                                      d["dt_bias"], d["lower_bound"], d["scale"], state,
-                                     d["cu_seqlens"], final_state=state)
+                                     d["cu_seqlens"], final_state=state, kernel=kernel)
     torch.cuda.synchronize()
     assert fin.data_ptr() == state.data_ptr()
     check(oracle_mod, inp, out, fin, tag="in place")
 
 
-def test_null_initial_state(oracle_mod):
+@pytest.mark.parametrize("kernel", [kda.KERNEL_AUTO, kda.KERNEL_PIPE])
+def test_null_initial_state(oracle_mod, kernel):
     inp = W.make_inputs(W.custom([70, 3], 2, seed=24))
-    out, fin = run_gpu(inp, init=None)
+    out, fin = run_gpu(inp, kernel, init=None)
     check(oracle_mod, inp, out, fin, zero_init=True, tag="null initial state")
 
 
-def test_rows_past_last_sequence_untouched(oracle_mod):
-    inp = W.make_inputs(W.custom([50, 20], 2, seed=25, pad_tokens=9))
+@pytest.mark.parametrize("kernel", [kda.KERNEL_AUTO, kda.KERNEL_PIPE])
+def test_rows_past_last_sequence_untouched(oracle_mod, kernel):
+    inp = W.make_inputs(W.custom([50, 20, 128], 2, seed=25, pad_tokens=9))
     sentinel = torch.full(inp["q"].shape, 7.0, dtype=torch.bfloat16, device="cuda")
-    out, fin = run_gpu(inp, out=sentinel)
-    assert torch.all(out[70:].float() == 7.0)
+    out, fin = run_gpu(inp, kernel, out=sentinel)
+    assert torch.all(out[198:].float() == 7.0)
     check(oracle_mod, inp, out, fin, tag="padded")
 
 
+@pytest.mark.parametrize("kernel", [kda.KERNEL_AUTO, kda.KERNEL_PIPE])
 @pytest.mark.parametrize("sd", ["f32", "bf16"])
-def test_empty_sequences_pass_state_through(sd):
+def test_empty_sequences_pass_state_through(sd, kernel):
     inp = W.make_inputs(W.custom([0, 0, 5, 0], 2, state_dtype=sd, seed=26))
-    out, fin = run_gpu(inp)
+    out, fin = run_gpu(inp, kernel)
     s0 = inp["initial_state"]
     for n in (0, 1, 3):
         assert torch.equal(fin[n].cpu(), s0[n])   # bit-exact copy
@@ -322,11 +355,12 @@ def test_errors_returned_with_a_device():
     assert e.value.code == kda.ERR_WORKSPACE_TOO_SMALL
 
 
-def test_cuda_graph_capture_and_replay(oracle_mod):
+@pytest.mark.parametrize("kernel", [kda.KERNEL_AUTO, kda.KERNEL_PIPE])
+def test_cuda_graph_capture_and_replay(oracle_mod, kernel):
     """Capture the call on a side stream, replay it, compare with eager."""
     inp = W.make_inputs(W.custom([200, 64, 3], 4, seed=30))
     d = to_dev(inp)
-    out_e, fin_e = run_gpu(inp)
+    out_e, fin_e = run_gpu(inp, kernel)
     out = torch.empty_like(d["q"])
     fin = torch.empty_like(d["initial_state"])
     ws = kda.alloc_workspace(d["q"].shape[0], 4, 3)
@@ -335,11 +369,13 @@ def test_cuda_graph_capture_and_replay(oracle_mod):
             d["lower_bound"], d["scale"], d["initial_state"], d["cu_seqlens"])
     side.wait_stream(torch.cuda.current_stream())
     with torch.cuda.stream(side):        # warm-up outside capture
-        kda.chunk_prefill_fwd(*args, out=out, final_state=fin, workspace=ws, stream=side)
+        kda.chunk_prefill_fwd(*args, out=out, final_state=fin, workspace=ws, stream=side,
+                              kernel=kernel)
     side.synchronize()
     graph = torch.cuda.CUDAGraph()
     with torch.cuda.graph(graph, stream=side):
-        kda.chunk_prefill_fwd(*args, out=out, final_state=fin, workspace=ws, stream=side)
+        kda.chunk_prefill_fwd(*args, out=out, final_state=fin, workspace=ws, stream=side,
+                              kernel=kernel)
     out.zero_()
     fin.zero_()
     graph.replay()
@@ -426,22 +462,25 @@ def test_helpers_refused_when_they_cannot_run():
     assert e.value.code == kda.ERR_INVALID_ARG
 
 
-def test_bounded_wait_runs_out_and_the_context_survives(monkeypatch):
-    """Failure detection without a GPU fault: with KDA_TEST_DROP_ONE_RECORD=1 the first
-    helper CTA claims its first chunk and never publishes the record.  The fused CTA that
-    needs it waits a bounded time (about a second), records KDA_ERR_DEVICE_TIMEOUT in the
-    workspace and ends; the next call on the same context and workspace is correct."""
+def test_bounded_wait_runs_out_and_the_context_survives():
+    """Failure detection without a GPU fault: with the library's test hook on
+    (kda_test_drop_one_record) the first helper CTA claims its first chunk and never
+    publishes the record.  The fused CTA that needs it waits a bounded time (about a
+    second), records KDA_ERR_DEVICE_TIMEOUT in the workspace and ends; the next call on the
+    same context and workspace is correct."""
     inp = W.make_inputs(W.custom([1024, 1024], 2, seed=44))
     d = to_dev(inp)
     T = d["q"].shape[0]
     ws = helper_workspace(T, 2, 2)
     args = (d["q"], d["k"], d["v"], d["g"], d["beta"], d["A_log"], d["dt_bias"],
             d["lower_bound"], d["scale"], d["initial_state"], d["cu_seqlens"])
-    monkeypatch.setenv("KDA_TEST_DROP_ONE_RECORD", "1")
-    kda.chunk_prefill_fwd(*args, workspace=ws, kernel=kda.KERNEL_TC_HELPERS)
-    torch.cuda.synchronize()
+    kda.test_drop_one_record(True)
+    try:
+        kda.chunk_prefill_fwd(*args, workspace=ws, kernel=kda.KERNEL_TC_HELPERS)
+        torch.cuda.synchronize()
+    finally:
+        kda.test_drop_one_record(False)
     assert kda.last_device_status(ws) == kda.ERR_DEVICE_TIMEOUT
-    monkeypatch.delenv("KDA_TEST_DROP_ONE_RECORD")
     out, fin = kda.chunk_prefill_fwd(*args, workspace=ws, kernel=kda.KERNEL_TC_HELPERS)
     torch.cuda.synchronize()
     assert kda.last_device_status(ws) == kda.OK
