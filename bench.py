@@ -256,11 +256,14 @@ def run_reference(args, w):
     print(json.dumps(line), flush=True)
 
 
-# phase stamps of the pipelined kernel (slots of the 16 per chunk; see kda_pipe_kernel.cu)
-CHAIN_SLOTS = {0: "stage full", 1: "G1a issued", 2: "G1a done", 3: "G1b done", 4: "G2 done",
-               5: "O stored"}
-KSIDE_SLOTS = {8: "inputs landed", 9: "gate, norms, factors", 10: "operand tiles",
-               11: "A|QK MMA done", 12: "A/QK extracted", 13: "T inverse", 14: "stage handed over"}
+# phase stamps of the pipelined kernel: 32 slots per chunk (see kda_pipe_kernel.cu)
+# chain stamp slots (CTA 0, thread 0) and the k-side ones (thread 128); 32 slots per chunk
+CHAIN_SLOTS = {0: "stage full", 2: "S_b stored", 3: "G1a issued", 4: "G1a done", 5: "X_b stored",
+               6: "G1b done", 7: "U_b stored", 8: "G2 done", 10: "O stored"}
+KSIDE_SLOTS = {16: "inputs landed", 17: "gate and norms", 18: "factors", 19: "stage parts free",
+               20: "tile rows done", 21: "tiles fenced", 22: "A|QK MMA done",
+               23: "A/QK loaded", 24: "A/QK extracted", 25: "T inverse", 26: "T tiles free",
+               27: "T tiles stored", 28: "T tiles fenced", 29: "stage handed over"}
 
 
 def run_stamps(args):
@@ -274,10 +277,9 @@ def run_stamps(args):
     w = W.workload(args.workload, args.n) if args.workload == 3 else W.workload(args.workload)
     dev = torch.device("cuda", torch.cuda.current_device())
     d = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in W.make_inputs(w).items()}
-    T, H, N = sum(w.lengths), w.heads, w.num_seqs
     ws_bytes = 1 << 16
     ws = torch.zeros(ws_bytes, dtype=torch.uint8, device=dev)
-    off = (ws_bytes - 8192) & ~255
+    off = (ws_bytes - 16384) & ~255
     for _ in range(max(3, args.warmup) + 1):
         ws[off:].zero_()
         kda.chunk_prefill_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], d["A_log"],
@@ -287,23 +289,32 @@ def run_stamps(args):
     st = kda.last_device_status(ws)
     if st != kda.OK:
         raise kda.KDAError(st, "device status")
-    stamps = ws[off:off + 8192].cpu().view(torch.int64).view(64, 16).tolist()
+    stamps = ws[off:off + 16384].cpu().view(torch.int64).view(64, 32).tolist()
     nch = min(64, (max(w.lengths) + 63) // 64)
     inner = range(1, max(2, nch - 1))
 
-    def med(a, b, prev_b=False):
-        vals = [stamps[c][b] - (stamps[c - 1][a] if prev_b else stamps[c][a]) for c in inner]
+    def med(a, b, prev=False):
+        vals = [stamps[c][b] - (stamps[c - 1][a] if prev else stamps[c][a]) for c in inner]
         return statistics.median(vals) if vals else 0
 
+    ks = sorted(KSIDE_SLOTS)
     res = {"workload": w.name, "chunks_of_cta0": nch, "unit": "SM cycles (clock64), median",
-           "chunk_period": med(14, 14, True),
-           "kside": {f"{KSIDE_SLOTS[a]} -> {KSIDE_SLOTS[a + 1]}": med(a, a + 1)
-                     for a in range(8, 14)},
-           "kside_wait_for_inputs": med(14, 8, True),
-           "chain": {f"{CHAIN_SLOTS[a]} -> {CHAIN_SLOTS[a + 1]}": med(a, a + 1)
-                     for a in range(0, 5)},
-           "chain_wait_for_stage": med(5, 0, True),
-           "chain_start_after_handover": med(14, 0)}
+           "chunk_period": med(29, 29, True),
+           "kside": {f"{KSIDE_SLOTS[a]} -> {KSIDE_SLOTS[b]}": med(a, b) for a, b in zip(ks, ks[1:])},
+           "kside_wait_for_inputs (handover c-1 -> inputs landed c)": med(29, 16, True),
+           "kside_mma_issue (tiles fenced -> MMA issued)": med(21, 31),
+           "kside_next_inputs_issued (tiles fenced -> issued)": med(21, 30),
+           "chain": {f"{CHAIN_SLOTS[a]} -> {CHAIN_SLOTS[b]}": med(a, b)
+                     for a, b in zip(sorted(CHAIN_SLOTS), sorted(CHAIN_SLOTS)[1:])},
+           "chain_wait_for_stage (O stored c-1 -> stage full c)": med(10, 0, True),
+           "handover -> chain start": med(29, 0),
+           "chain G1a done (c-1) -> kside stage parts free (c)": med(4, 19, True),
+           "kside detail": {"K3 factor loads": med(18, 13), "K3 waits for [Kg; Qg]": med(13, 19),
+                            "K4 MMA issue": med(21, 31), "K4 wait for QK/Ke free": med(21, 1),
+                            "K4 Ke from Kc + MMA wait": med(1, 22),
+                            "K6 substitution": med(24, 14), "K6 level 1": med(14, 15),
+                            "K6 level 2a": med(15, 9), "K6 level 2b": med(9, 25),
+                            "K7 wait for the chain": med(11, 12)}}
     print(json.dumps(res, indent=1), flush=True)
 
 

@@ -192,10 +192,11 @@ int fwd_impl(const void* q, const void* k, const void* v, const void* g, const v
   p.test_drop_record =
       (p.helpers && g_test_drop_record.load(std::memory_order_relaxed) != 0) ? 1 : 0;
 #ifdef KDA_PHASE_STAMPS
-  // stamps build: the last 8 KB of a workspace of at least 16 KB take the per-chunk stamps
-  if (kernel == KDA_KERNEL_PIPE && workspace_bytes >= 16384)
+  // stamps build: the last 16 KB of a workspace of at least 32 KB take the per-chunk stamps
+  // (64 chunks x 32 slots of CTA 0)
+  if (kernel == KDA_KERNEL_PIPE && workspace_bytes >= 32768)
     p.stamps = reinterpret_cast<unsigned long long*>(static_cast<unsigned char*>(workspace) +
-                                                     ((workspace_bytes - 8192) & ~(size_t)255));
+                                                     ((workspace_bytes - 16384) & ~(size_t)255));
 #endif
   p.out_index = scatter ? out_index : nullptr;
   p.out_rows = out_rows;

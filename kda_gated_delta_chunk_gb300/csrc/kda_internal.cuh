@@ -68,7 +68,7 @@ struct Params {
   // of the longest sequence's head 0 unpublished, so the bounded wait of the fused CTA that
   // needs it runs out
   int32_t test_drop_record;
-  // builds with -DKDA_PHASE_STAMPS only: per-chunk clock64 stamps of CTA 0 (16 per chunk,
+  // builds with -DKDA_PHASE_STAMPS only: per-chunk clock64 stamps of CTA 0 (32 per chunk,
   // first 64 chunks); null otherwise
   unsigned long long* stamps;
 };

@@ -6,10 +6,10 @@
 // "chain").  The fused kernel of kda_tc_kernel.cuh runs the two halves one after
 // the other; here they run on different warps at the same time:
 //   warps 0-3   chain of chunk c: thread i <-> TMEM lane i <-> value channel i;
-//   warps 4-11  k-side of chunk c+1: gate, cumsum, norms, operand tiles, the A|QK
-//               extraction and the T -> bf16 conversion;
-//   warps 12-15 k-side of chunk c+1: per-channel anchors and factors, row norms,
-//               beta, the UT inverse, the k-side MMA and the input TMA.
+//   warps 4-19  k-side of chunk c+1: gate, cumsum, norms, operand tiles, the A|QK
+//               extraction and the T -> bf16 conversion on all 16 warps; per-channel
+//               anchors and factors, row norms, beta and the UT inverse on warps 4-7;
+//               one thread each issues the k-side MMA and the input TMA.
 // The k-side hands each chunk over through one shared-memory stage guarded by
 // mbarriers (stage full: k-side -> chain; stage parts free: chain -> k-side).
 //
@@ -31,7 +31,7 @@
 // The chain's products, all tcgen05 kind::f16 with M = 128 = value channel:
 //   [X^T | O^T]  = S_b^T [Kg | Qg]^T          (S_b = bf16 S^T in TMEM, N = 128)
 //   U^T          = V^T (T diag b)^T + X_b^T T^T   (X_b = bf16(X^T diag(-b inv_k)))
-//   O^T         += U_b^T QK^T,  S^T += U_b^T Ke  (U_b = bf16(U^T diag(inv_k)))
+//   [O^T | S^T] += U_b^T [QK | Ke]             (U_b = bf16(U^T diag(inv_k)), N = 192)
 // and the k-side's: [A | QK] = [Kr; Qr] [Kc; Kc2]^T (M = 128, N = 96) over the
 // exponent-anchored operands of kda_tc_kernel.cu (two 32-token blocks anchored at
 // their 16th token; Kc2 carries the block-0 columns seen from block 1).
@@ -52,7 +52,7 @@ using namespace tcc;
 
 constexpr int PC = 64;            // chunk
 constexpr int PD = kHeadDim;      // 128
-constexpr int PNT = 512;
+constexpr int PNT = 640;
 constexpr int kPipeMaxRankSeqs = 128;
 
 // ---- shared memory (offsets from a 1024-byte aligned base)
@@ -67,12 +67,11 @@ constexpr int PS_TM = PS_NM + 64 * NS * 4;   //       T [64][NS]
 constexpr int PS_Y = PS_TM + 64 * NS * 4;    //       product scratch [32][NS]
 // the stage (chain operands of one chunk)
 constexpr int PS_WQ = 106496;         // [Kg; Qg] K-major 128 rows (tokens) x 128 (dk)
-constexpr int PS_V = 139264;          // v: two SW128 boxes [64 tok][64 dv]; after U: O staging
-                                      //    [64 tok][128 dv] bf16 row-major
+constexpr int PS_V = 139264;          // v: two SW128 boxes [64 tok][64 dv]
 constexpr int PS_TB = 155648;         // T diag(b) K-major 64 x 64
 constexpr int PS_TT = 163840;         // T K-major 64 x 64
-constexpr int PS_QK = 172032;         // QK (masked, raw) K-major 64 x 64
-constexpr int PS_KE = 180224;         // Ke MN-major: 128 dk (2 blocks of 64, 8 KB apart) x 64 tok
+constexpr int PS_QK = 172032;         // [QK | Ke] MN-major, N = 192 in blocks of 64, 8 KB apart:
+constexpr int PS_KE = 180224;         //   QK (n = row r, k = token s; masked, raw), then Ke (n = dk)
 // small things
 constexpr int PS_VEC = 196608;        // [3 by chunk % 3]: decay[128] iq[64] ik[64] nbik[64] fp32
 constexpr int kVecFloats = 320;
@@ -82,7 +81,7 @@ constexpr int PS_SS = PS_FAC + 6 * 128 * 4;           // row sums of squares: q 
 constexpr int PS_RSC = PS_SS + 128 * 4;               // row power-of-two scales, bf16x2 [128]
 constexpr int PS_BETA = PS_RSC + 128 * 4;             // b [64]
 constexpr int PS_BAR = PS_BETA + 64 * 4;              // mbarriers
-constexpr int PS_TSLOT = PS_BAR + 16 * 8;
+constexpr int PS_TSLOT = PS_BAR + 16 * 8;   // (10 mbarriers used)
 constexpr int PS_FLAGS = PS_TSLOT + 16;
 constexpr int PS_END = PS_FLAGS + 16;
 constexpr int PIPE_SMEM = PS_END + 1024;
@@ -99,12 +98,13 @@ static_assert(PIPE_SMEM <= 227 * 1024, "shared memory");
 constexpr int B_IN = 0;      // q, k, g of the k-side's chunk landed (TMA tx)
 constexpr int B_V = 1;       // v of the chain's chunk landed (TMA tx)
 constexpr int B_FULL = 2;    // stage written by the k-side (1 arrival)
-constexpr int B_FREEA = 3;   // chain done with [Kg; Qg], T diag(b), T (and v)
+constexpr int B_FREEA = 3;   // chain done with [Kg; Qg]
 constexpr int B_FREEB = 4;   // chain done with QK, Ke
 constexpr int B_KMMA = 5;    // k-side A|QK MMA done
 constexpr int B_G1A = 6;     // chain: [X^T | O^T] done
 constexpr int B_G1B = 7;     // chain: U^T done
 constexpr int B_G2 = 8;      // chain: O^T, S^T updates done
+constexpr int B_FREEC = 9;   // chain done with T diag(b), T
 
 // ---- tensor memory columns (fp32 unless noted; lane = value channel, or row for D)
 constexpr uint32_t TM_XU = 0;     // X^T, then U^T   64 cols (col = token)
@@ -119,14 +119,21 @@ constexpr uint32_t TM_NCOLS = 512;
 constexpr uint32_t ID_D96 = idesc_bf16(128, 96, 0, 0);    // [Kr;Qr] x [Kc;Kc2]^T
 constexpr uint32_t ID_G1A = idesc_bf16(128, 128, 0, 0);   // S_b x [Kg|Qg]^T
 constexpr uint32_t ID_UP = idesc_bf16(128, 64, 1, 0);     // V^T (MN-major) x (T diag b)^T
-constexpr uint32_t ID_N64 = idesc_bf16(128, 64, 0, 0);    // X_b x T^T,  U_b x QK^T
-constexpr uint32_t ID_KE = idesc_bf16(128, 128, 0, 1);    // U_b x Ke (MN-major)
+constexpr uint32_t ID_N64 = idesc_bf16(128, 64, 0, 0);    // X_b x T^T
+constexpr uint32_t ID_G2 = idesc_bf16(128, 192, 0, 1);    // U_b x [QK | Ke] (MN-major)
 
 #ifdef KDA_PHASE_STAMPS
+// The clock is read in an asm statement with a memory clobber, so that it keeps its place
+// relative to the barriers (also asm with memory clobbers) it is meant to bracket.
+__device__ __forceinline__ unsigned long long stamp_clock() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%clock64;" : "=l"(t) : : "memory");
+  return t;
+}
 #define PSTAMP(cond, c, slot)                                                       \
   do {                                                                              \
     if ((cond) && p.stamps != nullptr && blockIdx.x == 0 && (c) < 64)               \
-      p.stamps[(c) * 16 + (slot)] = (unsigned long long)clock64();                  \
+      p.stamps[(c) * 32 + (slot)] = stamp_clock();                                  \
   } while (0)
 #else
 #define PSTAMP(cond, c, slot) \
@@ -135,8 +142,11 @@ constexpr uint32_t ID_KE = idesc_bf16(128, 128, 0, 1);    // U_b x Ke (MN-major)
 #endif
 
 // barrier `id` over `count` threads with an OR reduction of `pred` (group-uniform result)
+// (the warp reconverges first: bar.red is an aligned barrier, and callers come out of
+// lane-divergent code such as one lane's mbarrier wait)
 __device__ __forceinline__ bool bar_any(uint32_t id, uint32_t count, bool pred) {
   uint32_t r;
+  __syncwarp();
   asm volatile(
       "{\n\t.reg .pred p, q;\n\t"
       "setp.ne.b32 p, %1, 0;\n\t"
@@ -147,25 +157,37 @@ __device__ __forceinline__ bool bar_any(uint32_t id, uint32_t count, bool pred) 
       : "memory");
   return r != 0;
 }
-__device__ __forceinline__ void tma_store_2d(const void* tmap, int x, int y, uint32_t src) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
-          reinterpret_cast<uint64_t>(tmap)),
-      "r"(x), "r"(y), "r"(src)
-      : "memory");
+// bar.sync over `count` threads, after the warp has reconverged
+__device__ __forceinline__ void group_sync(uint32_t id, uint32_t count) {
+  __syncwarp();
+  named_barrier_sync(id, count);
 }
-__device__ __forceinline__ uint4 lds128(const unsigned char* base, uint32_t off) {
-  return *reinterpret_cast<const uint4*>(base + off);
+// One thread's bounded wait for a phase: a non-blocking test first (most waits find the
+// phase complete), then hardware-parked retries.
+__device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity) {
+  if (mbar_test_wait(bar, parity)) return true;
+  return mbar_wait_sleep(bar, parity);
 }
-// byte offset of the 16-byte chunk holding columns 8o..8o+7 of row r in a tile of two
-// SW128 boxes [64 rows][64 cols] 8 KB apart (what a TMA box of 64 columns writes)
-__device__ __forceinline__ uint32_t in_off(int r, int o) {
-  return (uint32_t)((o >> 3) * 8192 + r * 128 + (((o & 7) ^ (r & 7)) << 4));
+// The chain's MMA waits are short and on the critical path: poll first (a parked thread
+// takes a while to wake), then fall back to the parked, bounded wait.
+__device__ __forceinline__ bool wait_spin(uint32_t bar, uint32_t parity) {
+  for (int i = 0; i < 4096; ++i)
+    if (mbar_test_wait(bar, parity)) return true;
+  return mbar_wait_sleep(bar, parity);
+}
+__device__ __forceinline__ void wgemm16(const float* A, const float* B, float* dst, float sign,
+                                     int lane) {
+  warp_gemm_16x16<16>(A, B, dst, sign, lane);
+}
+__device__ __forceinline__ void wgemm32(const float* A, const float* B, float* dst, float sign,
+                                     int lane) {
+  warp_gemm_16x16<32>(A, B, dst, sign, lane);
 }
 
 struct PipeMaps {
-  CUtensorMap q, k, g, v;   // [T][H*128] bf16, box {64, 64}, 128-byte swizzle
-  CUtensorMap out;          // [T][H*128] bf16, box {128, 64}, no swizzle
+  // q, k, g, v as [2H blocks of 64 cols][T rows][64 cols] bf16, box {64, 64, 2}, 128-byte
+  // swizzle: one load brings the 128 columns of a head as two SW128 tiles
+  CUtensorMap q, k, g, v;
 };
 
 __global__ void __launch_bounds__(PNT, 1)
@@ -210,6 +232,7 @@ __global__ void __launch_bounds__(PNT, 1)
   const size_t HD = (size_t)H * PD;
   const size_t sbase = ((size_t)n * H + h) * PD * PD;
   const int xcol = h * PD;
+  const int zblk = 2 * h;   // first 64-column block of this head in the 3-D views
 
   if (tid == 0) {
     mbar_init(bar(B_IN), 1);
@@ -221,6 +244,7 @@ __global__ void __launch_bounds__(PNT, 1)
     mbar_init(bar(B_G1A), 1);
     mbar_init(bar(B_G1B), 1);
     mbar_init(bar(B_G2), 1);
+    mbar_init(bar(B_FREEC), 1);
     mbar_fence_init();
   }
   if (warp == 0) {
@@ -243,11 +267,9 @@ __global__ void __launch_bounds__(PNT, 1)
     int cfail = 0;  // chunk at which the loop stopped (all pending phases have its parity)
     if (tid == 0) {
       tma_prefetch_desc(&maps.v);
-      tma_prefetch_desc(&maps.out);
       if (nch > 0) {
         mbar_expect_tx(bar(B_V), 16384);
-        tma_load_2d(sb + PS_V, &maps.v, xcol, t0, bar(B_V));
-        tma_load_2d(sb + PS_V + 8192, &maps.v, xcol + 64, t0, bar(B_V));
+        tma_load_3d(sb + PS_V, &maps.v, 0, t0, zblk, bar(B_V));
         pend |= 1;
       }
     }
@@ -255,16 +277,18 @@ __global__ void __launch_bounds__(PNT, 1)
 #pragma unroll 1
     for (int cb = 0; cb < 4; ++cb) {
       uint32_t r[32];
+      if (p.initial_state == nullptr) {
 #pragma unroll
-      for (int j = 0; j < 32; ++j) {
-        float s = 0.0f;
-        if (p.initial_state) {
-          const size_t idx = sbase + (size_t)(cb * 32 + j) * PD + dv;
-          s = p.state_bf16
-                  ? __bfloat162float(static_cast<const __nv_bfloat16*>(p.initial_state)[idx])
-                  : static_cast<const float*>(p.initial_state)[idx];
-        }
-        r[j] = __float_as_uint(s);
+        for (int j2 = 0; j2 < 32; ++j2) r[j2] = 0u;
+      } else if (p.state_bf16) {
+        const __nv_bfloat16* src = static_cast<const __nv_bfloat16*>(p.initial_state) + sbase +
+                                   (size_t)cb * 32 * PD + dv;
+#pragma unroll
+        for (int j2 = 0; j2 < 32; ++j2) r[j2] = __float_as_uint(__bfloat162float(src[j2 * PD]));
+      } else {
+        const float* src = static_cast<const float*>(p.initial_state) + sbase + (size_t)cb * 32 * PD + dv;
+#pragma unroll
+        for (int j2 = 0; j2 < 32; ++j2) r[j2] = __float_as_uint(src[j2 * PD]);
       }
       tmem_st32(tmem + lb + TM_S + cb * 32, r);
     }
@@ -277,14 +301,19 @@ __global__ void __launch_bounds__(PNT, 1)
       const float* vec = vecs + (c % 3) * kVecFloats;
       cfail = c;
 
-      // C0: the stage and v of chunk c have landed
-      bool ok = mbar_wait(bar(B_FULL), par);
-      const bool v_ok = mbar_wait(bar(B_V), par);
-      if (tid == 0 && v_ok) pend &= ~1;
-      ok = ok && v_ok;
+      // C0: the stage and v of chunk c have landed (thread 0 waits; the group parks on the
+      //     barrier that carries the outcome)
+      bool ok = true;
+      if (tid == 0) {
+        ok = wait_phase(bar(B_FULL), par);
+        const bool v_ok = wait_phase(bar(B_V), par);
+        if (v_ok) pend &= ~1;
+        ok = ok && v_ok;
+      }
+      if (bar_any(4, 128, !ok)) { failed = true; site = 39; break; }
       PSTAMP(tid == 0, c, 0);
-      if (ok && L < PC) {   // v rows past the sequence end -> 0 (they meet zero columns of
-                            // T diag(b), but must not carry inf or nan into the product)
+      if (L < PC) {   // v rows past the sequence end -> 0 (they meet zero columns of
+                      // T diag(b), but must not carry inf or nan into the product)
         for (int idx = tid; idx < (PC - L) * 16; idx += 128) {
           const int r = L + idx / 16, cc = idx % 16;
           *reinterpret_cast<uint4*>(sm + PS_V + (cc >> 3) * 8192 + r * 128 +
@@ -293,25 +322,26 @@ __global__ void __launch_bounds__(PNT, 1)
         fence_proxy_async();
       }
       tc_fence_after();
-      // C1a: S_b = bf16(S^T)
+      // C1a: S_b = bf16(S^T), 64 key columns at a time
 #pragma unroll 1
-      for (int cb = 0; cb < 4; cb += 2) {
+      for (int hh = 0; hh < 2; ++hh) {
         uint32_t x[32], y[32], pk[16];
-        tmem_ld32(tmem + lb + TM_S + cb * 32, x);
-        tmem_ld32(tmem + lb + TM_S + cb * 32 + 32, y);
+        tmem_ld32(tmem + lb + TM_S + hh * 64, x);
+        tmem_ld32(tmem + lb + TM_S + hh * 64 + 32, y);
         tmem_wait_ld();
 #pragma unroll
-        for (int j = 0; j < 16; ++j)
-          pk[j] = pack_bf16x2(__uint_as_float(x[2 * j]), __uint_as_float(x[2 * j + 1]));
-        tmem_st16(tmem + lb + TM_SB + cb * 16, pk);
+        for (int j2 = 0; j2 < 16; ++j2)
+          pk[j2] = pack_bf16x2(__uint_as_float(x[2 * j2]), __uint_as_float(x[2 * j2 + 1]));
+        tmem_st16(tmem + lb + TM_SB + hh * 32, pk);
 #pragma unroll
-        for (int j = 0; j < 16; ++j)
-          pk[j] = pack_bf16x2(__uint_as_float(y[2 * j]), __uint_as_float(y[2 * j + 1]));
-        tmem_st16(tmem + lb + TM_SB + cb * 16 + 16, pk);
+        for (int j2 = 0; j2 < 16; ++j2)
+          pk[j2] = pack_bf16x2(__uint_as_float(y[2 * j2]), __uint_as_float(y[2 * j2 + 1]));
+        tmem_st16(tmem + lb + TM_SB + hh * 32 + 16, pk);
       }
       tmem_wait_st();
       tc_fence_before();
-      if (bar_any(4, 128, !ok)) { failed = true; site = 40; break; }
+      group_sync(4, 128);
+      PSTAMP(tid == 0, c, 2);
       // G1a: [X^T | O^T] = S_b [Kg | Qg]^T
       if (tid == 0) {
         tc_fence_after();
@@ -321,7 +351,7 @@ __global__ void __launch_bounds__(PNT, 1)
                       ks > 0);
         mma_commit(bar(B_G1A));
         pend |= 2;
-        PSTAMP(true, c, 1);
+        PSTAMP(true, c, 3);
       }
       // C1b: S^T *= 2^G_last (per key column), while G1a runs
 #pragma unroll 1
@@ -340,17 +370,23 @@ __global__ void __launch_bounds__(PNT, 1)
         tmem_st32(tmem + lb + TM_S + cb * 32, x);
       }
       tmem_wait_st();
-      // C2: X_b = bf16(X^T diag(-b inv_k))
-      ok = mbar_wait(bar(B_G1A), par);
-      if (tid == 0 && ok) pend &= ~2;
-      PSTAMP(tid == 0, c, 2);
+      if (tid == 0) {
+        ok = wait_spin(bar(B_G1A), par);
+        if (ok) {
+          pend &= ~2;
+          mbar_arrive(bar(B_FREEA));   // [Kg; Qg] is free
+        }
+      }
+      if (bar_any(4, 128, !ok)) { failed = true; site = 40; break; }
+      PSTAMP(tid == 0, c, 4);
       tc_fence_after();
-      {
-        uint32_t x[32], y[32], pk[16];
-        tmem_ld32(tmem + lb + TM_XU, x);
-        tmem_ld32(tmem + lb + TM_XU + 32, y);
+      // C2: X_b = bf16(X^T diag(-b inv_k)), 32 tokens at a time
+#pragma unroll 1
+      for (int hh = 0; hh < 2; ++hh) {
+        uint32_t x[32], pk[16];
+        tmem_ld32(tmem + lb + TM_XU + hh * 32, x);
         tmem_wait_ld();
-        const float* nb = vec + 256;
+        const float* nb = vec + 256 + hh * 32;
 #pragma unroll
         for (int j4 = 0; j4 < 8; ++j4) {
           const float4 f = ld4(nb + 4 * j4);
@@ -359,20 +395,12 @@ __global__ void __launch_bounds__(PNT, 1)
           pk[2 * j4 + 1] = pack_bf16x2(__uint_as_float(x[4 * j4 + 2]) * f.z,
                                        __uint_as_float(x[4 * j4 + 3]) * f.w);
         }
-        tmem_st16(tmem + lb + TM_XB, pk);
-#pragma unroll
-        for (int j4 = 0; j4 < 8; ++j4) {
-          const float4 f = ld4(nb + 32 + 4 * j4);
-          pk[2 * j4] = pack_bf16x2(__uint_as_float(y[4 * j4]) * f.x,
-                                   __uint_as_float(y[4 * j4 + 1]) * f.y);
-          pk[2 * j4 + 1] = pack_bf16x2(__uint_as_float(y[4 * j4 + 2]) * f.z,
-                                       __uint_as_float(y[4 * j4 + 3]) * f.w);
-        }
-        tmem_st16(tmem + lb + TM_XB + 16, pk);
+        tmem_st16(tmem + lb + TM_XB + hh * 16, pk);
       }
       tmem_wait_st();
       tc_fence_before();
-      if (bar_any(4, 128, !ok)) { failed = true; site = 41; break; }
+      group_sync(4, 128);
+      PSTAMP(tid == 0, c, 5);
       // G1b: U^T = V^T (T diag b)^T + X_b^T T^T
       if (tid == 0) {
         tc_fence_after();
@@ -385,21 +413,27 @@ __global__ void __launch_bounds__(PNT, 1)
           mma_bf16_ts(tmem + TM_XU, tmem + TM_XB + 8 * ks, kdesc(sb + PS_TT, 64, ks), ID_N64, 1);
         mma_commit(bar(B_G1B));
         pend |= 4;
+        ok = wait_spin(bar(B_G1B), par);
+        if (ok) {
+          pend &= ~4;
+          mbar_arrive(bar(B_FREEC));   // T diag(b), T are free
+          if (c + 1 < nch) {           // v is free: the next chunk's v
+            mbar_expect_tx(bar(B_V), 16384);
+            tma_load_3d(sb + PS_V, &maps.v, 0, c0 + PC, zblk, bar(B_V));
+            pend |= 1;
+          }
+        }
       }
-      ok = mbar_wait(bar(B_G1B), par);
-      if (tid == 0 && ok) {
-        pend &= ~4;
-        mbar_arrive(bar(B_FREEA));   // [Kg; Qg], T diag(b), T are free
-      }
-      PSTAMP(tid == 0, c, 3);
+      if (bar_any(4, 128, !ok)) { failed = true; site = 41; break; }
+      PSTAMP(tid == 0, c, 6);
       tc_fence_after();
       // C3: U_b = bf16(U^T diag(inv_k))
-      {
-        uint32_t x[32], y[32], pk[16];
-        tmem_ld32(tmem + lb + TM_XU, x);
-        tmem_ld32(tmem + lb + TM_XU + 32, y);
+#pragma unroll 1
+      for (int hh = 0; hh < 2; ++hh) {
+        uint32_t x[32], pk[16];
+        tmem_ld32(tmem + lb + TM_XU + hh * 32, x);
         tmem_wait_ld();
-        const float* ik = vec + 192;
+        const float* ik = vec + 192 + hh * 32;
 #pragma unroll
         for (int j4 = 0; j4 < 8; ++j4) {
           const float4 f = ld4(ik + 4 * j4);
@@ -408,84 +442,60 @@ __global__ void __launch_bounds__(PNT, 1)
           pk[2 * j4 + 1] = pack_bf16x2(__uint_as_float(x[4 * j4 + 2]) * f.z,
                                        __uint_as_float(x[4 * j4 + 3]) * f.w);
         }
-        tmem_st16(tmem + lb + TM_UB, pk);
-#pragma unroll
-        for (int j4 = 0; j4 < 8; ++j4) {
-          const float4 f = ld4(ik + 32 + 4 * j4);
-          pk[2 * j4] = pack_bf16x2(__uint_as_float(y[4 * j4]) * f.x,
-                                   __uint_as_float(y[4 * j4 + 1]) * f.y);
-          pk[2 * j4 + 1] = pack_bf16x2(__uint_as_float(y[4 * j4 + 2]) * f.z,
-                                       __uint_as_float(y[4 * j4 + 3]) * f.w);
-        }
-        tmem_st16(tmem + lb + TM_UB + 16, pk);
+        tmem_st16(tmem + lb + TM_UB + hh * 16, pk);
       }
       tmem_wait_st();
       tc_fence_before();
-      if (bar_any(4, 128, !ok)) { failed = true; site = 42; break; }
-      // G2: O^T += U_b^T QK^T, S^T += U_b^T Ke
+      group_sync(4, 128);
+      PSTAMP(tid == 0, c, 7);
+      // G2: [O^T | S^T] += U_b^T [QK | Ke]^T (one N = 192 group)
       if (tid == 0) {
         tc_fence_after();
 #pragma unroll
         for (int ks = 0; ks < 4; ++ks)
-          mma_bf16_ts(tmem + TM_O, tmem + TM_UB + 8 * ks, kdesc(sb + PS_QK, 64, ks), ID_N64, 1);
-#pragma unroll
-        for (int ks = 0; ks < 4; ++ks)
-          mma_bf16_ts(tmem + TM_S, tmem + TM_UB + 8 * ks, mndesc(sb + PS_KE, 8192, ks), ID_KE, 1);
+          mma_bf16_ts(tmem + TM_O, tmem + TM_UB + 8 * ks, mndesc(sb + PS_QK, 8192, ks), ID_G2, 1);
         mma_commit(bar(B_G2));
         pend |= 8;
+        ok = wait_spin(bar(B_G2), par);
+        if (ok) {
+          pend &= ~8;
+          mbar_arrive(bar(B_FREEB));   // QK, Ke are free
+        }
       }
-      ok = mbar_wait(bar(B_G2), par);
-      if (tid == 0 && ok) {
-        pend &= ~8;
-        mbar_arrive(bar(B_FREEB));   // QK, Ke are free
-      }
-      PSTAMP(tid == 0, c, 4);
+      if (bar_any(4, 128, !ok)) { failed = true; site = 42; break; }
+      PSTAMP(tid == 0, c, 8);
       tc_fence_after();
-      // C4: O^T diag(inv_q) -> bf16 staging [token][dv] (over v, free since G1b)
+      // C4: O^T diag(inv_q) -> out rows < L of this value channel (a warp writes 64
+      //     contiguous bytes of each row)
       {
-        uint32_t x[32], y[32];
-        tmem_ld32(tmem + lb + TM_O, x);
-        tmem_ld32(tmem + lb + TM_O + 32, y);
-        tmem_wait_ld();
         const float* iq = vec + 128;
-        __nv_bfloat16* ost = reinterpret_cast<__nv_bfloat16*>(sm + PS_V);
+        __nv_bfloat16* orow = p.out + (size_t)c0 * HD + xcol + dv;
+#pragma unroll 1
+        for (int qq = 0; qq < 4; ++qq) {
+          uint32_t x[16];
+          tmem_ld16(tmem + lb + TM_O + qq * 16, x);
+          tmem_wait_ld();
 #pragma unroll
-        for (int j = 0; j < 32; ++j)
-          ost[j * PD + dv] = __float2bfloat16_rn(__uint_as_float(x[j]) * iq[j]);
+          for (int t4 = 0; t4 < 4; ++t4) {
+            const float4 f = ld4(iq + qq * 16 + 4 * t4);
+            const float fv[4] = {f.x, f.y, f.z, f.w};
 #pragma unroll
-        for (int j = 0; j < 32; ++j)
-          ost[(32 + j) * PD + dv] = __float2bfloat16_rn(__uint_as_float(y[j]) * iq[32 + j]);
-      }
-      fence_proxy_async();
-      tc_fence_before();
-      if (bar_any(4, 128, !ok)) { failed = true; site = 43; break; }
-      if (L == PC) {
-        if (tid == 0) {
-          tma_store_2d(&maps.out, xcol, c0, sb + PS_V);
-          bulk_commit();
-          bulk_wait_read();   // the staging is read: v of the next chunk may land there
-          if (c + 1 < nch) {
-            mbar_expect_tx(bar(B_V), 16384);
-            tma_load_2d(sb + PS_V, &maps.v, xcol, c0 + PC, bar(B_V));
-            tma_load_2d(sb + PS_V + 8192, &maps.v, xcol + 64, c0 + PC, bar(B_V));
-            pend |= 1;
+            for (int e = 0; e < 4; ++e) {
+              const int r = qq * 16 + 4 * t4 + e;
+              if (r < L) orow[(size_t)r * HD] = __float2bfloat16_rn(__uint_as_float(x[4 * t4 + e]) * fv[e]);
+            }
           }
         }
-      } else {   // the sequence's last chunk: rows < L only
-        for (int idx = tid; idx < L * 16; idx += 128) {
-          const int r = idx >> 4, v8 = idx & 15;
-          *reinterpret_cast<uint4*>(p.out + (size_t)(c0 + r) * HD + xcol + v8 * 8) =
-              *reinterpret_cast<const uint4*>(sm + PS_V + r * 256 + v8 * 16);
-        }
       }
-      PSTAMP(tid == 0, c, 5);
+      tc_fence_before();
+      PSTAMP(tid == 0, c, 10);
     }
     if (failed) {
       if (tid == 0) {
         record_error(p.status, KDA_ERR_DEVICE_TIMEOUT, site);
         // let copies and MMAs still in flight end (bounded) before the CTA exits
         const uint32_t fp = (uint32_t)(cfail & 1);
-        if (pend & 1) mbar_wait(bar(B_V), fp);
+        if (pend & 1) mbar_wait(bar(B_V), fp ^ (uint32_t)((pend & 4) == 0 && site == 41 ? 1 : 0));
         if (pend & 2) mbar_wait(bar(B_G1A), fp);
         if (pend & 4) mbar_wait(bar(B_G1B), fp);
         if (pend & 8) mbar_wait(bar(B_G2), fp);
@@ -497,28 +507,27 @@ __global__ void __launch_bounds__(PNT, 1)
         uint32_t r[32];
         tmem_ld32(tmem + lb + TM_S + cb * 32, r);
         tmem_wait_ld();
+        if (p.state_bf16) {
+          __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(p.final_state) + sbase + (size_t)cb * 32 * PD + dv;
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          const size_t idx = sbase + (size_t)(cb * 32 + j) * PD + dv;
-          const float s = __uint_as_float(r[j]);
-          if (p.state_bf16)
-            static_cast<__nv_bfloat16*>(p.final_state)[idx] = __float2bfloat16_rn(s);
-          else
-            static_cast<float*>(p.final_state)[idx] = s;
+          for (int j2 = 0; j2 < 32; ++j2) dst[j2 * PD] = __float2bfloat16_rn(__uint_as_float(r[j2]));
+        } else {
+          float* dst = static_cast<float*>(p.final_state) + sbase + (size_t)cb * 32 * PD + dv;
+#pragma unroll
+          for (int j2 = 0; j2 < 32; ++j2) dst[j2 * PD] = __uint_as_float(r[j2]);
         }
       }
     }
-    if (tid == 0) bulk_wait_all();
   } else {
     // =========================================================================== k-side
-    const int kt = tid - 128;                 // 0..383
-    const bool isA = kt < 256;                // warps 4-11: tiles; warps 12-15: scalars
-    const int ka = kt, wa = ka >> 5;          // (group A)
-    const int o = lane & 15;                  // octet: key channels 8o .. 8o+7
-    const int j = 2 * wa + (lane >> 4);       // row quad: rows 4j .. 4j+3
-    const int bsel = wa >> 2;                 // 32-token block of this thread's rows
-    const int kb = kt - 256;                  // 0..127 (group B)
-    const bool mma_thread = kb == 0, tma_thread = kb == 64;
+    // 512 threads.  Tile phases: thread (row quad j = warp, channel quad o4 = lane) owns rows
+    // 4j .. 4j+3 and key channels 4 o4 .. 4 o4 + 3.  Scalar phases and the inverse: the first
+    // 128 threads (warps 4-7).
+    const int kt = tid - 128;                 // 0..511
+    const int j = kt >> 5;                    // row quad
+    const int o4 = lane;                      // channel quad
+    const int bsel = j >> 3;                  // 32-token block of this thread's rows
+    const bool mma_thread = kt == 0, tma_thread = kt == 32, free_thread = kt == 64;
     float* GT = reinterpret_cast<float*>(sm + PS_GT);
     float* FAC = reinterpret_cast<float*>(sm + PS_FAC);
     float* SS = reinterpret_cast<float*>(sm + PS_SS);
@@ -530,31 +539,32 @@ __global__ void __launch_bounds__(PNT, 1)
     const float gate_scale = expf(p.A_log[h]);
     const float lb2 = p.lower_bound * kLog2e;
     const float sg = -gate_scale * kLog2e;   // sigmoid argument, log2 units: sg (g + dt_bias)
-    float sgd[8];
+    float sgd[4];
 #pragma unroll
-    for (int e = 0; e < 8; ++e) sgd[e] = isA ? sg * p.dt_bias[h * PD + 8 * o + e] : 0.0f;
+    for (int e = 0; e < 4; ++e) sgd[e] = sg * p.dt_bias[h * PD + 4 * o4 + e];
     int in_pend = 0;      // tma thread: an input load issued and not waited (its parity + 1)
     int kmma_pend = 0;    // the A|QK MMA issued and not waited (its parity + 1)
+    // byte offset of the 8 bytes holding columns 4 o4 .. 4 o4 + 3 of row r of an input tile
+    auto in8 = [&](int r) -> uint32_t {
+      return (uint32_t)((o4 >> 4) * 8192 + r * 128 + ((((o4 & 15) >> 1) ^ (r & 7)) << 4) +
+                        ((o4 & 1) << 3));
+    };
+    auto ld8b = [&](uint32_t off) -> uint2 { return *reinterpret_cast<const uint2*>(sm + off); };
+    auto st8b = [&](uint32_t off, uint32_t a, uint32_t b) {
+      *reinterpret_cast<uint2*>(sm + off) = make_uint2(a, b);
+    };
 
     auto issue_in = [&](int c) {   // q, k, g of chunk c -> the input tiles; chunk c+1 -> L2
       const int y = t0 + PC * c;
       mbar_expect_tx(bar(B_IN), 49152);
-      tma_load_2d(sb + PS_INQ, &maps.q, xcol, y, bar(B_IN));
-      tma_load_2d(sb + PS_INQ + 8192, &maps.q, xcol + 64, y, bar(B_IN));
-      tma_load_2d(sb + PS_INK, &maps.k, xcol, y, bar(B_IN));
-      tma_load_2d(sb + PS_INK + 8192, &maps.k, xcol + 64, y, bar(B_IN));
-      tma_load_2d(sb + PS_ING, &maps.g, xcol, y, bar(B_IN));
-      tma_load_2d(sb + PS_ING + 8192, &maps.g, xcol + 64, y, bar(B_IN));
+      tma_load_3d(sb + PS_INQ, &maps.q, 0, y, zblk, bar(B_IN));
+      tma_load_3d(sb + PS_INK, &maps.k, 0, y, zblk, bar(B_IN));
+      tma_load_3d(sb + PS_ING, &maps.g, 0, y, zblk, bar(B_IN));
       if (c + 1 < nch) {
-        const int y1 = y + PC;
-        tma_prefetch_2d(&maps.q, xcol, y1);
-        tma_prefetch_2d(&maps.q, xcol + 64, y1);
-        tma_prefetch_2d(&maps.k, xcol, y1);
-        tma_prefetch_2d(&maps.k, xcol + 64, y1);
-        tma_prefetch_2d(&maps.g, xcol, y1);
-        tma_prefetch_2d(&maps.g, xcol + 64, y1);
-        tma_prefetch_2d(&maps.v, xcol, y1);
-        tma_prefetch_2d(&maps.v, xcol + 64, y1);
+        tma_prefetch_3d(&maps.q, 0, y + PC, zblk);
+        tma_prefetch_3d(&maps.k, 0, y + PC, zblk);
+        tma_prefetch_3d(&maps.g, 0, y + PC, zblk);
+        tma_prefetch_3d(&maps.v, 0, y + PC, zblk);
       }
       in_pend = (c & 1) + 1;
     };
@@ -564,9 +574,10 @@ __global__ void __launch_bounds__(PNT, 1)
       tma_prefetch_desc(&maps.g);
       if (nch > 0) issue_in(0);
     }
-    // raw beta logits of the next chunk, fetched a chunk ahead (group B, kb < 64)
+    // raw beta logits of the next chunk, fetched a chunk ahead (threads 128 .. 191)
     float b_raw = 0.0f;
-    if (!isA && kb < PC && t0 + kb < t1) b_raw = __bfloat162float(p.beta[(size_t)(t0 + kb) * p.s_beta + h]);
+    const int bt = kt - 128;
+    if (bt >= 0 && bt < PC && t0 + bt < t1) b_raw = __bfloat162float(p.beta[(size_t)(t0 + bt) * p.s_beta + h]);
 
     for (int c = 0; c < nch; ++c) {
       const int c0 = t0 + PC * c;
@@ -574,87 +585,56 @@ __global__ void __launch_bounds__(PNT, 1)
       const uint32_t par = (uint32_t)(c & 1);
       float* vec = vecs + (c % 3) * kVecFloats;
       bool ok = true;
-      float cl[4][8];
+      float cl[4][4];   // inclusive cumsums of this thread's 4 rows, 4 channels
 
-      // ---- K1 (A): gate -> log2 decay, cumsum over this thread's 4 rows; sums of squares
-      //              (B): beta
-      if (isA) {
-        ok = mbar_wait(bar(B_IN), par);
-        PSTAMP(ka == 0, c, 8);
-        float pss[8];
+      // ---- K1: gate -> log2 decay, cumsum over this thread's 4 rows; row sums of squares
+      if (mma_thread) ok = wait_phase(bar(B_IN), par);
+      if (bar_any(1, 512, !ok)) { failed = true; site = 20; break; }
+      if (tma_thread) in_pend = 0;
+      PSTAMP(kt == 0, c, 16);
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const int r = 4 * j + i;
-          const bool valid = r < L;
-          const uint32_t off = in_off(r, o);
-          const uint4 gv = lds128(sm + PS_ING, off);
-          const uint32_t gw[4] = {gv.x, gv.y, gv.z, gv.w};
+      for (int i = 0; i < 4; ++i) {
+        const int r = 4 * j + i;
+        const bool valid = r < L;
+        const uint32_t off = in8(r);
+        const uint2 gv = ld8b(PS_ING + off);
+        const uint32_t gw[2] = {gv.x, gv.y};
 #pragma unroll
-          for (int pq = 0; pq < 4; ++pq) {
-            const float2 gf = unpack_bf16x2(gw[pq]);
-            float a0 = lb2 * rcpf(1.0f + ex2f(fmaf(gf.x, sg, sgd[2 * pq])));
-            float a1 = lb2 * rcpf(1.0f + ex2f(fmaf(gf.y, sg, sgd[2 * pq + 1])));
-            a0 = valid ? a0 : 0.0f;
-            a1 = valid ? a1 : 0.0f;
-            cl[i][2 * pq] = (i ? cl[i - 1][2 * pq] : 0.0f) + a0;
-            cl[i][2 * pq + 1] = (i ? cl[i - 1][2 * pq + 1] : 0.0f) + a1;
-          }
-          const uint4 qv = lds128(sm + PS_INQ, off);
-          const uint4 kv = lds128(sm + PS_INK, off);
-          const uint32_t qw[4] = {qv.x, qv.y, qv.z, qv.w}, kw[4] = {kv.x, kv.y, kv.z, kv.w};
-          float sq = 0.0f, sk = 0.0f;
-#pragma unroll
-          for (int pq = 0; pq < 4; ++pq) {
-            const float2 qf = unpack_bf16x2(qw[pq]), kf = unpack_bf16x2(kw[pq]);
-            sq = fmaf(qf.x, qf.x, fmaf(qf.y, qf.y, sq));
-            sk = fmaf(kf.x, kf.x, fmaf(kf.y, kf.y, sk));
-          }
-          pss[i] = valid ? sq : 0.0f;
-          pss[4 + i] = valid ? sk : 0.0f;
+        for (int pq = 0; pq < 2; ++pq) {
+          const float2 gf = unpack_bf16x2(gw[pq]);
+          float a0 = lb2 * rcpf(1.0f + ex2f(fmaf(gf.x, sg, sgd[2 * pq])));
+          float a1 = lb2 * rcpf(1.0f + ex2f(fmaf(gf.y, sg, sgd[2 * pq + 1])));
+          a0 = valid ? a0 : 0.0f;
+          a1 = valid ? a1 : 0.0f;
+          cl[i][2 * pq] = (i ? cl[i - 1][2 * pq] : 0.0f) + a0;
+          cl[i][2 * pq + 1] = (i ? cl[i - 1][2 * pq + 1] : 0.0f) + a1;
         }
-        // quad totals of the cumsum -> GT[j][channel]
-        *reinterpret_cast<float4*>(GT + j * 128 + 8 * o) =
-            make_float4(cl[3][0], cl[3][1], cl[3][2], cl[3][3]);
-        *reinterpret_cast<float4*>(GT + j * 128 + 8 * o + 4) =
-            make_float4(cl[3][4], cl[3][5], cl[3][6], cl[3][7]);
-        // reduce the 8 partial sums over the 16 octets of the half-warp (reduce-scatter)
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const bool up = (lane & 8) != 0;
-          const float send = up ? pss[i] : pss[i + 4];
-          const float keep = up ? pss[i + 4] : pss[i];
-          pss[i] = keep + __shfl_xor_sync(0xffffffffu, send, 8);
-        }
-#pragma unroll
-        for (int i = 0; i < 2; ++i) {
-          const bool up = (lane & 4) != 0;
-          const float send = up ? pss[i] : pss[i + 2];
-          const float keep = up ? pss[i + 2] : pss[i];
-          pss[i] = keep + __shfl_xor_sync(0xffffffffu, send, 4);
-        }
-        {
-          const bool up = (lane & 2) != 0;
-          const float send = up ? pss[0] : pss[1];
-          const float keep = up ? pss[1] : pss[0];
-          pss[0] = keep + __shfl_xor_sync(0xffffffffu, send, 2);
-        }
-        pss[0] += __shfl_xor_sync(0xffffffffu, pss[0], 1);
-        if ((lane & 1) == 0) {
-          const int k = ((lane >> 3) & 1) * 4 + ((lane >> 2) & 1) * 2 + ((lane >> 1) & 1);
-          SS[(k >> 2) * 64 + 4 * j + (k & 3)] = pss[0];
-        }
-      } else if (kb < PC) {
-        BETA[kb] = (kb < L) ? sigm(b_raw) : 0.0f;
-        b_raw = 0.0f;
-        if (c0 + PC + kb < t1) b_raw = __bfloat162float(p.beta[(size_t)(c0 + PC + kb) * p.s_beta + h]);
+        const uint2 qv = ld8b(PS_INQ + off), kv = ld8b(PS_INK + off);
+        const float2 q0 = unpack_bf16x2(qv.x), q1 = unpack_bf16x2(qv.y);
+        const float2 k0 = unpack_bf16x2(kv.x), k1 = unpack_bf16x2(kv.y);
+        const float sq = fmaf(q0.x, q0.x, fmaf(q0.y, q0.y, fmaf(q1.x, q1.x, q1.y * q1.y)));
+        const float sk = fmaf(k0.x, k0.x, fmaf(k0.y, k0.y, fmaf(k1.x, k1.x, k1.y * k1.y)));
+        // the row's two sums over the 32 channel quads of the warp: lanes with bit 4 clear
+        // end with q's, lanes with it set with k's
+        const bool up = (lane & 16) != 0;
+        float v = (up ? sk : sq) + __shfl_xor_sync(0xffffffffu, up ? sq : sk, 16);
+        v += __shfl_xor_sync(0xffffffffu, v, 8);
+        v += __shfl_xor_sync(0xffffffffu, v, 4);
+        v += __shfl_xor_sync(0xffffffffu, v, 2);
+        v += __shfl_xor_sync(0xffffffffu, v, 1);
+        if ((lane & 15) == 0) SS[(up ? 64 : 0) + r] = valid ? v : 0.0f;
       }
-      if (bar_any(1, 384, !ok)) { failed = true; site = 20; break; }
-      if (tma_thread) in_pend = 0;   // group A saw this chunk's inputs land
+      // quad totals of the cumsum -> GT[j][channel]
+      *reinterpret_cast<float4*>(GT + j * 128 + 4 * o4) =
+          make_float4(cl[3][0], cl[3][1], cl[3][2], cl[3][3]);
+      group_sync(1, 512);
+      PSTAMP(kt == 0, c, 17);
 
-      // ---- K2 (B): anchors and factors per key channel; row norms and scales
-      if (!isA) {
+      // ---- K2 (threads < 128): anchors and factors per key channel; row norms and scales;
+      //      (threads 128 .. 191): beta
+      if (kt < 128) {
         {
-          const int d = kb;
+          const int d = kt;
           float P[16];
           float run = 0.0f;
 #pragma unroll
@@ -674,55 +654,61 @@ __global__ void __launch_bounds__(PNT, 1)
           vec[d] = ex2f(g63);                  // decay of the state
         }
         {
-          const int r = kb & 63;
-          const float ss = SS[kb];
+          const int r = kt & 63;
+          const float ss = SS[kt];
           // ss < 2^(e+1) -> |row| < 2^ceil((e+1)/2): rows enter the operands times 2^-sh
           const int e = ((__float_as_int(ss) >> 23) & 255) - 127;
           const int sh = max(-60, min(60, (e + 2) >> 1));
           const float inv = (r < L) ? rsqrtf(ss + kL2Eps) * __int_as_float((127 + sh) << 23) : 0.0f;
-          if (kb < 64)
+          if (kt < 64)
             vec[128 + r] = p.scale * inv;
           else
             vec[192 + r] = inv;
           const uint32_t bb = (uint32_t)(127 - sh) << 7;   // bf16 bits of 2^-sh
-          RSC[kb] = bb | (bb << 16);
+          RSC[kt] = bb | (bb << 16);
         }
+      } else if (bt < PC) {
+        BETA[bt] = (bt < L) ? sigm(b_raw) : 0.0f;
+        b_raw = 0.0f;
+        if (c0 + PC + bt < t1) b_raw = __bfloat162float(p.beta[(size_t)(c0 + PC + bt) * p.s_beta + h]);
       }
-      named_barrier_sync(1, 384);
-      PSTAMP(ka == 0, c, 9);
+      group_sync(1, 512);
+      PSTAMP(kt == 0, c, 18);
 
-      // ---- K3 (A): operand tiles: [Kr; Qr], [Kc; Kc2] (own), Kg, Qg, Ke (stage)
-      if (isA) {
-        float mE[8], fa[8], fb[8], fc[8], fq[8];
+      // ---- K3: operand tiles [Kr; Qr], [Kc; Kc2] (own), Kg, Qg (stage)
+      {
+        float mE[4], fa[4], fb[4], fc[4], fq[4];
         {
-          const float4 m_a = ld4(GT + j * 128 + 8 * o), m_b = ld4(GT + j * 128 + 8 * o + 4);
-          mE[0] = m_a.x; mE[1] = m_a.y; mE[2] = m_a.z; mE[3] = m_a.w;
-          mE[4] = m_b.x; mE[5] = m_b.y; mE[6] = m_b.z; mE[7] = m_b.w;
-          const int ia = bsel ? 4 : 0, ib = bsel ? 2 : 1, ic = 2, iq = bsel ? 5 : 3;
-#pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            fa[e] = FAC[ia * 128 + 8 * o + e];
-            fb[e] = FAC[ib * 128 + 8 * o + e];
-            fc[e] = FAC[ic * 128 + 8 * o + e];
-            fq[e] = FAC[iq * 128 + 8 * o + e];
-          }
+          auto ld4f = [&](const float* src, float (&dst)[4]) {
+            const float4 a = ld4(src);
+            dst[0] = a.x; dst[1] = a.y; dst[2] = a.z; dst[3] = a.w;
+          };
+          ld4f(GT + j * 128 + 4 * o4, mE);
+          ld4f(FAC + (bsel ? 4 : 0) * 128 + 4 * o4, fa);
+          ld4f(FAC + (bsel ? 2 : 1) * 128 + 4 * o4, fb);
+          ld4f(FAC + 2 * 128 + 4 * o4, fc);
+          ld4f(FAC + (bsel ? 5 : 3) * 128 + 4 * o4, fq);
         }
+        PSTAMP(kt == 0, c, 13);
         // the chain has finished reading [Kg; Qg] of the previous chunk
-        if (c > 0) ok = mbar_wait(bar(B_FREEA), (uint32_t)((c - 1) & 1)) && ok;
-        uint32_t ke[4][4];
+        if (c > 0) {
+          if (mma_thread) ok = wait_phase(bar(B_FREEA), (uint32_t)((c - 1) & 1));
+          if (bar_any(1, 512, !ok)) { failed = true; site = 21; break; }
+        }
+        PSTAMP(kt == 0, c, 19);
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
           const int r = 4 * j + i;
           const bool valid = r < L;
-          const uint32_t off = in_off(r, o);
-          uint4 qv = lds128(sm + PS_INQ, off), kv = lds128(sm + PS_INK, off);
-          if (!valid) qv = kv = make_uint4(0, 0, 0, 0);
+          const uint32_t off = in8(r);
+          uint2 qv = ld8b(PS_INQ + off), kv = ld8b(PS_INK + off);
+          if (!valid) qv = kv = make_uint2(0, 0);
           const uint32_t rq = RSC[r], rk = RSC[64 + r];
-          const uint32_t q2[4] = {bmul2(qv.x, rq), bmul2(qv.y, rq), bmul2(qv.z, rq), bmul2(qv.w, rq)};
-          const uint32_t k2[4] = {bmul2(kv.x, rk), bmul2(kv.y, rk), bmul2(kv.z, rk), bmul2(kv.w, rk)};
-          uint32_t kr[4], qr[4], kc[4], kc2[4], kg[4], qg[4];
+          const uint32_t q2[2] = {bmul2(qv.x, rq), bmul2(qv.y, rq)};
+          const uint32_t k2[2] = {bmul2(kv.x, rk), bmul2(kv.y, rk)};
+          uint32_t kr[2], qr[2], kc[2], kc2[2], kg[2], qg[2];
 #pragma unroll
-          for (int pq = 0; pq < 4; ++pq) {
+          for (int pq = 0; pq < 2; ++pq) {
             const int e0 = 2 * pq, e1 = 2 * pq + 1;
             const float x0 = cl[i][e0] - mE[e0], x1 = cl[i][e1] - mE[e1];
             const float E0 = ex2f(x0), E1 = ex2f(x1);
@@ -733,131 +719,135 @@ __global__ void __launch_bounds__(PNT, 1)
             kc[pq] = bmul2(k2[pq], Ei2);
             uint32_t gq;
             if (bsel == 0) {
-              const float u0 = Ei0 * fa[e0], u1 = Ei1 * fa[e1];   // 2^(G31 - G)
-              kc2[pq] = bmul2(k2[pq], pack_bf16x2(u0 * fc[e0], u1 * fc[e1]));
-              ke[i][pq] = bmul2(k2[pq], pack_bf16x2(u0 * fb[e0], u1 * fb[e1]));
+              kc2[pq] = bmul2(k2[pq], pack_bf16x2((Ei0 * fa[e0]) * fc[e0], (Ei1 * fa[e1]) * fc[e1]));
               gq = pack_bf16x2(E0 * fq[e0], E1 * fq[e1]);
             } else {
-              ke[i][pq] = bmul2(k2[pq], pack_bf16x2(Ei0 * fa[e0], Ei1 * fa[e1]));
               gq = pack_bf16x2((E0 * fc[e0]) * fq[e0], (E1 * fc[e1]) * fq[e1]);
               kc2[pq] = 0u;
             }
             qg[pq] = bmul2(q2[pq], gq);
             kg[pq] = bmul2(k2[pq], gq);
           }
-          st_u128(sm, PS_RKQ + kmajor_off(r, 8 * o, 128), make_uint4(kr[0], kr[1], kr[2], kr[3]));
-          st_u128(sm, PS_RKQ + kmajor_off(64 + r, 8 * o, 128),
-                  make_uint4(qr[0], qr[1], qr[2], qr[3]));
-          st_u128(sm, PS_CKC + kmajor_off(r, 8 * o, 96), make_uint4(kc[0], kc[1], kc[2], kc[3]));
-          if (bsel == 0)
-            st_u128(sm, PS_CKC + kmajor_off(64 + r, 8 * o, 96),
-                    make_uint4(kc2[0], kc2[1], kc2[2], kc2[3]));
-          st_u128(sm, PS_WQ + kmajor_off(r, 8 * o, 128), make_uint4(kg[0], kg[1], kg[2], kg[3]));
-          st_u128(sm, PS_WQ + kmajor_off(64 + r, 8 * o, 128),
-                  make_uint4(qg[0], qg[1], qg[2], qg[3]));
+          st8b(PS_RKQ + kmajor_off(r, 4 * o4, 128), kr[0], kr[1]);
+          st8b(PS_RKQ + kmajor_off(64 + r, 4 * o4, 128), qr[0], qr[1]);
+          st8b(PS_CKC + kmajor_off(r, 4 * o4, 96), kc[0], kc[1]);
+          if (bsel == 0) st8b(PS_CKC + kmajor_off(64 + r, 4 * o4, 96), kc2[0], kc2[1]);
+          st8b(PS_WQ + kmajor_off(r, 4 * o4, 128), kg[0], kg[1]);
+          st8b(PS_WQ + kmajor_off(64 + r, 4 * o4, 128), qg[0], qg[1]);
         }
-        // the chain has finished reading QK and Ke of the previous chunk
-        if (c > 0) ok = mbar_wait(bar(B_FREEB), (uint32_t)((c - 1) & 1)) && ok;
+        PSTAMP(kt == 0, c, 20);
+        fence_proxy_async();
+        group_sync(1, 512);
+        PSTAMP(kt == 0, c, 21);
+
+        // ---- K4: [A | QK] on the tensor cores; the next chunk's inputs (the input tiles are
+        //      free); meanwhile Ke = Kc 2^(G_last - anchor) (stage), read from the Kc tile the
+        //      MMA is reading too
+        if (mma_thread) {
+          tc_fence_after();
 #pragma unroll
-        for (int i = 0; i < 4; ++i)
-          st_u128(sm, PS_KE + mnmajor_off(8 * o, 4 * j + i, 8192),
-                  make_uint4(ke[i][0], ke[i][1], ke[i][2], ke[i][3]));
+          for (int ks = 0; ks < 8; ++ks)
+            mma_bf16(tmem + TM_D, kdesc(sb + PS_RKQ, 128, ks), kdesc(sb + PS_CKC, 96, ks), ID_D96,
+                     ks > 0);
+          mma_commit(bar(B_KMMA));
+          PSTAMP(true, c, 31);
+        }
+        kmma_pend = (int)par + 1;
+        if (tma_thread && c + 1 < nch) issue_in(c + 1);
+        PSTAMP(tma_thread, c, 30);
+        if (c > 0) {   // the chain has finished reading QK and Ke of the previous chunk
+          if (free_thread) ok = wait_phase(bar(B_FREEB), (uint32_t)((c - 1) & 1));
+          if (bar_any(1, 512, !ok)) { failed = true; site = 25; break; }
+        }
+        PSTAMP(kt == 0, c, 1);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int r = 4 * j + i;
+          const uint2 kcv = ld8b(PS_CKC + kmajor_off(r, 4 * o4, 96));
+          const float2 a = unpack_bf16x2(kcv.x), b = unpack_bf16x2(kcv.y);
+          uint32_t w0, w1;
+          if (bsel == 0) {   // 2^(G31 - G) then 2^(G63 - G31)
+            w0 = pack_bf16x2((a.x * fa[0]) * fb[0], (a.y * fa[1]) * fb[1]);
+            w1 = pack_bf16x2((b.x * fa[2]) * fb[2], (b.y * fa[3]) * fb[3]);
+          } else {           // 2^(G63 - G47)
+            w0 = pack_bf16x2(a.x * fa[0], a.y * fa[1]);
+            w1 = pack_bf16x2(b.x * fa[2], b.y * fa[3]);
+          }
+          st8b(PS_KE + mnmajor_off(4 * o4, r, 8192), w0, w1);
+        }
         fence_proxy_async();
       }
-      PSTAMP(ka == 0, c, 10);
-      if (bar_any(1, 384, !ok)) { failed = true; site = 21; break; }
-
-      // ---- K4: [A | QK] on the tensor cores; the next chunk's inputs (the tiles are free)
-      if (mma_thread) {
-        tc_fence_after();
-#pragma unroll
-        for (int ks = 0; ks < 8; ++ks)
-          mma_bf16(tmem + TM_D, kdesc(sb + PS_RKQ, 128, ks), kdesc(sb + PS_CKC, 96, ks), ID_D96,
-                   ks > 0);
-        mma_commit(bar(B_KMMA));
-      }
-      kmma_pend = (int)par + 1;
-      if (tma_thread && c + 1 < nch) issue_in(c + 1);
-      ok = mbar_wait(bar(B_KMMA), par);
-      if (ok) kmma_pend = 0;
-      PSTAMP(ka == 0, c, 11);
+      if (mma_thread) ok = wait_phase(bar(B_KMMA), par);
+      if (bar_any(1, 512, !ok)) { failed = true; site = 24; break; }
+      kmma_pend = 0;
+      PSTAMP(kt == 0, c, 22);
       tc_fence_after();
 
-      // ---- K5 (A): A rows -> N (fp32), QK rows -> bf16 (stage); (B): T upper blocks -> 0
-      if (isA) {
-        const int q4 = wa & 3, cs = wa >> 2;
+      // ---- K5: A rows -> N (fp32), QK rows -> bf16, MN-major (stage).  Warp w reads TMEM
+      //      quadrant w % 4, a 16-column quarter of the row's 64 columns.
+      {
+        const int q4 = warp & 3, cq = (warp - 4) >> 2;
         const uint32_t lbase = (uint32_t)(32 * q4) << 16;
-        const int m = 32 * q4 + lane;
+        const int rr = 32 * (q4 & 1) + lane;          // row (of A or of QK)
+        const bool hi = (q4 & 1) != 0;                // rows 32-63
+        const bool zero_part = !hi && cq >= 2;        // rows < 32, tokens >= 32
         const float* ik = vec + 192;
+        uint32_t a[16];
+        if (!zero_part) {
+          // columns 16 cq .. 16 cq + 15 of the row; rows 32-63 take tokens 0-31 from D[:, 64:96]
+          tmem_ld16(tmem + lbase + TM_D + (hi && cq < 2 ? 64 + 16 * cq : 16 * cq), a);
+          tmem_wait_ld();
+        } else {
+#pragma unroll
+          for (int e = 0; e < 16; ++e) a[e] = 0u;
+        }
+        PSTAMP(kt == 0, c, 23);
         if (q4 < 2) {
-          const int r = m;
-          float* nrow = Nm + r * NS + 32 * cs;
-          if (q4 == 0 && cs == 1) {
+          const int r = rr;
+          float* nrow = Nm + r * NS + 16 * cq;
+          const float br = BETA[r] * ik[r];
 #pragma unroll
-            for (int s4 = 0; s4 < 8; ++s4)
-              *reinterpret_cast<float4*>(nrow + 4 * s4) = make_float4(0.f, 0.f, 0.f, 0.f);
-          } else {
-            uint32_t a[32];
-            tmem_ld32(tmem + lbase + TM_D + (cs == 1 ? 32 : (q4 == 0 ? 0 : 64)), a);
-            tmem_wait_ld();
-            const float br = BETA[r] * ik[r];
+          for (int s4 = 0; s4 < 4; ++s4) {
+            const float4 kk = ld4(ik + 16 * cq + 4 * s4);
+            const float kv4[4] = {kk.x, kk.y, kk.z, kk.w};
+            float w[4];
 #pragma unroll
-            for (int s4 = 0; s4 < 8; ++s4) {
-              const float4 kk = ld4(ik + 32 * cs + 4 * s4);
-              const float kv4[4] = {kk.x, kk.y, kk.z, kk.w};
-              float w[4];
-#pragma unroll
-              for (int e = 0; e < 4; ++e) {
-                const int s = 32 * cs + 4 * s4 + e;
-                w[e] = (s < r) ? br * kv4[e] * __uint_as_float(a[4 * s4 + e]) : 0.0f;
-              }
-              *reinterpret_cast<float4*>(nrow + 4 * s4) = make_float4(w[0], w[1], w[2], w[3]);
+            for (int e = 0; e < 4; ++e) {
+              const int s2 = 16 * cq + 4 * s4 + e;
+              w[e] = (s2 < r) ? br * kv4[e] * __uint_as_float(a[4 * s4 + e]) : 0.0f;
             }
+            *reinterpret_cast<float4*>(nrow + 4 * s4) = make_float4(w[0], w[1], w[2], w[3]);
           }
         } else {
-          const int r = m - 64;
-          if (q4 == 2 && cs == 1) {
+          const int r = rr;
+          // MN-major: element (r, s) at (s/8) * 1024 + (s%8) * 128 + chunk (r/8 ^ s%8)
+          const uint32_t base = (uint32_t)(cq * 2048 + (r & 7) * 2);
 #pragma unroll
-            for (int c8 = 0; c8 < 4; ++c8)
-              st_u128(sm, PS_QK + kmajor_off(r, 32 + 8 * c8, 64), make_uint4(0, 0, 0, 0));
-          } else {
-            uint32_t a[32];
-            tmem_ld32(tmem + lbase + TM_D + (cs == 1 ? 32 : (q4 == 2 ? 0 : 64)), a);
-            tmem_wait_ld();
-#pragma unroll
-            for (int c8 = 0; c8 < 4; ++c8) {
-              uint32_t w[4];
-#pragma unroll
-              for (int e = 0; e < 4; ++e) {
-                const int s = 32 * cs + 8 * c8 + 2 * e;
-                w[e] = pack_bf16x2(s <= r ? __uint_as_float(a[8 * c8 + 2 * e]) : 0.0f,
-                                   s + 1 <= r ? __uint_as_float(a[8 * c8 + 2 * e + 1]) : 0.0f);
-              }
-              st_u128(sm, PS_QK + kmajor_off(r, 32 * cs + 8 * c8, 64),
-                      make_uint4(w[0], w[1], w[2], w[3]));
-            }
+          for (int e = 0; e < 16; ++e) {
+            const int s2 = 16 * cq + e;
+            const __nv_bfloat16 val = __float2bfloat16_rn(s2 <= r ? __uint_as_float(a[e]) : 0.0f);
+            *reinterpret_cast<__nv_bfloat16*>(
+                sm + PS_QK + base + (e >> 3) * 1024 + (e & 7) * 128 + ((((r >> 3) ^ e) & 7) << 4)) = val;
           }
         }
-      } else {
-        // T above the diagonal 16 x 16 blocks is zero
-        for (int idx = kb; idx < 6 * 64; idx += 128) {
+      }
+      tc_fence_before();
+      group_sync(1, 512);
+      PSTAMP(kt == 0, c, 24);
+
+      // ---- K6 (threads < 128): T = (I + N)^-1: 16 x 16 diagonal blocks by substitution
+      //      (fp32), then the off-diagonal blocks as tf32 warp products, 16 -> 32 -> 64
+      if (kt < 128) {
+        const int wb = kt >> 5;
+        for (int idx = kt; idx < 6 * 64; idx += 128) {   // T above the diagonal blocks is zero
           const int b = idx >> 6, e = idx & 63;
           const int bi = (b < 3) ? 0 : (b < 5 ? 1 : 2);
           const int bj = (b < 3) ? b + 1 : (b < 5 ? b - 1 : 3);
           *reinterpret_cast<float4*>(Tm + (bi * 16 + (e >> 2)) * NS + bj * 16 + 4 * (e & 3)) =
               make_float4(0.f, 0.f, 0.f, 0.f);
         }
-      }
-      tc_fence_before();
-      if (bar_any(1, 384, !ok)) { failed = true; site = 22; break; }
-      PSTAMP(ka == 0, c, 12);
-
-      // ---- K6 (B): T = (I + N)^-1: 16 x 16 diagonal blocks by substitution (fp32), then
-      //               the off-diagonal blocks as tf32 warp products, 16 -> 32 -> 64
-      if (!isA) {
-        const int wb = kb >> 5;
         if (wb < 2) {
-          const int ob = (kb >> 4) * 16, jj = kb & 15;
+          const int ob = (kt >> 4) * 16, jj = kt & 15;
           float x[16];
 #pragma unroll
           for (int i = 0; i < 16; ++i) x[i] = (i == jj) ? 1.0f : 0.0f;
@@ -869,48 +859,54 @@ __global__ void __launch_bounds__(PNT, 1)
 #pragma unroll
           for (int i = 0; i < 16; ++i) Tm[(ob + i) * NS + ob + jj] = x[i];
         }
-        named_barrier_sync(3, 128);
+        PSTAMP(kt == 0, c, 14);
+        group_sync(3, 128);
         if (wb < 2) {   // pair (1,0) on warp 0 of the group, (3,2) on warp 1
           const int ro = (2 * wb + 1) * 16, co = 2 * wb * 16;
           float* Yw = Y + wb * 16 * NS;
-          warp_gemm_16x16<16>(Nm + ro * NS + co, Tm + co * NS + co, Yw, 1.0f, lane);
+          wgemm16(Nm + ro * NS + co, Tm + co * NS + co, Yw, 1.0f, lane);
           __syncwarp();
-          warp_gemm_16x16<16>(Tm + ro * NS + ro, Yw, Tm + ro * NS + co, -1.0f, lane);
+          wgemm16(Tm + ro * NS + ro, Yw, Tm + ro * NS + co, -1.0f, lane);
         }
-        named_barrier_sync(3, 128);
+        group_sync(3, 128);
+        PSTAMP(kt == 0, c, 15);
         const int mi = wb >> 1, ni = wb & 1;   // Y2 = N[32:64, 0:32] T[0:32, 0:32]
-        warp_gemm_16x16<32>(Nm + (32 + 16 * mi) * NS, Tm + 16 * ni, Y + 16 * mi * NS + 16 * ni,
-                            1.0f, lane);
-        named_barrier_sync(3, 128);            // T[32:64, 0:32] = -T[32:64, 32:64] Y2
-        warp_gemm_16x16<32>(Tm + (32 + 16 * mi) * NS + 32, Y + 16 * ni,
-                            Tm + (32 + 16 * mi) * NS + 16 * ni, -1.0f, lane);
+        wgemm32(Nm + (32 + 16 * mi) * NS, Tm + 16 * ni, Y + 16 * mi * NS + 16 * ni, 1.0f, lane);
+        group_sync(3, 128);                    // T[32:64, 0:32] = -T[32:64, 32:64] Y2
+        PSTAMP(kt == 0, c, 9);
+        wgemm32(Tm + (32 + 16 * mi) * NS + 32, Y + 16 * ni, Tm + (32 + 16 * mi) * NS + 16 * ni,
+                -1.0f, lane);
       }
-      named_barrier_sync(1, 384);
-      PSTAMP(ka == 0, c, 13);
+      group_sync(1, 512);
+      PSTAMP(kt == 0, c, 25);
 
-      // ---- K7 (A): T diag(b) and T -> bf16 (stage); (B): -b inv_k
-      if (isA) {
-#pragma unroll
-        for (int h2 = 0; h2 < 2; ++h2) {
-          const int item = ka + 256 * h2;
-          const int r = item >> 3, c8 = item & 7;
-          const float4 ta = ld4(Tm + r * NS + 8 * c8), tb = ld4(Tm + r * NS + 8 * c8 + 4);
-          const float4 ba = ld4(BETA + 8 * c8), bb = ld4(BETA + 8 * c8 + 4);
-          const uint32_t off = kmajor_off(r, 8 * c8, 64);
-          st_u128(sm, PS_TB + off,
-                  make_uint4(pack_bf16x2(ta.x * ba.x, ta.y * ba.y), pack_bf16x2(ta.z * ba.z, ta.w * ba.w),
-                             pack_bf16x2(tb.x * bb.x, tb.y * bb.y), pack_bf16x2(tb.z * bb.z, tb.w * bb.w)));
-          st_u128(sm, PS_TT + off,
-                  make_uint4(pack_bf16x2(ta.x, ta.y), pack_bf16x2(ta.z, ta.w),
-                             pack_bf16x2(tb.x, tb.y), pack_bf16x2(tb.z, tb.w)));
-        }
-        fence_proxy_async();
-      } else if (kb < PC) {
-        vec[256 + kb] = -BETA[kb] * vec[192 + kb];
+      // ---- K7: T diag(b) and T -> bf16 (stage); -b inv_k
+      PSTAMP(kt == 0, c, 11);
+      if (c > 0) {   // the chain has finished reading T diag(b) and T of the previous chunk
+        if (mma_thread) ok = wait_phase(bar(B_FREEC), (uint32_t)((c - 1) & 1));
+        PSTAMP(kt == 0, c, 12);
+        if (bar_any(1, 512, !ok)) { failed = true; site = 26; break; }
       }
-      named_barrier_sync(1, 384);
+      PSTAMP(kt == 0, c, 26);
+      {
+        const int r = kt & 63, c8 = kt >> 6;   // row r, columns 8 c8 .. 8 c8 + 7
+        const float4 ta = ld4(Tm + r * NS + 8 * c8), tb = ld4(Tm + r * NS + 8 * c8 + 4);
+        const float4 ba = ld4(BETA + 8 * c8), bb = ld4(BETA + 8 * c8 + 4);
+        const uint32_t off = kmajor_off(r, 8 * c8, 64);
+        st_u128(sm, PS_TB + off,
+                make_uint4(pack_bf16x2(ta.x * ba.x, ta.y * ba.y), pack_bf16x2(ta.z * ba.z, ta.w * ba.w),
+                           pack_bf16x2(tb.x * bb.x, tb.y * bb.y), pack_bf16x2(tb.z * bb.z, tb.w * bb.w)));
+        st_u128(sm, PS_TT + off,
+                make_uint4(pack_bf16x2(ta.x, ta.y), pack_bf16x2(ta.z, ta.w),
+                           pack_bf16x2(tb.x, tb.y), pack_bf16x2(tb.z, tb.w)));
+        if (kt < PC) vec[256 + kt] = -BETA[kt] * vec[192 + kt];
+      }
+      PSTAMP(kt == 0, c, 27);
+      fence_proxy_async();
+      PSTAMP(kt == 0, c, 28);
+      group_sync(1, 512);
       if (mma_thread) mbar_arrive(bar(B_FULL));   // the stage of chunk c is complete
-      PSTAMP(ka == 0, c, 14);
+      PSTAMP(kt == 0, c, 29);
     }
     if (failed) {
       if (kt == 0) record_error(p.status, KDA_ERR_DEVICE_TIMEOUT, site);
@@ -928,16 +924,16 @@ typedef CUresult (*EncodeTiledFnP)(CUtensorMap*, CUtensorMapDataType, cuuint32_t
                                    const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
                                    CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 
-// [T rows][H*128 cols] bf16 view with a row stride of `stride` elements
+// [2H blocks][T rows][64 cols] bf16 view of a [T][H*128] tensor with a row stride of
+// `stride` elements: dims {64, T, 2H}, strides {stride * 2, 128} bytes; box {64, 64, 2}
 bool make_pipe_map(EncodeTiledFnP enc, CUtensorMap* m, const void* base, int64_t T, int H,
-                   int64_t stride, int box_cols, bool swizzle) {
-  cuuint64_t dims[2] = {(cuuint64_t)H * PD, (cuuint64_t)(T > 0 ? T : 1)};
-  cuuint64_t strides[1] = {(cuuint64_t)stride * 2};
-  cuuint32_t box[2] = {(cuuint32_t)box_cols, (cuuint32_t)PC};
-  cuuint32_t es[2] = {1, 1};
-  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
-             es, CU_TENSOR_MAP_INTERLEAVE_NONE,
-             swizzle ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                   int64_t stride) {
+  cuuint64_t dims[3] = {64, (cuuint64_t)(T > 0 ? T : 1), (cuuint64_t)(2 * H)};
+  cuuint64_t strides[2] = {(cuuint64_t)stride * 2, 128};
+  cuuint32_t box[3] = {64, (cuuint32_t)PC, 2};
+  cuuint32_t es[3] = {1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
+             es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -966,12 +962,10 @@ cudaError_t launch_pipe(const Params& p, cudaStream_t stream) {
   const void* kb = p.k ? (const void*)p.k : (const void*)p.dt_bias;
   const void* gb = p.g ? (const void*)p.g : (const void*)p.dt_bias;
   const void* vb = p.v ? (const void*)p.v : (const void*)p.dt_bias;
-  const void* ob = p.out ? (const void*)p.out : (const void*)p.dt_bias;
-  if (!make_pipe_map(enc, &maps.q, qb, p.total_tokens, p.heads, p.s_q, 64, true) ||
-      !make_pipe_map(enc, &maps.k, kb, p.total_tokens, p.heads, p.s_k, 64, true) ||
-      !make_pipe_map(enc, &maps.g, gb, p.total_tokens, p.heads, p.s_g, 64, true) ||
-      !make_pipe_map(enc, &maps.v, vb, p.total_tokens, p.heads, p.s_v, 64, true) ||
-      !make_pipe_map(enc, &maps.out, ob, p.total_tokens, p.heads, (int64_t)p.heads * PD, PD, false))
+  if (!make_pipe_map(enc, &maps.q, qb, p.total_tokens, p.heads, p.s_q) ||
+      !make_pipe_map(enc, &maps.k, kb, p.total_tokens, p.heads, p.s_k) ||
+      !make_pipe_map(enc, &maps.g, gb, p.total_tokens, p.heads, p.s_g) ||
+      !make_pipe_map(enc, &maps.v, vb, p.total_tokens, p.heads, p.s_v))
     return cudaErrorInvalidValue;
   kda_pipe_kernel<<<(unsigned)blocks, PNT, PIPE_SMEM, stream>>>(p, maps);
   return cudaGetLastError();
