@@ -258,12 +258,17 @@ def run_reference(args, w):
 
 # phase stamps of the pipelined kernel: 32 slots per chunk (see kda_pipe_kernel.cu)
 # chain stamp slots (CTA 0, thread 0) and the k-side ones (thread 128); 32 slots per chunk
-CHAIN_SLOTS = {0: "stage full", 2: "S_b stored", 3: "G1a issued", 4: "G1a done", 5: "X_b stored",
-               6: "G1b done", 7: "U_b stored", 8: "G2 done", 10: "O stored"}
-KSIDE_SLOTS = {16: "inputs landed", 17: "gate and norms", 18: "factors", 19: "stage parts free",
-               20: "tile rows done", 21: "tiles fenced", 22: "A|QK MMA done",
-               23: "A/QK loaded", 24: "A/QK extracted", 25: "T inverse", 26: "T tiles free",
-               27: "T tiles stored", 28: "T tiles fenced", 29: "stage handed over"}
+CHAIN_SLOTS = {0: "stage full", 2: "S_b stored", 3: "G1a issued", 12: "S decayed",
+               26: "T operands stored", 4: "G1a done", 5: "X_b stored", 28: "G1b done (thread 0)",
+               27: "QK operand stored", 6: "chain group past G1b", 7: "U_b stored", 8: "G2 done",
+               10: "O stored"}
+CHAIN_ORDER = [0, 2, 3, 12, 26, 4, 5, 28, 27, 6, 7, 8, 10]
+KSIDE_SLOTS = {16: "inputs landed", 17: "gate and norms", 18: "factors", 13: "factor loads",
+               19: "stage parts free", 20: "tile rows done", 21: "tiles fenced",
+               22: "A|QK MMA done", 1: "Ke parts free", 23: "A loaded", 24: "N, Ke stored",
+               11: "T parts free", 14: "diagonal blocks", 15: "level 1", 9: "level 2a",
+               29: "stage handed over"}
+KSIDE_ORDER = [16, 17, 18, 13, 19, 20, 21, 22, 1, 23, 24, 11, 14, 15, 9, 29]
 
 
 def run_stamps(args):
@@ -297,24 +302,17 @@ def run_stamps(args):
         vals = [stamps[c][b] - (stamps[c - 1][a] if prev else stamps[c][a]) for c in inner]
         return statistics.median(vals) if vals else 0
 
-    ks = sorted(KSIDE_SLOTS)
+    ks, cs = KSIDE_ORDER, CHAIN_ORDER
     res = {"workload": w.name, "chunks_of_cta0": nch, "unit": "SM cycles (clock64), median",
            "chunk_period": med(29, 29, True),
            "kside": {f"{KSIDE_SLOTS[a]} -> {KSIDE_SLOTS[b]}": med(a, b) for a, b in zip(ks, ks[1:])},
            "kside_wait_for_inputs (handover c-1 -> inputs landed c)": med(29, 16, True),
            "kside_mma_issue (tiles fenced -> MMA issued)": med(21, 31),
            "kside_next_inputs_issued (tiles fenced -> issued)": med(21, 30),
-           "chain": {f"{CHAIN_SLOTS[a]} -> {CHAIN_SLOTS[b]}": med(a, b)
-                     for a, b in zip(sorted(CHAIN_SLOTS), sorted(CHAIN_SLOTS)[1:])},
+           "chain": {f"{CHAIN_SLOTS[a]} -> {CHAIN_SLOTS[b]}": med(a, b) for a, b in zip(cs, cs[1:])},
            "chain_wait_for_stage (O stored c-1 -> stage full c)": med(10, 0, True),
            "handover -> chain start": med(29, 0),
-           "chain G1a done (c-1) -> kside stage parts free (c)": med(4, 19, True),
-           "kside detail": {"K3 factor loads": med(18, 13), "K3 waits for [Kg; Qg]": med(13, 19),
-                            "K4 MMA issue": med(21, 31), "K4 wait for QK/Ke free": med(21, 1),
-                            "K4 Ke from Kc + MMA wait": med(1, 22),
-                            "K6 substitution": med(24, 14), "K6 level 1": med(14, 15),
-                            "K6 level 2a": med(15, 9), "K6 level 2b": med(9, 25),
-                            "K7 wait for the chain": med(11, 12)}}
+           "chain G1a done (c-1) -> kside stage parts free (c)": med(4, 19, True)}
     print(json.dumps(res, indent=1), flush=True)
 
 

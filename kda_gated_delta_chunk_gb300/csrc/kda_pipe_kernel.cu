@@ -5,11 +5,13 @@
 // decay-weighted Gram products and the UT inverse) and the state half (the
 // "chain").  The fused kernel of kda_tc_kernel.cuh runs the two halves one after
 // the other; here they run on different warps at the same time:
-//   warps 0-3   chain of chunk c: thread i <-> TMEM lane i <-> value channel i;
-//   warps 4-19  k-side of chunk c+1: gate, cumsum, norms, operand tiles, the A|QK
-//               extraction and the T -> bf16 conversion on all 16 warps; per-channel
-//               anchors and factors, row norms, beta and the UT inverse on warps 4-7;
-//               one thread each issues the k-side MMA and the input TMA.
+//   warps 0-3   chain of chunk c: thread i <-> TMEM lane i <-> value channel i; besides
+//               its own products it turns T into the bf16 operands of G1b and takes the
+//               QK rows out of the k-side's accumulator (both while its MMAs run);
+//   warps 4-19  k-side of chunk c+1: gate, cumsum, norms, operand tiles, the A
+//               extraction and Ke on all 16 warps; per-channel anchors and factors, row
+//               norms, beta and the UT inverse on warps 4-7; one thread each issues the
+//               k-side MMA and the input TMA.
 // The k-side hands each chunk over through one shared-memory stage guarded by
 // mbarriers (stage full: k-side -> chain; stage parts free: chain -> k-side).
 //
@@ -63,8 +65,7 @@ constexpr int PS_ING = 32768;         // g tile
 constexpr int PS_RKQ = 49152;         // [Kr; Qr] K-major 128 rows x 128 (until the A|QK MMA ends)
 constexpr int PS_CKC = 81920;         // [Kc; Kc2] K-major 96 rows x 128
 constexpr int PS_NM = PS_RKQ;         // then: N = diag(b inv_k) strict(A) diag(inv_k) [64][NS]
-constexpr int PS_TM = PS_NM + 64 * NS * 4;   //       T [64][NS]
-constexpr int PS_Y = PS_TM + 64 * NS * 4;    //       product scratch [32][NS]
+constexpr int PS_Y = PS_NM + 64 * NS * 4;    //       product scratch [32][NS]
 // the stage (chain operands of one chunk)
 constexpr int PS_WQ = 106496;         // [Kg; Qg] K-major 128 rows (tokens) x 128 (dk)
 constexpr int PS_V = 139264;          // v: two SW128 boxes [64 tok][64 dv]
@@ -72,20 +73,23 @@ constexpr int PS_TB = 155648;         // T diag(b) K-major 64 x 64
 constexpr int PS_TT = 163840;         // T K-major 64 x 64
 constexpr int PS_QK = 172032;         // [QK | Ke] MN-major, N = 192 in blocks of 64, 8 KB apart:
 constexpr int PS_KE = 180224;         //   QK (n = row r, k = token s; masked, raw), then Ke (n = dk)
+constexpr int PS_OST = PS_QK;         // the chain's O transpose scratch (1 KB per warp) once G2 has
+                                      //   read QK (the chain writes QK itself)
 // small things
-constexpr int PS_VEC = 196608;        // [3 by chunk % 3]: decay[128] iq[64] ik[64] nbik[64] fp32
-constexpr int kVecFloats = 320;
+constexpr int PS_VEC = 196608;        // [3 by chunk % 3]: decay[128] iq[64] ik[64] nbik[64] b[64] fp32
+constexpr int kVecFloats = 384;
 constexpr int PS_GT = PS_VEC + 3 * kVecFloats * 4;   // quad totals, then anchor offsets [16][128]
 constexpr int PS_FAC = PS_GT + 16 * 128 * 4;          // per-channel factors [6][128]
 constexpr int PS_SS = PS_FAC + 6 * 128 * 4;           // row sums of squares: q [64], k [64]
 constexpr int PS_RSC = PS_SS + 128 * 4;               // row power-of-two scales, bf16x2 [128]
-constexpr int PS_BETA = PS_RSC + 128 * 4;             // b [64]
-constexpr int PS_BAR = PS_BETA + 64 * 4;              // mbarriers
+constexpr int PS_BAR = PS_RSC + 128 * 4;              // mbarriers
 constexpr int PS_TSLOT = PS_BAR + 16 * 8;   // (10 mbarriers used)
 constexpr int PS_FLAGS = PS_TSLOT + 16;
-constexpr int PS_END = PS_FLAGS + 16;
+constexpr int PS_TM = PS_FLAGS + 16;      // T [64][NS] fp32
+constexpr int PS_END = PS_TM + 64 * NS * 4;
 constexpr int PIPE_SMEM = PS_END + 1024;
-static_assert(PS_Y + 32 * NS * 4 <= PS_WQ, "T scratch overlaps the stage");
+static_assert(PS_Y + 32 * NS * 4 <= PS_CKC, "N scratch overlaps the Kc tile (read until Ke)");
+static_assert(PS_TM % 16 == 0, "T rows are read as float4");
 static_assert(PS_CKC + 96 * 128 * 2 <= PS_WQ, "operands overlap the stage");
 static_assert(PS_KE + 16384 <= PS_VEC, "stage overlaps the vectors");
 static_assert(PS_WQ % 1024 == 0 && PS_V % 1024 == 0 && PS_TB % 1024 == 0 && PS_TT % 1024 == 0 &&
@@ -99,12 +103,13 @@ constexpr int B_IN = 0;      // q, k, g of the k-side's chunk landed (TMA tx)
 constexpr int B_V = 1;       // v of the chain's chunk landed (TMA tx)
 constexpr int B_FULL = 2;    // stage written by the k-side (1 arrival)
 constexpr int B_FREEA = 3;   // chain done with [Kg; Qg]
-constexpr int B_FREEB = 4;   // chain done with QK, Ke
+constexpr int B_FREEB = 4;   // chain done with Ke
 constexpr int B_KMMA = 5;    // k-side A|QK MMA done
 constexpr int B_G1A = 6;     // chain: [X^T | O^T] done
 constexpr int B_G1B = 7;     // chain: U^T done
 constexpr int B_G2 = 8;      // chain: O^T, S^T updates done
-constexpr int B_FREEC = 9;   // chain done with T diag(b), T
+constexpr int B_FREEC = 9;   // chain done with T (fp32) and T diag(b), T (bf16)
+constexpr int B_DFREE = 10;  // chain done with the QK rows of the k-side's D (TMEM)
 
 // ---- tensor memory columns (fp32 unless noted; lane = value channel, or row for D)
 constexpr uint32_t TM_XU = 0;     // X^T, then U^T   64 cols (col = token)
@@ -245,6 +250,7 @@ __global__ void __launch_bounds__(PNT, 1)
     mbar_init(bar(B_G1B), 1);
     mbar_init(bar(B_G2), 1);
     mbar_init(bar(B_FREEC), 1);
+    mbar_init(bar(B_DFREE), 1);
     mbar_fence_init();
   }
   if (warp == 0) {
@@ -273,6 +279,28 @@ __global__ void __launch_bounds__(PNT, 1)
         pend |= 1;
       }
     }
+    // C1a: S_b = bf16(S^T), 64 key columns at a time: the operand of the next chunk's G1a,
+    // made as soon as the state is final (before the first chunk, then after each G2)
+    auto convert_sb = [&]() {
+#pragma unroll 1
+      for (int hh = 0; hh < 2; ++hh) {
+        uint32_t x[32], y[32], pk[16];
+        tmem_ld32(tmem + lb + TM_S + hh * 64, x);
+        tmem_ld32(tmem + lb + TM_S + hh * 64 + 32, y);
+        tmem_wait_ld();
+#pragma unroll
+        for (int j2 = 0; j2 < 16; ++j2)
+          pk[j2] = pack_bf16x2(__uint_as_float(x[2 * j2]), __uint_as_float(x[2 * j2 + 1]));
+        tmem_st16(tmem + lb + TM_SB + hh * 32, pk);
+#pragma unroll
+        for (int j2 = 0; j2 < 16; ++j2)
+          pk[j2] = pack_bf16x2(__uint_as_float(y[2 * j2]), __uint_as_float(y[2 * j2 + 1]));
+        tmem_st16(tmem + lb + TM_SB + hh * 32 + 16, pk);
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      group_sync(4, 128);
+    };
     // state in: S^T[dv][dk] -> TMEM (lane = dv)
 #pragma unroll 1
     for (int cb = 0; cb < 4; ++cb) {
@@ -293,6 +321,10 @@ __global__ void __launch_bounds__(PNT, 1)
       tmem_st32(tmem + lb + TM_S + cb * 32, r);
     }
     tmem_wait_st();
+    tc_fence_before();
+    group_sync(4, 128);
+    tc_fence_after();
+    convert_sb();
 
     for (int c = 0; c < nch; ++c) {
       const int c0 = t0 + PC * c;
@@ -322,25 +354,6 @@ __global__ void __launch_bounds__(PNT, 1)
         fence_proxy_async();
       }
       tc_fence_after();
-      // C1a: S_b = bf16(S^T), 64 key columns at a time
-#pragma unroll 1
-      for (int hh = 0; hh < 2; ++hh) {
-        uint32_t x[32], y[32], pk[16];
-        tmem_ld32(tmem + lb + TM_S + hh * 64, x);
-        tmem_ld32(tmem + lb + TM_S + hh * 64 + 32, y);
-        tmem_wait_ld();
-#pragma unroll
-        for (int j2 = 0; j2 < 16; ++j2)
-          pk[j2] = pack_bf16x2(__uint_as_float(x[2 * j2]), __uint_as_float(x[2 * j2 + 1]));
-        tmem_st16(tmem + lb + TM_SB + hh * 32, pk);
-#pragma unroll
-        for (int j2 = 0; j2 < 16; ++j2)
-          pk[j2] = pack_bf16x2(__uint_as_float(y[2 * j2]), __uint_as_float(y[2 * j2 + 1]));
-        tmem_st16(tmem + lb + TM_SB + hh * 32 + 16, pk);
-      }
-      tmem_wait_st();
-      tc_fence_before();
-      group_sync(4, 128);
       PSTAMP(tid == 0, c, 2);
       // G1a: [X^T | O^T] = S_b [Kg | Qg]^T
       if (tid == 0) {
@@ -369,7 +382,29 @@ __global__ void __launch_bounds__(PNT, 1)
         }
         tmem_st32(tmem + lb + TM_S + cb * 32, x);
       }
+      PSTAMP(tid == 0, c, 12);
+      // C1c, also while G1a runs: T (fp32, from the k-side) -> the bf16 operands of G1b,
+      //     T diag(b) and T
+      {
+        const float* Tm = reinterpret_cast<const float*>(sm + PS_TM);
+        const float* bv = vec + 320;
+#pragma unroll
+        for (int it = tid; it < 512; it += 128) {
+          const int r = it & 63, c8 = it >> 6;   // row r, columns 8 c8 .. 8 c8 + 7
+          const float4 ta = ld4(Tm + r * NS + 8 * c8), tb = ld4(Tm + r * NS + 8 * c8 + 4);
+          const float4 ba = ld4(bv + 8 * c8), bb = ld4(bv + 8 * c8 + 4);
+          const uint32_t off = kmajor_off(r, 8 * c8, 64);
+          st_u128(sm, PS_TB + off,
+                  make_uint4(pack_bf16x2(ta.x * ba.x, ta.y * ba.y), pack_bf16x2(ta.z * ba.z, ta.w * ba.w),
+                             pack_bf16x2(tb.x * bb.x, tb.y * bb.y), pack_bf16x2(tb.z * bb.z, tb.w * bb.w)));
+          st_u128(sm, PS_TT + off,
+                  make_uint4(pack_bf16x2(ta.x, ta.y), pack_bf16x2(ta.z, ta.w),
+                             pack_bf16x2(tb.x, tb.y), pack_bf16x2(tb.z, tb.w)));
+        }
+      }
+      fence_proxy_async();   // read by G1b
       tmem_wait_st();
+      PSTAMP(tid == 0, c, 26);
       if (tid == 0) {
         ok = wait_spin(bar(B_G1A), par);
         if (ok) {
@@ -413,10 +448,38 @@ __global__ void __launch_bounds__(PNT, 1)
           mma_bf16_ts(tmem + TM_XU, tmem + TM_XB + 8 * ks, kdesc(sb + PS_TT, 64, ks), ID_N64, 1);
         mma_commit(bar(B_G1B));
         pend |= 4;
+      }
+      // C2b, while G1b runs: warps 2-3 take the QK rows (TMEM lanes 64-127 of the k-side's D)
+      //     into the MN-major bf16 operand of G2, so that D is free for the k-side's next product
+      if (warp >= 2) {
+        const int r = 32 * (warp & 1) + lane;   // row of QK
+#pragma unroll 1
+        for (int cq = 0; cq < 4; ++cq) {
+          uint32_t a[16];
+          // columns 16 cq .. 16 cq + 15 of the row; rows 32-63 take tokens 0-31 from D[:, 64:96]
+          tmem_ld16(tmem + lb + TM_D + (warp == 3 && cq < 2 ? 64 + 16 * cq : 16 * cq), a);
+          tmem_wait_ld();
+          // MN-major: element (r, s) at (s/8) * 1024 + (s%8) * 128 + chunk (r/8 ^ s%8)
+          const uint32_t base = (uint32_t)(cq * 2048 + (r & 7) * 2);
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            const int s2 = 16 * cq + e;
+            const __nv_bfloat16 val = __float2bfloat16_rn(s2 <= r ? __uint_as_float(a[e]) : 0.0f);
+            *reinterpret_cast<__nv_bfloat16*>(
+                sm + PS_QK + base + (e >> 3) * 1024 + (e & 7) * 128 + ((((r >> 3) ^ e) & 7) << 4)) = val;
+          }
+        }
+        fence_proxy_async();   // read by G2
+        tc_fence_before();
+        group_sync(2, 64);
+        if (tid == 64) mbar_arrive(bar(B_DFREE));   // the QK rows of D are free
+        PSTAMP(tid == 64, c, 27);
+      } else if (tid == 0) {   // meanwhile thread 0 waits for G1b
         ok = wait_spin(bar(B_G1B), par);
         if (ok) {
           pend &= ~4;
           mbar_arrive(bar(B_FREEC));   // T diag(b), T are free
+          PSTAMP(true, c, 28);
           if (c + 1 < nch) {           // v is free: the next chunk's v
             mbar_expect_tx(bar(B_V), 16384);
             tma_load_3d(sb + PS_V, &maps.v, 0, c0 + PC, zblk, bar(B_V));
@@ -459,17 +522,19 @@ __global__ void __launch_bounds__(PNT, 1)
         ok = wait_spin(bar(B_G2), par);
         if (ok) {
           pend &= ~8;
-          mbar_arrive(bar(B_FREEB));   // QK, Ke are free
+          mbar_arrive(bar(B_FREEB));   // Ke is free
         }
       }
       if (bar_any(4, 128, !ok)) { failed = true; site = 42; break; }
       PSTAMP(tid == 0, c, 8);
       tc_fence_after();
-      // C4: O^T diag(inv_q) -> out rows < L of this value channel (a warp writes 64
-      //     contiguous bytes of each row)
+      // C4: O^T diag(inv_q) -> out rows < L.  16 tokens at a time: each thread's 16 values
+      //     (its value channel) go to a per-warp [16 tok][32 dv] scratch, which the warp then
+      //     reads back as 32-byte row pieces for 16-byte global stores.
       {
         const float* iq = vec + 128;
-        __nv_bfloat16* orow = p.out + (size_t)c0 * HD + xcol + dv;
+        unsigned char* ost = sm + PS_OST + warp * 1024;
+        const int tok = lane >> 1, half = lane & 1;
 #pragma unroll 1
         for (int qq = 0; qq < 4; ++qq) {
           uint32_t x[16];
@@ -480,15 +545,30 @@ __global__ void __launch_bounds__(PNT, 1)
             const float4 f = ld4(iq + qq * 16 + 4 * t4);
             const float fv[4] = {f.x, f.y, f.z, f.w};
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const int r = qq * 16 + 4 * t4 + e;
-              if (r < L) orow[(size_t)r * HD] = __float2bfloat16_rn(__uint_as_float(x[4 * t4 + e]) * fv[e]);
-            }
+            for (int e = 0; e < 4; ++e)
+              *reinterpret_cast<__nv_bfloat16*>(ost + (4 * t4 + e) * 64 + lane * 2) =
+                  __float2bfloat16_rn(__uint_as_float(x[4 * t4 + e]) * fv[e]);
           }
+          __syncwarp();
+          const uint4 v0 = *reinterpret_cast<const uint4*>(ost + tok * 64 + half * 32);
+          const uint4 v1 = *reinterpret_cast<const uint4*>(ost + tok * 64 + half * 32 + 16);
+          const int r = qq * 16 + tok;
+          if (r < L) {
+            uint4* dst = reinterpret_cast<uint4*>(p.out + (size_t)(c0 + r) * HD + xcol + 32 * warp +
+                                                  16 * half);
+            dst[0] = v0;
+            dst[1] = v1;
+          }
+          __syncwarp();
         }
       }
       tc_fence_before();
+      group_sync(4, 128);   // the O scratch (over QK) is free for the next chunk's QK
       PSTAMP(tid == 0, c, 10);
+      if (c + 1 < nch) {
+        tc_fence_after();
+        convert_sb();
+      }
     }
     if (failed) {
       if (tid == 0) {
@@ -532,7 +612,6 @@ __global__ void __launch_bounds__(PNT, 1)
     float* FAC = reinterpret_cast<float*>(sm + PS_FAC);
     float* SS = reinterpret_cast<float*>(sm + PS_SS);
     uint32_t* RSC = reinterpret_cast<uint32_t*>(sm + PS_RSC);
-    float* BETA = reinterpret_cast<float*>(sm + PS_BETA);
     float* Nm = reinterpret_cast<float*>(sm + PS_NM);
     float* Tm = reinterpret_cast<float*>(sm + PS_TM);
     float* Y = reinterpret_cast<float*>(sm + PS_Y);
@@ -668,7 +747,7 @@ __global__ void __launch_bounds__(PNT, 1)
           RSC[kt] = bb | (bb << 16);
         }
       } else if (bt < PC) {
-        BETA[bt] = (bt < L) ? sigm(b_raw) : 0.0f;
+        vec[320 + bt] = (bt < L) ? sigm(b_raw) : 0.0f;   // b
         b_raw = 0.0f;
         if (c0 + PC + bt < t1) b_raw = __bfloat162float(p.beta[(size_t)(c0 + PC + bt) * p.s_beta + h]);
       }
@@ -677,7 +756,7 @@ __global__ void __launch_bounds__(PNT, 1)
 
       // ---- K3: operand tiles [Kr; Qr], [Kc; Kc2] (own), Kg, Qg (stage)
       {
-        float mE[4], fa[4], fb[4], fc[4], fq[4];
+        float mE[4], fa[4], fc[4], fq[4];
         {
           auto ld4f = [&](const float* src, float (&dst)[4]) {
             const float4 a = ld4(src);
@@ -685,7 +764,6 @@ __global__ void __launch_bounds__(PNT, 1)
           };
           ld4f(GT + j * 128 + 4 * o4, mE);
           ld4f(FAC + (bsel ? 4 : 0) * 128 + 4 * o4, fa);
-          ld4f(FAC + (bsel ? 2 : 1) * 128 + 4 * o4, fb);
           ld4f(FAC + 2 * 128 + 4 * o4, fc);
           ld4f(FAC + (bsel ? 5 : 3) * 128 + 4 * o4, fq);
         }
@@ -740,100 +818,96 @@ __global__ void __launch_bounds__(PNT, 1)
         group_sync(1, 512);
         PSTAMP(kt == 0, c, 21);
 
-        // ---- K4: [A | QK] on the tensor cores; the next chunk's inputs (the input tiles are
-        //      free); meanwhile Ke = Kc 2^(G_last - anchor) (stage), read from the Kc tile the
-        //      MMA is reading too
+        // ---- K4: [A | QK] on the tensor cores, once the chain has taken the previous QK out
+        //      of D; the next chunk's inputs (the input tiles are free)
         if (mma_thread) {
-          tc_fence_after();
+          if (c > 0) ok = wait_phase(bar(B_DFREE), (uint32_t)((c - 1) & 1));
+          if (ok) {
+            tc_fence_after();
 #pragma unroll
-          for (int ks = 0; ks < 8; ++ks)
-            mma_bf16(tmem + TM_D, kdesc(sb + PS_RKQ, 128, ks), kdesc(sb + PS_CKC, 96, ks), ID_D96,
-                     ks > 0);
-          mma_commit(bar(B_KMMA));
+            for (int ks = 0; ks < 8; ++ks)
+              mma_bf16(tmem + TM_D, kdesc(sb + PS_RKQ, 128, ks), kdesc(sb + PS_CKC, 96, ks),
+                       ID_D96, ks > 0);
+            mma_commit(bar(B_KMMA));
+            kmma_pend = (int)par + 1;
+          }
           PSTAMP(true, c, 31);
         }
-        kmma_pend = (int)par + 1;
         if (tma_thread && c + 1 < nch) issue_in(c + 1);
         PSTAMP(tma_thread, c, 30);
-        if (c > 0) {   // the chain has finished reading QK and Ke of the previous chunk
-          if (free_thread) ok = wait_phase(bar(B_FREEB), (uint32_t)((c - 1) & 1));
-          if (bar_any(1, 512, !ok)) { failed = true; site = 25; break; }
-        }
-        PSTAMP(kt == 0, c, 1);
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const int r = 4 * j + i;
-          const uint2 kcv = ld8b(PS_CKC + kmajor_off(r, 4 * o4, 96));
-          const float2 a = unpack_bf16x2(kcv.x), b = unpack_bf16x2(kcv.y);
-          uint32_t w0, w1;
-          if (bsel == 0) {   // 2^(G31 - G) then 2^(G63 - G31)
-            w0 = pack_bf16x2((a.x * fa[0]) * fb[0], (a.y * fa[1]) * fb[1]);
-            w1 = pack_bf16x2((b.x * fa[2]) * fb[2], (b.y * fa[3]) * fb[3]);
-          } else {           // 2^(G63 - G47)
-            w0 = pack_bf16x2(a.x * fa[0], a.y * fa[1]);
-            w1 = pack_bf16x2(b.x * fa[2], b.y * fa[3]);
-          }
-          st8b(PS_KE + mnmajor_off(4 * o4, r, 8192), w0, w1);
-        }
-        fence_proxy_async();
       }
-      if (mma_thread) ok = wait_phase(bar(B_KMMA), par);
+      if (mma_thread && ok) ok = wait_phase(bar(B_KMMA), par);
       if (bar_any(1, 512, !ok)) { failed = true; site = 24; break; }
       kmma_pend = 0;
       PSTAMP(kt == 0, c, 22);
       tc_fence_after();
 
-      // ---- K5: A rows -> N (fp32), QK rows -> bf16, MN-major (stage).  Warp w reads TMEM
-      //      quadrant w % 4, a 16-column quarter of the row's 64 columns.
-      {
+      // ---- K5: warps with w % 4 in {0, 1} read TMEM lanes 0-63 (rows of A), a 16-column
+      //      quarter of the row's 64 columns each -> N (fp32) and -b inv_k; the other eight
+      //      warps form Ke = Kc 2^(G_last - anchor) (stage) once the chain's last product of
+      //      the previous chunk has read Ke
+      if (c > 0) {
+        if (free_thread) ok = wait_phase(bar(B_FREEB), (uint32_t)((c - 1) & 1));
+        if (bar_any(1, 512, !ok)) { failed = true; site = 25; break; }
+      }
+      PSTAMP(kt == 0, c, 1);
+      if ((warp & 3) < 2) {
         const int q4 = warp & 3, cq = (warp - 4) >> 2;
         const uint32_t lbase = (uint32_t)(32 * q4) << 16;
-        const int rr = 32 * (q4 & 1) + lane;          // row (of A or of QK)
-        const bool hi = (q4 & 1) != 0;                // rows 32-63
-        const bool zero_part = !hi && cq >= 2;        // rows < 32, tokens >= 32
+        const int r = 32 * q4 + lane;
         const float* ik = vec + 192;
         uint32_t a[16];
-        if (!zero_part) {
+        if (!(q4 == 0 && cq >= 2)) {   // rows < 32 have no tokens >= 32 below the diagonal
           // columns 16 cq .. 16 cq + 15 of the row; rows 32-63 take tokens 0-31 from D[:, 64:96]
-          tmem_ld16(tmem + lbase + TM_D + (hi && cq < 2 ? 64 + 16 * cq : 16 * cq), a);
+          tmem_ld16(tmem + lbase + TM_D + (q4 == 1 && cq < 2 ? 64 + 16 * cq : 16 * cq), a);
           tmem_wait_ld();
         } else {
 #pragma unroll
           for (int e = 0; e < 16; ++e) a[e] = 0u;
         }
         PSTAMP(kt == 0, c, 23);
-        if (q4 < 2) {
-          const int r = rr;
-          float* nrow = Nm + r * NS + 16 * cq;
-          const float br = BETA[r] * ik[r];
+        float* nrow = Nm + r * NS + 16 * cq;
+        const float br = vec[320 + r] * ik[r];
+        if (cq == 0) vec[256 + r] = -br;
 #pragma unroll
-          for (int s4 = 0; s4 < 4; ++s4) {
-            const float4 kk = ld4(ik + 16 * cq + 4 * s4);
-            const float kv4[4] = {kk.x, kk.y, kk.z, kk.w};
-            float w[4];
+        for (int s4 = 0; s4 < 4; ++s4) {
+          const float4 kk = ld4(ik + 16 * cq + 4 * s4);
+          const float kv4[4] = {kk.x, kk.y, kk.z, kk.w};
+          float w[4];
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const int s2 = 16 * cq + 4 * s4 + e;
-              w[e] = (s2 < r) ? br * kv4[e] * __uint_as_float(a[4 * s4 + e]) : 0.0f;
-            }
-            *reinterpret_cast<float4*>(nrow + 4 * s4) = make_float4(w[0], w[1], w[2], w[3]);
+          for (int e = 0; e < 4; ++e) {
+            const int s2 = 16 * cq + 4 * s4 + e;
+            w[e] = (s2 < r) ? br * kv4[e] * __uint_as_float(a[4 * s4 + e]) : 0.0f;
           }
-        } else {
-          const int r = rr;
-          // MN-major: element (r, s) at (s/8) * 1024 + (s%8) * 128 + chunk (r/8 ^ s%8)
-          const uint32_t base = (uint32_t)(cq * 2048 + (r & 7) * 2);
-#pragma unroll
-          for (int e = 0; e < 16; ++e) {
-            const int s2 = 16 * cq + e;
-            const __nv_bfloat16 val = __float2bfloat16_rn(s2 <= r ? __uint_as_float(a[e]) : 0.0f);
-            *reinterpret_cast<__nv_bfloat16*>(
-                sm + PS_QK + base + (e >> 3) * 1024 + (e & 7) * 128 + ((((r >> 3) ^ e) & 7) << 4)) = val;
-          }
+          *reinterpret_cast<float4*>(nrow + 4 * s4) = make_float4(w[0], w[1], w[2], w[3]);
         }
+      } else {
+        // rows 8 kk .. 8 kk + 7, channels 4 o4 .. 4 o4 + 3
+        const int kk = 2 * ((warp - 4) >> 2) + (warp & 1);
+        const int kb = kk >> 2;   // 32-token block
+        const float4 fa4 = ld4(FAC + (kb ? 4 : 0) * 128 + 4 * o4);
+        const float4 fb4 = ld4(FAC + 1 * 128 + 4 * o4);
+        // block 0: 2^(G31 - G) then 2^(G63 - G31); block 1: 2^(G63 - G47)
+        const float f0 = kb ? fa4.x : fa4.x * fb4.x, f1 = kb ? fa4.y : fa4.y * fb4.y;
+        const float f2 = kb ? fa4.z : fa4.z * fb4.z, f3 = kb ? fa4.w : fa4.w * fb4.w;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const int r = 8 * kk + i;
+          const uint2 kcv = ld8b(PS_CKC + kmajor_off(r, 4 * o4, 96));
+          const float2 a = unpack_bf16x2(kcv.x), b = unpack_bf16x2(kcv.y);
+          st8b(PS_KE + mnmajor_off(4 * o4, r, 8192), pack_bf16x2(a.x * f0, a.y * f1),
+               pack_bf16x2(b.x * f2, b.y * f3));
+        }
+        fence_proxy_async();
       }
       tc_fence_before();
       group_sync(1, 512);
       PSTAMP(kt == 0, c, 24);
+      if (c > 0) {   // the chain has read T of the previous chunk (and the bf16 operands made of it)
+        if (mma_thread) ok = wait_phase(bar(B_FREEC), (uint32_t)((c - 1) & 1));
+        if (bar_any(1, 512, !ok)) { failed = true; site = 26; break; }
+      }
+      PSTAMP(kt == 0, c, 11);
 
       // ---- K6 (threads < 128): T = (I + N)^-1: 16 x 16 diagonal blocks by substitution
       //      (fp32), then the off-diagonal blocks as tf32 warp products, 16 -> 32 -> 64
@@ -847,21 +921,30 @@ __global__ void __launch_bounds__(PNT, 1)
               make_float4(0.f, 0.f, 0.f, 0.f);
         }
         if (wb < 2) {
-          const int ob = (kt >> 4) * 16, jj = kt & 15;
+          // warp wb: the diagonal blocks 2 wb (lanes 0-15) and 2 wb + 1 (lanes 16-31), lane =
+          // column, by forward substitution four columns of N at a time (16-byte row pieces);
+          // then the pair's off-diagonal block T[2wb+1][2wb] = -T[2wb+1]^ N[2wb+1][2wb] T[2wb]^
+          // (^ = diagonal block), which needs nothing from the other warps
+          const int ob = (lane >> 4) * 16 + 32 * wb, jj = lane & 15;
           float x[16];
 #pragma unroll
           for (int i = 0; i < 16; ++i) x[i] = (i == jj) ? 1.0f : 0.0f;
 #pragma unroll
-          for (int k = 0; k < 15; ++k) {
+          for (int k0 = 0; k0 < 16; k0 += 4) {
 #pragma unroll
-            for (int i = k + 1; i < 16; ++i) x[i] = fmaf(-Nm[(ob + i) * NS + ob + k], x[k], x[i]);
+            for (int i = k0 + 1; i < 16; ++i) {
+              const float4 nv = ld4(Nm + (ob + i) * NS + ob + k0);
+              float acc = fmaf(-nv.x, x[k0], x[i]);
+              if (i > k0 + 1) acc = fmaf(-nv.y, x[k0 + 1], acc);
+              if (i > k0 + 2) acc = fmaf(-nv.z, x[k0 + 2], acc);
+              if (i > k0 + 3) acc = fmaf(-nv.w, x[k0 + 3], acc);
+              x[i] = acc;
+            }
           }
 #pragma unroll
           for (int i = 0; i < 16; ++i) Tm[(ob + i) * NS + ob + jj] = x[i];
-        }
-        PSTAMP(kt == 0, c, 14);
-        group_sync(3, 128);
-        if (wb < 2) {   // pair (1,0) on warp 0 of the group, (3,2) on warp 1
+          __syncwarp();
+          PSTAMP(kt == 0, c, 14);
           const int ro = (2 * wb + 1) * 16, co = 2 * wb * 16;
           float* Yw = Y + wb * 16 * NS;
           wgemm16(Nm + ro * NS + co, Tm + co * NS + co, Yw, 1.0f, lane);
@@ -877,33 +960,6 @@ __global__ void __launch_bounds__(PNT, 1)
         wgemm32(Tm + (32 + 16 * mi) * NS + 32, Y + 16 * ni, Tm + (32 + 16 * mi) * NS + 16 * ni,
                 -1.0f, lane);
       }
-      group_sync(1, 512);
-      PSTAMP(kt == 0, c, 25);
-
-      // ---- K7: T diag(b) and T -> bf16 (stage); -b inv_k
-      PSTAMP(kt == 0, c, 11);
-      if (c > 0) {   // the chain has finished reading T diag(b) and T of the previous chunk
-        if (mma_thread) ok = wait_phase(bar(B_FREEC), (uint32_t)((c - 1) & 1));
-        PSTAMP(kt == 0, c, 12);
-        if (bar_any(1, 512, !ok)) { failed = true; site = 26; break; }
-      }
-      PSTAMP(kt == 0, c, 26);
-      {
-        const int r = kt & 63, c8 = kt >> 6;   // row r, columns 8 c8 .. 8 c8 + 7
-        const float4 ta = ld4(Tm + r * NS + 8 * c8), tb = ld4(Tm + r * NS + 8 * c8 + 4);
-        const float4 ba = ld4(BETA + 8 * c8), bb = ld4(BETA + 8 * c8 + 4);
-        const uint32_t off = kmajor_off(r, 8 * c8, 64);
-        st_u128(sm, PS_TB + off,
-                make_uint4(pack_bf16x2(ta.x * ba.x, ta.y * ba.y), pack_bf16x2(ta.z * ba.z, ta.w * ba.w),
-                           pack_bf16x2(tb.x * bb.x, tb.y * bb.y), pack_bf16x2(tb.z * bb.z, tb.w * bb.w)));
-        st_u128(sm, PS_TT + off,
-                make_uint4(pack_bf16x2(ta.x, ta.y), pack_bf16x2(ta.z, ta.w),
-                           pack_bf16x2(tb.x, tb.y), pack_bf16x2(tb.z, tb.w)));
-        if (kt < PC) vec[256 + kt] = -BETA[kt] * vec[192 + kt];
-      }
-      PSTAMP(kt == 0, c, 27);
-      fence_proxy_async();
-      PSTAMP(kt == 0, c, 28);
       group_sync(1, 512);
       if (mma_thread) mbar_arrive(bar(B_FULL));   // the stage of chunk c is complete
       PSTAMP(kt == 0, c, 29);
