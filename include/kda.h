@@ -91,9 +91,10 @@ typedef struct CUstream_st* kda_stream_t;
 /* kernel selectors for kda_chunk_prefill_fwd_ex */
 #define KDA_KERNEL_AUTO 0  /* SPLIT when the value split triggers and the
                               workspace holds its records; else TC_HELPERS
-                              when at least 8 SMs stay free, N <= 128, the
-                              sequences average 4 or more chunks and the
-                              workspace holds the records; else TC          */
+                              when N * heads <= min(SMs - 8, 5 SMs / 8),
+                              N <= 128, the sequences average 4 or more
+                              chunks and the workspace holds the records;
+                              else PIPE (TC when the caller fixed P > 1)     */
 #define KDA_KERNEL_TC 1    /* fused tcgen05 + TMA chunk kernel, C = 64: one CTA
                               per (sequence, head[, value slice])            */
 #define KDA_KERNEL_REF 2   /* plain-CUDA-core chunk kernel (GPU parity aid)    */
@@ -112,7 +113,6 @@ typedef struct CUstream_st* kda_stream_t;
                               one CTA per (sequence, head) whose k-side warps
                               build chunk c+1's operands while its chain warps
                               run chunk c; no value split (vsplit -1 or 1),
-                              dense outputs only (not the _scatter entry point),
                               needs only the 256-byte workspace               */
 
 /*
@@ -125,8 +125,8 @@ typedef struct CUstream_st* kda_stream_t;
  * The workspace starts with the device status word (256 bytes: all the
  * fused kernel needs).  When some batch of up to max_seqs sequences would
  * take the value split on the current device (2 * heads * N <= SM count;
- * 152 SMs are assumed when no device answers) or leave at least 8 SMs to
- * k-side helpers (heads * N + 8 <= SM count), it also holds the records of
+ * 152 SMs are assumed when no device answers) or take k-side helpers
+ * (heads * N <= min(SM count - 8, 5 SM count / 8)), it also holds the records of
  * those paths: a 1 KB header, then 66,560 bytes per (chunk slot, head),
  * with ceil(total_tokens / 64) + N slots for the largest such N -- about
  * 1 KB per token-head -- and, for the helpers, one int32 claim word per
@@ -322,7 +322,7 @@ int kda_device_check(int device);
  * The path a kda_chunk_prefill_fwd_ex call with these sizes, workspace size
  * and selectors would take on the current device, without enqueuing
  * anything: *kernel_out gets KDA_KERNEL_TC, KDA_KERNEL_TC_HELPERS,
- * KDA_KERNEL_SPLIT or KDA_KERNEL_REF (AUTO resolved), *vsplit_out the value split factor P and
+ * KDA_KERNEL_SPLIT, KDA_KERNEL_PIPE or KDA_KERNEL_REF (AUTO resolved), *vsplit_out the value split factor P and
  * *launches_out the number of kernels the call enqueues (0, 1 or 2); any
  * output pointer may be NULL.  Returns the code such a call would return
  * for its sizes, selectors and workspace size (pointer checks aside), or

@@ -69,8 +69,10 @@ int validate(const void* q, const void* k, const void* v, const void* g, const v
 
 // The path of a call: validated selectors, then AUTO resolved.  The split path (k-side
 // records + chain per value slice) needs its record area in the workspace; AUTO takes it
-// when the value split triggers and the workspace holds the records, else the fused kernel
-// with one CTA per (sequence, head).
+// when the value split triggers and the workspace holds the records.  Otherwise one CTA
+// per (sequence, head): the warp-specialised kernel, or, while at most 5/8 of the SMs
+// would be busy, the fused kernel with k-side helper CTAs on the free ones (on GB300 at
+// 2048-token sequences the helpers win up to about 90 chains and lose from about 110).
 int plan(int64_t total_tokens, int32_t num_seqs, int32_t heads, size_t workspace_bytes,
          int vsplit, int kernel, int sms, int* kernel_out, int* vsplit_out, int* launches_out) {
   if (vsplit != -1 && vsplit != 1 && vsplit != 2 && vsplit != 4 && vsplit != 8)
@@ -97,11 +99,11 @@ int plan(int64_t total_tokens, int32_t num_seqs, int32_t heads, size_t workspace
     if (P > 1 && workspace_bytes >= split_need && total_tokens > 0) {
       kernel = KDA_KERNEL_SPLIT;
     } else {
-      kernel = KDA_KERNEL_TC;
       if (vsplit == -1) P = 1;
-      // the fused kernel leaves SMs free: helpers take the far ends of the sequences
+      kernel = P == 1 ? KDA_KERNEL_PIPE : KDA_KERNEL_TC;
+      // many SMs left free: helpers take the far ends of the sequences
       if (P == 1 && num_seqs > 0 && num_seqs <= kda::kHelperMaxSeqs &&
-          (int64_t)num_seqs * heads + kda::kHelperMinFreeSms <= sms &&
+          (int64_t)num_seqs * heads <= kda::helper_max_chains(sms) &&
           ((total_tokens + kda::kChunk - 1) / kda::kChunk) * num_seqs * heads < ((int64_t)1 << 30) &&
           total_tokens >= (int64_t)4 * kda::kChunk * num_seqs && workspace_bytes >= help_need)
         kernel = KDA_KERNEL_TC_HELPERS;
@@ -148,7 +150,6 @@ int fwd_impl(const void* q, const void* k, const void* v, const void* g, const v
   if (kernel != KDA_KERNEL_AUTO && kernel != KDA_KERNEL_TC && kernel != KDA_KERNEL_REF &&
       kernel != KDA_KERNEL_SPLIT && kernel != KDA_KERNEL_TC_HELPERS && kernel != KDA_KERNEL_PIPE)
     return KDA_ERR_INVALID_ARG;
-  if (kernel == KDA_KERNEL_PIPE && scatter) return KDA_ERR_INVALID_ARG;
   int dev = 0, sms = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) {
     cudaGetLastError();
@@ -288,11 +289,10 @@ size_t kda_workspace_size(int64_t total_tokens, int32_t heads, int32_t max_seqs)
     const int32_t n_split = (int32_t)std::min<int64_t>(max_seqs, sms / (2 * (int64_t)heads));
     need = std::max(need, kda::split_workspace_bytes(total_tokens, heads, n_split));
   }
-  // ... and for the fused kernel's k-side helpers: N * heads + 8 <= SMs
-  if (heads > 0 && total_tokens > 0 && max_seqs > 0 &&
-      (int64_t)heads + kda::kHelperMinFreeSms <= sms) {
+  // ... and for the fused kernel's k-side helpers: N * heads <= helper_max_chains(SMs)
+  if (heads > 0 && total_tokens > 0 && max_seqs > 0 && heads <= kda::helper_max_chains(sms)) {
     const int32_t n_help = (int32_t)std::min<int64_t>(
-        std::min<int64_t>(max_seqs, kda::kHelperMaxSeqs), (sms - kda::kHelperMinFreeSms) / (int64_t)heads);
+        std::min<int64_t>(max_seqs, kda::kHelperMaxSeqs), kda::helper_max_chains(sms) / heads);
     need = std::max(need, kda::helper_workspace_bytes(total_tokens, heads, n_help));
   }
   return (need + 15) & ~(size_t)15;

@@ -147,6 +147,12 @@ inline size_t split_workspace_bytes(int64_t total_tokens, int32_t heads, int32_t
 constexpr int kClaimFree = 0, kClaimHelper = 1, kClaimReady = 2, kClaimOwn = 3;
 constexpr int kHelperCounterWord = 128;   // int index in the workspace header
 constexpr int kHelperMinFreeSms = 8;      // helpers only with at least this many free SMs
+// Most (sequence, head) chains AUTO gives helpers: at least kHelperMinFreeSms SMs free and
+// at most 5/8 of the SMs busy (beyond that the warp-specialised kernel is faster on GB300)
+inline int64_t helper_max_chains(int sms) {
+  const int64_t a = (int64_t)sms - kHelperMinFreeSms, b = 5 * (int64_t)sms / 8;
+  return a < b ? a : b;
+}
 constexpr int kHelperMaxSeqs = 128;       // ... and at most this many sequences
 __host__ __device__ inline size_t helper_claims_offset(int64_t total_tokens, int32_t heads,
                                                        int32_t num_seqs) {

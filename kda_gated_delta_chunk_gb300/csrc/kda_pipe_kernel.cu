@@ -553,9 +553,9 @@ __global__ void __launch_bounds__(PNT, 1)
           const uint4 v0 = *reinterpret_cast<const uint4*>(ost + tok * 64 + half * 32);
           const uint4 v1 = *reinterpret_cast<const uint4*>(ost + tok * 64 + half * 32 + 16);
           const int r = qq * 16 + tok;
-          if (r < L) {
-            uint4* dst = reinterpret_cast<uint4*>(p.out + (size_t)(c0 + r) * HD + xcol + 32 * warp +
-                                                  16 * half);
+          const int64_t orow = r < L ? out_row(p, c0 + r) : -1;   // the row map, if any
+          if (orow >= 0) {
+            uint4* dst = reinterpret_cast<uint4*>(p.out + orow * HD + xcol + 32 * warp + 16 * half);
             dst[0] = v0;
             dst[1] = v1;
           }
@@ -1006,7 +1006,7 @@ cudaError_t launch_pipe(const Params& p, cudaStream_t stream) {
                                 PIPE_SMEM);
   });
   if (e != cudaSuccess) return e;
-  if (p.vsplit != 1 || p.out_index != nullptr || p.helpers) return cudaErrorInvalidValue;
+  if (p.vsplit != 1 || p.helpers) return cudaErrorInvalidValue;
   const long long blocks = (long long)p.num_seqs * p.heads;
   if (blocks <= 0) return cudaSuccess;
   if (blocks > 0x7fffffffLL) return cudaErrorInvalidValue;

@@ -61,9 +61,9 @@ def _sms():
 
 def test_workspace_size_holds_split_records(L):
     """Records for ceil(T/64) + N chunk slots per head whenever some batch of up to
-    max_seqs sequences would take the value split (2 H N <= SMs) or leave 8 SMs to k-side
-    helpers (H N + 8 <= SMs, N <= 128; plus a 4-byte claim word per slot and head), else
-    256 bytes; rounded up to 16."""
+    max_seqs sequences would take the value split (2 H N <= SMs) or the k-side helpers
+    (H N <= min(SMs - 8, 5 SMs / 8), N <= 128; plus a 4-byte claim word per slot and head),
+    else 256 bytes; rounded up to 16."""
     sms = _sms()
     cases = [(1000, 2, 3), (16384, 16, 1), (16384, 16, 8), (4096, 8, 7), (64, 1, 500),
              (65536, 32, 64), (65536, 160, 2)]
@@ -73,8 +73,9 @@ def test_workspace_size_holds_split_records(L):
         if 2 * H <= sms:
             n_split = min(N, sms // (2 * H))
             need = max(need, 1024 + ((T + 63) // 64 + n_split) * H * SLOT_HEAD_BYTES)
-        if H + 8 <= sms:
-            n_help = min(N, 128, (sms - 8) // H)
+        max_chains = min(sms - 8, 5 * sms // 8)
+        if H <= max_chains:
+            n_help = min(N, 128, max_chains // H)
             need = max(need, 1024 + ((T + 63) // 64 + n_help) * H * (SLOT_HEAD_BYTES + 4))
         assert got == (need + 15) // 16 * 16, (T, H, N)
         assert got % 16 == 0
@@ -122,13 +123,13 @@ def _records_only(lengths, H):
 
 @pytest.mark.parametrize("shape,H,want", [
     ("tiny", 2, (kda.KERNEL_SPLIT, 8, 2)),                 # 1 x 128
-    ("batched", 16, (kda.KERNEL_TC_HELPERS, 1, 2)),        # 128 chains leave 24 SMs free
+    ("batched", 16, (kda.KERNEL_PIPE, 1, 1)),              # 128 chains: over 5/8 of the SMs
     ("long", 16, (kda.KERNEL_SPLIT, 8, 2)),                # 1 x 16384
     ("v1", 8, (kda.KERNEL_SPLIT, 8, 2)),                   # N x 4096, H = 8
     ("v2", 8, (kda.KERNEL_SPLIT, 8, 2)),
     ("v3", 8, (kda.KERNEL_SPLIT, 4, 2)),
     ("v7", 8, (kda.KERNEL_SPLIT, 2, 2)),
-    ("ragged", 32, (kda.KERNEL_TC, 1, 1)),                 # 2048 chains: no SM left over
+    ("ragged", 32, (kda.KERNEL_PIPE, 1, 1)),               # 2048 chains: no SM left over
 ])
 def test_auto_dispatch_of_the_benchmark_shapes(L, shape, H, want):
     lengths = {"tiny": [128], "batched": [2048] * 8, "long": [16384], "v1": [4096],
@@ -138,37 +139,42 @@ def test_auto_dispatch_of_the_benchmark_shapes(L, shape, H, want):
 
 
 def test_auto_helper_conditions(L):
-    # at least 8 SMs stay free: 18 x 8 = 144 chains leave 8, 19 x 8 = 152 leave none
-    assert _auto([2048] * 18, 8)[0] == kda.KERNEL_TC_HELPERS
-    assert _auto([2048] * 19, 8)[0] == kda.KERNEL_TC
-    # the same batch on a smaller part: 136 > 132 SMs
-    assert _auto([2048] * 8, 16, sms=148)[0] == kda.KERNEL_TC_HELPERS
-    assert _auto([2048] * 8, 16, sms=132)[0] == kda.KERNEL_TC
-    # at most 128 sequences
-    assert _auto([256] * 128, 1)[0] == kda.KERNEL_TC_HELPERS
-    assert _auto([256] * 129, 1)[0] == kda.KERNEL_TC
+    # helpers while at most min(SMs - 8, 5 SMs / 8) chains run (95 of 152), else the
+    # warp-specialised kernel: 11 x 8 = 88 chains and 12 x 8 = 96
+    assert _auto([2048] * 11, 8)[0] == kda.KERNEL_TC_HELPERS
+    assert _auto([2048] * 12, 8) == (kda.KERNEL_PIPE, 1, 1)
+    # 5 x 16 = 80 chains: 5/8 of 128 SMs is 80, of 127 it is 79
+    assert _auto([2048] * 5, 16, sms=128)[0] == kda.KERNEL_TC_HELPERS
+    assert _auto([2048] * 5, 16, sms=127)[0] == kda.KERNEL_PIPE
+    # on a small part the 8 free SMs bind first: 5/8 of 20 is 12, 20 - 8 = 12 as well;
+    # 13 chains of 1 head exceed both
+    assert _auto([256] * 12, 1, sms=20)[0] == kda.KERNEL_TC_HELPERS
+    assert _auto([256] * 13, 1, sms=20)[0] == kda.KERNEL_PIPE
     # sequences of at least 4 chunks on average
-    assert _auto([256] * 8, 16)[0] == kda.KERNEL_TC_HELPERS
-    assert _auto([255] * 8, 16)[0] == kda.KERNEL_TC
+    assert _auto([256] * 5, 16)[0] == kda.KERNEL_TC_HELPERS
+    assert _auto([255] * 5, 16)[0] == kda.KERNEL_PIPE
     # the claim words must fit as well as the records
-    lengths = [2048] * 8
-    assert _auto(lengths, 16, ws=_records_only(lengths, 16)) == (kda.KERNEL_TC, 1, 1)
+    lengths = [2048] * 5
+    assert _auto(lengths, 16, ws=_records_only(lengths, 16)) == (kda.KERNEL_PIPE, 1, 1)
     claims = ((sum(lengths) + 63) // 64 + len(lengths)) * 16 * 4   # a word per (slot, head)
-    assert _auto(lengths, 16, ws=_records_only(lengths, 16) + claims - 4)[0] == kda.KERNEL_TC
+    assert _auto(lengths, 16, ws=_records_only(lengths, 16) + claims - 4)[0] == kda.KERNEL_PIPE
     assert _auto(lengths, 16, ws=_records_only(lengths, 16) + claims)[0] == \
         kda.KERNEL_TC_HELPERS
 
 
 def test_auto_without_room_for_records_runs_the_fused_kernel(L):
     # the value split triggers, but a bare status workspace holds no records
-    assert _auto([16384], 16, ws=256) == (kda.KERNEL_TC, 1, 1)
+    assert _auto([16384], 16, ws=256) == (kda.KERNEL_PIPE, 1, 1)
     # a split factor given by the caller stays, on the fused kernel
     assert _auto([16384], 16, ws=256, vsplit=4) == (kda.KERNEL_TC, 4, 1)
     assert _auto([16384], 16, ws=_records_only([16384], 16)) == (kda.KERNEL_SPLIT, 8, 2)
 
 
 def test_forced_kernels_and_refusals(L):
-    assert _auto([2048] * 8, 16, kernel=kda.KERNEL_SPLIT) == (kda.KERNEL_SPLIT, 1, 2)
+    # a forced split with records for all eight sequences (more than the default workspace
+    # of eight sequences holds: AUTO takes neither the split nor helpers there)
+    assert _auto([2048] * 8, 16, kernel=kda.KERNEL_SPLIT, ws=_records_only([2048] * 8, 16)) == \
+        (kda.KERNEL_SPLIT, 1, 2)
     assert _auto([2048] * 8, 16, kernel=kda.KERNEL_TC) == (kda.KERNEL_TC, 1, 1)
     assert _auto([2048] * 8, 16, kernel=kda.KERNEL_REF) == (kda.KERNEL_REF, 1, 1)
     assert _auto([16384], 16, kernel=kda.KERNEL_TC_HELPERS) == (kda.KERNEL_TC_HELPERS, 1, 2)
@@ -192,9 +198,9 @@ def test_forced_kernels_and_refusals(L):
 
 
 def test_launch_counts_of_degenerate_batches(L):
-    assert kda.plan_for(0, 0, 16, 256, GB300_SMS) == (kda.KERNEL_TC, 1, 0)     # no sequences
+    assert kda.plan_for(0, 0, 16, 256, GB300_SMS) == (kda.KERNEL_PIPE, 1, 0)   # no sequences
     # sequences that are all empty: no records to make, one launch writes the states
-    assert kda.plan_for(0, 3, 8, 1 << 20, GB300_SMS) == (kda.KERNEL_TC, 1, 1)
+    assert kda.plan_for(0, 3, 8, 1 << 20, GB300_SMS) == (kda.KERNEL_PIPE, 1, 1)
     # a forced split path keeps its documented record area, a slot per sequence included
     ws = _records_only([0, 0, 0], 8)
     assert kda.plan_for(0, 3, 8, ws, GB300_SMS, kernel=kda.KERNEL_SPLIT) == (kda.KERNEL_SPLIT, 4, 1)

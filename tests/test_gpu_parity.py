@@ -174,8 +174,9 @@ def test_auto_takes_split_path_when_it_triggers(oracle_mod, cfg):
 
 
 def test_split_falls_back_to_fused_on_small_workspace(oracle_mod):
-    """AUTO with a workspace below the split path's record area runs the fused
-    kernel; forcing the split path with it is refused."""
+    """AUTO with a workspace below the split path's record area runs one CTA per
+    (sequence, head) -- the warp-specialised kernel; forcing the split path with it is
+    refused."""
     inp = W.make_inputs(W.custom([150, 70], 2, seed=31))
     d = to_dev(inp)
     small = torch.zeros(256, dtype=torch.uint8, device="cuda")
@@ -183,7 +184,7 @@ def test_split_falls_back_to_fused_on_small_workspace(oracle_mod):
             d["lower_bound"], d["scale"], d["initial_state"], d["cu_seqlens"])
     out, fin = kda.chunk_prefill_fwd(*args, workspace=small)
     torch.cuda.synchronize()
-    out_t, fin_t = run_gpu(inp, kda.KERNEL_TC, vsplit=1)
+    out_t, fin_t = run_gpu(inp, kda.KERNEL_PIPE, vsplit=1)
     assert torch.equal(out, out_t) and torch.equal(fin, fin_t)
     check(oracle_mod, inp, out, fin, tag="small workspace")
     with pytest.raises(kda.KDAError) as e:
@@ -404,17 +405,21 @@ def test_helpers_agree_with_the_fused_kernel_alone(oracle_mod, lengths, H):
     check(oracle_mod, inp, out_h, fin_h, heads=heads, tag=f"helpers {N}x{H}")
 
 
-def test_auto_takes_helpers_on_the_benchmark_shape():
-    """8 x 2048, H = 16 leaves 24 of 152 SMs free: AUTO runs the fused kernel with helpers."""
+def test_auto_dispatch_on_the_device():
+    """8 x 2048, H = 16 keeps more than 5/8 of the 152 SMs busy: AUTO runs the
+    warp-specialised kernel; 5 x 2048 (80 chains) leaves enough free for helpers."""
     sms = torch.cuda.get_device_properties(0).multi_processor_count
+    max_chains = min(sms - 8, 5 * sms // 8)
     T, N, H = 16384, 8, 16
     path, P, launches = kda.plan(T, N, H, kda.workspace_size(T, H, N), -1, kda.KERNEL_AUTO)
-    if N * H + 8 <= sms:
+    if N * H > max_chains:
+        assert (path, P, launches) == (kda.KERNEL_PIPE, 1, 1)
+    T, N = 10240, 5
+    path, P, launches = kda.plan(T, N, H, kda.workspace_size(T, H, N), -1, kda.KERNEL_AUTO)
+    if N * H <= max_chains and 2 * N * H > sms:
         assert (path, P, launches) == (kda.KERNEL_TC_HELPERS, 1, 2)
-    else:
-        assert path == kda.KERNEL_TC
     path, P, launches = kda.plan(T, N, H, 256, -1, kda.KERNEL_AUTO)   # no room for records
-    assert (path, P, launches) == (kda.KERNEL_TC, 1, 1)
+    assert (path, P, launches) == (kda.KERNEL_PIPE, 1, 1)
 
 
 def test_helpers_under_cuda_graph_replay(oracle_mod):

@@ -65,7 +65,8 @@ def check_placed(buf, rows, dense, T_used):
 
 @pytest.mark.parametrize("kernel,vsplit", [(kda.KERNEL_TC, 1), (kda.KERNEL_TC, 2),
                                            (kda.KERNEL_TC_HELPERS, -1), (kda.KERNEL_SPLIT, 1),
-                                           (kda.KERNEL_SPLIT, 4), (kda.KERNEL_REF, 1)])
+                                           (kda.KERNEL_SPLIT, 4), (kda.KERNEL_REF, 1),
+                                           (kda.KERNEL_PIPE, 1)])
 def test_prefill_scatter_places_the_dense_rows(kernel, vsplit):
     """Ragged sequences (a 1-token and an empty one, tails), tokens past cu_seqlens[N]."""
     inp = W.make_inputs(W.custom([130, 1, 0, 64, 257, 70], 2, seed=61, pad_tokens=5))
@@ -87,7 +88,7 @@ def test_prefill_scatter_places_the_dense_rows(kernel, vsplit):
 
 
 def test_prefill_scatter_on_the_benchmark_shape():
-    """8 x 2048, H = 16 through AUTO (the fused kernel with helpers): rows in reverse order."""
+    """8 x 2048, H = 16 through AUTO (the warp-specialised kernel): rows in reverse order."""
     inp = W.make_inputs(W.workload(1))
     d = dev(inp)
     T, H, N = d["q"].shape[0], 16, 8
@@ -140,7 +141,8 @@ def test_mixed_step_writes_one_layer_output(oracle_mod):
         assert np.abs(got - o_ref).max() <= tol
 
 
-@pytest.mark.parametrize("kernel", [kda.KERNEL_TC, kda.KERNEL_SPLIT, kda.KERNEL_REF])
+@pytest.mark.parametrize("kernel", [kda.KERNEL_TC, kda.KERNEL_SPLIT, kda.KERNEL_REF,
+                                    kda.KERNEL_PIPE])
 def test_out_of_range_rows_are_reported_and_skipped(kernel):
     inp = W.make_inputs(W.custom([100, 40], 2, seed=68))
     d = dev(inp)
