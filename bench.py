@@ -4,7 +4,8 @@ One step = one kda_chunk_prefill_fwd call over the whole batch (every step of
 the method runs inside that call's kernels).  Prints ONE JSON line (rank 0).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                  [--kernel auto|tc|split|ref] [--workload 1] [--no-cpu-baseline]
+                  [--kernel auto|tc|split|ref|helpers|pipe] [--workload 1]
+                  [--no-cpu-baseline] [--stamps]
 
 value       tokens/s of the whole job (all ranks), inputs resident in HBM;
             device time from CUDA events over exactly K steps, max over ranks.
@@ -13,12 +14,19 @@ e2e         the same metric through the C ABI with host buffers: pinned
             copies of out and final_state, all inside the timed region.
 roofline    the prefill call against the HBM roofline: algorithmic bytes per
             call / mean call time (CUDA events on the launch stream).  On the
-            default workload the call is one launch of the fused tcgen05
+            default workload AUTO runs one launch of the warp-specialised
             kernel; on the split path (few sequences x heads) it is the
             k-side kernel followed by the chain kernel.
+launch_us   mean, median, min and max of the K per-call event times.
+graph       the same call captured in a CUDA graph (8 calls per graph over the
+            rotating input sets), replayed 60 times: microseconds per call.
 cpu_baseline  the fp64 CPU oracle (test infrastructure) on a bounded sample
-            of the same workload, on this host's cores (rank 0, N=1 only).
+            of the same workload, on this host's cores (rank 0, N=1 only);
+            cpu_baseline_1thread the same oracle on one thread.
 --impl reference  times that oracle as the reference arm.
+--stamps    the per-chunk phase breakdown of the warp-specialised kernel: builds
+            the -DKDA_PHASE_STAMPS variant of the library and prints medians of
+            the clock64 stamps of CTA 0 (not a bench line).
 
 L2: the inputs (352 MB per step) exceed the 129 MB L2, and four copies of
 them are rotated so that no step finds the previous step's data in L2.
@@ -190,8 +198,9 @@ def max_over_ranks(x: float, world: int) -> float:
     return float(t.item())
 
 
-def oracle_sample_run(inp, heads):
-    """The fp64 oracle on all sequences of the workload for the given heads."""
+def oracle_sample_run(inp, heads, num_threads=0):
+    """The fp64 oracle on all sequences of the workload for the given heads (num_threads 0:
+    all the cores the oracle finds)."""
     import oracle
     N = inp["cu_seqlens"].numel() - 1
     sub = W.select(inp, range(N), heads)
@@ -200,7 +209,7 @@ def oracle_sample_run(inp, heads):
             f(sub["A_log"]), f(sub["dt_bias"]), sub["lower_bound"], sub["scale"],
             f(sub["initial_state"]), sub["cu_seqlens"].numpy())
     t0 = time.perf_counter()
-    oracle.kda_oracle_fwd(*args)
+    oracle.kda_oracle_fwd(*args, num_threads=num_threads)
     return time.perf_counter() - t0
 
 
@@ -224,6 +233,46 @@ def cpu_baseline(inp, w: W.Workload, budget_s: float = 10.0):
                       f"{w.heads} heads ({T * h * reps} token-heads, fp64, {t:.2f} s); "
                       f"tokens/s = token-heads/s / {w.heads}",
             "seconds": t}
+
+
+def cpu_baseline_one_thread(inp, w: W.Workload, budget_s: float = 4.0):
+    """The oracle on one host thread: whole passes over all sequences for as many heads as
+    fit in about budget_s (at least one head, one pass)."""
+    import oracle
+    oracle.build()
+    T = sum(w.lengths)
+    t = oracle_sample_run(inp, [0], num_threads=1)
+    h = 1
+    while h < w.heads and t * (h + 1) / h <= budget_s:
+        t += oracle_sample_run(inp, [h], num_threads=1)
+        h += 1
+    return {"value": T * h / t / w.heads, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"{w.name}: all {w.num_seqs} sequences x {h} of {w.heads} heads on one "
+                      f"thread ({T * h} token-heads, fp64, {t:.2f} s); tokens/s = token-heads/s "
+                      f"/ {w.heads}", "seconds": t}
+
+
+def graph_timing(step, stream, calls: int = 8, replays: int = 60):
+    """The same call captured in a CUDA graph (`calls` calls over the rotating input sets per
+    graph) and replayed `replays` times after 3 warm-up replays: microseconds per call."""
+    g = torch.cuda.CUDAGraph()
+    stream.synchronize()
+    with torch.cuda.graph(g, stream=stream):
+        for i in range(calls):
+            step(i)
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            g.replay()
+    stream.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    with torch.cuda.stream(stream):
+        for _ in range(replays):
+            g.replay()
+    e1.record(stream)
+    e1.synchronize()
+    return {"us_per_layer": 1e3 * e0.elapsed_time(e1) / (replays * calls),
+            "replays": replays, "calls_per_replay": calls}
 
 
 def run_reference(args, w):
@@ -653,6 +702,15 @@ def main():
         st = kda.last_device_status(d["ws"], stream)
         if st != kda.OK:
             raise kda.KDAError(st, "device status after the timed steps")
+    launch_us = sorted(1e6 * x for x in launch_s)
+    launch_stats = {"mean": 1e6 * sum(launch_s) / K, "median": statistics.median(launch_us),
+                    "min": launch_us[0], "max": launch_us[-1], "samples": K}
+    # the same call under CUDA-graph replay (after the timed region, outside it)
+    graph = graph_timing(step, stream) if world == 1 else None
+    for d in sets:
+        st = kda.last_device_status(d["ws"], stream)
+        if st != kda.OK:
+            raise kda.KDAError(st, "device status after the graph replays")
 
     # ---- end to end through the C ABI with host buffers.  Every step copies its inputs
     #      from pinned host memory and reads its out and final_state back; steps are
@@ -745,9 +803,13 @@ def main():
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": KE},
         "gpu_launches": K * launches_per_step,
         "clocks": clocks,
+        "launch_us": launch_stats,
     }
+    if graph is not None:
+        line["graph"] = graph
     if world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(host, w)
+        line["cpu_baseline_1thread"] = cpu_baseline_one_thread(host, w)
     print(json.dumps(line), flush=True)
     if world > 1:
         torch.distributed.destroy_process_group()

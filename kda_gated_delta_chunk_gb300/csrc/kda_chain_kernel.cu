@@ -402,18 +402,19 @@ bool make_chain_maps(ChainMaps* m, const Params& p, int dv) {
 
 template <int DV>
 cudaError_t launch_chain_dv(const Params& p, cudaStream_t stream) {
-  static bool attr_set[64] = {};
+  static PerDeviceOnce attr_once;   // the shared-memory attribute, once per device
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   constexpr int smem = ChainSmem<DV>::BYTES;
-  if (dev >= 0 && dev < 64 && !attr_set[dev]) {
+  e = attr_once.run(dev, [&]() -> cudaError_t {
     for (auto fn : {kda_chain_kernel<DV, false>, kda_chain_kernel<DV, true>}) {
-      e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-      if (e != cudaSuccess) return e;
+      const cudaError_t r = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+      if (r != cudaSuccess) return r;
     }
-    attr_set[dev] = true;
-  }
+    return cudaSuccess;
+  });
+  if (e != cudaSuccess) return e;
   ChainMaps maps;
   if (!make_chain_maps(&maps, p, DV)) return cudaErrorInvalidValue;
   const long long blocks = (long long)p.num_seqs * p.heads * (128 / DV);

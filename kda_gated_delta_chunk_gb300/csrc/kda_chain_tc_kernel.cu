@@ -409,17 +409,18 @@ typedef CUresult (*EncodeTiledFn3)(CUtensorMap*, CUtensorMapDataType, cuuint32_t
 }  // namespace
 
 cudaError_t launch_chain_tc(const Params& p, cudaStream_t stream) {
-  static bool attr_set[64] = {};
+  static PerDeviceOnce attr_once;   // the shared-memory attribute, once per device
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  if (dev >= 0 && dev < 64 && !attr_set[dev]) {
+  e = attr_once.run(dev, [&]() -> cudaError_t {
     for (auto fn : {kda_chain_tc_kernel<false>, kda_chain_tc_kernel<true>}) {
       e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM3_BYTES);
       if (e != cudaSuccess) return e;
     }
-    attr_set[dev] = true;
-  }
+    return cudaSuccess;
+  });
+  if (e != cudaSuccess) return e;
   const long long blocks = (long long)p.num_seqs * p.heads;
   if (blocks <= 0) return cudaSuccess;
   if (blocks > 0x7fffffffLL) return cudaErrorInvalidValue;

@@ -709,16 +709,17 @@ bool make_in_map(EncodeTiledFnK enc, CUtensorMap* m, const void* base, int64_t T
 }  // namespace
 
 cudaError_t launch_kside(const Params& p, cudaStream_t stream) {
-  static bool attr_set[64] = {};
+  static PerDeviceOnce attr_once;   // the shared-memory attribute, once per device
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  if (dev >= 0 && dev < 64 && !attr_set[dev]) {
+  e = attr_once.run(dev, [&]() -> cudaError_t {
     e = cudaFuncSetAttribute(kda_kside_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              K_SMEM_BYTES);
     if (e != cudaSuccess) return e;
-    attr_set[dev] = true;
-  }
+    return cudaSuccess;
+  });
+  if (e != cudaSuccess) return e;
   const int64_t items = split_slots(p.total_tokens, p.num_seqs) * p.heads;
   if (items <= 0 || p.total_tokens == 0) return cudaSuccess;
   if (items > 0x7fffffffLL - 4096) return cudaErrorInvalidValue;
@@ -739,16 +740,17 @@ cudaError_t launch_kside(const Params& p, cudaStream_t stream) {
 // launched as its programmatic dependent: they start once every fused CTA has cleared its
 // claim words, run beside it, and the grid completes after it.
 cudaError_t launch_kside_helpers(const Params& p, cudaStream_t stream) {
-  static bool attr_set[64] = {};
+  static PerDeviceOnce attr_once;   // the shared-memory attribute, once per device
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  if (dev >= 0 && dev < 64 && !attr_set[dev]) {
+  e = attr_once.run(dev, [&]() -> cudaError_t {
     e = cudaFuncSetAttribute(kda_kside_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              K_SMEM_BYTES);
     if (e != cudaSuccess) return e;
-    attr_set[dev] = true;
-  }
+    return cudaSuccess;
+  });
+  if (e != cudaSuccess) return e;
   const int64_t free_sms = (int64_t)p.sm_count - (int64_t)p.num_seqs * p.heads;
   if (p.total_tokens == 0 || free_sms <= 0 || p.num_seqs > kHelperMaxSeqs ||
       ((p.total_tokens + C - 1) / C) * p.num_seqs * p.heads >= (1 << 30))

@@ -197,19 +197,20 @@ int proj_smem_first() { return 2 * PM * PKS * 2 + 4 * 256 * 4 + 16; }
 cudaError_t launch_proj(const void* x, int64_t ldx, const void* w_ab, const void* w_b, void* y,
                         int64_t ldy, void* z, int64_t ldz, int32_t m, int32_t k, int32_t n_ab,
                         int32_t r, int32_t n_b, void* workspace, cudaStream_t stream) {
-  static bool attr_set[64] = {};
+  static PerDeviceOnce attr_once;   // the shared-memory attribute, once per device
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   const int smem1 = proj_smem_first();
-  if (dev >= 0 && dev < 64 && !attr_set[dev]) {
+  e = attr_once.run(dev, [&]() -> cudaError_t {
     e = cudaFuncSetAttribute(kda_proj_n_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem1);
     if (e != cudaSuccess) return e;
     e = cudaFuncSetAttribute(kda_proj_k_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              2 * PM * (512 + 8) * 2);
     if (e != cudaSuccess) return e;
-    attr_set[dev] = true;
-  }
+    return cudaSuccess;
+  });
+  if (e != cudaSuccess) return e;
   ProjParams pp;
   pp.x = static_cast<const __nv_bfloat16*>(x);
   pp.w_ab = static_cast<const __nv_bfloat16*>(w_ab);

@@ -99,16 +99,17 @@ bool make_map(EncodeTiledFn enc, CUtensorMap* m, const void* base, int64_t T, in
 void* tensor_map_encoder() { return reinterpret_cast<void*>(encode_fn()); }
 
 cudaError_t launch_tc(const Params& p, cudaStream_t stream) {
-  static bool attr_set[64] = {};
+  static PerDeviceOnce attr_once;   // the shared-memory attribute, once per device
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  if (dev >= 0 && dev < 64 && !attr_set[dev]) {
+  e = attr_once.run(dev, [&]() -> cudaError_t {
     e = cudaFuncSetAttribute(kda_tc_chunk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              SMEM_BYTES);
     if (e != cudaSuccess) return e;
-    attr_set[dev] = true;
-  }
+    return cudaSuccess;
+  });
+  if (e != cudaSuccess) return e;
   const long long blocks = (long long)p.num_seqs * p.heads * p.vsplit;
   if (blocks <= 0) return cudaSuccess;
   if (blocks > 0x7fffffffLL) return cudaErrorInvalidValue;

@@ -10,16 +10,17 @@ namespace kda {
 cudaError_t launch_tc_rowmap(const Params& p, unsigned blocks, const CUtensorMap& mq,
                              const CUtensorMap& mk, const CUtensorMap& mg, const CUtensorMap& mv,
                              cudaStream_t stream) {
-  static bool attr_set[64] = {};
+  static PerDeviceOnce attr_once;   // the shared-memory attribute, once per device
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  if (dev >= 0 && dev < 64 && !attr_set[dev]) {
+  e = attr_once.run(dev, [&]() -> cudaError_t {
     e = cudaFuncSetAttribute(kda_tc_chunk_kernel_rowmap,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES_MAP);
     if (e != cudaSuccess) return e;
-    attr_set[dev] = true;
-  }
+    return cudaSuccess;
+  });
+  if (e != cudaSuccess) return e;
   kda_tc_chunk_kernel_rowmap<<<blocks, NT, SMEM_BYTES_MAP, stream>>>(p, mq, mk, mg, mv);
   return cudaGetLastError();
 }
