@@ -42,6 +42,8 @@
 // KDA_ERR_DEVICE_TIMEOUT and both warp groups leave their loops in step.
 #include <cuda.h>
 
+#include <type_traits>
+
 #include "kda_internal.cuh"
 #include "kda_sm100.cuh"
 #include "kda_tc_common.cuh"
@@ -618,16 +620,20 @@ __global__ void __launch_bounds__(PNT, 1)
     const float gate_scale = expf(p.A_log[h]);
     const float lb2 = p.lower_bound * kLog2e;
     const float sg = -gate_scale * kLog2e;   // sigmoid argument, log2 units: sg (g + dt_bias)
-    float sgd[4];
-#pragma unroll
-    for (int e = 0; e < 4; ++e) sgd[e] = sg * p.dt_bias[h * PD + 4 * o4 + e];
+    const float2 sgd01 = make_float2(sg * p.dt_bias[h * PD + 4 * o4], sg * p.dt_bias[h * PD + 4 * o4 + 1]);
+    const float2 sgd23 = make_float2(sg * p.dt_bias[h * PD + 4 * o4 + 2], sg * p.dt_bias[h * PD + 4 * o4 + 3]);
+    // byte offsets of this thread's 8-byte piece (channels 4 o4 .. 4 o4 + 3) of row 4 j + i in a
+    // 128-byte-row SW128 tile: the row part (rows 4j .. 4j + 3 share (r & 7) >> 2 = j & 1) and
+    // the 64-column block part, which depends on the tile's row count
+    const uint32_t xo = (uint32_t)(((o4 & 15) >> 1) ^ (4 * (j & 1)));
+    auto in8_row = [&](int i) -> uint32_t {
+      return (uint32_t)((4 * j + i) * 128) + ((xo ^ (uint32_t)i) << 4) + (uint32_t)((o4 & 1) << 3);
+    };
+    const uint32_t in_row = (uint32_t)((o4 >> 4) * 8192);      // q, k, g input tiles (64 rows)
+    const uint32_t rkq_col = (uint32_t)((o4 >> 4) * 16384);    // [Kr; Qr], [Kg; Qg] (128 rows)
+    const uint32_t ckc_col = (uint32_t)((o4 >> 4) * 12288);    // [Kc; Kc2] (96 rows)
     int in_pend = 0;      // tma thread: an input load issued and not waited (its parity + 1)
     int kmma_pend = 0;    // the A|QK MMA issued and not waited (its parity + 1)
-    // byte offset of the 8 bytes holding columns 4 o4 .. 4 o4 + 3 of row r of an input tile
-    auto in8 = [&](int r) -> uint32_t {
-      return (uint32_t)((o4 >> 4) * 8192 + r * 128 + ((((o4 & 15) >> 1) ^ (r & 7)) << 4) +
-                        ((o4 & 1) << 3));
-    };
     auto ld8b = [&](uint32_t off) -> uint2 { return *reinterpret_cast<const uint2*>(sm + off); };
     auto st8b = [&](uint32_t off, uint32_t a, uint32_t b) {
       *reinterpret_cast<uint2*>(sm + off) = make_uint2(a, b);
@@ -671,37 +677,51 @@ __global__ void __launch_bounds__(PNT, 1)
       if (bar_any(1, 512, !ok)) { failed = true; site = 20; break; }
       if (tma_thread) in_pend = 0;
       PSTAMP(kt == 0, c, 16);
+      {
+        // two channels per packed fp32x2 operation throughout
+        const float2 sg2 = make_float2(sg, sg), lb22 = make_float2(lb2, lb2);
+        const float2 one2 = make_float2(1.0f, 1.0f), zero2 = make_float2(0.0f, 0.0f);
+        float2 run0 = zero2, run1 = zero2;   // running cumsums, channels 0-1 and 2-3
+        float v[8];                           // row sums of squares: q rows 0-3, k rows 0-3
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const int r = 4 * j + i;
-        const bool valid = r < L;
-        const uint32_t off = in8(r);
-        const uint2 gv = ld8b(PS_ING + off);
-        const uint32_t gw[2] = {gv.x, gv.y};
-#pragma unroll
-        for (int pq = 0; pq < 2; ++pq) {
-          const float2 gf = unpack_bf16x2(gw[pq]);
-          float a0 = lb2 * rcpf(1.0f + ex2f(fmaf(gf.x, sg, sgd[2 * pq])));
-          float a1 = lb2 * rcpf(1.0f + ex2f(fmaf(gf.y, sg, sgd[2 * pq + 1])));
-          a0 = valid ? a0 : 0.0f;
-          a1 = valid ? a1 : 0.0f;
-          cl[i][2 * pq] = (i ? cl[i - 1][2 * pq] : 0.0f) + a0;
-          cl[i][2 * pq + 1] = (i ? cl[i - 1][2 * pq + 1] : 0.0f) + a1;
+        for (int i = 0; i < 4; ++i) {
+          const bool valid = 4 * j + i < L;   // the same for the whole warp
+          const uint32_t off = in_row + in8_row(i);
+          const uint2 gv = ld8b(PS_ING + off);
+          const float2 z0 = __ffma2_rn(unpack_bf16x2(gv.x), sg2, sgd01);
+          const float2 z1 = __ffma2_rn(unpack_bf16x2(gv.y), sg2, sgd23);
+          const float2 d0 = __fadd2_rn(make_float2(ex2f(z0.x), ex2f(z0.y)), one2);
+          const float2 d1 = __fadd2_rn(make_float2(ex2f(z1.x), ex2f(z1.y)), one2);
+          float2 a0 = __fmul2_rn(make_float2(rcpf(d0.x), rcpf(d0.y)), lb22);
+          float2 a1 = __fmul2_rn(make_float2(rcpf(d1.x), rcpf(d1.y)), lb22);
+          if (!valid) a0 = a1 = zero2;
+          run0 = __fadd2_rn(run0, a0);
+          run1 = __fadd2_rn(run1, a1);
+          cl[i][0] = run0.x; cl[i][1] = run0.y; cl[i][2] = run1.x; cl[i][3] = run1.y;
+          const uint2 qv = ld8b(PS_INQ + off), kv = ld8b(PS_INK + off);
+          const float2 q01 = unpack_bf16x2(qv.x), q23 = unpack_bf16x2(qv.y);
+          const float2 k01 = unpack_bf16x2(kv.x), k23 = unpack_bf16x2(kv.y);
+          const float2 sq = __ffma2_rn(q23, q23, __fmul2_rn(q01, q01));
+          const float2 sk = __ffma2_rn(k23, k23, __fmul2_rn(k01, k01));
+          v[i] = valid ? sq.x + sq.y : 0.0f;
+          v[4 + i] = valid ? sk.x + sk.y : 0.0f;
         }
-        const uint2 qv = ld8b(PS_INQ + off), kv = ld8b(PS_INK + off);
-        const float2 q0 = unpack_bf16x2(qv.x), q1 = unpack_bf16x2(qv.y);
-        const float2 k0 = unpack_bf16x2(kv.x), k1 = unpack_bf16x2(kv.y);
-        const float sq = fmaf(q0.x, q0.x, fmaf(q0.y, q0.y, fmaf(q1.x, q1.x, q1.y * q1.y)));
-        const float sk = fmaf(k0.x, k0.x, fmaf(k0.y, k0.y, fmaf(k1.x, k1.x, k1.y * k1.y)));
-        // the row's two sums over the 32 channel quads of the warp: lanes with bit 4 clear
-        // end with q's, lanes with it set with k's
-        const bool up = (lane & 16) != 0;
-        float v = (up ? sk : sq) + __shfl_xor_sync(0xffffffffu, up ? sq : sk, 16);
-        v += __shfl_xor_sync(0xffffffffu, v, 8);
-        v += __shfl_xor_sync(0xffffffffu, v, 4);
-        v += __shfl_xor_sync(0xffffffffu, v, 2);
-        v += __shfl_xor_sync(0xffffffffu, v, 1);
-        if ((lane & 15) == 0) SS[(up ? 64 : 0) + r] = valid ? v : 0.0f;
+        // the eight row sums over the warp's 32 channel quads, by a butterfly that halves the
+        // values each lane carries at each of the first three steps: lane bit 4 picks q or k,
+        // bit 3 the row pair, bit 2 the row; lanes with bits 0-1 clear end with a full sum
+        const bool h4 = (lane & 16) != 0, h3 = (lane & 8) != 0, h2 = (lane & 4) != 0;
+        float w4[4];
+#pragma unroll
+        for (int m = 0; m < 4; ++m)
+          w4[m] = (h4 ? v[4 + m] : v[m]) + __shfl_xor_sync(0xffffffffu, h4 ? v[m] : v[4 + m], 16);
+        float w2[2];
+#pragma unroll
+        for (int m = 0; m < 2; ++m)
+          w2[m] = (h3 ? w4[2 + m] : w4[m]) + __shfl_xor_sync(0xffffffffu, h3 ? w4[m] : w4[2 + m], 8);
+        float w1 = (h2 ? w2[1] : w2[0]) + __shfl_xor_sync(0xffffffffu, h2 ? w2[0] : w2[1], 4);
+        w1 += __shfl_xor_sync(0xffffffffu, w1, 2);
+        w1 += __shfl_xor_sync(0xffffffffu, w1, 1);
+        if ((lane & 3) == 0) SS[(h4 ? 64 : 0) + 4 * j + (h3 ? 2 : 0) + (h2 ? 1 : 0)] = w1;
       }
       // quad totals of the cumsum -> GT[j][channel]
       *reinterpret_cast<float4*>(GT + j * 128 + 4 * o4) =
@@ -754,19 +774,11 @@ __global__ void __launch_bounds__(PNT, 1)
       group_sync(1, 512);
       PSTAMP(kt == 0, c, 18);
 
-      // ---- K3: operand tiles [Kr; Qr], [Kc; Kc2] (own), Kg, Qg (stage)
+      // ---- K3: operand tiles [Kr; Qr], [Kc; Kc2] (own), Kg, Qg (stage).  The warp's rows lie in
+      //      one 32-token block (bsel), so the block's variant is chosen once per warp.
       {
-        float mE[4], fa[4], fc[4], fq[4];
-        {
-          auto ld4f = [&](const float* src, float (&dst)[4]) {
-            const float4 a = ld4(src);
-            dst[0] = a.x; dst[1] = a.y; dst[2] = a.z; dst[3] = a.w;
-          };
-          ld4f(GT + j * 128 + 4 * o4, mE);
-          ld4f(FAC + (bsel ? 4 : 0) * 128 + 4 * o4, fa);
-          ld4f(FAC + 2 * 128 + 4 * o4, fc);
-          ld4f(FAC + (bsel ? 5 : 3) * 128 + 4 * o4, fq);
-        }
+        const float4 mE4 = ld4(GT + j * 128 + 4 * o4);
+        const float2 nm01 = make_float2(-mE4.x, -mE4.y), nm23 = make_float2(-mE4.z, -mE4.w);
         PSTAMP(kt == 0, c, 13);
         // the chain has finished reading [Kg; Qg] of the previous chunk
         if (c > 0) {
@@ -774,45 +786,62 @@ __global__ void __launch_bounds__(PNT, 1)
           if (bar_any(1, 512, !ok)) { failed = true; site = 21; break; }
         }
         PSTAMP(kt == 0, c, 19);
+        // block 0: Kc2 = Kc 2^(G31 - anchor0) 2^(anchor1 - G31), Kg = Kr 2^anchor0;
+        // block 1: Kg = Kr 2^(anchor1 - G31) 2^G31 (Kc2 has no block-1 rows).  The factors are
+        // applied one after the other, never multiplied together first: their product alone
+        // can leave the fp32 range (2^(anchor1 - anchor0) under strong decay) while the
+        // operand it scales stays representable.
+        auto tiles = [&](auto blk) {
+          constexpr bool B0 = decltype(blk)::value;
+          const float4 fc4 = ld4(FAC + 2 * 128 + 4 * o4);
+          const float4 fq4 = ld4(FAC + (B0 ? 3 : 5) * 128 + 4 * o4);
+          const float4 fa4 = ld4(FAC + 0 * 128 + 4 * o4);
+          // Kg/Qg: (E [fc]) fq; Kc2: (Ei fa) fc
+          const float2 fc01 = make_float2(fc4.x, fc4.y), fc23 = make_float2(fc4.z, fc4.w);
+          const float2 fq01 = make_float2(fq4.x, fq4.y), fq23 = make_float2(fq4.z, fq4.w);
+          const float2 fa01 = make_float2(fa4.x, fa4.y), fa23 = make_float2(fa4.z, fa4.w);
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const int r = 4 * j + i;
-          const bool valid = r < L;
-          const uint32_t off = in8(r);
-          uint2 qv = ld8b(PS_INQ + off), kv = ld8b(PS_INK + off);
-          if (!valid) qv = kv = make_uint2(0, 0);
-          const uint32_t rq = RSC[r], rk = RSC[64 + r];
-          const uint32_t q2[2] = {bmul2(qv.x, rq), bmul2(qv.y, rq)};
-          const uint32_t k2[2] = {bmul2(kv.x, rk), bmul2(kv.y, rk)};
-          uint32_t kr[2], qr[2], kc[2], kc2[2], kg[2], qg[2];
+          for (int i = 0; i < 4; ++i) {
+            const int r = 4 * j + i;
+            const uint32_t ro = in8_row(i);
+            uint2 qv = ld8b(PS_INQ + in_row + ro), kv = ld8b(PS_INK + in_row + ro);
+            if (r >= L) qv = kv = make_uint2(0, 0);
+            const uint32_t rq = RSC[r], rk = RSC[64 + r];
+            const uint32_t q2[2] = {bmul2(qv.x, rq), bmul2(qv.y, rq)};
+            const uint32_t k2[2] = {bmul2(kv.x, rk), bmul2(kv.y, rk)};
+            uint32_t kr[2], qr[2], kc[2], kc2[2], kg[2], qg[2];
 #pragma unroll
-          for (int pq = 0; pq < 2; ++pq) {
-            const int e0 = 2 * pq, e1 = 2 * pq + 1;
-            const float x0 = cl[i][e0] - mE[e0], x1 = cl[i][e1] - mE[e1];
-            const float E0 = ex2f(x0), E1 = ex2f(x1);
-            const float Ei0 = ex2f(-x0), Ei1 = ex2f(-x1);
-            const uint32_t E2 = pack_bf16x2(E0, E1), Ei2 = pack_bf16x2(Ei0, Ei1);
-            kr[pq] = bmul2(k2[pq], E2);
-            qr[pq] = bmul2(q2[pq], E2);
-            kc[pq] = bmul2(k2[pq], Ei2);
-            uint32_t gq;
-            if (bsel == 0) {
-              kc2[pq] = bmul2(k2[pq], pack_bf16x2((Ei0 * fa[e0]) * fc[e0], (Ei1 * fa[e1]) * fc[e1]));
-              gq = pack_bf16x2(E0 * fq[e0], E1 * fq[e1]);
-            } else {
-              gq = pack_bf16x2((E0 * fc[e0]) * fq[e0], (E1 * fc[e1]) * fq[e1]);
-              kc2[pq] = 0u;
+            for (int pq = 0; pq < 2; ++pq) {
+              const float2 x = __fadd2_rn(make_float2(cl[i][2 * pq], cl[i][2 * pq + 1]),
+                                          pq ? nm23 : nm01);
+              const float2 E = make_float2(ex2f(x.x), ex2f(x.y));
+              const float2 Ei = make_float2(ex2f(-x.x), ex2f(-x.y));
+              const uint32_t E2 = pack_bf16x2(E.x, E.y), Ei2 = pack_bf16x2(Ei.x, Ei.y);
+              kr[pq] = bmul2(k2[pq], E2);
+              qr[pq] = bmul2(q2[pq], E2);
+              kc[pq] = bmul2(k2[pq], Ei2);
+              const float2 gq = B0 ? __fmul2_rn(E, pq ? fq23 : fq01)
+                                   : __fmul2_rn(__fmul2_rn(E, pq ? fc23 : fc01), pq ? fq23 : fq01);
+              const uint32_t gq2 = pack_bf16x2(gq.x, gq.y);
+              if (B0) {
+                const float2 cc = __fmul2_rn(__fmul2_rn(Ei, pq ? fa23 : fa01), pq ? fc23 : fc01);
+                kc2[pq] = bmul2(k2[pq], pack_bf16x2(cc.x, cc.y));
+              }
+              qg[pq] = bmul2(q2[pq], gq2);
+              kg[pq] = bmul2(k2[pq], gq2);
             }
-            qg[pq] = bmul2(q2[pq], gq);
-            kg[pq] = bmul2(k2[pq], gq);
+            st8b(PS_RKQ + rkq_col + ro, kr[0], kr[1]);
+            st8b(PS_RKQ + rkq_col + 8192 + ro, qr[0], qr[1]);
+            st8b(PS_CKC + ckc_col + ro, kc[0], kc[1]);
+            if (B0) st8b(PS_CKC + ckc_col + 8192 + ro, kc2[0], kc2[1]);
+            st8b(PS_WQ + rkq_col + ro, kg[0], kg[1]);
+            st8b(PS_WQ + rkq_col + 8192 + ro, qg[0], qg[1]);
           }
-          st8b(PS_RKQ + kmajor_off(r, 4 * o4, 128), kr[0], kr[1]);
-          st8b(PS_RKQ + kmajor_off(64 + r, 4 * o4, 128), qr[0], qr[1]);
-          st8b(PS_CKC + kmajor_off(r, 4 * o4, 96), kc[0], kc[1]);
-          if (bsel == 0) st8b(PS_CKC + kmajor_off(64 + r, 4 * o4, 96), kc2[0], kc2[1]);
-          st8b(PS_WQ + kmajor_off(r, 4 * o4, 128), kg[0], kg[1]);
-          st8b(PS_WQ + kmajor_off(64 + r, 4 * o4, 128), qg[0], qg[1]);
-        }
+        };
+        if (bsel == 0)
+          tiles(std::true_type{});
+        else
+          tiles(std::false_type{});
         PSTAMP(kt == 0, c, 20);
         fence_proxy_async();
         group_sync(1, 512);
@@ -887,16 +916,20 @@ __global__ void __launch_bounds__(PNT, 1)
         const int kb = kk >> 2;   // 32-token block
         const float4 fa4 = ld4(FAC + (kb ? 4 : 0) * 128 + 4 * o4);
         const float4 fb4 = ld4(FAC + 1 * 128 + 4 * o4);
-        // block 0: 2^(G31 - G) then 2^(G63 - G31); block 1: 2^(G63 - G47)
-        const float f0 = kb ? fa4.x : fa4.x * fb4.x, f1 = kb ? fa4.y : fa4.y * fb4.y;
-        const float f2 = kb ? fa4.z : fa4.z * fb4.z, f3 = kb ? fa4.w : fa4.w * fb4.w;
+        // block 0: 2^(G31 - anchor0) then 2^(G63 - G31), one after the other (their product
+        // alone can underflow); block 1: 2^(G63 - anchor1)
+        const float2 fa01 = make_float2(fa4.x, fa4.y), fa23 = make_float2(fa4.z, fa4.w);
+        const float2 fb01 = make_float2(fb4.x, fb4.y), fb23 = make_float2(fb4.z, fb4.w);
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
           const int r = 8 * kk + i;
           const uint2 kcv = ld8b(PS_CKC + kmajor_off(r, 4 * o4, 96));
-          const float2 a = unpack_bf16x2(kcv.x), b = unpack_bf16x2(kcv.y);
-          st8b(PS_KE + mnmajor_off(4 * o4, r, 8192), pack_bf16x2(a.x * f0, a.y * f1),
-               pack_bf16x2(b.x * f2, b.y * f3));
+          float2 a = __fmul2_rn(unpack_bf16x2(kcv.x), fa01), b = __fmul2_rn(unpack_bf16x2(kcv.y), fa23);
+          if (!kb) {
+            a = __fmul2_rn(a, fb01);
+            b = __fmul2_rn(b, fb23);
+          }
+          st8b(PS_KE + mnmajor_off(4 * o4, r, 8192), pack_bf16x2(a.x, a.y), pack_bf16x2(b.x, b.y));
         }
         fence_proxy_async();
       }

@@ -220,6 +220,41 @@ def test_extreme_gates(oracle_mod, kernel, lb, shift):
     check(oracle_mod, inp, out, fin, tag=f"gates lb={lb} shift={shift} k{kernel}")
 
 
+@pytest.mark.parametrize("kernel", KERNELS)
+def test_strong_uniform_decay_keeps_adjacent_terms(oracle_mod, kernel):
+    """Every channel decays by about 2^-5 per token (lb = -5, sigmoid 0.7), so the anchors of
+    the two 32-token blocks lie about 2^-160 apart: a factor formed as their ratio alone
+    underflows fp32, while each term it would scale (a token and its neighbour) stays large.
+    q = k (one shared key row per head) and values only at token 31 make those neighbour terms
+    carry the second block's outputs: a kernel that drops them gets those rows wrong by 100%
+    of their size, against bf16-level (< 1%) relative error when they are kept."""
+    w = W.custom([70, 64], 2, seed=35, lower_bound=-5.0)
+    inp = W.make_inputs(w)
+    T, H, D = inp["q"].shape
+    gen = torch.Generator().manual_seed(36)
+    krow = torch.randn(H, D, generator=gen)
+    inp["k"] = krow.expand(T, H, D).to(torch.bfloat16).contiguous()
+    inp["q"] = inp["k"].clone()
+    # (g + dt_bias) e^A_log = 0.85 in every channel: sigmoid 0.70, decay 5 * 0.70 nats a token
+    x = 0.85 / torch.exp(inp["A_log"].float())[:, None] - inp["dt_bias"].float()
+    inp["g"] = x[None].expand(T, H, D).to(torch.bfloat16).contiguous()
+    v = torch.zeros_like(inp["v"])
+    starts = inp["cu_seqlens"][:-1].tolist()
+    for st in starts:
+        v[st + 31] = inp["v"][st + 31]
+    inp["v"] = v
+    out, fin = run_gpu(inp, kernel)
+    check(oracle_mod, inp, out, fin, tag=f"strong uniform decay k{kernel}")
+    rows, o_ref, _ = oracle_sub(oracle_mod, inp, range(len(starts)), range(H), False)
+    o_gpu = f64(out.cpu().index_select(0, rows))
+    pos = {int(r): i for i, r in enumerate(rows.tolist())}
+    for n, st in enumerate(starts):
+        idx = [pos[t] for t in range(st + 32, min(st + 64, int(inp["cu_seqlens"][n + 1])))]
+        ref, got = o_ref[idx], o_gpu[idx]
+        rel = np.linalg.norm(got - ref) / np.linalg.norm(ref)
+        assert rel < 0.05, (n, rel)
+
+
 def fused_views(d, extra_cols=64, beta_pad=3):
     """q, k, v, g as views into one fused [T, 4 * H * 128 + extra_cols] buffer and beta as a
     view into a wider [T, H + beta_pad] buffer (the layout of a fused projection output)."""
