@@ -110,7 +110,7 @@ constexpr int B_KMMA = 5;    // k-side A|QK MMA done
 constexpr int B_G1A = 6;     // chain: [X^T | O^T] done
 constexpr int B_G1B = 7;     // chain: U^T done
 constexpr int B_G2 = 8;      // chain: O^T, S^T updates done
-constexpr int B_FREEC = 9;   // chain done with T (fp32) and T diag(b), T (bf16)
+constexpr int B_FREEC = 9;   // chain done with T (fp32), which it turns into its own bf16 operands
 constexpr int B_DFREE = 10;  // chain done with the QK rows of the k-side's D (TMEM)
 
 // ---- tensor memory columns (fp32 unless noted; lane = value channel, or row for D)
@@ -415,6 +415,7 @@ __global__ void __launch_bounds__(PNT, 1)
         }
       }
       if (bar_any(4, 128, !ok)) { failed = true; site = 40; break; }
+      if (tid == 0) mbar_arrive(bar(B_FREEC));   // T (fp32) has been read by all four warps
       PSTAMP(tid == 0, c, 4);
       tc_fence_after();
       // C2: X_b = bf16(X^T diag(-b inv_k)), 32 tokens at a time
@@ -480,7 +481,6 @@ __global__ void __launch_bounds__(PNT, 1)
         ok = wait_spin(bar(B_G1B), par);
         if (ok) {
           pend &= ~4;
-          mbar_arrive(bar(B_FREEC));   // T diag(b), T are free
           PSTAMP(true, c, 28);
           if (c + 1 < nch) {           // v is free: the next chunk's v
             mbar_expect_tx(bar(B_V), 16384);
