@@ -307,11 +307,11 @@ def run_reference(args, w):
 
 # phase stamps of the pipelined kernel: 32 slots per chunk (see kda_pipe_kernel.cu)
 # chain stamp slots (CTA 0, thread 0) and the k-side ones (thread 128); 32 slots per chunk
-CHAIN_SLOTS = {0: "stage full", 2: "S_b stored", 3: "G1a issued", 12: "S decayed",
-               26: "T operands stored", 4: "G1a done", 5: "X_b stored", 28: "G1b done (thread 0)",
-               27: "QK operand stored", 6: "chain group past G1b", 7: "U_b stored", 8: "G2 done",
-               10: "O stored"}
-CHAIN_ORDER = [0, 2, 3, 12, 26, 4, 5, 28, 27, 6, 7, 8, 10]
+CHAIN_SLOTS = {0: "stage part A full", 2: "v ready", 3: "G1a issued", 12: "S decayed",
+               4: "G1a done", 5: "X_b stored", 26: "T full, T operands stored",
+               28: "G1b done (thread 0)", 27: "QK operand stored", 6: "chain group past G1b",
+               7: "U_b stored", 8: "G2 done", 10: "O stored"}
+CHAIN_ORDER = [0, 2, 3, 12, 4, 5, 26, 28, 27, 6, 7, 8, 10]
 KSIDE_SLOTS = {16: "inputs landed", 17: "gate and norms", 18: "factors", 13: "factor loads",
                19: "stage parts free", 20: "tile rows done", 21: "tiles fenced",
                22: "A|QK MMA done", 1: "Ke parts free", 23: "A loaded", 24: "N, Ke stored",

@@ -112,6 +112,7 @@ constexpr int B_G1B = 7;     // chain: U^T done
 constexpr int B_G2 = 8;      // chain: O^T, S^T updates done
 constexpr int B_FREEC = 9;   // chain done with T (fp32), which it turns into its own bf16 operands
 constexpr int B_DFREE = 10;  // chain done with the QK rows of the k-side's D (TMEM)
+constexpr int B_FULLA = 11;  // the first part of the stage ([Kg; Qg], the chunk's vectors)
 
 // ---- tensor memory columns (fp32 unless noted; lane = value channel, or row for D)
 constexpr uint32_t TM_XU = 0;     // X^T, then U^T   64 cols (col = token)
@@ -253,6 +254,7 @@ __global__ void __launch_bounds__(PNT, 1)
     mbar_init(bar(B_G2), 1);
     mbar_init(bar(B_FREEC), 1);
     mbar_init(bar(B_DFREE), 1);
+    mbar_init(bar(B_FULLA), 1);
     mbar_fence_init();
   }
   if (warp == 0) {
@@ -335,11 +337,12 @@ __global__ void __launch_bounds__(PNT, 1)
       const float* vec = vecs + (c % 3) * kVecFloats;
       cfail = c;
 
-      // C0: the stage and v of chunk c have landed (thread 0 waits; the group parks on the
-      //     barrier that carries the outcome)
+      // C0: the first part of the stage ([Kg; Qg] and the vectors) and v of chunk c have
+      //     landed (thread 0 waits; the group parks on the barrier that carries the outcome);
+      //     T comes later, once the k-side has inverted it
       bool ok = true;
       if (tid == 0) {
-        ok = wait_phase(bar(B_FULL), par);
+        ok = wait_phase(bar(B_FULLA), par);
         const bool v_ok = wait_phase(bar(B_V), par);
         if (v_ok) pend &= ~1;
         ok = ok && v_ok;
@@ -385,28 +388,7 @@ __global__ void __launch_bounds__(PNT, 1)
         tmem_st32(tmem + lb + TM_S + cb * 32, x);
       }
       PSTAMP(tid == 0, c, 12);
-      // C1c, also while G1a runs: T (fp32, from the k-side) -> the bf16 operands of G1b,
-      //     T diag(b) and T
-      {
-        const float* Tm = reinterpret_cast<const float*>(sm + PS_TM);
-        const float* bv = vec + 320;
-#pragma unroll
-        for (int it = tid; it < 512; it += 128) {
-          const int r = it & 63, c8 = it >> 6;   // row r, columns 8 c8 .. 8 c8 + 7
-          const float4 ta = ld4(Tm + r * NS + 8 * c8), tb = ld4(Tm + r * NS + 8 * c8 + 4);
-          const float4 ba = ld4(bv + 8 * c8), bb = ld4(bv + 8 * c8 + 4);
-          const uint32_t off = kmajor_off(r, 8 * c8, 64);
-          st_u128(sm, PS_TB + off,
-                  make_uint4(pack_bf16x2(ta.x * ba.x, ta.y * ba.y), pack_bf16x2(ta.z * ba.z, ta.w * ba.w),
-                             pack_bf16x2(tb.x * bb.x, tb.y * bb.y), pack_bf16x2(tb.z * bb.z, tb.w * bb.w)));
-          st_u128(sm, PS_TT + off,
-                  make_uint4(pack_bf16x2(ta.x, ta.y), pack_bf16x2(ta.z, ta.w),
-                             pack_bf16x2(tb.x, tb.y), pack_bf16x2(tb.z, tb.w)));
-        }
-      }
-      fence_proxy_async();   // read by G1b
       tmem_wait_st();
-      PSTAMP(tid == 0, c, 26);
       if (tid == 0) {
         ok = wait_spin(bar(B_G1A), par);
         if (ok) {
@@ -415,7 +397,6 @@ __global__ void __launch_bounds__(PNT, 1)
         }
       }
       if (bar_any(4, 128, !ok)) { failed = true; site = 40; break; }
-      if (tid == 0) mbar_arrive(bar(B_FREEC));   // T (fp32) has been read by all four warps
       PSTAMP(tid == 0, c, 4);
       tc_fence_after();
       // C2: X_b = bf16(X^T diag(-b inv_k)), 32 tokens at a time
@@ -436,11 +417,35 @@ __global__ void __launch_bounds__(PNT, 1)
         tmem_st16(tmem + lb + TM_XB + hh * 16, pk);
       }
       tmem_wait_st();
+      PSTAMP(tid == 0, c, 5);
+      if (tid == 0) ok = wait_phase(bar(B_FULL), par);   // T of chunk c
+      if (bar_any(4, 128, !ok)) { failed = true; site = 43; break; }
+      // C1c: once the k-side has handed over T (fp32): the bf16 operands of G1b, T diag(b)
+      //     and T
+      {
+        const float* Tm = reinterpret_cast<const float*>(sm + PS_TM);
+        const float* bv = vec + 320;
+#pragma unroll
+        for (int it = tid; it < 512; it += 128) {
+          const int r = it & 63, c8 = it >> 6;   // row r, columns 8 c8 .. 8 c8 + 7
+          const float4 ta = ld4(Tm + r * NS + 8 * c8), tb = ld4(Tm + r * NS + 8 * c8 + 4);
+          const float4 ba = ld4(bv + 8 * c8), bb = ld4(bv + 8 * c8 + 4);
+          const uint32_t off = kmajor_off(r, 8 * c8, 64);
+          st_u128(sm, PS_TB + off,
+                  make_uint4(pack_bf16x2(ta.x * ba.x, ta.y * ba.y), pack_bf16x2(ta.z * ba.z, ta.w * ba.w),
+                             pack_bf16x2(tb.x * bb.x, tb.y * bb.y), pack_bf16x2(tb.z * bb.z, tb.w * bb.w)));
+          st_u128(sm, PS_TT + off,
+                  make_uint4(pack_bf16x2(ta.x, ta.y), pack_bf16x2(ta.z, ta.w),
+                             pack_bf16x2(tb.x, tb.y), pack_bf16x2(tb.z, tb.w)));
+        }
+      }
+      fence_proxy_async();   // read by G1b
       tc_fence_before();
       group_sync(4, 128);
-      PSTAMP(tid == 0, c, 5);
+      PSTAMP(tid == 0, c, 26);
       // G1b: U^T = V^T (T diag b)^T + X_b^T T^T
       if (tid == 0) {
+        mbar_arrive(bar(B_FREEC));   // T (fp32) has been read by all four warps
         tc_fence_after();
 #pragma unroll
         for (int ks = 0; ks < 4; ++ks)
@@ -777,6 +782,7 @@ __global__ void __launch_bounds__(PNT, 1)
       // ---- K3: operand tiles [Kr; Qr], [Kc; Kc2] (own), Kg, Qg (stage).  The warp's rows lie in
       //      one 32-token block (bsel), so the block's variant is chosen once per warp.
       {
+        if (kt < PC) vec[256 + kt] = -vec[320 + kt] * vec[192 + kt];   // -b inv_k, for the chain
         const float4 mE4 = ld4(GT + j * 128 + 4 * o4);
         const float2 nm01 = make_float2(-mE4.x, -mE4.y), nm23 = make_float2(-mE4.z, -mE4.w);
         PSTAMP(kt == 0, c, 13);
@@ -845,6 +851,7 @@ __global__ void __launch_bounds__(PNT, 1)
         PSTAMP(kt == 0, c, 20);
         fence_proxy_async();
         group_sync(1, 512);
+        if (mma_thread) mbar_arrive(bar(B_FULLA));   // [Kg; Qg] and the vectors of chunk c
         PSTAMP(kt == 0, c, 21);
 
         // ---- K4: [A | QK] on the tensor cores, once the chain has taken the previous QK out
@@ -897,7 +904,6 @@ __global__ void __launch_bounds__(PNT, 1)
         PSTAMP(kt == 0, c, 23);
         float* nrow = Nm + r * NS + 16 * cq;
         const float br = vec[320 + r] * ik[r];
-        if (cq == 0) vec[256 + r] = -br;
 #pragma unroll
         for (int s4 = 0; s4 < 4; ++s4) {
           const float4 kk = ld4(ik + 16 * cq + 4 * s4);
