@@ -75,7 +75,7 @@ constexpr int PS_TB = 155648;         // T diag(b) K-major 64 x 64
 constexpr int PS_TT = 163840;         // T K-major 64 x 64
 constexpr int PS_QK = 172032;         // [QK | Ke] MN-major, N = 192 in blocks of 64, 8 KB apart:
 constexpr int PS_KE = 180224;         //   QK (n = row r, k = token s; masked, raw), then Ke (n = dk)
-constexpr int PS_OST = PS_QK;         // the chain's O transpose scratch (1 KB per warp) once G2 has
+constexpr int PS_OST = PS_QK;         // the chain's O transpose scratch (2 KB per warp) once G2 has
                                       //   read QK (the chain writes QK itself)
 // small things
 constexpr int PS_VEC = 196608;        // [3 by chunk % 3]: decay[128] iq[64] ik[64] nbik[64] b[64] fp32
@@ -535,21 +535,21 @@ __global__ void __launch_bounds__(PNT, 1)
       if (bar_any(4, 128, !ok)) { failed = true; site = 42; break; }
       PSTAMP(tid == 0, c, 8);
       tc_fence_after();
-      // C4: O^T diag(inv_q) -> out rows < L.  16 tokens at a time: each thread's 16 values
-      //     (its value channel) go to a per-warp [16 tok][32 dv] scratch, which the warp then
+      // C4: O^T diag(inv_q) -> out rows < L.  32 tokens at a time: each thread's 32 values
+      //     (its value channel) go to a per-warp [32 tok][32 dv] scratch, which the warp then
       //     reads back as 32-byte row pieces for 16-byte global stores.
       {
         const float* iq = vec + 128;
-        unsigned char* ost = sm + PS_OST + warp * 1024;
+        unsigned char* ost = sm + PS_OST + warp * 2048;
         const int tok = lane >> 1, half = lane & 1;
 #pragma unroll 1
-        for (int qq = 0; qq < 4; ++qq) {
-          uint32_t x[16];
-          tmem_ld16(tmem + lb + TM_O + qq * 16, x);
+        for (int qp = 0; qp < 2; ++qp) {
+          uint32_t x[32];
+          tmem_ld32(tmem + lb + TM_O + qp * 32, x);
           tmem_wait_ld();
 #pragma unroll
-          for (int t4 = 0; t4 < 4; ++t4) {
-            const float4 f = ld4(iq + qq * 16 + 4 * t4);
+          for (int t4 = 0; t4 < 8; ++t4) {
+            const float4 f = ld4(iq + qp * 32 + 4 * t4);
             const float fv[4] = {f.x, f.y, f.z, f.w};
 #pragma unroll
             for (int e = 0; e < 4; ++e)
@@ -557,14 +557,18 @@ __global__ void __launch_bounds__(PNT, 1)
                   __float2bfloat16_rn(__uint_as_float(x[4 * t4 + e]) * fv[e]);
           }
           __syncwarp();
-          const uint4 v0 = *reinterpret_cast<const uint4*>(ost + tok * 64 + half * 32);
-          const uint4 v1 = *reinterpret_cast<const uint4*>(ost + tok * 64 + half * 32 + 16);
-          const int r = qq * 16 + tok;
-          const int64_t orow = r < L ? out_row(p, c0 + r) : -1;   // the row map, if any
-          if (orow >= 0) {
-            uint4* dst = reinterpret_cast<uint4*>(p.out + orow * HD + xcol + 32 * warp + 16 * half);
-            dst[0] = v0;
-            dst[1] = v1;
+#pragma unroll
+          for (int hh = 0; hh < 2; ++hh) {
+            const int tl = 16 * hh + tok;   // token within the 32
+            const uint4 v0 = *reinterpret_cast<const uint4*>(ost + tl * 64 + half * 32);
+            const uint4 v1 = *reinterpret_cast<const uint4*>(ost + tl * 64 + half * 32 + 16);
+            const int r = qp * 32 + tl;
+            const int64_t orow = r < L ? out_row(p, c0 + r) : -1;   // the row map, if any
+            if (orow >= 0) {
+              uint4* dst = reinterpret_cast<uint4*>(p.out + orow * HD + xcol + 32 * warp + 16 * half);
+              dst[0] = v0;
+              dst[1] = v1;
+            }
           }
           __syncwarp();
         }
