@@ -16,8 +16,9 @@
 // mbarriers (stage full: k-side -> chain; stage parts free: chain -> k-side).
 //
 // Per chunk (rows r, s = tokens; G = inclusive cumsum of the log2 decay over the
-// chunk, per key channel; raw q, k rows scaled by a power of two to norm <= 1;
-// inv_q = scale / |q|, inv_k = 1 / |k| carried as per-token scalars):
+// chunk, per key channel; raw k rows scaled by a power of two to norm <= 1, with
+// inv_k = 1 / |k| carried as a per-token scalar; q rows enter as q scale / |q|, so that
+// inv_q = 1 below):
 //   A[r,s]  = b_r inv_k_r inv_k_s  k_r.(k_s 2^(G_r - G_s))   (s < r)
 //   QK[r,s] =                      q_r.(k_s 2^(G_r - G_s))   (s <= r)
 //   T = (I + A)^-1
@@ -78,7 +79,7 @@ constexpr int PS_KE = 180224;         //   QK (n = row r, k = token s; masked, r
 constexpr int PS_OST = PS_QK;         // the chain's O transpose scratch (2 KB per warp) once G2 has
                                       //   read QK (the chain writes QK itself)
 // small things
-constexpr int PS_VEC = 196608;        // [3 by chunk % 3]: decay[128] iq[64] ik[64] nbik[64] b[64] fp32
+constexpr int PS_VEC = 196608;        // [3 by chunk % 3]: decay[128] (unused)[64] ik[64] nbik[64] b[64]
 constexpr int kVecFloats = 384;
 constexpr int PS_GT = PS_VEC + 3 * kVecFloats * 4;   // quad totals, then anchor offsets [16][128]
 constexpr int PS_FAC = PS_GT + 16 * 128 * 4;          // per-channel factors [6][128]
@@ -535,11 +536,11 @@ __global__ void __launch_bounds__(PNT, 1)
       if (bar_any(4, 128, !ok)) { failed = true; site = 42; break; }
       PSTAMP(tid == 0, c, 8);
       tc_fence_after();
-      // C4: O^T diag(inv_q) -> out rows < L.  32 tokens at a time: each thread's 32 values
-      //     (its value channel) go to a per-warp [32 tok][32 dv] scratch, which the warp then
-      //     reads back as 32-byte row pieces for 16-byte global stores.
+      // C4: O -> out rows < L (O is normalised already: the q rows entered the products as
+      //     q scale / |q|).  32 tokens at a time: each thread's 32 values (its value channel)
+      //     go to a per-warp [32 tok][32 dv] scratch, which the warp then reads back as 32-byte
+      //     row pieces for 16-byte global stores.
       {
-        const float* iq = vec + 128;
         unsigned char* ost = sm + PS_OST + warp * 2048;
         const int tok = lane >> 1, half = lane & 1;
 #pragma unroll 1
@@ -548,14 +549,9 @@ __global__ void __launch_bounds__(PNT, 1)
           tmem_ld32(tmem + lb + TM_O + qp * 32, x);
           tmem_wait_ld();
 #pragma unroll
-          for (int t4 = 0; t4 < 8; ++t4) {
-            const float4 f = ld4(iq + qp * 32 + 4 * t4);
-            const float fv[4] = {f.x, f.y, f.z, f.w};
-#pragma unroll
-            for (int e = 0; e < 4; ++e)
-              *reinterpret_cast<__nv_bfloat16*>(ost + (4 * t4 + e) * 64 + lane * 2) =
-                  __float2bfloat16_rn(__uint_as_float(x[4 * t4 + e]) * fv[e]);
-          }
+          for (int t = 0; t < 32; ++t)
+            *reinterpret_cast<__nv_bfloat16*>(ost + t * 64 + lane * 2) =
+                __float2bfloat16_rn(__uint_as_float(x[t]));
           __syncwarp();
 #pragma unroll
           for (int hh = 0; hh < 2; ++hh) {
@@ -767,13 +763,17 @@ __global__ void __launch_bounds__(PNT, 1)
           // ss < 2^(e+1) -> |row| < 2^ceil((e+1)/2): rows enter the operands times 2^-sh
           const int e = ((__float_as_int(ss) >> 23) & 255) - 127;
           const int sh = max(-60, min(60, (e + 2) >> 1));
-          const float inv = (r < L) ? rsqrtf(ss + kL2Eps) * __int_as_float((127 + sh) << 23) : 0.0f;
-          if (kt < 64)
-            vec[128 + r] = p.scale * inv;
-          else
-            vec[192 + r] = inv;
-          const uint32_t bb = (uint32_t)(127 - sh) << 7;   // bf16 bits of 2^-sh
-          RSC[kt] = bb | (bb << 16);
+          const float rs = (r < L) ? rsqrtf(ss + kL2Eps) : 0.0f;
+          if (kt < 64) {
+            // q rows enter the operands as q scale / |q| (their norm is scale): O comes out of
+            // the products already normalised
+            const uint32_t qs = pack_bf16x2(p.scale * rs, p.scale * rs);
+            RSC[kt] = qs;
+          } else {
+            vec[192 + r] = rs * __int_as_float((127 + sh) << 23);   // 1 / |k| against k 2^-sh
+            const uint32_t bb = (uint32_t)(127 - sh) << 7;           // bf16 bits of 2^-sh
+            RSC[kt] = bb | (bb << 16);
+          }
         }
       } else if (bt < PC) {
         vec[320 + bt] = (bt < L) ? sigm(b_raw) : 0.0f;   // b
