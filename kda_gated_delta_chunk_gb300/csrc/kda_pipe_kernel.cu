@@ -886,8 +886,10 @@ __global__ void __launch_bounds__(PNT, 1)
       //      quarter of the row's 64 columns each -> N (fp32) and -b inv_k; the other eight
       //      warps form Ke = Kc 2^(G_last - anchor) (stage) once the chain's last product of
       //      the previous chunk has read Ke
+      // (one barrier for both waits: Ke's buffer here, T's before K6)
       if (c > 0) {
         if (free_thread) ok = wait_phase(bar(B_FREEB), (uint32_t)((c - 1) & 1));
+        if (mma_thread) ok = wait_phase(bar(B_FREEC), (uint32_t)((c - 1) & 1));
         if (bar_any(1, 512, !ok)) { failed = true; site = 25; break; }
       }
       PSTAMP(kt == 0, c, 1);
@@ -946,10 +948,6 @@ __global__ void __launch_bounds__(PNT, 1)
       tc_fence_before();
       group_sync(1, 512);
       PSTAMP(kt == 0, c, 24);
-      if (c > 0) {   // the chain has read T of the previous chunk (and the bf16 operands made of it)
-        if (mma_thread) ok = wait_phase(bar(B_FREEC), (uint32_t)((c - 1) & 1));
-        if (bar_any(1, 512, !ok)) { failed = true; site = 26; break; }
-      }
       PSTAMP(kt == 0, c, 11);
 
       // ---- K6 (threads < 128): T = (I + N)^-1: 16 x 16 diagonal blocks by substitution
