@@ -780,7 +780,10 @@ __global__ void __launch_bounds__(PNT, 1)
         b_raw = 0.0f;
         if (c0 + PC + bt < t1) b_raw = __bfloat162float(p.beta[(size_t)(c0 + PC + bt) * p.s_beta + h]);
       }
-      group_sync(1, 512);
+      // the barrier that ends K2 also carries the wait for the chain to have read [Kg; Qg] of
+      // the previous chunk (K3 overwrites it)
+      if (c > 0 && mma_thread) ok = wait_phase(bar(B_FREEA), (uint32_t)((c - 1) & 1));
+      if (bar_any(1, 512, !ok)) { failed = true; site = 21; break; }
       PSTAMP(kt == 0, c, 18);
 
       // ---- K3: operand tiles [Kr; Qr], [Kc; Kc2] (own), Kg, Qg (stage).  The warp's rows lie in
@@ -790,11 +793,6 @@ __global__ void __launch_bounds__(PNT, 1)
         const float4 mE4 = ld4(GT + j * 128 + 4 * o4);
         const float2 nm01 = make_float2(-mE4.x, -mE4.y), nm23 = make_float2(-mE4.z, -mE4.w);
         PSTAMP(kt == 0, c, 13);
-        // the chain has finished reading [Kg; Qg] of the previous chunk
-        if (c > 0) {
-          if (mma_thread) ok = wait_phase(bar(B_FREEA), (uint32_t)((c - 1) & 1));
-          if (bar_any(1, 512, !ok)) { failed = true; site = 21; break; }
-        }
         PSTAMP(kt == 0, c, 19);
         // block 0: Kc2 = Kc 2^(G31 - anchor0) 2^(anchor1 - G31), Kg = Kr 2^anchor0;
         // block 1: Kg = Kr 2^(anchor1 - G31) 2^G31 (Kc2 has no block-1 rows).  The factors are
