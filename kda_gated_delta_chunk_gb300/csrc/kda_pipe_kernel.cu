@@ -665,9 +665,11 @@ __global__ void __launch_bounds__(PNT, 1)
       if (nch > 0) issue_in(0);
     }
     // raw beta logits of the next chunk, fetched a chunk ahead (threads 128 .. 191)
-    float b_raw = 0.0f;
+    // (kept as the raw bf16 bits, converted only when used a chunk later, so that no warp
+    // waits for the global load before the barrier that ends K2)
+    unsigned short b_raw = 0;
     const int bt = kt - 128;
-    if (bt >= 0 && bt < PC && t0 + bt < t1) b_raw = __bfloat162float(p.beta[(size_t)(t0 + bt) * p.s_beta + h]);
+    if (bt >= 0 && bt < PC && t0 + bt < t1) b_raw = __bfloat16_as_ushort(p.beta[(size_t)(t0 + bt) * p.s_beta + h]);
 
     for (int c = 0; c < nch; ++c) {
       const int c0 = t0 + PC * c;
@@ -776,9 +778,9 @@ __global__ void __launch_bounds__(PNT, 1)
           }
         }
       } else if (bt < PC) {
-        vec[320 + bt] = (bt < L) ? sigm(b_raw) : 0.0f;   // b
-        b_raw = 0.0f;
-        if (c0 + PC + bt < t1) b_raw = __bfloat162float(p.beta[(size_t)(c0 + PC + bt) * p.s_beta + h]);
+        vec[320 + bt] = (bt < L) ? sigm(__uint_as_float((uint32_t)b_raw << 16)) : 0.0f;   // b
+        b_raw = 0;
+        if (c0 + PC + bt < t1) b_raw = __bfloat16_as_ushort(p.beta[(size_t)(c0 + PC + bt) * p.s_beta + h]);
       }
       // the barrier that ends K2 also carries the wait for the chain to have read [Kg; Qg] of
       // the previous chunk (K3 overwrites it)
