@@ -1,4 +1,5 @@
-// Split path, second kernel: the serial inter-chunk chain for one value slice.
+// Split path, second kernel: the serial inter-chunk chain for one value slice of 32 or 16
+// columns (P = 4 or 8; P = 2 runs on tcgen05, kda_chain_vs_kernel.cu).
 //
 // The chunk-parallel k-side kernel has already written, for every (chunk, head),
 // a record with -W, Qg (raw q times 2^Gam), Ke (raw k times 2^(Gam_last - Gam)),
@@ -431,9 +432,12 @@ cudaError_t launch_split(const Params& p, cudaStream_t stream) {
   if (p.vsplit != 1 && p.vsplit != 2 && p.vsplit != 4 && p.vsplit != 8) return cudaErrorInvalidValue;
   cudaError_t e = launch_kside(p, stream);
   if (e != cudaSuccess) return e;
+  // P = 2 on tcgen05 (kda_chain_vs_kernel.cu); the narrower slices keep the warp-level
+  // products of this file, which measured 12-23% faster there (per-instruction tcgen05
+  // overheads do not shrink with N = 32 or 16)
   switch (p.vsplit) {
     case 1: return launch_chain_tc(p, stream);
-    case 2: return launch_chain_dv<64>(p, stream);
+    case 2: return launch_chain_vs(p, stream);
     case 4: return launch_chain_dv<32>(p, stream);
     default: return launch_chain_dv<16>(p, stream);
   }

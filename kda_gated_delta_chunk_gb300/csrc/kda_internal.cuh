@@ -120,6 +120,7 @@ cudaError_t launch_pipe(const Params& p, cudaStream_t stream);
 // per value slice; launch_split runs both.
 cudaError_t launch_kside(const Params& p, cudaStream_t stream);
 cudaError_t launch_chain_tc(const Params& p, cudaStream_t stream);   // P = 1
+cudaError_t launch_chain_vs(const Params& p, cudaStream_t stream);   // P = 2
 // Token-by-token form (decode / speculative verify); token_states may be null.
 cudaError_t launch_recurrent(const Params& p, void* token_states, cudaStream_t stream);
 cudaError_t launch_split(const Params& p, cudaStream_t stream);

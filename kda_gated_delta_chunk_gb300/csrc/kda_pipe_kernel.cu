@@ -794,8 +794,6 @@ __global__ void __launch_bounds__(PNT, 1)
         if (kt < PC) vec[256 + kt] = -vec[320 + kt] * vec[192 + kt];   // -b inv_k, for the chain
         const float4 mE4 = ld4(GT + j * 128 + 4 * o4);
         const float2 nm01 = make_float2(-mE4.x, -mE4.y), nm23 = make_float2(-mE4.z, -mE4.w);
-        PSTAMP(kt == 0, c, 13);
-        PSTAMP(kt == 0, c, 19);
         // block 0: Kc2 = Kc 2^(G31 - anchor0) 2^(anchor1 - G31), Kg = Kr 2^anchor0;
         // block 1: Kg = Kr 2^(anchor1 - G31) 2^G31 (Kc2 has no block-1 rows).  The factors are
         // applied one after the other, never multiplied together first: their product alone
@@ -948,7 +946,6 @@ __global__ void __launch_bounds__(PNT, 1)
       tc_fence_before();
       group_sync(1, 512);
       PSTAMP(kt == 0, c, 24);
-      PSTAMP(kt == 0, c, 11);
 
       // ---- K6 (threads < 128): T = (I + N)^-1: 16 x 16 diagonal blocks by substitution
       //      (fp32), then the off-diagonal blocks as tf32 warp products, 16 -> 32 -> 64
@@ -961,6 +958,7 @@ __global__ void __launch_bounds__(PNT, 1)
           *reinterpret_cast<float4*>(Tm + (bi * 16 + (e >> 2)) * NS + bj * 16 + 4 * (e & 3)) =
               make_float4(0.f, 0.f, 0.f, 0.f);
         }
+        PSTAMP(kt == 0, c, 19);
         if (wb < 2) {
           // warp wb: the diagonal blocks 2 wb (lanes 0-15) and 2 wb + 1 (lanes 16-31), lane =
           // column, by forward substitution four columns of N at a time (16-byte row pieces);
@@ -986,11 +984,15 @@ __global__ void __launch_bounds__(PNT, 1)
           for (int i = 0; i < 16; ++i) Tm[(ob + i) * NS + ob + jj] = x[i];
           __syncwarp();
           PSTAMP(kt == 0, c, 14);
+          PSTAMP(kt == 32, c, 25);
           const int ro = (2 * wb + 1) * 16, co = 2 * wb * 16;
           float* Yw = Y + wb * 16 * NS;
           wgemm16(Nm + ro * NS + co, Tm + co * NS + co, Yw, 1.0f, lane);
           __syncwarp();
+          PSTAMP(kt == 0, c, 11);
           wgemm16(Tm + ro * NS + ro, Yw, Tm + ro * NS + co, -1.0f, lane);
+          __syncwarp();
+          PSTAMP(kt == 0, c, 13);
         }
         group_sync(3, 128);
         PSTAMP(kt == 0, c, 15);

@@ -65,7 +65,8 @@ def check_placed(buf, rows, dense, T_used):
 
 @pytest.mark.parametrize("kernel,vsplit", [(kda.KERNEL_TC, 1), (kda.KERNEL_TC, 2),
                                            (kda.KERNEL_TC_HELPERS, -1), (kda.KERNEL_SPLIT, 1),
-                                           (kda.KERNEL_SPLIT, 4), (kda.KERNEL_REF, 1),
+                                           (kda.KERNEL_SPLIT, 2), (kda.KERNEL_SPLIT, 4),
+                                           (kda.KERNEL_SPLIT, 8), (kda.KERNEL_REF, 1),
                                            (kda.KERNEL_PIPE, 1)])
 def test_prefill_scatter_places_the_dense_rows(kernel, vsplit):
     """Ragged sequences (a 1-token and an empty one, tails), tokens past cu_seqlens[N]."""

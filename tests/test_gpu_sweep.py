@@ -45,7 +45,8 @@ def draw_case(seed):
 
 
 PATHS = [("tc", kda.KERNEL_TC, 1), ("tc_p4", kda.KERNEL_TC, 4), ("helpers", kda.KERNEL_TC_HELPERS, -1),
-         ("split", kda.KERNEL_SPLIT, -1), ("ref", kda.KERNEL_REF, 1), ("pipe", kda.KERNEL_PIPE, 1)]
+         ("split", kda.KERNEL_SPLIT, -1), ("split_p2", kda.KERNEL_SPLIT, 2), ("ref", kda.KERNEL_REF, 1),
+         ("pipe", kda.KERNEL_PIPE, 1)]
 
 
 @pytest.mark.parametrize("seed", range(12))
