@@ -312,12 +312,13 @@ CHAIN_SLOTS = {0: "stage part A full", 2: "v ready", 3: "G1a issued", 12: "S dec
                28: "G1b done (thread 0)", 27: "QK operand stored", 6: "chain group past G1b",
                7: "U_b stored", 8: "G2 done", 10: "O stored"}
 CHAIN_ORDER = [0, 2, 3, 12, 4, 5, 26, 28, 27, 6, 7, 8, 10]
-KSIDE_SLOTS = {16: "inputs landed", 17: "gate and norms", 18: "factors", 13: "factor loads",
-               19: "stage parts free", 20: "tile rows done", 21: "tiles fenced",
-               22: "A|QK MMA done", 1: "Ke parts free", 23: "A loaded", 24: "N, Ke stored",
-               11: "T parts free", 14: "diagonal blocks", 15: "level 1", 9: "level 2a",
+KSIDE_SLOTS = {16: "inputs landed", 17: "gate and norms", 18: "factors, [Kg; Qg] free",
+               20: "tile rows done", 21: "tiles fenced", 22: "A|QK MMA done",
+               1: "Ke and T parts free", 23: "A loaded", 24: "N, Ke stored",
+               19: "upper blocks zeroed", 14: "diagonal blocks", 11: "level 1 first product",
+               13: "level 1 second product", 15: "level 1", 9: "level 2a",
                29: "stage handed over"}
-KSIDE_ORDER = [16, 17, 18, 13, 19, 20, 21, 22, 1, 23, 24, 11, 14, 15, 9, 29]
+KSIDE_ORDER = [16, 17, 18, 20, 21, 22, 1, 23, 24, 19, 14, 11, 13, 15, 9, 29]
 
 
 def run_stamps(args):
@@ -361,7 +362,8 @@ def run_stamps(args):
            "chain": {f"{CHAIN_SLOTS[a]} -> {CHAIN_SLOTS[b]}": med(a, b) for a, b in zip(cs, cs[1:])},
            "chain_wait_for_stage (O stored c-1 -> stage full c)": med(10, 0, True),
            "handover -> chain start": med(29, 0),
-           "chain G1a done (c-1) -> kside stage parts free (c)": med(4, 19, True)}
+           "chain G1a done (c-1) -> kside factors, [Kg; Qg] free (c)": med(4, 18, True),
+           "inverse: diagonal blocks of warp 5 (N stored -> done)": med(24, 25)}
     print(json.dumps(res, indent=1), flush=True)
 
 
