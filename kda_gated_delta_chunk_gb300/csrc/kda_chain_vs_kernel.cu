@@ -34,7 +34,9 @@ namespace {
 
 using namespace sm100;
 
-constexpr int NT4 = 128;   // 4 warps: thread i <-> TMEM lane i
+// 8 warps: warp w reads TMEM lanes 32 (w % 4) .. 32 (w % 4) + 31 and value columns
+// [DV/2 (w / 4), DV/2 (w / 4 + 1)) of the slice
+constexpr int NT4 = 256;
 
 // ---- shared memory (offsets from a 1024-byte aligned base)
 constexpr int VS_V = kRecBytes + 1024;        // v tile [64 tok][64 cols] SW128 after the record
@@ -84,7 +86,9 @@ struct ChainVsMaps {
 template <int DV, bool kRowMap>
 __global__ void __launch_bounds__(NT4, 1)
     kda_chain_vs_kernel(const __grid_constant__ Params p, const __grid_constant__ ChainVsMaps maps) {
+  static_assert(DV % 32 == 0, "two column halves of 16 or more");
   constexpr int P = 128 / DV;
+  constexpr int DH = DV / 2;   // columns per thread
   constexpr uint32_t T_X0 = 0, T_Y = 2 * DV, T_S = 3 * DV, T_COLS = 4 * DV;
   // [-W; Qg] (MN-major) x S_b;  K-major A x MN-major B (T diag b, QK, Ke against V, U_b)
   constexpr uint32_t ID_MN = idesc_bf16(128, DV, 1, 1);
@@ -92,7 +96,7 @@ __global__ void __launch_bounds__(NT4, 1)
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   const uint32_t sb = smem_u32(sm);
-  const int tid = threadIdx.x, warp = tid >> 5;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + VS_TSLOT);
   const uint32_t bar_full0 = sb + VS_BAR, bar_g1 = bar_full0 + 16, bar_g2 = bar_full0 + 24;
 
@@ -129,8 +133,10 @@ __global__ void __launch_bounds__(NT4, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tslot;
-  const uint32_t lb = (uint32_t)(32 * warp) << 16;   // this warp's TMEM lane quadrant
-  const int dk = tid;                                // key channel = TMEM lane
+  const int q4 = warp & 3;
+  const uint32_t lb = (uint32_t)(32 * q4) << 16;   // this warp's TMEM lane quadrant
+  const int row = 32 * q4 + lane;                  // TMEM lane: key channel, or accumulator row
+  const int ch = DH * (warp >> 2);                 // first column of this thread's half
 
   auto rec_src = [&](int i) {
     return reinterpret_cast<const unsigned char*>(p.status) + kSplitHeader +
@@ -152,18 +158,18 @@ __global__ void __launch_bounds__(NT4, 1)
     if (nch > 1) prefetch_l2(1);
   }
 
-  // ---- state in: row dk of the slice, DV values -> TMEM
+  // ---- state in: row (key channel) `row` of the slice, this thread's DH values -> TMEM
   {
-    uint32_t r[DV];
+    uint32_t r[DH];
 #pragma unroll
-    for (int j = 0; j < DV; ++j) r[j] = 0u;
+    for (int j = 0; j < DH; ++j) r[j] = 0u;
     if (p.initial_state) {
-      const size_t idx = sbase + (size_t)dk * 128 + dv0;
+      const size_t idx = sbase + (size_t)row * 128 + dv0 + ch;
       if (p.state_bf16) {
         const uint4* src = reinterpret_cast<const uint4*>(
             static_cast<const __nv_bfloat16*>(p.initial_state) + idx);
 #pragma unroll
-        for (int j = 0; j < DV / 8; ++j) {
+        for (int j = 0; j < DH / 8; ++j) {
           const uint4 w = src[j];
           const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
@@ -175,7 +181,7 @@ __global__ void __launch_bounds__(NT4, 1)
       } else {
         const float4* src = reinterpret_cast<const float4*>(static_cast<const float*>(p.initial_state) + idx);
 #pragma unroll
-        for (int j = 0; j < DV / 4; ++j) {
+        for (int j = 0; j < DH / 4; ++j) {
           const float4 w = src[j];
           r[4 * j] = __float_as_uint(w.x);
           r[4 * j + 1] = __float_as_uint(w.y);
@@ -184,21 +190,21 @@ __global__ void __launch_bounds__(NT4, 1)
         }
       }
     }
-    tmem_st_dv<DV>(tmem + lb + T_S, r);
+    tmem_st_dv<DH>(tmem + lb + T_S + ch, r);
     tmem_wait_st();
   }
 
-  // O of a finished chunk (threads 64-127: X rows 64-127 = its tokens) -> out
+  // O of a finished chunk (warps with q4 >= 2: X rows 64-127 = its tokens) -> out
   auto drain_o = [&](uint32_t tx, int c0, int L, float iq, int64_t orow) {
-    const int t = tid - 64;
-    uint32_t x[DV];
-    tmem_ld_dv<DV>(tmem + lb + tx, x);
+    const int t = row - 64;
+    uint32_t x[DH];
+    tmem_ld_dv<DH>(tmem + lb + tx + ch, x);
     tmem_wait_ld();
-    const int64_t row = kRowMap ? orow : (int64_t)(c0 + t);
-    if (t < L && row >= 0) {
-      uint4* dst = reinterpret_cast<uint4*>(p.out + (size_t)row * HD + xcol);
+    const int64_t orw = kRowMap ? orow : (int64_t)(c0 + t);
+    if (t < L && orw >= 0) {
+      uint4* dst = reinterpret_cast<uint4*>(p.out + (size_t)orw * HD + xcol + ch);
 #pragma unroll
-      for (int j = 0; j < DV / 8; ++j)
+      for (int j = 0; j < DH / 8; ++j)
         dst[j] = make_uint4(pack_bf16x2(__uint_as_float(x[8 * j]) * iq, __uint_as_float(x[8 * j + 1]) * iq),
                             pack_bf16x2(__uint_as_float(x[8 * j + 2]) * iq, __uint_as_float(x[8 * j + 3]) * iq),
                             pack_bf16x2(__uint_as_float(x[8 * j + 4]) * iq, __uint_as_float(x[8 * j + 5]) * iq),
@@ -247,22 +253,22 @@ __global__ void __launch_bounds__(NT4, 1)
             make_uint4(0, 0, 0, 0);
     }
 
-    // ---- 2. S_b = bf16(S) (MN-major row dk); S *= 2^Gam_last[dk]
+    // ---- 2. S_b = bf16(S) (MN-major K row = key channel); S *= 2^Gam_last[key channel]
     {
-      uint32_t s[DV];
-      tmem_ld_dv<DV>(tmem + lb + T_S, s);
+      uint32_t s[DH];
+      tmem_ld_dv<DH>(tmem + lb + T_S + ch, s);
       tmem_wait_ld();
 #pragma unroll
-      for (int j = 0; j < DV / 8; ++j)
-        *reinterpret_cast<uint4*>(sm + VS_SB + mn_piece(dk, j)) =
+      for (int j = 0; j < DH / 8; ++j)
+        *reinterpret_cast<uint4*>(sm + VS_SB + mn_piece(row, ch / 8 + j)) =
             make_uint4(pack_bf16x2(__uint_as_float(s[8 * j]), __uint_as_float(s[8 * j + 1])),
                        pack_bf16x2(__uint_as_float(s[8 * j + 2]), __uint_as_float(s[8 * j + 3])),
                        pack_bf16x2(__uint_as_float(s[8 * j + 4]), __uint_as_float(s[8 * j + 5])),
                        pack_bf16x2(__uint_as_float(s[8 * j + 6]), __uint_as_float(s[8 * j + 7])));
-      const float d = vec[dk];
+      const float d = vec[row];
 #pragma unroll
-      for (int j = 0; j < DV; ++j) s[j] = __float_as_uint(__uint_as_float(s[j]) * d);
-      tmem_st_dv<DV>(tmem + lb + T_S, s);
+      for (int j = 0; j < DH; ++j) s[j] = __float_as_uint(__uint_as_float(s[j]) * d);
+      tmem_st_dv<DH>(tmem + lb + T_S + ch, s);
       tmem_wait_st();
     }
     fence_proxy_async();   // S_b and the zeroed v rows are read by the tensor cores
@@ -282,13 +288,13 @@ __global__ void __launch_bounds__(NT4, 1)
       mma_commit(bar_g1);
       mma_out = 1;
     }
-    if (i > 0 && tid >= 64) {
+    if (i > 0 && q4 >= 2) {
       tc_fence_after();
       drain_o(T_X0 + (uint32_t)((buf ^ 1) * DV), c0 - kChunk, L_prev, iq_prev, orow_prev);
     }
-    if (tid >= 64) {   // this chunk's scalars for its own drain (the stage is reused)
-      iq_prev = vec[128 + tid - 64];
-      orow_prev = (kRowMap && tid - 64 < L) ? out_row(p, c0 + tid - 64) : -1;
+    if (q4 >= 2) {   // this chunk's scalars for its own drain (the stage is reused)
+      iq_prev = vec[128 + row - 64];
+      orow_prev = (kRowMap && row - 64 < L) ? out_row(p, c0 + row - 64) : -1;
     }
     L_prev = L;
     {
@@ -302,20 +308,20 @@ __global__ void __launch_bounds__(NT4, 1)
     }
     tc_fence_after();
 
-    // ---- 4. U_b = bf16((X + Y) diag(1/|k|)), rows 0-63 (threads 0-63 = tokens)
-    if (tid < 64) {
-      uint32_t x[DV], y[DV];
-      tmem_ld_dv<DV>(tmem + lb + tx, x);
-      tmem_ld_dv<DV>(tmem + lb + T_Y, y);
+    // ---- 4. U_b = bf16((X + Y) diag(1/|k|)), rows 0-63 (warps with q4 < 2: tokens)
+    if (q4 < 2) {
+      uint32_t x[DH], y[DH];
+      tmem_ld_dv<DH>(tmem + lb + tx + ch, x);
+      tmem_ld_dv<DH>(tmem + lb + T_Y + ch, y);
       tmem_wait_ld();
-      const float ik = vec[192 + tid];
+      const float ik = vec[192 + row];
 #pragma unroll
-      for (int j = 0; j < DV / 8; ++j) {
+      for (int j = 0; j < DH / 8; ++j) {
         float u[8];
 #pragma unroll
         for (int e = 0; e < 8; ++e)
           u[e] = (__uint_as_float(x[8 * j + e]) + __uint_as_float(y[8 * j + e])) * ik;
-        *reinterpret_cast<uint4*>(sm + VS_UB + mn_piece(tid, j)) =
+        *reinterpret_cast<uint4*>(sm + VS_UB + mn_piece(row, ch / 8 + j)) =
             make_uint4(pack_bf16x2(u[0], u[1]), pack_bf16x2(u[2], u[3]), pack_bf16x2(u[4], u[5]),
                        pack_bf16x2(u[6], u[7]));
       }
@@ -359,18 +365,18 @@ __global__ void __launch_bounds__(NT4, 1)
       if (mma_out == 2) mbar_wait(bar_g2, ph_mma);
     }
   } else {
-    if (nch > 0 && tid >= 64)   // O of the last chunk
+    if (nch > 0 && q4 >= 2)   // O of the last chunk
       drain_o(T_X0 + (uint32_t)(((nch - 1) & 1) * DV), t0 + kChunk * (nch - 1), L_prev, iq_prev,
               orow_prev);
     // ---- state out
-    uint32_t r[DV];
-    tmem_ld_dv<DV>(tmem + lb + T_S, r);
+    uint32_t r[DH];
+    tmem_ld_dv<DH>(tmem + lb + T_S + ch, r);
     tmem_wait_ld();
-    const size_t idx = sbase + (size_t)dk * 128 + dv0;
+    const size_t idx = sbase + (size_t)row * 128 + dv0 + ch;
     if (p.state_bf16) {
       uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.final_state) + idx);
 #pragma unroll
-      for (int j = 0; j < DV / 8; ++j)
+      for (int j = 0; j < DH / 8; ++j)
         dst[j] = make_uint4(pack_bf16x2(__uint_as_float(r[8 * j]), __uint_as_float(r[8 * j + 1])),
                             pack_bf16x2(__uint_as_float(r[8 * j + 2]), __uint_as_float(r[8 * j + 3])),
                             pack_bf16x2(__uint_as_float(r[8 * j + 4]), __uint_as_float(r[8 * j + 5])),
@@ -378,7 +384,7 @@ __global__ void __launch_bounds__(NT4, 1)
     } else {
       float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.final_state) + idx);
 #pragma unroll
-      for (int j = 0; j < DV / 4; ++j)
+      for (int j = 0; j < DH / 4; ++j)
         dst[j] = make_float4(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]),
                              __uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3]));
     }
