@@ -14,9 +14,9 @@
 //   O  = (Qg S + QK (U/|k|)) scale/|q|  -> out
 //   S  = diag(2^Gam_last) S + Ke^T (U/|k|)
 // The products are narrow (N = DV), so they run as warp-level mma.sync tiles
-// (bf16 in, fp32 accumulate) with S held in registers; the records of the next
-// chunks (one ahead, or two for the 16-column slice) are copied in while this one
-// is processed.
+// (bf16 in, fp32 accumulate) with S held in registers by eight consumer warps; a ninth
+// warp copies the records of the next chunks (one ahead, or two for the 16-column slice)
+// in while this one is processed, so that no consumer stalls on issuing a copy.
 #include <cuda.h>
 
 #include "kda_internal.cuh"
@@ -27,7 +27,8 @@ namespace {
 
 using namespace sm100;
 
-constexpr int NT2 = 256;   // 8 warps
+constexpr int NTC = 256;        // 8 consumer warps: the products, staging and stores
+constexpr int NT2 = NTC + 32;   // + 1 producer warp: the record and v copies
 
 constexpr int B_WQ = kRecWQ, B_QKE = kRecQKE, B_TB = kRecTB, B_VEC = kRecVec;
 constexpr int B_V = kRecBytes + 1024;   // V slice (aligned up to 1 KB)
@@ -44,7 +45,7 @@ struct ChainSmem {
   static constexpr int OFF_BAR = OFF_UB + 64 * SP * 2;
   static constexpr int OFF_MISC = OFF_BAR + 64;
   static constexpr int BYTES = OFF_MISC + 64 + 1024;
-  static_assert(BUF % 1024 == 0 && NB * 8 <= 64, "record buffers");
+  static_assert(BUF % 1024 == 0 && 2 * NB * 8 <= 64, "record buffers and their mbarriers");
   static_assert(BYTES <= 227 * 1024, "shared memory");
 };
 
@@ -105,7 +106,8 @@ __global__ void __launch_bounds__(NT2, 1)
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int g = lane >> 2, t = lane & 3;
   constexpr int NB = L_::NB;
-  const uint32_t bar0 = sb + L_::OFF_BAR;   // one mbarrier per record buffer, 8 bytes apart
+  const uint32_t bar0 = sb + L_::OFF_BAR;   // full: one mbarrier per record buffer, 8 bytes apart
+  const uint32_t empty0 = bar0 + 8 * NB;    // empty: the consumers are done with the buffer
 
   const int H = p.heads;
   const int unit = blockIdx.x;
@@ -118,7 +120,10 @@ __global__ void __launch_bounds__(NT2, 1)
     return;
   }
   if (tid == 0) {
-    for (int b = 0; b < NB; ++b) mbar_init(bar0 + 8 * b, 1);
+    for (int b = 0; b < NB; ++b) {
+      mbar_init(bar0 + 8 * b, 1);
+      mbar_init(empty0 + 8 * b, 1);
+    }
     mbar_fence_init();
   }
   __syncthreads();
@@ -129,7 +134,7 @@ __global__ void __launch_bounds__(NT2, 1)
   const size_t HD = (size_t)H * 128;
   const size_t sbase = ((size_t)n * H + h) * 128 * 128;
 
-  auto issue = [&](int i, int buf) {
+  auto issue = [&](int i, int buf) {   // (producer lane)
     const uint32_t base = sb + buf * L_::BUF;
     const uint32_t bar = bar0 + 8 * buf;
     const int64_t rec = (int64_t)(slot0 + i) * H + h;
@@ -139,6 +144,41 @@ __global__ void __launch_bounds__(NT2, 1)
     bulk_load(base, src, kRecBytes, bar);   // the record is contiguous at both ends
     tma_load_2d(base + B_V, &maps.v, h * 128 + dv0, t0 + kChunk * i, bar);
   };
+
+  // record + v slice of chunk i -> L2.  With three buffers the record copy itself is issued
+  // two chunks ahead, and a bulk prefetch of it as well only adds work for the TMA unit.
+  auto prefetch_l2 = [&](int i) {
+    if constexpr (NB == 2)
+      l2_prefetch(reinterpret_cast<const unsigned char*>(p.status) + kSplitHeader +
+                      ((int64_t)(slot0 + i) * H + h) * kRecBytes,
+                  kRecBytes);
+    tma_prefetch_2d(&maps.v, h * 128 + dv0, t0 + kChunk * i);
+  };
+
+  if (warp == NTC / 32) {
+    // ---- producer: copies chunk j into buffer j % NB once the consumers are done with
+    //      chunk j - NB there, so that no consumer thread stalls on issuing a copy
+    if (lane == 0) {
+      uint32_t eph = 0;   // bit b: parity of buffer b's next "empty" phase
+      int issued = 0;     // chunks 0 .. issued-1 have been copied (buffer j % NB)
+      for (int j = 0; j < nch; ++j) {
+        const int b = j % NB;
+        if (j >= NB) {
+          if (!mbar_wait(empty0 + 8 * b, (eph >> b) & 1u)) break;
+          eph ^= 1u << b;
+        }
+        issue(j, b);
+        issued = j + 1;
+        if (j + 2 < nch) prefetch_l2(j + 2);
+      }
+      // no copy may still be landing when the CTA exits (bounded waits; on the normal path
+      // every phase has completed already): buffer b took (issued - b + NB - 1) / NB copies
+#pragma unroll
+      for (int b = 0; b < NB; ++b)
+        if (b < issued) mbar_wait(bar0 + 8 * b, (uint32_t)(((issued - b + NB - 1) / NB - 1) & 1));
+    }
+    return;
+  }
 
   // ---- state in: this warp's S rows (key channels 16w..16w+15), all DV columns
   float S[DV / 8][4];
@@ -165,26 +205,9 @@ __global__ void __launch_bounds__(NT2, 1)
       *reinterpret_cast<uint32_t*>(sbf + ((r0 + 8) * SP + c) * 2) = bf2(S[nt][2], S[nt][3]);
     }
   };
-  // record + v slice of chunk i -> L2.  With three buffers the record copy itself is issued
-  // two chunks ahead, and a bulk prefetch of it as well only adds work for the TMA unit.
-  auto prefetch_l2 = [&](int i) {
-    if constexpr (NB == 2)
-      l2_prefetch(reinterpret_cast<const unsigned char*>(p.status) + kSplitHeader +
-                      ((int64_t)(slot0 + i) * H + h) * kRecBytes,
-                  kRecBytes);
-    tma_prefetch_2d(&maps.v, h * 128 + dv0, t0 + kChunk * i);
-  };
   stage_s(0);
   uint32_t phase = 0;   // bit b: parity to wait for on buffer b
-  int pending = 0;   // buffers with a fetch in flight (thread 0's view)
-  if (tid == 0) {   // chunks 0 .. NB-2 into their buffers; the next two to L2
-    for (int i = 0; i < NB - 1 && i < nch; ++i) {
-      issue(i, i);
-      pending |= 1 << i;
-    }
-    for (int i = NB - 1; i <= NB && i < nch; ++i) prefetch_l2(i);
-  }
-  __syncthreads();
+  group_sync(1, NTC);
 
   bool failed = false;
   const int mt = warp & 3;                 // 16-token row tile of U and O
@@ -195,25 +218,18 @@ __global__ void __launch_bounds__(NT2, 1)
     const int sidx = i & 1;                  // S bf16 staging of this chunk
     const int c0 = t0 + kChunk * i;
     const int L = min(kChunk, t1 - c0);
-    if (tid == 0 && i + NB - 1 < nch) {     // into the buffer chunk i-1 has finished with
-      const int nb = (i + NB - 1) % NB;
-      issue(i + NB - 1, nb);
-      pending |= 1 << nb;
-      if (i + NB + 1 < nch) prefetch_l2(i + NB + 1);
-    }
     const bool ok = mbar_wait(bar0 + 8 * buf, (phase >> buf) & 1u);
-    if (__syncthreads_or(!ok)) { failed = true; break; }
+    if (bar_any(1, NTC, !ok)) { failed = true; break; }
     phase ^= 1u << buf;
-    pending &= ~(1 << buf);
     unsigned char* rb = sm + buf * L_::BUF;
     const uint32_t rbs = smem_u32(rb);
     const float* vec = reinterpret_cast<const float*>(rb + B_VEC);   // decay[128], iq[64], ik[64]
     if (L < kChunk) {   // v rows past the sequence end -> 0
-      for (int idx = tid; idx < (kChunk - L) * DV / 2; idx += NT2) {
+      for (int idx = tid; idx < (kChunk - L) * DV / 2; idx += NTC) {
         const int r = L + idx / (DV / 2), c = 2 * (idx % (DV / 2));
         *reinterpret_cast<uint32_t*>(rb + B_V + swv<DV>(r, c)) = 0u;
       }
-      __syncthreads();
+      group_sync(1, NTC);
     }
 
     const uint32_t sbf = sb + L_::OFF_SB + sidx * 128 * SP * 2;   // S bf16 of this chunk
@@ -273,7 +289,7 @@ __global__ void __launch_bounds__(NT2, 1)
             bf2(u[2] * ik1, u[3] * ik1);
       }
     }
-    __syncthreads();
+    group_sync(1, NTC);
 
     // ---- O = (Qg S + QK U') scale/|q|  -> out
     {
@@ -346,16 +362,12 @@ __global__ void __launch_bounds__(NT2, 1)
         for (int e = 0; e < 4; ++e) S[nt][e] += S2[nt][e];
     }
     stage_s(sidx ^ 1);
-    __syncthreads();
+    group_sync(1, NTC);
+    if (tid == 0) mbar_arrive(empty0 + 8 * buf);   // every consumer is done with the buffer
   }
 
-  if (failed) {
-    if (tid == 0) {
-      record_error(p.status, KDA_ERR_DEVICE_TIMEOUT, 4);
-      // let fetches still in flight land (bounded) before the CTA exits
-      for (int b = 0; b < NB; ++b)
-        if (pending & (1 << b)) mbar_wait(bar0 + 8 * b, (phase >> b) & 1u);
-    }
+  if (failed) {   // (the producer lets the copies in flight land before it exits)
+    if (tid == 0) record_error(p.status, KDA_ERR_DEVICE_TIMEOUT, 4);
     return;
   }
   // ---- state out

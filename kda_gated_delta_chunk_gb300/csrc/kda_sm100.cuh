@@ -109,6 +109,27 @@ __device__ __forceinline__ void named_barrier_sync(uint32_t id, uint32_t count) 
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
 
+// barrier `id` over `count` threads with an OR reduction of `pred` (group-uniform result)
+// (the warp reconverges first: bar.red is an aligned barrier, and callers come out of
+// lane-divergent code such as one lane's mbarrier wait)
+__device__ __forceinline__ bool bar_any(uint32_t id, uint32_t count, bool pred) {
+  uint32_t r;
+  __syncwarp();
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.b32 p, %1, 0;\n\t"
+      "bar.red.or.pred q, %2, %3, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"((uint32_t)pred), "r"(id), "r"(count)
+      : "memory");
+  return r != 0;
+}
+// bar.sync over `count` threads, after the warp has reconverged
+__device__ __forceinline__ void group_sync(uint32_t id, uint32_t count) {
+  __syncwarp();
+  named_barrier_sync(id, count);
+}
 // Generic-proxy shared-memory writes -> visible to the async proxy (TMA,
 // tensor core).  Every thread that wrote an operand tile runs this before
 // the barrier that precedes the MMA issue.
