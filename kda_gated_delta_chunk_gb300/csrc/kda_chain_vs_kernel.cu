@@ -23,7 +23,8 @@
 // only on its own A row.  S_b, U_b (written here) and the v tile (TMA) are MN-major B
 // operands: K rows of 128 bytes in the 128-byte swizzle, of which the first DV columns are
 // the operand.  X is double-buffered, so that O of chunk c is drained while the first
-// products of chunk c+1 run.
+// products of chunk c+1 run; a producer warp copies the records and v tiles in, two stages
+// deep, so that no consumer stalls on issuing a copy.
 #include <cuda.h>
 
 #include "kda_internal.cuh"
@@ -34,17 +35,18 @@ namespace {
 
 using namespace sm100;
 
-// 8 warps: warp w reads TMEM lanes 32 (w % 4) .. 32 (w % 4) + 31 and value columns
-// [DV/2 (w / 4), DV/2 (w / 4 + 1)) of the slice
-constexpr int NT4 = 256;
+// 8 consumer warps: warp w reads TMEM lanes 32 (w % 4) .. 32 (w % 4) + 31 and value columns
+// [DV/2 (w / 4), DV/2 (w / 4 + 1)) of the slice; a ninth warp copies the records in
+constexpr int NTC4 = 256;
+constexpr int NT4 = NTC4 + 32;
 
 // ---- shared memory (offsets from a 1024-byte aligned base)
 constexpr int VS_V = kRecBytes + 1024;        // v tile [64 tok][64 cols] SW128 after the record
 constexpr int VS_STAGE = VS_V + 8192;         // record + v of one chunk
 constexpr int VS_SB = 2 * VS_STAGE;           // S_b: MN-major [128 dk][DV] in 128-byte rows
 constexpr int VS_UB = VS_SB + 16384;          // U_b: MN-major [64 tok][DV] in 128-byte rows
-constexpr int VS_BAR = VS_UB + 8192;          // full[2], g1, g2
-constexpr int VS_TSLOT = VS_BAR + 32;
+constexpr int VS_BAR = VS_UB + 8192;          // full[2], empty[2], g1, g2
+constexpr int VS_TSLOT = VS_BAR + 48;
 constexpr int VS_USED = VS_TSLOT + 16;
 constexpr int VS_BYTES = VS_USED + 1024;
 static_assert(VS_V % 1024 == 0 && VS_STAGE % 1024 == 0 && VS_SB % 1024 == 0 &&
@@ -98,7 +100,8 @@ __global__ void __launch_bounds__(NT4, 1)
   const uint32_t sb = smem_u32(sm);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + VS_TSLOT);
-  const uint32_t bar_full0 = sb + VS_BAR, bar_g1 = bar_full0 + 16, bar_g2 = bar_full0 + 24;
+  const uint32_t bar_full0 = sb + VS_BAR, bar_empty0 = bar_full0 + 16;
+  const uint32_t bar_g1 = bar_full0 + 32, bar_g2 = bar_full0 + 40;
 
   const int H = p.heads;
   const int unit = blockIdx.x;
@@ -120,6 +123,8 @@ __global__ void __launch_bounds__(NT4, 1)
   if (tid == 0) {
     mbar_init(bar_full0, 1);
     mbar_init(bar_full0 + 8, 1);
+    mbar_init(bar_empty0, 1);
+    mbar_init(bar_empty0 + 8, 1);
     mbar_init(bar_g1, 1);
     mbar_init(bar_g2, 1);
     mbar_fence_init();
@@ -142,7 +147,7 @@ __global__ void __launch_bounds__(NT4, 1)
     return reinterpret_cast<const unsigned char*>(p.status) + kSplitHeader +
            ((int64_t)(slot0 + i) * H + h) * kRecBytes;
   };
-  auto issue = [&](int i) {   // record + v columns [dv0, dv0 + 64) of chunk i -> stage i & 1
+  auto issue = [&](int i) {   // (producer) record + v columns [dv0, dv0 + 64) of chunk i -> stage i & 1
     const uint32_t st = sb + (i & 1) * VS_STAGE;
     const uint32_t bar = bar_full0 + 8 * (i & 1);
     mbar_expect_tx(bar, kRecBytes + 8192);
@@ -153,9 +158,28 @@ __global__ void __launch_bounds__(NT4, 1)
     l2_prefetch(rec_src(i), kRecBytes);
     tma_prefetch_2d(&maps.v, xcol, t0 + kChunk * i);
   };
-  if (tid == 0 && nch > 0) {
-    issue(0);
-    if (nch > 1) prefetch_l2(1);
+  if (warp == NTC4 / 32) {
+    // ---- producer: copies chunk j into stage j & 1 once the consumers are done with chunk
+    //      j - 2 there, so that no consumer stalls on issuing a copy
+    if (lane == 0) {
+      uint32_t eph = 0;   // bit b: parity of stage b's next "empty" phase
+      int issued = 0;
+      for (int j = 0; j < nch; ++j) {
+        const int b = j & 1;
+        if (j >= 2) {
+          if (!mbar_wait(bar_empty0 + 8 * b, (eph >> b) & 1u)) break;
+          eph ^= 1u << b;
+        }
+        issue(j);
+        issued = j + 1;
+        if (j + 1 < nch) prefetch_l2(j + 1);
+      }
+      // no copy may still be landing when the CTA exits (bounded; on the normal path every
+      // phase has completed already): stage b took (issued - b + 1) / 2 copies
+      for (int b = 0; b < 2; ++b)
+        if (b < issued) mbar_wait(bar_full0 + 8 * b, (uint32_t)(((issued - b + 1) / 2 - 1) & 1));
+    }
+    return;
   }
 
   // ---- state in: row (key channel) `row` of the slice, this thread's DH values -> TMEM
@@ -214,7 +238,6 @@ __global__ void __launch_bounds__(NT4, 1)
 
   uint32_t phase = 0;   // bit b: parity of stage b's next fill
   uint32_t ph_mma = 0;  // one fill per chunk of both bar_g1 and bar_g2
-  int pending = (nch > 0) ? 1 : 0;   // stages with a fetch in flight (thread 0's view)
   int mma_out = 0;      // 1: group 1 committed and not waited, 2: group 2 (thread 0)
   bool failed = false;
   int site = 0;
@@ -236,19 +259,11 @@ __global__ void __launch_bounds__(NT4, 1)
     //      the other stage (its last reader, group 2 of the previous chunk, has completed)
     {
       const bool ok = tid != 0 || mbar_wait(bar_full0 + 8 * buf, (phase >> buf) & 1u);
-      if (__syncthreads_or(!ok)) { failed = true; site = 61; break; }
+      if (bar_any(1, NTC4, !ok)) { failed = true; site = 61; break; }
       phase ^= 1u << buf;
-      if (tid == 0) {
-        pending &= ~(1 << buf);
-        if (i + 1 < nch) {
-          issue(i + 1);
-          pending |= 1 << (buf ^ 1);
-        }
-        if (i + 2 < nch) prefetch_l2(i + 2);
-      }
     }
     if (L < kChunk) {   // v rows past the sequence end -> 0
-      for (int idx = tid; idx < (kChunk - L) * 8; idx += NT4)
+      for (int idx = tid; idx < (kChunk - L) * 8; idx += NTC4)
         *reinterpret_cast<uint4*>(stp + VS_V + (L + idx / 8) * 128 + (idx % 8) * 16) =
             make_uint4(0, 0, 0, 0);
     }
@@ -273,7 +288,7 @@ __global__ void __launch_bounds__(NT4, 1)
     }
     fence_proxy_async();   // S_b and the zeroed v rows are read by the tensor cores
     tc_fence_before();
-    __syncthreads();   // (A)
+    group_sync(1, NTC4);   // (A)
 
     // ---- 3. X = [-W; Qg] S_b, Y = [T diag(b); *] V; meanwhile O of the previous chunk
     if (tid == 0) {
@@ -304,7 +319,7 @@ __global__ void __launch_bounds__(NT4, 1)
         if (ok) mma_out = 0;
       }
       tc_fence_before();
-      if (__syncthreads_or(!ok)) { failed = true; site = 62; break; }   // (B)
+      if (bar_any(1, NTC4, !ok)) { failed = true; site = 62; break; }   // (B)
     }
     tc_fence_after();
 
@@ -328,7 +343,7 @@ __global__ void __launch_bounds__(NT4, 1)
       fence_proxy_async();   // U_b is read by the tensor cores
     }
     tc_fence_before();
-    __syncthreads();   // (C)
+    group_sync(1, NTC4);   // (C)
 
     // ---- 5. X += [*; QK] U_b (O in rows 64-127), S += Ke^T U_b
     if (tid == 0) {
@@ -349,8 +364,9 @@ __global__ void __launch_bounds__(NT4, 1)
         if (ok) mma_out = 0;
       }
       tc_fence_before();
-      if (__syncthreads_or(!ok)) { failed = true; site = 63; break; }   // (D)
+      if (bar_any(1, NTC4, !ok)) { failed = true; site = 63; break; }   // (D)
       ph_mma ^= 1u;
+      if (tid == 0) mbar_arrive(bar_empty0 + 8 * buf);   // the stage is free for chunk i + 2
     }
     tc_fence_after();
   }
@@ -358,9 +374,8 @@ __global__ void __launch_bounds__(NT4, 1)
   if (failed) {
     if (tid == 0) {
       record_error(p.status, KDA_ERR_DEVICE_TIMEOUT, site);
-      // let fetches and MMAs still in flight finish (bounded) before the CTA exits
-      if (pending & 1) mbar_wait(bar_full0, phase & 1u);
-      if (pending & 2) mbar_wait(bar_full0 + 8, (phase >> 1) & 1u);
+      // let MMAs still in flight finish (bounded) before the CTA exits (the producer does the
+      // same for its copies)
       if (mma_out == 1) mbar_wait(bar_g1, ph_mma);
       if (mma_out == 2) mbar_wait(bar_g2, ph_mma);
     }
@@ -390,7 +405,7 @@ __global__ void __launch_bounds__(NT4, 1)
     }
   }
   tc_fence_before();
-  __syncthreads();
+  group_sync(1, NTC4);
   if (warp == 0) tmem_dealloc(tmem, T_COLS);
 }
 
