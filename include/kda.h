@@ -101,8 +101,10 @@ typedef struct CUstream_st* kda_stream_t;
 #define KDA_KERNEL_SPLIT 3 /* the K1/K2 structure of PR #52458: a chunk-parallel
                               k-side kernel writes per-(chunk, head) records to
                               the workspace, then one chain CTA per (sequence,
-                              head, value slice of 128 / P columns); P = 1 runs
-                              the chain on tcgen05 with the state in TMEM   */
+                              head, value slice of 128 / P columns); P = 1 and
+                              P = 2 run the chain on tcgen05 with the state
+                              (slice) in TMEM, P = 4 and 8 on warp-level
+                              MMAs with the slice in registers             */
 #define KDA_KERNEL_TC_HELPERS 4 /* TC (P = 1) plus k-side helper CTAs on the SMs
                               it leaves free: they write records for chunks
                               taken from the end of each sequence, which the
