@@ -9,9 +9,10 @@
 //               its own products it turns T into the bf16 operands of G1b and takes the
 //               QK rows out of the k-side's accumulator (both while its MMAs run);
 //   warps 4-19  k-side of chunk c+1: gate, cumsum, norms, operand tiles, the A
-//               extraction and Ke on all 16 warps; per-channel anchors and factors, row
-//               norms, beta and the UT inverse on warps 4-7; one thread each issues the
-//               k-side MMA and the input TMA.
+//               extraction and Ke on all 16 warps; per-channel anchors and factors on
+//               warps 4-11 (one 32-token block each half), row scales on 12-15, beta on
+//               16-17; the UT inverse on warps 4-7; one thread each issues the k-side MMA
+//               and the input TMA.
 // The k-side hands each chunk over through one shared-memory stage guarded by
 // mbarriers (stage full: k-side -> chain; stage parts free: chain -> k-side).
 //
@@ -643,11 +644,11 @@ __global__ void __launch_bounds__(PNT, 1)
       tma_prefetch_desc(&maps.g);
       if (nch > 0) issue_in(0);
     }
-    // raw beta logits of the next chunk, fetched a chunk ahead (threads 128 .. 191)
+    // raw beta logits of the next chunk, fetched a chunk ahead (threads 384 .. 447)
     // (kept as the raw bf16 bits, converted only when used a chunk later, so that no warp
     // waits for the global load before the barrier that ends K2)
     unsigned short b_raw = 0;
-    const int bt = kt - 128;
+    const int bt = kt - 384;
     if (bt >= 0 && bt < PC && t0 + bt < t1) b_raw = __bfloat16_as_ushort(p.beta[(size_t)(t0 + bt) * p.s_beta + h]);
 
     for (int c = 0; c < nch; ++c) {
@@ -715,46 +716,53 @@ __global__ void __launch_bounds__(PNT, 1)
       group_sync(1, 512);
       PSTAMP(kt == 0, c, 17);
 
-      // ---- K2 (threads < 128): anchors and factors per key channel; row norms and scales;
-      //      (threads 128 .. 191): beta
-      if (kt < 128) {
-        {
-          const int d = kt;
-          float P[16];
-          float run = 0.0f;
+      // ---- K2: anchors and factors per key channel, one 32-token block per thread group
+      //      (threads < 128: block 0, 128 .. 255: block 1); row norms and scales (256 .. 383);
+      //      beta (384 .. 447)
+      if (kt < 256) {
+        const int d = kt & 127, blk = kt >> 7;
+        float Q[8];   // inclusive prefix over the block's eight row quads
+        float run = 0.0f;
 #pragma unroll
-          for (int q = 0; q < 16; ++q) {
-            run += GT[q * 128 + d];
-            P[q] = run;
-          }
-          const float m0 = P[3], g31 = P[7], m1 = P[11], g63 = P[15];
-#pragma unroll
-          for (int q = 0; q < 16; ++q) GT[q * 128 + d] = (q < 8 ? m0 : m1) - (q ? P[q - 1] : 0.0f);
-          FAC[0 * 128 + d] = ex2f(g31 - m0);   // Ke, Kc2 of block 0, step 1: 2^(G31 - G)
-          FAC[1 * 128 + d] = ex2f(g63 - g31);  // Ke of block 0, step 2
-          FAC[2 * 128 + d] = ex2f(m1 - g31);   // Kc2 step 2; Qg/Kg of block 1, step 1
-          FAC[3 * 128 + d] = ex2f(m0);         // Qg/Kg of block 0
-          FAC[4 * 128 + d] = ex2f(g63 - m1);   // Ke of block 1
-          FAC[5 * 128 + d] = ex2f(g31);        // Qg/Kg of block 1, step 2
-          vec[d] = ex2f(g63);                  // decay of the state
+        for (int q = 0; q < 8; ++q) {
+          run += GT[(8 * blk + q) * 128 + d];
+          Q[q] = run;
         }
-        {
-          const int r = kt & 63;
-          const float ss = SS[kt];
-          // ss < 2^(e+1) -> |row| < 2^ceil((e+1)/2): rows enter the operands times 2^-sh
-          const int e = ((__float_as_int(ss) >> 23) & 255) - 127;
-          const int sh = max(-60, min(60, (e + 2) >> 1));
-          const float rs = (r < L) ? rsqrtf(ss + kL2Eps) : 0.0f;
-          if (kt < 64) {
-            // q rows enter the operands as q scale / |q| (their norm is scale): O comes out of
-            // the products already normalised
-            const uint32_t qs = pack_bf16x2(p.scale * rs, p.scale * rs);
-            RSC[kt] = qs;
-          } else {
-            vec[192 + r] = rs * __int_as_float((127 + sh) << 23);   // 1 / |k| against k 2^-sh
-            const uint32_t bb = (uint32_t)(127 - sh) << 7;           // bf16 bits of 2^-sh
-            RSC[kt] = bb | (bb << 16);
-          }
+        float g31 = 0.0f;   // block 1: the total of block 0 (for the state decay)
+        if (blk) {
+#pragma unroll
+          for (int q = 0; q < 8; ++q) g31 += GT[q * 128 + d];
+        }
+        group_sync(5, 256);   // every quad total has been read
+        // anchor offsets of the block's quads: the anchor (the block's total up to its 16th
+        // token) minus the total before the quad; block 0's total cancels in block 1
+#pragma unroll
+        for (int q = 0; q < 8; ++q) GT[(8 * blk + q) * 128 + d] = Q[3] - (q ? Q[q - 1] : 0.0f);
+        if (!blk) {   // Q = G over tokens 0-31
+          FAC[0 * 128 + d] = ex2f(Q[7] - Q[3]);   // Ke, Kc2 of block 0, step 1: 2^(G31 - G)
+          FAC[3 * 128 + d] = ex2f(Q[3]);          // Qg/Kg of block 0
+          FAC[5 * 128 + d] = ex2f(Q[7]);          // Qg/Kg of block 1, step 2: 2^G31
+        } else {      // Q = G - G31 over tokens 32-63
+          FAC[1 * 128 + d] = ex2f(Q[7]);          // Ke of block 0, step 2: 2^(G63 - G31)
+          FAC[2 * 128 + d] = ex2f(Q[3]);          // Kc2 step 2; Qg/Kg of block 1, step 1
+          FAC[4 * 128 + d] = ex2f(Q[7] - Q[3]);   // Ke of block 1
+          vec[d] = ex2f(g31 + Q[7]);              // decay of the state: 2^G63
+        }
+      } else if (kt < 384) {
+        const int rr = kt - 256, r = rr & 63;
+        const float ss = SS[rr];
+        // ss < 2^(e+1) -> |row| < 2^ceil((e+1)/2): rows enter the operands times 2^-sh
+        const int e = ((__float_as_int(ss) >> 23) & 255) - 127;
+        const int sh = max(-60, min(60, (e + 2) >> 1));
+        const float rs = (r < L) ? rsqrtf(ss + kL2Eps) : 0.0f;
+        if (rr < 64) {
+          // q rows enter the operands as q scale / |q| (their norm is scale): O comes out of
+          // the products already normalised
+          RSC[rr] = pack_bf16x2(p.scale * rs, p.scale * rs);
+        } else {
+          vec[192 + r] = rs * __int_as_float((127 + sh) << 23);   // 1 / |k| against k 2^-sh
+          const uint32_t bb = (uint32_t)(127 - sh) << 7;           // bf16 bits of 2^-sh
+          RSC[rr] = bb | (bb << 16);
         }
       } else if (bt < PC) {
         vec[320 + bt] = (bt < L) ? sigm(__uint_as_float((uint32_t)b_raw << 16)) : 0.0f;   // b
