@@ -87,7 +87,7 @@ constexpr int PS_FAC = PS_GT + 16 * 128 * 4;          // per-channel factors [6]
 constexpr int PS_SS = PS_FAC + 6 * 128 * 4;           // row sums of squares: q [64], k [64]
 constexpr int PS_RSC = PS_SS + 128 * 4;               // row power-of-two scales, bf16x2 [128]
 constexpr int PS_BAR = PS_RSC + 128 * 4;              // mbarriers
-constexpr int PS_TSLOT = PS_BAR + 16 * 8;   // (10 mbarriers used)
+constexpr int PS_TSLOT = PS_BAR + 16 * 8;   // (12 mbarriers used)
 constexpr int PS_FLAGS = PS_TSLOT + 16;
 constexpr int PS_TM = PS_FLAGS + 16;      // T [64][NS] fp32
 constexpr int PS_END = PS_TM + 64 * NS * 4;
