@@ -291,75 +291,137 @@ __global__ void __launch_bounds__(NT2, 1)
     }
     group_sync(1, NTC);
 
-    // ---- O = (Qg S + QK U') scale/|q|  -> out
-    {
-#pragma unroll
-      for (int ks = 0; ks < 4; ++ks) {
-        uint32_t a[4];
-        const int row = 16 * mt + (lane & 15), col = 16 * ks + 8 * (lane >> 4);
-        ldsm_x4(rbs + B_QKE + sw128(row, col, 192), a);   // QK: rows 0-63 of [QK; Ke]
-#pragma unroll
-        for (int j = 0; j < NPW; ++j) {
-          uint32_t b[2];
-          const int k = 16 * ks + (lane & 15), c = 8 * (ng + 2 * j);
-          ldsm_x2_t(ubf + (k * SP + c) * 2, b);
-          mma16816((ks & 1) ? O1[j] : O[j], a, b[0], b[1]);
-        }
-      }
-      const int r0 = 16 * mt + g;
-      const float iq0 = vec[128 + r0], iq1 = vec[128 + r0 + 8];
-      int64_t row0 = c0 + r0, row1 = c0 + r0 + 8;
-      bool w0 = r0 < L, w1 = r0 + 8 < L;
-      if (kRowMap) {
-        row0 = w0 ? out_row(p, row0) : -1;
-        row1 = w1 ? out_row(p, row1) : -1;
-        w0 = row0 >= 0;
-        w1 = row1 >= 0;
-      }
-#pragma unroll
-      for (int j = 0; j < NPW; ++j) {
-        const int c = dv0 + 8 * (ng + 2 * j) + 2 * t;
-        if (w0)
-          *reinterpret_cast<uint32_t*>(p.out + (size_t)row0 * HD + h * 128 + c) =
-              bf2((O[j][0] + O1[j][0]) * iq0, (O[j][1] + O1[j][1]) * iq0);
-        if (w1)
-          *reinterpret_cast<uint32_t*>(p.out + (size_t)row1 * HD + h * 128 + c) =
-              bf2((O[j][2] + O1[j][2]) * iq1, (O[j][3] + O1[j][3]) * iq1);
-      }
-    }
-
-    // ---- S = diag(2^Gam_last) S + Ke^T U'   (this warp: key rows 16 warp.., all columns;
-    //      tokens 32-63 of the product in a second accumulator)
-    {
-      const float d0 = vec[16 * warp + g], d1 = vec[16 * warp + g + 8];
-      float S2[DV / 8][4];
-#pragma unroll
-      for (int nt = 0; nt < DV / 8; ++nt) {
-        S[nt][0] *= d0;
-        S[nt][1] *= d0;
-        S[nt][2] *= d1;
-        S[nt][3] *= d1;
-        S2[nt][0] = S2[nt][1] = S2[nt][2] = S2[nt][3] = 0.0f;
-      }
-#pragma unroll
-      for (int ks = 0; ks < 4; ++ks) {
-        uint32_t a[4];
-        {   // A = Ke^T: rows 64 + dk of [QK; Ke], K = token
-          const int row = 16 * warp + (lane & 15), col = 16 * ks + 8 * (lane >> 4);
-          ldsm_x4(rbs + B_QKE + sw128(64 + row, col, 192), a);
-        }
-#pragma unroll
+    if constexpr (DV == 16) {
+      // ---- 16-column slice: O = (Qg S + QK U') scale/|q| -> out and S = diag(2^Gam_last) S +
+      //      Ke^T U' in one k-step loop: the two products' mma chains are independent, so their
+      //      latencies overlap, and O's U' fragments are the ones S loads anyway (4% faster at
+      //      DV = 16, 4% slower at DV = 32, which keeps the two loops below).  S: this warp's key
+      //      rows 16 warp.., all columns; each product's tokens 32-63 go to a second accumulator.
+      {
+        const float d0 = vec[16 * warp + g], d1 = vec[16 * warp + g + 8];
+        float S2[DV / 8][4];
+  #pragma unroll
         for (int nt = 0; nt < DV / 8; ++nt) {
-          uint32_t b[2];
-          const int k = 16 * ks + (lane & 15), c = 8 * nt;
-          ldsm_x2_t(ubf + (k * SP + c) * 2, b);
-          mma16816(ks < 2 ? S[nt] : S2[nt], a, b[0], b[1]);
+          S[nt][0] *= d0;
+          S[nt][1] *= d0;
+          S[nt][2] *= d1;
+          S[nt][3] *= d1;
+          S2[nt][0] = S2[nt][1] = S2[nt][2] = S2[nt][3] = 0.0f;
+        }
+  #pragma unroll
+        for (int ks = 0; ks < 4; ++ks) {
+          uint32_t aq[4], ak[4];
+          {
+            const int col = 16 * ks + 8 * (lane >> 4);
+            ldsm_x4(rbs + B_QKE + sw128(16 * mt + (lane & 15), col, 192), aq);        // QK rows
+            ldsm_x4(rbs + B_QKE + sw128(64 + 16 * warp + (lane & 15), col, 192), ak);  // Ke^T
+          }
+  #pragma unroll
+          for (int nt = 0; nt < DV / 8; ++nt) {
+            uint32_t b[2];
+            const int k = 16 * ks + (lane & 15), c = 8 * nt;
+            ldsm_x2_t(ubf + (k * SP + c) * 2, b);
+            if ((nt & 1) == ng)   // O: this warp's n8 tiles ng, ng + 2, ...
+              mma16816((ks & 1) ? O1[nt >> 1] : O[nt >> 1], aq, b[0], b[1]);
+            mma16816(ks < 2 ? S[nt] : S2[nt], ak, b[0], b[1]);
+          }
+        }
+        const int r0 = 16 * mt + g;
+        const float iq0 = vec[128 + r0], iq1 = vec[128 + r0 + 8];
+        int64_t row0 = c0 + r0, row1 = c0 + r0 + 8;
+        bool w0 = r0 < L, w1 = r0 + 8 < L;
+        if (kRowMap) {
+          row0 = w0 ? out_row(p, row0) : -1;
+          row1 = w1 ? out_row(p, row1) : -1;
+          w0 = row0 >= 0;
+          w1 = row1 >= 0;
+        }
+  #pragma unroll
+        for (int j = 0; j < NPW; ++j) {
+          const int c = dv0 + 8 * (ng + 2 * j) + 2 * t;
+          if (w0)
+            *reinterpret_cast<uint32_t*>(p.out + (size_t)row0 * HD + h * 128 + c) =
+                bf2((O[j][0] + O1[j][0]) * iq0, (O[j][1] + O1[j][1]) * iq0);
+          if (w1)
+            *reinterpret_cast<uint32_t*>(p.out + (size_t)row1 * HD + h * 128 + c) =
+                bf2((O[j][2] + O1[j][2]) * iq1, (O[j][3] + O1[j][3]) * iq1);
+        }
+  #pragma unroll
+        for (int nt = 0; nt < DV / 8; ++nt)
+  #pragma unroll
+          for (int e = 0; e < 4; ++e) S[nt][e] += S2[nt][e];
+      }
+    } else {
+      // ---- O = (Qg S + QK U') scale/|q|  -> out
+      {
+  #pragma unroll
+        for (int ks = 0; ks < 4; ++ks) {
+          uint32_t a[4];
+          const int row = 16 * mt + (lane & 15), col = 16 * ks + 8 * (lane >> 4);
+          ldsm_x4(rbs + B_QKE + sw128(row, col, 192), a);   // QK: rows 0-63 of [QK; Ke]
+  #pragma unroll
+          for (int j = 0; j < NPW; ++j) {
+            uint32_t b[2];
+            const int k = 16 * ks + (lane & 15), c = 8 * (ng + 2 * j);
+            ldsm_x2_t(ubf + (k * SP + c) * 2, b);
+            mma16816((ks & 1) ? O1[j] : O[j], a, b[0], b[1]);
+          }
+        }
+        const int r0 = 16 * mt + g;
+        const float iq0 = vec[128 + r0], iq1 = vec[128 + r0 + 8];
+        int64_t row0 = c0 + r0, row1 = c0 + r0 + 8;
+        bool w0 = r0 < L, w1 = r0 + 8 < L;
+        if (kRowMap) {
+          row0 = w0 ? out_row(p, row0) : -1;
+          row1 = w1 ? out_row(p, row1) : -1;
+          w0 = row0 >= 0;
+          w1 = row1 >= 0;
+        }
+  #pragma unroll
+        for (int j = 0; j < NPW; ++j) {
+          const int c = dv0 + 8 * (ng + 2 * j) + 2 * t;
+          if (w0)
+            *reinterpret_cast<uint32_t*>(p.out + (size_t)row0 * HD + h * 128 + c) =
+                bf2((O[j][0] + O1[j][0]) * iq0, (O[j][1] + O1[j][1]) * iq0);
+          if (w1)
+            *reinterpret_cast<uint32_t*>(p.out + (size_t)row1 * HD + h * 128 + c) =
+                bf2((O[j][2] + O1[j][2]) * iq1, (O[j][3] + O1[j][3]) * iq1);
         }
       }
-#pragma unroll
-      for (int nt = 0; nt < DV / 8; ++nt)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) S[nt][e] += S2[nt][e];
+
+      // ---- S = diag(2^Gam_last) S + Ke^T U'   (this warp: key rows 16 warp.., all columns;
+      //      tokens 32-63 of the product in a second accumulator)
+      {
+        const float d0 = vec[16 * warp + g], d1 = vec[16 * warp + g + 8];
+        float S2[DV / 8][4];
+  #pragma unroll
+        for (int nt = 0; nt < DV / 8; ++nt) {
+          S[nt][0] *= d0;
+          S[nt][1] *= d0;
+          S[nt][2] *= d1;
+          S[nt][3] *= d1;
+          S2[nt][0] = S2[nt][1] = S2[nt][2] = S2[nt][3] = 0.0f;
+        }
+  #pragma unroll
+        for (int ks = 0; ks < 4; ++ks) {
+          uint32_t a[4];
+          {   // A = Ke^T: rows 64 + dk of [QK; Ke], K = token
+            const int row = 16 * warp + (lane & 15), col = 16 * ks + 8 * (lane >> 4);
+            ldsm_x4(rbs + B_QKE + sw128(64 + row, col, 192), a);
+          }
+  #pragma unroll
+          for (int nt = 0; nt < DV / 8; ++nt) {
+            uint32_t b[2];
+            const int k = 16 * ks + (lane & 15), c = 8 * nt;
+            ldsm_x2_t(ubf + (k * SP + c) * 2, b);
+            mma16816(ks < 2 ? S[nt] : S2[nt], a, b[0], b[1]);
+          }
+        }
+  #pragma unroll
+        for (int nt = 0; nt < DV / 8; ++nt)
+  #pragma unroll
+          for (int e = 0; e < 4; ++e) S[nt][e] += S2[nt][e];
+      }
     }
     stage_s(sidx ^ 1);
     group_sync(1, NTC);
