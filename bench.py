@@ -81,34 +81,46 @@ def load_peaks():
 
 # host-only translation unit (argument checks, planning, the C entry points): no device code
 HOST_ONLY_SOURCES = ("kda_api.cu",)
+# the sources a kernel is built from, where that is a strict subset (headers included): its
+# committed traffic figure stays valid while these are unchanged.  Other kernels hash every
+# device source.
+KERNEL_SOURCES = {
+    "kda_pipe_kernel": ("kda_pipe_kernel.cu", "kda_internal.cuh", "kda_sm100.cuh",
+                        "kda_tc_common.cuh"),
+}
 
 
-def kernel_source_hash() -> str:
-    """Hash of the kernels' CUDA sources (every file but the host-only ones) with comments and
-    blank space removed: it changes when kernel or launch code does, not when a comment or
-    a host-side entry point does."""
+def kernel_source_hash(kernel_name: str | None = None) -> str:
+    """Hash of a kernel's CUDA sources (KERNEL_SOURCES, else every file but the host-only
+    ones) with comments and blank space removed: it changes when kernel or launch code does,
+    not when a comment or a host-side entry point does."""
     import re
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "kda_gated_delta_chunk_gb300", "csrc")
+    names = KERNEL_SOURCES.get(kernel_name) if kernel_name else None
     for name in sorted(os.listdir(csrc)):
-        if name.endswith((".cu", ".cuh")) and name not in HOST_ONLY_SOURCES:
-            text = open(os.path.join(csrc, name), encoding="utf-8").read()
-            text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
-            text = re.sub(r"//[^\n]*", " ", text)
-            text = " ".join(text.split())
-            h.update(name.encode() + b"\0" + text.encode())
+        if not name.endswith((".cu", ".cuh")) or name in HOST_ONLY_SOURCES:
+            continue
+        if names is not None and name not in names:
+            continue
+        text = open(os.path.join(csrc, name), encoding="utf-8").read()
+        text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+        text = re.sub(r"//[^\n]*", " ", text)
+        text = " ".join(text.split())
+        h.update(name.encode() + b"\0" + text.encode())
     return h.hexdigest()[:16]
 
 
 def load_traffic(kernel_name: str, workload: str):
     """DRAM bytes per launch from the committed ncu summary, if it was taken
-    on the current kernel sources and this workload (else None)."""
+    on the current sources of that kernel and this workload (else None)."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(p):
         return None
     d = json.load(open(p))
     ent = d.get(kernel_name)
-    if not ent or ent.get("source_hash") != kernel_source_hash() or ent.get("workload") != workload:
+    if (not ent or ent.get("source_hash") != kernel_source_hash(kernel_name)
+            or ent.get("workload") != workload):
         return None
     return ent.get("dram_bytes_per_launch")
 
