@@ -313,24 +313,25 @@ __global__ void __launch_bounds__(NT, 2)
 
     // ---- P2a: gate -> log2 decay, cumsum inside each 8-row group of this thread; the
     //           partial sums of squares of q and k
-    float cl0[16], cl1[16];
+    // (the thread's channel pair as packed fp32x2 throughout: the same roundings, half the
+    // instructions)
+    float2 cl[16];
+    const float2 sg2 = make_float2(sg, sg), sgd = make_float2(sg0, sg1);
 #pragma unroll
     for (int gh = 0; gh < 2; ++gh) {
-      float run0 = 0.0f, run1 = 0.0f;
+      float2 run = make_float2(0.0f, 0.0f);
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
         const int r = 16 * rq + 8 * gh + i;
         const float2 gv = unpack_bf16x2(ld_u32(sm + K_ING, (uint32_t)(r * 256 + d0 * 2)));
-        float a0 = lb2 * rcpf(1.0f + ex2f(fmaf(gv.x, sg, sg0)));
-        float a1 = lb2 * rcpf(1.0f + ex2f(fmaf(gv.y, sg, sg1)));
-        a0 = (r < L) ? a0 : 0.0f;
-        a1 = (r < L) ? a1 : 0.0f;
-        run0 += a0;
-        run1 += a1;
-        cl0[8 * gh + i] = run0;
-        cl1[8 * gh + i] = run1;
+        const float2 z = __ffma2_rn(gv, sg2, sgd);
+        const float2 dd = __fadd2_rn(make_float2(ex2f(z.x), ex2f(z.y)), make_float2(1.0f, 1.0f));
+        float2 a = __fmul2_rn(make_float2(rcpf(dd.x), rcpf(dd.y)), make_float2(lb2, lb2));
+        if (r >= L) a = make_float2(0.0f, 0.0f);
+        run = __fadd2_rn(run, a);
+        cl[8 * gh + i] = run;
       }
-      *reinterpret_cast<float2*>(gt + (2 * rq + gh) * 128 + d0) = make_float2(run0, run1);
+      *reinterpret_cast<float2*>(gt + (2 * rq + gh) * 128 + d0) = run;
       // sums of squares of the group's q and k rows over this warp's 64 channels,
       // reduce-scattered: lanes 2j, 2j + 1 end with the sum of v[j] ([0, 8) q, [8, 16) k)
       float v[16];
@@ -421,38 +422,38 @@ __global__ void __launch_bounds__(NT, 2)
           }
         }
       }
+      const float2 cA2 = make_float2(cA[0], cA[1]), cB2 = make_float2(cB[0], cB[1]);
+      const float2 cX2 = make_float2(cX[0], cX[1]), cR2 = make_float2(cR[0], cR[1]);
 #pragma unroll
       for (int gh = 0; gh < 2; ++gh) {
         uint32_t qg[8], ke[8];
+        const float2 nmE = make_float2(-mE[gh][0], -mE[gh][1]);
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
           const int ii = 8 * gh + i;
           const int r = 16 * rq + ii;
           const uint32_t q2 = bmul2(ld_u32(sm + K_INQ, (uint32_t)(r * 256 + d0 * 2)), rsc[r]);
           const uint32_t k2 = bmul2(ld_u32(sm + K_INK, (uint32_t)(r * 256 + d0 * 2)), rsc[64 + r]);
-          const float e0 = cl0[ii] - mE[gh][0], e1 = cl1[ii] - mE[gh][1];
-          const float E0 = ex2f(e0), E1 = ex2f(e1), Ei0 = ex2f(-e0), Ei1 = ex2f(-e1);
-          const uint32_t E2 = pack_bf16x2(E0, E1), Ei2 = pack_bf16x2(Ei0, Ei1);
+          const float2 e = __fadd2_rn(cl[ii], nmE);
+          const float2 E = make_float2(ex2f(e.x), ex2f(e.y));
+          const float2 Ei = make_float2(ex2f(-e.x), ex2f(-e.y));
+          const uint32_t E2 = pack_bf16x2(E.x, E.y), Ei2 = pack_bf16x2(Ei.x, Ei.y);
           st_u32(sm, K_RKQ + kmajor_off(r, d0, 128), bmul2(k2, E2));
           st_u32(sm, K_RKQ + kmajor_off(64 + r, d0, 128), bmul2(q2, E2));
           st_u32(sm, K_CKC + kmajor_off(r, d0, 96), bmul2(k2, Ei2));
-          float g0, g1, ke0, ke1;
+          float2 gg, kk;
           if (blk == 0) {
-            const float oc0 = Ei0 * cB[0], oc1 = Ei1 * cB[1];    // 2^(B0 - c_s)
-            st_u32(sm, K_CKC + kmajor_off(64 + r, d0, 96),
-                   bmul2(k2, pack_bf16x2(oc0 * cX[0], oc1 * cX[1])));
-            g0 = E0 * cA[0];
-            g1 = E1 * cA[1];
-            ke0 = oc0 * cR[0];
-            ke1 = oc1 * cR[1];
+            const float2 oc = __fmul2_rn(Ei, cB2);    // 2^(B0 - c_s)
+            const float2 c2 = __fmul2_rn(oc, cX2);
+            st_u32(sm, K_CKC + kmajor_off(64 + r, d0, 96), bmul2(k2, pack_bf16x2(c2.x, c2.y)));
+            gg = __fmul2_rn(E, cA2);
+            kk = __fmul2_rn(oc, cR2);
           } else {
-            g0 = (E0 * cA[0]) * cR[0];
-            g1 = (E1 * cA[1]) * cR[1];
-            ke0 = Ei0 * cB[0];
-            ke1 = Ei1 * cB[1];
+            gg = __fmul2_rn(__fmul2_rn(E, cA2), cR2);
+            kk = __fmul2_rn(Ei, cB2);
           }
-          qg[i] = bmul2(q2, pack_bf16x2(g0, g1));
-          ke[i] = bmul2(k2, pack_bf16x2(ke0, ke1));
+          qg[i] = bmul2(q2, pack_bf16x2(gg.x, gg.y));
+          ke[i] = bmul2(k2, pack_bf16x2(kk.x, kk.y));
         }
         // 8 consecutive tokens of one channel = one 16-byte chunk of each image
         const int r0 = 16 * rq + 8 * gh;
