@@ -161,19 +161,22 @@ def chunk_forward(q, k, v, g, beta, A_log, dt_bias, lower_bound, scale,
                             assert np.all(np.isfinite(f[name])), name
                     KK = np.zeros((L, L))
                     QK = np.zeros((L, L))
-                    for i in range(f["nb"]):
-                        r0, r1 = i * sub, min(L, (i + 1) * sub)
-                        Er, Eir = f["E"][r0:r1], f["Ei"][r0:r1]
-                        KK[r0:r1, r0:r1] = rnd(kh[r0:r1] * Er) @ rnd(kh[r0:r1] * Eir).T
-                        QK[r0:r1, r0:r1] = rnd(qh[r0:r1] * Er) @ rnd(kh[r0:r1] * Eir).T
-                        for j in range(i):
-                            s0, s1 = j * sub, (j + 1) * sub
-                            pr, pc = f["pair_row"][(i, j)], f["pair_col"][(i, j)]
-                            if check_finite:
-                                assert np.all(np.isfinite(pr)) and np.all(np.isfinite(pc))
-                            colop = rnd(kh[s0:s1] * pc)
-                            KK[r0:r1, s0:s1] = rnd(kh[r0:r1] * pr) @ colop.T
-                            QK[r0:r1, s0:s1] = rnd(qh[r0:r1] * pr) @ colop.T
+                    # (inside a diagonal block the anti-causal entries, s > r, can overflow:
+                    # their factors grow the other way; np.tril below drops them)
+                    with np.errstate(over="ignore", invalid="ignore"):
+                        for i in range(f["nb"]):
+                            r0, r1 = i * sub, min(L, (i + 1) * sub)
+                            Er, Eir = f["E"][r0:r1], f["Ei"][r0:r1]
+                            KK[r0:r1, r0:r1] = rnd(kh[r0:r1] * Er) @ rnd(kh[r0:r1] * Eir).T
+                            QK[r0:r1, r0:r1] = rnd(qh[r0:r1] * Er) @ rnd(kh[r0:r1] * Eir).T
+                            for j in range(i):
+                                s0, s1 = j * sub, (j + 1) * sub
+                                pr, pc = f["pair_row"][(i, j)], f["pair_col"][(i, j)]
+                                if check_finite:
+                                    assert np.all(np.isfinite(pr)) and np.all(np.isfinite(pc))
+                                colop = rnd(kh[s0:s1] * pc)
+                                KK[r0:r1, s0:s1] = rnd(kh[r0:r1] * pr) @ colop.T
+                                QK[r0:r1, s0:s1] = rnd(qh[r0:r1] * pr) @ colop.T
                     KK = np.tril(KK, -1)
                     QK = np.tril(QK, 0)
                     g_row = np.asarray(f["g_row"], np.float64)
