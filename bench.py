@@ -92,8 +92,8 @@ KERNEL_SOURCES = {
 
 def kernel_source_hash(kernel_name: str | None = None) -> str:
     """Hash of a kernel's CUDA sources (KERNEL_SOURCES, else every file but the host-only
-    ones) with comments and blank space removed: it changes when kernel or launch code does,
-    not when a comment or a host-side entry point does."""
+    ones) with comments, phase stamps and blank space removed: it changes when kernel or
+    launch code does, not when a comment, a stamp or a host-side entry point does."""
     import re
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "kda_gated_delta_chunk_gb300", "csrc")
@@ -106,6 +106,7 @@ def kernel_source_hash(kernel_name: str | None = None) -> str:
         text = open(os.path.join(csrc, name), encoding="utf-8").read()
         text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
         text = re.sub(r"//[^\n]*", " ", text)
+        text = re.sub(r"PSTAMP\([^;]*\);", " ", text)   # phase stamps: empty outside the stamps build
         text = " ".join(text.split())
         h.update(name.encode() + b"\0" + text.encode())
     return h.hexdigest()[:16]
@@ -324,19 +325,19 @@ CHAIN_SLOTS = {0: "stage part A full", 2: "v ready", 3: "G1a issued", 12: "S dec
                28: "G1b done (thread 0)", 27: "QK operand stored", 6: "chain group past G1b",
                7: "U_b stored", 8: "G2 done", 10: "O stored"}
 CHAIN_ORDER = [0, 2, 3, 12, 4, 5, 26, 28, 27, 6, 7, 8, 10]
-KSIDE_SLOTS = {16: "inputs landed", 17: "gate and norms", 18: "factors, [Kg; Qg] free",
-               20: "tile rows done", 21: "tiles fenced", 22: "A|QK MMA done",
-               1: "Ke and T parts free", 23: "A loaded", 24: "N, Ke stored",
-               19: "upper blocks zeroed", 14: "diagonal blocks", 11: "level 1 first product",
-               13: "level 1 second product", 15: "level 1", 9: "level 2a",
-               29: "stage handed over"}
-KSIDE_ORDER = [16, 17, 18, 20, 21, 22, 1, 23, 24, 19, 14, 11, 13, 15, 9, 29]
+KSIDE_SLOTS = {19: "loop top", 25: "input wait (MMA thread)", 16: "inputs landed",
+               17: "gate and norms", 18: "factors, [Kg; Qg] free", 20: "tile rows done",
+               21: "tiles fenced", 22: "A|QK MMA done", 1: "Ke and T parts free",
+               24: "N, Ke stored", 29: "inverse, stage handed over"}
+KSIDE_ORDER = [19, 25, 16, 17, 18, 20, 21, 22, 1, 24, 29]
 
 
 def run_stamps(args):
     """Phase breakdown of KDA_KERNEL_PIPE: build the phase-stamp variant of the library
     (-DKDA_PHASE_STAMPS), run the workload a few times, read the clock64 stamps CTA 0 (the
-    longest sequence, head 0) wrote per chunk, print medians over its inner chunks."""
+    longest sequence, head 0) wrote per chunk, print medians over its inner chunks.  The
+    k-side's stamps come from a thread of warp 19, which the inverse does not use: stamps
+    taken by a warp inside a phase lengthen that phase."""
     from kda_gated_delta_chunk_gb300 import build as kbuild
     import kda_gated_delta_chunk_gb300 as kda
     path = kbuild.build(stamps=True)
@@ -375,7 +376,8 @@ def run_stamps(args):
            "chain_wait_for_stage (O stored c-1 -> stage full c)": med(10, 0, True),
            "handover -> chain start": med(29, 0),
            "chain G1a done (c-1) -> kside factors, [Kg; Qg] free (c)": med(4, 18, True),
-           "inverse: diagonal blocks of warp 5 (N stored -> done)": med(24, 25)}
+           "chain QK rows of D free (c-1) -> kside tiles fenced (c)": med(27, 21, True),
+           "chain G2 done (c-1) -> kside Ke and T parts free (c)": med(8, 1, True)}
     print(json.dumps(res, indent=1), flush=True)
 
 

@@ -660,10 +660,12 @@ __global__ void __launch_bounds__(PNT, 1)
       float cl[4][4];   // inclusive cumsums of this thread's 4 rows, 4 channels
 
       // ---- K1: gate -> log2 decay, cumsum over this thread's 4 rows; row sums of squares
+      PSTAMP(kt == 480, c, 19);
       if (mma_thread) ok = wait_phase(bar(B_IN), par);
+      PSTAMP(mma_thread, c, 25);
       if (bar_any(1, 512, !ok)) { failed = true; site = 20; break; }
       if (tma_thread) in_pend = 0;
-      PSTAMP(kt == 0, c, 16);
+      PSTAMP(kt == 480, c, 16);
       {
         // two channels per packed fp32x2 operation throughout
         const float2 sg2 = make_float2(sg, sg), lb22 = make_float2(lb2, lb2);
@@ -714,7 +716,7 @@ __global__ void __launch_bounds__(PNT, 1)
       *reinterpret_cast<float4*>(GT + j * 128 + 4 * o4) =
           make_float4(cl[3][0], cl[3][1], cl[3][2], cl[3][3]);
       group_sync(1, 512);
-      PSTAMP(kt == 0, c, 17);
+      PSTAMP(kt == 480, c, 17);
 
       // ---- K2: anchors and factors per key channel, one 32-token block per thread group
       //      (threads < 128: block 0, 128 .. 255: block 1); row norms and scales (256 .. 383);
@@ -773,7 +775,7 @@ __global__ void __launch_bounds__(PNT, 1)
       // the previous chunk (K3 overwrites it)
       if (c > 0 && mma_thread) ok = wait_phase(bar(B_FREEA), (uint32_t)((c - 1) & 1));
       if (bar_any(1, 512, !ok)) { failed = true; site = 21; break; }
-      PSTAMP(kt == 0, c, 18);
+      PSTAMP(kt == 480, c, 18);
 
       // ---- K3: operand tiles [Kr; Qr], [Kc; Kc2] (own), Kg, Qg (stage).  The warp's rows lie in
       //      one 32-token block (bsel), so the block's variant is chosen once per warp.
@@ -837,11 +839,11 @@ __global__ void __launch_bounds__(PNT, 1)
           tiles(std::true_type{});
         else
           tiles(std::false_type{});
-        PSTAMP(kt == 0, c, 20);
+        PSTAMP(kt == 480, c, 20);
         fence_proxy_async();
         group_sync(1, 512);
         if (mma_thread) mbar_arrive(bar(B_FULLA));   // [Kg; Qg] and the vectors of chunk c
-        PSTAMP(kt == 0, c, 21);
+        PSTAMP(kt == 480, c, 21);
 
         // ---- K4: [A | QK] on the tensor cores, once the chain has taken the previous QK out
         //      of D; the next chunk's inputs (the input tiles are free)
@@ -864,7 +866,7 @@ __global__ void __launch_bounds__(PNT, 1)
       if (mma_thread && ok) ok = wait_phase(bar(B_KMMA), par);
       if (bar_any(1, 512, !ok)) { failed = true; site = 24; break; }
       kmma_pend = 0;
-      PSTAMP(kt == 0, c, 22);
+      PSTAMP(kt == 480, c, 22);
       tc_fence_after();
 
       // ---- K5: warps with w % 4 in {0, 1} read TMEM lanes 0-63 (rows of A), a 16-column
@@ -877,7 +879,7 @@ __global__ void __launch_bounds__(PNT, 1)
         if (mma_thread) ok = wait_phase(bar(B_FREEC), (uint32_t)((c - 1) & 1));
         if (bar_any(1, 512, !ok)) { failed = true; site = 25; break; }
       }
-      PSTAMP(kt == 0, c, 1);
+      PSTAMP(kt == 480, c, 1);
       if ((warp & 3) < 2) {
         const int q4 = warp & 3, cq = (warp - 4) >> 2;
         const uint32_t lbase = (uint32_t)(32 * q4) << 16;
@@ -892,7 +894,6 @@ __global__ void __launch_bounds__(PNT, 1)
 #pragma unroll
           for (int e = 0; e < 16; ++e) a[e] = 0u;
         }
-        PSTAMP(kt == 0, c, 23);
         float* nrow = Nm + r * NS + 16 * cq;
         const float br = vec[320 + r] * ik[r];
 #pragma unroll
@@ -932,7 +933,7 @@ __global__ void __launch_bounds__(PNT, 1)
       }
       tc_fence_before();
       group_sync(1, 512);
-      PSTAMP(kt == 0, c, 24);
+      PSTAMP(kt == 480, c, 24);
 
       // ---- K6 (threads < 128): T = (I + N)^-1: 16 x 16 diagonal blocks by substitution
       //      (fp32), then the off-diagonal blocks as tf32 warp products, 16 -> 32 -> 64
@@ -945,7 +946,6 @@ __global__ void __launch_bounds__(PNT, 1)
           *reinterpret_cast<float4*>(Tm + (bi * 16 + (e >> 2)) * NS + bj * 16 + 4 * (e & 3)) =
               make_float4(0.f, 0.f, 0.f, 0.f);
         }
-        PSTAMP(kt == 0, c, 19);
         if (wb < 2) {
           // warp wb: the diagonal blocks 2 wb (lanes 0-15) and 2 wb + 1 (lanes 16-31), lane =
           // column, by forward substitution four columns of N at a time (16-byte row pieces);
@@ -970,29 +970,23 @@ __global__ void __launch_bounds__(PNT, 1)
 #pragma unroll
           for (int i = 0; i < 16; ++i) Tm[(ob + i) * NS + ob + jj] = x[i];
           __syncwarp();
-          PSTAMP(kt == 0, c, 14);
-          PSTAMP(kt == 32, c, 25);
           const int ro = (2 * wb + 1) * 16, co = 2 * wb * 16;
           float* Yw = Y + wb * 16 * NS;
           wgemm16(Nm + ro * NS + co, Tm + co * NS + co, Yw, 1.0f, lane);
           __syncwarp();
-          PSTAMP(kt == 0, c, 11);
           wgemm16(Tm + ro * NS + ro, Yw, Tm + ro * NS + co, -1.0f, lane);
           __syncwarp();
-          PSTAMP(kt == 0, c, 13);
         }
         group_sync(3, 128);
-        PSTAMP(kt == 0, c, 15);
         const int mi = wb >> 1, ni = wb & 1;   // Y2 = N[32:64, 0:32] T[0:32, 0:32]
         wgemm32(Nm + (32 + 16 * mi) * NS, Tm + 16 * ni, Y + 16 * mi * NS + 16 * ni, 1.0f, lane);
         group_sync(3, 128);                    // T[32:64, 0:32] = -T[32:64, 32:64] Y2
-        PSTAMP(kt == 0, c, 9);
         wgemm32(Tm + (32 + 16 * mi) * NS + 32, Y + 16 * ni, Tm + (32 + 16 * mi) * NS + 16 * ni,
                 -1.0f, lane);
       }
       group_sync(1, 512);
       if (mma_thread) mbar_arrive(bar(B_FULL));   // the stage of chunk c is complete
-      PSTAMP(kt == 0, c, 29);
+      PSTAMP(kt == 480, c, 29);
     }
     if (failed) {
       if (kt == 0) record_error(p.status, KDA_ERR_DEVICE_TIMEOUT, site);
