@@ -137,6 +137,17 @@ def test_bf16_state(oracle_mod, kernel):
     check(oracle_mod, inp, out, fin, tag=f"bf16 state k{kernel}")
 
 
+@pytest.mark.parametrize("vsplit", [2, 4, 8])
+def test_bf16_state_value_slices(oracle_mod, vsplit):
+    """The split path's value-slice chains read and write a bf16 state (P = 2: the tcgen05
+    chain, 64 columns a slice in two 32-column halves; P = 4, 8: the warp-level chain)."""
+    w = W.custom([300, 5, 64, 129], 4, state_dtype="bf16", seed=23)
+    inp = W.make_inputs(w)
+    out, fin = run_gpu(inp, kda.KERNEL_SPLIT, vsplit)
+    assert fin.dtype == torch.bfloat16
+    check(oracle_mod, inp, out, fin, tag=f"bf16 state split P{vsplit}")
+
+
 @pytest.mark.parametrize("cfg", [1, 2])
 @pytest.mark.parametrize("kernel", [kda.KERNEL_AUTO, kda.KERNEL_TC, kda.KERNEL_SPLIT,
                                     kda.KERNEL_TC_HELPERS, kda.KERNEL_PIPE])
