@@ -365,9 +365,10 @@ void kda_test_drop_one_record(int on);
  * this entry point.
  *
  * Arguments, layouts and ownership are those of kda_chunk_prefill_fwd
- * without the workspace; the fused tcgen05 kernel runs unsplit (KDA_KERNEL_TC,
- * P = 1, as AUTO's fused fallback; never the split path, whose records need
- * a real workspace).
+ * without the workspace; the warp-specialised tcgen05 kernel runs
+ * (KDA_KERNEL_PIPE, P = 1: AUTO's choice whenever the workspace holds no
+ * per-chunk records; never the split path, whose records need a real
+ * workspace).
  * The scratch it needs (the 16-byte device status word) lives in a 256-byte
  * file-scope device array of this library, which every GPU that loads the
  * library holds until exit.  The library allocates nothing: no cudaMalloc,
@@ -382,8 +383,8 @@ void kda_test_drop_one_record(int on);
  *     GPU race on the array.  Device-side errors land in the array and are
  *     not reported back here; use kda_chunk_prefill_fwd with a workspace to
  *     read them.
- *   - Returns the codes of kda_chunk_prefill_fwd (the fused kernel needs
- *     only the 256 bytes the array holds).
+ *   - Returns the codes of kda_chunk_prefill_fwd (the kernel needs only
+ *     the 256 bytes the array holds).
  */
 int kda_chunk_prefill_fwd_noalloc(const void* q, const void* k, const void* v, const void* g,
                                   const void* beta, const float* A_log, const float* dt_bias,

@@ -15,8 +15,8 @@
 // the process: after a cudaDeviceReset (which unloads the library's device
 // module) this entry point must not be called again on that device.
 //
-// The fused kernel runs unsplit (P = 1), as the regular entry point's AUTO
-// does whenever it falls back to the fused kernel.
+// The warp-specialised kernel runs (KDA_KERNEL_PIPE, P = 1): the regular entry
+// point's AUTO choice whenever the workspace holds no per-chunk records.
 //
 // Every call shares the array.  Each call clears the status word on its
 // stream before the kernel runs; calls that overlap on the GPU (different
@@ -60,8 +60,8 @@ extern "C" int kda_chunk_prefill_fwd_noalloc(
     const void* initial_state, const int32_t* cu_seqlens, void* out, void* final_state,
     int state_dtype, kda_stream_t stream, int64_t total_tokens, int32_t num_seqs,
     int32_t heads) {
-  // The fused tcgen05 kernel needs only the status words; the split path (whose per-chunk
-  // records need a real workspace) is never taken here.
+  // The warp-specialised kernel needs only the status words; the split path (whose
+  // per-chunk records need a real workspace) is never taken here.
   static_assert(kda::kWorkspaceBytes <= kNoAllocScratchBytes, "scratch too small");
   if (total_tokens < 0 || num_seqs < 0 || heads <= 0) return KDA_ERR_INVALID_ARG;
   int dev = 0;
@@ -81,5 +81,5 @@ extern "C" int kda_chunk_prefill_fwd_noalloc(
   return kda_chunk_prefill_fwd_ex(q, k, v, g, beta, A_log, dt_bias, lower_bound, scale,
                                   initial_state, cu_seqlens, out, final_state, state_dtype,
                                   scratch, stream, total_tokens, num_seqs, heads,
-                                  (size_t)kNoAllocScratchBytes, 1, KDA_KERNEL_TC);
+                                  (size_t)kNoAllocScratchBytes, 1, KDA_KERNEL_PIPE);
 }
