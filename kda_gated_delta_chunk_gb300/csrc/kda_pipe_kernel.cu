@@ -255,6 +255,7 @@ __global__ void __launch_bounds__(PNT, 1)
     const int dv = tid;                                  // value channel = TMEM lane
     const uint32_t lb = (uint32_t)(32 * warp) << 16;     // lane base of this warp
     int pend = 0;   // thread 0: bit 0 v load, 1 G1A, 2 G1B, 3 G2 issued and not waited
+    int v_chunk = 0;   // thread 0: the chunk whose v load is pending (bit 0 of pend)
     int cfail = 0;  // chunk at which the loop stopped (all pending phases have its parity)
     if (tid == 0) {
       tma_prefetch_desc(&maps.v);
@@ -472,6 +473,7 @@ __global__ void __launch_bounds__(PNT, 1)
             mbar_expect_tx(bar(B_V), 16384);
             tma_load_3d(sb + PS_V, &maps.v, 0, c0 + PC, zblk, bar(B_V));
             pend |= 1;
+            v_chunk = c + 1;
           }
         }
       }
@@ -562,7 +564,7 @@ __global__ void __launch_bounds__(PNT, 1)
         record_error(p.status, KDA_ERR_DEVICE_TIMEOUT, site);
         // let copies and MMAs still in flight end (bounded) before the CTA exits
         const uint32_t fp = (uint32_t)(cfail & 1);
-        if (pend & 1) mbar_wait(bar(B_V), fp ^ (uint32_t)((pend & 4) == 0 && site == 41 ? 1 : 0));
+        if (pend & 1) mbar_wait(bar(B_V), (uint32_t)(v_chunk & 1));
         if (pend & 2) mbar_wait(bar(B_G1A), fp);
         if (pend & 4) mbar_wait(bar(B_G1B), fp);
         if (pend & 8) mbar_wait(bar(B_G2), fp);
