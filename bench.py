@@ -4,7 +4,7 @@ One step = one kda_chunk_prefill_fwd call over the whole batch (every step of
 the method runs inside that call's kernels).  Prints ONE JSON line (rank 0).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                  [--kernel auto|tc|split|ref|helpers|pipe] [--workload 1]
+                  [--kernel auto|tc|split|streamed|ref|helpers|pipe] [--workload 1]
                   [--no-cpu-baseline] [--stamps]
 
 value       tokens/s of the whole job (all ranks), inputs resident in HBM;
@@ -16,7 +16,9 @@ roofline    the prefill call against the HBM roofline: algorithmic bytes per
             call / mean call time (CUDA events on the launch stream).  On the
             default workload AUTO runs one launch of the warp-specialised
             kernel; on the split path (few sequences x heads) it is the
-            k-side kernel followed by the chain kernel.
+            k-side kernel followed by the chain kernel, or (streamed, AUTO's
+            choice where the chains leave half of the SMs free) the chain
+            kernel running beside the k-side kernel.
 launch_us   mean, median, min and max of the K per-call event times.
 graph       the same call captured in a CUDA graph (8 calls per graph over the
             rotating input sets), replayed 60 times: microseconds per call.
@@ -584,7 +586,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--kernel", default="auto",
-                    choices=["auto", "tc", "helpers", "split", "ref", "pipe"])
+                    choices=["auto", "tc", "helpers", "split", "streamed", "ref", "pipe"])
     ap.add_argument("--workload", type=int, default=1)
     ap.add_argument("--n", type=int, default=None, help="sequences of the V-split workload (3)")
     ap.add_argument("--vsplit", type=int, default=-1, help="-1 automatic, or 1/2/4/8")
@@ -624,8 +626,8 @@ def main():
     barrier(world)
     kbuild.build()
     kernel = {"auto": kda.KERNEL_AUTO, "tc": kda.KERNEL_TC, "ref": kda.KERNEL_REF,
-              "split": kda.KERNEL_SPLIT, "helpers": kda.KERNEL_TC_HELPERS,
-              "pipe": kda.KERNEL_PIPE}[args.kernel]
+              "split": kda.KERNEL_SPLIT, "streamed": kda.KERNEL_SPLIT_STREAMED,
+              "helpers": kda.KERNEL_TC_HELPERS, "pipe": kda.KERNEL_PIPE}[args.kernel]
     dev = torch.device("cuda", torch.cuda.current_device())
     rc = kda.device_check(dev.index)
     if rc != kda.OK:
@@ -642,7 +644,8 @@ def main():
             d["out"] = torch.empty_like(d["q"])
             d["fin"] = torch.empty_like(d["initial_state"])
             d["ws"] = kda.alloc_workspace(T, H, N, device=dev)
-            if kernel in (kda.KERNEL_SPLIT, kda.KERNEL_TC_HELPERS):   # records (+ claim words)
+            if kernel in (kda.KERNEL_SPLIT, kda.KERNEL_SPLIT_STREAMED,
+                          kda.KERNEL_TC_HELPERS):   # records (+ claim words)
                 n_ws = 1024 + ((T + 63) // 64 + N) * H * (66560 + 4)
                 d["ws"] = torch.zeros(max(n_ws, d["ws"].numel()), dtype=torch.uint8, device=dev)
             sets.append(d)
@@ -792,6 +795,7 @@ def main():
 
     kernel_name = {kda.KERNEL_TC: "kda_tc_chunk_kernel", kda.KERNEL_REF: "kda_ref_chunk_kernel",
                    kda.KERNEL_SPLIT: "kda_split_path", kda.KERNEL_TC_HELPERS: "kda_tc_helpers_path",
+                   kda.KERNEL_SPLIT_STREAMED: "kda_split_streamed_path",
                    kda.KERNEL_PIPE: "kda_pipe_kernel"}[path]
     hbm, tflops, peak_kind = load_peaks()
     abytes = algorithmic_bytes(w)

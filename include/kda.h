@@ -89,8 +89,11 @@ typedef struct CUstream_st* kda_stream_t;
                                             outside [0, out_rows)            */
 
 /* kernel selectors for kda_chunk_prefill_fwd_ex */
-#define KDA_KERNEL_AUTO 0  /* SPLIT when the value split triggers and the
-                              workspace holds its records; else TC_HELPERS
+#define KDA_KERNEL_AUTO 0  /* SPLIT_STREAMED when N * heads * P <= SMs / 2 for
+                              P = 8 or 4 and the workspace holds the records
+                              and claim words; else SPLIT when the value
+                              split triggers and the workspace holds its
+                              records; else TC_HELPERS
                               when N * heads <= min(SMs - 8, 5 SMs / 8),
                               N <= 128, the sequences average 4 or more
                               chunks and the workspace holds the records;
@@ -116,6 +119,14 @@ typedef struct CUstream_st* kda_stream_t;
                               build chunk c+1's operands while its chain warps
                               run chunk c; no value split (vsplit -1 or 1),
                               needs only the 256-byte workspace               */
+#define KDA_KERNEL_SPLIT_STREAMED 6 /* SPLIT with P = 4 or 8 and the chain kernel
+                              launched beside the k-side kernel (programmatic
+                              dependent launch): the chain CTAs take
+                              N * heads * P SMs, the k-side CTAs the others,
+                              and each chain CTA copies a record as soon as
+                              its claim word says it is written (bounded
+                              wait).  Needs 2 * N * heads * P <= SM count,
+                              N <= 128 and the workspace of TC_HELPERS        */
 
 /*
  * Bytes of device workspace a call needs for up to `total_tokens` tokens,
@@ -169,7 +180,9 @@ int kda_chunk_prefill_fwd(const void* q, const void* k, const void* v, const voi
  * KDA_ERR_WORKSPACE_TOO_SMALL.  KDA_KERNEL_TC_HELPERS needs the same plus
  * 4 bytes per (chunk slot, head), vsplit -1 or 1 (else
  * KDA_ERR_INVALID_ARG), num_seqs * heads below the SM count and num_seqs
- * <= 128 (else KDA_ERR_INVALID_ARG).
+ * <= 128 (else KDA_ERR_INVALID_ARG).  KDA_KERNEL_SPLIT_STREAMED needs that
+ * workspace too, vsplit -1 (P = 8, else 4), 4 or 8, 2 * num_seqs * heads * P
+ * at most the SM count and num_seqs <= 128 (else KDA_ERR_INVALID_ARG).
  */
 int kda_chunk_prefill_fwd_ex(const void* q, const void* k, const void* v, const void* g,
                              const void* beta, const float* A_log, const float* dt_bias,
@@ -324,7 +337,8 @@ int kda_device_check(int device);
  * The path a kda_chunk_prefill_fwd_ex call with these sizes, workspace size
  * and selectors would take on the current device, without enqueuing
  * anything: *kernel_out gets KDA_KERNEL_TC, KDA_KERNEL_TC_HELPERS,
- * KDA_KERNEL_SPLIT, KDA_KERNEL_PIPE or KDA_KERNEL_REF (AUTO resolved), *vsplit_out the value split factor P and
+ * KDA_KERNEL_SPLIT, KDA_KERNEL_SPLIT_STREAMED, KDA_KERNEL_PIPE or
+ * KDA_KERNEL_REF (AUTO resolved), *vsplit_out the value split factor P and
  * *launches_out the number of kernels the call enqueues (0, 1 or 2); any
  * output pointer may be NULL.  Returns the code such a call would return
  * for its sizes, selectors and workspace size (pointer checks aside), or
@@ -351,7 +365,9 @@ int kda_plan_for(int64_t total_tokens, int32_t num_seqs, int32_t heads, size_t w
  * calls that take KDA_KERNEL_TC_HELPERS have the helpers leave one claimed
  * record unpublished (the last chunk of the longest sequence's head 0), so
  * the bounded device wait of the fused CTA that needs it runs out and the
- * call records KDA_ERR_DEVICE_TIMEOUT.  Off at load.  Read once per call
+ * call records KDA_ERR_DEVICE_TIMEOUT; calls that take
+ * KDA_KERNEL_SPLIT_STREAMED leave the record of that sequence's first chunk
+ * of head 0 unpublished, with the same outcome for its chain CTAs.  Off at load.  Read once per call
  * from an atomic flag (no environment lookup).  The pages have no
  * counterpart.
  */

@@ -15,7 +15,8 @@ names follow the C ABI in ``include/kda.h``:
                   cu_seqlens, token_states=False, ...) -> (out, final_state, token_states)
     plan(total_tokens, num_seqs, heads, workspace_bytes, vsplit, kernel)
         -> (kernel, vsplit, launches)
-    KERNEL_AUTO / KERNEL_TC / KERNEL_TC_HELPERS / KERNEL_SPLIT / KERNEL_REF / KERNEL_PIPE
+    KERNEL_AUTO / KERNEL_TC / KERNEL_TC_HELPERS / KERNEL_SPLIT / KERNEL_SPLIT_STREAMED /
+    KERNEL_REF / KERNEL_PIPE
     last_device_status(workspace) -> int
     status_string(code) -> str
 
@@ -36,6 +37,7 @@ LIB_PATH = os.path.join(_PKG, "libkda.so")
 HEAD_DIM = 128
 STATE_F32, STATE_BF16 = 0, 1
 KERNEL_AUTO, KERNEL_TC, KERNEL_REF, KERNEL_SPLIT, KERNEL_TC_HELPERS, KERNEL_PIPE = 0, 1, 2, 3, 4, 5
+KERNEL_SPLIT_STREAMED = 6
 OK = 0
 ERR_INVALID_ARG = -1
 ERR_UNSUPPORTED_DEVICE = -2

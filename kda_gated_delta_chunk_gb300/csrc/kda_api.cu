@@ -67,6 +67,23 @@ int validate(const void* q, const void* k, const void* v, const void* g, const v
   return KDA_OK;
 }
 
+bool known_kernel(int kernel) {
+  return kernel == KDA_KERNEL_AUTO || kernel == KDA_KERNEL_TC || kernel == KDA_KERNEL_REF ||
+         kernel == KDA_KERNEL_SPLIT || kernel == KDA_KERNEL_TC_HELPERS ||
+         kernel == KDA_KERNEL_PIPE || kernel == KDA_KERNEL_SPLIT_STREAMED;
+}
+
+// Value split of the streamed split path: the widest warp-level chain (P = 8, else 4) whose
+// N * heads * P CTAs leave at least half of the SMs to the k-side kernel running beside it;
+// 0 when none does.
+int stream_vsplit(int32_t num_seqs, int32_t heads, int sms) {
+  const int64_t units = (int64_t)num_seqs * heads;
+  if (units <= 0 || num_seqs > kda::kHelperMaxSeqs) return 0;
+  for (int P = 8; P >= 4; P /= 2)
+    if (2 * units * P <= sms) return P;
+  return 0;
+}
+
 // The path of a call: validated selectors, then AUTO resolved.  The split path (k-side
 // records + chain per value slice) needs its record area in the workspace; AUTO takes it
 // when the value split triggers and the workspace holds the records.  Otherwise one CTA
@@ -77,14 +94,21 @@ int plan(int64_t total_tokens, int32_t num_seqs, int32_t heads, size_t workspace
          int vsplit, int kernel, int sms, int* kernel_out, int* vsplit_out, int* launches_out) {
   if (vsplit != -1 && vsplit != 1 && vsplit != 2 && vsplit != 4 && vsplit != 8)
     return KDA_ERR_INVALID_ARG;
-  if (kernel != KDA_KERNEL_AUTO && kernel != KDA_KERNEL_TC && kernel != KDA_KERNEL_REF &&
-      kernel != KDA_KERNEL_SPLIT && kernel != KDA_KERNEL_TC_HELPERS && kernel != KDA_KERNEL_PIPE)
-    return KDA_ERR_INVALID_ARG;
+  if (!known_kernel(kernel)) return KDA_ERR_INVALID_ARG;
   const size_t split_need = kda::split_workspace_bytes(total_tokens, heads, num_seqs);
   const size_t help_need = kda::helper_workspace_bytes(total_tokens, heads, num_seqs);
   int P = vsplit == -1 ? kda_choose_vsplit(num_seqs, heads, sms) : vsplit;
+  const bool chunk_count_ok =
+      ((total_tokens + kda::kChunk - 1) / kda::kChunk) * num_seqs * heads < ((int64_t)1 << 30);
+  const int P_stream = stream_vsplit(num_seqs, heads, sms);
   if (kernel == KDA_KERNEL_SPLIT) {
     if (workspace_bytes < split_need) return KDA_ERR_WORKSPACE_TOO_SMALL;
+  } else if (kernel == KDA_KERNEL_SPLIT_STREAMED) {
+    if (vsplit == -1) P = P_stream;
+    if ((P != 4 && P != 8) || num_seqs > kda::kHelperMaxSeqs || !chunk_count_ok ||
+        2 * (int64_t)num_seqs * heads * P > sms)
+      return KDA_ERR_INVALID_ARG;
+    if (workspace_bytes < help_need) return KDA_ERR_WORKSPACE_TOO_SMALL;
   } else if (kernel == KDA_KERNEL_PIPE) {
     if (vsplit != -1 && vsplit != 1) return KDA_ERR_INVALID_ARG;
     P = 1;
@@ -96,7 +120,11 @@ int plan(int64_t total_tokens, int32_t num_seqs, int32_t heads, size_t workspace
     if (workspace_bytes < help_need) return KDA_ERR_WORKSPACE_TOO_SMALL;
     P = 1;
   } else if (kernel == KDA_KERNEL_AUTO) {
-    if (P > 1 && workspace_bytes >= split_need && total_tokens > 0) {
+    if (vsplit == -1 && P > 1 && P_stream > 0 && chunk_count_ok && workspace_bytes >= help_need &&
+        total_tokens > 0) {
+      kernel = KDA_KERNEL_SPLIT_STREAMED;
+      P = P_stream;
+    } else if (P > 1 && workspace_bytes >= split_need && total_tokens > 0) {
       kernel = KDA_KERNEL_SPLIT;
     } else {
       if (vsplit == -1) P = 1;
@@ -110,7 +138,8 @@ int plan(int64_t total_tokens, int32_t num_seqs, int32_t heads, size_t workspace
     }
   }
   int launches = num_seqs == 0 ? 0 : 1;
-  if (kernel == KDA_KERNEL_SPLIT && num_seqs > 0) launches = total_tokens > 0 ? 2 : 1;
+  if ((kernel == KDA_KERNEL_SPLIT || kernel == KDA_KERNEL_SPLIT_STREAMED) && num_seqs > 0)
+    launches = total_tokens > 0 ? 2 : 1;
   if (kernel == KDA_KERNEL_TC_HELPERS && num_seqs > 0 && total_tokens > 0) launches = 2;
   if (kernel_out) *kernel_out = kernel;
   if (vsplit_out) *vsplit_out = P;
@@ -147,9 +176,7 @@ int fwd_impl(const void* q, const void* k, const void* v, const void* g, const v
   // selectors first: they are host-side checks and need no device
   if (vsplit != -1 && vsplit != 1 && vsplit != 2 && vsplit != 4 && vsplit != 8)
     return KDA_ERR_INVALID_ARG;
-  if (kernel != KDA_KERNEL_AUTO && kernel != KDA_KERNEL_TC && kernel != KDA_KERNEL_REF &&
-      kernel != KDA_KERNEL_SPLIT && kernel != KDA_KERNEL_TC_HELPERS && kernel != KDA_KERNEL_PIPE)
-    return KDA_ERR_INVALID_ARG;
+  if (!known_kernel(kernel)) return KDA_ERR_INVALID_ARG;
   int dev = 0, sms = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) {
     cudaGetLastError();
@@ -190,8 +217,9 @@ int fwd_impl(const void* q, const void* k, const void* v, const void* g, const v
   p.s_g = st[3];
   p.s_beta = st[4];
   p.helpers = (kernel == KDA_KERNEL_TC_HELPERS && total_tokens > 0) ? 1 : 0;
+  p.stream_sms = (kernel == KDA_KERNEL_SPLIT_STREAMED && total_tokens > 0) ? num_seqs * heads * P : 0;
   p.test_drop_record =
-      (p.helpers && g_test_drop_record.load(std::memory_order_relaxed) != 0) ? 1 : 0;
+      ((p.helpers || p.stream_sms > 0) && g_test_drop_record.load(std::memory_order_relaxed) != 0) ? 1 : 0;
 #ifdef KDA_PHASE_STAMPS
   // stamps build: the last 16 KB of a workspace of at least 32 KB take the per-chunk stamps
   // (64 chunks x 32 slots of CTA 0)
@@ -204,7 +232,8 @@ int fwd_impl(const void* q, const void* k, const void* v, const void* g, const v
 
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   cudaError_t err = (kernel == KDA_KERNEL_REF)     ? kda::launch_ref(p, s)
-                    : (kernel == KDA_KERNEL_SPLIT) ? kda::launch_split(p, s)
+                    : (kernel == KDA_KERNEL_SPLIT || kernel == KDA_KERNEL_SPLIT_STREAMED)
+                        ? kda::launch_split(p, s)
                     : (kernel == KDA_KERNEL_PIPE)  ? kda::launch_pipe(p, s)
                                                    : kda::launch_tc(p, s);
   if (err != cudaSuccess) {

@@ -93,6 +93,31 @@ struct ChainMaps {
   CUtensorMap v;        // v as [T][H*128] bf16, box {DV, 64}
 };
 
+// Streamed split path, at the end of every chain CTA (threads 0 .. nthr-1 of it; `sync` is a
+// barrier over them): once the k-side grid has completed, the last chain CTA to finish clears
+// the claim words of the call and the path's counters, so that the next call starts from zero.
+template <typename Sync>
+__device__ void stream_finish(const Params& p, int tid, int nthr, int* last_s, Sync sync) {
+  if (tid == 0) {
+    pdl_wait();
+    __threadfence();
+    *last_s = atomicAdd(p.status + kStreamDoneWord, 1) == (int)gridDim.x - 1;
+  }
+  sync();
+  if (!*last_s) return;
+  __threadfence();
+  int* claims = reinterpret_cast<int*>(reinterpret_cast<unsigned char*>(p.status) +
+                                       helper_claims_offset(p.total_tokens, p.heads, p.num_seqs));
+  const int64_t items = split_slots(p.total_tokens, p.num_seqs) * p.heads;
+  for (int64_t i = tid; i < items; i += nthr) claims[i] = kClaimFree;
+  if (tid == 0) {
+    p.status[kStreamCounterWord] = 0;
+    p.status[kStreamYieldWord] = 0;
+    p.status[kStreamDoneWord] = 0;
+    p.status[kStreamStartWord] = 0;
+  }
+}
+
 // kRowMap: outputs through the out_index row map (its own instantiation)
 template <int DV, bool kRowMap>
 __global__ void __launch_bounds__(NT2, 1)
@@ -115,8 +140,11 @@ __global__ void __launch_bounds__(NT2, 1)
   const int h = (unit / P) % H;
   const int n = unit / (P * H);
   const int t0 = p.cu_seqlens[n], t1 = p.cu_seqlens[n + 1];
+  const bool streamed = p.stream_sms > 0;
+  int* last_s = reinterpret_cast<int*>(sm + L_::OFF_MISC);
   if (t0 < 0 || t1 < t0 || (int64_t)t1 > p.total_tokens || p.cu_seqlens[0] != 0) {
     if (tid == 0) record_error(p.status, KDA_ERR_BAD_CU_SEQLENS, 3);
+    if (streamed) stream_finish(p, tid, NT2, last_s, [] { __syncthreads(); });
     return;
   }
   if (tid == 0) {
@@ -166,6 +194,17 @@ __global__ void __launch_bounds__(NT2, 1)
         if (j >= NB) {
           if (!mbar_wait(empty0 + 8 * b, (eph >> b) & 1u)) break;
           eph ^= 1u << b;
+        }
+        if (streamed) {   // the record is published by the k-side kernel running beside
+          const int64_t slot = slot0 + j;
+          if (!wait_flag(reinterpret_cast<const int*>(reinterpret_cast<const unsigned char*>(p.status) +
+                                                      helper_claims_offset(p.total_tokens, H, p.num_seqs)) +
+                             claim_index(slot, h, p.total_tokens, p.num_seqs),
+                         kClaimStreamed)) {
+            record_error(p.status, KDA_ERR_DEVICE_TIMEOUT, 5);
+            break;
+          }
+          fence_proxy_async_global();   // its generic stores -> this bulk copy
         }
         issue(j, b);
         issued = j + 1;
@@ -430,6 +469,7 @@ __global__ void __launch_bounds__(NT2, 1)
 
   if (failed) {   // (the producer lets the copies in flight land before it exits)
     if (tid == 0) record_error(p.status, KDA_ERR_DEVICE_TIMEOUT, 4);
+    if (streamed) stream_finish(p, tid, NTC, last_s, [] { group_sync(1, NTC); });
     return;
   }
   // ---- state out
@@ -445,6 +485,7 @@ __global__ void __launch_bounds__(NT2, 1)
       else
         static_cast<float*>(p.final_state)[idx] = S[nt][e];
     }
+  if (streamed) stream_finish(p, tid, NTC, last_s, [] { group_sync(1, NTC); });
 }
 
 }  // namespace
@@ -493,17 +534,28 @@ cudaError_t launch_chain_dv(const Params& p, cudaStream_t stream) {
   ChainMaps maps;
   if (!make_chain_maps(&maps, p, DV)) return cudaErrorInvalidValue;
   const long long blocks = (long long)p.num_seqs * p.heads * (128 / DV);
-  if (p.out_index)
-    kda_chain_kernel<DV, true><<<(unsigned)blocks, NT2, smem, stream>>>(p, maps);
-  else
-    kda_chain_kernel<DV, false><<<(unsigned)blocks, NT2, smem, stream>>>(p, maps);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)blocks);
+  cfg.blockDim = dim3(NT2);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = p.stream_sms > 0 ? 1 : 0;   // streamed: beside the k-side kernel
+  if (p.out_index) return cudaLaunchKernelEx(&cfg, kda_chain_kernel<DV, true>, p, maps);
+  return cudaLaunchKernelEx(&cfg, kda_chain_kernel<DV, false>, p, maps);
 }
 
 }  // namespace
 
 cudaError_t launch_split(const Params& p, cudaStream_t stream) {
   if (p.vsplit != 1 && p.vsplit != 2 && p.vsplit != 4 && p.vsplit != 8) return cudaErrorInvalidValue;
+  // streamed (the chain beside the k-side kernel): the warp-level chains, with SMs to spare
+  if (p.stream_sms > 0 &&
+      (p.vsplit < 4 || p.stream_sms != p.num_seqs * p.heads * p.vsplit || p.stream_sms >= p.sm_count))
+    return cudaErrorInvalidValue;
   cudaError_t e = launch_kside(p, stream);
   if (e != cudaSuccess) return e;
   // P = 2 on tcgen05 (kda_chain_vs_kernel.cu); the narrower slices keep the warp-level

@@ -68,6 +68,11 @@ struct Params {
   // of the longest sequence's head 0 unpublished, so the bounded wait of the fused CTA that
   // needs it runs out
   int32_t test_drop_record;
+  // split path only, when > 0: the chain kernel runs beside the k-side kernel (programmatic
+  // dependent launch).  k-side CTAs that start on an SM whose %smid is below this value leave
+  // it to the chain CTAs (at most two per such SM), and each chain CTA copies a record once
+  // its claim word reads kClaimStreamed
+  int32_t stream_sms;
   // builds with -DKDA_PHASE_STAMPS only: per-chunk clock64 stamps of CTA 0 (32 per chunk,
   // first 64 chunks); null otherwise
   unsigned long long* stamps;
@@ -155,6 +160,15 @@ inline int64_t helper_max_chains(int sms) {
   return a < b ? a : b;
 }
 constexpr int kHelperMaxSeqs = 128;       // ... and at most this many sequences
+// Streamed split path: the k-side kernel takes items from its own counter, first chunk index
+// first, and publishes each record by setting its claim word to kClaimStreamed; the chain
+// CTAs copy records as they appear.  Header words: that counter, the k-side CTAs that left
+// their SM to the chains, the chain CTAs that have finished, the k-side CTAs that have
+// started.  The last chain CTA to finish clears the four and the claim words of the call,
+// so that every call starts from zero.
+constexpr int kClaimStreamed = 4;
+constexpr int kStreamCounterWord = 129, kStreamYieldWord = 130, kStreamDoneWord = 131,
+              kStreamStartWord = 132;
 __host__ __device__ inline size_t helper_claims_offset(int64_t total_tokens, int32_t heads,
                                                        int32_t num_seqs) {
   return (size_t)kSplitHeader + (size_t)split_slots(total_tokens, num_seqs) * heads * kRecBytes;

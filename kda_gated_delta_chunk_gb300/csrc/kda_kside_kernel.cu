@@ -120,25 +120,27 @@ __device__ void find_item(const Params& p, const int* cu, int k, int total, int*
 // Helper mode (behind the fused kernel): the next item from the shared counter, in the
 // order last chunk index first, then (sequence by decreasing length, head).  It is claimed
 // only when its processing starts.  `ord` lists the sequences longest first, so a
-// sequence without chunk `col` ends that column for every helper.
+// sequence without chunk `col` ends that column for every helper.  Streamed split path:
+// the same walk from the first chunk index on, with the counter of that path.
 __device__ void find_helper_item(const Params& p, const int* cu, const int* ord, int max_chunks,
                                  int* out) {
   out[0] = -1;
   out[1] = out[2] = out[3] = out[4] = 0;
   const int NH = p.num_seqs * p.heads;
-  int* counter = p.status + kHelperCounterWord;
+  const bool fwd = p.stream_sms > 0;
+  int* counter = p.status + (fwd ? kStreamCounterWord : kHelperCounterWord);
   const int limit = max_chunks * NH;   // below 2^30 (checked on the host)
   while (true) {
     const int idx = atomicAdd(counter, 1);
     if (idx < 0 || idx >= limit) return;
-    const int col = max_chunks - 1 - idx / NH;
+    const int col = fwd ? idx / NH : max_chunks - 1 - idx / NH;
     const int r = idx % NH;
     const int n = ord[r / p.heads], hh = r % p.heads;
     const int a = cu[n], b = cu[n + 1];
     if (a < 0 || b < a || (int64_t)b > p.total_tokens) return;   // malformed: the fused kernel reports it
     const int64_t s = (int64_t)a + (int64_t)C * col;
     if (s >= b) {   // no chunk `col` here nor in any shorter sequence: skip to the next column
-      atomicMax(counter, (max_chunks - col) * NH);
+      atomicMax(counter, (idx / NH + 1) * NH);
       continue;
     }
     out[0] = ((a >> 6) + n + col) * p.heads + hh;
@@ -179,6 +181,32 @@ __global__ void __launch_bounds__(NT, 2)
   uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + K_TSLOT);
   const uint32_t bar_in = sb + K_BAR, bar_mma = bar_in + 8;
   unsigned char* ws = reinterpret_cast<unsigned char*>(p.status) + kSplitHeader;
+  const bool streamed = p.stream_sms > 0;
+  if (streamed) {
+    pdl_launch_dependents();   // the chain grid may start once every k-side CTA has begun
+    // leave the SMs below stream_sms to the chain CTAs (at most two CTAs per such SM yield,
+    // so that at least 2 (SMs - stream_sms) of the grid's CTAs make records wherever they run)
+    bool yield = false;
+    if (tid == 0) {
+      atomicAdd(p.status + kStreamStartWord, 1);
+      if ((int)sm_id() < p.stream_sms)
+        yield = atomicAdd(p.status + kStreamYieldWord, 1) < 2 * p.stream_sms;
+    }
+    if (__syncthreads_or(yield)) {
+      // give up the tensor-memory allocation permit (the SM takes no further CTA of this
+      // grid while a resident one still holds it), then hold the SM until every CTA of the
+      // grid has started (a few microseconds; 20 at most), so that the CTAs still waiting to
+      // be placed land beside this one, not on the SMs the chains will need later
+      if (warp == 0) tmem_relinquish();
+      if (tid == 0) {
+        const uint64_t w0 = globaltimer_ns();
+        while (ld_relaxed_gpu(p.status + kStreamStartWord) < (int)gridDim.x &&
+               globaltimer_ns() - w0 < 20000ull)
+          __nanosleep(128);
+      }
+      return;
+    }
+  }
 
   const int H = p.heads;
   const int total = (int)(split_slots(p.total_tokens, p.num_seqs) * H);
@@ -194,7 +222,7 @@ __global__ void __launch_bounds__(NT, 2)
   // longest (at most ceil(T / 64) even for malformed cu_seqlens)
   int* maxc_s = reinterpret_cast<int*>(sm + K_MAXC);
   int* ord = reinterpret_cast<int*>(sm + K_ORD);
-  if (p.helpers) {
+  if (p.helpers || streamed) {
     const int N = p.num_seqs;
     if (tid == 0) *maxc_s = 0;
     __syncthreads();
@@ -212,9 +240,9 @@ __global__ void __launch_bounds__(NT, 2)
     if (tid == 0) {
       *maxc_s = min(*maxc_s, (int)((p.total_tokens + C - 1) / C));
       // test hook (Params::test_drop_record): the item of the counter's first index, the last
-      // chunk of the longest sequence's head 0, is left unpublished
+      // chunk (streamed: the first chunk) of the longest sequence's head 0, is left unpublished
       const int n0 = ord[0];
-      flags[6] = ((cu[n0] >> 6) + n0 + *maxc_s - 1) * H;
+      flags[6] = ((cu[n0] >> 6) + n0 + (streamed ? 0 : *maxc_s - 1)) * H;
     }
     __syncthreads();
   }
@@ -226,7 +254,7 @@ __global__ void __launch_bounds__(NT, 2)
     tma_prefetch_desc(&tm_k);
     tma_prefetch_desc(&tm_g);
     flags[8] = -1;
-    if (p.helpers) {   // the next item is found during T of the current one
+    if (p.helpers || streamed) {   // the next item is found during T of the current one
       find_helper_item(p, cu, reinterpret_cast<const int*>(sm + K_ORD), *reinterpret_cast<const int*>(sm + K_MAXC), flags);
     } else {
       find_item(p, cu, 0, total, flags);
@@ -582,7 +610,7 @@ __global__ void __launch_bounds__(NT, 2)
                           Tm + (32 + 16 * mi) * NS + 16 * ni, -1.0f, lane);
     } else if (tid == 128) {
       flags[16] = -1;
-      if (p.helpers)
+      if (p.helpers || streamed)
         find_helper_item(p, cu, reinterpret_cast<const int*>(sm + K_ORD),
                          *reinterpret_cast<const int*>(sm + K_MAXC), flags + 8);
       else if (flags[8] >= 0)
@@ -674,9 +702,9 @@ __global__ void __launch_bounds__(NT, 2)
     }
     tc_fence_before();
     __syncthreads();
-    if (p.helpers && tid == 0 && !(p.test_drop_record && item == flags[6])) {
+    if ((p.helpers || streamed) && tid == 0 && !(p.test_drop_record && item == flags[6])) {
       __threadfence();   // publish the record (the barrier orders every thread's part of it
-      st_release_gpu(helper_claim(p, item), kClaimReady);   // before this fence)
+      st_release_gpu(helper_claim(p, item), streamed ? kClaimStreamed : kClaimReady);   // before this fence)
     }
   }
 
@@ -732,7 +760,11 @@ cudaError_t launch_kside(const Params& p, cudaStream_t stream) {
       !make_in_map(enc, &mg, p.g, p.total_tokens, p.heads, p.s_g))
     return cudaErrorInvalidValue;
   const int64_t cap = 2 * (int64_t)p.sm_count;
-  const int64_t grid = items < cap ? items : cap;
+  // streamed: two CTAs per SM, of which those on the chains' SMs step aside
+  const int64_t grid = (items < cap && p.stream_sms == 0) ? items : cap;
+  if (p.stream_sms > 0 && (p.num_seqs > kHelperMaxSeqs ||
+                           ((p.total_tokens + C - 1) / C) * p.num_seqs * p.heads >= (1 << 30)))
+    return cudaErrorInvalidValue;
   kda_kside_kernel<<<(unsigned)grid, NT, K_SMEM_BYTES, stream>>>(p, mq, mk, mg);
   return cudaGetLastError();
 }

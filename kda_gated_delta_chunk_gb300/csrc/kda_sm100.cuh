@@ -173,6 +173,13 @@ __device__ __forceinline__ bool wait_flag(const int* p, int v) {
   }
 }
 
+// The SM this thread runs on (%smid: a scheduling hint, not guaranteed to be contiguous).
+__device__ __forceinline__ uint32_t sm_id() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%smid;" : "=r"(r));
+  return r;
+}
+
 // ------------------------------------------------------------ programmatic dependent launch
 // This CTA no longer holds back the launch of the grid that depends on this one.
 __device__ __forceinline__ void pdl_launch_dependents() {

@@ -122,12 +122,12 @@ def _records_only(lengths, H):
 
 
 @pytest.mark.parametrize("shape,H,want", [
-    ("tiny", 2, (kda.KERNEL_SPLIT, 8, 2)),                 # 1 x 128
+    ("tiny", 2, (kda.KERNEL_SPLIT_STREAMED, 8, 2)),        # 1 x 128
     ("batched", 16, (kda.KERNEL_PIPE, 1, 1)),              # 128 chains: over 5/8 of the SMs
-    ("long", 16, (kda.KERNEL_SPLIT, 8, 2)),                # 1 x 16384
-    ("v1", 8, (kda.KERNEL_SPLIT, 8, 2)),                   # N x 4096, H = 8
-    ("v2", 8, (kda.KERNEL_SPLIT, 8, 2)),
-    ("v3", 8, (kda.KERNEL_SPLIT, 4, 2)),
+    ("long", 16, (kda.KERNEL_SPLIT_STREAMED, 4, 2)),       # 1 x 16384: 64 chain CTAs
+    ("v1", 8, (kda.KERNEL_SPLIT_STREAMED, 8, 2)),          # N x 4096, H = 8
+    ("v2", 8, (kda.KERNEL_SPLIT_STREAMED, 4, 2)),
+    ("v3", 8, (kda.KERNEL_SPLIT, 4, 2)),                   # 24 x 4 chain CTAs: over half
     ("v7", 8, (kda.KERNEL_SPLIT, 2, 2)),
     ("ragged", 32, (kda.KERNEL_PIPE, 1, 1)),               # 2048 chains: no SM left over
 ])
@@ -160,6 +160,50 @@ def test_auto_helper_conditions(L):
     assert _auto(lengths, 16, ws=_records_only(lengths, 16) + claims - 4)[0] == kda.KERNEL_PIPE
     assert _auto(lengths, 16, ws=_records_only(lengths, 16) + claims)[0] == \
         kda.KERNEL_TC_HELPERS
+
+
+def test_auto_streamed_split_conditions(L):
+    # P = 8 while 2 N H 8 <= SMs, else P = 4 while 2 N H 4 <= SMs, else the plain split
+    assert _auto([4096] * 9, 1) == (kda.KERNEL_SPLIT_STREAMED, 8, 2)
+    assert _auto([4096] * 10, 1) == (kda.KERNEL_SPLIT_STREAMED, 4, 2)
+    assert _auto([4096] * 19, 1) == (kda.KERNEL_SPLIT_STREAMED, 4, 2)
+    assert _auto([4096] * 20, 1) == (kda.KERNEL_SPLIT, 4, 2)
+    # the claim words must fit as well as the records
+    lengths = [4096] * 2
+    assert _auto(lengths, 8, ws=_records_only(lengths, 8)) == (kda.KERNEL_SPLIT, 8, 2)
+    claims = ((sum(lengths) + 63) // 64 + len(lengths)) * 8 * 4
+    assert _auto(lengths, 8, ws=_records_only(lengths, 8) + claims - 4) == (kda.KERNEL_SPLIT, 8, 2)
+    assert _auto(lengths, 8, ws=_records_only(lengths, 8) + claims) == \
+        (kda.KERNEL_SPLIT_STREAMED, 4, 2)
+    # at most 128 sequences (shown on a part with enough SMs for the split)
+    def full(lengths, H):   # records and claim words
+        return 1024 + ((sum(lengths) + 63) // 64 + len(lengths)) * H * (66560 + 4)
+    assert _auto([64] * 128, 1, sms=4096, ws=full([64] * 128, 1)) == \
+        (kda.KERNEL_SPLIT_STREAMED, 8, 2)
+    assert _auto([64] * 129, 1, sms=4096, ws=full([64] * 129, 1)) == (kda.KERNEL_SPLIT, 8, 2)
+    # a split factor given by the caller keeps the plain split under AUTO
+    assert _auto([16384], 16, vsplit=4) == (kda.KERNEL_SPLIT, 4, 2)
+
+
+def test_forced_streamed_split(L):
+    assert _auto([16384], 16, kernel=kda.KERNEL_SPLIT_STREAMED) == (kda.KERNEL_SPLIT_STREAMED, 4, 2)
+    assert _auto([4096], 8, kernel=kda.KERNEL_SPLIT_STREAMED, vsplit=4) == \
+        (kda.KERNEL_SPLIT_STREAMED, 4, 2)
+    refused = [
+        (dict(vsplit=2), kda.ERR_INVALID_ARG),                 # warp-level chains only
+        (dict(vsplit=1), kda.ERR_INVALID_ARG),
+        (dict(vsplit=8), kda.ERR_INVALID_ARG),                 # 2 x 16 x 8 > 152
+        (dict(sms=127), kda.ERR_INVALID_ARG),                  # 2 x 16 x 4 > 127
+        (dict(ws=_records_only([16384], 16)), kda.ERR_WORKSPACE_TOO_SMALL),
+    ]
+    for kw, code in refused:
+        with pytest.raises(kda.KDAError) as e:
+            _auto([16384], 16, kernel=kda.KERNEL_SPLIT_STREAMED, **kw)
+        assert e.value.code == code, kw
+    # no tokens: one launch writes the states
+    ws = 1024 + (0 + 1) * 8 * (66560 + 4)   # one slot per sequence
+    assert kda.plan_for(0, 1, 8, ws, GB300_SMS, kernel=kda.KERNEL_SPLIT_STREAMED) == \
+        (kda.KERNEL_SPLIT_STREAMED, 8, 1)
 
 
 def test_auto_without_room_for_records_runs_the_fused_kernel(L):

@@ -24,7 +24,7 @@ pytestmark = pytest.mark.gpu
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 TOL = json.load(open(os.path.join(ROOT, "tests", "golden", "tolerances.json")))["max_abs"]
 KERNELS = [kda.KERNEL_REF, kda.KERNEL_TC, kda.KERNEL_SPLIT, kda.KERNEL_TC_HELPERS,
-           kda.KERNEL_PIPE]
+           kda.KERNEL_PIPE, kda.KERNEL_SPLIT_STREAMED]
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -58,7 +58,7 @@ def helper_workspace(T, H, N):
 def workspace_for(kernel, T, H, N):
     if kernel == kda.KERNEL_SPLIT:
         return split_workspace(T, H, N)
-    if kernel == kda.KERNEL_TC_HELPERS:
+    if kernel in (kda.KERNEL_TC_HELPERS, kda.KERNEL_SPLIT_STREAMED):
         return helper_workspace(T, H, N)
     return None
 
@@ -122,6 +122,8 @@ def test_ragged_tiles_and_tails(oracle_mod, kernel, vsplit):
     """Several chunks, ragged tails, a 1-token and an empty sequence."""
     if kernel in (kda.KERNEL_TC_HELPERS, kda.KERNEL_PIPE) and vsplit != 1:
         pytest.skip("the helpers and the pipelined kernel run unsplit only")
+    if kernel == kda.KERNEL_SPLIT_STREAMED:
+        pytest.skip("27 chains need more than the SMs' half at P = 4 (streamed cases below)")
     w = W.custom([1, 63, 64, 65, 130, 0, 200, 17, 129], 3, seed=21)
     inp = W.make_inputs(w)
     out, fin = run_gpu(inp, kernel, vsplit)
@@ -176,12 +178,73 @@ def test_workload3_vsplit_vs_unsplit(oracle_mod, n):
 
 @pytest.mark.parametrize("cfg", [2, 3])
 def test_auto_takes_split_path_when_it_triggers(oracle_mod, cfg):
-    """One long sequence (16 heads) and 2 x 4096 (8 heads): AUTO runs the split
-    path (k-side records + chain per value slice) -- same values as forcing it."""
+    """One long sequence (16 heads) and 2 x 4096 (8 heads): AUTO runs the streamed split
+    path (the chain beside the k-side kernel, P = 4) -- the same bits as forcing it, and as
+    the plain split path at P = 4 (the same records and the same chain arithmetic, only
+    started earlier)."""
     inp = W.make_inputs(W.workload(cfg, 2) if cfg == 3 else W.workload(cfg))
+    T, H, N = inp["q"].shape[0], inp["q"].shape[1], inp["cu_seqlens"].numel() - 1
+    assert kda.plan(T, N, H, kda.workspace_size(T, H, N), -1, kda.KERNEL_AUTO)[:2] == \
+        (kda.KERNEL_SPLIT_STREAMED, 4)
     out_a, fin_a = run_gpu(inp)
-    out_s, fin_s = run_gpu(inp, kda.KERNEL_SPLIT)
+    out_s, fin_s = run_gpu(inp, kda.KERNEL_SPLIT_STREAMED)
     assert torch.equal(out_a, out_s) and torch.equal(fin_a, fin_s)
+    out_p, fin_p = run_gpu(inp, kda.KERNEL_SPLIT, vsplit=4)
+    assert torch.equal(out_a, out_p) and torch.equal(fin_a, fin_p)
+
+
+@pytest.mark.parametrize("lengths,H,sd,P", [
+    ([1, 63, 64, 65, 130, 0, 200], 2, "f32", 4),     # ragged tails, 1-token and empty
+    ([300, 5, 64, 129, 900], 3, "bf16", 4),
+    ([2048, 2048], 2, "f32", 8),
+    ([8192], 4, "f32", 8),
+    ([100], 1, "bf16", 8),
+])
+def test_streamed_split_against_the_oracle(oracle_mod, lengths, H, sd, P):
+    """The streamed split path (chain CTAs copying each record as the k-side kernel
+    publishes it) on ragged batches and both state dtypes; one workspace serves a second
+    call with new inputs, and the path's header words are back at zero after each call."""
+    N, T = len(lengths), sum(lengths)
+    ws = helper_workspace(T, H, N)
+    for seed in (51, 52):
+        inp = W.make_inputs(W.custom(lengths, H, state_dtype=sd, seed=seed))
+        d = to_dev(inp)
+        out, fin = kda.chunk_prefill_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], d["A_log"],
+                                         d["dt_bias"], d["lower_bound"], d["scale"],
+                                         d["initial_state"], d["cu_seqlens"], workspace=ws,
+                                         state_dtype=inp["initial_state"].dtype, vsplit=P,
+                                         kernel=kda.KERNEL_SPLIT_STREAMED)
+        torch.cuda.synchronize()
+        assert kda.last_device_status(ws) == kda.OK
+        assert ws[512:532].view(torch.int32)[1:].cpu().tolist() == [0, 0, 0, 0]
+        check(oracle_mod, inp, out, fin, tag=f"streamed P{P} {lengths} seed {seed}")
+
+
+def test_streamed_split_dropped_record_times_out():
+    """Failure detection on the streamed split path without a GPU fault: with the test hook
+    on, the k-side kernel leaves the record of the first chunk of head 0 unpublished; the
+    chain CTAs that need it give up after a bounded wait and the call records
+    KDA_ERR_DEVICE_TIMEOUT.  The next call on the same workspace is correct: the last chain
+    CTA cleared the path's claim words and counters on the way out."""
+    inp = W.make_inputs(W.custom([1024, 1024], 2, seed=45))
+    d = to_dev(inp)
+    T = d["q"].shape[0]
+    ws = helper_workspace(T, 2, 2)
+    args = (d["q"], d["k"], d["v"], d["g"], d["beta"], d["A_log"], d["dt_bias"],
+            d["lower_bound"], d["scale"], d["initial_state"], d["cu_seqlens"])
+    kda.test_drop_one_record(True)
+    try:
+        kda.chunk_prefill_fwd(*args, workspace=ws, kernel=kda.KERNEL_SPLIT_STREAMED)
+        torch.cuda.synchronize()
+    finally:
+        kda.test_drop_one_record(False)
+    assert kda.last_device_status(ws) == kda.ERR_DEVICE_TIMEOUT
+    assert ws[512:532].view(torch.int32)[1:].cpu().tolist() == [0, 0, 0, 0]
+    out, fin = kda.chunk_prefill_fwd(*args, workspace=ws, kernel=kda.KERNEL_SPLIT_STREAMED)
+    torch.cuda.synchronize()
+    assert kda.last_device_status(ws) == kda.OK
+    out_p, fin_p = run_gpu(inp, kda.KERNEL_SPLIT, vsplit=8)
+    assert torch.equal(out, out_p) and torch.equal(fin, fin_p)
 
 
 def test_split_falls_back_to_fused_on_small_workspace(oracle_mod):
@@ -402,9 +465,10 @@ def test_errors_returned_with_a_device():
     assert e.value.code == kda.ERR_WORKSPACE_TOO_SMALL
 
 
-@pytest.mark.parametrize("kernel", [kda.KERNEL_AUTO, kda.KERNEL_PIPE])
+@pytest.mark.parametrize("kernel", [kda.KERNEL_AUTO, kda.KERNEL_PIPE, kda.KERNEL_SPLIT_STREAMED])
 def test_cuda_graph_capture_and_replay(oracle_mod, kernel):
-    """Capture the call on a side stream, replay it, compare with eager."""
+    """Capture the call on a side stream, replay it three times, compare with eager (AUTO
+    takes the streamed split path on this batch: 12 chains x P = 4)."""
     inp = W.make_inputs(W.custom([200, 64, 3], 4, seed=30))
     d = to_dev(inp)
     out_e, fin_e = run_gpu(inp, kernel)
@@ -423,11 +487,13 @@ def test_cuda_graph_capture_and_replay(oracle_mod, kernel):
     with torch.cuda.graph(graph, stream=side):
         kda.chunk_prefill_fwd(*args, out=out, final_state=fin, workspace=ws, stream=side,
                               kernel=kernel)
-    out.zero_()
-    fin.zero_()
-    graph.replay()
-    torch.cuda.synchronize()
-    assert torch.equal(out, out_e) and torch.equal(fin, fin_e)
+    for _ in range(3):
+        out.zero_()
+        fin.zero_()
+        graph.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(out, out_e) and torch.equal(fin, fin_e)
+    assert kda.last_device_status(ws) == kda.OK
 
 
 # ----------------------------------------------------------------- k-side helpers

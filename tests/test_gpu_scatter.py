@@ -67,7 +67,8 @@ def check_placed(buf, rows, dense, T_used):
                                            (kda.KERNEL_TC_HELPERS, -1), (kda.KERNEL_SPLIT, 1),
                                            (kda.KERNEL_SPLIT, 2), (kda.KERNEL_SPLIT, 4),
                                            (kda.KERNEL_SPLIT, 8), (kda.KERNEL_REF, 1),
-                                           (kda.KERNEL_PIPE, 1)])
+                                           (kda.KERNEL_PIPE, 1),
+                                           (kda.KERNEL_SPLIT_STREAMED, 4)])
 def test_prefill_scatter_places_the_dense_rows(kernel, vsplit):
     """Ragged sequences (a 1-token and an empty one, tails), tokens past cu_seqlens[N]."""
     inp = W.make_inputs(W.custom([130, 1, 0, 64, 257, 70], 2, seed=61, pad_tokens=5))
