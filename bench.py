@@ -28,7 +28,8 @@ cpu_baseline  the fp64 CPU oracle (test infrastructure) on a bounded sample
 --impl reference  times that oracle as the reference arm.
 --stamps    the per-chunk phase breakdown of the warp-specialised kernel: builds
             the -DKDA_PHASE_STAMPS variant of the library and prints medians of
-            the clock64 stamps of CTA 0 (not a bench line).
+            the clock64 stamps of CTA 0 (not a bench line); with --kernel split
+            or streamed, the timeline of the split path's CTAs instead.
 
 L2: the inputs (352 MB per step) exceed the 129 MB L2, and four copies of
 them are rotated so that no step finds the previous step's data in L2.
@@ -108,7 +109,7 @@ def kernel_source_hash(kernel_name: str | None = None) -> str:
         text = open(os.path.join(csrc, name), encoding="utf-8").read()
         text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
         text = re.sub(r"//[^\n]*", " ", text)
-        text = re.sub(r"PSTAMP\([^;]*\);", " ", text)   # phase stamps: empty outside the stamps build
+        text = re.sub(r"[PT]STAMP\([^;]*\);", " ", text)   # stamps: empty outside the stamps build
         text = " ".join(text.split())
         h.update(name.encode() + b"\0" + text.encode())
     return h.hexdigest()[:16]
@@ -334,6 +335,51 @@ KSIDE_SLOTS = {19: "loop top", 25: "input wait (MMA thread)", 16: "inputs landed
 KSIDE_ORDER = [19, 25, 16, 17, 18, 20, 21, 22, 1, 24, 29]
 
 
+def run_split_timeline(args, kda, w, d, dev):
+    """Timeline of one split-path call (--kernel split or streamed) in the stamps build:
+    when each k-side CTA and each warp-level chain CTA (P = 4, 8) started and ended, when
+    each chain CTA's first record was ready (streamed), which k-side CTAs left their SM to
+    the chains; microseconds from the first k-side CTA's start, (min, median, max)."""
+    kernel = kda.KERNEL_SPLIT_STREAMED if args.kernel == "streamed" else kda.KERNEL_SPLIT
+    T, H, N = sum(w.lengths), w.heads, w.num_seqs
+    need = 1024 + ((T + 63) // 64 + N) * H * (66560 + 4)
+    ws_bytes = need + 65536
+    ws = torch.zeros(ws_bytes, dtype=torch.uint8, device=dev)
+    off = (ws_bytes - 32768) & ~255
+    for _ in range(max(3, args.warmup) + 1):
+        ws[off:].zero_()
+        kda.chunk_prefill_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], d["A_log"],
+                              d["dt_bias"], d["lower_bound"], d["scale"], d["initial_state"],
+                              d["cu_seqlens"], workspace=ws, kernel=kernel, vsplit=args.vsplit)
+    torch.cuda.synchronize()
+    st = kda.last_device_status(ws)
+    if st != kda.OK:
+        raise kda.KDAError(st, "device status")
+    _, P, _ = kda.plan(T, N, H, ws_bytes, args.vsplit, kernel)
+    words = ws[off:off + 32768].cpu().view(torch.int64).tolist()
+    nk = min(512, 2 * torch.cuda.get_device_properties(dev).multi_processor_count)
+    ks = [words[1024 + 4 * b:1024 + 4 * b + 4] for b in range(nk)]
+    ks = [k for k in ks if k[0] > 0]
+    ch = [words[4 * b:4 * b + 4] for b in range(min(256, N * H * P))]
+    t0 = min(k[0] for k in ks)
+
+    def q3(vals):
+        vals = sorted((v - t0) / 1e3 for v in vals)
+        return [round(vals[0], 1), round(vals[len(vals) // 2], 1), round(vals[-1], 1)] if vals else None
+    res = {"workload": w.name, "path": "streamed" if kernel == kda.KERNEL_SPLIT_STREAMED else "split",
+           "vsplit": P, "unit": "us from the first k-side CTA's start: min, median, max",
+           "kside_ctas": len(ks), "kside_ctas_that_left_their_sm": sum(k[3] >= 65536 for k in ks),
+           "kside_start": q3([k[0] for k in ks]), "kside_end": q3([k[1] for k in ks]),
+           "kside_end_working_ctas": q3([k[1] for k in ks if k[3] < 65536])}
+    if P >= 4:
+        res.update({"chain_ctas": len(ch), "chain_start": q3([c[0] for c in ch]),
+                    "chain_end": q3([c[2] for c in ch]),
+                    "chain_sms_distinct": len({c[3] for c in ch})})
+        if kernel == kda.KERNEL_SPLIT_STREAMED:
+            res["chain_first_record_ready"] = q3([c[1] for c in ch])
+    print(json.dumps(res, indent=1), flush=True)
+
+
 def run_stamps(args):
     """Phase breakdown of KDA_KERNEL_PIPE: build the phase-stamp variant of the library
     (-DKDA_PHASE_STAMPS), run the workload a few times, read the clock64 stamps CTA 0 (the
@@ -347,6 +393,8 @@ def run_stamps(args):
     w = W.workload(args.workload, args.n) if args.workload == 3 else W.workload(args.workload)
     dev = torch.device("cuda", torch.cuda.current_device())
     d = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in W.make_inputs(w).items()}
+    if args.kernel in ("split", "streamed"):
+        return run_split_timeline(args, kda, w, d, dev)
     ws_bytes = 1 << 16
     ws = torch.zeros(ws_bytes, dtype=torch.uint8, device=dev)
     off = (ws_bytes - 16384) & ~255

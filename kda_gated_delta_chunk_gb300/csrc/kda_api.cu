@@ -226,6 +226,12 @@ int fwd_impl(const void* q, const void* k, const void* v, const void* g, const v
   if (kernel == KDA_KERNEL_PIPE && workspace_bytes >= 32768)
     p.stamps = reinterpret_cast<unsigned long long*>(static_cast<unsigned char*>(workspace) +
                                                      ((workspace_bytes - 16384) & ~(size_t)255));
+  // ... and for the split path, the last 32 KB of a workspace at least that much larger than
+  // the call's records and claim words take its timeline (TSTAMP in kda_internal.cuh)
+  if ((kernel == KDA_KERNEL_SPLIT || kernel == KDA_KERNEL_SPLIT_STREAMED) &&
+      workspace_bytes >= kda::helper_workspace_bytes(total_tokens, heads, num_seqs) + 33024)
+    p.stamps = reinterpret_cast<unsigned long long*>(static_cast<unsigned char*>(workspace) +
+                                                     ((workspace_bytes - 32768) & ~(size_t)255));
 #endif
   p.out_index = scatter ? out_index : nullptr;
   p.out_rows = out_rows;

@@ -142,6 +142,10 @@ __global__ void __launch_bounds__(NT2, 1)
   const int t0 = p.cu_seqlens[n], t1 = p.cu_seqlens[n + 1];
   const bool streamed = p.stream_sms > 0;
   int* last_s = reinterpret_cast<int*>(sm + L_::OFF_MISC);
+  if (tid == 0 && unit < 256) {
+    TSTAMP(4 * unit, globaltimer_ns());
+    TSTAMP(4 * unit + 3, sm_id());
+  }
   if (t0 < 0 || t1 < t0 || (int64_t)t1 > p.total_tokens || p.cu_seqlens[0] != 0) {
     if (tid == 0) record_error(p.status, KDA_ERR_BAD_CU_SEQLENS, 3);
     if (streamed) stream_finish(p, tid, NT2, last_s, [] { __syncthreads(); });
@@ -205,6 +209,7 @@ __global__ void __launch_bounds__(NT2, 1)
             break;
           }
           fence_proxy_async_global();   // its generic stores -> this bulk copy
+          if (j == 0 && unit < 256) TSTAMP(4 * unit + 1, globaltimer_ns());
         }
         issue(j, b);
         issued = j + 1;
@@ -485,6 +490,7 @@ __global__ void __launch_bounds__(NT2, 1)
       else
         static_cast<float*>(p.final_state)[idx] = S[nt][e];
     }
+  if (tid == 0 && unit < 256) TSTAMP(4 * unit + 2, globaltimer_ns());
   if (streamed) stream_finish(p, tid, NTC, last_s, [] { group_sync(1, NTC); });
 }
 

@@ -78,6 +78,22 @@ struct Params {
   unsigned long long* stamps;
 };
 
+// Timeline stamps of the split path, in builds with -DKDA_PHASE_STAMPS only (nothing
+// otherwise): word `index` of Params::stamps gets `value`.  Warp-level chain CTA b < 256:
+// words 4b .. 4b+3 = start, first record ready (streamed), end (globaltimer ns), %smid.
+// k-side CTA b < 512: words 1024 + 4b .. = start, end, unused, %smid (+ 65536 when the CTA
+// left its SM to the chains).
+#ifdef KDA_PHASE_STAMPS
+#define TSTAMP(index, value)                              \
+  do {                                                    \
+    if (p.stamps != nullptr) p.stamps[(index)] = (value); \
+  } while (0)
+#else
+#define TSTAMP(index, value) \
+  do {                       \
+  } while (0)
+#endif
+
 // A per-device one-time host step (a kernel's shared-memory attribute): the fast path is one
 // atomic load; the first calls on a device serialise on a mutex, so two host threads that
 // make a device's first call at the same time both see the step done.

@@ -182,6 +182,10 @@ __global__ void __launch_bounds__(NT, 2)
   const uint32_t bar_in = sb + K_BAR, bar_mma = bar_in + 8;
   unsigned char* ws = reinterpret_cast<unsigned char*>(p.status) + kSplitHeader;
   const bool streamed = p.stream_sms > 0;
+  if (tid == 0 && blockIdx.x < 512) {
+    TSTAMP(1024 + 4 * blockIdx.x, globaltimer_ns());
+    TSTAMP(1024 + 4 * blockIdx.x + 3, sm_id());
+  }
   if (streamed) {
     pdl_launch_dependents();   // the chain grid may start once every k-side CTA has begun
     // leave the SMs below stream_sms to the chain CTAs (at most two CTAs per such SM yield,
@@ -203,6 +207,10 @@ __global__ void __launch_bounds__(NT, 2)
         while (ld_relaxed_gpu(p.status + kStreamStartWord) < (int)gridDim.x &&
                globaltimer_ns() - w0 < 20000ull)
           __nanosleep(128);
+      }
+      if (tid == 0 && blockIdx.x < 512) {
+        TSTAMP(1024 + 4 * blockIdx.x + 1, globaltimer_ns());
+        TSTAMP(1024 + 4 * blockIdx.x + 3, sm_id() + 65536u);
       }
       return;
     }
@@ -715,6 +723,7 @@ __global__ void __launch_bounds__(NT, 2)
   tc_fence_before();
   __syncthreads();
   if (warp == 0) tmem_dealloc(tmem, TM_COLS);
+  if (tid == 0 && blockIdx.x < 512) TSTAMP(1024 + 4 * blockIdx.x + 1, globaltimer_ns());
   // a helper grid completes only after the fused kernel it serves
   if (p.helpers) pdl_wait();
 }
