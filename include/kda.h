@@ -90,7 +90,8 @@ typedef struct CUstream_st* kda_stream_t;
 
 /* kernel selectors for kda_chunk_prefill_fwd_ex */
 #define KDA_KERNEL_AUTO 0  /* SPLIT_STREAMED when N * heads * P <= SMs / 2 for
-                              P = 8 or 4 and the workspace holds the records
+                              P = 8 or 4, the sequences average 2048 tokens
+                              or more and the workspace holds the records
                               and claim words; else SPLIT when the value
                               split triggers and the workspace holds its
                               records; else TC_HELPERS

@@ -75,7 +75,11 @@ bool known_kernel(int kernel) {
 
 // Value split of the streamed split path: the widest warp-level chain (P = 8, else 4) whose
 // N * heads * P CTAs leave at least half of the SMs to the k-side kernel running beside it;
-// 0 when none does.
+// 0 when none does.  AUTO takes the streamed path only for sequences of 32 chunks or more on
+// average: below that the overlap saves less than the k-side kernel loses on the chains'
+// SMs (graph-timed on GB300: 4 x 512 tokens, H = 4: 21.4 us plain, 26.4 streamed; 1 x 2048,
+// H = 8: 48.6 and 48.3; 1 x 4096, H = 8: 97.0 and 84.9).
+constexpr int64_t kStreamMinTokensPerSeq = 2048;
 int stream_vsplit(int32_t num_seqs, int32_t heads, int sms) {
   const int64_t units = (int64_t)num_seqs * heads;
   if (units <= 0 || num_seqs > kda::kHelperMaxSeqs) return 0;
@@ -121,7 +125,7 @@ int plan(int64_t total_tokens, int32_t num_seqs, int32_t heads, size_t workspace
     P = 1;
   } else if (kernel == KDA_KERNEL_AUTO) {
     if (vsplit == -1 && P > 1 && P_stream > 0 && chunk_count_ok && workspace_bytes >= help_need &&
-        total_tokens > 0) {
+        total_tokens > 0 && total_tokens >= kStreamMinTokensPerSeq * num_seqs) {
       kernel = KDA_KERNEL_SPLIT_STREAMED;
       P = P_stream;
     } else if (P > 1 && workspace_bytes >= split_need && total_tokens > 0) {

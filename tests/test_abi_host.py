@@ -122,7 +122,7 @@ def _records_only(lengths, H):
 
 
 @pytest.mark.parametrize("shape,H,want", [
-    ("tiny", 2, (kda.KERNEL_SPLIT_STREAMED, 8, 2)),        # 1 x 128
+    ("tiny", 2, (kda.KERNEL_SPLIT, 8, 2)),                 # 1 x 128: too short to stream
     ("batched", 16, (kda.KERNEL_PIPE, 1, 1)),              # 128 chains: over 5/8 of the SMs
     ("long", 16, (kda.KERNEL_SPLIT_STREAMED, 4, 2)),       # 1 x 16384: 64 chain CTAs
     ("v1", 8, (kda.KERNEL_SPLIT_STREAMED, 8, 2)),          # N x 4096, H = 8
@@ -165,6 +165,11 @@ def test_auto_helper_conditions(L):
 def test_auto_streamed_split_conditions(L):
     # P = 8 while 2 N H 8 <= SMs, else P = 4 while 2 N H 4 <= SMs, else the plain split
     assert _auto([4096] * 9, 1) == (kda.KERNEL_SPLIT_STREAMED, 8, 2)
+    # sequences of 2048 tokens or more on average
+    assert _auto([2048], 8) == (kda.KERNEL_SPLIT_STREAMED, 8, 2)
+    assert _auto([2047], 8) == (kda.KERNEL_SPLIT, 8, 2)
+    assert _auto([4000, 96], 4) == (kda.KERNEL_SPLIT_STREAMED, 8, 2)
+    assert _auto([4000, 95], 4) == (kda.KERNEL_SPLIT, 8, 2)
     assert _auto([4096] * 10, 1) == (kda.KERNEL_SPLIT_STREAMED, 4, 2)
     assert _auto([4096] * 19, 1) == (kda.KERNEL_SPLIT_STREAMED, 4, 2)
     assert _auto([4096] * 20, 1) == (kda.KERNEL_SPLIT, 4, 2)
@@ -178,9 +183,10 @@ def test_auto_streamed_split_conditions(L):
     # at most 128 sequences (shown on a part with enough SMs for the split)
     def full(lengths, H):   # records and claim words
         return 1024 + ((sum(lengths) + 63) // 64 + len(lengths)) * H * (66560 + 4)
-    assert _auto([64] * 128, 1, sms=4096, ws=full([64] * 128, 1)) == \
+    assert _auto([2048] * 128, 1, sms=4096, ws=full([2048] * 128, 1)) == \
         (kda.KERNEL_SPLIT_STREAMED, 8, 2)
-    assert _auto([64] * 129, 1, sms=4096, ws=full([64] * 129, 1)) == (kda.KERNEL_SPLIT, 8, 2)
+    assert _auto([2048] * 129, 1, sms=4096, ws=full([2048] * 129, 1)) == \
+        (kda.KERNEL_SPLIT, 8, 2)
     # a split factor given by the caller keeps the plain split under AUTO
     assert _auto([16384], 16, vsplit=4) == (kda.KERNEL_SPLIT, 4, 2)
 

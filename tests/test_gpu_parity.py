@@ -468,7 +468,8 @@ def test_errors_returned_with_a_device():
 @pytest.mark.parametrize("kernel", [kda.KERNEL_AUTO, kda.KERNEL_PIPE, kda.KERNEL_SPLIT_STREAMED])
 def test_cuda_graph_capture_and_replay(oracle_mod, kernel):
     """Capture the call on a side stream, replay it three times, compare with eager (AUTO
-    takes the streamed split path on this batch: 12 chains x P = 4)."""
+    takes the split path on this batch; the streamed split path, forced, runs 12 chains x
+    P = 4 beside its k-side kernel)."""
     inp = W.make_inputs(W.custom([200, 64, 3], 4, seed=30))
     d = to_dev(inp)
     out_e, fin_e = run_gpu(inp, kernel)
