@@ -90,7 +90,7 @@ typedef struct CUstream_st* kda_stream_t;
 
 /* kernel selectors for kda_chunk_prefill_fwd_ex */
 #define KDA_KERNEL_AUTO 0  /* SPLIT_STREAMED when N * heads * P <= SMs / 2 for
-                              P = 8 or 4, the sequences average 2048 tokens
+                              P = 8, 4 or 2, the sequences average 2048 tokens
                               or more and the workspace holds the records
                               and claim words; else SPLIT when the value
                               split triggers and the workspace holds its
@@ -120,7 +120,7 @@ typedef struct CUstream_st* kda_stream_t;
                               build chunk c+1's operands while its chain warps
                               run chunk c; no value split (vsplit -1 or 1),
                               needs only the 256-byte workspace               */
-#define KDA_KERNEL_SPLIT_STREAMED 6 /* SPLIT with P = 4 or 8 and the chain kernel
+#define KDA_KERNEL_SPLIT_STREAMED 6 /* SPLIT with P = 2, 4 or 8 and the chain kernel
                               launched beside the k-side kernel (programmatic
                               dependent launch): the chain CTAs take
                               N * heads * P SMs, the k-side CTAs the others,
@@ -182,8 +182,9 @@ int kda_chunk_prefill_fwd(const void* q, const void* k, const void* v, const voi
  * 4 bytes per (chunk slot, head), vsplit -1 or 1 (else
  * KDA_ERR_INVALID_ARG), num_seqs * heads below the SM count and num_seqs
  * <= 128 (else KDA_ERR_INVALID_ARG).  KDA_KERNEL_SPLIT_STREAMED needs that
- * workspace too, vsplit -1 (P = 8, else 4), 4 or 8, 2 * num_seqs * heads * P
- * at most the SM count and num_seqs <= 128 (else KDA_ERR_INVALID_ARG).
+ * workspace too, vsplit -1 (P = 8, else 4, else 2), 2, 4 or 8,
+ * 2 * num_seqs * heads * P at most the SM count and num_seqs <= 128 (else
+ * KDA_ERR_INVALID_ARG).
  */
 int kda_chunk_prefill_fwd_ex(const void* q, const void* k, const void* v, const void* g,
                              const void* beta, const float* A_log, const float* dt_bias,

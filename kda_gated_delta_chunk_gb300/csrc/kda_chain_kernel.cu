@@ -21,6 +21,7 @@
 
 #include "kda_internal.cuh"
 #include "kda_sm100.cuh"
+#include "kda_stream.cuh"
 
 namespace kda {
 namespace {
@@ -92,31 +93,6 @@ __device__ __forceinline__ uint32_t swv(int row, int col) {
 struct ChainMaps {
   CUtensorMap v;        // v as [T][H*128] bf16, box {DV, 64}
 };
-
-// Streamed split path, at the end of every chain CTA (threads 0 .. nthr-1 of it; `sync` is a
-// barrier over them): once the k-side grid has completed, the last chain CTA to finish clears
-// the claim words of the call and the path's counters, so that the next call starts from zero.
-template <typename Sync>
-__device__ void stream_finish(const Params& p, int tid, int nthr, int* last_s, Sync sync) {
-  if (tid == 0) {
-    pdl_wait();
-    __threadfence();
-    *last_s = atomicAdd(p.status + kStreamDoneWord, 1) == (int)gridDim.x - 1;
-  }
-  sync();
-  if (!*last_s) return;
-  __threadfence();
-  int* claims = reinterpret_cast<int*>(reinterpret_cast<unsigned char*>(p.status) +
-                                       helper_claims_offset(p.total_tokens, p.heads, p.num_seqs));
-  const int64_t items = split_slots(p.total_tokens, p.num_seqs) * p.heads;
-  for (int64_t i = tid; i < items; i += nthr) claims[i] = kClaimFree;
-  if (tid == 0) {
-    p.status[kStreamCounterWord] = 0;
-    p.status[kStreamYieldWord] = 0;
-    p.status[kStreamDoneWord] = 0;
-    p.status[kStreamStartWord] = 0;
-  }
-}
 
 // kRowMap: outputs through the out_index row map (its own instantiation)
 template <int DV, bool kRowMap>
@@ -199,18 +175,9 @@ __global__ void __launch_bounds__(NT2, 1)
           if (!mbar_wait(empty0 + 8 * b, (eph >> b) & 1u)) break;
           eph ^= 1u << b;
         }
-        if (streamed) {   // the record is published by the k-side kernel running beside
-          const int64_t slot = slot0 + j;
-          if (!wait_flag(reinterpret_cast<const int*>(reinterpret_cast<const unsigned char*>(p.status) +
-                                                      helper_claims_offset(p.total_tokens, H, p.num_seqs)) +
-                             claim_index(slot, h, p.total_tokens, p.num_seqs),
-                         kClaimStreamed)) {
-            record_error(p.status, KDA_ERR_DEVICE_TIMEOUT, 5);
-            break;
-          }
-          fence_proxy_async_global();   // its generic stores -> this bulk copy
-          if (j == 0 && unit < 256) TSTAMP(4 * unit + 1, globaltimer_ns());
-        }
+        // streamed: the record is published by the k-side kernel running beside
+        if (streamed && !stream_wait_record(p, slot0 + j, h, 5)) break;
+        if (streamed && j == 0 && unit < 256) TSTAMP(4 * unit + 1, globaltimer_ns());
         issue(j, b);
         issued = j + 1;
         if (j + 2 < nch) prefetch_l2(j + 2);
@@ -558,9 +525,9 @@ cudaError_t launch_chain_dv(const Params& p, cudaStream_t stream) {
 
 cudaError_t launch_split(const Params& p, cudaStream_t stream) {
   if (p.vsplit != 1 && p.vsplit != 2 && p.vsplit != 4 && p.vsplit != 8) return cudaErrorInvalidValue;
-  // streamed (the chain beside the k-side kernel): the warp-level chains, with SMs to spare
+  // streamed (the chain beside the k-side kernel): P = 2, 4 or 8, with SMs to spare
   if (p.stream_sms > 0 &&
-      (p.vsplit < 4 || p.stream_sms != p.num_seqs * p.heads * p.vsplit || p.stream_sms >= p.sm_count))
+      (p.vsplit < 2 || p.stream_sms != p.num_seqs * p.heads * p.vsplit || p.stream_sms >= p.sm_count))
     return cudaErrorInvalidValue;
   cudaError_t e = launch_kside(p, stream);
   if (e != cudaSuccess) return e;

@@ -28,6 +28,7 @@
 #include <cuda.h>
 
 #include "kda_internal.cuh"
+#include "kda_stream.cuh"
 #include "kda_sm100.cuh"
 
 namespace kda {
@@ -109,8 +110,11 @@ __global__ void __launch_bounds__(NT4, 1)
   const int h = (unit / P) % H;
   const int n = unit / (P * H);
   const int t0 = p.cu_seqlens[n], t1 = p.cu_seqlens[n + 1];
+  const bool streamed = p.stream_sms > 0;
+  int* last_s = reinterpret_cast<int*>(sm + VS_TSLOT + 4);
   if (t0 < 0 || t1 < t0 || (int64_t)t1 > p.total_tokens || p.cu_seqlens[0] != 0) {
     if (tid == 0) record_error(p.status, KDA_ERR_BAD_CU_SEQLENS, 6);
+    if (streamed) stream_finish(p, tid, NT4, last_s, [] { __syncthreads(); });
     return;
   }
   const int nch = (t1 - t0 + kChunk - 1) / kChunk;
@@ -170,6 +174,8 @@ __global__ void __launch_bounds__(NT4, 1)
           if (!mbar_wait(bar_empty0 + 8 * b, (eph >> b) & 1u)) break;
           eph ^= 1u << b;
         }
+        // streamed: the record is published by the k-side kernel running beside
+        if (streamed && !stream_wait_record(p, slot0 + j, h, 7)) break;
         issue(j);
         issued = j + 1;
         if (j + 1 < nch) prefetch_l2(j + 1);
@@ -407,6 +413,7 @@ __global__ void __launch_bounds__(NT4, 1)
   tc_fence_before();
   group_sync(1, NTC4);
   if (warp == 0) tmem_dealloc(tmem, T_COLS);
+  if (streamed) stream_finish(p, tid, NTC4, last_s, [] { group_sync(1, NTC4); });
 }
 
 typedef CUresult (*EncodeTiledFn4)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
@@ -443,11 +450,18 @@ cudaError_t launch_chain_vs_dv(const Params& p, cudaStream_t stream) {
           es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
     return cudaErrorInvalidValue;
-  if (p.out_index)
-    kda_chain_vs_kernel<DV, true><<<(unsigned)blocks, NT4, VS_BYTES, stream>>>(p, maps);
-  else
-    kda_chain_vs_kernel<DV, false><<<(unsigned)blocks, NT4, VS_BYTES, stream>>>(p, maps);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)blocks);
+  cfg.blockDim = dim3(NT4);
+  cfg.dynamicSmemBytes = VS_BYTES;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = p.stream_sms > 0 ? 1 : 0;   // streamed: beside the k-side kernel
+  if (p.out_index) return cudaLaunchKernelEx(&cfg, kda_chain_vs_kernel<DV, true>, p, maps);
+  return cudaLaunchKernelEx(&cfg, kda_chain_vs_kernel<DV, false>, p, maps);
 }
 
 }  // namespace

@@ -127,7 +127,7 @@ def _records_only(lengths, H):
     ("long", 16, (kda.KERNEL_SPLIT_STREAMED, 4, 2)),       # 1 x 16384: 64 chain CTAs
     ("v1", 8, (kda.KERNEL_SPLIT_STREAMED, 8, 2)),          # N x 4096, H = 8
     ("v2", 8, (kda.KERNEL_SPLIT_STREAMED, 4, 2)),
-    ("v3", 8, (kda.KERNEL_SPLIT, 4, 2)),                   # 24 x 4 chain CTAs: over half
+    ("v3", 8, (kda.KERNEL_SPLIT_STREAMED, 2, 2)),          # 24 x 2 chain CTAs
     ("v7", 8, (kda.KERNEL_SPLIT, 2, 2)),
     ("ragged", 32, (kda.KERNEL_PIPE, 1, 1)),               # 2048 chains: no SM left over
 ])
@@ -163,7 +163,8 @@ def test_auto_helper_conditions(L):
 
 
 def test_auto_streamed_split_conditions(L):
-    # P = 8 while 2 N H 8 <= SMs, else P = 4 while 2 N H 4 <= SMs, else the plain split
+    # P = 8 while 2 N H 8 <= SMs, else P = 4 while 2 N H 4 <= SMs, else P = 2 while
+    # 2 N H 2 <= SMs, else the plain split
     assert _auto([4096] * 9, 1) == (kda.KERNEL_SPLIT_STREAMED, 8, 2)
     # sequences of 2048 tokens or more on average
     assert _auto([2048], 8) == (kda.KERNEL_SPLIT_STREAMED, 8, 2)
@@ -172,7 +173,9 @@ def test_auto_streamed_split_conditions(L):
     assert _auto([4000, 95], 4) == (kda.KERNEL_SPLIT, 8, 2)
     assert _auto([4096] * 10, 1) == (kda.KERNEL_SPLIT_STREAMED, 4, 2)
     assert _auto([4096] * 19, 1) == (kda.KERNEL_SPLIT_STREAMED, 4, 2)
-    assert _auto([4096] * 20, 1) == (kda.KERNEL_SPLIT, 4, 2)
+    assert _auto([4096] * 20, 1) == (kda.KERNEL_SPLIT_STREAMED, 2, 2)
+    assert _auto([4096] * 38, 1) == (kda.KERNEL_SPLIT_STREAMED, 2, 2)
+    assert _auto([4096] * 39, 1) == (kda.KERNEL_SPLIT, 2, 2)
     # the claim words must fit as well as the records
     lengths = [4096] * 2
     assert _auto(lengths, 8, ws=_records_only(lengths, 8)) == (kda.KERNEL_SPLIT, 8, 2)
@@ -193,13 +196,15 @@ def test_auto_streamed_split_conditions(L):
 
 def test_forced_streamed_split(L):
     assert _auto([16384], 16, kernel=kda.KERNEL_SPLIT_STREAMED) == (kda.KERNEL_SPLIT_STREAMED, 4, 2)
+    assert _auto([16384], 16, kernel=kda.KERNEL_SPLIT_STREAMED, vsplit=2) == \
+        (kda.KERNEL_SPLIT_STREAMED, 2, 2)
     assert _auto([4096], 8, kernel=kda.KERNEL_SPLIT_STREAMED, vsplit=4) == \
         (kda.KERNEL_SPLIT_STREAMED, 4, 2)
     refused = [
-        (dict(vsplit=2), kda.ERR_INVALID_ARG),                 # warp-level chains only
-        (dict(vsplit=1), kda.ERR_INVALID_ARG),
+        (dict(vsplit=1), kda.ERR_INVALID_ARG),                 # a value split only
         (dict(vsplit=8), kda.ERR_INVALID_ARG),                 # 2 x 16 x 8 > 152
-        (dict(sms=127), kda.ERR_INVALID_ARG),                  # 2 x 16 x 4 > 127
+        (dict(sms=127, vsplit=4), kda.ERR_INVALID_ARG),        # 2 x 16 x 4 > 127
+        (dict(sms=63), kda.ERR_INVALID_ARG),                   # 2 x 16 x 2 > 63
         (dict(ws=_records_only([16384], 16)), kda.ERR_WORKSPACE_TOO_SMALL),
     ]
     for kw, code in refused:

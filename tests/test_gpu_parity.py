@@ -176,20 +176,20 @@ def test_workload3_vsplit_vs_unsplit(oracle_mod, n):
     check(oracle_mod, inp, out_1, fin_1, heads=heads, tag=f"w3 n={n} P=1")
 
 
-@pytest.mark.parametrize("cfg", [2, 3])
-def test_auto_takes_split_path_when_it_triggers(oracle_mod, cfg):
-    """One long sequence (16 heads) and 2 x 4096 (8 heads): AUTO runs the streamed split
-    path (the chain beside the k-side kernel, P = 4) -- the same bits as forcing it, and as
-    the plain split path at P = 4 (the same records and the same chain arithmetic, only
-    started earlier)."""
-    inp = W.make_inputs(W.workload(cfg, 2) if cfg == 3 else W.workload(cfg))
+@pytest.mark.parametrize("cfg,n,P", [(2, None, 4), (3, 2, 4), (3, 3, 2)])
+def test_auto_takes_split_path_when_it_triggers(oracle_mod, cfg, n, P):
+    """One long sequence (16 heads), 2 x 4096 and 3 x 4096 (8 heads): AUTO runs the
+    streamed split path (the chain beside the k-side kernel; P = 4, 4 and 2, the tcgen05
+    chain at P = 2) -- the same bits as forcing it, and as the plain split path at the same
+    P (the same records and the same chain arithmetic, only started earlier)."""
+    inp = W.make_inputs(W.workload(cfg, n) if cfg == 3 else W.workload(cfg))
     T, H, N = inp["q"].shape[0], inp["q"].shape[1], inp["cu_seqlens"].numel() - 1
     assert kda.plan(T, N, H, kda.workspace_size(T, H, N), -1, kda.KERNEL_AUTO)[:2] == \
-        (kda.KERNEL_SPLIT_STREAMED, 4)
+        (kda.KERNEL_SPLIT_STREAMED, P)
     out_a, fin_a = run_gpu(inp)
     out_s, fin_s = run_gpu(inp, kda.KERNEL_SPLIT_STREAMED)
     assert torch.equal(out_a, out_s) and torch.equal(fin_a, fin_s)
-    out_p, fin_p = run_gpu(inp, kda.KERNEL_SPLIT, vsplit=4)
+    out_p, fin_p = run_gpu(inp, kda.KERNEL_SPLIT, vsplit=P)
     assert torch.equal(out_a, out_p) and torch.equal(fin_a, fin_p)
 
 
@@ -199,6 +199,8 @@ def test_auto_takes_split_path_when_it_triggers(oracle_mod, cfg):
     ([2048, 2048], 2, "f32", 8),
     ([8192], 4, "f32", 8),
     ([100], 1, "bf16", 8),
+    ([1, 63, 64, 65, 130, 0, 200], 2, "f32", 2),     # the tcgen05 chain at P = 2
+    ([300, 5, 64, 129, 900], 3, "bf16", 2),
 ])
 def test_streamed_split_against_the_oracle(oracle_mod, lengths, H, sd, P):
     """The streamed split path (chain CTAs copying each record as the k-side kernel
