@@ -90,7 +90,8 @@ typedef struct CUstream_st* kda_stream_t;
 
 /* kernel selectors for kda_chunk_prefill_fwd_ex */
 #define KDA_KERNEL_AUTO 0  /* SPLIT_STREAMED when N * heads * P <= SMs / 2 for
-                              P = 8, 4 or 2, the sequences average 2048 tokens
+                              P = 8, 4 or 2, or N * heads <= 3 SMs / 8 for
+                              P = 1, the sequences average 2048 tokens
                               or more and the workspace holds the records
                               and claim words; else SPLIT when the value
                               split triggers and the workspace holds its
@@ -120,13 +121,14 @@ typedef struct CUstream_st* kda_stream_t;
                               build chunk c+1's operands while its chain warps
                               run chunk c; no value split (vsplit -1 or 1),
                               needs only the 256-byte workspace               */
-#define KDA_KERNEL_SPLIT_STREAMED 6 /* SPLIT with P = 2, 4 or 8 and the chain kernel
+#define KDA_KERNEL_SPLIT_STREAMED 6 /* SPLIT (any P) with the chain kernel
                               launched beside the k-side kernel (programmatic
                               dependent launch): the chain CTAs take
                               N * heads * P SMs, the k-side CTAs the others,
                               and each chain CTA copies a record as soon as
                               its claim word says it is written (bounded
-                              wait).  Needs 2 * N * heads * P <= SM count,
+                              wait).  Needs 2 * N * heads * P <= SM count
+                              (P > 1) or 8 * N * heads <= 3 SM count (P = 1),
                               N <= 128 and the workspace of TC_HELPERS        */
 
 /*
@@ -182,8 +184,9 @@ int kda_chunk_prefill_fwd(const void* q, const void* k, const void* v, const voi
  * 4 bytes per (chunk slot, head), vsplit -1 or 1 (else
  * KDA_ERR_INVALID_ARG), num_seqs * heads below the SM count and num_seqs
  * <= 128 (else KDA_ERR_INVALID_ARG).  KDA_KERNEL_SPLIT_STREAMED needs that
- * workspace too, vsplit -1 (P = 8, else 4, else 2), 2, 4 or 8,
- * 2 * num_seqs * heads * P at most the SM count and num_seqs <= 128 (else
+ * workspace too, vsplit -1 (P = 8, else 4, else 2, else 1) or a fixed P,
+ * 2 * num_seqs * heads * P at most the SM count (P > 1; for P = 1,
+ * 8 * num_seqs * heads at most 3 SM count) and num_seqs <= 128 (else
  * KDA_ERR_INVALID_ARG).
  */
 int kda_chunk_prefill_fwd_ex(const void* q, const void* k, const void* v, const void* g,

@@ -75,17 +75,21 @@ bool known_kernel(int kernel) {
 
 // Value split of the streamed split path: the narrowest value slice (P = 8, else 4, else 2)
 // whose N * heads * P chain CTAs leave at least half of the SMs to the k-side kernel running
-// beside it; 0 when none does.  AUTO takes the streamed path only for sequences of 32 chunks or more on
-// average: below that the overlap saves less than the k-side kernel loses on the chains'
-// SMs (graph-timed on GB300: 4 x 512 tokens, H = 4: 21.4 us plain, 26.4 streamed; 1 x 2048,
-// H = 8: 48.6 and 48.3; 1 x 4096, H = 8: 97.0 and 84.9).
+// beside it; else the unsplit tcgen05 chain (P = 1) while its N * heads CTAs leave 5/8 of the
+// SMs (measured on GB300, 4096-token sequences, H = 8, plain split at P = 2 against streamed
+// P = 1: 5 sequences 209.7 / 211.9 us, 6: 227.2 / 213.6, 7: 241.8 / 224.1, 8: 262.0 / 265.4,
+// 9: 276.3 / 322.2); 0 when none of these holds.  AUTO takes the streamed path only for
+// sequences of 32 chunks or more on average: below that the overlap saves less than the
+// k-side kernel loses on the chains' SMs (graph-timed on GB300: 4 x 512 tokens, H = 4:
+// 21.4 us plain, 26.4 streamed; 1 x 2048, H = 8: 48.6 and 48.3; 1 x 4096, H = 8: 97.0 and
+// 84.9).
 constexpr int64_t kStreamMinTokensPerSeq = 2048;
 int stream_vsplit(int32_t num_seqs, int32_t heads, int sms) {
   const int64_t units = (int64_t)num_seqs * heads;
   if (units <= 0 || num_seqs > kda::kHelperMaxSeqs) return 0;
   for (int P = 8; P >= 2; P /= 2)
     if (2 * units * P <= sms) return P;
-  return 0;
+  return 8 * units <= 3 * (int64_t)sms ? 1 : 0;
 }
 
 // The path of a call: validated selectors, then AUTO resolved.  The split path (k-side
@@ -109,8 +113,8 @@ int plan(int64_t total_tokens, int32_t num_seqs, int32_t heads, size_t workspace
     if (workspace_bytes < split_need) return KDA_ERR_WORKSPACE_TOO_SMALL;
   } else if (kernel == KDA_KERNEL_SPLIT_STREAMED) {
     if (vsplit == -1) P = P_stream;
-    if ((P != 2 && P != 4 && P != 8) || num_seqs > kda::kHelperMaxSeqs || !chunk_count_ok ||
-        2 * (int64_t)num_seqs * heads * P > sms)
+    if ((P != 1 && P != 2 && P != 4 && P != 8) || num_seqs > kda::kHelperMaxSeqs || !chunk_count_ok ||
+        (P > 1 ? 2 * (int64_t)num_seqs * heads * P > sms : 8 * (int64_t)num_seqs * heads > 3 * (int64_t)sms))
       return KDA_ERR_INVALID_ARG;
     if (workspace_bytes < help_need) return KDA_ERR_WORKSPACE_TOO_SMALL;
   } else if (kernel == KDA_KERNEL_PIPE) {

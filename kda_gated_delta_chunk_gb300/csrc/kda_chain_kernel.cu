@@ -525,9 +525,9 @@ cudaError_t launch_chain_dv(const Params& p, cudaStream_t stream) {
 
 cudaError_t launch_split(const Params& p, cudaStream_t stream) {
   if (p.vsplit != 1 && p.vsplit != 2 && p.vsplit != 4 && p.vsplit != 8) return cudaErrorInvalidValue;
-  // streamed (the chain beside the k-side kernel): P = 2, 4 or 8, with SMs to spare
+  // streamed (the chain beside the k-side kernel): with SMs to spare
   if (p.stream_sms > 0 &&
-      (p.vsplit < 2 || p.stream_sms != p.num_seqs * p.heads * p.vsplit || p.stream_sms >= p.sm_count))
+      (p.stream_sms != p.num_seqs * p.heads * p.vsplit || p.stream_sms >= p.sm_count))
     return cudaErrorInvalidValue;
   cudaError_t e = launch_kside(p, stream);
   if (e != cudaSuccess) return e;

@@ -18,6 +18,7 @@
 #include <cuda.h>
 
 #include "kda_internal.cuh"
+#include "kda_stream.cuh"
 #include "kda_sm100.cuh"
 
 namespace kda {
@@ -110,8 +111,11 @@ __global__ void __launch_bounds__(NT3, 1)
   __syncthreads();
   const int n = flags[0];
   const int t0 = p.cu_seqlens[n], t1 = p.cu_seqlens[n + 1];
+  const bool streamed = p.stream_sms > 0;
+  int* last_s = flags + 1;
   if (t0 < 0 || t1 < t0 || (int64_t)t1 > p.total_tokens || p.cu_seqlens[0] != 0) {
     if (tid == 0) record_error(p.status, KDA_ERR_BAD_CU_SEQLENS, 5);
+    if (streamed) stream_finish(p, tid, NT3, last_s, [] { __syncthreads(); });
     return;
   }
   const int nch = (t1 - t0 + kChunk - 1) / kChunk;
@@ -158,8 +162,14 @@ __global__ void __launch_bounds__(NT3, 1)
     tma_prefetch_2d(&maps.v, xcol, t0 + kChunk * i);
     tma_prefetch_2d(&maps.v, xcol + 64, t0 + kChunk * i);
   };
+  // streamed: each record is published by the k-side kernel running beside (thread 0 waits
+  // for it before the copy; a wait that gives up stops the loop at the next barrier)
+  bool rec_fail = false;
   if (tid == 0 && nch > 0) {
-    issue(0);
+    if (!streamed || stream_wait_record(p, slot0, h, 8))
+      issue(0);
+    else
+      rec_fail = true;
     if (nch > 1) prefetch_l2(1);
     if (nch > 2) prefetch_l2(2);
   }
@@ -193,7 +203,7 @@ __global__ void __launch_bounds__(NT3, 1)
   uint32_t ph_mma = 0;
   bool failed = false;
   int site = 0;
-  int pending = (nch > 0) ? 1 : 0;   // stages with a fetch in flight (thread 0's view)
+  int pending = (nch > 0 && !rec_fail) ? 1 : 0;   // stages with a fetch in flight (thread 0's view)
   bool mma_out = false;              // an MMA commit not yet waited for (thread 0)
   int L_prev = 0;
 
@@ -307,14 +317,18 @@ __global__ void __launch_bounds__(NT3, 1)
       mma_commit(bar_u);
       mma_out = true;
       if (i + 1 < nch) {
-        issue(i + 1);
-        pending |= 1 << (buf ^ 1);
+        if (!streamed || stream_wait_record(p, slot0 + i + 1, h, 8)) {
+          issue(i + 1);
+          pending |= 1 << (buf ^ 1);
+        } else {
+          rec_fail = true;
+        }
       }
       if (i + 3 < nch) prefetch_l2(i + 3);
     }
     if (i > 0) store_o(c0 - kChunk, L_prev, buf ^ 1);
     {
-      const bool ok = tid != 0 || mbar_wait(bar_u, ph_mma);
+      const bool ok = tid != 0 || (mbar_wait(bar_u, ph_mma) && !rec_fail);
       tc_fence_before();
       if (__syncthreads_or(!ok)) { failed = true; site = 53; break; }   // (B)
     }
@@ -399,6 +413,7 @@ __global__ void __launch_bounds__(NT3, 1)
   tc_fence_before();
   __syncthreads();
   if (warp == 0) tmem_dealloc(tmem, T_COLS);
+  if (streamed) stream_finish(p, tid, NT3, last_s, [] { __syncthreads(); });
 }
 
 typedef CUresult (*EncodeTiledFn3)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
@@ -436,11 +451,18 @@ cudaError_t launch_chain_tc(const Params& p, cudaStream_t stream) {
           es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
     return cudaErrorInvalidValue;
-  if (p.out_index)
-    kda_chain_tc_kernel<true><<<(unsigned)blocks, NT3, SMEM3_BYTES, stream>>>(p, maps);
-  else
-    kda_chain_tc_kernel<false><<<(unsigned)blocks, NT3, SMEM3_BYTES, stream>>>(p, maps);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)blocks);
+  cfg.blockDim = dim3(NT3);
+  cfg.dynamicSmemBytes = SMEM3_BYTES;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = p.stream_sms > 0 ? 1 : 0;   // streamed: beside the k-side kernel
+  if (p.out_index) return cudaLaunchKernelEx(&cfg, kda_chain_tc_kernel<true>, p, maps);
+  return cudaLaunchKernelEx(&cfg, kda_chain_tc_kernel<false>, p, maps);
 }
 
 }  // namespace kda

@@ -128,7 +128,7 @@ def _records_only(lengths, H):
     ("v1", 8, (kda.KERNEL_SPLIT_STREAMED, 8, 2)),          # N x 4096, H = 8
     ("v2", 8, (kda.KERNEL_SPLIT_STREAMED, 4, 2)),
     ("v3", 8, (kda.KERNEL_SPLIT_STREAMED, 2, 2)),          # 24 x 2 chain CTAs
-    ("v7", 8, (kda.KERNEL_SPLIT, 2, 2)),
+    ("v7", 8, (kda.KERNEL_SPLIT_STREAMED, 1, 2)),          # 56 unsplit chain CTAs
     ("ragged", 32, (kda.KERNEL_PIPE, 1, 1)),               # 2048 chains: no SM left over
 ])
 def test_auto_dispatch_of_the_benchmark_shapes(L, shape, H, want):
@@ -175,7 +175,9 @@ def test_auto_streamed_split_conditions(L):
     assert _auto([4096] * 19, 1) == (kda.KERNEL_SPLIT_STREAMED, 4, 2)
     assert _auto([4096] * 20, 1) == (kda.KERNEL_SPLIT_STREAMED, 2, 2)
     assert _auto([4096] * 38, 1) == (kda.KERNEL_SPLIT_STREAMED, 2, 2)
-    assert _auto([4096] * 39, 1) == (kda.KERNEL_SPLIT, 2, 2)
+    assert _auto([4096] * 39, 1) == (kda.KERNEL_SPLIT_STREAMED, 1, 2)   # 8 x 39 <= 3 x 152
+    assert _auto([4096] * 57, 1) == (kda.KERNEL_SPLIT_STREAMED, 1, 2)
+    assert _auto([4096] * 58, 1) == (kda.KERNEL_SPLIT, 2, 2)
     # the claim words must fit as well as the records
     lengths = [4096] * 2
     assert _auto(lengths, 8, ws=_records_only(lengths, 8)) == (kda.KERNEL_SPLIT, 8, 2)
@@ -198,13 +200,16 @@ def test_forced_streamed_split(L):
     assert _auto([16384], 16, kernel=kda.KERNEL_SPLIT_STREAMED) == (kda.KERNEL_SPLIT_STREAMED, 4, 2)
     assert _auto([16384], 16, kernel=kda.KERNEL_SPLIT_STREAMED, vsplit=2) == \
         (kda.KERNEL_SPLIT_STREAMED, 2, 2)
+    assert _auto([16384], 16, kernel=kda.KERNEL_SPLIT_STREAMED, vsplit=1) == \
+        (kda.KERNEL_SPLIT_STREAMED, 1, 2)
     assert _auto([4096], 8, kernel=kda.KERNEL_SPLIT_STREAMED, vsplit=4) == \
         (kda.KERNEL_SPLIT_STREAMED, 4, 2)
     refused = [
-        (dict(vsplit=1), kda.ERR_INVALID_ARG),                 # a value split only
+        (dict(vsplit=3), kda.ERR_INVALID_ARG),
         (dict(vsplit=8), kda.ERR_INVALID_ARG),                 # 2 x 16 x 8 > 152
         (dict(sms=127, vsplit=4), kda.ERR_INVALID_ARG),        # 2 x 16 x 4 > 127
-        (dict(sms=63), kda.ERR_INVALID_ARG),                   # 2 x 16 x 2 > 63
+        (dict(sms=63, vsplit=2), kda.ERR_INVALID_ARG),         # 2 x 16 x 2 > 63
+        (dict(sms=42), kda.ERR_INVALID_ARG),                   # and 8 x 16 > 3 x 42
         (dict(ws=_records_only([16384], 16)), kda.ERR_WORKSPACE_TOO_SMALL),
     ]
     for kw, code in refused:

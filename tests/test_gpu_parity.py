@@ -176,11 +176,11 @@ def test_workload3_vsplit_vs_unsplit(oracle_mod, n):
     check(oracle_mod, inp, out_1, fin_1, heads=heads, tag=f"w3 n={n} P=1")
 
 
-@pytest.mark.parametrize("cfg,n,P", [(2, None, 4), (3, 2, 4), (3, 3, 2)])
+@pytest.mark.parametrize("cfg,n,P", [(2, None, 4), (3, 2, 4), (3, 3, 2), (3, 7, 1)])
 def test_auto_takes_split_path_when_it_triggers(oracle_mod, cfg, n, P):
-    """One long sequence (16 heads), 2 x 4096 and 3 x 4096 (8 heads): AUTO runs the
-    streamed split path (the chain beside the k-side kernel; P = 4, 4 and 2, the tcgen05
-    chain at P = 2) -- the same bits as forcing it, and as the plain split path at the same
+    """One long sequence (16 heads), 2, 3 and 7 x 4096 (8 heads): AUTO runs the streamed
+    split path (the chain beside the k-side kernel; P = 4, 4, 2 and 1, the tcgen05 chains
+    at P = 2 and 1) -- the same bits as forcing it, and as the plain split path at the same
     P (the same records and the same chain arithmetic, only started earlier)."""
     inp = W.make_inputs(W.workload(cfg, n) if cfg == 3 else W.workload(cfg))
     T, H, N = inp["q"].shape[0], inp["q"].shape[1], inp["cu_seqlens"].numel() - 1
@@ -201,6 +201,8 @@ def test_auto_takes_split_path_when_it_triggers(oracle_mod, cfg, n, P):
     ([100], 1, "bf16", 8),
     ([1, 63, 64, 65, 130, 0, 200], 2, "f32", 2),     # the tcgen05 chain at P = 2
     ([300, 5, 64, 129, 900], 3, "bf16", 2),
+    ([1, 63, 64, 65, 130, 0, 200], 2, "f32", 1),     # the unsplit tcgen05 chain
+    ([300, 5, 64, 129, 900], 3, "bf16", 1),
 ])
 def test_streamed_split_against_the_oracle(oracle_mod, lengths, H, sd, P):
     """The streamed split path (chain CTAs copying each record as the k-side kernel
