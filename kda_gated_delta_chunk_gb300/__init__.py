@@ -207,19 +207,21 @@ def _need(t, name, dtype, shape=None, token_strided=False):
     be strided: the rest must be dense (views into a wider buffer, e.g. a fused projection)."""
     if not isinstance(t, torch.Tensor):
         raise TypeError(f"{name} must be a torch.Tensor")
-    if t.device.type != "cuda":
+    if not t.is_cuda:
         raise ValueError(f"{name} must be a CUDA tensor")
     if t.dtype != dtype:
         raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
-    if shape is not None and tuple(t.shape) != tuple(shape):
+    if shape is not None and t.shape != tuple(shape):
         raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+    if t.is_contiguous():
+        return
     if token_strided:
         inner = 1
         for size, stride in zip(reversed(t.shape[1:]), reversed(t.stride()[1:])):
             if size > 1 and stride != inner:
                 raise ValueError(f"{name}: only the token dimension may be strided")
             inner *= size
-    elif not t.is_contiguous():
+    else:
         raise ValueError(f"{name} must be contiguous")
 
 
