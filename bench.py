@@ -5,7 +5,7 @@ the method runs inside that call's kernels).  Prints ONE JSON line (rank 0).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                   [--kernel auto|tc|split|streamed|ref|helpers|pipe] [--workload 1]
-                  [--no-cpu-baseline] [--stamps]
+                  [--no-cpu-baseline] [--stamps] [--range-call]
 
 value       tokens/s of the whole job (all ranks), inputs resident in HBM;
             device time from CUDA events over exactly K steps, max over ranks.
@@ -30,6 +30,8 @@ cpu_baseline  the fp64 CPU oracle (test infrastructure) on a bounded sample
             the -DKDA_PHASE_STAMPS variant of the library and prints medians of
             the clock64 stamps of CTA 0 (not a bench line); with --kernel split
             or streamed, the timeline of the split path's CTAs instead.
+--range-call  one call between cudaProfilerStart/Stop, for an ncu range replay
+            of a call whose kernels overlap (not a bench line).
 
 L2: the inputs (352 MB per step) exceed the 129 MB L2, and four copies of
 them are rotated so that no step finds the previous step's data in L2.
@@ -87,9 +89,14 @@ HOST_ONLY_SOURCES = ("kda_api.cu",)
 # the sources a kernel is built from, where that is a strict subset (headers included): its
 # committed traffic figure stays valid while these are unchanged.  Other kernels hash every
 # device source.
+_SPLIT_SOURCES = ("kda_kside_kernel.cu", "kda_chain_kernel.cu", "kda_chain_vs_kernel.cu",
+                  "kda_chain_tc_kernel.cu", "kda_stream.cuh", "kda_internal.cuh", "kda_sm100.cuh",
+                  "kda_tc_common.cuh")
 KERNEL_SOURCES = {
     "kda_pipe_kernel": ("kda_pipe_kernel.cu", "kda_internal.cuh", "kda_sm100.cuh",
                         "kda_tc_common.cuh"),
+    "kda_split_path": _SPLIT_SOURCES,
+    "kda_split_streamed_path": _SPLIT_SOURCES,
 }
 
 
@@ -380,6 +387,44 @@ def run_split_timeline(args, kda, w, d, dev):
     print(json.dumps(res, indent=1), flush=True)
 
 
+def run_range_call(args):
+    """One call of the workload between cudaProfilerStart and cudaProfilerStop (after
+    max(3, --warmup) untimed calls), for `ncu --replay-mode app-range`: the DRAM traffic of a
+    call whose kernels overlap (the streamed split path), which kernel replay serialises."""
+    from kda_gated_delta_chunk_gb300 import build as kbuild
+    import kda_gated_delta_chunk_gb300 as kda
+    kbuild.build()
+    kernel = {"auto": kda.KERNEL_AUTO, "tc": kda.KERNEL_TC, "ref": kda.KERNEL_REF,
+              "split": kda.KERNEL_SPLIT, "streamed": kda.KERNEL_SPLIT_STREAMED,
+              "helpers": kda.KERNEL_TC_HELPERS, "pipe": kda.KERNEL_PIPE}[args.kernel]
+    w = W.workload(args.workload, args.n) if args.workload == 3 else W.workload(args.workload)
+    dev = torch.device("cuda", torch.cuda.current_device())
+    d = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in W.make_inputs(w).items()}
+    T, H, N = sum(w.lengths), w.heads, w.num_seqs
+    ws = torch.zeros(max(kda.workspace_size(T, H, N), 1024 + ((T + 63) // 64 + N) * H * (66560 + 4)),
+                     dtype=torch.uint8, device=dev)
+    out, fin = torch.empty_like(d["q"]), torch.empty_like(d["initial_state"])
+
+    def call():
+        kda.chunk_prefill_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], d["A_log"],
+                              d["dt_bias"], d["lower_bound"], d["scale"], d["initial_state"],
+                              d["cu_seqlens"], out=out, final_state=fin, workspace=ws,
+                              kernel=kernel, vsplit=args.vsplit)
+    for _ in range(max(3, args.warmup)):
+        call()
+    torch.cuda.synchronize()
+    torch.cuda.profiler.start()
+    call()
+    torch.cuda.synchronize()
+    torch.cuda.profiler.stop()
+    st = kda.last_device_status(ws)
+    if st != kda.OK:
+        raise kda.KDAError(st, "device status")
+    path, P, launches = kda.plan(T, N, H, ws.numel(), args.vsplit, kernel)
+    print(json.dumps({"workload": w.name, "path": path, "vsplit": P, "launches": launches}),
+          flush=True)
+
+
 def run_stamps(args):
     """Phase breakdown of KDA_KERNEL_PIPE: build the phase-stamp variant of the library
     (-DKDA_PHASE_STAMPS), run the workload a few times, read the clock64 stamps CTA 0 (the
@@ -651,9 +696,14 @@ def main():
     ap.add_argument("--stamps", action="store_true",
                     help="per-chunk phase breakdown of the pipelined kernel from the phase-stamp "
                          "build (clock64 stamps of CTA 0), then exit")
+    ap.add_argument("--range-call", action="store_true",
+                    help="one prefill call (after --warmup calls) between cudaProfilerStart and "
+                         "cudaProfilerStop, for an ncu range replay of the whole call, then exit")
     args = ap.parse_args()
     if args.stamps:
         return run_stamps(args)
+    if args.range_call:
+        return run_range_call(args)
     if args.decode > 0:
         return run_decode(args)
     if args.scatter:
