@@ -145,10 +145,14 @@ typedef struct CUstream_st* kda_stream_t;
  * (heads * N <= min(SM count - 8, 5 SM count / 8)), it also holds the records of
  * those paths: a 1 KB header, then 66,560 bytes per (chunk slot, head),
  * with ceil(total_tokens / 64) + N slots for the largest such N -- about
- * 1 KB per token-head -- and, for the helpers, one int32 claim word per
+ * 1 KB per token-head -- and, for the helpers and the streamed split path
+ * (whose batches lie inside the helpers' band), one int32 claim word per
  * (chunk slot, head).  A smaller workspace (at least 256 bytes) is
  * accepted; KDA_KERNEL_AUTO then runs the fused kernel alone.  Always a
- * multiple of 16; 0 for negative arguments.
+ * multiple of 16; 0 for negative arguments.  The header's counters and
+ * the claim words are left at zero by every call that completes (after a
+ * device timeout too), so a zero-filled workspace can be reused by any
+ * number of calls.
  */
 size_t kda_workspace_size(int64_t total_tokens, int32_t heads, int32_t max_seqs);
 
