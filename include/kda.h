@@ -150,10 +150,10 @@ typedef struct CUstream_st* kda_stream_t;
  * (chunk slot, head).  A smaller workspace (at least 256 bytes) is
  * accepted; KDA_KERNEL_AUTO then runs the fused kernel alone.  Always a
  * multiple of 16; 0 for negative arguments.  A zero-filled workspace can
- * serve any number of calls, of any path: the streamed split path and the
- * warp-specialised kernel leave their header counters and claim words at
- * zero when a call ends (after a device timeout too), and the helpers
- * reset theirs when a call starts.
+ * serve any number of calls, of any path: the streamed split path leaves
+ * its header counters and claim words at zero when a call ends (after a
+ * device timeout too), the helpers reset theirs when a call starts, and
+ * the other paths use neither.
  */
 size_t kda_workspace_size(int64_t total_tokens, int32_t heads, int32_t max_seqs);
 
