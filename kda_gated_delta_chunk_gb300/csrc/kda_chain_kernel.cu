@@ -16,7 +16,9 @@
 // The products are narrow (N = DV), so they run as warp-level mma.sync tiles
 // (bf16 in, fp32 accumulate) with S held in registers by eight consumer warps; a ninth
 // warp copies the records of the next chunks (one ahead, or two for the 16-column slice)
-// in while this one is processed, so that no consumer stalls on issuing a copy.
+// in while this one is processed, so that no consumer stalls on issuing a copy.  On the
+// streamed split path that warp first waits for each record's claim word, the k-side
+// kernel running beside this one (kda_stream.cuh).
 #include <cuda.h>
 
 #include "kda_internal.cuh"

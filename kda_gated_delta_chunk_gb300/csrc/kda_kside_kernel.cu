@@ -23,6 +23,13 @@
 // it leaves free, the CTAs take items from a shared counter, last chunk index
 // first, claim each as they start it and publish the record with a release
 // store; the first claim lost to the sequence's own CTA ends a helper.
+//
+// Streamed mode (KDA_KERNEL_SPLIT_STREAMED, Params::stream_sms > 0): the chain kernel
+// is this grid's programmatic dependent and runs beside it.  Every CTA lets it start
+// at once; the CTAs that start on the chains' SMs (%smid below stream_sms, at most
+// two per such SM) give up the tensor-memory allocation permit, wait until the whole
+// grid has started and leave; the others take items from the path's counter, first
+// chunk index first, and publish each record through its claim word.
 #include <cuda.h>
 
 #include "kda_internal.cuh"
