@@ -77,3 +77,23 @@ def test_the_batched_workload_is_bound_by_hbm():
     t_hbm = bench.algorithmic_bytes(w) / (hbm_gbs * 1e9)
     t_tensor = bench.algorithmic_flops(w) / (bf16_tflops * 1e12)
     assert t_hbm > t_tensor
+
+
+def test_kernel_source_sets_name_existing_device_sources():
+    """Every file a per-kernel source hash covers exists, so a renamed or removed file cannot
+    leave a committed traffic figure keyed to sources that are no longer built."""
+    csrc = os.path.join(ROOT, "kda_gated_delta_chunk_gb300", "csrc")
+    for name, files in bench.KERNEL_SOURCES.items():
+        for f in files:
+            assert os.path.isfile(os.path.join(csrc, f)), (name, f)
+            assert f not in bench.HOST_ONLY_SOURCES, (name, f)
+
+
+def test_committed_traffic_entries_name_their_capture():
+    """Each traffic figure names the profile summary it came from, and that file is committed."""
+    import json
+    t = json.load(open(os.path.join(ROOT, "profiles", "traffic.json")))
+    for name, ent in t.items():
+        assert ent["dram_bytes_per_launch"] > 0, name
+        assert os.path.isfile(os.path.join(ROOT, ent["capture"])), (name, ent["capture"])
+        assert len(ent["source_hash"]) == 16, name
