@@ -608,3 +608,43 @@ def test_bounded_wait_runs_out_and_the_context_survives():
     assert kda.last_device_status(ws) == kda.OK
     out_t, fin_t = run_gpu(inp, kda.KERNEL_TC, vsplit=1)
     assert torch.equal(out, out_t) and torch.equal(fin, fin_t)
+
+
+def test_streamed_split_beside_other_work():
+    """The streamed split path relies on no placement: with the warp-specialised kernel of
+    another batch filling most SMs from a second stream, and a second streamed call on a
+    third, every call still completes with status OK and the same bits as run alone (its
+    k-side CTAs that cannot start at once start later; the chains wait for records a bounded
+    time, far longer than the other work takes)."""
+    inp_a = W.make_inputs(W.custom([4096], 8, seed=71))
+    inp_b = W.make_inputs(W.custom([2048] * 8, 16, seed=72))
+    inp_c = W.make_inputs(W.custom([4096, 4096], 8, seed=73))
+    alone = [run_gpu(inp_a, kda.KERNEL_SPLIT_STREAMED), run_gpu(inp_b, kda.KERNEL_PIPE),
+             run_gpu(inp_c, kda.KERNEL_SPLIT_STREAMED)]
+    streams = [torch.cuda.Stream() for _ in range(3)]
+    calls = []
+    for inp, kern, s in zip((inp_a, inp_b, inp_c),
+                            (kda.KERNEL_SPLIT_STREAMED, kda.KERNEL_PIPE, kda.KERNEL_SPLIT_STREAMED),
+                            streams):
+        d = to_dev(inp)
+        T, H, N = d["q"].shape[0], d["q"].shape[1], d["cu_seqlens"].numel() - 1
+        ws = helper_workspace(T, H, N)
+        calls.append((d, kern, s, ws))
+    torch.cuda.synchronize()
+    results = []
+    for _ in range(3):   # several rounds, the three calls in flight together each time
+        outs = []
+        for d, kern, s, ws in (calls[1], calls[0], calls[2]):   # the big one first
+            s.wait_stream(torch.cuda.current_stream())
+            with torch.cuda.stream(s):
+                outs.append(kda.chunk_prefill_fwd(
+                    d["q"], d["k"], d["v"], d["g"], d["beta"], d["A_log"], d["dt_bias"],
+                    d["lower_bound"], d["scale"], d["initial_state"], d["cu_seqlens"],
+                    workspace=ws, stream=s, kernel=kern))
+        torch.cuda.synchronize()
+        for d, kern, s, ws in calls:
+            assert kda.last_device_status(ws) == kda.OK
+        results.append([outs[1], outs[0], outs[2]])
+    for res in results:
+        for (o, f), (o_ref, f_ref) in zip(res, alone):
+            assert torch.equal(o, o_ref) and torch.equal(f, f_ref)
