@@ -272,18 +272,35 @@ __global__ void __launch_bounds__(NT2, 1)
         ldsm_x4_t(rbs + B_WQ + mnmajor_off(64 + m0, k, 16384), aq0);
         ldsm_x4_t(rbs + B_WQ + mnmajor_off(64 + m0, k + 64, 16384), aq1);
       }
+      const int kb = 16 * ks + (lane & 15);
+      if constexpr (NPW >= 2) {   // two adjacent n8 tiles per ldmatrix
 #pragma unroll
-      for (int j = 0; j < NPW; ++j) {
+        for (int j = 0; j < NPW; j += 2) {
+          uint32_t bv[4], b0[4], b1[4];
+          const int c = 8 * (NPW * ng + j) + 8 * (lane >> 4);
+          ldsm_x4_t(rbs + B_V + swv<DV>(kb, c), bv);
+          ldsm_x4_t(sbf + (kb * SP + c) * 2, b0);
+          ldsm_x4_t(sbf + ((kb + 64) * SP + c) * 2, b1);
+#pragma unroll
+          for (int q = 0; q < 2; ++q) {
+            mma16816(U[j + q], a, bv[2 * q], bv[2 * q + 1]);
+            mma16816(U1[j + q], aw0, b0[2 * q], b0[2 * q + 1]);
+            mma16816(U2[j + q], aw1, b1[2 * q], b1[2 * q + 1]);
+            mma16816(O[j + q], aq0, b0[2 * q], b0[2 * q + 1]);
+            mma16816(O1[j + q], aq1, b1[2 * q], b1[2 * q + 1]);
+          }
+        }
+      } else {
         uint32_t bv[2], b0[2], b1[2];
-        const int k = 16 * ks + (lane & 15), c = 8 * (ng + 2 * j);
-        ldsm_x2_t(rbs + B_V + swv<DV>(k, c), bv);
-        ldsm_x2_t(sbf + (k * SP + c) * 2, b0);
-        ldsm_x2_t(sbf + ((k + 64) * SP + c) * 2, b1);
-        mma16816(U[j], a, bv[0], bv[1]);
-        mma16816(U1[j], aw0, b0[0], b0[1]);
-        mma16816(U2[j], aw1, b1[0], b1[1]);
-        mma16816(O[j], aq0, b0[0], b0[1]);
-        mma16816(O1[j], aq1, b1[0], b1[1]);
+        const int c = 8 * ng;
+        ldsm_x2_t(rbs + B_V + swv<DV>(kb, c), bv);
+        ldsm_x2_t(sbf + (kb * SP + c) * 2, b0);
+        ldsm_x2_t(sbf + ((kb + 64) * SP + c) * 2, b1);
+        mma16816(U[0], a, bv[0], bv[1]);
+        mma16816(U1[0], aw0, b0[0], b0[1]);
+        mma16816(U2[0], aw1, b1[0], b1[1]);
+        mma16816(O[0], aq0, b0[0], b0[1]);
+        mma16816(O1[0], aq1, b1[0], b1[1]);
       }
     }
     // U / |k| (per token row) -> bf16 staging
@@ -292,7 +309,7 @@ __global__ void __launch_bounds__(NT2, 1)
       unsigned char* ub = sm + L_::OFF_UB;
 #pragma unroll
       for (int j = 0; j < NPW; ++j) {
-        const int c = 8 * (ng + 2 * j) + 2 * t;
+        const int c = 8 * (NPW * ng + j) + 2 * t;
         float u[4];
 #pragma unroll
         for (int e = 0; e < 4; ++e) u[e] = U[j][e] + (U1[j][e] + U2[j][e]);
@@ -329,14 +346,14 @@ __global__ void __launch_bounds__(NT2, 1)
             ldsm_x4(rbs + B_QKE + sw128(16 * mt + (lane & 15), col, 192), aq);        // QK rows
             ldsm_x4(rbs + B_QKE + sw128(64 + 16 * warp + (lane & 15), col, 192), ak);  // Ke^T
           }
-  #pragma unroll
-          for (int nt = 0; nt < DV / 8; ++nt) {
-            uint32_t b[2];
-            const int k = 16 * ks + (lane & 15), c = 8 * nt;
-            ldsm_x2_t(ubf + (k * SP + c) * 2, b);
-            if ((nt & 1) == ng)   // O: this warp's n8 tiles ng, ng + 2, ...
-              mma16816((ks & 1) ? O1[nt >> 1] : O[nt >> 1], aq, b[0], b[1]);
-            mma16816(ks < 2 ? S[nt] : S2[nt], ak, b[0], b[1]);
+          {   // both n8 tiles of U' in one ldmatrix; O takes this warp's tile ng
+            uint32_t b[4];
+            const int k = 16 * ks + (lane & 15), c = 8 * (lane >> 4);
+            ldsm_x4_t(ubf + (k * SP + c) * 2, b);
+            const uint32_t bo0 = ng ? b[2] : b[0], bo1 = ng ? b[3] : b[1];   // (no indexing by ng)
+            mma16816((ks & 1) ? O1[0] : O[0], aq, bo0, bo1);
+            mma16816(ks < 2 ? S[0] : S2[0], ak, b[0], b[1]);
+            mma16816(ks < 2 ? S[1] : S2[1], ak, b[2], b[3]);
           }
         }
         const int r0 = 16 * mt + g;
@@ -351,7 +368,7 @@ __global__ void __launch_bounds__(NT2, 1)
         }
   #pragma unroll
         for (int j = 0; j < NPW; ++j) {
-          const int c = dv0 + 8 * (ng + 2 * j) + 2 * t;
+          const int c = dv0 + 8 * (NPW * ng + j) + 2 * t;
           if (w0)
             *reinterpret_cast<uint32_t*>(p.out + (size_t)row0 * HD + h * 128 + c) =
                 bf2((O[j][0] + O1[j][0]) * iq0, (O[j][1] + O1[j][1]) * iq0);
@@ -373,11 +390,12 @@ __global__ void __launch_bounds__(NT2, 1)
           const int row = 16 * mt + (lane & 15), col = 16 * ks + 8 * (lane >> 4);
           ldsm_x4(rbs + B_QKE + sw128(row, col, 192), a);   // QK: rows 0-63 of [QK; Ke]
   #pragma unroll
-          for (int j = 0; j < NPW; ++j) {
-            uint32_t b[2];
-            const int k = 16 * ks + (lane & 15), c = 8 * (ng + 2 * j);
-            ldsm_x2_t(ubf + (k * SP + c) * 2, b);
+          for (int j = 0; j < NPW; j += 2) {   // two adjacent n8 tiles per ldmatrix
+            uint32_t b[4];
+            const int k = 16 * ks + (lane & 15), c = 8 * (NPW * ng + j) + 8 * (lane >> 4);
+            ldsm_x4_t(ubf + (k * SP + c) * 2, b);
             mma16816((ks & 1) ? O1[j] : O[j], a, b[0], b[1]);
+            mma16816((ks & 1) ? O1[j + 1] : O[j + 1], a, b[2], b[3]);
           }
         }
         const int r0 = 16 * mt + g;
@@ -392,7 +410,7 @@ __global__ void __launch_bounds__(NT2, 1)
         }
   #pragma unroll
         for (int j = 0; j < NPW; ++j) {
-          const int c = dv0 + 8 * (ng + 2 * j) + 2 * t;
+          const int c = dv0 + 8 * (NPW * ng + j) + 2 * t;
           if (w0)
             *reinterpret_cast<uint32_t*>(p.out + (size_t)row0 * HD + h * 128 + c) =
                 bf2((O[j][0] + O1[j][0]) * iq0, (O[j][1] + O1[j][1]) * iq0);
@@ -423,11 +441,12 @@ __global__ void __launch_bounds__(NT2, 1)
             ldsm_x4(rbs + B_QKE + sw128(64 + row, col, 192), a);
           }
   #pragma unroll
-          for (int nt = 0; nt < DV / 8; ++nt) {
-            uint32_t b[2];
-            const int k = 16 * ks + (lane & 15), c = 8 * nt;
-            ldsm_x2_t(ubf + (k * SP + c) * 2, b);
+          for (int nt = 0; nt < DV / 8; nt += 2) {   // two n8 tiles per ldmatrix
+            uint32_t b[4];
+            const int k = 16 * ks + (lane & 15), c = 8 * nt + 8 * (lane >> 4);
+            ldsm_x4_t(ubf + (k * SP + c) * 2, b);
             mma16816(ks < 2 ? S[nt] : S2[nt], a, b[0], b[1]);
+            mma16816(ks < 2 ? S[nt + 1] : S2[nt + 1], a, b[2], b[3]);
           }
         }
   #pragma unroll
