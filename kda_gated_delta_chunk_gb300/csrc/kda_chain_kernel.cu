@@ -556,11 +556,23 @@ cudaError_t launch_split(const Params& p, cudaStream_t stream) {
   // products of this file, which measured 12-23% faster there (per-instruction tcgen05
   // overheads do not shrink with N = 32 or 16)
   switch (p.vsplit) {
-    case 1: return launch_chain_tc(p, stream);
-    case 2: return launch_chain_vs(p, stream);
-    case 4: return launch_chain_dv<32>(p, stream);
-    default: return launch_chain_dv<16>(p, stream);
+    case 1: e = launch_chain_tc(p, stream); break;
+    case 2: e = launch_chain_vs(p, stream); break;
+    case 4: e = launch_chain_dv<32>(p, stream); break;
+    default: e = launch_chain_dv<16>(p, stream); break;
   }
+  if (e != cudaSuccess && p.stream_sms > 0) {
+    // streamed, and the chain that clears the call's claim words and counters did not start:
+    // clear them behind the k-side kernel, so that no later call reads this call's records
+    // as its own (the launch error is still returned)
+    cudaGetLastError();
+    unsigned char* ws = reinterpret_cast<unsigned char*>(p.status);
+    cudaMemsetAsync(ws + kStreamCounterWord * sizeof(int), 0,
+                    (kStreamStartWord - kStreamCounterWord + 1) * sizeof(int), stream);
+    cudaMemsetAsync(ws + helper_claims_offset(p.total_tokens, p.heads, p.num_seqs), 0,
+                    (size_t)split_slots(p.total_tokens, p.num_seqs) * p.heads * sizeof(int), stream);
+  }
+  return e;
 }
 
 }  // namespace kda
